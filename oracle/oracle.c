@@ -1,0 +1,340 @@
+/*
+ * oracle.c -- float64 CPU oracle for fused LM-head token scoring.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
+ * load this file: only the tests, the smoke check and the bench's CPU
+ * baseline do.  It shares no code, header, table or helper with the CUDA
+ * library; it is the plain definition of what that library computes,
+ * written out so a reader can check it against the pages by eye.
+ *
+ * What it follows (pages and sections):
+ *   - miles PR #2764 summary (prhub), "Implementation breakdown" item 2 and
+ *     the math_utils.py snippet: logits are upcast (here: exact float64),
+ *     then divided by the temperature after the upcast; log-prob and
+ *     entropy are taken from the same upcast values.
+ *   - miles PR #4645, "How it works" (Op, Selection): logits z = h W^T for
+ *     the scored (response) rows only; log-prob of the target and entropy
+ *     per row; backward = gradient of sum(g1*logp + g2*ent) w.r.t. h and W.
+ *   - DeepSeek-V4 book ch. 19, "Never materialize logits" / "TileLang KL
+ *     kernel": exact full-vocabulary KL between teacher and student heads,
+ *     read here as KL(teacher || student) = sum_v p_t (log p_t - log p_s).
+ *
+ * Definitions (per scored row r, all in float64 from the exact values of
+ * the bf16/fp16 inputs):
+ *   z_v   = sum_k h[r,k] W[v,k]          z'_v = z_v / tau
+ *   LSE   = m + log(sum_v exp(z'_v - m)),  m = max_v z'_v   (two passes)
+ *   p_v   = exp(z'_v - LSE)
+ *   logp  = z'_tgt - LSE
+ *   ent   = LSE - sum_v p_v z'_v          Ez = sum_v p_v z'_v
+ *   KL    = sum_v p_t,v ((z_t,v - LSE_t) - (z_s,v - LSE_s))
+ *   G_v   = (g1 (1[v=tgt] - p_v) - g2 p_v (z'_v - Ez)) / tau
+ *   dh[r] = sum_v G_v W[v,:]              dW[v,:] += G_v h[r,:]
+ *
+ * The z rows are held whole (no blocking of the vocabulary, no online
+ * rescaling): this is the definition, not the fast method.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Element types of the matrices handed to the oracle. */
+enum { ORC_BF16 = 0, ORC_FP16 = 1, ORC_F64 = 2 };
+
+/* Rows of h whose logits are held at once. */
+#define ORC_ROW_BLOCK 32
+
+static double orc_bf16(uint16_t b)
+{
+    /* bf16 is the top half of an IEEE binary32: exact widening. */
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static double orc_fp16(uint16_t b)
+{
+    /* IEEE binary16: 1 sign, 5 exponent (bias 15), 10 fraction bits. */
+    int sign = (b >> 15) & 1;
+    int e = (b >> 10) & 0x1f;
+    int f = b & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);             /* subnormal: f * 2^-24 */
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + f), e - 25); /* (1 + f/1024) * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+/* Decode n consecutive elements starting at element offset off. */
+static void orc_decode(const void *p, int type, int64_t off, int64_t n, double *out)
+{
+    int64_t i;
+    if (type == ORC_BF16) {
+        const uint16_t *q = (const uint16_t *)p + off;
+        for (i = 0; i < n; ++i) out[i] = orc_bf16(q[i]);
+    } else if (type == ORC_FP16) {
+        const uint16_t *q = (const uint16_t *)p + off;
+        for (i = 0; i < n; ++i) out[i] = orc_fp16(q[i]);
+    } else {
+        const double *q = (const double *)p + off;
+        for (i = 0; i < n; ++i) out[i] = q[i];
+    }
+}
+
+int orc_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void orc_decode_array(const void *p, int type, int64_t n, double *out)
+{
+    orc_decode(p, type, 0, n, out);
+}
+
+/*
+ * z[b][v] = sum_k h[rows[b],k] * W[v,k] for b < nb, all v < V.
+ * hd holds the nb decoded h rows (nb x H).  W is decoded one vocab row at a
+ * time.
+ */
+static void orc_logits_block(const double *hd, int64_t nb, int64_t H, int64_t V,
+                             const void *W, int wtype, int64_t ld_w, double *z)
+{
+    int64_t v;
+#pragma omp parallel
+    {
+        double *wd = (double *)malloc((size_t)H * sizeof(double));
+#pragma omp for schedule(static)
+        for (v = 0; v < V; ++v) {
+            int64_t b, k;
+            orc_decode(W, wtype, v * ld_w, H, wd);
+            for (b = 0; b < nb; ++b) {
+                const double *hr = hd + b * H;
+                double acc = 0.0;
+                for (k = 0; k < H; ++k) acc += hr[k] * wd[k];
+                z[b * V + v] = acc;
+            }
+        }
+        free(wd);
+    }
+}
+
+/* Decode the h rows rows[i0 .. i0+nb) into hd (nb x H). */
+static void orc_gather_h(const void *h, int htype, int64_t ld_h, const int64_t *rows,
+                         int64_t i0, int64_t nb, int64_t H, double *hd)
+{
+    int64_t b;
+    for (b = 0; b < nb; ++b) orc_decode(h, htype, rows[i0 + b] * ld_h, H, hd + b * H);
+}
+
+/* Two-pass log-sum-exp of x[0..V) (max shift, then sum of exponentials). */
+static double orc_lse(const double *x, int64_t V)
+{
+    double m = -INFINITY, s = 0.0;
+    int64_t v;
+    for (v = 0; v < V; ++v)
+        if (x[v] > m) m = x[v];
+    for (v = 0; v < V; ++v) s += exp(x[v] - m);
+    return m + log(s);
+}
+
+/*
+ * Log-prob of the target and entropy of softmax(z/tau) for the rows
+ * rows[0..n) of h (indices into h; duplicates allowed).  targets is indexed
+ * by the original h row.  Any of the four outputs may be NULL.
+ * Returns 0, or -1 on an out-of-range row or target (outputs for that row
+ * are NaN and the scan continues).
+ */
+int orc_logprob_entropy(int64_t H, int64_t V,
+                        const void *h, int htype, int64_t ld_h,
+                        const void *W, int wtype, int64_t ld_w,
+                        const int64_t *rows, int64_t n, int64_t T,
+                        const int64_t *targets, double tau,
+                        double *logp, double *ent, double *lse_out, double *ez_out)
+{
+    int rc = 0;
+    int64_t i0;
+    double *hd = (double *)malloc((size_t)ORC_ROW_BLOCK * H * sizeof(double));
+    double *z = (double *)malloc((size_t)ORC_ROW_BLOCK * V * sizeof(double));
+    if (!hd || !z) { free(hd); free(z); return -2; }
+    for (i0 = 0; i0 < n; i0 += ORC_ROW_BLOCK) {
+        int64_t nb = n - i0 < ORC_ROW_BLOCK ? n - i0 : ORC_ROW_BLOCK;
+        int64_t b;
+        int bad_row = 0;
+        for (b = 0; b < nb; ++b)
+            if (rows[i0 + b] < 0 || rows[i0 + b] >= T) bad_row = 1;
+        if (bad_row) {
+            /* Keep the plain path simple: score valid rows one at a time. */
+            for (b = 0; b < nb; ++b) {
+                int64_t i = i0 + b;
+                if (rows[i] < 0 || rows[i] >= T) {
+                    if (logp) logp[i] = NAN;
+                    if (ent) ent[i] = NAN;
+                    if (lse_out) lse_out[i] = NAN;
+                    if (ez_out) ez_out[i] = NAN;
+                    rc = -1;
+                } else {
+                    int r = orc_logprob_entropy(H, V, h, htype, ld_h, W, wtype, ld_w,
+                                                rows + i, 1, T, targets, tau,
+                                                logp ? logp + i : NULL, ent ? ent + i : NULL,
+                                                lse_out ? lse_out + i : NULL,
+                                                ez_out ? ez_out + i : NULL);
+                    if (r) rc = r;
+                }
+            }
+            continue;
+        }
+        orc_gather_h(h, htype, ld_h, rows, i0, nb, H, hd);
+        orc_logits_block(hd, nb, H, V, W, wtype, ld_w, z);
+        for (b = 0; b < nb; ++b) {
+            int64_t i = i0 + b, v;
+            double *zr = z + b * V;
+            double L, ez = 0.0;
+            int64_t tgt = targets ? targets[rows[i]] : -1;
+            /* upcast first (already float64), then temperature. */
+            for (v = 0; v < V; ++v) zr[v] = zr[v] / tau;
+            L = orc_lse(zr, V);
+            for (v = 0; v < V; ++v) ez += exp(zr[v] - L) * zr[v];
+            if (logp) {
+                if (tgt >= 0 && tgt < V) logp[i] = zr[tgt] - L;
+                else { logp[i] = NAN; rc = -1; }
+            }
+            if (ent) ent[i] = L - ez;
+            if (lse_out) lse_out[i] = L;
+            if (ez_out) ez_out[i] = ez;
+        }
+    }
+    free(hd);
+    free(z);
+    return rc;
+}
+
+/*
+ * Full-vocabulary KL(teacher || student) per scored row.  Both heads share
+ * H and V; the temperature is 1.
+ */
+int orc_kl(int64_t H, int64_t V,
+           const void *h_s, const void *W_s, const void *h_t, const void *W_t,
+           int type, int64_t ld_h, int64_t ld_w,
+           const int64_t *rows, int64_t n, double *kl)
+{
+    int64_t i0;
+    double *hds = (double *)malloc((size_t)ORC_ROW_BLOCK * H * sizeof(double));
+    double *hdt = (double *)malloc((size_t)ORC_ROW_BLOCK * H * sizeof(double));
+    double *zs = (double *)malloc((size_t)ORC_ROW_BLOCK * V * sizeof(double));
+    double *zt = (double *)malloc((size_t)ORC_ROW_BLOCK * V * sizeof(double));
+    if (!hds || !hdt || !zs || !zt) { free(hds); free(hdt); free(zs); free(zt); return -2; }
+    for (i0 = 0; i0 < n; i0 += ORC_ROW_BLOCK) {
+        int64_t nb = n - i0 < ORC_ROW_BLOCK ? n - i0 : ORC_ROW_BLOCK;
+        int64_t b;
+        orc_gather_h(h_s, type, ld_h, rows, i0, nb, H, hds);
+        orc_gather_h(h_t, type, ld_h, rows, i0, nb, H, hdt);
+        orc_logits_block(hds, nb, H, V, W_s, type, ld_w, zs);
+        orc_logits_block(hdt, nb, H, V, W_t, type, ld_w, zt);
+        for (b = 0; b < nb; ++b) {
+            const double *s = zs + b * V, *t = zt + b * V;
+            double Ls = orc_lse(s, V), Lt = orc_lse(t, V), acc = 0.0;
+            int64_t v;
+            for (v = 0; v < V; ++v) {
+                double lpt = t[v] - Lt, lps = s[v] - Ls;
+                acc += exp(lpt) * (lpt - lps);
+            }
+            kl[i0 + b] = acc;
+        }
+    }
+    free(hds); free(hdt); free(zs); free(zt);
+    return 0;
+}
+
+/*
+ * Backward of L = sum_i g1[i] logp[i] + g2[i] ent[i] over the scored rows
+ * rows[0..n).
+ *   dh_rows (n x H, float64) receives sum_v G_iv W[v,:] for scored position
+ *     i; the caller scatters it to h row rows[i] (adding duplicates).
+ *   dW_sel (nv x H, float64) receives dW[vsel[j],:] = sum_i G_i,vsel[j] h[rows[i],:]
+ *     for the nv selected vocab rows (vsel may be NULL with nv = V for all).
+ * Either output may be NULL.  Caller zero-fills dW_sel.
+ */
+int orc_backward(int64_t H, int64_t V,
+                 const void *h, int htype, int64_t ld_h,
+                 const void *W, int wtype, int64_t ld_w,
+                 const int64_t *rows, int64_t n, int64_t T,
+                 const int64_t *targets, double tau,
+                 const double *g1, const double *g2,
+                 double *dh_rows, const int64_t *vsel, int64_t nv, double *dW_sel)
+{
+    int64_t i0;
+    double *hd = (double *)malloc((size_t)ORC_ROW_BLOCK * H * sizeof(double));
+    double *z = (double *)malloc((size_t)ORC_ROW_BLOCK * V * sizeof(double));
+    if (!hd || !z) { free(hd); free(z); return -2; }
+    for (i0 = 0; i0 < n; i0 += ORC_ROW_BLOCK) {
+        int64_t nb = n - i0 < ORC_ROW_BLOCK ? n - i0 : ORC_ROW_BLOCK;
+        int64_t b;
+        for (b = 0; b < nb; ++b)
+            if (rows[i0 + b] < 0 || rows[i0 + b] >= T) { free(hd); free(z); return -1; }
+        orc_gather_h(h, htype, ld_h, rows, i0, nb, H, hd);
+        orc_logits_block(hd, nb, H, V, W, wtype, ld_w, z);
+        /* z row b becomes the gradient row G_b in place. */
+        for (b = 0; b < nb; ++b) {
+            int64_t i = i0 + b, v;
+            double *zr = z + b * V;
+            double L, ez = 0.0;
+            int64_t tgt = targets[rows[i]];
+            if (tgt < 0 || tgt >= V) { free(hd); free(z); return -1; }
+            for (v = 0; v < V; ++v) zr[v] = zr[v] / tau;
+            L = orc_lse(zr, V);
+            for (v = 0; v < V; ++v) ez += exp(zr[v] - L) * zr[v];
+            for (v = 0; v < V; ++v) {
+                double p = exp(zr[v] - L);
+                double onehot = (v == tgt) ? 1.0 : 0.0;
+                zr[v] = (g1[i] * (onehot - p) - g2[i] * p * (zr[v] - ez)) / tau;
+            }
+        }
+        if (dh_rows) {
+            /* dh_rows[i] = sum_v G_iv W[v,:]; threads own slices of the
+             * hidden dimension so each W element is decoded once. */
+            int64_t k0, k;
+            double *acc = (double *)calloc((size_t)nb * H, sizeof(double));
+#pragma omp parallel for schedule(static)
+            for (k0 = 0; k0 < H; k0 += 64) {
+                int64_t kn = H - k0 < 64 ? H - k0 : 64, v, bb, kk;
+                double wseg[64];
+                for (v = 0; v < V; ++v) {
+                    orc_decode(W, wtype, v * ld_w + k0, kn, wseg);
+                    for (bb = 0; bb < nb; ++bb) {
+                        double g = z[bb * V + v];
+                        double *a = acc + bb * H + k0;
+                        for (kk = 0; kk < kn; ++kk) a[kk] += g * wseg[kk];
+                    }
+                }
+            }
+            for (b = 0; b < nb; ++b)
+                for (k = 0; k < H; ++k) dh_rows[(i0 + b) * H + k] = acc[b * H + k];
+            free(acc);
+        }
+        if (dW_sel) {
+            int64_t j;
+#pragma omp parallel for schedule(static)
+            for (j = 0; j < nv; ++j) {
+                int64_t v = vsel ? vsel[j] : j, bb, k;
+                for (bb = 0; bb < nb; ++bb) {
+                    double g = z[bb * V + v];
+                    const double *hr = hd + bb * H;
+                    for (k = 0; k < H; ++k) dW_sel[j * H + k] += g * hr[k];
+                }
+            }
+        }
+    }
+    free(hd); free(z);
+    return 0;
+}

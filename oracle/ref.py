@@ -1,0 +1,132 @@
+"""NumPy float64 restatement of the oracle.
+
+Test infrastructure only (see the package docstring).  Independent of
+``oracle.c``: its own decoding of the storage formats, its own two-pass
+log-sum-exp, with ``numpy.matmul`` (float64 BLAS) as the one library step
+for the logits.  Used to cross-check the C oracle and for the large
+full-vocabulary passes that the C loops are too slow for (the per-row
+statistics every dW element depends on).
+
+Definitions: miles PR #2764 summary (prhub), "Implementation breakdown"
+item 2 and its math_utils.py snippet (upcast, then divide by the
+temperature); miles PR #4645, "How it works" (scored rows only, log-prob
+and entropy per row, backward through h and W); DeepSeek-V4 book ch. 19,
+"TileLang KL kernel" (exact full-vocabulary KL, read as KL(t || s)).
+"""
+import numpy as np
+
+
+def decode(x, dtype):
+    """Exact float64 values of a bf16/fp16 bit-pattern array (or a float array)."""
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            x = x.detach().cpu()
+            if x.dtype in (torch.bfloat16, torch.float16):
+                x = x.contiguous().view(torch.int16).numpy().view(np.uint16)
+            else:
+                x = x.numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    x = np.asarray(x)
+    if dtype == "bf16":
+        with np.errstate(invalid="ignore"):   # NaN payloads widen with a warning
+            return (x.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    if dtype == "fp16":
+        return x.astype(np.uint16).view(np.float16).astype(np.float64)
+    return x.astype(np.float64)
+
+
+def _rows(rows, T):
+    return np.arange(T) if rows is None else np.asarray(rows, dtype=np.int64)
+
+
+def _lse(zp):
+    """Row-wise log-sum-exp, max shift then sum (two passes)."""
+    m = zp.max(axis=1, keepdims=True)
+    return (m + np.log(np.exp(zp - m).sum(axis=1, keepdims=True)))[:, 0]
+
+
+def row_stats(hd, Wd, rows, tau, block=256):
+    """lse and Ez' = sum_v p_v z'_v per scored row, from decoded float64 h, W."""
+    rows = _rows(rows, hd.shape[0])
+    lse = np.empty(rows.shape[0])
+    ez = np.empty(rows.shape[0])
+    for i0 in range(0, rows.shape[0], block):
+        zp = (hd[rows[i0:i0 + block]] @ Wd.T) / tau
+        L = _lse(zp)
+        p = np.exp(zp - L[:, None])
+        lse[i0:i0 + block] = L
+        ez[i0:i0 + block] = (p * zp).sum(axis=1)
+    return lse, ez
+
+
+def logprob_entropy(h, W, targets, rows, tau, dtype, block=256):
+    hd, Wd = decode(h, dtype), decode(W, dtype)
+    rows = _rows(rows, hd.shape[0])
+    tg = np.asarray(targets, dtype=np.int64)[rows]
+    lse, ez = row_stats(hd, Wd, rows, tau, block)
+    zt = np.einsum("ik,ik->i", hd[rows], Wd[tg]) / tau
+    return {"logp": zt - lse, "ent": lse - ez, "lse": lse, "ez": ez}
+
+
+def kl(h_s, W_s, h_t, W_t, rows, dtype, block=256):
+    hs, Ws, ht, Wt = (decode(a, dtype) for a in (h_s, W_s, h_t, W_t))
+    rows = _rows(rows, hs.shape[0])
+    out = np.empty(rows.shape[0])
+    for i0 in range(0, rows.shape[0], block):
+        r = rows[i0:i0 + block]
+        ls = hs[r] @ Ws.T
+        lt = ht[r] @ Wt.T
+        ls = ls - _lse(ls)[:, None]
+        lt = lt - _lse(lt)[:, None]
+        out[i0:i0 + block] = (np.exp(lt) * (lt - ls)).sum(axis=1)
+    return out
+
+
+def grad_logits(zp, tgt, lse, ez, g1, g2, tau):
+    """dL/dz for L = g1 logp + g2 ent, rows of z' = z/tau (float64)."""
+    p = np.exp(zp - lse[:, None])
+    onehot = np.zeros_like(zp)
+    onehot[np.arange(zp.shape[0]), tgt] = 1.0
+    return (g1[:, None] * (onehot - p) - g2[:, None] * p * (zp - ez[:, None])) / tau
+
+
+def backward(h, W, targets, rows, tau, g1, g2, dtype, dh_rows_sel=None, vsel=None,
+             block=256, stats=None):
+    """Gradients of sum(g1 logp + g2 ent).
+
+    dh_rows_sel: positions i (into rows) whose dh rows to return (default all).
+    vsel: vocabulary rows of dW to return (default all).  dW needs every
+    scored row's statistics, which this computes with a float64 matmul pass
+    over the full vocabulary unless ``stats=(lse, ez)`` is supplied (each
+    computed by :func:`row_stats`).
+    Returns (dh_rows [len(sel),H], dW_sel [len(vsel),H]).
+    """
+    hd, Wd = decode(h, dtype), decode(W, dtype)
+    rows = _rows(rows, hd.shape[0])
+    n = rows.shape[0]
+    g1 = np.asarray(g1, dtype=np.float64)
+    g2 = np.asarray(g2, dtype=np.float64)
+    tg = np.asarray(targets, dtype=np.int64)[rows]
+    sel = np.arange(n) if dh_rows_sel is None else np.asarray(dh_rows_sel, dtype=np.int64)
+    vs = np.arange(Wd.shape[0]) if vsel is None else np.asarray(vsel, dtype=np.int64)
+
+    # dh rows: only the selected positions' statistics are needed.
+    dh = np.empty((sel.shape[0], hd.shape[1]))
+    for i0 in range(0, sel.shape[0], block):
+        s = sel[i0:i0 + block]
+        zp = (hd[rows[s]] @ Wd.T) / tau
+        L = _lse(zp)
+        ez = (np.exp(zp - L[:, None]) * zp).sum(axis=1)
+        G = grad_logits(zp, tg[s], L, ez, g1[s], g2[s], tau)
+        dh[i0:i0 + block] = G @ Wd
+
+    # dW rows: every scored row contributes to every vocabulary row.
+    lse, ez = stats if stats is not None else row_stats(hd, Wd, rows, tau, block)
+    zp = (hd[rows] @ Wd[vs].T) / tau                       # [n, len(vs)]
+    p = np.exp(zp - lse[:, None])
+    onehot = (tg[:, None] == vs[None, :]).astype(np.float64)
+    G = (g1[:, None] * (onehot - p) - g2[:, None] * p * (zp - ez[:, None])) / tau
+    dW = G.T @ hd[rows]
+    return dh, dW

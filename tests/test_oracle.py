@@ -1,0 +1,376 @@
+"""Pins for the float64 oracle (CPU only).
+
+The oracle is the reference every GPU parity test trusts, so it is pinned
+here to things other than itself: exact decoding of every storage bit
+pattern, closed forms (W = 0, one dominant logit, two classes, identical
+KL heads), invariants (shift, temperature as a scale, row subsets and
+order), 50-digit brute force on tiny inputs, and central finite
+differences of its own forward for the backward.  Each C-oracle result is
+also cross-checked against the independent NumPy restatement.
+"""
+import math
+from decimal import Decimal, getcontext
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import coracle, ref
+import workloads
+
+LN = math.log
+
+
+def _bits(x, dtype):
+    t = torch.as_tensor(x, dtype=torch.float32).to(workloads.TORCH_DTYPES[dtype])
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+# --------------------------------------------------------------------------
+# storage decoding
+
+def test_decode_every_bf16_pattern():
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    want = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).double().numpy()
+    for got in (coracle.decode(bits, "bf16"), ref.decode(bits, "bf16")):
+        nan = np.isnan(want)
+        assert np.array_equal(np.isnan(got), nan)
+        assert np.array_equal(got[~nan], want[~nan])
+
+
+def test_decode_every_fp16_pattern():
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    want = torch.from_numpy(bits.view(np.int16)).view(torch.float16).double().numpy()
+    for got in (coracle.decode(bits, "fp16"), ref.decode(bits, "fp16")):
+        nan = np.isnan(want)
+        assert np.array_equal(np.isnan(got), nan)
+        assert np.array_equal(got[~nan], want[~nan])
+    # spot values of the format itself
+    assert coracle.decode(np.array([0x3C00, 0x0001, 0x7BFF, 0xC000], np.uint16), "fp16").tolist() \
+        == [1.0, 2.0 ** -24, 65504.0, -2.0]
+
+
+# --------------------------------------------------------------------------
+# closed forms
+
+@pytest.mark.parametrize("V,H", [(8192, 16), (151936, 8), (38016, 8)])
+@pytest.mark.parametrize("tau", [0.7, 1.0, 3.0])
+def test_zero_weight_gives_uniform(V, H, tau):
+    rng = np.random.default_rng(0)
+    h = _bits(rng.standard_normal((3, H)), "bf16")
+    W = np.zeros((V, H), np.uint16)                      # +0.0 in bf16
+    tg = rng.integers(0, V, size=3)
+    o = coracle.logprob_entropy(h, W, tg, None, tau, "bf16")
+    np.testing.assert_allclose(o["logp"], -LN(V), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(o["ent"], LN(V), rtol=0, atol=1e-12)
+    if V == 8192:
+        assert abs(LN(V) - 9.010913) < 1e-6
+    if V == 151936:
+        assert abs(LN(V) - 11.931215) < 1e-6
+
+
+def test_one_hot_dominant_row():
+    """W[tgt] = c h / |h|^2 puts logit c on the target; the rest are O(1)."""
+    rng = np.random.default_rng(1)
+    H, V = 64, 1000
+    hf = rng.standard_normal((4, H))
+    Wf = rng.standard_normal((V, H)) * 0.01
+    tg = np.array([3, 500, 999, 0])
+    for i in range(4):
+        Wf[tg[i]] = 60.0 * hf[i] / (hf[i] @ hf[i])
+    o = coracle.logprob_entropy(hf, Wf, tg, None, 1.0, "f64")
+    z = hf @ Wf.T
+    for i in range(4):
+        margin = z[i, tg[i]] - np.max(np.delete(z[i], tg[i]))
+        assert margin >= 40
+    assert np.all(o["logp"] <= 0) and np.all(o["logp"] >= -V * math.exp(-40))
+    assert np.all(o["ent"] >= 0) and np.all(o["ent"] <= V * math.exp(-40) * 62)
+
+
+@pytest.mark.parametrize("tau", [0.5, 1.0, 2.0])
+def test_two_classes(tau):
+    rng = np.random.default_rng(2)
+    h = rng.standard_normal((5, 3))
+    W = rng.standard_normal((2, 3))
+    tg = np.array([0, 1, 1, 0, 1])
+    o = coracle.logprob_entropy(h, W, tg, None, tau, "f64")
+    z = h @ W.T / tau
+    for i in range(5):
+        d = z[i, tg[i]] - z[i, 1 - tg[i]]
+        assert o["logp"][i] == pytest.approx(-math.log1p(math.exp(-d)), abs=1e-13)
+        p = 1.0 / (1.0 + math.exp(-(z[i, 0] - z[i, 1])))
+        assert o["ent"][i] == pytest.approx(-(p * LN(p) + (1 - p) * LN(1 - p)), abs=1e-13)
+
+
+def test_large_temperature_entropy_tends_to_log_v():
+    rng = np.random.default_rng(3)
+    h = rng.standard_normal((2, 16))
+    W = rng.standard_normal((100, 16))
+    tg = np.array([1, 2])
+    o = coracle.logprob_entropy(h, W, tg, None, 1e6, "f64")
+    np.testing.assert_allclose(o["ent"], LN(100), atol=1e-8)
+    np.testing.assert_allclose(o["logp"], -LN(100), atol=1e-4)
+
+
+# --------------------------------------------------------------------------
+# invariants
+
+def _random_case(seed, T=12, H=24, V=300, dtype="bf16"):
+    w = workloads.WORKLOADS[0].scaled(T=T, H=H, V=V, dtype=dtype, seed=seed, w_std=0.3)
+    return workloads.make(w)
+
+
+def test_bounds_on_config0():
+    d = workloads.make(0)
+    o = coracle.logprob_entropy(d["h"], d["W"], d["targets"], None, 1.0, "bf16")
+    assert o["rc"] == 0
+    assert np.all(o["logp"] <= 0)
+    assert np.all(o["ent"] >= 0) and np.all(o["ent"] <= LN(8192))
+
+
+def test_shift_invariance():
+    """Append a column: every logit of a row shifts by s_r c; outputs do not move."""
+    rng = np.random.default_rng(4)
+    h = rng.standard_normal((6, 10))
+    W = rng.standard_normal((50, 10)) * 0.5
+    tg = rng.integers(0, 50, size=6)
+    s = rng.standard_normal((6, 1)) * 3
+    h2 = np.hstack([h, s])
+    W2 = np.hstack([W, np.full((50, 1), 2.5)])
+    for tau in (0.7, 1.0):
+        a = coracle.logprob_entropy(h, W, tg, None, tau, "f64")
+        b = coracle.logprob_entropy(h2, W2, tg, None, tau, "f64")
+        for k in ("logp", "ent", "ez"):
+            if k == "ez":
+                np.testing.assert_allclose(b[k] - a[k], (s[:, 0] * 2.5) / tau, atol=1e-10)
+            else:
+                np.testing.assert_allclose(a[k], b[k], atol=1e-11)
+
+
+def test_temperature_is_a_scale_of_the_logits():
+    rng = np.random.default_rng(5)
+    h = rng.standard_normal((7, 9))
+    W = rng.standard_normal((40, 9))
+    tg = rng.integers(0, 40, size=7)
+    a = coracle.logprob_entropy(h, W, tg, None, 0.7, "f64")
+    b = coracle.logprob_entropy(h, W / 0.7, tg, None, 1.0, "f64")
+    for k in ("logp", "ent", "lse", "ez"):
+        np.testing.assert_allclose(a[k], b[k], rtol=1e-12, atol=1e-12)
+
+
+def test_row_subsets_and_order_do_not_matter():
+    """Chunked equals unchunked: any split, order or repetition of rows."""
+    d = _random_case(6, T=40)
+    full = coracle.logprob_entropy(d["h"], d["W"], d["targets"], None, 0.7, "bf16")
+    rows = np.array([39, 0, 5, 5, 17, 38, 1])
+    part = coracle.logprob_entropy(d["h"], d["W"], d["targets"], rows, 0.7, "bf16")
+    for k in ("logp", "ent", "lse", "ez"):
+        np.testing.assert_array_equal(part[k], full[k][rows])
+    for chunk in (1, 3, 16):
+        got = np.concatenate([
+            coracle.logprob_entropy(d["h"], d["W"], d["targets"], np.arange(i, min(i + chunk, 40)),
+                                    0.7, "bf16")["logp"] for i in range(0, 40, chunk)])
+        np.testing.assert_array_equal(got, full["logp"])
+
+
+def test_targets_follow_the_original_row():
+    d = _random_case(7, T=10)
+    rows = np.array([9, 2, 4])
+    tg = d["targets"].numpy().copy()
+    o = coracle.logprob_entropy(d["h"], d["W"], tg, rows, 1.0, "bf16")
+    hd = ref.decode(d["h"], "bf16")
+    Wd = ref.decode(d["W"], "bf16")
+    for i, r in enumerate(rows):
+        z = hd[r] @ Wd.T
+        m = z.max()
+        lse = m + LN(np.exp(z - m).sum())
+        assert o["logp"][i] == pytest.approx(z[tg[r]] - lse, abs=1e-12)
+
+
+def test_bad_target_and_row_give_nan():
+    d = _random_case(8, T=6)
+    tg = d["targets"].numpy().copy()
+    tg[2] = 10 ** 6
+    o = coracle.logprob_entropy(d["h"], d["W"], tg, np.array([0, 2, 7, 1]), 1.0, "bf16")
+    assert o["rc"] == -1
+    assert np.isnan(o["logp"][1]) and np.isfinite(o["ent"][1])
+    assert np.isnan(o["logp"][2]) and np.isnan(o["ent"][2])
+    assert np.isfinite(o["logp"][0]) and np.isfinite(o["logp"][3])
+
+
+# --------------------------------------------------------------------------
+# 50-digit brute force on tiny inputs
+
+def _dec_forward(h, W, tg, rows, tau):
+    getcontext().prec = 50
+    out = []
+    for r in rows:
+        z = [sum(Decimal(float(h[r, k])) * Decimal(float(W[v, k])) for k in range(h.shape[1]))
+             / Decimal(repr(tau)) for v in range(W.shape[0])]
+        S = sum((x.exp() for x in z), Decimal(0))
+        lse = S.ln()
+        ez = sum(((x - lse).exp() * x for x in z), Decimal(0))
+        out.append((float(z[tg[r]] - lse), float(lse - ez), float(lse), float(ez)))
+    return np.array(out)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("tau", [0.7, 1.0])
+def test_brute_force_forward(dtype, tau):
+    d = _random_case(9, T=7, H=13, V=37, dtype=dtype)
+    rows = np.array([6, 0, 3, 3])
+    tg = d["targets"].numpy()
+    hd, Wd = ref.decode(d["h"], dtype), ref.decode(d["W"], dtype)
+    want = _dec_forward(hd, Wd, tg, rows, tau)
+    c = coracle.logprob_entropy(d["h"], d["W"], tg, rows, tau, dtype)
+    n = ref.logprob_entropy(d["h"], d["W"], tg, rows, tau, dtype)
+    for o in (c, n):
+        got = np.stack([o["logp"], o["ent"], o["lse"], o["ez"]], axis=1)
+        np.testing.assert_allclose(got, want, rtol=1e-13, atol=1e-13)
+
+
+def _dec_kl(hs, Ws, ht, Wt, rows):
+    getcontext().prec = 50
+    out = []
+    for r in rows:
+        def lsm(h, W):
+            z = [sum(Decimal(float(h[r, k])) * Decimal(float(W[v, k])) for k in range(h.shape[1]))
+                 for v in range(W.shape[0])]
+            L = sum((x.exp() for x in z), Decimal(0)).ln()
+            return [x - L for x in z]
+        ls, lt = lsm(hs, Ws), lsm(ht, Wt)
+        out.append(float(sum((b.exp() * (b - a) for a, b in zip(ls, lt)), Decimal(0))))
+    return np.array(out)
+
+
+def test_brute_force_kl():
+    w = workloads.WORKLOADS[3].scaled(T=5, H=11, V=29, w_std=0.4, seed=10)
+    d = workloads.make(w)
+    rows = np.array([4, 1, 0])
+    dec = [ref.decode(d[k], "bf16") for k in ("h_s", "W_s", "h_t", "W_t")]
+    want = _dec_kl(*dec, rows)
+    np.testing.assert_allclose(coracle.kl(d["h_s"], d["W_s"], d["h_t"], d["W_t"], rows, "bf16"),
+                               want, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(ref.kl(d["h_s"], d["W_s"], d["h_t"], d["W_t"], rows, "bf16"),
+                               want, rtol=1e-12, atol=1e-14)
+
+
+def test_kl_closed_forms():
+    w = workloads.WORKLOADS[3].scaled(T=6, H=16, V=64, seed=11)
+    d = workloads.make(w)
+    same = coracle.kl(d["h_s"], d["W_s"], d["h_s"], d["W_s"], None, "bf16")
+    assert np.all(np.abs(same) < 1e-14)
+    diff = coracle.kl(d["h_s"], d["W_s"], d["h_t"], d["W_t"], None, "bf16")
+    assert np.all(diff > 0)
+    # two classes: KL of Bernoulli(q) from Bernoulli(p)
+    rng = np.random.default_rng(12)
+    hs, ht = rng.standard_normal((3, 4)), rng.standard_normal((3, 4))
+    Ws, Wt = rng.standard_normal((2, 4)), rng.standard_normal((2, 4))
+    got = coracle.kl(hs, Ws, ht, Wt, None, "f64")
+    for i in range(3):
+        zs, zt = hs[i] @ Ws.T, ht[i] @ Wt.T
+        p = 1 / (1 + math.exp(zs[1] - zs[0]))
+        q = 1 / (1 + math.exp(zt[1] - zt[0]))
+        assert got[i] == pytest.approx(q * LN(q / p) + (1 - q) * LN((1 - q) / (1 - p)), abs=1e-13)
+
+
+# --------------------------------------------------------------------------
+# backward
+
+def _loss(h, W, tg, rows, tau, g1, g2):
+    o = coracle.logprob_entropy(h, W, tg, rows, tau, "f64")
+    return float(np.sum(g1 * o["logp"] + g2 * o["ent"]))
+
+
+@pytest.mark.parametrize("tau", [0.7, 1.0])
+def test_backward_matches_finite_differences(tau):
+    rng = np.random.default_rng(13)
+    T, H, V = 6, 5, 7
+    h = rng.standard_normal((T, H))
+    W = rng.standard_normal((V, H)) * 0.7
+    tg = rng.integers(0, V, size=T)
+    rows = np.array([5, 0, 2, 3])
+    g1, g2 = rng.standard_normal(4), rng.standard_normal(4)
+    dh_rows, dW = coracle.backward(h, W, tg, rows, tau, g1, g2, "f64")
+    dh = coracle.scatter_rows(dh_rows, rows, T)
+    eps = 1e-6
+    num_h = np.zeros_like(h)
+    for r in range(T):
+        for k in range(H):
+            hp, hm = h.copy(), h.copy()
+            hp[r, k] += eps
+            hm[r, k] -= eps
+            num_h[r, k] = (_loss(hp, W, tg, rows, tau, g1, g2)
+                           - _loss(hm, W, tg, rows, tau, g1, g2)) / (2 * eps)
+    num_W = np.zeros_like(W)
+    for v in range(V):
+        for k in range(H):
+            Wp, Wm = W.copy(), W.copy()
+            Wp[v, k] += eps
+            Wm[v, k] -= eps
+            num_W[v, k] = (_loss(h, Wp, tg, rows, tau, g1, g2)
+                           - _loss(h, Wm, tg, rows, tau, g1, g2)) / (2 * eps)
+    assert np.linalg.norm(dh - num_h) <= 1e-6 * np.linalg.norm(num_h)
+    assert np.linalg.norm(dW - num_W) <= 1e-6 * np.linalg.norm(num_W)
+    assert np.all(dh[[1, 4]] == 0)                     # unscored rows
+    rdh, rdW = ref.backward(h, W, tg, rows, tau, g1, g2, "f64")
+    np.testing.assert_allclose(rdh, dh_rows, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(rdW, dW, rtol=1e-10, atol=1e-12)
+
+
+def test_backward_dw_columns_sum_to_zero():
+    """sum_v G_rv = 0 for every row, hence sum_v dW[v,:] = 0."""
+    w = workloads.WORKLOADS[4].scaled(T=24, H=32, V=500, seed=14)
+    d = workloads.make(w)
+    rows = d["row_idx"].numpy()
+    _, dW = coracle.backward(d["h"], d["W"], d["targets"], rows, 0.7, d["g1"].numpy(),
+                             d["g2"].numpy(), "bf16", want_dh=False)
+    scale = np.abs(dW).sum(axis=0)
+    assert np.all(np.abs(dW.sum(axis=0)) <= 1e-12 * scale + 1e-15)
+
+
+def test_backward_subsets_match_full():
+    w = workloads.WORKLOADS[4].scaled(T=30, H=24, V=260, seed=15)
+    d = workloads.make(w)
+    rows = d["row_idx"].numpy()
+    g1, g2 = d["g1"].numpy(), d["g2"].numpy()
+    dh, dW = coracle.backward(d["h"], d["W"], d["targets"], rows, 0.7, g1, g2, "bf16")
+    vsel = np.array([0, 7, 259, 100])
+    _, dWs = coracle.backward(d["h"], d["W"], d["targets"], rows, 0.7, g1, g2, "bf16",
+                              want_dh=False, vsel=vsel)
+    np.testing.assert_allclose(dWs, dW[vsel], rtol=1e-13, atol=1e-15)
+    sel = np.array([2, 0])
+    rdh, rdW = ref.backward(d["h"], d["W"], d["targets"], rows, 0.7, g1, g2, "bf16",
+                            dh_rows_sel=sel, vsel=vsel)
+    np.testing.assert_allclose(rdh, dh[sel], rtol=1e-10, atol=1e-13)
+    np.testing.assert_allclose(rdW, dW[vsel], rtol=1e-10, atol=1e-13)
+
+
+# --------------------------------------------------------------------------
+# the two restatements agree on real workload shapes
+
+def test_c_and_numpy_agree_config0():
+    d = workloads.make(0)
+    c = coracle.logprob_entropy(d["h"], d["W"], d["targets"], None, 1.0, "bf16")
+    n = ref.logprob_entropy(d["h"], d["W"], d["targets"], None, 1.0, "bf16")
+    for k in ("logp", "ent", "lse", "ez"):
+        np.testing.assert_allclose(c[k], n[k], rtol=1e-12, atol=1e-11)
+
+
+def test_c_and_numpy_agree_packed_fp16():
+    w = workloads.WORKLOADS[2].scaled(T=3000, H=64, V=1000)
+    d = workloads.make(w)
+    rows = d["row_idx"].numpy()
+    assert 0 < rows.shape[0] < 3000
+    c = coracle.logprob_entropy(d["h"], d["W"], d["targets"], rows, 1.0, "fp16")
+    n = ref.logprob_entropy(d["h"], d["W"], d["targets"], rows, 1.0, "fp16")
+    for k in ("logp", "ent"):
+        np.testing.assert_allclose(c[k], n[k], rtol=1e-12, atol=1e-11)
+
+
+def test_c_and_numpy_agree_kl():
+    w = workloads.WORKLOADS[3].scaled(T=40, H=64, V=900)
+    d = workloads.make(w)
+    a = coracle.kl(d["h_s"], d["W_s"], d["h_t"], d["W_t"], None, "bf16")
+    b = ref.kl(d["h_s"], d["W_s"], d["h_t"], d["W_t"], None, "bf16")
+    np.testing.assert_allclose(a, b, rtol=1e-10, atol=1e-13)
