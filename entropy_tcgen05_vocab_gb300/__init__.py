@@ -1,0 +1,272 @@
+"""Fused LM-head token scoring on GB300 (sm_103a): Python binding of libfusedlogp.
+
+This module only marshals arguments: it checks tensor layouts, allocates the
+outputs and the workspace with torch, and passes raw device pointers and the
+current CUDA stream to the C ABI declared in ``include/fusedlogp.h``.  Every
+step of the computation runs in the library's CUDA kernels; there is no CPU
+or PyTorch fallback, and a missing library raises.
+
+    logp, ent = logprob_entropy(h, W, targets, row_idx, temperature)
+    kl = kl_divergence(h_s, W_s, h_t, W_t, row_idx)
+    dh, dW = backward(h, W, targets, row_idx, temperature, g1, g2)
+    logp, ent = FusedLogProbEntropy.apply(h, W, targets, row_idx, temperature)
+"""
+import ctypes
+import os
+
+import torch
+
+from . import _build
+
+__all__ = ["lib", "build", "workspace_size", "logprob_entropy", "kl_divergence", "backward",
+           "read_device_status", "plan", "row_chunks", "FusedLogProbEntropy", "FlpError",
+           "OP_LOGPROB_ENTROPY", "OP_KL", "OP_BACKWARD"]
+
+OP_LOGPROB_ENTROPY, OP_KL, OP_BACKWARD = 0, 1, 2
+_DTYPES = {torch.bfloat16: 0, torch.float16: 1}
+
+
+class FlpError(RuntimeError):
+    def __init__(self, status, msg):
+        super().__init__("libfusedlogp: %s (status %d)" % (msg, status))
+        self.status = status
+
+
+class FlpShape(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int64), ("H", ctypes.c_int64), ("V", ctypes.c_int64),
+                ("n_rows", ctypes.c_int64), ("dtype", ctypes.c_int),
+                ("ld_h", ctypes.c_int64), ("ld_w", ctypes.c_int64)]
+
+
+class FlpDeviceStatus(ctypes.Structure):
+    _fields_ = [("bad_targets", ctypes.c_uint32), ("bad_rows", ctypes.c_uint32),
+                ("timeouts", ctypes.c_uint32), ("reserved", ctypes.c_uint32)]
+
+
+class FlpPlan(ctypes.Structure):
+    _fields_ = [("row_tiles", ctypes.c_int32), ("vocab_tiles", ctypes.c_int32),
+                ("block_n", ctypes.c_int32), ("splits", ctypes.c_int32),
+                ("tiles_per_split", ctypes.c_int32), ("band", ctypes.c_int32),
+                ("items", ctypes.c_int32), ("grid", ctypes.c_int32),
+                ("max_tiles_per_cta", ctypes.c_int64)]
+
+
+_lib = None
+
+
+def build(force=False, verbose=False):
+    """Compile libfusedlogp.so in-tree (nvcc, sm_103a)."""
+    return _build.build(force=force, verbose=verbose)
+
+
+def lib():
+    """The loaded library.  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_build.LIB):
+        raise RuntimeError("libfusedlogp.so is not built; call entropy_tcgen05_vocab_gb300.build()")
+    L = ctypes.CDLL(_build.LIB)
+    vp, i64, f32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    shp = ctypes.POINTER(FlpShape)
+    L.flp_workspace_size.argtypes = [shp, ctypes.c_int]
+    L.flp_workspace_size.restype = sz
+    L.flp_logprob_entropy.argtypes = [shp, vp, vp, vp, vp, f32, vp, vp, vp, vp, vp, sz, vp]
+    L.flp_kl.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.flp_backward.argtypes = [shp, vp, vp, vp, vp, f32, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.flp_read_device_status.argtypes = [vp, ctypes.POINTER(FlpDeviceStatus), vp]
+    L.flp_status_string.argtypes = [ctypes.c_int]
+    L.flp_status_string.restype = ctypes.c_char_p
+    L.flp_last_error.restype = ctypes.c_char_p
+    L.flp_plan_scoring.argtypes = [shp, ctypes.c_int, ctypes.c_int32, ctypes.POINTER(FlpPlan)]
+    L.flp_row_chunks.argtypes = [i64, i64, ctypes.POINTER(ctypes.c_int64), i64]
+    L.flp_row_chunks.restype = i64
+    for f in (L.flp_logprob_entropy, L.flp_kl, L.flp_backward, L.flp_read_device_status,
+              L.flp_plan_scoring):
+        f.restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def _check(status):
+    if status != 0:
+        L = lib()
+        msg = L.flp_last_error().decode() or L.flp_status_string(status).decode()
+        raise FlpError(status, msg)
+
+
+def make_shape(T, H, V, n_rows, dtype, ld_h=None, ld_w=None):
+    return FlpShape(T, H, V, n_rows, _DTYPES[dtype] if isinstance(dtype, torch.dtype) else dtype,
+                    H if ld_h is None else ld_h, H if ld_w is None else ld_w)
+
+
+def workspace_size(shape, op):
+    return int(lib().flp_workspace_size(ctypes.byref(shape), op))
+
+
+def plan(shape, op, num_sms):
+    """Tiling plan the library would use on a device with ``num_sms`` SMs."""
+    out = FlpPlan()
+    _check(lib().flp_plan_scoring(ctypes.byref(shape), op, num_sms, ctypes.byref(out)))
+    return {k: getattr(out, k) for k, _ in FlpPlan._fields_}
+
+
+def row_chunks(n_rows, chunk_rows):
+    """Row-chunk lengths of the backward (the pages' chunk rule)."""
+    k = lib().flp_row_chunks(n_rows, chunk_rows, None, 0)
+    buf = (ctypes.c_int64 * max(k, 1))()
+    lib().flp_row_chunks(n_rows, chunk_rows, buf, k)
+    return [int(buf[i]) for i in range(k)]
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _matrix(x, name):
+    if not isinstance(x, torch.Tensor) or not x.is_cuda:
+        raise TypeError("%s must be a CUDA tensor" % name)
+    if x.dim() != 2 or x.dtype not in _DTYPES or x.stride(1) != 1:
+        raise TypeError("%s must be a 2-D bf16/fp16 tensor with unit column stride" % name)
+    return x
+
+
+def _index(x, name, device):
+    if x is None:
+        return None
+    if not isinstance(x, torch.Tensor) or x.device != device:
+        raise TypeError("%s must be a tensor on %s" % (name, device))
+    return x.to(torch.int64).contiguous()
+
+
+def _vector(x, name, n, device):
+    if x is None:
+        return None
+    if not isinstance(x, torch.Tensor) or x.device != device or x.numel() != n:
+        raise TypeError("%s must be a [%d] tensor on %s" % (name, n, device))
+    return x.to(torch.float32).contiguous()
+
+
+def _workspace(shape, op, device, workspace):
+    need = workspace_size(shape, op)
+    if need == 0:
+        raise FlpError(1, "invalid shape")
+    if workspace is not None and workspace.numel() >= need:
+        return workspace
+    return torch.empty(need, dtype=torch.uint8, device=device)
+
+
+def logprob_entropy(h, W, targets, row_idx=None, temperature=1.0, *, return_stats=False,
+                    workspace=None):
+    """Target log-prob and entropy of softmax(h[row_idx] W^T / temperature).
+
+    h [T,H] and W [V,H] bf16/fp16 on the same GPU; targets int64 [T] indexed
+    by h row; row_idx int64 [n] (or None: every row).  Returns float32 [n]
+    tensors (logp, ent), plus (lse, ez) if ``return_stats``.
+    """
+    _matrix(h, "h")
+    _matrix(W, "W")
+    dev = h.device
+    if W.device != dev or W.dtype != h.dtype or W.shape[1] != h.shape[1]:
+        raise TypeError("W must match h in device, dtype and hidden size")
+    tg = _index(targets, "targets", dev)
+    ri = _index(row_idx, "row_idx", dev)
+    n = h.shape[0] if ri is None else ri.numel()
+    shape = make_shape(h.shape[0], h.shape[1], W.shape[0], n, h.dtype, h.stride(0), W.stride(0))
+    logp = torch.empty(n, dtype=torch.float32, device=dev)
+    ent = torch.empty(n, dtype=torch.float32, device=dev)
+    lse = torch.empty(n, dtype=torch.float32, device=dev) if return_stats else None
+    ez = torch.empty(n, dtype=torch.float32, device=dev) if return_stats else None
+    ws = _workspace(shape, OP_LOGPROB_ENTROPY, dev, workspace)
+    with torch.cuda.device(dev):
+        _check(lib().flp_logprob_entropy(ctypes.byref(shape), _ptr(h), _ptr(W), _ptr(tg), _ptr(ri),
+                                         float(temperature), _ptr(logp), _ptr(ent), _ptr(lse),
+                                         _ptr(ez), _ptr(ws), ws.numel(), _stream(dev)))
+    if return_stats:
+        return logp, ent, lse, ez
+    return logp, ent
+
+
+def kl_divergence(h_s, W_s, h_t, W_t, row_idx=None, *, workspace=None):
+    """Full-vocabulary KL(teacher || student) per scored row (float32 [n])."""
+    for x, nm in ((h_s, "h_s"), (W_s, "W_s"), (h_t, "h_t"), (W_t, "W_t")):
+        _matrix(x, nm)
+    dev = h_s.device
+    if not (h_s.shape == h_t.shape and W_s.shape == W_t.shape and h_s.shape[1] == W_s.shape[1]):
+        raise TypeError("student and teacher must share shapes")
+    if h_t.stride(0) != h_s.stride(0) or W_t.stride(0) != W_s.stride(0):
+        raise TypeError("student and teacher must share row strides")
+    if len({x.dtype for x in (h_s, W_s, h_t, W_t)}) != 1:
+        raise TypeError("student and teacher must share dtype")
+    ri = _index(row_idx, "row_idx", dev)
+    n = h_s.shape[0] if ri is None else ri.numel()
+    shape = make_shape(h_s.shape[0], h_s.shape[1], W_s.shape[0], n, h_s.dtype, h_s.stride(0),
+                       W_s.stride(0))
+    out = torch.empty(n, dtype=torch.float32, device=dev)
+    ws = _workspace(shape, OP_KL, dev, workspace)
+    with torch.cuda.device(dev):
+        _check(lib().flp_kl(ctypes.byref(shape), _ptr(h_s), _ptr(W_s), _ptr(h_t), _ptr(W_t),
+                            _ptr(ri), _ptr(out), _ptr(ws), ws.numel(), _stream(dev)))
+    return out
+
+
+def backward(h, W, targets, row_idx, temperature, g1, g2, lse=None, ez=None, *, workspace=None):
+    """dL/dh (dtype of h, [T,H]) and dL/dW (float32 [V,H]) of
+    L = sum g1 * logp + g2 * ent, by tile recompute."""
+    _matrix(h, "h")
+    _matrix(W, "W")
+    dev = h.device
+    tg = _index(targets, "targets", dev)
+    ri = _index(row_idx, "row_idx", dev)
+    n = h.shape[0] if ri is None else ri.numel()
+    g1 = _vector(g1, "g1", n, dev)
+    g2 = _vector(g2, "g2", n, dev)
+    lse = _vector(lse, "lse", n, dev)
+    ez = _vector(ez, "ez", n, dev)
+    shape = make_shape(h.shape[0], h.shape[1], W.shape[0], n, h.dtype, h.shape[1], W.shape[1])
+    dh = torch.empty((h.shape[0], h.shape[1]), dtype=h.dtype, device=dev)
+    dW = torch.empty((W.shape[0], W.shape[1]), dtype=torch.float32, device=dev)
+    if h.stride(0) != h.shape[1] or W.stride(0) != W.shape[1]:
+        h = h.contiguous()
+        W = W.contiguous()
+    ws = _workspace(shape, OP_BACKWARD, dev, workspace)
+    with torch.cuda.device(dev):
+        _check(lib().flp_backward(ctypes.byref(shape), _ptr(h), _ptr(W), _ptr(tg), _ptr(ri),
+                                  float(temperature), _ptr(g1), _ptr(g2), _ptr(lse), _ptr(ez),
+                                  _ptr(dh), _ptr(dW), _ptr(ws), ws.numel(), _stream(dev)))
+    return dh, dW
+
+
+def read_device_status(workspace, device=None):
+    """Counters the device recorded on ``workspace`` (synchronises the stream)."""
+    dev = workspace.device if device is None else device
+    st = FlpDeviceStatus()
+    rc = lib().flp_read_device_status(_ptr(workspace), ctypes.byref(st), _stream(dev))
+    if rc not in (0, 5):
+        _check(rc)
+    return {k: getattr(st, k) for k, _ in FlpDeviceStatus._fields_[:3]}
+
+
+class FusedLogProbEntropy(torch.autograd.Function):
+    """Autograd op: (h, W) -> (logp, ent); backward by tile recompute."""
+
+    @staticmethod
+    def forward(ctx, h, W, targets, row_idx=None, temperature=1.0):
+        logp, ent, lse, ez = logprob_entropy(h, W, targets, row_idx, temperature,
+                                             return_stats=True)
+        ctx.save_for_backward(h, W, targets, row_idx, lse, ez)
+        ctx.temperature = temperature
+        return logp, ent
+
+    @staticmethod
+    def backward(ctx, g_logp, g_ent):
+        h, W, targets, row_idx, lse, ez = ctx.saved_tensors
+        n = lse.numel()
+        g1 = g_logp if g_logp is not None else torch.zeros(n, device=h.device)
+        g2 = g_ent if g_ent is not None else torch.zeros(n, device=h.device)
+        dh, dW = backward(h, W, targets, row_idx, ctx.temperature, g1, g2, lse, ez)
+        return dh, dW.to(W.dtype), None, None, None

@@ -1,0 +1,426 @@
+// api.cu -- host side of libfusedlogp: argument validation, workspace
+// layout, the tiling planner, tensor-map construction and the C entry
+// points declared in include/fusedlogp.h.
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+#include <vector>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fusedlogp.h"
+#include "launch.h"
+
+namespace flp {
+namespace {
+
+thread_local char g_err[512] = "";
+
+flp_status fail(flp_status s, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof g_err, fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+flp_status cuda_fail(cudaError_t e, const char *what) {
+  return fail(FLP_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr int64_t kMaxSplits = 64;
+constexpr size_t kAlign = 1024;
+constexpr size_t kStatusBytes = 256;
+// Upper bound of the backward's logit-gradient chunk.
+constexpr int64_t kGradChunkBytes = int64_t(4) << 30;
+// L2 budget of one band's hidden rows.
+constexpr int64_t kBandBytes = int64_t(48) << 20;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+bool shape_ok(const flp_shape *s, const char **why) {
+  if (!s) return *why = "shape is NULL", false;
+  if (s->T < 0 || s->H <= 0 || s->V <= 0 || s->n_rows < 0) return *why = "negative or zero size", false;
+  if (s->dtype != FLP_BF16 && s->dtype != FLP_FP16) return *why = "dtype must be FLP_BF16 or FLP_FP16", false;
+  if (s->H % 8 || s->ld_h % 8 || s->ld_w % 8) return *why = "H, ld_h and ld_w must be multiples of 8", false;
+  if (s->ld_h < s->H || s->ld_w < s->H) return *why = "ld_h and ld_w must be >= H", false;
+  // Tile coordinates and row indices inside the kernels are 32-bit.
+  if (s->n_rows > (int64_t(1) << 30) || s->V > (int64_t(1) << 30) || s->H > (int64_t(1) << 24))
+    return *why = "size beyond the 32-bit tiling range", false;
+  return true;
+}
+
+int vocab_tiles(int64_t V, int bn) { return static_cast<int>(cdiv(V, bn)); }
+
+int max_splits(int64_t V, int bn) {
+  return static_cast<int>(std::min<int64_t>(vocab_tiles(V, bn), kMaxSplits));
+}
+
+// Rows of the backward's logit-gradient chunk.
+int64_t grad_chunk_rows(const flp_shape *s) {
+  const int64_t ldg = cdiv(s->V, 8) * 8;
+  int64_t r = kGradChunkBytes / (ldg * 2);
+  r = std::max<int64_t>(128, r / 128 * 128);
+  return std::min<int64_t>(r, std::max<int64_t>(s->n_rows, 1));
+}
+
+struct Layout {
+  size_t status = 0, zt = 0, pm = 0, ps = 0, pb = 0, pc = 0, pm2 = 0, ps2 = 0;
+  size_t hs = 0, hs2 = 0, lse = 0, ez = 0, g = 0, total = 0;
+  int64_t grad_rows = 0;
+};
+
+Layout layout_for(const flp_shape *s, flp_op op) {
+  Layout L;
+  const size_t n = static_cast<size_t>(s->n_rows);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes);
+    return o;
+  };
+  L.status = take(kStatusBytes);
+  const int bn = (op == FLP_OP_KL) ? kKlBN : kFwdBN;
+  const size_t sm = static_cast<size_t>(max_splits(s->V, bn));
+  L.pm = take(sm * n * 4);
+  L.ps = take(sm * n * 4);
+  L.pb = take(sm * n * 4);
+  if (op == FLP_OP_KL) {
+    L.pm2 = take(sm * n * 4);
+    L.ps2 = take(sm * n * 4);
+  } else {
+    L.zt = take(n * 4);
+  }
+  L.hs = take(n * static_cast<size_t>(s->H) * 2);
+  if (op == FLP_OP_KL) L.hs2 = take(n * static_cast<size_t>(s->H) * 2);
+  if (op == FLP_OP_BACKWARD) {
+    L.lse = take(n * 4);
+    L.ez = take(n * 4);
+    L.grad_rows = grad_chunk_rows(s);
+    L.g = take(static_cast<size_t>(L.grad_rows) * static_cast<size_t>(cdiv(s->V, 8) * 8) * 2);
+  }
+  L.total = off;
+  return L;
+}
+
+// ------------------------------------------------------------------ planner
+struct PlanKey {
+  int64_t n, V, H;
+  int bn, sms;
+  bool operator<(const PlanKey &o) const {
+    return std::tie(n, V, H, bn, sms) < std::tie(o.n, o.V, o.H, o.bn, o.sms);
+  }
+};
+
+struct Plan {
+  Schedule sch;
+  int grid;
+  int64_t max_load;
+};
+
+std::mutex g_plan_mu;
+std::map<PlanKey, Plan> g_plans;
+
+Plan make_plan(int64_t n, int64_t V, int64_t H, int bn, int num_sms) {
+  Plan best{};
+  Schedule s{};
+  s.n = static_cast<int>(n);
+  s.V = static_cast<int>(V);
+  s.row_tiles = static_cast<int>(cdiv(n, 128));
+  s.vocab_tiles = vocab_tiles(V, bn);
+  s.k_blocks = static_cast<int>(cdiv(H, 64));
+  const int64_t a_tile_bytes = 128 * H * 2;
+  s.band = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(s.row_tiles, kBandBytes / a_tile_bytes)));
+  const int smax = max_splits(V, bn);
+  std::vector<int64_t> loads;
+  int64_t best_load = -1;
+  for (int S = 1; S <= smax; ++S) {
+    const int tps = static_cast<int>(cdiv(s.vocab_tiles, S));
+    if (cdiv(s.vocab_tiles, tps) != S) continue;  // an equivalent, smaller S exists
+    Schedule c = s;
+    c.splits = S;
+    c.tiles_per_split = tps;
+    c.items = s.row_tiles * S;
+    if (c.items > (1 << 22)) break;
+    const int grid = std::min(c.items, num_sms);
+    loads.assign(grid, 0);
+    for (int it = 0; it < c.items; ++it) {
+      int mt, sp, v0, v1;
+      c.item(it, mt, sp, v0, v1);
+      loads[it % grid] += v1 - v0;
+    }
+    const int64_t mk = *std::max_element(loads.begin(), loads.end());
+    // Keep the smallest S whose makespan is within 0.5% of the best.
+    if (best_load < 0 || mk * 1000 < best_load * 995) {
+      best_load = mk;
+      best.sch = c;
+      best.grid = grid;
+      best.max_load = mk;
+    }
+  }
+  return best;
+}
+
+Plan plan_cached(int64_t n, int64_t V, int64_t H, int bn, int num_sms) {
+  const PlanKey k{n, V, H, bn, num_sms};
+  std::lock_guard<std::mutex> g(g_plan_mu);
+  auto it = g_plans.find(k);
+  if (it != g_plans.end()) return it->second;
+  if (g_plans.size() > 256) g_plans.clear();
+  Plan p = make_plan(n, V, H, bn, num_sms);
+  g_plans.emplace(k, p);
+  return p;
+}
+
+// ------------------------------------------------------------------ device
+struct DeviceInfo {
+  int sms = 0;
+  bool ok = false;
+};
+
+std::mutex g_dev_mu;
+std::map<int, DeviceInfo> g_devs;
+
+flp_status device_info(DeviceInfo *out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> g(g_dev_mu);
+  auto it = g_devs.find(dev);
+  if (it == g_devs.end()) {
+    DeviceInfo d;
+    int major = 0, minor = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    d.ok = (major == 10 && minor == 3);
+    it = g_devs.emplace(dev, d).first;
+  }
+  if (!it->second.ok)
+    return fail(FLP_ERR_UNSUPPORTED, "device %d is not compute capability 10.3 (sm_103a)", dev);
+  *out = it->second;
+  return FLP_OK;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+flp_status get_encoder(EncodeTiledFn *out) {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+    if (err == cudaSuccess && q == cudaDriverEntryPointSuccess) fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  if (!fn) return fail(FLP_ERR_CUDA, "cuTensorMapEncodeTiled unavailable (%s)", cudaGetErrorString(err));
+  *out = fn;
+  return FLP_OK;
+}
+
+// 2-D map over a row-major [outer, ld] matrix of 16-bit elements using
+// `inner` columns; boxes of box_inner x box_outer, 128-byte swizzle.
+flp_status make_map(CUtensorMap *m, flp_dtype dt, const void *base, int64_t inner, int64_t outer,
+                    int64_t ld, int box_inner, int box_outer) {
+  EncodeTiledFn enc;
+  flp_status st = get_encoder(&enc);
+  if (st != FLP_OK) return st;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_outer)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(m, dt == FLP_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                         2, const_cast<void *>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FLP_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  return FLP_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+flp_status check_common(const flp_shape *s, flp_op op, const void *ws, size_t ws_bytes) {
+  const char *why = nullptr;
+  if (!shape_ok(s, &why)) return fail(FLP_ERR_INVALID_ARG, "%s", why);
+  if (!ws) return fail(FLP_ERR_WORKSPACE, "workspace is NULL");
+  const size_t need = layout_for(s, op).total;
+  if (ws_bytes < need)
+    return fail(FLP_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, need);
+  if (reinterpret_cast<uintptr_t>(ws) % 256)
+    return fail(FLP_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  return FLP_OK;
+}
+
+template <class T>
+T *at(void *ws, size_t off) {
+  return reinterpret_cast<T *>(static_cast<char *>(ws) + off);
+}
+
+}  // namespace
+}  // namespace flp
+
+using namespace flp;
+
+extern "C" {
+
+size_t flp_workspace_size(const flp_shape *shape, flp_op op) {
+  const char *why = nullptr;
+  if (!shape_ok(shape, &why)) return 0;
+  if (op != FLP_OP_LOGPROB_ENTROPY && op != FLP_OP_KL && op != FLP_OP_BACKWARD) return 0;
+  return layout_for(shape, op).total;
+}
+
+const char *flp_status_string(flp_status s) {
+  switch (s) {
+    case FLP_OK: return "ok";
+    case FLP_ERR_INVALID_ARG: return "invalid argument";
+    case FLP_ERR_UNSUPPORTED: return "unsupported device or size";
+    case FLP_ERR_WORKSPACE: return "workspace missing or too small";
+    case FLP_ERR_CUDA: return "CUDA error";
+    case FLP_ERR_DEVICE_STATUS: return "the device recorded a problem";
+  }
+  return "unknown status";
+}
+
+const char *flp_last_error(void) { return g_err; }
+
+flp_status flp_plan_scoring(const flp_shape *shape, flp_op op, int32_t num_sms, flp_plan *out) {
+  const char *why = nullptr;
+  if (!shape_ok(shape, &why)) return fail(FLP_ERR_INVALID_ARG, "%s", why);
+  if (!out || num_sms <= 0) return fail(FLP_ERR_INVALID_ARG, "out is NULL or num_sms <= 0");
+  if (op != FLP_OP_LOGPROB_ENTROPY && op != FLP_OP_KL && op != FLP_OP_BACKWARD)
+    return fail(FLP_ERR_INVALID_ARG, "unknown op");
+  std::memset(out, 0, sizeof *out);
+  if (shape->n_rows == 0) return FLP_OK;
+  const int bn = op == FLP_OP_KL ? kKlBN : kFwdBN;
+  const Plan p = plan_cached(shape->n_rows, shape->V, shape->H, bn, num_sms);
+  out->row_tiles = p.sch.row_tiles;
+  out->vocab_tiles = p.sch.vocab_tiles;
+  out->block_n = bn;
+  out->splits = p.sch.splits;
+  out->tiles_per_split = p.sch.tiles_per_split;
+  out->band = p.sch.band;
+  out->items = p.sch.items;
+  out->grid = p.grid;
+  out->max_tiles_per_cta = p.max_load;
+  return FLP_OK;
+}
+
+int64_t flp_row_chunks(int64_t n_rows, int64_t chunk_rows, int64_t *out_lengths, int64_t max_out) {
+  if (n_rows <= 0 || chunk_rows <= 0) return 0;
+  const int64_t num = (n_rows - 1) / chunk_rows + 1;
+  const int64_t each = cdiv(n_rows, num);
+  int64_t k = 0;
+  for (int64_t start = 0; start < n_rows; start += each, ++k)
+    if (out_lengths && k < max_out) out_lengths[k] = std::min(each, n_rows - start);
+  return k;
+}
+
+flp_status flp_logprob_entropy(const flp_shape *s, const void *h, const void *W,
+                               const int64_t *targets, const int64_t *row_idx, float temperature,
+                               float *out_logp, float *out_ent, float *out_lse, float *out_ez,
+                               void *ws, size_t ws_bytes, flp_stream_t stream) {
+  g_err[0] = 0;
+  flp_status st = check_common(s, FLP_OP_LOGPROB_ENTROPY, ws, ws_bytes);
+  if (st != FLP_OK) return st;
+  if (!(std::isfinite(temperature) && temperature > 0.f))
+    return fail(FLP_ERR_INVALID_ARG, "temperature must be finite and > 0");
+  if (!row_idx && s->n_rows != s->T)
+    return fail(FLP_ERR_INVALID_ARG, "row_idx is NULL but n_rows != T");
+  if (s->n_rows == 0) return FLP_OK;
+  if (!h || !W || !targets || !out_logp || !out_ent)
+    return fail(FLP_ERR_INVALID_ARG, "h, W, targets, out_logp and out_ent are required");
+  if (!aligned16(h) || !aligned16(W)) return fail(FLP_ERR_INVALID_ARG, "h and W must be 16-byte aligned");
+  DeviceInfo dev;
+  if ((st = device_info(&dev)) != FLP_OK) return st;
+
+  const Layout L = layout_for(s, FLP_OP_LOGPROB_ENTROPY);
+  const Plan p = plan_cached(s->n_rows, s->V, s->H, kFwdBN, dev.sms);
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  FwdArgs a{};
+  const void *A = h;
+  int64_t lda = s->ld_h;
+  if (row_idx) {
+    A = at<void>(ws, L.hs);
+    lda = s->H;
+  }
+  if ((st = make_map(&a.tmA, s->dtype, A, s->H, s->n_rows, lda, 64, 128)) != FLP_OK) return st;
+  if ((st = make_map(&a.tmB, s->dtype, W, s->H, s->V, s->ld_w, 64, kFwdBN)) != FLP_OK) return st;
+  a.sch = p.sch;
+  a.grid = p.grid;
+  a.bf16 = s->dtype == FLP_BF16;
+  a.targets = targets;
+  a.row_idx = row_idx;
+  a.T = s->T;
+  a.inv_tau = 1.0f / temperature;
+  a.scale_log2 = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+  a.pm = at<float>(ws, L.pm);
+  a.ps = at<float>(ws, L.ps);
+  a.pb = at<float>(ws, L.pb);
+  a.zt = at<float>(ws, L.zt);
+  a.out_logp = out_logp;
+  a.out_ent = out_ent;
+  a.out_lse = out_lse;
+  a.out_ez = out_ez;
+  a.status = at<uint32_t>(ws, L.status);
+
+  cudaError_t e = cudaMemsetAsync(a.status, 0, kStatusBytes, cs);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(status)");
+  if (row_idx) {
+    e = launch_gather(h, s->ld_h, row_idx, s->n_rows, s->T, s->H, at<void>(ws, L.hs), dev.sms, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "gather launch");
+  }
+  if ((e = launch_fwd_scoring(a, cs)) != cudaSuccess) return cuda_fail(e, "scoring launch");
+  if ((e = launch_fwd_merge(a, cs)) != cudaSuccess) return cuda_fail(e, "merge launch");
+  return FLP_OK;
+}
+
+flp_status flp_kl(const flp_shape *s, const void *, const void *, const void *, const void *,
+                  const int64_t *, float *, void *ws, size_t ws_bytes, flp_stream_t) {
+  g_err[0] = 0;
+  flp_status st = check_common(s, FLP_OP_KL, ws, ws_bytes);
+  if (st != FLP_OK) return st;
+  return fail(FLP_ERR_UNSUPPORTED, "flp_kl is not built yet");
+}
+
+flp_status flp_backward(const flp_shape *s, const void *, const void *, const int64_t *,
+                        const int64_t *, float, const float *, const float *, const float *,
+                        const float *, void *, float *, void *ws, size_t ws_bytes, flp_stream_t) {
+  g_err[0] = 0;
+  flp_status st = check_common(s, FLP_OP_BACKWARD, ws, ws_bytes);
+  if (st != FLP_OK) return st;
+  return fail(FLP_ERR_UNSUPPORTED, "flp_backward is not built yet");
+}
+
+flp_status flp_read_device_status(const void *ws, flp_device_status *out, flp_stream_t stream) {
+  g_err[0] = 0;
+  if (!ws || !out) return fail(FLP_ERR_INVALID_ARG, "workspace and out are required");
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(cs);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  uint32_t w[4];
+  e = cudaMemcpy(w, ws, sizeof w, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(status)");
+  out->bad_targets = w[kStatBadTarget];
+  out->bad_rows = w[kStatBadRow];
+  out->timeouts = w[kStatTimeout];
+  out->reserved = 0;
+  if (out->bad_targets || out->bad_rows || out->timeouts)
+    return fail(FLP_ERR_DEVICE_STATUS, "device status: %u bad targets, %u bad rows, %u timeouts",
+                out->bad_targets, out->bad_rows, out->timeouts);
+  return FLP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,254 @@
+// kernels_fwd.cu -- forward scoring: response-row gather, the fused
+// logits-tile -> online log-sum-exp/entropy pipeline, and the merge of the
+// per-split partial states into log-prob and entropy.
+//
+// Arithmetic (miles PR #2764 summary, "Implementation breakdown" item 2:
+// upcast first, temperature in FP32 after the upcast; entropy from the same
+// values).  The tensor cores accumulate z = h W^T in FP32; nothing is rounded
+// to model precision.  The epilogue works in base 2 on y = z * (log2 e / tau)
+// (one FP32 multiply per logit: z/tau and the change of base folded), so
+// every exponential is one ex2 on the special-function unit:
+//   m = max y,  S = sum 2^(y-m),  B = sum 2^(y-m) (y-m)
+// When m grows to m' the running sums are rescaled with a = 2^(m-m'):
+//   S <- a S,  B <- a (B + (m-m') S).
+// Then ln 2 (m + log2 S) = LSE(z/tau) and ln 2 (log2 S - B/S) = entropy.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "launch.h"
+#include "vocab_pipeline.cuh"
+
+namespace flp {
+
+constexpr float kLn2 = 0.693147180559945309f;
+
+// ---------------------------------------------------------------- row gather
+// hs[i, :] = h[row_idx[i], :] in 16-byte units, one warp per row.  Rows with
+// an out-of-range index are zero-filled (the merge reports them).
+__global__ void gather_rows_kernel(const uint4 *__restrict__ h, int64_t ld_h16,
+                                   const int64_t *__restrict__ row_idx, int64_t n, int64_t T,
+                                   int64_t H16, uint4 *__restrict__ hs) {
+  const int64_t warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  for (int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; i < n;
+       i += warps) {
+    const int64_t r = row_idx[i];
+    uint4 *dst = hs + i * H16;
+    if (r < 0 || r >= T) {
+      for (int64_t k = lane; k < H16; k += 32) dst[k] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
+    const uint4 *src = h + r * ld_h16;
+    for (int64_t k = lane; k < H16; k += 32) dst[k] = __ldg(src + k);
+  }
+}
+
+// ---------------------------------------------------------------- epilogue
+struct LseEpi {
+  struct Params {
+    const int64_t *targets;  // [T], by h row
+    const int64_t *row_idx;  // [n] or null
+    int64_t T;
+    int n;
+    int V;
+    float sl;                // log2(e) / tau
+    float *pm, *ps, *pb;     // [splits][n] partial m, S, B
+    float *zt;               // [n] raw FP32 logit of the target
+  };
+  const Params p;
+  float m, s0, s1, b0, b1, zt;
+  int tgt;
+  bool found;
+
+  __device__ __forceinline__ explicit LseEpi(const Params &pp) : p(pp) {}
+
+  __device__ __forceinline__ void begin(int /*mt*/, int row) {
+    m = -FLT_MAX;
+    s0 = s1 = b0 = b1 = 0.f;
+    zt = 0.f;
+    found = false;
+    tgt = -1;
+    if (row < p.n) {
+      const int64_t r = p.row_idx ? p.row_idx[row] : row;
+      if (r >= 0 && r < p.T) {
+        const int64_t t = p.targets[r];
+        if (t >= 0 && t < p.V) tgt = static_cast<int>(t);
+      }
+    }
+  }
+
+  __device__ __forceinline__ void rescale(float cmax) {
+    const float mn = fmaxf(m, cmax * p.sl);
+    if (mn > m) {
+      const float d = m - mn;
+      const float a = ex2(d);
+      b0 = a * fmaf(d, s0, b0);
+      b1 = a * fmaf(d, s1, b1);
+      s0 *= a;
+      s1 *= a;
+      m = mn;
+    }
+  }
+
+  __device__ __forceinline__ void fold_full(const float (&x)[32]) {
+    float cmax = x[0];
+#pragma unroll
+    for (int j = 1; j < 32; ++j) cmax = fmaxf(cmax, x[j]);
+    rescale(cmax);
+    const float nm = -m;
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+      const float d0 = fmaf(x[j], p.sl, nm);
+      const float d1 = fmaf(x[j + 1], p.sl, nm);
+      const float e0 = ex2(d0);
+      const float e1 = ex2(d1);
+      s0 += e0;
+      s1 += e1;
+      b0 = fmaf(e0, d0, b0);
+      b1 = fmaf(e1, d1, b1);
+    }
+  }
+
+  __device__ __forceinline__ void fold_masked(const float (&x)[32], int nv) {
+    float cmax = -FLT_MAX;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < nv) cmax = fmaxf(cmax, x[j]);
+    rescale(cmax);
+    const float nm = -m;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (j < nv) {
+        const float d = fmaf(x[j], p.sl, nm);
+        const float e = ex2(d);
+        s0 += e;
+        b0 = fmaf(e, d, b0);
+      }
+    }
+  }
+
+  __device__ __forceinline__ void tile(uint32_t taddr, int col0) {
+#pragma unroll 1
+    for (int c = 0; c < 8; ++c) {
+      const int cb = col0 + c * 32;
+      if (cb >= p.V) break;  // same for the whole warp
+      float x[32];
+      tmem_ld32(taddr + c * 32, x);
+      if (cb + 32 <= p.V)
+        fold_full(x);
+      else
+        fold_masked(x, p.V - cb);
+      const int rel = tgt - cb;
+      if (static_cast<unsigned>(rel) < 32u) {
+        float t = x[0];
+#pragma unroll
+        for (int j = 1; j < 32; ++j) t = (rel == j) ? x[j] : t;
+        zt = t;
+        found = true;
+      }
+    }
+  }
+
+  __device__ __forceinline__ void end(int split, int row) {
+    if (row >= p.n) return;
+    const size_t o = static_cast<size_t>(split) * p.n + row;
+    p.pm[o] = m;
+    p.ps[o] = s0 + s1;
+    p.pb[o] = b0 + b1;
+    if (found) p.zt[row] = zt;
+  }
+};
+
+// ---------------------------------------------------------------- merge
+// One thread per scored row: merge the split partials (m_i, S_i, B_i) with
+// M = max m_i, S = sum S_i 2^(m_i-M), B = sum 2^(m_i-M) (B_i + (m_i-M) S_i),
+// then logp = z_tgt/tau - LSE and entropy = ln2 (log2 S - B/S).
+__global__ void merge_kernel(int n, int splits, const float *__restrict__ pm,
+                             const float *__restrict__ ps, const float *__restrict__ pb,
+                             const float *__restrict__ zt, const int64_t *__restrict__ targets,
+                             const int64_t *__restrict__ row_idx, int64_t T, int V,
+                             float inv_tau, float *__restrict__ out_logp,
+                             float *__restrict__ out_ent, float *__restrict__ out_lse,
+                             float *__restrict__ out_ez, uint32_t *status) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  float M = -FLT_MAX;
+  for (int s = 0; s < splits; ++s) M = fmaxf(M, pm[static_cast<size_t>(s) * n + i]);
+  float S = 0.f, B = 0.f;
+  for (int s = 0; s < splits; ++s) {
+    const size_t o = static_cast<size_t>(s) * n + i;
+    const float d = pm[o] - M;
+    const float a = exp2f(d);
+    const float si = ps[o];
+    S = fmaf(si, a, S);
+    B = fmaf(a, fmaf(d, si, pb[o]), B);
+  }
+  const float l2s = log2f(S);
+  float lse = kLn2 * (M + l2s);
+  float ent = kLn2 * (l2s - B / S);
+  float logp;
+  const int64_t r = row_idx ? row_idx[i] : i;
+  if (r < 0 || r >= T) {
+    atomicAdd(status + kStatBadRow, 1u);
+    lse = ent = logp = __int_as_float(0x7fc00000);
+  } else {
+    const int64_t t = targets[r];
+    if (t < 0 || t >= V) {
+      atomicAdd(status + kStatBadTarget, 1u);
+      logp = __int_as_float(0x7fc00000);
+    } else {
+      logp = zt[i] * inv_tau - lse;
+    }
+  }
+  out_logp[i] = logp;
+  out_ent[i] = ent;
+  if (out_lse) out_lse[i] = lse;
+  if (out_ez) out_ez[i] = lse - ent;
+}
+
+// ---------------------------------------------------------------- launchers
+cudaError_t launch_gather(const void *h, int64_t ld_h, const int64_t *row_idx, int64_t n,
+                          int64_t T, int64_t H, void *hs, int num_sms, cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  const int64_t warps_needed = n;
+  int64_t blocks = (warps_needed + 7) / 8;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+  if (blocks > cap) blocks = cap;
+  gather_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      static_cast<const uint4 *>(h), ld_h / 8, row_idx, n, T, H / 8, static_cast<uint4 *>(hs));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_scoring(const FwdArgs &a, cudaStream_t stream) {
+  using L = PipeLayout<kFwdBN, kFwdStages>;
+  auto kern = vocab_pipeline_kernel<kFwdBN, kFwdStages, LseEpi>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  LseEpi::Params p;
+  p.targets = a.targets;
+  p.row_idx = a.row_idx;
+  p.T = a.T;
+  p.n = a.sch.n;
+  p.V = a.sch.V;
+  p.sl = a.scale_log2;
+  p.pm = a.pm;
+  p.ps = a.ps;
+  p.pb = a.pb;
+  p.zt = a.zt;
+  const uint32_t idesc = idesc_f16(a.bf16, kBM, kFwdBN, false, false);
+  kern<<<a.grid, kPipeThreads, L::kSmemBytes, stream>>>(a.tmA, a.tmB, a.sch, idesc, p, a.status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_merge(const FwdArgs &a, cudaStream_t stream) {
+  const int n = a.sch.n;
+  merge_kernel<<<(n + 255) / 256, 256, 0, stream>>>(
+      n, a.sch.splits, a.pm, a.ps, a.pb, a.zt, a.targets, a.row_idx, a.T, a.sch.V, a.inv_tau,
+      a.out_logp, a.out_ent, a.out_lse, a.out_ez, a.status);
+  return cudaGetLastError();
+}
+
+int fwd_smem_bytes() { return PipeLayout<kFwdBN, kFwdStages>::kSmemBytes; }
+
+}  // namespace flp

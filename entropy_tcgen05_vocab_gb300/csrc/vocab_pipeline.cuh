@@ -1,0 +1,247 @@
+// vocab_pipeline.cuh -- the persistent tensor-core pipeline that streams the
+// LM-head weight W past 128-row tiles of hidden states and hands each
+// 128 x BN FP32 logit tile, straight out of tensor memory, to an epilogue.
+//
+// This is the "output layer on the rows it scores, a tile at a time" loop of
+// miles PR #4645 ("How it works": Op) with the tile living in TMEM instead
+// of a [tile, vocab] buffer: no logit ever reaches global memory.
+//
+// Work decomposition.  Rows are cut into 128-row tiles, the vocabulary into
+// BN-column tiles.  A work item is (row tile, vocabulary split): one CTA
+// sweeps the split's vocabulary tiles for its row tile, keeping per-row
+// running state in registers, and emits one partial state per row and item.
+// Items are ordered band by band (a band = `band` consecutive row tiles, all
+// splits of the band, row tiles fastest) so the CTAs resident at one time
+// share the same weight tiles and each W tile is read from HBM about once
+// per band while the band's hidden rows stay in L2.  Persistent CTAs take
+// items round robin.
+//
+// Roles (192 threads):
+//   warp 0     TMA producer: A (hidden rows, K-major) and B (W rows, K-major)
+//              per 64-wide K block into a STAGES-deep ring of 128B-swizzled
+//              shared-memory stages.
+//   warp 1     TMEM allocation + tcgen05.mma issue (one elected lane),
+//              M=128, N=BN, K=16 per instruction, FP32 accumulators in a
+//              double-buffered TMEM region (2 x BN columns).
+//   warps 2-5  epilogue: tcgen05.ld of their 32 TMEM lanes (= 32 rows),
+//              32 columns at a time, folded by the Epi policy.
+#pragma once
+
+#include <cfloat>
+#include <cstdint>
+
+#include "ptx.cuh"
+#include "schedule.h"
+
+namespace flp {
+
+constexpr int kBM = 128;         // rows per tile (TMEM lanes)
+constexpr int kBK = 64;          // K elements per stage = one 128-byte swizzle row
+constexpr int kUmmaK = 16;       // K per tcgen05.mma kind::f16
+constexpr int kEpiWarps = 4;
+constexpr int kPipeThreads = 64 + 32 * kEpiWarps;
+
+
+template <int BN, int STAGES>
+struct PipeLayout {
+  static constexpr int kABytes = kBM * kBK * 2;
+  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kTmemCols = 2 * BN;
+  static constexpr int kBarrierBytes = 8 * (2 * STAGES + 5) + 16;
+  // + 1024 so the stage ring can be aligned to a swizzle atom.
+  static constexpr int kSmemBytes = STAGES * kStageBytes + kBarrierBytes + 1024;
+  static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM columns must be a power of two");
+};
+
+__device__ __forceinline__ void record_timeout(uint32_t *status, volatile int *abort_flag) {
+  *abort_flag = 1;
+  atomicAdd(status + kStatTimeout, 1u);
+}
+
+// Epi must provide:
+//   struct Params;
+//   __device__ Epi(const Params&);
+//   __device__ void begin(int mt, int row);               row = global scored row of this thread
+//   __device__ void tile(uint32_t taddr, int col0);       taddr = TMEM address of this warp's
+//                                                          lanes at the tile's first column
+//   __device__ void end(int split, int row);
+template <int BN, int STAGES, class Epi>
+__global__ void __launch_bounds__(kPipeThreads, 1)
+    vocab_pipeline_kernel(const __grid_constant__ CUtensorMap tmA,
+                          const __grid_constant__ CUtensorMap tmB, const Schedule sch,
+                          const uint32_t idesc, const typename Epi::Params ep,
+                          uint32_t *status) {
+  using L = PipeLayout<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * L::kStageBytes);
+  uint64_t *empty = full + STAGES;
+  uint64_t *tfull = empty + STAGES;
+  uint64_t *tempty = tfull + 2;
+  uint64_t *drain = tempty + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], kEpiWarps);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, L::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t armed = 0;  // bit s: stage s has been armed at least once
+    bool ok = true;
+    for (int it = blockIdx.x; ok && it < sch.items; it += gridDim.x) {
+      int mt, sp, vt0, vt1;
+      sch.item(it, mt, sp, vt0, vt1);
+      for (int vt = vt0; ok && vt < vt1; ++vt) {
+        for (int kb = 0; kb < sch.k_blocks; ++kb) {
+          if (lane == 0) ok = mbar_wait(&empty[stage], phase ^ 1u, abort_flag);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          if (lane == 0) {
+            uint8_t *sa = smem + stage * L::kStageBytes;
+            mbar_arrive_expect_tx(&full[stage], L::kStageBytes);
+            tma_load_2d(sa, &tmA, &full[stage], kb * kBK, mt * kBM);
+            tma_load_2d(sa + L::kABytes, &tmB, &full[stage], kb * kBK, vt * BN);
+          }
+          armed |= 1u << stage;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+    if (!ok) {
+      if (lane == 0) {
+        record_timeout(status, abort_flag);
+        // Let the copies already in flight land before the CTA leaves.
+        for (int s = 0; s < STAGES; ++s) {
+          if (!(armed & (1u << s))) continue;
+          // Stage s was last armed in the phase before the current one for
+          // stages behind `stage`, in the current one otherwise.
+          const uint32_t par = (s < stage) ? phase : (phase ^ 1u);
+          int never = 0;
+          mbar_wait(&full[s], par, &never);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; ok && it < sch.items; it += gridDim.x) {
+      int mt, sp, vt0, vt1;
+      sch.item(it, mt, sp, vt0, vt1);
+      for (int vt = vt0; ok && vt < vt1; ++vt) {
+        if (lane == 0) ok = mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < sch.k_blocks; ++kb) {
+          if (lane == 0) ok = mbar_wait(&full[stage], phase, abort_flag);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t a0 = smem_u32(smem + stage * L::kStageBytes);
+            const uint32_t b0 = a0 + L::kABytes;
+#pragma unroll
+            for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
+              const uint64_t ad = sdesc_sw128(a0 + kk * kUmmaK * 2, 16, 1024);
+              const uint64_t bd = sdesc_sw128(b0 + kk * kUmmaK * 2, 16, 1024);
+              mma_f16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            }
+            mma_commit(&empty[stage]);  // frees the stage when these MMAs finish
+          }
+          __syncwarp();
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        if (lane == 0) mma_commit(&tfull[acc]);  // accumulator ready for the epilogue
+        __syncwarp();
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+    }
+    if (!ok && lane == 0) {
+      record_timeout(status, abort_flag);
+      // Wait for the MMAs already issued before TMEM is released.
+      mma_commit(drain);
+      int never = 0;
+      mbar_wait(drain, 0, &never);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int lg = warp & 3;  // the TMEM lane quarter this warp may access
+    const uint32_t lane_off = static_cast<uint32_t>(lg * 32) << 16;
+    Epi epi(ep);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; ok && it < sch.items; it += gridDim.x) {
+      int mt, sp, vt0, vt1;
+      sch.item(it, mt, sp, vt0, vt1);
+      const int row = mt * kBM + lg * 32 + lane;
+      epi.begin(mt, row);
+      for (int vt = vt0; vt < vt1; ++vt) {
+        if (lane == 0) ok = mbar_wait(&tfull[acc], acc_phase, abort_flag);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        tc_fence_after();
+        epi.tile(tmem_base + lane_off + static_cast<uint32_t>(acc * BN), vt * BN);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      if (!ok) break;
+      epi.end(sp, row);
+    }
+    if (!ok && lane == 0) record_timeout(status, abort_flag);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, L::kTmemCols);
+}
+
+}  // namespace flp

@@ -1,0 +1,212 @@
+/*
+ * fusedlogp.h -- C ABI of libfusedlogp: fused LM-head token scoring on one
+ * GB300 GPU (sm_103a).
+ *
+ * For each scored row r of the hidden states h[T,H] the library forms the
+ * logits z = h[r] W^T one vocabulary tile at a time on the tensor cores
+ * (FP32 accumulation), divides by the temperature in FP32 after that
+ * upcast, and folds each tile into a per-row online log-sum-exp.  The
+ * [T,V] logits are never written to memory.
+ *
+ * Pages this follows:
+ *   - miles PR #2764 summary (prhub), "Implementation breakdown" items 2-4:
+ *     upcast each chunk of logits to FP32, then apply the temperature in
+ *     FP32; log-prob and entropy come from the same upcast values; FP16
+ *     and BF16 inputs are both accepted; sums accumulate in FP32.
+ *   - miles PR #4645 ("--log-probs-backend fused_lm_head"), "How it works":
+ *     the output layer runs only on the rows that are scored (response
+ *     rows), tile by tile, and the [tokens x vocab] logits and their
+ *     gradient are never materialised; the backward replays each tile.
+ *   - DeepSeek-V4 book ch. 19, "Never materialize logits" and "TileLang KL
+ *     kernel": teacher logits are rebuilt from cached hidden states through
+ *     the teacher head and an exact full-vocabulary KL is computed without
+ *     either logit tensor existing in memory, in a fixed (static) memory
+ *     layout.
+ *
+ * Conventions for every entry point:
+ *   - All array arguments are DEVICE pointers owned by the caller.  The
+ *     library allocates no device memory during a call: scratch space is the
+ *     caller's workspace, sized by flp_workspace_size().
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream) and is asynchronous.  No call synchronises, except
+ *     flp_read_device_status().
+ *   - Arguments are validated on the host before anything is enqueued; a
+ *     call that returns an error has enqueued nothing, except FLP_ERR_CUDA
+ *     from a failed launch.  flp_last_error() gives a one-line reason.
+ *   - Data-dependent problems do not fail the call: a target outside [0,V)
+ *     or a row_idx entry outside [0,T) yields NaN in that row's outputs and
+ *     is counted in the workspace's device status (flp_read_device_status).
+ *   - Matrices are row-major.  h is [T, ld_h] with H <= ld_h used columns;
+ *     W is [V, ld_w].  H, ld_h and ld_w must be multiples of 8 and h, W
+ *     16-byte aligned (tensor-memory-access copies move 16-byte units).
+ *   - n_rows == 0 is valid and enqueues nothing (the "no scored rows" case).
+ */
+#ifndef FUSEDLOGP_H
+#define FUSEDLOGP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without including the CUDA headers. */
+typedef struct CUstream_st *flp_stream_t;
+
+typedef enum {
+    FLP_OK = 0,
+    FLP_ERR_INVALID_ARG = 1,   /* null pointer, bad size, stride, alignment or temperature */
+    FLP_ERR_UNSUPPORTED = 2,   /* no usable sm_103a device, or a size beyond int32 tiling */
+    FLP_ERR_WORKSPACE = 3,     /* workspace null or smaller than flp_workspace_size() */
+    FLP_ERR_CUDA = 4,          /* a CUDA runtime/driver call or a launch failed */
+    FLP_ERR_DEVICE_STATUS = 5  /* flp_read_device_status(): the device recorded a problem */
+} flp_status;
+
+typedef enum { FLP_BF16 = 0, FLP_FP16 = 1 } flp_dtype;
+
+typedef enum {
+    FLP_OP_LOGPROB_ENTROPY = 0,
+    FLP_OP_KL = 1,
+    FLP_OP_BACKWARD = 2
+} flp_op;
+
+/*
+ * Problem shape.  n_rows is the number of scored rows: the length of
+ * row_idx, or T when row_idx is NULL.  dtype is the element type of h and W
+ * (and of dh in the backward).
+ */
+typedef struct {
+    int64_t T;       /* rows of h; entries of targets */
+    int64_t H;       /* hidden size: the contraction length */
+    int64_t V;       /* vocabulary size: rows of W */
+    int64_t n_rows;  /* scored rows */
+    flp_dtype dtype; /* FLP_BF16 or FLP_FP16 */
+    int64_t ld_h;    /* row stride of h (and dh) in elements, >= H */
+    int64_t ld_w;    /* row stride of W (and dW) in elements, >= H */
+} flp_shape;
+
+/* Problems the device counted during the last call on a workspace. */
+typedef struct {
+    uint32_t bad_targets; /* scored rows whose target was outside [0, V) */
+    uint32_t bad_rows;    /* row_idx entries outside [0, T) */
+    uint32_t timeouts;    /* pipeline waits that gave up; outputs of that call are invalid */
+    uint32_t reserved;
+} flp_device_status;
+
+/*
+ * Bytes of workspace `op` needs for `shape` (0 if the shape is invalid).
+ * The size is a function of the shape alone (not of the device or of
+ * whether row_idx is given); it is about n_rows*H*2 bytes for the gathered
+ * rows, plus O(n_rows * 64) bytes of per-row partial state, plus, for the
+ * backward, one bounded chunk of the bf16/fp16 logit gradient (at most
+ * 4 GiB; never a [T,V] buffer for the forward or KL).
+ */
+size_t flp_workspace_size(const flp_shape *shape, flp_op op);
+
+/*
+ * Target log-probability and entropy of softmax(z / temperature) per
+ * scored row, z = h[row] W^T.
+ *
+ *   h            [T, ld_h] bf16/fp16 hidden states
+ *   W            [V, ld_w] bf16/fp16 output-layer (LM head) weight
+ *   targets      [T] int64 target token of each h row (indexed by h row,
+ *                not by scored position)
+ *   row_idx      [n_rows] int64 rows of h to score, any order, duplicates
+ *                allowed; NULL scores rows 0..T-1 (then n_rows must be T)
+ *   temperature  finite and > 0; applied in FP32 after the FP32 upcast
+ *                (1 is an exact no-op)
+ *   out_logp     [n_rows] float: z'_tgt - logsumexp(z'),  z' = z / temperature
+ *   out_ent      [n_rows] float: entropy (nats) of softmax(z')
+ *   out_lse      [n_rows] float or NULL: logsumexp(z')
+ *   out_ez       [n_rows] float or NULL: E_p[z'] = out_lse - out_ent
+ * Outputs are compact, in row_idx order.
+ */
+flp_status flp_logprob_entropy(const flp_shape *shape, const void *h, const void *W,
+                               const int64_t *targets, const int64_t *row_idx,
+                               float temperature, float *out_logp, float *out_ent,
+                               float *out_lse, float *out_ez,
+                               void *workspace, size_t workspace_bytes, flp_stream_t stream);
+
+/*
+ * Full-vocabulary KL(teacher || student) per scored row:
+ *   KL = sum_v p_t,v (log p_t,v - log p_s,v),
+ *   p_s = softmax(h_s[row] W_s^T),  p_t = softmax(h_t[row] W_t^T),
+ * temperature 1, neither logit tensor materialised.  Student and teacher
+ * share shape (T, H, V, dtype, ld_h, ld_w).
+ *   h_s, h_t     [T, ld_h];  W_s, W_t [V, ld_w]
+ *   row_idx      [n_rows] int64 or NULL (all rows)
+ *   out_kl       [n_rows] float
+ */
+flp_status flp_kl(const flp_shape *shape, const void *h_s, const void *W_s,
+                  const void *h_t, const void *W_t, const int64_t *row_idx,
+                  float *out_kl, void *workspace, size_t workspace_bytes,
+                  flp_stream_t stream);
+
+/*
+ * Gradients of L = sum_i g1[i] logp_i + g2[i] ent_i (logp, ent as in
+ * flp_logprob_entropy) by tile recompute:
+ *   G_iv = (g1[i] (1[v = tgt_i] - p_iv) - g2[i] p_iv (z'_iv - E_p[z'_i])) / temperature
+ *   dh[row_idx[i], :] = sum_v G_iv W[v, :]      (dtype of h; rows not scored are 0)
+ *   dW[v, :]          = sum_i G_iv h[row_idx[i], :]   (float32, overwritten)
+ *   g1, g2       [n_rows] float upstream gradients of logp and ent
+ *   lse, ez      [n_rows] float from a previous flp_logprob_entropy with
+ *                the same inputs (out_lse, out_ez), or both NULL: the
+ *                statistics are then recomputed (one extra forward pass)
+ *   dh           [T, ld_h] dtype; dW [V, ld_w] float32
+ * row_idx entries must be distinct (a row scored twice would need its dh
+ * contributions summed; that is a precondition, not checked).
+ */
+flp_status flp_backward(const flp_shape *shape, const void *h, const void *W,
+                        const int64_t *targets, const int64_t *row_idx,
+                        float temperature, const float *g1, const float *g2,
+                        const float *lse, const float *ez, void *dh, float *dW,
+                        void *workspace, size_t workspace_bytes, flp_stream_t stream);
+
+/*
+ * Synchronises `stream` and copies the device status of the last call that
+ * used `workspace`.  Returns FLP_ERR_DEVICE_STATUS if any counter is
+ * non-zero (the counters are still copied), FLP_OK otherwise.
+ */
+flp_status flp_read_device_status(const void *workspace, flp_device_status *out,
+                                  flp_stream_t stream);
+
+/* Static description of a status code. */
+const char *flp_status_string(flp_status status);
+
+/* One-line reason for the last failure on the calling host thread ("" if none). */
+const char *flp_last_error(void);
+
+/*
+ * Tiling plan of the scoring kernels, for inspection and tests (pure host
+ * function; no GPU needed).  num_sms is the number of SMs to plan for.
+ */
+typedef struct {
+    int32_t row_tiles;      /* ceil(n_rows / 128) */
+    int32_t vocab_tiles;    /* ceil(V / block_n) */
+    int32_t block_n;        /* vocabulary columns per tensor-core tile */
+    int32_t splits;         /* vocabulary splits per row tile (partial states per row) */
+    int32_t tiles_per_split;
+    int32_t band;           /* row tiles that share the weight stream in one band */
+    int32_t items;          /* work items = row_tiles * splits */
+    int32_t grid;           /* persistent CTAs launched */
+    int64_t max_tiles_per_cta; /* load of the busiest CTA, in 128 x block_n tiles */
+} flp_plan;
+
+flp_status flp_plan_scoring(const flp_shape *shape, flp_op op, int32_t num_sms, flp_plan *out);
+
+/*
+ * Row chunks of the backward: the scored rows are processed in
+ * num_chunks = (n_rows - 1) / chunk_rows + 1 chunks of at most
+ * ceil(n_rows / num_chunks) rows each (the last one shorter), the chunking
+ * rule of the pages' calculate_log_probs_and_entropy.  Writes up to
+ * `max_out` chunk lengths; returns the number of chunks (0 for n_rows = 0).
+ */
+int64_t flp_row_chunks(int64_t n_rows, int64_t chunk_rows, int64_t *out_lengths,
+                       int64_t max_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FUSEDLOGP_H */

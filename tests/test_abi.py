@@ -1,0 +1,161 @@
+"""The C ABI on the host (CPU only, no GPU calls).
+
+Checks that libfusedlogp builds, loads and exports every function that
+include/fusedlogp.h declares; that invalid arguments are rejected on the host
+before anything is enqueued; the workspace formula; the tiling planner's
+invariants; and the backward's row-chunk rule against the pages' printed
+example and torch.chunk.
+"""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+import torch
+
+import entropy_tcgen05_vocab_gb300 as flp
+import workloads
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+FAKE = ctypes.c_void_p(1 << 20)   # never dereferenced: validation fails first
+
+
+@pytest.fixture(scope="module")
+def L():
+    flp.build()
+    return flp.lib()
+
+
+def declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"\b(flp_\w+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_function(L):
+    names = declared_functions()
+    assert len(names) >= 9
+    for nm in names:
+        assert hasattr(L, nm), nm
+
+
+def test_status_strings(L):
+    for code in range(6):
+        assert L.flp_status_string(code)
+    assert L.flp_status_string(99) == b"unknown status"
+
+
+def _shape(T=256, H=512, V=8192, n=256, dtype=0, ld_h=None, ld_w=None):
+    return flp.FlpShape(T, H, V, n, dtype, H if ld_h is None else ld_h, H if ld_w is None else ld_w)
+
+
+def _fwd(L, shape, tau=1.0, ws_bytes=1 << 40, ws=FAKE, h=FAKE, W=FAKE, row_idx=None,
+         targets=FAKE, out=FAKE):
+    return L.flp_logprob_entropy(ctypes.byref(shape) if shape is not None else None, h, W,
+                                 targets, row_idx, tau, out, out, None, None, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(H=0), dict(V=0), dict(T=-1), dict(n=-1), dict(H=100), dict(ld_h=500),
+    dict(ld_w=516 + 2), dict(dtype=7)])
+def test_invalid_shapes_rejected(L, bad):
+    kw = dict(T=256, H=512, V=8192, n=256)
+    kw.update(bad)
+    assert _fwd(L, _shape(**kw)) == 1
+    assert L.flp_last_error()
+    assert L.flp_workspace_size(ctypes.byref(_shape(**kw)), 0) == 0
+
+
+@pytest.mark.parametrize("tau", [0.0, -1.0, float("nan"), float("inf")])
+def test_bad_temperature_rejected(L, tau):
+    assert _fwd(L, _shape(), tau=tau) == 1
+    assert b"temperature" in L.flp_last_error()
+
+
+def test_host_validation_order(L):
+    assert _fwd(L, None) == 1
+    assert _fwd(L, _shape(), ws=None) == 3
+    assert _fwd(L, _shape(), ws_bytes=100) == 3
+    assert _fwd(L, _shape(), ws=ctypes.c_void_p((1 << 20) + 8)) == 1       # workspace alignment
+    assert _fwd(L, _shape(n=200)) == 1                                     # row_idx NULL, n != T
+    assert _fwd(L, _shape(), h=None) == 1
+    assert _fwd(L, _shape(), h=ctypes.c_void_p((1 << 20) + 8)) == 1        # 16-byte alignment
+    assert _fwd(L, _shape(), targets=None) == 1
+    # nothing to score: valid and a no-op, even with null data pointers
+    assert _fwd(L, _shape(n=0), row_idx=FAKE, h=None, W=None, targets=None, out=None) == 0
+
+
+def test_kl_and_backward_validate_on_host(L):
+    s = _shape()
+    assert L.flp_kl(ctypes.byref(s), FAKE, FAKE, FAKE, FAKE, None, FAKE, None, 0, None) == 3
+    assert L.flp_backward(ctypes.byref(s), FAKE, FAKE, FAKE, None, ctypes.c_float(1.0), FAKE,
+                          FAKE, None, None, FAKE, FAKE, None, 0, None) == 3
+    bad = _shape(H=12)
+    assert L.flp_kl(ctypes.byref(bad), FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, 1 << 40,
+                    None) == 1
+
+
+def test_workspace_formula(L):
+    for wid, w in workloads.WORKLOADS.items():
+        n = {"all": w.T, "packed": 29492, "bernoulli": 9843}[w.rows]
+        s = _shape(T=w.T, H=w.H, V=w.V, n=n)
+        for op in (0, 1, 2):
+            b = L.flp_workspace_size(ctypes.byref(s), op)
+            assert b > 0
+            gathered = n * w.H * 2 * (2 if op == 1 else 1)
+            assert b >= gathered
+            if op in (0, 1):
+                # per-row state only: far below a [n, V] FP32 logit buffer
+                assert b - gathered <= n * 64 * 4 * 5 + (1 << 20)
+                if w.V >= 38016:
+                    assert b < n * w.V * 4
+            else:
+                assert b <= gathered + n * 64 * 4 * 4 + (4 << 30) + (1 << 20)
+    # monotone in the number of scored rows
+    a = L.flp_workspace_size(ctypes.byref(_shape(T=4096, H=4096, V=151936, n=1000)), 0)
+    b = L.flp_workspace_size(ctypes.byref(_shape(T=4096, H=4096, V=151936, n=2000)), 0)
+    assert b > a
+
+
+@pytest.mark.parametrize("wid", [0, 1, 2, 3, 4])
+@pytest.mark.parametrize("sms", [152, 148, 7])
+def test_planner_covers_all_tiles_and_balances(L, wid, sms):
+    w = workloads.WORKLOADS[wid]
+    n = {"all": w.T, "packed": 29492, "bernoulli": 9843}[w.rows]
+    op = 1 if w.kind == "kl" else 0
+    p = flp.plan(_shape(T=w.T, H=w.H, V=w.V, n=n), op, sms)
+    bn = 128 if op == 1 else 256
+    assert p["block_n"] == bn
+    assert p["row_tiles"] == math.ceil(n / 128)
+    assert p["vocab_tiles"] == math.ceil(w.V / bn)
+    assert 1 <= p["splits"] <= 64
+    S, tps = p["splits"], p["tiles_per_split"]
+    assert tps * (S - 1) < p["vocab_tiles"] <= tps * S       # every split non-empty
+    assert p["items"] == p["row_tiles"] * S
+    assert p["grid"] == min(p["items"], sms)
+    total = p["row_tiles"] * p["vocab_tiles"]
+    ideal = math.ceil(total / p["grid"])
+    assert ideal <= p["max_tiles_per_cta"] <= ideal + tps
+    if total >= 50 * sms:
+        assert p["max_tiles_per_cta"] <= 1.04 * total / sms + 1
+
+
+def test_row_chunks_match_the_pages_example(L):
+    rows = [list(map(int, ln.split())) for ln in open(os.path.join(ROOT, "tests", "golden",
+                                                                     "chunk_shapes.txt"))
+            if ln.strip() and not ln.startswith("#")]
+    for n, c, *lengths in rows:
+        assert flp.row_chunks(n, c) == lengths
+
+
+@pytest.mark.parametrize("n,c", [(1, 1), (9, 4), (10, 4), (4096, 4096), (9843, 4096),
+                                 (100, 7), (7, 100), (129, 128)])
+def test_row_chunks_follow_torch_chunk(L, n, c):
+    want = [t.numel() for t in torch.arange(n).chunk((n - 1) // c + 1)]
+    assert flp.row_chunks(n, c) == want
+    assert flp.row_chunks(0, c) == []
