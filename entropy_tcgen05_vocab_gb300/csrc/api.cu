@@ -337,9 +337,9 @@ flp_status flp_logprob_entropy(const flp_shape *s, const void *h, const void *W,
   if (st != FLP_OK) return st;
   if (!(std::isfinite(temperature) && temperature > 0.f))
     return fail(FLP_ERR_INVALID_ARG, "temperature must be finite and > 0");
+  if (s->n_rows == 0) return FLP_OK;
   if (!row_idx && s->n_rows != s->T)
     return fail(FLP_ERR_INVALID_ARG, "row_idx is NULL but n_rows != T");
-  if (s->n_rows == 0) return FLP_OK;
   if (!h || !W || !targets || !out_logp || !out_ent)
     return fail(FLP_ERR_INVALID_ARG, "h, W, targets, out_logp and out_ent are required");
   if (!aligned16(h) || !aligned16(W)) return fail(FLP_ERR_INVALID_ARG, "h and W must be 16-byte aligned");
