@@ -1,0 +1,471 @@
+#!/usr/bin/env python
+"""Benchmark of fused LM-head scoring (libfusedlogp) on GB300.
+
+A step is one fused log-prob + entropy call over the forward-scoring workload
+(T = 4096 scored rows, H = 4096, V = 151,936, bf16, temperature 0.7): the
+tensor-core logit tiles, the FP32 online log-sum-exp/entropy fold and the
+split merge.  Inputs are resident in HBM; the 1.24 GB weight is larger than
+L2 and is streamed from HBM every step, so no L2 flush is needed.
+
+Prints ONE JSON line (rank 0):
+  value       scored tokens/s over all ranks (device-timed, CUDA events)
+  roofline    achieved TFLOP/s of the tensor-core kernel (2 n V H flops per
+              launch / its event-timed duration) against the measured bf16
+              peak in MEASURED_PEAKS.json; DRAM traffic from the committed
+              ncu summary when it matches the current kernel sources
+  e2e         the same metric through the public API with the step's inputs
+              copied from pinned host memory and the results read back
+  cpu_baseline the float64 oracle on a bounded row sample on the host cores
+  workloads   the other workloads (long packed fp16, KL, backward) measured
+              the same way, when available
+
+--impl reference times the float64 CPU oracle (the reference arm of this
+build: the pages ship no runnable implementation) on the same workload.
+
+Multi-GPU: the path has no exchange step; under torchrun each rank scores its
+own replica of the workload (weak scaling) and the time is the max over ranks.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "scored tokens/s and TFLOP/s (% of GB300 dense BF16 peak), fused logp+entropy"
+UNIT = "scored tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FWD_KERNEL_SOURCES = ["ptx.cuh", "schedule.h", "vocab_pipeline.cuh", "kernels_fwd.cu", "launch.h"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "vocab_pipeline_forward-scoring.txt")
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=300)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", type=int, default=1)
+    p.add_argument("--no-extra", action="store_true", help="skip the other workloads")
+    p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    p.add_argument("--no-e2e", action="store_true", help="skip the end-to-end loop")
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------- utilities
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return ws, int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        d["source"] = "measured"
+        return d
+    d = dict(FALLBACK_PEAKS)
+    d["source"] = "fallback"
+    return d
+
+
+def kernel_sources_sha():
+    h = hashlib.sha256()
+    for fn in FWD_KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "entropy_tcgen05_vocab_gb300", "csrc", fn), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None, "no ncu summary"
+    kv = {}
+    for ln in open(TRAFFIC_FILE):
+        if ":" in ln and not ln.startswith("#"):
+            k, v = ln.split(":", 1)
+            kv[k.strip()] = v.strip()
+    if kv.get("kernel_sources_sha256") != kernel_sources_sha():
+        return None, "kernel changed since the ncu capture"
+    try:
+        return int(kv["dram_bytes_per_launch"]), TRAFFIC_FILE
+    except (KeyError, ValueError):
+        return None, "no dram_bytes_per_launch"
+
+
+REASON_BITS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x100: "display_clock_setting"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.out = tempfile.TemporaryFile(mode="w+")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index),
+                 "--query-gpu=timestamp,clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        self.proc.wait()
+        self.out.seek(0)
+        rows = []
+        for ln in self.out.read().splitlines():
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) != 4:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append((float(parts[1]), float(parts[2]), int(parts[3], 16), ts))
+            except (ValueError, IndexError):
+                continue
+        if not rows:
+            return None
+        # samples inside the timed region (fall back to all non-idle samples)
+        inside = [r for r in rows if self.t0 is not None and self.t0 - 0.05 <= r[3] <= self.t1 + 0.05]
+        busy = inside or [r for r in rows if r[2] & 0x1 == 0] or rows
+        mhz = sorted(r[0] for r in busy)
+        reasons = set()
+        for r in busy:
+            for bit, name in REASON_BITS.items():
+                if r[2] & bit and name != "gpu_idle":
+                    reasons.add(name)
+        return {"sm_mhz": mhz[len(mhz) // 2], "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(busy),
+                "in_timed_region": bool(inside)}
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- workloads
+def describe(d):
+    w = d["workload"]
+    return {"workload": "%s (T=%d, H=%d, V=%d, %s, tau=%g)" % (w.name, w.T, w.H, w.V, w.dtype, w.tau),
+            "T": w.T, "H": w.H, "V": w.V, "n_rows": d["n"], "dtype": w.dtype,
+            "temperature": w.tau, "row_selection": w.rows,
+            "l2": "inputs larger than L2: W is %.2f GB and is streamed from HBM every step"
+                  % (w.V * w.H * 2 / 1e9)}
+
+
+def flops_per_call(d):
+    w = d["workload"]
+    mult = {"fwd": 2, "kl": 4, "bwd": 6}[w.kind]
+    return mult * d["n"] * w.V * w.H
+
+
+def call_once(flp, d, ws, stats=None):
+    w = d["workload"]
+    if w.kind == "fwd":
+        return flp.logprob_entropy(d["h"], d["W"], d["targets"], d["row_idx"], d["tau"],
+                                   workspace=ws)
+    if w.kind == "kl":
+        return flp.kl_divergence(d["h_s"], d["W_s"], d["h_t"], d["W_t"], d["row_idx"],
+                                 workspace=ws)
+    lse, ez = stats
+    return flp.backward(d["h"], d["W"], d["targets"], d["row_idx"], d["tau"], d["g1"], d["g2"],
+                        lse, ez, workspace=ws)
+
+
+def op_of(d):
+    return {"fwd": 0, "kl": 1, "bwd": 2}[d["workload"].kind]
+
+
+def launches_per_call(d):
+    w = d["workload"]
+    gather = 1 if d["row_idx"] is not None else 0
+    if w.kind == "fwd":
+        return gather + 2
+    if w.kind == "kl":
+        return 2 * gather + 2
+    return None
+
+
+def time_device(flp, d, steps, warmup, world, device, sampler=None):
+    """Device time of `steps` calls (CUDA events) and of their tensor-core kernels."""
+    w = d["workload"]
+    shape = flp.make_shape(w.T, w.H, w.V, d["n"], d["h"].dtype if "h" in d else d["h_s"].dtype)
+    ws = torch.empty(flp.workspace_size(shape, op_of(d)), dtype=torch.uint8, device=device)
+    stats = None
+    if w.kind == "bwd":
+        _, _, lse, ez = flp.logprob_entropy(d["h"], d["W"], d["targets"], d["row_idx"], d["tau"],
+                                            return_stats=True)
+        stats = (lse, ez)
+    for _ in range(warmup):
+        call_once(flp, d, ws, stats)
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for a, b in kev:          # create the events before they are handed to the library
+        a.record()
+        b.record()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(device)
+    barrier(world)
+    torch.cuda.synchronize(device)
+    if sampler:
+        sampler.mark("t0")
+    t0.record()
+    for a, b in kev:
+        flp.set_kernel_events(a, b)
+        call_once(flp, d, ws, stats)
+    t1.record()
+    torch.cuda.synchronize(device)
+    barrier(world)
+    torch.cuda.synchronize(device)
+    if sampler:
+        sampler.mark("t1")
+    total_ms = t0.elapsed_time(t1)
+    kernel_ms = [a.elapsed_time(b) for a, b in kev]
+    status = flp.read_device_status(ws)
+    if any(status.values()):
+        raise RuntimeError("device status after timing: %s" % status)
+    return total_ms, float(np.mean(kernel_ms)), ws
+
+
+def time_e2e(flp, d, ws, steps, world, device):
+    """Through the public API with the step's inputs copied from pinned host
+    memory (hidden rows, targets, row selection) and the results read back;
+    the weight is a resident model parameter."""
+    h_pin = d["h"].cpu().pin_memory()
+    t_pin = d["targets"].cpu().pin_memory()
+    r_pin = None if d["row_idx"] is None else d["row_idx"].cpu().pin_memory()
+    h_dev, t_dev = torch.empty_like(d["h"]), torch.empty_like(d["targets"])
+    r_dev = None if r_pin is None else torch.empty_like(d["row_idx"])
+    n = d["n"]
+    lp_pin = torch.empty(n, dtype=torch.float32).pin_memory()
+    en_pin = torch.empty(n, dtype=torch.float32).pin_memory()
+    h2d = h_pin.numel() * h_pin.element_size() + t_pin.numel() * 8 + (0 if r_pin is None else r_pin.numel() * 8)
+    d2h = 2 * n * 4
+
+    def step():
+        h_dev.copy_(h_pin, non_blocking=True)
+        t_dev.copy_(t_pin, non_blocking=True)
+        if r_pin is not None:
+            r_dev.copy_(r_pin, non_blocking=True)
+        logp, ent = flp.logprob_entropy(h_dev, d["W"], t_dev, r_dev, d["tau"], workspace=ws)
+        lp_pin.copy_(logp, non_blocking=True)
+        en_pin.copy_(ent, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(device)
+    barrier(world)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(steps):
+        step()
+    t1.record()
+    torch.cuda.synchronize(device)
+    barrier(world)
+    return t0.elapsed_time(t1), h2d, d2h
+
+
+def cpu_oracle_rate(d, seconds, calib_rows=2):
+    """Oracle rows per second on a bounded sample of the workload's rows."""
+    from oracle import coracle
+    w = d["workload"]
+    h, W = d["h"].cpu(), d["W"].cpu()
+    tg = d["targets"].cpu().numpy()
+    rows_all = np.arange(w.T) if d["row_idx"] is None else d["row_idx"].cpu().numpy()
+    t = time.perf_counter()
+    coracle.logprob_entropy(h, W, tg, rows_all[:calib_rows], d["tau"], w.dtype)
+    per_row = max((time.perf_counter() - t) / calib_rows, 1e-6)
+    k = int(max(1, min(len(rows_all), seconds / per_row)))
+    pos = np.linspace(0, len(rows_all) - 1, k).astype(np.int64)
+    t = time.perf_counter()
+    coracle.logprob_entropy(h, W, tg, rows_all[pos], d["tau"], w.dtype)
+    dt = time.perf_counter() - t
+    return k / dt, k, dt, coracle.num_threads()
+
+
+# ---------------------------------------------------------------- arms
+def run_ours(args):
+    import entropy_tcgen05_vocab_gb300 as flp
+    import workloads
+
+    world, rank, local = dist_info()
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    flp.build()
+    flp.lib()
+    P = peaks()
+
+    d = workloads.make(args.workload, device=device)
+    sampler = ClockSampler(device.index) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    total_ms, kernel_ms, ws = time_device(flp, d, args.steps, args.warmup, world, device, sampler)
+    clocks = sampler.stop() if sampler else None
+    total_ms = max_over_ranks(total_ms, world, device)
+    n = d["n"]
+    value = world * n * args.steps / (total_ms / 1e3)
+    fl = flops_per_call(d)
+    achieved = fl / (kernel_ms / 1e3) / 1e12
+    traffic, traffic_src = recorded_traffic()
+
+    e2e = None
+    if not args.no_e2e:
+        e2e_steps = min(args.steps, 100)
+        e2e_ms, h2d, d2h = time_e2e(flp, d, ws, e2e_steps, world, device)
+        e2e_ms = max_over_ranks(e2e_ms, world, device)
+        e2e = {"value": world * n * e2e_steps / (e2e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e2e_ms / e2e_steps, "resident": "W (model weight)"}
+
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": d["workload"].dtype,
+        "data": "synthetic (seeded; shapes and distributions of the pages' workloads)",
+        "config": dict(describe(d), parallelism="replicas" if world > 1 else "single GPU"),
+        "tflops": world * fl * args.steps / (total_ms / 1e3) / 1e12,
+        "pct_of_bf16_peak": 100.0 * fl * args.steps / (total_ms / 1e3) / 1e12 / P["bf16_tflops"],
+        "kernel_ms": kernel_ms,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": P["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": achieved / P["bf16_tflops"], "traffic": traffic,
+                     "kernel": "vocab_pipeline_kernel<256,4,LseEpi>",
+                     "peak_kind": "bf16 dense, burst, %s" % P["source"],
+                     "frac_of_sustained": achieved / P["bf16_tflops_sustained"],
+                     "algorithmic_flops_per_launch": fl,
+                     "traffic_source": traffic_src},
+        "e2e": e2e,
+        "clocks": clocks,
+        "gpu_launches": launches_per_call(d) * args.steps,
+    }
+
+    if not args.no_extra:
+        extra = {}
+        for wid in (2, 3, 4):
+            if wid == args.workload:
+                continue
+            try:
+                dx = workloads.make(wid, device=device)
+                steps = 20
+                tms, kms, _ = time_device(flp, dx, steps, 3, world, device)
+                tms = max_over_ranks(tms, world, device)
+                flx = flops_per_call(dx)
+                extra[dx["workload"].name] = {
+                    "config": describe(dx), "scored_tokens_per_s": world * dx["n"] * steps / (tms / 1e3),
+                    "ms_per_step": tms / steps, "kernel_ms": kms,
+                    "tflops": flx / (tms / steps / 1e3) / 1e12,
+                    "pct_of_bf16_peak": 100 * flx / (tms / steps / 1e3) / 1e12 / P["bf16_tflops"],
+                    "algorithmic_flops_per_call": flx}
+                del dx
+            except Exception as e:  # a workload whose op is not available is reported, not fatal
+                extra[workloads.WORKLOADS[wid].name] = {"unavailable": str(e).splitlines()[0][:200]}
+            torch.cuda.empty_cache()
+        out["workloads"] = extra
+
+    if rank == 0 and world == 1 and not args.no_cpu:
+        rate, k, dt, cores = cpu_oracle_rate(d, args.cpu_seconds)
+        out["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+                               "sample": "%d of %d rows of the same workload (float64 C oracle, "
+                                         "%.1f s)" % (k, n, dt)}
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def run_reference(args):
+    world, rank, local = dist_info()
+    if rank != 0:
+        return
+    import workloads
+    from oracle import coracle
+
+    device = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
+    d = workloads.make(args.workload, device=device)
+    w = d["workload"]
+    h, W = d["h"].cpu(), d["W"].cpu()
+    tg = d["targets"].cpu().numpy()
+    rows_all = np.arange(w.T) if d["row_idx"] is None else d["row_idx"].cpu().numpy()
+    # size each step so the whole run stays within about two minutes
+    t = time.perf_counter()
+    coracle.logprob_entropy(h, W, tg, rows_all[:1], d["tau"], w.dtype)
+    per_row = max(time.perf_counter() - t, 1e-6)
+    k = int(max(1, min(64, 120.0 / (args.steps + args.warmup) / per_row)))
+    rng = np.random.default_rng(0)
+
+    def step():
+        pos = np.sort(rng.choice(len(rows_all), size=k, replace=False))
+        coracle.logprob_entropy(h, W, tg, rows_all[pos], d["tau"], w.dtype)
+
+    for _ in range(args.warmup):
+        step()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t
+    value = k * args.steps / dt
+    cores = coracle.num_threads()
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; shapes and distributions of the pages' workloads)",
+        "config": describe(d),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": "%d random rows of %d per step (float64 C oracle)" % (k, d["n"])},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

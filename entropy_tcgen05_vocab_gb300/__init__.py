@@ -19,7 +19,7 @@ import torch
 from . import _build
 
 __all__ = ["lib", "build", "workspace_size", "logprob_entropy", "kl_divergence", "backward",
-           "read_device_status", "plan", "row_chunks", "FusedLogProbEntropy", "FlpError",
+           "read_device_status", "plan", "set_kernel_events", "row_chunks", "FusedLogProbEntropy", "FlpError",
            "OP_LOGPROB_ENTROPY", "OP_KL", "OP_BACKWARD"]
 
 OP_LOGPROB_ENTROPY, OP_KL, OP_BACKWARD = 0, 1, 2
@@ -81,6 +81,8 @@ def lib():
     L.flp_plan_scoring.argtypes = [shp, ctypes.c_int, ctypes.c_int32, ctypes.POINTER(FlpPlan)]
     L.flp_row_chunks.argtypes = [i64, i64, ctypes.POINTER(ctypes.c_int64), i64]
     L.flp_row_chunks.restype = i64
+    L.flp_set_kernel_events.argtypes = [vp, vp]
+    L.flp_set_kernel_events.restype = ctypes.c_int
     for f in (L.flp_logprob_entropy, L.flp_kl, L.flp_backward, L.flp_read_device_status,
               L.flp_plan_scoring):
         f.restype = ctypes.c_int
@@ -117,6 +119,13 @@ def row_chunks(n_rows, chunk_rows):
     buf = (ctypes.c_int64 * max(k, 1))()
     lib().flp_row_chunks(n_rows, chunk_rows, buf, k)
     return [int(buf[i]) for i in range(k)]
+
+
+def set_kernel_events(before, after):
+    """Have the next call on this thread record two torch.cuda.Events around
+    its tensor-core kernels (both must have been recorded once, so that they
+    exist)."""
+    lib().flp_set_kernel_events(ctypes.c_void_p(before.cuda_event), ctypes.c_void_p(after.cuda_event))
 
 
 def _ptr(t):

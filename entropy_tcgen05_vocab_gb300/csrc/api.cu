@@ -21,6 +21,15 @@ namespace flp {
 namespace {
 
 thread_local char g_err[512] = "";
+thread_local cudaEvent_t g_ev_before = nullptr, g_ev_after = nullptr;
+
+// Records the measurement-hook events (if set) around the tensor-core work.
+struct KernelEvents {
+  cudaEvent_t before, after;
+  KernelEvents() : before(g_ev_before), after(g_ev_after) { g_ev_before = g_ev_after = nullptr; }
+  cudaError_t start(cudaStream_t s) const { return before ? cudaEventRecord(before, s) : cudaSuccess; }
+  cudaError_t stop(cudaStream_t s) const { return after ? cudaEventRecord(after, s) : cudaSuccess; }
+};
 
 flp_status fail(flp_status s, const char *fmt, ...) {
   va_list ap;
@@ -296,6 +305,12 @@ const char *flp_status_string(flp_status s) {
 
 const char *flp_last_error(void) { return g_err; }
 
+flp_status flp_set_kernel_events(void *before, void *after) {
+  g_ev_before = static_cast<cudaEvent_t>(before);
+  g_ev_after = static_cast<cudaEvent_t>(after);
+  return FLP_OK;
+}
+
 flp_status flp_plan_scoring(const flp_shape *shape, flp_op op, int32_t num_sms, flp_plan *out) {
   const char *why = nullptr;
   if (!shape_ok(shape, &why)) return fail(FLP_ERR_INVALID_ARG, "%s", why);
@@ -333,6 +348,7 @@ flp_status flp_logprob_entropy(const flp_shape *s, const void *h, const void *W,
                                float *out_logp, float *out_ent, float *out_lse, float *out_ez,
                                void *ws, size_t ws_bytes, flp_stream_t stream) {
   g_err[0] = 0;
+  const KernelEvents ev;
   flp_status st = check_common(s, FLP_OP_LOGPROB_ENTROPY, ws, ws_bytes);
   if (st != FLP_OK) return st;
   if (!(std::isfinite(temperature) && temperature > 0.f))
@@ -382,7 +398,9 @@ flp_status flp_logprob_entropy(const flp_shape *s, const void *h, const void *W,
     e = launch_gather(h, s->ld_h, row_idx, s->n_rows, s->T, s->H, at<void>(ws, L.hs), dev.sms, cs);
     if (e != cudaSuccess) return cuda_fail(e, "gather launch");
   }
+  if ((e = ev.start(cs)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
   if ((e = launch_fwd_scoring(a, cs)) != cudaSuccess) return cuda_fail(e, "scoring launch");
+  if ((e = ev.stop(cs)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
   if ((e = launch_fwd_merge(a, cs)) != cudaSuccess) return cuda_fail(e, "merge launch");
   return FLP_OK;
 }

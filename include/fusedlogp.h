@@ -171,6 +171,15 @@ flp_status flp_backward(const flp_shape *shape, const void *h, const void *W,
 flp_status flp_read_device_status(const void *workspace, flp_device_status *out,
                                   flp_stream_t stream);
 
+/*
+ * Measurement hook.  Makes the NEXT scoring call on the calling host thread
+ * record `before` (a cudaEvent_t) on its stream immediately before its
+ * tensor-core kernels and `after` immediately after them, so a caller can
+ * time the dominant kernel(s) apart from the small gather/merge kernels.
+ * The events are used once and then forgotten; pass NULLs to cancel.
+ */
+flp_status flp_set_kernel_events(void *before, void *after);
+
 /* Static description of a status code. */
 const char *flp_status_string(flp_status status);
 
