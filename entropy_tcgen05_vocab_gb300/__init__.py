@@ -81,6 +81,8 @@ def lib():
     L.flp_plan_scoring.argtypes = [shp, ctypes.c_int, ctypes.c_int32, ctypes.POINTER(FlpPlan)]
     L.flp_row_chunks.argtypes = [i64, i64, ctypes.POINTER(ctypes.c_int64), i64]
     L.flp_row_chunks.restype = i64
+    L.flp_logprob_entropy_noalloc.argtypes = [shp, vp, vp, vp, vp, f32, vp, vp, vp, vp, vp]
+    L.flp_logprob_entropy_noalloc.restype = ctypes.c_int
     L.flp_set_kernel_events.argtypes = [vp, vp]
     L.flp_set_kernel_events.restype = ctypes.c_int
     for f in (L.flp_logprob_entropy, L.flp_kl, L.flp_backward, L.flp_read_device_status,

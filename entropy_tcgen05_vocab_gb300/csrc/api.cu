@@ -277,6 +277,33 @@ T *at(void *ws, size_t off) {
   return reinterpret_cast<T *>(static_cast<char *>(ws) + off);
 }
 
+// ---------------------------------------------------------------- static scratch
+// Scratch of flp_logprob_entropy_noalloc: one array per device, sized at
+// build time, so that entry point never allocates device memory.
+static_assert(FLP_NOALLOC_SCRATCH_BYTES % kAlign == 0, "scratch size");
+static __device__ __align__(256) unsigned char g_noalloc_scratch[FLP_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_scratch_mu;
+std::map<int, void *> g_scratch_addr;
+
+// Device address of the array on the current device; looked up once per
+// device with that device current.
+flp_status noalloc_scratch(void **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> g(g_scratch_mu);
+  auto it = g_scratch_addr.find(dev);
+  if (it == g_scratch_addr.end()) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+    it = g_scratch_addr.emplace(dev, p).first;
+  }
+  *out = it->second;
+  return FLP_OK;
+}
+
 }  // namespace
 }  // namespace flp
 
@@ -420,6 +447,27 @@ flp_status flp_backward(const flp_shape *s, const void *, const void *, const in
   flp_status st = check_common(s, FLP_OP_BACKWARD, ws, ws_bytes);
   if (st != FLP_OK) return st;
   return fail(FLP_ERR_UNSUPPORTED, "flp_backward is not built yet");
+}
+
+flp_status flp_logprob_entropy_noalloc(const flp_shape *s, const void *h, const void *W,
+                                       const int64_t *targets, const int64_t *row_idx,
+                                       float temperature, float *out_logp, float *out_ent,
+                                       float *out_lse, float *out_ez, flp_stream_t stream) {
+  g_err[0] = 0;
+  const char *why = nullptr;
+  if (!shape_ok(s, &why)) return fail(FLP_ERR_INVALID_ARG, "%s", why);
+  const size_t need = layout_for(s, FLP_OP_LOGPROB_ENTROPY).total;
+  if (need > FLP_NOALLOC_SCRATCH_BYTES)
+    return fail(FLP_ERR_WORKSPACE,
+                "problem needs %zu bytes of scratch; the static scratch holds %zu "
+                "(use flp_logprob_entropy with a workspace)",
+                need, static_cast<size_t>(FLP_NOALLOC_SCRATCH_BYTES));
+  if (s->n_rows == 0) return FLP_OK;
+  void *scratch = nullptr;
+  const flp_status st = noalloc_scratch(&scratch);
+  if (st != FLP_OK) return st;
+  return flp_logprob_entropy(s, h, W, targets, row_idx, temperature, out_logp, out_ent, out_lse,
+                             out_ez, scratch, FLP_NOALLOC_SCRATCH_BYTES, stream);
 }
 
 flp_status flp_read_device_status(const void *ws, flp_device_status *out, flp_stream_t stream) {

@@ -172,6 +172,42 @@ flp_status flp_read_device_status(const void *workspace, flp_device_status *out,
                                   flp_stream_t stream);
 
 /*
+ * Log-prob and entropy without a caller workspace (no counterpart in the
+ * pages: this entry point exists for callers that cannot hand the library
+ * device memory).  Some callers have no way to allocate device memory at the
+ * point where they score: a host program or plugin that owns no allocator, a
+ * framework whose memory pool already holds the device's free memory, or a
+ * latency-critical loop where cudaMalloc, which may synchronise the device,
+ * is not allowed.  This variant takes the same arguments as
+ * flp_logprob_entropy minus the workspace and allocates nothing: its scratch
+ * space is one statically sized device array inside the library,
+ * FLP_NOALLOC_SCRATCH_BYTES (16 MiB), which every GPU that loads the library
+ * holds until the process exits.
+ *
+ *   - A problem whose workspace (flp_workspace_size(shape,
+ *     FLP_OP_LOGPROB_ENTROPY)) exceeds FLP_NOALLOC_SCRATCH_BYTES is rejected
+ *     with FLP_ERR_WORKSPACE before anything is enqueued.  For example
+ *     4,096 rows x H 4,096 x V 151,936 without row_idx fits; with row_idx the
+ *     gathered rows alone need n_rows * H * 2 bytes.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls in the process share the one array, and it keeps the last
+ *     call's contents (the status words are cleared at the start of every
+ *     call).  Calls whose GPU work overlaps -- on two streams, or from two
+ *     host threads -- race on it and give wrong results: serialise them.
+ *   - The device status counters of these calls live inside the shared
+ *     array and are not exposed; a bad target or row still shows up as NaN
+ *     in that row's outputs.
+ */
+#define FLP_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+flp_status flp_logprob_entropy_noalloc(const flp_shape *shape, const void *h, const void *W,
+                                       const int64_t *targets, const int64_t *row_idx,
+                                       float temperature, float *out_logp, float *out_ent,
+                                       float *out_lse, float *out_ez, flp_stream_t stream);
+
+/*
  * Measurement hook.  Makes the NEXT scoring call on the calling host thread
  * record `before` (a cudaEvent_t) on its stream immediately before its
  * tensor-core kernels and `after` immediately after them, so a caller can
