@@ -432,12 +432,64 @@ flp_status flp_logprob_entropy(const flp_shape *s, const void *h, const void *W,
   return FLP_OK;
 }
 
-flp_status flp_kl(const flp_shape *s, const void *, const void *, const void *, const void *,
-                  const int64_t *, float *, void *ws, size_t ws_bytes, flp_stream_t) {
+flp_status flp_kl(const flp_shape *s, const void *h_s, const void *W_s, const void *h_t,
+                  const void *W_t, const int64_t *row_idx, float *out_kl, void *ws,
+                  size_t ws_bytes, flp_stream_t stream) {
   g_err[0] = 0;
+  const KernelEvents ev;
   flp_status st = check_common(s, FLP_OP_KL, ws, ws_bytes);
   if (st != FLP_OK) return st;
-  return fail(FLP_ERR_UNSUPPORTED, "flp_kl is not built yet");
+  if (s->n_rows == 0) return FLP_OK;
+  if (!row_idx && s->n_rows != s->T)
+    return fail(FLP_ERR_INVALID_ARG, "row_idx is NULL but n_rows != T");
+  if (!h_s || !W_s || !h_t || !W_t || !out_kl)
+    return fail(FLP_ERR_INVALID_ARG, "h_s, W_s, h_t, W_t and out_kl are required");
+  if (!aligned16(h_s) || !aligned16(W_s) || !aligned16(h_t) || !aligned16(W_t))
+    return fail(FLP_ERR_INVALID_ARG, "h_s, W_s, h_t and W_t must be 16-byte aligned");
+  DeviceInfo dev;
+  if ((st = device_info(&dev)) != FLP_OK) return st;
+
+  const Layout L = layout_for(s, FLP_OP_KL);
+  const Plan p = plan_cached(s->n_rows, s->V, s->H, kKlBN, dev.sms);
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  KlArgs a{};
+  const void *As = h_s, *At = h_t;
+  int64_t lda = s->ld_h;
+  if (row_idx) {
+    As = at<void>(ws, L.hs);
+    At = at<void>(ws, L.hs2);
+    lda = s->H;
+  }
+  if ((st = make_map(&a.tmAs, s->dtype, As, s->H, s->n_rows, lda, 64, 128)) != FLP_OK) return st;
+  if ((st = make_map(&a.tmAt, s->dtype, At, s->H, s->n_rows, lda, 64, 128)) != FLP_OK) return st;
+  if ((st = make_map(&a.tmBs, s->dtype, W_s, s->H, s->V, s->ld_w, 64, kKlBN)) != FLP_OK) return st;
+  if ((st = make_map(&a.tmBt, s->dtype, W_t, s->H, s->V, s->ld_w, 64, kKlBN)) != FLP_OK) return st;
+  a.sch = p.sch;
+  a.grid = p.grid;
+  a.bf16 = s->dtype == FLP_BF16;
+  a.row_idx = row_idx;
+  a.T = s->T;
+  a.pmt = at<float>(ws, L.pm);
+  a.pst = at<float>(ws, L.ps);
+  a.pct = at<float>(ws, L.pb);
+  a.pms = at<float>(ws, L.pm2);
+  a.pss = at<float>(ws, L.ps2);
+  a.out_kl = out_kl;
+  a.status = at<uint32_t>(ws, L.status);
+
+  cudaError_t e = cudaMemsetAsync(a.status, 0, kStatusBytes, cs);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(status)");
+  if (row_idx) {
+    e = launch_gather(h_s, s->ld_h, row_idx, s->n_rows, s->T, s->H, at<void>(ws, L.hs), dev.sms, cs);
+    if (e == cudaSuccess)
+      e = launch_gather(h_t, s->ld_h, row_idx, s->n_rows, s->T, s->H, at<void>(ws, L.hs2), dev.sms, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "gather launch");
+  }
+  if ((e = ev.start(cs)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+  if ((e = launch_kl(a, cs)) != cudaSuccess) return cuda_fail(e, "KL launch");
+  if ((e = ev.stop(cs)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+  if ((e = launch_kl_merge(a, cs)) != cudaSuccess) return cuda_fail(e, "KL merge launch");
+  return FLP_OK;
 }
 
 flp_status flp_backward(const flp_shape *s, const void *, const void *, const int64_t *,

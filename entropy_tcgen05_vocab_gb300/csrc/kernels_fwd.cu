@@ -220,8 +220,8 @@ cudaError_t launch_gather(const void *h, int64_t ld_h, const int64_t *row_idx, i
 }
 
 cudaError_t launch_fwd_scoring(const FwdArgs &a, cudaStream_t stream) {
-  using L = PipeLayout<kFwdBN, kFwdStages>;
-  auto kern = vocab_pipeline_kernel<kFwdBN, kFwdStages, LseEpi>;
+  using L = PipeLayout<kFwdBN, kFwdStages, 1>;
+  auto kern = vocab_pipeline_kernel<kFwdBN, kFwdStages, 1, LseEpi>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -237,7 +237,8 @@ cudaError_t launch_fwd_scoring(const FwdArgs &a, cudaStream_t stream) {
   p.pb = a.pb;
   p.zt = a.zt;
   const uint32_t idesc = idesc_f16(a.bf16, kBM, kFwdBN, false, false);
-  kern<<<a.grid, kPipeThreads, L::kSmemBytes, stream>>>(a.tmA, a.tmB, a.sch, idesc, p, a.status);
+  kern<<<a.grid, kPipeThreads, L::kSmemBytes, stream>>>(a.tmA, a.tmB, a.tmA, a.tmB, a.sch, idesc,
+                                                          p, a.status);
   return cudaGetLastError();
 }
 
@@ -249,6 +250,6 @@ cudaError_t launch_fwd_merge(const FwdArgs &a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-int fwd_smem_bytes() { return PipeLayout<kFwdBN, kFwdStages>::kSmemBytes; }
+int fwd_smem_bytes() { return PipeLayout<kFwdBN, kFwdStages, 1>::kSmemBytes; }
 
 }  // namespace flp

@@ -1,0 +1,196 @@
+// kernels_kl.cu -- full-vocabulary KL(teacher || student) without either
+// logit tensor in memory (DeepSeek-V4 book ch. 19, "Never materialize
+// logits" and "TileLang KL kernel": the teacher's logits are rebuilt from its
+// cached hidden states through its prediction head and the exact KL is taken
+// directly).
+//
+// Both heads run on the same (row tile, vocabulary tile): the pipeline issues
+// two tcgen05 GEMMs per K step into two TMEM accumulators, z_s = h_s W_s^T and
+// z_t = h_t W_t^T.  The epilogue keeps, per row, in base 2 (y = z log2 e):
+//   teacher  m_t = max y_t,  S_t = sum 2^(y_t - m_t),
+//            C_t = sum 2^(y_t - m_t) (z_t - z_s)      (natural units)
+//   student  m_s = max y_s,  S_s = sum 2^(y_s - m_s)
+// rescaling S and C by 2^(m - m') when a running max grows.  Then
+//   KL = sum_v p_t (log p_t - log p_s) = C_t / S_t - LSE_t + LSE_s,
+//   LSE = ln 2 (m + log2 S).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "launch.h"
+#include "vocab_pipeline.cuh"
+
+namespace flp {
+
+namespace {
+constexpr float kLn2f = 0.693147180559945309f;
+constexpr float kLog2e = 1.442695040888963407f;
+}  // namespace
+
+struct KlEpi {
+  struct Params {
+    int n;
+    int V;
+    float *pmt, *pst, *pct, *pms, *pss;  // [splits][n]
+  };
+  const Params p;
+  float mt, st0, st1, ct0, ct1, ms, ss0, ss1;
+
+  __device__ __forceinline__ explicit KlEpi(const Params &pp) : p(pp) {}
+
+  __device__ __forceinline__ void begin(int /*mt*/, int /*row*/) {
+    mt = ms = -FLT_MAX;
+    st0 = st1 = ct0 = ct1 = ss0 = ss1 = 0.f;
+  }
+
+  __device__ __forceinline__ void rescale(float cmax_t, float cmax_s) {
+    const float nt = fmaxf(mt, cmax_t * kLog2e);
+    if (nt > mt) {
+      const float a = ex2(mt - nt);
+      st0 *= a;
+      st1 *= a;
+      ct0 *= a;
+      ct1 *= a;
+      mt = nt;
+    }
+    const float ns = fmaxf(ms, cmax_s * kLog2e);
+    if (ns > ms) {
+      const float a = ex2(ms - ns);
+      ss0 *= a;
+      ss1 *= a;
+      ms = ns;
+    }
+  }
+
+  __device__ __forceinline__ void fold_full(const float (&xs)[32], const float (&xt)[32]) {
+    float cs = xs[0], ct = xt[0];
+#pragma unroll
+    for (int j = 1; j < 32; ++j) {
+      cs = fmaxf(cs, xs[j]);
+      ct = fmaxf(ct, xt[j]);
+    }
+    rescale(ct, cs);
+    const float nmt = -mt, nms = -ms;
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+      const float et0 = ex2(fmaf(xt[j], kLog2e, nmt));
+      const float et1 = ex2(fmaf(xt[j + 1], kLog2e, nmt));
+      st0 += et0;
+      st1 += et1;
+      ct0 = fmaf(et0, xt[j] - xs[j], ct0);
+      ct1 = fmaf(et1, xt[j + 1] - xs[j + 1], ct1);
+      ss0 += ex2(fmaf(xs[j], kLog2e, nms));
+      ss1 += ex2(fmaf(xs[j + 1], kLog2e, nms));
+    }
+  }
+
+  __device__ __forceinline__ void fold_masked(const float (&xs)[32], const float (&xt)[32],
+                                              int nv) {
+    float cs = -FLT_MAX, ct = -FLT_MAX;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (j < nv) {
+        cs = fmaxf(cs, xs[j]);
+        ct = fmaxf(ct, xt[j]);
+      }
+    }
+    rescale(ct, cs);
+    const float nmt = -mt, nms = -ms;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (j < nv) {
+        const float et = ex2(fmaf(xt[j], kLog2e, nmt));
+        st0 += et;
+        ct0 = fmaf(et, xt[j] - xs[j], ct0);
+        ss0 += ex2(fmaf(xs[j], kLog2e, nms));
+      }
+    }
+  }
+
+  __device__ __forceinline__ void tile(uint32_t taddr, int col0) {
+#pragma unroll 1
+    for (int c = 0; c < kKlBN / 32; ++c) {
+      const int cb = col0 + c * 32;
+      if (cb >= p.V) break;  // same for the whole warp
+      float xs[32], xt[32];
+      tmem_ld32(taddr + c * 32, xs);
+      tmem_ld32(taddr + kKlBN + c * 32, xt);
+      if (cb + 32 <= p.V)
+        fold_full(xs, xt);
+      else
+        fold_masked(xs, xt, p.V - cb);
+    }
+  }
+
+  __device__ __forceinline__ void end(int split, int row) {
+    if (row >= p.n) return;
+    const size_t o = static_cast<size_t>(split) * p.n + row;
+    p.pmt[o] = mt;
+    p.pst[o] = st0 + st1;
+    p.pct[o] = ct0 + ct1;
+    p.pms[o] = ms;
+    p.pss[o] = ss0 + ss1;
+  }
+};
+
+// One thread per scored row: merge the split partials and finish the KL.
+__global__ void kl_merge_kernel(int n, int splits, const float *__restrict__ pmt,
+                                const float *__restrict__ pst, const float *__restrict__ pct,
+                                const float *__restrict__ pms, const float *__restrict__ pss,
+                                const int64_t *__restrict__ row_idx, int64_t T,
+                                float *__restrict__ out_kl, uint32_t *status) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  float Mt = -FLT_MAX, Ms = -FLT_MAX;
+  for (int s = 0; s < splits; ++s) {
+    const size_t o = static_cast<size_t>(s) * n + i;
+    Mt = fmaxf(Mt, pmt[o]);
+    Ms = fmaxf(Ms, pms[o]);
+  }
+  float St = 0.f, Ct = 0.f, Ss = 0.f;
+  for (int s = 0; s < splits; ++s) {
+    const size_t o = static_cast<size_t>(s) * n + i;
+    const float at = exp2f(pmt[o] - Mt);
+    St = fmaf(pst[o], at, St);
+    Ct = fmaf(pct[o], at, Ct);
+    Ss = fmaf(pss[o], exp2f(pms[o] - Ms), Ss);
+  }
+  float kl = Ct / St - kLn2f * ((Mt - Ms) + (log2f(St) - log2f(Ss)));
+  if (row_idx) {
+    const int64_t r = row_idx[i];
+    if (r < 0 || r >= T) {
+      atomicAdd(status + kStatBadRow, 1u);
+      kl = __int_as_float(0x7fc00000);
+    }
+  }
+  out_kl[i] = kl;
+}
+
+cudaError_t launch_kl(const KlArgs &a, cudaStream_t stream) {
+  using L = PipeLayout<kKlBN, kKlStages, 2>;
+  auto kern = vocab_pipeline_kernel<kKlBN, kKlStages, 2, KlEpi>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  KlEpi::Params p;
+  p.n = a.sch.n;
+  p.V = a.sch.V;
+  p.pmt = a.pmt;
+  p.pst = a.pst;
+  p.pct = a.pct;
+  p.pms = a.pms;
+  p.pss = a.pss;
+  const uint32_t idesc = idesc_f16(a.bf16, kBM, kKlBN, false, false);
+  kern<<<a.grid, kPipeThreads, L::kSmemBytes, stream>>>(a.tmAs, a.tmBs, a.tmAt, a.tmBt, a.sch,
+                                                          idesc, p, a.status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kl_merge(const KlArgs &a, cudaStream_t stream) {
+  const int n = a.sch.n;
+  kl_merge_kernel<<<(n + 255) / 256, 256, 0, stream>>>(n, a.sch.splits, a.pmt, a.pst, a.pct,
+                                                       a.pms, a.pss, a.row_idx, a.T, a.out_kl,
+                                                       a.status);
+  return cudaGetLastError();
+}
+
+}  // namespace flp

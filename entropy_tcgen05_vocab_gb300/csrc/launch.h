@@ -53,6 +53,8 @@ cudaError_t launch_gather(const void *h, int64_t ld_h, const int64_t *row_idx, i
                           int64_t T, int64_t H, void *hs, int num_sms, cudaStream_t stream);
 cudaError_t launch_fwd_scoring(const FwdArgs &a, cudaStream_t stream);
 cudaError_t launch_fwd_merge(const FwdArgs &a, cudaStream_t stream);
+cudaError_t launch_kl(const KlArgs &a, cudaStream_t stream);
+cudaError_t launch_kl_merge(const KlArgs &a, cudaStream_t stream);
 int fwd_smem_bytes();
 
 }  // namespace flp

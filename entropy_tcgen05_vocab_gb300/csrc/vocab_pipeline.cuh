@@ -42,12 +42,17 @@ constexpr int kEpiWarps = 4;
 constexpr int kPipeThreads = 64 + 32 * kEpiWarps;
 
 
-template <int BN, int STAGES>
+// NOPS independent GEMMs share one tile (the KL pipeline runs the student and
+// the teacher head side by side, NOPS = 2).  Stage layout:
+// [A_0 .. A_{NOPS-1} | B_0 .. B_{NOPS-1}]; TMEM: two accumulator buffers of
+// NOPS x BN columns (GEMM op at column offset op * BN inside a buffer).
+template <int BN, int STAGES, int NOPS = 1>
 struct PipeLayout {
   static constexpr int kABytes = kBM * kBK * 2;
   static constexpr int kBBytes = BN * kBK * 2;
-  static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kTmemCols = 2 * BN;
+  static constexpr int kStageBytes = NOPS * (kABytes + kBBytes);
+  static constexpr int kAccCols = NOPS * BN;
+  static constexpr int kTmemCols = 2 * kAccCols;
   static constexpr int kBarrierBytes = 8 * (2 * STAGES + 5) + 16;
   // + 1024 so the stage ring can be aligned to a swizzle atom.
   static constexpr int kSmemBytes = STAGES * kStageBytes + kBarrierBytes + 1024;
@@ -65,14 +70,18 @@ __device__ __forceinline__ void record_timeout(uint32_t *status, volatile int *a
 //   __device__ void begin(int mt, int row);               row = global scored row of this thread
 //   __device__ void tile(uint32_t taddr, int col0);       taddr = TMEM address of this warp's
 //                                                          lanes at the tile's first column
+//                                                          (GEMM op at + op * BN)
 //   __device__ void end(int split, int row);
-template <int BN, int STAGES, class Epi>
+template <int BN, int STAGES, int NOPS, class Epi>
 __global__ void __launch_bounds__(kPipeThreads, 1)
-    vocab_pipeline_kernel(const __grid_constant__ CUtensorMap tmA,
-                          const __grid_constant__ CUtensorMap tmB, const Schedule sch,
+    vocab_pipeline_kernel(const __grid_constant__ CUtensorMap tmA0,
+                          const __grid_constant__ CUtensorMap tmB0,
+                          const __grid_constant__ CUtensorMap tmA1,
+                          const __grid_constant__ CUtensorMap tmB1, const Schedule sch,
                           const uint32_t idesc, const typename Epi::Params ep,
                           uint32_t *status) {
-  using L = PipeLayout<BN, STAGES>;
+  using L = PipeLayout<BN, STAGES, NOPS>;
+  static_assert(NOPS == 1 || NOPS == 2, "one or two GEMMs per tile");
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -101,8 +110,12 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    prefetch_tmap(&tmA);
-    prefetch_tmap(&tmB);
+    prefetch_tmap(&tmA0);
+    prefetch_tmap(&tmB0);
+    if (NOPS == 2) {
+      prefetch_tmap(&tmA1);
+      prefetch_tmap(&tmB1);
+    }
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, L::kTmemCols);
@@ -129,9 +142,14 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
           if (!ok) break;
           if (lane == 0) {
             uint8_t *sa = smem + stage * L::kStageBytes;
+            uint8_t *sb = sa + NOPS * L::kABytes;
             mbar_arrive_expect_tx(&full[stage], L::kStageBytes);
-            tma_load_2d(sa, &tmA, &full[stage], kb * kBK, mt * kBM);
-            tma_load_2d(sa + L::kABytes, &tmB, &full[stage], kb * kBK, vt * BN);
+            tma_load_2d(sa, &tmA0, &full[stage], kb * kBK, mt * kBM);
+            tma_load_2d(sb, &tmB0, &full[stage], kb * kBK, vt * BN);
+            if (NOPS == 2) {
+              tma_load_2d(sa + L::kABytes, &tmA1, &full[stage], kb * kBK, mt * kBM);
+              tma_load_2d(sb + L::kBBytes, &tmB1, &full[stage], kb * kBK, vt * BN);
+            }
           }
           armed |= 1u << stage;
           if (++stage == STAGES) {
@@ -170,7 +188,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * L::kAccCols);
         for (int kb = 0; kb < sch.k_blocks; ++kb) {
           if (lane == 0) ok = mbar_wait(&full[stage], phase, abort_flag);
           ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -178,12 +196,15 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
           tc_fence_after();
           if (lane == 0) {
             const uint32_t a0 = smem_u32(smem + stage * L::kStageBytes);
-            const uint32_t b0 = a0 + L::kABytes;
+            const uint32_t b0 = a0 + NOPS * L::kABytes;
 #pragma unroll
             for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
-              const uint64_t ad = sdesc_sw128(a0 + kk * kUmmaK * 2, 16, 1024);
-              const uint64_t bd = sdesc_sw128(b0 + kk * kUmmaK * 2, 16, 1024);
-              mma_f16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+#pragma unroll
+              for (int op = 0; op < NOPS; ++op) {
+                const uint64_t ad = sdesc_sw128(a0 + op * L::kABytes + kk * kUmmaK * 2, 16, 1024);
+                const uint64_t bd = sdesc_sw128(b0 + op * L::kBBytes + kk * kUmmaK * 2, 16, 1024);
+                mma_f16(d_tmem + op * BN, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+              }
             }
             mma_commit(&empty[stage]);  // frees the stage when these MMAs finish
           }
@@ -225,7 +246,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         tc_fence_after();
-        epi.tile(tmem_base + lane_off + static_cast<uint32_t>(acc * BN), vt * BN);
+        epi.tile(tmem_base + lane_off + static_cast<uint32_t>(acc * L::kAccCols), vt * BN);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[acc]);

@@ -1,0 +1,110 @@
+"""GPU parity of flp_kl (full-vocabulary KL(teacher || student)) against the
+float64 oracle.  Element by element on small cases spanning several row and
+vocabulary tiles with ragged tails; on seeded row samples at the full size of
+the distillation workload (T 8192, H 4096, V 129,280, bf16).  Tolerance
+|d KL| <= 1e-3 absolute.
+"""
+import numpy as np
+import pytest
+import torch
+
+import entropy_tcgen05_vocab_gb300 as flp
+import workloads
+from oracle import coracle, ref
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    flp.build()
+    flp.lib()
+
+
+def _check(got, want, tol=TOL):
+    g = got.detach().cpu().double().numpy()
+    assert np.all(np.isfinite(g))
+    err = np.abs(g - want)
+    assert err.max() <= tol, "max |dKL| %.3e at %d" % (err.max(), int(err.argmax()))
+    return float(err.max())
+
+
+def _case(T, H, V, dtype="bf16", seed=31, rows=None):
+    w = workloads.WORKLOADS[3].scaled(T=T, H=H, V=V, dtype=dtype, seed=seed)
+    d = workloads.make(w, device="cuda")
+    kl = flp.kl_divergence(d["h_s"], d["W_s"], d["h_t"], d["W_t"], rows)
+    torch.cuda.synchronize()
+    want = coracle.kl(d["h_s"].cpu(), d["W_s"].cpu(), d["h_t"].cpu(), d["W_t"].cpu(),
+                      None if rows is None else rows.cpu().numpy(), dtype)
+    return kl, want, d
+
+
+@pytest.mark.parametrize("T,H,V", [
+    (256, 512, 8192),    # whole tiles
+    (300, 256, 5000),    # ragged rows and vocabulary (5000 = 39 x 128 + 8)
+    (1, 64, 33),         # one row, V just past one 32-column chunk
+    (130, 520, 1000),    # H not a multiple of 64
+])
+def test_kl_small(T, H, V):
+    kl, want, _ = _case(T, H, V)
+    assert np.all(want > 0)
+    _check(kl, want)
+
+
+def test_kl_fp16_with_row_idx():
+    rows = torch.tensor([5, 0, 299, 5, 128, 127, 200], device="cuda")
+    kl, want, _ = _case(300, 256, 4000, dtype="fp16", seed=32, rows=rows)
+    _check(kl, want)
+
+
+def test_kl_of_identical_heads_is_zero():
+    w = workloads.WORKLOADS[3].scaled(T=260, H=256, V=6000, seed=33)
+    d = workloads.make(w, device="cuda")
+    kl = flp.kl_divergence(d["h_s"], d["W_s"], d["h_s"], d["W_s"])
+    assert torch.all(kl.abs() <= 1e-6), kl.abs().max()
+    # distinct copies of the same values: exactly the same logits, KL = 0
+    kl2 = flp.kl_divergence(d["h_s"], d["W_s"], d["h_s"].clone(), d["W_s"].clone())
+    assert torch.all(kl2.abs() <= 1e-6)
+
+
+def test_kl_small_and_sensitive_when_heads_nearly_agree():
+    # teacher = student weights, hidden states 0.01 apart: KL ~ 1e-4
+    w = workloads.WORKLOADS[3].scaled(T=200, H=256, V=7000, seed=34, teacher_noise=0.01)
+    d = workloads.make(w, device="cuda")
+    kl = flp.kl_divergence(d["h_s"], d["W_s"], d["h_t"], d["W_s"])
+    want = coracle.kl(d["h_s"].cpu(), d["W_s"].cpu(), d["h_t"].cpu(), d["W_s"].cpu(), None,
+                      "bf16")
+    assert want.max() < 1e-2
+    _check(kl, want, tol=2e-5)
+
+
+def test_kl_bad_rows_are_nan_and_counted():
+    w = workloads.WORKLOADS[3].scaled(T=100, H=128, V=2000, seed=35)
+    d = workloads.make(w, device="cuda")
+    rows = torch.tensor([3, 100, -2, 7], device="cuda")
+    shape = flp.make_shape(100, 128, 2000, 4, torch.bfloat16)
+    ws = torch.empty(flp.workspace_size(shape, flp.OP_KL), dtype=torch.uint8, device="cuda")
+    kl = flp.kl_divergence(d["h_s"], d["W_s"], d["h_t"], d["W_t"], rows, workspace=ws)
+    st = flp.read_device_status(ws)
+    assert st["bad_rows"] == 2 and st["timeouts"] == 0
+    k = kl.cpu().numpy()
+    assert np.isnan(k[[1, 2]]).all() and np.isfinite(k[[0, 3]]).all()
+    want = coracle.kl(d["h_s"].cpu(), d["W_s"].cpu(), d["h_t"].cpu(), d["W_t"].cpu(),
+                      np.array([3, 7]), "bf16")
+    _check(kl[[0, 3]], want)
+
+
+def test_distillation_workload_sampled():
+    d = workloads.make(3, device="cuda")
+    kl = flp.kl_divergence(d["h_s"], d["W_s"], d["h_t"], d["W_t"])
+    torch.cuda.synchronize()
+    n = d["n"]
+    pos = np.unique(np.concatenate([workloads.sample_rows(n, 192, seed=3), [0, n - 1]]))
+    want = ref.kl(d["h_s"].cpu(), d["W_s"].cpu(), d["h_t"].cpu(), d["W_t"].cpu(), pos, "bf16")
+    e = _check(kl[torch.from_numpy(pos).cuda()], want)
+    k = kl.cpu().numpy()
+    assert np.all(np.isfinite(k)) and np.all(k >= -1e-4)
+    print("distillation workload: %d sampled rows, max|dKL| %.2e, mean KL %.3f" % (len(pos), e, k.mean()))
