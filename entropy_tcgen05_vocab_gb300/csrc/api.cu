@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -72,11 +73,16 @@ int max_splits(int64_t V, int bn) {
   return static_cast<int>(std::min<int64_t>(vocab_tiles(V, bn), kMaxSplits));
 }
 
-// Rows of the backward's logit-gradient chunk.
+// Rows of the backward's logit-gradient chunk: as many as fit in 4 GiB, or
+// fewer if FLP_GRAD_CHUNK_ROWS asks for it (a memory/tuning knob).
 int64_t grad_chunk_rows(const flp_shape *s) {
   const int64_t ldg = cdiv(s->V, 8) * 8;
   int64_t r = kGradChunkBytes / (ldg * 2);
   r = std::max<int64_t>(128, r / 128 * 128);
+  if (const char *env = std::getenv("FLP_GRAD_CHUNK_ROWS")) {
+    const long long want = std::atoll(env);
+    if (want > 0) r = std::min<int64_t>(r, want);
+  }
   return std::min<int64_t>(r, std::max<int64_t>(s->n_rows, 1));
 }
 
@@ -492,13 +498,145 @@ flp_status flp_kl(const flp_shape *s, const void *h_s, const void *W_s, const vo
   return FLP_OK;
 }
 
-flp_status flp_backward(const flp_shape *s, const void *, const void *, const int64_t *,
-                        const int64_t *, float, const float *, const float *, const float *,
-                        const float *, void *, float *, void *ws, size_t ws_bytes, flp_stream_t) {
+flp_status flp_backward(const flp_shape *s, const void *h, const void *W, const int64_t *targets,
+                        const int64_t *row_idx, float temperature, const float *g1,
+                        const float *g2, const float *lse, const float *ez, void *dh, float *dW,
+                        void *ws, size_t ws_bytes, flp_stream_t stream) {
   g_err[0] = 0;
+  const KernelEvents ev;
   flp_status st = check_common(s, FLP_OP_BACKWARD, ws, ws_bytes);
   if (st != FLP_OK) return st;
-  return fail(FLP_ERR_UNSUPPORTED, "flp_backward is not built yet");
+  if (!(std::isfinite(temperature) && temperature > 0.f))
+    return fail(FLP_ERR_INVALID_ARG, "temperature must be finite and > 0");
+  if (!dh || !dW) return fail(FLP_ERR_INVALID_ARG, "dh and dW are required");
+  if (!aligned16(dh) || !aligned16(dW)) return fail(FLP_ERR_INVALID_ARG, "dh and dW must be 16-byte aligned");
+  if ((lse == nullptr) != (ez == nullptr))
+    return fail(FLP_ERR_INVALID_ARG, "lse and ez must both be given or both be NULL");
+  if (s->n_rows > 0) {
+    if (!h || !W || !targets || !g1 || !g2)
+      return fail(FLP_ERR_INVALID_ARG, "h, W, targets, g1 and g2 are required");
+    if (!aligned16(h) || !aligned16(W)) return fail(FLP_ERR_INVALID_ARG, "h and W must be 16-byte aligned");
+    if (!row_idx && s->n_rows != s->T)
+      return fail(FLP_ERR_INVALID_ARG, "row_idx is NULL but n_rows != T");
+  }
+  DeviceInfo dev;
+  if ((st = device_info(&dev)) != FLP_OK) return st;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const Layout L = layout_for(s, FLP_OP_BACKWARD);
+  uint32_t *status = at<uint32_t>(ws, L.status);
+  const size_t esz = 2;
+  cudaError_t e = cudaMemsetAsync(status, 0, kStatusBytes, cs);
+  // rows that are not scored get a zero gradient
+  if (e == cudaSuccess && s->T > 0)
+    e = cudaMemset2DAsync(dh, s->ld_h * esz, 0, s->H * esz, s->T, cs);
+  if (e == cudaSuccess && s->n_rows == 0)
+    e = cudaMemset2DAsync(dW, s->ld_w * 4, 0, s->H * 4, s->V, cs);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemset");
+  if (s->n_rows == 0) return FLP_OK;
+
+  const void *A = h;
+  int64_t lda = s->ld_h;
+  if (row_idx) {
+    A = at<void>(ws, L.hs);
+    lda = s->H;
+    e = launch_gather(h, s->ld_h, row_idx, s->n_rows, s->T, s->H, at<void>(ws, L.hs), dev.sms, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "gather launch");
+  }
+  const float inv_tau = 1.0f / temperature;
+  const float sl = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+  if ((e = ev.start(cs)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+
+  // Per-row statistics (LSE, E[z']) unless the caller kept them from the forward.
+  if (!lse) {
+    FwdArgs a{};
+    const Plan p = plan_cached(s->n_rows, s->V, s->H, kFwdBN, dev.sms);
+    if ((st = make_map(&a.tmA, s->dtype, A, s->H, s->n_rows, lda, 64, 128)) != FLP_OK) return st;
+    if ((st = make_map(&a.tmB, s->dtype, W, s->H, s->V, s->ld_w, 64, kFwdBN)) != FLP_OK) return st;
+    a.sch = p.sch;
+    a.grid = p.grid;
+    a.bf16 = s->dtype == FLP_BF16;
+    a.targets = targets;
+    a.row_idx = row_idx;
+    a.T = s->T;
+    a.inv_tau = inv_tau;
+    a.scale_log2 = sl;
+    a.pm = at<float>(ws, L.pm);
+    a.ps = at<float>(ws, L.ps);
+    a.pb = at<float>(ws, L.pb);
+    a.zt = at<float>(ws, L.zt);
+    a.out_lse = at<float>(ws, L.lse);
+    a.out_ez = at<float>(ws, L.ez);
+    a.status = status;
+    if ((e = launch_fwd_scoring(a, cs)) != cudaSuccess) return cuda_fail(e, "stats launch");
+    if ((e = launch_fwd_merge(a, cs)) != cudaSuccess) return cuda_fail(e, "stats merge launch");
+    lse = a.out_lse;
+    ez = a.out_ez;
+  }
+
+  const int64_t ldg = cdiv(s->V, 8) * 8;
+  void *G = at<void>(ws, L.g);
+  const int64_t n = s->n_rows;
+  const int64_t num = (n - 1) / L.grad_rows + 1;
+  const int64_t each = cdiv(n, num);
+  const char *eb = static_cast<const char *>(A);
+  for (int64_t r0 = 0; r0 < n; r0 += each) {
+    const int rc = static_cast<int>(std::min(each, n - r0));
+    const void *Ar = eb + static_cast<size_t>(r0) * lda * esz;
+    // 1. G = d loss / d z for the chunk's rows
+    GradArgs ga{};
+    const Plan p = plan_cached(rc, s->V, s->H, kFwdBN, dev.sms);
+    if ((st = make_map(&ga.tmA, s->dtype, Ar, s->H, rc, lda, 64, 128)) != FLP_OK) return st;
+    if ((st = make_map(&ga.tmB, s->dtype, W, s->H, s->V, s->ld_w, 64, kFwdBN)) != FLP_OK) return st;
+    ga.sch = p.sch;
+    ga.grid = p.grid;
+    ga.bf16 = s->dtype == FLP_BF16;
+    ga.r0 = static_cast<int>(r0);
+    ga.T = s->T;
+    ga.targets = targets;
+    ga.row_idx = row_idx;
+    ga.lse = lse;
+    ga.ez = ez;
+    ga.g1 = g1;
+    ga.g2 = g2;
+    ga.scale_log2 = sl;
+    ga.inv_tau = inv_tau;
+    ga.G = G;
+    ga.ldg = ldg;
+    ga.status = status;
+    if ((e = launch_grad(ga, cs)) != cudaSuccess) return cuda_fail(e, "grad launch");
+    // 2. dh[rows] = G W   (M = rc, N = H, K = V; W is MN-major for this product)
+    GemmArgs da{};
+    if ((st = make_map(&da.tmA, s->dtype, G, s->V, rc, ldg, 64, 128)) != FLP_OK) return st;
+    if ((st = make_map(&da.tmB, s->dtype, W, s->H, s->V, s->ld_w, 64, 64)) != FLP_OK) return st;
+    da.M = rc;
+    da.N = static_cast<int>(s->H);
+    da.K = static_cast<int>(s->V);
+    da.grid = std::min(gemm_tiles(da.M, da.N), dev.sms);
+    da.bf16 = ga.bf16;
+    da.status = status;
+    da.r0 = static_cast<int>(r0);
+    da.T = s->T;
+    da.row_idx = row_idx;
+    da.dh = dh;
+    da.ld_dh = s->ld_h;
+    if ((e = launch_dh_gemm(da, cs)) != cudaSuccess) return cuda_fail(e, "dh launch");
+    // 3. dW (+)= G^T h[rows]   (M = V, N = H, K = rc; both operands MN-major)
+    GemmArgs wa{};
+    if ((st = make_map(&wa.tmA, s->dtype, G, s->V, rc, ldg, 64, 64)) != FLP_OK) return st;
+    if ((st = make_map(&wa.tmB, s->dtype, Ar, s->H, rc, lda, 64, 64)) != FLP_OK) return st;
+    wa.M = static_cast<int>(s->V);
+    wa.N = static_cast<int>(s->H);
+    wa.K = rc;
+    wa.grid = std::min(gemm_tiles(wa.M, wa.N), dev.sms);
+    wa.bf16 = ga.bf16;
+    wa.status = status;
+    wa.dW = dW;
+    wa.ld_dw = s->ld_w;
+    wa.accumulate = r0 > 0;
+    if ((e = launch_dw_gemm(wa, cs)) != cudaSuccess) return cuda_fail(e, "dW launch");
+  }
+  if ((e = ev.stop(cs)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+  return FLP_OK;
 }
 
 flp_status flp_logprob_entropy_noalloc(const flp_shape *s, const void *h, const void *W,

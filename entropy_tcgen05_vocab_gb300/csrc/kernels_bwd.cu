@@ -1,0 +1,301 @@
+// kernels_bwd.cu -- backward of L = sum_i g1_i logp_i + g2_i ent_i by tile
+// recompute (miles PR #4645, "How it works": Op -- the backward replays each
+// tile instead of keeping the [tokens x vocab] logits or their gradient).
+//
+// For a chunk of R scored rows:
+//   1. grad pass: the vocabulary pipeline recomputes z = h W^T tile by tile
+//      and its epilogue turns each FP32 logit straight into the gradient of
+//      the loss w.r.t. that logit,
+//        G_v = (g1 (1[v = tgt] - p_v) - g2 p_v (z'_v - E_p[z'])) / tau,
+//        p_v = exp(z'_v - LSE),  z' = z / tau,
+//      with LSE and E_p[z'] from the forward statistics, written in the
+//      model dtype into the bounded chunk buffer G [R, V];
+//   2. dh[rows] = G W           (tcgen05 GEMM, K = V, W read MN-major);
+//   3. dW (+)= G^T h[rows]      (tcgen05 GEMM, K = R, both operands MN-major).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "gemm_pipeline.cuh"
+#include "launch.h"
+#include "vocab_pipeline.cuh"
+
+namespace flp {
+
+namespace {
+constexpr float kLog2eF = 1.442695040888963407f;
+
+__device__ __forceinline__ uint32_t pack2(float a, float b, bool bf16) {
+  if (bf16) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&v);
+  }
+  const __half2 v = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+__device__ __forceinline__ uint16_t pack1(float a, bool bf16) {
+  if (bf16) {
+    const __nv_bfloat16 v = __float2bfloat16_rn(a);
+    return *reinterpret_cast<const uint16_t *>(&v);
+  }
+  const __half v = __float2half_rn(a);
+  return *reinterpret_cast<const uint16_t *>(&v);
+}
+
+// 32 FP32 values -> 32 16-bit values at dst (64 bytes, 16-byte aligned).
+__device__ __forceinline__ void store32_16(void *dst, const float (&v)[32], bool bf16) {
+  uint4 *d = static_cast<uint4 *>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 u;
+    u.x = pack2(v[8 * q + 0], v[8 * q + 1], bf16);
+    u.y = pack2(v[8 * q + 2], v[8 * q + 3], bf16);
+    u.z = pack2(v[8 * q + 4], v[8 * q + 5], bf16);
+    u.w = pack2(v[8 * q + 6], v[8 * q + 7], bf16);
+    d[q] = u;
+  }
+}
+}  // namespace
+
+// ---------------------------------------------------------------- grad pass
+struct GradEpi {
+  struct Params {
+    int n;       // rows in the chunk
+    int V;
+    int r0;      // first scored position of the chunk
+    int64_t T;
+    const int64_t *targets;
+    const int64_t *row_idx;
+    const float *lse, *ez, *g1, *g2;
+    float sl, inv_tau;
+    uint16_t *G;  // [n, ldg]
+    int64_t ldg;
+    bool bf16;
+  };
+  const Params p;
+  float lse2, ez, a1, a2;
+  int tgt;
+  bool valid;
+  uint16_t *grow;
+
+  __device__ __forceinline__ explicit GradEpi(const Params &pp) : p(pp) {}
+
+  __device__ __forceinline__ void begin(int /*mt*/, int row) {
+    valid = row < p.n;
+    tgt = -1;
+    lse2 = ez = a1 = a2 = 0.f;
+    grow = p.G + static_cast<int64_t>(valid ? row : 0) * p.ldg;
+    if (!valid) return;
+    const int i = p.r0 + row;
+    lse2 = p.lse[i] * kLog2eF;
+    ez = p.ez[i];
+    a1 = p.g1[i] * p.inv_tau;
+    a2 = p.g2[i] * p.inv_tau;
+    const int64_t r = p.row_idx ? p.row_idx[i] : i;
+    if (r >= 0 && r < p.T) {
+      const int64_t t = p.targets[r];
+      if (t >= 0 && t < p.V) tgt = static_cast<int>(t);
+    }
+  }
+
+  __device__ __forceinline__ void tile(uint32_t taddr, int col0) {
+#pragma unroll 1
+    for (int c = 0; c < kFwdBN / 32; ++c) {
+      const int cb = col0 + c * 32;
+      if (cb >= p.V) break;  // same for the whole warp
+      float x[32];
+      tmem_ld32(taddr + c * 32, x);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float pr = ex2(fmaf(x[j], p.sl, -lse2));
+        const float zp = x[j] * p.inv_tau;
+        x[j] = -pr * fmaf(a2, zp - ez, a1);
+      }
+      const int rel = tgt - cb;
+      if (static_cast<unsigned>(rel) < 32u) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] += (rel == j) ? a1 : 0.f;
+      }
+      if (!valid) continue;
+      if (cb + 32 <= p.V) {
+        store32_16(grow + cb, x, p.bf16);
+      } else {
+        const int nv = p.V - cb;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < nv) grow[cb + j] = pack1(x[j], p.bf16);
+      }
+    }
+  }
+
+  __device__ __forceinline__ void end(int, int) {}
+};
+
+// ---------------------------------------------------------------- dh = G W
+struct DhEpi {
+  struct Params {
+    int R, H, r0;
+    int64_t T;
+    const int64_t *row_idx;
+    uint16_t *dh;
+    int64_t ld;
+    bool bf16;
+  };
+  const Params p;
+  __device__ __forceinline__ explicit DhEpi(const Params &pp) : p(pp) {}
+
+  __device__ __forceinline__ void tile(uint32_t taddr, int mt, int nt, int lg, int lane) {
+    const int row = mt * kBM + lg * 32 + lane;
+    bool valid = row < p.R;
+    int64_t orig = 0;
+    if (valid) {
+      orig = p.row_idx ? p.row_idx[p.r0 + row] : p.r0 + row;
+      valid = orig >= 0 && orig < p.T;
+    }
+    uint16_t *drow = p.dh + (valid ? orig : 0) * p.ld;
+#pragma unroll 1
+    for (int c = 0; c < kGemmBN / 32; ++c) {
+      const int col = nt * kGemmBN + c * 32;
+      if (col >= p.H) break;
+      float x[32];
+      tmem_ld32(taddr + c * 32, x);
+      if (!valid) continue;
+      if (col + 32 <= p.H) {
+        store32_16(drow + col, x, p.bf16);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (col + j < p.H) drow[col + j] = pack1(x[j], p.bf16);
+      }
+    }
+  }
+};
+
+// ---------------------------------------------------------------- dW = G^T h
+struct DwEpi {
+  struct Params {
+    int V, H;
+    float *dW;
+    int64_t ld;
+    int accumulate;
+  };
+  const Params p;
+  __device__ __forceinline__ explicit DwEpi(const Params &pp) : p(pp) {}
+
+  __device__ __forceinline__ void tile(uint32_t taddr, int mt, int nt, int lg, int lane) {
+    const int v = mt * kBM + lg * 32 + lane;
+    const bool valid = v < p.V;
+    float *drow = p.dW + static_cast<int64_t>(valid ? v : 0) * p.ld;
+#pragma unroll 1
+    for (int c = 0; c < kGemmBN / 32; ++c) {
+      const int col = nt * kGemmBN + c * 32;
+      if (col >= p.H) break;
+      float x[32];
+      tmem_ld32(taddr + c * 32, x);
+      if (!valid) continue;
+      if (col + 32 <= p.H) {
+        float4 *d = reinterpret_cast<float4 *>(drow + col);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          float4 o = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+          if (p.accumulate) {
+            const float4 prev = d[q];
+            o.x += prev.x;
+            o.y += prev.y;
+            o.z += prev.z;
+            o.w += prev.w;
+          }
+          d[q] = o;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (col + j < p.H) drow[col + j] = p.accumulate ? drow[col + j] + x[j] : x[j];
+      }
+    }
+  }
+};
+
+// ---------------------------------------------------------------- launchers
+cudaError_t launch_grad(const GradArgs &a, cudaStream_t stream) {
+  using L = PipeLayout<kFwdBN, kFwdStages, 1>;
+  auto kern = vocab_pipeline_kernel<kFwdBN, kFwdStages, 1, GradEpi>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  GradEpi::Params p;
+  p.n = a.sch.n;
+  p.V = a.sch.V;
+  p.r0 = a.r0;
+  p.T = a.T;
+  p.targets = a.targets;
+  p.row_idx = a.row_idx;
+  p.lse = a.lse;
+  p.ez = a.ez;
+  p.g1 = a.g1;
+  p.g2 = a.g2;
+  p.sl = a.scale_log2;
+  p.inv_tau = a.inv_tau;
+  p.G = static_cast<uint16_t *>(a.G);
+  p.ldg = a.ldg;
+  p.bf16 = a.bf16;
+  const uint32_t idesc = idesc_f16(a.bf16, kBM, kFwdBN, false, false);
+  kern<<<a.grid, kPipeThreads, L::kSmemBytes, stream>>>(a.tmA, a.tmB, a.tmA, a.tmB, a.sch, idesc,
+                                                          p, a.status);
+  return cudaGetLastError();
+}
+
+static GemmShape gemm_shape(int M, int N, int K) {
+  GemmShape g;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.m_tiles = (M + kBM - 1) / kBM;
+  g.n_tiles = (N + kGemmBN - 1) / kGemmBN;
+  g.tiles = g.m_tiles * g.n_tiles;
+  g.k_blocks = (K + kBK - 1) / kBK;
+  return g;
+}
+
+int gemm_tiles(int M, int N) { return gemm_shape(M, N, 1).tiles; }
+
+cudaError_t launch_dh_gemm(const GemmArgs &a, cudaStream_t stream) {
+  auto kern = gemm_kernel<false, true, DhEpi>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       GemmLayout::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  DhEpi::Params p;
+  p.R = a.M;
+  p.H = a.N;
+  p.r0 = a.r0;
+  p.T = a.T;
+  p.row_idx = a.row_idx;
+  p.dh = static_cast<uint16_t *>(a.dh);
+  p.ld = a.ld_dh;
+  p.bf16 = a.bf16;
+  const uint32_t idesc = idesc_f16(a.bf16, kBM, kGemmBN, false, true);
+  kern<<<a.grid, kPipeThreads, GemmLayout::kSmemBytes, stream>>>(
+      a.tmA, a.tmB, gemm_shape(a.M, a.N, a.K), idesc, p, a.status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dw_gemm(const GemmArgs &a, cudaStream_t stream) {
+  auto kern = gemm_kernel<true, true, DwEpi>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       GemmLayout::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  DwEpi::Params p;
+  p.V = a.M;
+  p.H = a.N;
+  p.dW = a.dW;
+  p.ld = a.ld_dw;
+  p.accumulate = a.accumulate;
+  const uint32_t idesc = idesc_f16(a.bf16, kBM, kGemmBN, true, true);
+  kern<<<a.grid, kPipeThreads, GemmLayout::kSmemBytes, stream>>>(
+      a.tmA, a.tmB, gemm_shape(a.M, a.N, a.K), idesc, p, a.status);
+  return cudaGetLastError();
+}
+
+}  // namespace flp

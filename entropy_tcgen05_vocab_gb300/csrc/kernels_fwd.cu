@@ -200,8 +200,8 @@ __global__ void merge_kernel(int n, int splits, const float *__restrict__ pm,
       logp = zt[i] * inv_tau - lse;
     }
   }
-  out_logp[i] = logp;
-  out_ent[i] = ent;
+  if (out_logp) out_logp[i] = logp;
+  if (out_ent) out_ent[i] = ent;
   if (out_lse) out_lse[i] = lse;
   if (out_ez) out_ez[i] = lse - ent;
 }

@@ -49,12 +49,51 @@ struct KlArgs {
   uint32_t *status;
 };
 
+struct GradArgs {
+  CUtensorMap tmA;  // the chunk's scored hidden rows [R, H], box 64 x 128
+  CUtensorMap tmB;  // W [V, H], box 64 x kFwdBN
+  Schedule sch;     // over the chunk's R rows
+  int grid;
+  bool bf16;
+  int r0;           // first scored position of the chunk
+  int64_t T;
+  const int64_t *targets;
+  const int64_t *row_idx;
+  const float *lse, *ez, *g1, *g2;  // indexed by scored position
+  float scale_log2, inv_tau;
+  void *G;          // [R, ldg] model dtype
+  int64_t ldg;
+  uint32_t *status;
+};
+
+struct GemmArgs {
+  CUtensorMap tmA, tmB;
+  int M, N, K;
+  int grid;
+  bool bf16;
+  uint32_t *status;
+  // dh epilogue: row i of the product goes to dh[row_idx[r0 + i]]
+  int r0;
+  int64_t T;
+  const int64_t *row_idx;
+  void *dh;
+  int64_t ld_dh;
+  // dW epilogue
+  float *dW;
+  int64_t ld_dw;
+  int accumulate;
+};
+
 cudaError_t launch_gather(const void *h, int64_t ld_h, const int64_t *row_idx, int64_t n,
                           int64_t T, int64_t H, void *hs, int num_sms, cudaStream_t stream);
 cudaError_t launch_fwd_scoring(const FwdArgs &a, cudaStream_t stream);
 cudaError_t launch_fwd_merge(const FwdArgs &a, cudaStream_t stream);
 cudaError_t launch_kl(const KlArgs &a, cudaStream_t stream);
 cudaError_t launch_kl_merge(const KlArgs &a, cudaStream_t stream);
+cudaError_t launch_grad(const GradArgs &a, cudaStream_t stream);
+cudaError_t launch_dh_gemm(const GemmArgs &a, cudaStream_t stream);
+cudaError_t launch_dw_gemm(const GemmArgs &a, cudaStream_t stream);
+int gemm_tiles(int M, int N);
 int fwd_smem_bytes();
 
 }  // namespace flp

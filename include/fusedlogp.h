@@ -156,6 +156,10 @@ flp_status flp_kl(const flp_shape *shape, const void *h_s, const void *W_s,
  *   dh           [T, ld_h] dtype; dW [V, ld_w] float32
  * row_idx entries must be distinct (a row scored twice would need its dh
  * contributions summed; that is a precondition, not checked).
+ * n_rows == 0 writes zeros to dh and dW.  The scored rows are processed in
+ * chunks of at most flp's chunk size (as many rows as keep the chunk's
+ * logit gradient within 4 GiB; the environment variable FLP_GRAD_CHUNK_ROWS,
+ * read at each call, can lower it); chunk lengths follow flp_row_chunks.
  */
 flp_status flp_backward(const flp_shape *shape, const void *h, const void *W,
                         const int64_t *targets, const int64_t *row_idx,

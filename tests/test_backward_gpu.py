@@ -1,0 +1,163 @@
+"""GPU parity of flp_backward (dL/dh, dL/dW of sum g1 logp + g2 ent) against
+the float64 oracle.
+
+Tolerance (per tensor): ||d - ref||_F <= 1e-2 ||ref||_F, and every element
+within 1e-2 max|ref|.  Small cases compare dh and dW in full, across several
+row and vocabulary tiles, ragged hidden and vocabulary sizes, fp16, several
+row chunks and caller-supplied statistics.  At the full backward workload
+(16,384 rows, 60 % scored, H 4096, V 151,936) dh is compared on sampled rows,
+dW is checked through a property that holds at any size (its columns sum to
+zero because every row of G sums to zero), and dW is compared exactly on
+sampled vocabulary rows at the same H and V with fewer scored rows.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import entropy_tcgen05_vocab_gb300 as flp
+import workloads
+from oracle import coracle, ref
+
+pytestmark = pytest.mark.gpu
+RTOL = 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    flp.build()
+    flp.lib()
+
+
+def _rel(got, want, what):
+    g = got.detach().cpu().double().numpy() if isinstance(got, torch.Tensor) else got
+    assert np.all(np.isfinite(g)), what + ": non-finite"
+    fro = np.linalg.norm(g - want) / max(np.linalg.norm(want), 1e-30)
+    ele = np.abs(g - want).max() / max(np.abs(want).max(), 1e-30)
+    assert fro <= RTOL and ele <= RTOL, "%s: rel Frobenius %.2e, rel max %.2e" % (what, fro, ele)
+    return fro
+
+
+def _case(T, H, V, dtype="bf16", seed=41, tau=0.7, all_rows=False):
+    w = workloads.WORKLOADS[4].scaled(T=T, H=H, V=V, dtype=dtype, seed=seed, tau=tau)
+    d = workloads.make(w, device="cuda")
+    if all_rows:
+        d["row_idx"] = None
+        d["n"] = T
+        g = torch.Generator().manual_seed(seed)
+        d["g1"] = torch.randn(T, generator=g).cuda()
+        d["g2"] = torch.randn(T, generator=g).cuda()
+    return d
+
+
+def _oracle(d, dtype):
+    rows = None if d["row_idx"] is None else d["row_idx"].cpu().numpy()
+    dh_rows, dW = coracle.backward(d["h"].cpu(), d["W"].cpu(), d["targets"].cpu().numpy(), rows,
+                                   d["tau"], d["g1"].cpu().numpy(), d["g2"].cpu().numpy(), dtype)
+    T = d["h"].shape[0]
+    dh = coracle.scatter_rows(dh_rows, np.arange(T) if rows is None else rows, T)
+    return dh, dW
+
+
+@pytest.mark.parametrize("T,H,V,dtype", [
+    (300, 256, 3000, "bf16"),     # several row/vocab tiles, ragged tails
+    (260, 520, 3001, "bf16"),     # H not a multiple of 64 or 256; V odd (padded G rows)
+    (200, 128, 2048, "fp16"),
+    (129, 64, 300, "bf16"),
+])
+def test_backward_small(T, H, V, dtype):
+    d = _case(T, H, V, dtype=dtype)
+    dh, dW = flp.backward(d["h"], d["W"], d["targets"], d["row_idx"], d["tau"], d["g1"], d["g2"])
+    torch.cuda.synchronize()
+    ref_dh, ref_dW = _oracle(d, dtype)
+    _rel(dh, ref_dh, "dh")
+    _rel(dW, ref_dW, "dW")
+    scored = np.zeros(T, bool)
+    scored[d["row_idx"].cpu().numpy()] = True
+    assert torch.count_nonzero(dh[torch.from_numpy(~scored).cuda()]) == 0
+
+
+def test_backward_all_rows_and_supplied_statistics():
+    d = _case(384, 256, 4000, all_rows=True, tau=1.0)
+    logp, ent, lse, ez = flp.logprob_entropy(d["h"], d["W"], d["targets"], None, 1.0,
+                                             return_stats=True)
+    a = flp.backward(d["h"], d["W"], d["targets"], None, 1.0, d["g1"], d["g2"])
+    b = flp.backward(d["h"], d["W"], d["targets"], None, 1.0, d["g1"], d["g2"], lse, ez)
+    torch.cuda.synchronize()
+    ref_dh, ref_dW = _oracle(d, "bf16")
+    for dh, dW in (a, b):
+        _rel(dh, ref_dh, "dh")
+        _rel(dW, ref_dW, "dW")
+
+
+def test_backward_several_row_chunks(monkeypatch):
+    d = _case(700, 256, 3000, seed=42)
+    n = d["n"]
+    monkeypatch.setenv("FLP_GRAD_CHUNK_ROWS", "128")
+    assert len(flp.row_chunks(n, 128)) >= 3
+    dh, dW = flp.backward(d["h"], d["W"], d["targets"], d["row_idx"], d["tau"], d["g1"], d["g2"])
+    torch.cuda.synchronize()
+    ref_dh, ref_dW = _oracle(d, "bf16")
+    _rel(dh, ref_dh, "dh")
+    _rel(dW, ref_dW, "dW")
+
+
+def test_backward_no_scored_rows_gives_zeros():
+    d = _case(64, 128, 512)
+    rows = torch.zeros(0, dtype=torch.int64, device="cuda")
+    e = torch.zeros(0, device="cuda")
+    dh, dW = flp.backward(d["h"], d["W"], d["targets"], rows, 0.7, e, e)
+    assert torch.count_nonzero(dh) == 0 and torch.count_nonzero(dW) == 0
+
+
+def test_autograd_function_matches_backward():
+    d = _case(256, 128, 2000, seed=43)
+    h = d["h"].clone().requires_grad_(True)
+    W = d["W"].clone().requires_grad_(True)
+    logp, ent = flp.FusedLogProbEntropy.apply(h, W, d["targets"], d["row_idx"], d["tau"])
+    (logp * d["g1"] + ent * d["g2"]).sum().backward()
+    dh, dW = flp.backward(d["h"], d["W"], d["targets"], d["row_idx"], d["tau"], d["g1"], d["g2"])
+    assert torch.equal(h.grad, dh)
+    assert torch.allclose(W.grad.float(), dW.to(torch.bfloat16).float())
+
+
+def test_backward_workload_full_size():
+    d = workloads.make(4, device="cuda")
+    dh, dW = flp.backward(d["h"], d["W"], d["targets"], d["row_idx"], d["tau"], d["g1"], d["g2"])
+    torch.cuda.synchronize()
+    n = d["n"]
+    rows = d["row_idx"].cpu().numpy()
+    # dh on sampled scored rows (each needs only its own row statistics)
+    sel = workloads.sample_rows(n, 96, seed=4)
+    want, _ = ref.backward(d["h"].cpu(), d["W"].cpu(), d["targets"].cpu().numpy(), rows, d["tau"],
+                           d["g1"].cpu().numpy(), d["g2"].cpu().numpy(), "bf16",
+                           dh_rows_sel=sel, vsel=np.zeros(0, np.int64),
+                           stats=(np.zeros(n), np.zeros(n)))
+    _rel(dh[torch.from_numpy(rows[sel]).cuda()], want, "dh (sampled rows)")
+    # unscored rows are zero
+    scored = torch.zeros(d["h"].shape[0], dtype=torch.bool, device="cuda")
+    scored[d["row_idx"]] = True
+    assert torch.count_nonzero(dh[~scored]) == 0
+    # dW: every row of G sums to zero, so the columns of dW sum to zero
+    colsum = dW.double().sum(0)
+    scale = dW.double().abs().sum(0)
+    assert torch.all(colsum.abs() <= 2e-3 * scale), (colsum.abs() / scale).max()
+    assert torch.isfinite(dW).all()
+
+
+def test_backward_dw_rows_exact_at_full_vocabulary():
+    # same H, V and launch shape as the full workload, 1,200 scored rows
+    w = workloads.WORKLOADS[4].scaled(T=2000)
+    d = workloads.make(w, device="cuda")
+    rows = d["row_idx"].cpu().numpy()
+    dh, dW = flp.backward(d["h"], d["W"], d["targets"], d["row_idx"], d["tau"], d["g1"], d["g2"])
+    torch.cuda.synchronize()
+    vsel = np.concatenate([workloads.sample_rows(w.V, 64, seed=44),
+                           d["targets"].cpu().numpy()[rows[:8]], [w.V - 1]])
+    _, want = ref.backward(d["h"].cpu(), d["W"].cpu(), d["targets"].cpu().numpy(), rows, d["tau"],
+                           d["g1"].cpu().numpy(), d["g2"].cpu().numpy(), "bf16",
+                           dh_rows_sel=np.zeros(0, np.int64), vsel=vsel)
+    _rel(dW[torch.from_numpy(vsel).cuda()], want, "dW (sampled vocabulary rows)")
