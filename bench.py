@@ -126,7 +126,7 @@ class ClockSampler:
             self.out = tempfile.TemporaryFile(mode="w+")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index),
-                 "--query-gpu=timestamp,clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+                 "--query-gpu=timestamp,clocks.sm,clocks.max.sm,clocks_event_reasons.active,power.draw",
                  "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=self.out, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
@@ -146,12 +146,13 @@ class ClockSampler:
         rows = []
         for ln in self.out.read().splitlines():
             parts = [x.strip() for x in ln.split(",")]
-            if len(parts) != 4:
+            if len(parts) != 5:
                 continue
             try:
                 ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
                 ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
-                rows.append((float(parts[1]), float(parts[2]), int(parts[3], 16), ts))
+                pw = float(parts[4]) if parts[4] not in ("[N/A]", "N/A") else float("nan")
+                rows.append((float(parts[1]), float(parts[2]), int(parts[3], 16), ts, pw))
             except (ValueError, IndexError):
                 continue
         if not rows:
@@ -165,9 +166,11 @@ class ClockSampler:
             for bit, name in REASON_BITS.items():
                 if r[2] & bit and name != "gpu_idle":
                     reasons.add(name)
+        pw = sorted(r[4] for r in busy if r[4] == r[4])
         return {"sm_mhz": mhz[len(mhz) // 2], "sm_max_mhz": max(r[1] for r in rows),
                 "reasons": sorted(reasons), "samples": len(busy),
-                "in_timed_region": bool(inside)}
+                "in_timed_region": bool(inside),
+                "power_w": pw[len(pw) // 2] if pw else None}
 
 
 def barrier(world):

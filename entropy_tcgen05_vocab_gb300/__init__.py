@@ -45,7 +45,8 @@ class FlpDeviceStatus(ctypes.Structure):
 
 class FlpPlan(ctypes.Structure):
     _fields_ = [("row_tiles", ctypes.c_int32), ("vocab_tiles", ctypes.c_int32),
-                ("block_n", ctypes.c_int32), ("splits", ctypes.c_int32),
+                ("block_m", ctypes.c_int32), ("block_n", ctypes.c_int32),
+                ("cta_group", ctypes.c_int32), ("splits", ctypes.c_int32),
                 ("tiles_per_split", ctypes.c_int32), ("band", ctypes.c_int32),
                 ("items", ctypes.c_int32), ("grid", ctypes.c_int32),
                 ("max_tiles_per_cta", ctypes.c_int64)]

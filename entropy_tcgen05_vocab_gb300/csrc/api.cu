@@ -128,12 +128,14 @@ Layout layout_for(const flp_shape *s, flp_op op) {
 // ------------------------------------------------------------------ planner
 struct PlanKey {
   int64_t n, V, H;
-  int bn, sms;
+  int bn, units, bm;
   bool operator<(const PlanKey &o) const {
-    return std::tie(n, V, H, bn, sms) < std::tie(o.n, o.V, o.H, o.bn, o.sms);
+    return std::tie(n, V, H, bn, units, bm) < std::tie(o.n, o.V, o.H, o.bn, o.units, o.bm);
   }
 };
 
+// `units` = CTAs (or CTA pairs) resident at once; `grid` is in the same
+// units (the kernel launch multiplies by the CTA-group size).
 struct Plan {
   Schedule sch;
   int grid;
@@ -143,15 +145,15 @@ struct Plan {
 std::mutex g_plan_mu;
 std::map<PlanKey, Plan> g_plans;
 
-Plan make_plan(int64_t n, int64_t V, int64_t H, int bn, int num_sms) {
+Plan make_plan(int64_t n, int64_t V, int64_t H, int bn, int num_sms, int bm) {
   Plan best{};
   Schedule s{};
   s.n = static_cast<int>(n);
   s.V = static_cast<int>(V);
-  s.row_tiles = static_cast<int>(cdiv(n, 128));
+  s.row_tiles = static_cast<int>(cdiv(n, bm));
   s.vocab_tiles = vocab_tiles(V, bn);
   s.k_blocks = static_cast<int>(cdiv(H, 64));
-  const int64_t a_tile_bytes = 128 * H * 2;
+  const int64_t a_tile_bytes = bm * H * 2;
   s.band = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(s.row_tiles, kBandBytes / a_tile_bytes)));
   const int smax = max_splits(V, bn);
   std::vector<int64_t> loads;
@@ -183,13 +185,13 @@ Plan make_plan(int64_t n, int64_t V, int64_t H, int bn, int num_sms) {
   return best;
 }
 
-Plan plan_cached(int64_t n, int64_t V, int64_t H, int bn, int num_sms) {
-  const PlanKey k{n, V, H, bn, num_sms};
+Plan plan_cached(int64_t n, int64_t V, int64_t H, int bn, int units, int bm) {
+  const PlanKey k{n, V, H, bn, units, bm};
   std::lock_guard<std::mutex> g(g_plan_mu);
   auto it = g_plans.find(k);
   if (it != g_plans.end()) return it->second;
   if (g_plans.size() > 256) g_plans.clear();
-  Plan p = make_plan(n, V, H, bn, num_sms);
+  Plan p = make_plan(n, V, H, bn, units, bm);
   g_plans.emplace(k, p);
   return p;
 }
@@ -353,15 +355,19 @@ flp_status flp_plan_scoring(const flp_shape *shape, flp_op op, int32_t num_sms, 
   std::memset(out, 0, sizeof *out);
   if (shape->n_rows == 0) return FLP_OK;
   const int bn = op == FLP_OP_KL ? kKlBN : kFwdBN;
-  const Plan p = plan_cached(shape->n_rows, shape->V, shape->H, bn, num_sms);
+  const int cg = op == FLP_OP_KL ? kKlCG : kFwdCG;
+  const int units = std::max(1, num_sms / cg);
+  const Plan p = plan_cached(shape->n_rows, shape->V, shape->H, bn, units, 128 * cg);
   out->row_tiles = p.sch.row_tiles;
   out->vocab_tiles = p.sch.vocab_tiles;
+  out->block_m = 128 * cg;
   out->block_n = bn;
+  out->cta_group = cg;
   out->splits = p.sch.splits;
   out->tiles_per_split = p.sch.tiles_per_split;
   out->band = p.sch.band;
   out->items = p.sch.items;
-  out->grid = p.grid;
+  out->grid = p.grid * cg;
   out->max_tiles_per_cta = p.max_load;
   return FLP_OK;
 }
@@ -396,7 +402,7 @@ flp_status flp_logprob_entropy(const flp_shape *s, const void *h, const void *W,
   if ((st = device_info(&dev)) != FLP_OK) return st;
 
   const Layout L = layout_for(s, FLP_OP_LOGPROB_ENTROPY);
-  const Plan p = plan_cached(s->n_rows, s->V, s->H, kFwdBN, dev.sms);
+  const Plan p = plan_cached(s->n_rows, s->V, s->H, kFwdBN, fwd_units(dev.sms), 128 * kFwdCG);
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   FwdArgs a{};
   const void *A = h;
@@ -406,9 +412,10 @@ flp_status flp_logprob_entropy(const flp_shape *s, const void *h, const void *W,
     lda = s->H;
   }
   if ((st = make_map(&a.tmA, s->dtype, A, s->H, s->n_rows, lda, 64, 128)) != FLP_OK) return st;
-  if ((st = make_map(&a.tmB, s->dtype, W, s->H, s->V, s->ld_w, 64, kFwdBN)) != FLP_OK) return st;
+  if ((st = make_map(&a.tmB, s->dtype, W, s->H, s->V, s->ld_w, 64, kFwdBN / kFwdCG)) != FLP_OK)
+    return st;
   a.sch = p.sch;
-  a.grid = p.grid;
+  a.grid = p.grid * kFwdCG;
   a.bf16 = s->dtype == FLP_BF16;
   a.targets = targets;
   a.row_idx = row_idx;
@@ -456,7 +463,7 @@ flp_status flp_kl(const flp_shape *s, const void *h_s, const void *W_s, const vo
   if ((st = device_info(&dev)) != FLP_OK) return st;
 
   const Layout L = layout_for(s, FLP_OP_KL);
-  const Plan p = plan_cached(s->n_rows, s->V, s->H, kKlBN, dev.sms);
+  const Plan p = plan_cached(s->n_rows, s->V, s->H, kKlBN, kl_units(dev.sms), 128 * kKlCG);
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   KlArgs a{};
   const void *As = h_s, *At = h_t;
@@ -468,10 +475,12 @@ flp_status flp_kl(const flp_shape *s, const void *h_s, const void *W_s, const vo
   }
   if ((st = make_map(&a.tmAs, s->dtype, As, s->H, s->n_rows, lda, 64, 128)) != FLP_OK) return st;
   if ((st = make_map(&a.tmAt, s->dtype, At, s->H, s->n_rows, lda, 64, 128)) != FLP_OK) return st;
-  if ((st = make_map(&a.tmBs, s->dtype, W_s, s->H, s->V, s->ld_w, 64, kKlBN)) != FLP_OK) return st;
-  if ((st = make_map(&a.tmBt, s->dtype, W_t, s->H, s->V, s->ld_w, 64, kKlBN)) != FLP_OK) return st;
+  if ((st = make_map(&a.tmBs, s->dtype, W_s, s->H, s->V, s->ld_w, 64, kKlBN / kKlCG)) != FLP_OK)
+    return st;
+  if ((st = make_map(&a.tmBt, s->dtype, W_t, s->H, s->V, s->ld_w, 64, kKlBN / kKlCG)) != FLP_OK)
+    return st;
   a.sch = p.sch;
-  a.grid = p.grid;
+  a.grid = p.grid * kKlCG;
   a.bf16 = s->dtype == FLP_BF16;
   a.row_idx = row_idx;
   a.T = s->T;
@@ -549,11 +558,12 @@ flp_status flp_backward(const flp_shape *s, const void *h, const void *W, const 
   // Per-row statistics (LSE, E[z']) unless the caller kept them from the forward.
   if (!lse) {
     FwdArgs a{};
-    const Plan p = plan_cached(s->n_rows, s->V, s->H, kFwdBN, dev.sms);
+    const Plan p = plan_cached(s->n_rows, s->V, s->H, kFwdBN, fwd_units(dev.sms), 128 * kFwdCG);
     if ((st = make_map(&a.tmA, s->dtype, A, s->H, s->n_rows, lda, 64, 128)) != FLP_OK) return st;
-    if ((st = make_map(&a.tmB, s->dtype, W, s->H, s->V, s->ld_w, 64, kFwdBN)) != FLP_OK) return st;
+    if ((st = make_map(&a.tmB, s->dtype, W, s->H, s->V, s->ld_w, 64, kFwdBN / kFwdCG)) != FLP_OK)
+      return st;
     a.sch = p.sch;
-    a.grid = p.grid;
+    a.grid = p.grid * kFwdCG;
     a.bf16 = s->dtype == FLP_BF16;
     a.targets = targets;
     a.row_idx = row_idx;
@@ -584,11 +594,12 @@ flp_status flp_backward(const flp_shape *s, const void *h, const void *W, const 
     const void *Ar = eb + static_cast<size_t>(r0) * lda * esz;
     // 1. G = d loss / d z for the chunk's rows
     GradArgs ga{};
-    const Plan p = plan_cached(rc, s->V, s->H, kFwdBN, dev.sms);
+    const Plan p = plan_cached(rc, s->V, s->H, kFwdBN, grad_units(dev.sms), 128 * kFwdCG);
     if ((st = make_map(&ga.tmA, s->dtype, Ar, s->H, rc, lda, 64, 128)) != FLP_OK) return st;
-    if ((st = make_map(&ga.tmB, s->dtype, W, s->H, s->V, s->ld_w, 64, kFwdBN)) != FLP_OK) return st;
+    if ((st = make_map(&ga.tmB, s->dtype, W, s->H, s->V, s->ld_w, 64, kFwdBN / kFwdCG)) != FLP_OK)
+      return st;
     ga.sch = p.sch;
-    ga.grid = p.grid;
+    ga.grid = p.grid * kFwdCG;
     ga.bf16 = s->dtype == FLP_BF16;
     ga.r0 = static_cast<int>(r0);
     ga.T = s->T;

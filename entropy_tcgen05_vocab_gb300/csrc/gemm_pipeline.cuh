@@ -73,8 +73,8 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     prefetch_tmap(&tmB);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, L::kTmemCols);
-    tmem_relinquish();
+    tmem_alloc<1>(tmem_slot, L::kTmemCols);
+    tmem_relinquish<1>();
   }
   tc_fence_before();
   __syncthreads();
@@ -203,7 +203,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, L::kTmemCols);
+  if (warp == 1) tmem_dealloc<1>(tmem_base, L::kTmemCols);
 }
 
 }  // namespace flp

@@ -19,6 +19,7 @@
 
 #include "gemm_pipeline.cuh"
 #include "launch.h"
+#include "launch_util.cuh"
 #include "vocab_pipeline.cuh"
 
 namespace flp {
@@ -219,12 +220,10 @@ struct DwEpi {
 };
 
 // ---------------------------------------------------------------- launchers
+using GradLayout = PipeLayout<kFwdBN, kFwdStages, 1, kFwdCG>;
+#define GRAD_KERNEL vocab_pipeline_kernel<kFwdBN, kFwdStages, 1, GradEpi, kFwdCG>
+
 cudaError_t launch_grad(const GradArgs &a, cudaStream_t stream) {
-  using L = PipeLayout<kFwdBN, kFwdStages, 1>;
-  auto kern = vocab_pipeline_kernel<kFwdBN, kFwdStages, 1, GradEpi>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
-  if (e != cudaSuccess) return e;
   GradEpi::Params p;
   p.n = a.sch.n;
   p.V = a.sch.V;
@@ -241,10 +240,18 @@ cudaError_t launch_grad(const GradArgs &a, cudaStream_t stream) {
   p.G = static_cast<uint16_t *>(a.G);
   p.ldg = a.ldg;
   p.bf16 = a.bf16;
-  const uint32_t idesc = idesc_f16(a.bf16, kBM, kFwdBN, false, false);
-  kern<<<a.grid, kPipeThreads, L::kSmemBytes, stream>>>(a.tmA, a.tmB, a.tmA, a.tmB, a.sch, idesc,
-                                                          p, a.status);
-  return cudaGetLastError();
+  const uint32_t idesc = idesc_f16(a.bf16, kBM * kFwdCG, kFwdBN, false, false);
+  return launch_persistent(GRAD_KERNEL, a.grid, GradLayout::kSmemBytes, kFwdCG, stream, a.tmA,
+                           a.tmB, a.tmA, a.tmB, a.sch, idesc, p, a.status);
+}
+
+int grad_units(int num_sms) {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return resident_units(GRAD_KERNEL, GradLayout::kSmemBytes, kFwdCG, num_sms);
+  if (!cached[dev]) cached[dev] = resident_units(GRAD_KERNEL, GradLayout::kSmemBytes, kFwdCG, num_sms);
+  return cached[dev];
 }
 
 static GemmShape gemm_shape(int M, int N, int K) {

@@ -16,6 +16,7 @@
 #include <cuda_runtime.h>
 
 #include "launch.h"
+#include "launch_util.cuh"
 #include "vocab_pipeline.cuh"
 
 namespace flp {
@@ -219,12 +220,10 @@ cudaError_t launch_gather(const void *h, int64_t ld_h, const int64_t *row_idx, i
   return cudaGetLastError();
 }
 
+using FwdLayout = PipeLayout<kFwdBN, kFwdStages, 1, kFwdCG>;
+#define FWD_KERNEL vocab_pipeline_kernel<kFwdBN, kFwdStages, 1, LseEpi, kFwdCG>
+
 cudaError_t launch_fwd_scoring(const FwdArgs &a, cudaStream_t stream) {
-  using L = PipeLayout<kFwdBN, kFwdStages, 1>;
-  auto kern = vocab_pipeline_kernel<kFwdBN, kFwdStages, 1, LseEpi>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
-  if (e != cudaSuccess) return e;
   LseEpi::Params p;
   p.targets = a.targets;
   p.row_idx = a.row_idx;
@@ -236,10 +235,18 @@ cudaError_t launch_fwd_scoring(const FwdArgs &a, cudaStream_t stream) {
   p.ps = a.ps;
   p.pb = a.pb;
   p.zt = a.zt;
-  const uint32_t idesc = idesc_f16(a.bf16, kBM, kFwdBN, false, false);
-  kern<<<a.grid, kPipeThreads, L::kSmemBytes, stream>>>(a.tmA, a.tmB, a.tmA, a.tmB, a.sch, idesc,
-                                                          p, a.status);
-  return cudaGetLastError();
+  const uint32_t idesc = idesc_f16(a.bf16, kBM * kFwdCG, kFwdBN, false, false);
+  return launch_persistent(FWD_KERNEL, a.grid, FwdLayout::kSmemBytes, kFwdCG, stream, a.tmA,
+                           a.tmB, a.tmA, a.tmB, a.sch, idesc, p, a.status);
+}
+
+int fwd_units(int num_sms) {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return resident_units(FWD_KERNEL, FwdLayout::kSmemBytes, kFwdCG, num_sms);
+  if (!cached[dev]) cached[dev] = resident_units(FWD_KERNEL, FwdLayout::kSmemBytes, kFwdCG, num_sms);
+  return cached[dev];
 }
 
 cudaError_t launch_fwd_merge(const FwdArgs &a, cudaStream_t stream) {
@@ -250,6 +257,6 @@ cudaError_t launch_fwd_merge(const FwdArgs &a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-int fwd_smem_bytes() { return PipeLayout<kFwdBN, kFwdStages, 1>::kSmemBytes; }
+int fwd_smem_bytes() { return FwdLayout::kSmemBytes; }
 
 }  // namespace flp

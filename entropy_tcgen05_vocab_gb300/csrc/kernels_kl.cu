@@ -17,6 +17,7 @@
 #include <cuda_runtime.h>
 
 #include "launch.h"
+#include "launch_util.cuh"
 #include "vocab_pipeline.cuh"
 
 namespace flp {
@@ -165,12 +166,10 @@ __global__ void kl_merge_kernel(int n, int splits, const float *__restrict__ pmt
   out_kl[i] = kl;
 }
 
+using KlLayout = PipeLayout<kKlBN, kKlStages, 2, kKlCG>;
+#define KL_KERNEL vocab_pipeline_kernel<kKlBN, kKlStages, 2, KlEpi, kKlCG>
+
 cudaError_t launch_kl(const KlArgs &a, cudaStream_t stream) {
-  using L = PipeLayout<kKlBN, kKlStages, 2>;
-  auto kern = vocab_pipeline_kernel<kKlBN, kKlStages, 2, KlEpi>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
-  if (e != cudaSuccess) return e;
   KlEpi::Params p;
   p.n = a.sch.n;
   p.V = a.sch.V;
@@ -179,10 +178,18 @@ cudaError_t launch_kl(const KlArgs &a, cudaStream_t stream) {
   p.pct = a.pct;
   p.pms = a.pms;
   p.pss = a.pss;
-  const uint32_t idesc = idesc_f16(a.bf16, kBM, kKlBN, false, false);
-  kern<<<a.grid, kPipeThreads, L::kSmemBytes, stream>>>(a.tmAs, a.tmBs, a.tmAt, a.tmBt, a.sch,
-                                                          idesc, p, a.status);
-  return cudaGetLastError();
+  const uint32_t idesc = idesc_f16(a.bf16, kBM * kKlCG, kKlBN, false, false);
+  return launch_persistent(KL_KERNEL, a.grid, KlLayout::kSmemBytes, kKlCG, stream, a.tmAs, a.tmBs,
+                           a.tmAt, a.tmBt, a.sch, idesc, p, a.status);
+}
+
+int kl_units(int num_sms) {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return resident_units(KL_KERNEL, KlLayout::kSmemBytes, kKlCG, num_sms);
+  if (!cached[dev]) cached[dev] = resident_units(KL_KERNEL, KlLayout::kSmemBytes, kKlCG, num_sms);
+  return cached[dev];
 }
 
 cudaError_t launch_kl_merge(const KlArgs &a, cudaStream_t stream) {

@@ -12,12 +12,16 @@
 
 namespace flp {
 
-// Tile shape of the forward scoring pipeline.
+// Tile shape of the forward scoring and gradient pipelines: CTA pairs
+// (cta_group::2) on 256-row x 256-column tiles, 6 stages of 32 KB per CTA.
 constexpr int kFwdBN = 256;
-constexpr int kFwdStages = 4;
-// Tile shape of the KL pipeline (two accumulators per tile).
+constexpr int kFwdCG = 2;
+constexpr int kFwdStages = 6;
+// Tile shape of the KL pipeline (two accumulators per tile): CTA pairs on
+// 256-row x 128-column tiles, 4 stages of 48 KB per CTA.
 constexpr int kKlBN = 128;
-constexpr int kKlStages = 3;
+constexpr int kKlCG = 2;
+constexpr int kKlStages = 4;
 
 
 struct FwdArgs {
@@ -95,5 +99,9 @@ cudaError_t launch_dh_gemm(const GemmArgs &a, cudaStream_t stream);
 cudaError_t launch_dw_gemm(const GemmArgs &a, cudaStream_t stream);
 int gemm_tiles(int M, int N);
 int fwd_smem_bytes();
+// CTAs or CTA pairs of each pipeline that can be resident at once.
+int fwd_units(int num_sms);
+int grad_units(int num_sms);
+int kl_units(int num_sms);
 
 }  // namespace flp

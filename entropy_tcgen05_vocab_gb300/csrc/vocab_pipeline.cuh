@@ -1,30 +1,40 @@
 // vocab_pipeline.cuh -- the persistent tensor-core pipeline that streams the
-// LM-head weight W past 128-row tiles of hidden states and hands each
-// 128 x BN FP32 logit tile, straight out of tensor memory, to an epilogue.
+// LM-head weight W past tiles of hidden-state rows and hands each FP32 logit
+// tile, straight out of tensor memory, to an epilogue.
 //
 // This is the "output layer on the rows it scores, a tile at a time" loop of
 // miles PR #4645 ("How it works": Op) with the tile living in TMEM instead
 // of a [tile, vocab] buffer: no logit ever reaches global memory.
 //
-// Work decomposition.  Rows are cut into 128-row tiles, the vocabulary into
-// BN-column tiles.  A work item is (row tile, vocabulary split): one CTA
-// sweeps the split's vocabulary tiles for its row tile, keeping per-row
-// running state in registers, and emits one partial state per row and item.
-// Items are ordered band by band (a band = `band` consecutive row tiles, all
-// splits of the band, row tiles fastest) so the CTAs resident at one time
-// share the same weight tiles and each W tile is read from HBM about once
-// per band while the band's hidden rows stay in L2.  Persistent CTAs take
-// items round robin.
+// Work decomposition.  Rows are cut into row tiles of 128 x CG rows, the
+// vocabulary into BN-column tiles.  A work item is (row tile, vocabulary
+// split): one CTA (CG = 1) or one CTA pair (CG = 2) sweeps the split's
+// vocabulary tiles for its row tile, keeping per-row running state in
+// registers, and emits one partial state per row and item.  Items are ordered
+// band by band (a band = `band` consecutive row tiles, all splits of the
+// band, row tiles fastest) so the CTAs resident at one time share the same
+// weight tiles and each W tile is read from HBM about once per band while
+// the band's hidden rows stay in L2.  Persistent CTAs (pairs) take items
+// round robin.
 //
-// Roles (192 threads):
+// Roles (192 threads per CTA):
 //   warp 0     TMA producer: A (hidden rows, K-major) and B (W rows, K-major)
 //              per 64-wide K block into a STAGES-deep ring of 128B-swizzled
 //              shared-memory stages.
 //   warp 1     TMEM allocation + tcgen05.mma issue (one elected lane),
-//              M=128, N=BN, K=16 per instruction, FP32 accumulators in a
-//              double-buffered TMEM region (2 x BN columns).
+//              M = 128 x CG, N = BN, K = 16 per instruction, FP32 accumulators
+//              in a double-buffered TMEM region.
 //   warps 2-5  epilogue: tcgen05.ld of their 32 TMEM lanes (= 32 rows),
 //              32 columns at a time, folded by the Epi policy.
+//
+// CTA pairs (CG = 2, cluster of 2): each CTA loads its own 128 rows of A and
+// its half (BN/2 rows) of B; the leader (rank 0) issues tcgen05.mma.cta_group::2
+// for the 256 x BN tile, which reads both CTAs' shared memory and writes
+// each CTA's 128 rows of the accumulator into that CTA's TMEM.  Both halves'
+// TMA bytes complete on the leader's "full" barrier; the leader's commits
+// multicast to both CTAs' "empty" and "accumulator full" barriers; both
+// CTAs' epilogues arrive on the leader's "accumulator empty" barrier.  This
+// halves the B traffic each SM pulls from L2 per flop.
 #pragma once
 
 #include <cfloat>
@@ -35,21 +45,22 @@
 
 namespace flp {
 
-constexpr int kBM = 128;         // rows per tile (TMEM lanes)
+constexpr int kBM = 128;         // rows per CTA tile (TMEM lanes)
 constexpr int kBK = 64;          // K elements per stage = one 128-byte swizzle row
 constexpr int kUmmaK = 16;       // K per tcgen05.mma kind::f16
 constexpr int kEpiWarps = 4;
 constexpr int kPipeThreads = 64 + 32 * kEpiWarps;
 
-
 // NOPS independent GEMMs share one tile (the KL pipeline runs the student and
-// the teacher head side by side, NOPS = 2).  Stage layout:
-// [A_0 .. A_{NOPS-1} | B_0 .. B_{NOPS-1}]; TMEM: two accumulator buffers of
-// NOPS x BN columns (GEMM op at column offset op * BN inside a buffer).
-template <int BN, int STAGES, int NOPS = 1>
+// the teacher head side by side, NOPS = 2).  Per-CTA stage layout:
+// [A_0 .. A_{NOPS-1} | B_0 .. B_{NOPS-1}] with B_i holding BN / CG rows; TMEM:
+// two accumulator buffers of NOPS x BN columns (GEMM op at column offset
+// op * BN inside a buffer).
+template <int BN, int STAGES, int NOPS = 1, int CG = 1>
 struct PipeLayout {
   static constexpr int kABytes = kBM * kBK * 2;
-  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kBRows = BN / CG;
+  static constexpr int kBBytes = kBRows * kBK * 2;
   static constexpr int kStageBytes = NOPS * (kABytes + kBBytes);
   static constexpr int kAccCols = NOPS * BN;
   static constexpr int kTmemCols = 2 * kAccCols;
@@ -57,11 +68,23 @@ struct PipeLayout {
   // + 1024 so the stage ring can be aligned to a swizzle atom.
   static constexpr int kSmemBytes = STAGES * kStageBytes + kBarrierBytes + 1024;
   static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM columns must be a power of two");
+  static_assert(CG == 1 || CG == 2, "one CTA or a CTA pair");
 };
 
+// Sets this CTA's abort flag (and, for a pair, the peer's) and counts the
+// timeout in the device status word.
+template <int CG>
 __device__ __forceinline__ void record_timeout(uint32_t *status, volatile int *abort_flag) {
   *abort_flag = 1;
+  if (CG == 2) {
+    const uint32_t peer = cluster_ctarank() ^ 1u;
+    st_cluster_u32(mapa_shared(smem_u32(const_cast<int *>(abort_flag)), peer), 1u);
+  }
   atomicAdd(status + kStatTimeout, 1u);
+}
+
+__device__ __forceinline__ void record_timeout(uint32_t *status, volatile int *abort_flag) {
+  record_timeout<1>(status, abort_flag);
 }
 
 // Epi must provide:
@@ -72,7 +95,8 @@ __device__ __forceinline__ void record_timeout(uint32_t *status, volatile int *a
 //                                                          lanes at the tile's first column
 //                                                          (GEMM op at + op * BN)
 //   __device__ void end(int split, int row);
-template <int BN, int STAGES, int NOPS, class Epi>
+// CG = 2 kernels must be launched with a cluster dimension of 2.
+template <int BN, int STAGES, int NOPS, class Epi, int CG = 1>
 __global__ void __launch_bounds__(kPipeThreads, 1)
     vocab_pipeline_kernel(const __grid_constant__ CUtensorMap tmA0,
                           const __grid_constant__ CUtensorMap tmB0,
@@ -80,8 +104,9 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                           const __grid_constant__ CUtensorMap tmB1, const Schedule sch,
                           const uint32_t idesc, const typename Epi::Params ep,
                           uint32_t *status) {
-  using L = PipeLayout<BN, STAGES, NOPS>;
+  using L = PipeLayout<BN, STAGES, NOPS, CG>;
   static_assert(NOPS == 1 || NOPS == 2, "one or two GEMMs per tile");
+  constexpr bool kPair = CG == 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -95,6 +120,10 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int unit = blockIdx.x / CG;          // CTA (pair) index
+  const int num_units = gridDim.x / CG;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -103,7 +132,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], kEpiWarps);
+      mbar_init(&tempty[a], kEpiWarps * CG);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -118,11 +147,14 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     }
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, L::kTmemCols);
-    tmem_relinquish();
+    tmem_alloc<CG>(tmem_slot, L::kTmemCols);
+    tmem_relinquish<CG>();
   }
   tc_fence_before();
-  __syncthreads();
+  if (kPair)
+    cluster_sync();
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -132,10 +164,14 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     uint32_t phase = 0;
     uint32_t armed = 0;  // bit s: stage s has been armed at least once
     bool ok = true;
-    for (int it = blockIdx.x; ok && it < sch.items; it += gridDim.x) {
+    // the pair's bytes all complete on the leader's "full" barriers
+    const uint32_t full_dst = kPair ? mapa_shared(smem_u32(full), 0) : smem_u32(full);
+    for (int it = unit; ok && it < sch.items; it += num_units) {
       int mt, sp, vt0, vt1;
       sch.item(it, mt, sp, vt0, vt1);
+      const int arow = mt * (kBM * CG) + static_cast<int>(rank) * kBM;
       for (int vt = vt0; ok && vt < vt1; ++vt) {
+        const int brow = vt * BN + static_cast<int>(rank) * L::kBRows;
         for (int kb = 0; kb < sch.k_blocks; ++kb) {
           if (lane == 0) ok = mbar_wait(&empty[stage], phase ^ 1u, abort_flag);
           ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -143,12 +179,22 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
           if (lane == 0) {
             uint8_t *sa = smem + stage * L::kStageBytes;
             uint8_t *sb = sa + NOPS * L::kABytes;
-            mbar_arrive_expect_tx(&full[stage], L::kStageBytes);
-            tma_load_2d(sa, &tmA0, &full[stage], kb * kBK, mt * kBM);
-            tma_load_2d(sb, &tmB0, &full[stage], kb * kBK, vt * BN);
-            if (NOPS == 2) {
-              tma_load_2d(sa + L::kABytes, &tmA1, &full[stage], kb * kBK, mt * kBM);
-              tma_load_2d(sb + L::kBBytes, &tmB1, &full[stage], kb * kBK, vt * BN);
+            if (leader) mbar_arrive_expect_tx(&full[stage], CG * L::kStageBytes);
+            if (kPair) {
+              const uint32_t fb = full_dst + stage * 8;
+              tma_load_2d_pair(sa, &tmA0, fb, kb * kBK, arow);
+              tma_load_2d_pair(sb, &tmB0, fb, kb * kBK, brow);
+              if (NOPS == 2) {
+                tma_load_2d_pair(sa + L::kABytes, &tmA1, fb, kb * kBK, arow);
+                tma_load_2d_pair(sb + L::kBBytes, &tmB1, fb, kb * kBK, brow);
+              }
+            } else {
+              tma_load_2d(sa, &tmA0, &full[stage], kb * kBK, arow);
+              tma_load_2d(sb, &tmB0, &full[stage], kb * kBK, brow);
+              if (NOPS == 2) {
+                tma_load_2d(sa + L::kABytes, &tmA1, &full[stage], kb * kBK, arow);
+                tma_load_2d(sb + L::kBBytes, &tmB1, &full[stage], kb * kBK, brow);
+              }
             }
           }
           armed |= 1u << stage;
@@ -161,85 +207,108 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     }
     if (!ok) {
       if (lane == 0) {
-        record_timeout(status, abort_flag);
-        // Let the copies already in flight land before the CTA leaves.
-        for (int s = 0; s < STAGES; ++s) {
-          if (!(armed & (1u << s))) continue;
-          // Stage s was last armed in the phase before the current one for
-          // stages behind `stage`, in the current one otherwise.
-          const uint32_t par = (s < stage) ? phase : (phase ^ 1u);
-          int never = 0;
-          mbar_wait(&full[s], par, &never);
+        record_timeout<CG>(status, abort_flag);
+        if (leader) {
+          // Let the copies already in flight land before the CTA leaves.
+          for (int s = 0; s < STAGES; ++s) {
+            if (!(armed & (1u << s))) continue;
+            // Stage s was last armed in the current phase for stages behind
+            // `stage`, in the previous one otherwise.
+            const uint32_t par = (s < stage) ? phase : (phase ^ 1u);
+            int never = 0;
+            mbar_wait(&full[s], par, &never);
+          }
         }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    int stage = 0;
-    uint32_t phase = 0;
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    bool ok = true;
-    for (int it = blockIdx.x; ok && it < sch.items; it += gridDim.x) {
-      int mt, sp, vt0, vt1;
-      sch.item(it, mt, sp, vt0, vt1);
-      for (int vt = vt0; ok && vt < vt1; ++vt) {
-        if (lane == 0) ok = mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * L::kAccCols);
-        for (int kb = 0; kb < sch.k_blocks; ++kb) {
-          if (lane == 0) ok = mbar_wait(&full[stage], phase, abort_flag);
+    if (leader) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int it = unit; ok && it < sch.items; it += num_units) {
+        int mt, sp, vt0, vt1;
+        sch.item(it, mt, sp, vt0, vt1);
+        for (int vt = vt0; ok && vt < vt1; ++vt) {
+          if (lane == 0) ok = mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag);
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
           tc_fence_after();
-          if (lane == 0) {
-            const uint32_t a0 = smem_u32(smem + stage * L::kStageBytes);
-            const uint32_t b0 = a0 + NOPS * L::kABytes;
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * L::kAccCols);
+          for (int kb = 0; kb < sch.k_blocks; ++kb) {
+            if (lane == 0) ok = mbar_wait(&full[stage], phase, abort_flag);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            if (lane == 0) {
+              const uint32_t a0 = smem_u32(smem + stage * L::kStageBytes);
+              const uint32_t b0 = a0 + NOPS * L::kABytes;
 #pragma unroll
-            for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
+              for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
 #pragma unroll
-              for (int op = 0; op < NOPS; ++op) {
-                const uint64_t ad = sdesc_sw128(a0 + op * L::kABytes + kk * kUmmaK * 2, 16, 1024);
-                const uint64_t bd = sdesc_sw128(b0 + op * L::kBBytes + kk * kUmmaK * 2, 16, 1024);
-                mma_f16(d_tmem + op * BN, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                for (int op = 0; op < NOPS; ++op) {
+                  const uint64_t ad =
+                      sdesc_sw128(a0 + op * L::kABytes + kk * kUmmaK * 2, 16, 1024);
+                  const uint64_t bd =
+                      sdesc_sw128(b0 + op * L::kBBytes + kk * kUmmaK * 2, 16, 1024);
+                  if (kPair)
+                    mma_f16_pair(d_tmem + op * BN, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                  else
+                    mma_f16(d_tmem + op * BN, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                }
               }
+              // frees the stage (in both CTAs of a pair) when these MMAs finish
+              if (kPair)
+                mma_commit_pair(&empty[stage], 0x3);
+              else
+                mma_commit(&empty[stage]);
             }
-            mma_commit(&empty[stage]);  // frees the stage when these MMAs finish
+            __syncwarp();
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          if (lane == 0) {  // accumulator ready for the epilogue(s)
+            if (kPair)
+              mma_commit_pair(&tfull[acc], 0x3);
+            else
+              mma_commit(&tfull[acc]);
           }
           __syncwarp();
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1u;
         }
-        if (!ok) break;
-        if (lane == 0) mma_commit(&tfull[acc]);  // accumulator ready for the epilogue
-        __syncwarp();
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
       }
-    }
-    if (!ok && lane == 0) {
-      record_timeout(status, abort_flag);
-      // Wait for the MMAs already issued before TMEM is released.
-      mma_commit(drain);
-      int never = 0;
-      mbar_wait(drain, 0, &never);
+      if (!ok && lane == 0) {
+        record_timeout<CG>(status, abort_flag);
+        // Wait for the MMAs already issued before TMEM is released.
+        if (kPair)
+          mma_commit_pair_local(drain);
+        else
+          mma_commit(drain);
+        int never = 0;
+        mbar_wait(drain, 0, &never);
+      }
     }
   } else {
     // ------------------------------------------------------------ epilogue
     const int lg = warp & 3;  // the TMEM lane quarter this warp may access
     const uint32_t lane_off = static_cast<uint32_t>(lg * 32) << 16;
+    // the pair's "accumulator empty" barriers live in the leader
+    const uint32_t tempty_dst = kPair ? mapa_shared(smem_u32(tempty), 0) : smem_u32(tempty);
     Epi epi(ep);
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int it = blockIdx.x; ok && it < sch.items; it += gridDim.x) {
+    for (int it = unit; ok && it < sch.items; it += num_units) {
       int mt, sp, vt0, vt1;
       sch.item(it, mt, sp, vt0, vt1);
-      const int row = mt * kBM + lg * 32 + lane;
+      const int row = mt * (kBM * CG) + static_cast<int>(rank) * kBM + lg * 32 + lane;
       epi.begin(mt, row);
       for (int vt = vt0; vt < vt1; ++vt) {
         if (lane == 0) ok = mbar_wait(&tfull[acc], acc_phase, abort_flag);
@@ -249,20 +318,28 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
         epi.tile(tmem_base + lane_off + static_cast<uint32_t>(acc * L::kAccCols), vt * BN);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[acc]);
+        if (lane == 0) {
+          if (kPair)
+            mbar_arrive_cluster(tempty_dst + acc * 8);
+          else
+            mbar_arrive(&tempty[acc]);
+        }
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }
       if (!ok) break;
       epi.end(sp, row);
     }
-    if (!ok && lane == 0) record_timeout(status, abort_flag);
+    if (!ok && lane == 0) record_timeout<CG>(status, abort_flag);
   }
 
   tc_fence_before();
-  __syncthreads();
+  if (kPair)
+    cluster_sync();
+  else
+    __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, L::kTmemCols);
+  if (warp == 1) tmem_dealloc<CG>(tmem_base, L::kTmemCols);
 }
 
 }  // namespace flp

@@ -231,15 +231,17 @@ const char *flp_last_error(void);
  * function; no GPU needed).  num_sms is the number of SMs to plan for.
  */
 typedef struct {
-    int32_t row_tiles;      /* ceil(n_rows / 128) */
+    int32_t row_tiles;      /* ceil(n_rows / block_m) */
     int32_t vocab_tiles;    /* ceil(V / block_n) */
+    int32_t block_m;        /* scored rows per tensor-core tile (128 x cta_group) */
     int32_t block_n;        /* vocabulary columns per tensor-core tile */
+    int32_t cta_group;      /* CTAs that share one tile (2: tcgen05 CTA pairs) */
     int32_t splits;         /* vocabulary splits per row tile (partial states per row) */
     int32_t tiles_per_split;
     int32_t band;           /* row tiles that share the weight stream in one band */
     int32_t items;          /* work items = row_tiles * splits */
-    int32_t grid;           /* persistent CTAs launched */
-    int64_t max_tiles_per_cta; /* load of the busiest CTA, in 128 x block_n tiles */
+    int32_t grid;           /* persistent CTAs launched (a multiple of cta_group) */
+    int64_t max_tiles_per_cta; /* load of the busiest CTA (pair), in block_m x block_n tiles */
 } flp_plan;
 
 flp_status flp_plan_scoring(const flp_shape *shape, flp_op op, int32_t num_sms, flp_plan *out);

@@ -130,19 +130,22 @@ def test_planner_covers_all_tiles_and_balances(L, wid, sms):
     op = 1 if w.kind == "kl" else 0
     p = flp.plan(_shape(T=w.T, H=w.H, V=w.V, n=n), op, sms)
     bn = 128 if op == 1 else 256
+    cg = p["cta_group"]
+    assert cg in (1, 2) and p["block_m"] == 128 * cg
     assert p["block_n"] == bn
-    assert p["row_tiles"] == math.ceil(n / 128)
+    assert p["row_tiles"] == math.ceil(n / p["block_m"])
     assert p["vocab_tiles"] == math.ceil(w.V / bn)
     assert 1 <= p["splits"] <= 64
     S, tps = p["splits"], p["tiles_per_split"]
     assert tps * (S - 1) < p["vocab_tiles"] <= tps * S       # every split non-empty
     assert p["items"] == p["row_tiles"] * S
-    assert p["grid"] == min(p["items"], sms)
+    units = max(1, sms // cg)
+    assert p["grid"] == cg * min(p["items"], units)
     total = p["row_tiles"] * p["vocab_tiles"]
-    ideal = math.ceil(total / p["grid"])
+    ideal = math.ceil(total / (p["grid"] // cg))
     assert ideal <= p["max_tiles_per_cta"] <= ideal + tps
-    if total >= 50 * sms:
-        assert p["max_tiles_per_cta"] <= 1.04 * total / sms + 1
+    if total >= 50 * units:
+        assert p["max_tiles_per_cta"] <= 1.04 * total / units + 1
 
 
 def test_row_chunks_match_the_pages_example(L):
