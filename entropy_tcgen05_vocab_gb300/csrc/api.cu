@@ -127,12 +127,22 @@ Layout layout_for(const flp_shape *s, flp_op op) {
 
 // ------------------------------------------------------------------ planner
 struct PlanKey {
-  int64_t n, V, H;
+  int64_t n, V, H, band_bytes;
   int bn, units, bm;
   bool operator<(const PlanKey &o) const {
-    return std::tie(n, V, H, bn, units, bm) < std::tie(o.n, o.V, o.H, o.bn, o.units, o.bm);
+    return std::tie(n, V, H, band_bytes, bn, units, bm) <
+           std::tie(o.n, o.V, o.H, o.band_bytes, o.bn, o.units, o.bm);
   }
 };
+
+// L2 budget of one band's hidden rows (FLP_BAND_MB overrides it).
+int64_t band_budget() {
+  if (const char *env = std::getenv("FLP_BAND_MB")) {
+    const long long mb = std::atoll(env);
+    if (mb > 0) return static_cast<int64_t>(mb) << 20;
+  }
+  return kBandBytes;
+}
 
 // `units` = CTAs (or CTA pairs) resident at once; `grid` is in the same
 // units (the kernel launch multiplies by the CTA-group size).
@@ -145,7 +155,7 @@ struct Plan {
 std::mutex g_plan_mu;
 std::map<PlanKey, Plan> g_plans;
 
-Plan make_plan(int64_t n, int64_t V, int64_t H, int bn, int num_sms, int bm) {
+Plan make_plan(int64_t n, int64_t V, int64_t H, int bn, int num_sms, int bm, int64_t band_bytes) {
   Plan best{};
   Schedule s{};
   s.n = static_cast<int>(n);
@@ -154,7 +164,7 @@ Plan make_plan(int64_t n, int64_t V, int64_t H, int bn, int num_sms, int bm) {
   s.vocab_tiles = vocab_tiles(V, bn);
   s.k_blocks = static_cast<int>(cdiv(H, 64));
   const int64_t a_tile_bytes = bm * H * 2;
-  s.band = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(s.row_tiles, kBandBytes / a_tile_bytes)));
+  s.band = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(s.row_tiles, band_bytes / a_tile_bytes)));
   const int smax = max_splits(V, bn);
   std::vector<int64_t> loads;
   int64_t best_load = -1;
@@ -186,12 +196,13 @@ Plan make_plan(int64_t n, int64_t V, int64_t H, int bn, int num_sms, int bm) {
 }
 
 Plan plan_cached(int64_t n, int64_t V, int64_t H, int bn, int units, int bm) {
-  const PlanKey k{n, V, H, bn, units, bm};
+  const int64_t band_bytes = band_budget();
+  const PlanKey k{n, V, H, band_bytes, bn, units, bm};
   std::lock_guard<std::mutex> g(g_plan_mu);
   auto it = g_plans.find(k);
   if (it != g_plans.end()) return it->second;
   if (g_plans.size() > 256) g_plans.clear();
-  Plan p = make_plan(n, V, H, bn, units, bm);
+  Plan p = make_plan(n, V, H, bn, units, bm, band_bytes);
   g_plans.emplace(k, p);
   return p;
 }

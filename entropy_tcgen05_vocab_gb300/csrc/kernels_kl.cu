@@ -166,8 +166,8 @@ __global__ void kl_merge_kernel(int n, int splits, const float *__restrict__ pmt
   out_kl[i] = kl;
 }
 
-using KlLayout = PipeLayout<kKlBN, kKlStages, 2, kKlCG>;
-#define KL_KERNEL vocab_pipeline_kernel<kKlBN, kKlStages, 2, KlEpi, kKlCG>
+using KlLayout = PipeLayout<kKlBN, kKlStages, 2, kKlCG, kKlAcc>;
+#define KL_KERNEL vocab_pipeline_kernel<kKlBN, kKlStages, 2, KlEpi, kKlCG, kKlAcc>
 
 cudaError_t launch_kl(const KlArgs &a, cudaStream_t stream) {
   KlEpi::Params p;

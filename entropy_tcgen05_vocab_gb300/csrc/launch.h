@@ -17,11 +17,15 @@ namespace flp {
 constexpr int kFwdBN = 256;
 constexpr int kFwdCG = 2;
 constexpr int kFwdStages = 6;
-// Tile shape of the KL pipeline (two accumulators per tile): CTA pairs on
-// 256-row x 128-column tiles, 4 stages of 48 KB per CTA.
-constexpr int kKlBN = 128;
+// Tile shape of the KL pipeline (student and teacher accumulators per tile):
+// CTA pairs on 256-row x 256-column tiles, 3 stages of 64 KB per CTA, one
+// accumulator buffer (2 x 256 TMEM columns).  Against 128-column tiles with
+// double-buffered accumulators this needs a third less operand traffic per
+// flop, which pays for the epilogue no longer overlapping the MMAs.
+constexpr int kKlBN = 256;
 constexpr int kKlCG = 2;
-constexpr int kKlStages = 4;
+constexpr int kKlStages = 3;
+constexpr int kKlAcc = 1;
 
 
 struct FwdArgs {

@@ -54,16 +54,17 @@ constexpr int kPipeThreads = 64 + 32 * kEpiWarps;
 // NOPS independent GEMMs share one tile (the KL pipeline runs the student and
 // the teacher head side by side, NOPS = 2).  Per-CTA stage layout:
 // [A_0 .. A_{NOPS-1} | B_0 .. B_{NOPS-1}] with B_i holding BN / CG rows; TMEM:
-// two accumulator buffers of NOPS x BN columns (GEMM op at column offset
-// op * BN inside a buffer).
-template <int BN, int STAGES, int NOPS = 1, int CG = 1>
+// NACC accumulator buffers (2: the epilogue of one tile overlaps the MMAs of
+// the next) of NOPS x BN columns (GEMM op at column offset op * BN).
+template <int BN, int STAGES, int NOPS = 1, int CG = 1, int NACC = 2>
 struct PipeLayout {
   static constexpr int kABytes = kBM * kBK * 2;
   static constexpr int kBRows = BN / CG;
   static constexpr int kBBytes = kBRows * kBK * 2;
   static constexpr int kStageBytes = NOPS * (kABytes + kBBytes);
   static constexpr int kAccCols = NOPS * BN;
-  static constexpr int kTmemCols = 2 * kAccCols;
+  static constexpr int kTmemCols = NACC * kAccCols;
+  static_assert(NACC == 1 || NACC == 2, "one or two accumulator buffers");
   static constexpr int kBarrierBytes = 8 * (2 * STAGES + 5) + 16;
   // + 1024 so the stage ring can be aligned to a swizzle atom.
   static constexpr int kSmemBytes = STAGES * kStageBytes + kBarrierBytes + 1024;
@@ -96,7 +97,7 @@ __device__ __forceinline__ void record_timeout(uint32_t *status, volatile int *a
 //                                                          (GEMM op at + op * BN)
 //   __device__ void end(int split, int row);
 // CG = 2 kernels must be launched with a cluster dimension of 2.
-template <int BN, int STAGES, int NOPS, class Epi, int CG = 1>
+template <int BN, int STAGES, int NOPS, class Epi, int CG = 1, int NACC = 2>
 __global__ void __launch_bounds__(kPipeThreads, 1)
     vocab_pipeline_kernel(const __grid_constant__ CUtensorMap tmA0,
                           const __grid_constant__ CUtensorMap tmB0,
@@ -104,7 +105,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                           const __grid_constant__ CUtensorMap tmB1, const Schedule sch,
                           const uint32_t idesc, const typename Epi::Params ep,
                           uint32_t *status) {
-  using L = PipeLayout<BN, STAGES, NOPS, CG>;
+  using L = PipeLayout<BN, STAGES, NOPS, CG, NACC>;
   static_assert(NOPS == 1 || NOPS == 2, "one or two GEMMs per tile");
   constexpr bool kPair = CG == 2;
   extern __shared__ uint8_t smem_raw[];
@@ -280,7 +281,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
               mma_commit(&tfull[acc]);
           }
           __syncwarp();
-          acc ^= 1;
+          if (NACC == 2) acc ^= 1;
           if (acc == 0) acc_phase ^= 1u;
         }
       }
@@ -324,7 +325,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
           else
             mbar_arrive(&tempty[acc]);
         }
-        acc ^= 1;
+        if (NACC == 2) acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }
       if (!ok) break;

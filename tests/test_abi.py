@@ -129,7 +129,7 @@ def test_planner_covers_all_tiles_and_balances(L, wid, sms):
     n = {"all": w.T, "packed": 29492, "bernoulli": 9843}[w.rows]
     op = 1 if w.kind == "kl" else 0
     p = flp.plan(_shape(T=w.T, H=w.H, V=w.V, n=n), op, sms)
-    bn = 128 if op == 1 else 256
+    bn = 256
     cg = p["cta_group"]
     assert cg in (1, 2) and p["block_m"] == 128 * cg
     assert p["block_n"] == bn
