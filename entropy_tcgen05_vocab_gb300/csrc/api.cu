@@ -633,7 +633,7 @@ flp_status flp_backward(const flp_shape *s, const void *h, const void *W, const 
     da.M = rc;
     da.N = static_cast<int>(s->H);
     da.K = static_cast<int>(s->V);
-    da.grid = std::min(gemm_tiles(da.M, da.N), dev.sms);
+    da.grid = gemm_cta_group() * std::min(gemm_tiles(da.M, da.N), gemm_units(dev.sms));
     da.bf16 = ga.bf16;
     da.status = status;
     da.r0 = static_cast<int>(r0);
@@ -649,7 +649,7 @@ flp_status flp_backward(const flp_shape *s, const void *h, const void *W, const 
     wa.M = static_cast<int>(s->V);
     wa.N = static_cast<int>(s->H);
     wa.K = rc;
-    wa.grid = std::min(gemm_tiles(wa.M, wa.N), dev.sms);
+    wa.grid = gemm_cta_group() * std::min(gemm_tiles(wa.M, wa.N), gemm_units(dev.sms));
     wa.bf16 = ga.bf16;
     wa.status = status;
     wa.dW = dW;

@@ -1,6 +1,6 @@
 // gemm_pipeline.cuh -- persistent tcgen05 GEMM D[M,N] = A[M,K] B[N,K]^T with
-// 128 x 256 output tiles and an epilogue policy, for the two GEMMs of the
-// backward (dh = G W and dW = G^T h).
+// (128 x CG) x 256 output tiles and an epilogue policy, for the two GEMMs of
+// the backward (dh = G W and dW = G^T h).
 //
 // Operands may be K-major (K contiguous) or MN-major (M or N contiguous):
 //   K-major  : one TMA box {64 (K), rows} per stage, 128-byte swizzle rows
@@ -10,8 +10,12 @@
 //              elements; descriptor lbo = 8192 (next 64-element M/N block =
 //              next box), sbo = 1024 (next 8 K-rows), K step of 16 = +2048 B.
 // Roles are those of the vocabulary pipeline: warp 0 TMA producer, warp 1
-// TMEM allocation + MMA issue, warps 2-5 epilogue; 4-stage ring of
-// A 16 KB + B 32 KB; double-buffered 256-column TMEM accumulators.
+// TMEM allocation + MMA issue, warps 2-5 epilogue; double-buffered
+// 256-column TMEM accumulators.  With CG = 2 (cluster of 2) the pair computes
+// a 256 x 256 tile: each CTA loads its 128 rows of A and 128 of the 256
+// columns of B, the leader issues tcgen05.mma.cta_group::2, and each CTA's
+// TMEM holds its 128 output rows (the same protocol as the vocabulary
+// pipeline).
 #pragma once
 
 #include <cstdint>
@@ -22,25 +26,30 @@
 namespace flp {
 
 constexpr int kGemmBN = 256;
-constexpr int kGemmStages = 4;
 
 struct GemmShape {
   int M, N, K;
   int m_tiles, n_tiles, tiles, k_blocks;
 };
 
-using GemmLayout = PipeLayout<kGemmBN, kGemmStages, 1>;
+template <int CG>
+struct GemmCfg {
+  static constexpr int kStages = CG == 2 ? 6 : 4;
+  using L = PipeLayout<kGemmBN, kStages, 1, CG, 2>;
+};
 
 // Epi must provide: struct Params; Epi(const Params&);
-//   void tile(uint32_t taddr, int mt, int nt, int lg, int lane)
-template <bool A_MN, bool B_MN, class Epi>
+//   void tile(uint32_t taddr, int row0, int nt, int lg, int lane)
+// where row0 is the first output row held by this CTA's TMEM for the tile.
+template <bool A_MN, bool B_MN, class Epi, int CG = 1>
 __global__ void __launch_bounds__(kPipeThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const GemmShape g, const uint32_t idesc, const typename Epi::Params ep,
                 uint32_t *status) {
-  using L = GemmLayout;
-  constexpr int STAGES = kGemmStages;
+  using L = typename GemmCfg<CG>::L;
+  constexpr int STAGES = GemmCfg<CG>::kStages;
   constexpr int BN = kGemmBN;
+  constexpr bool kPair = CG == 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -54,6 +63,10 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int unit = blockIdx.x / CG;
+  const int num_units = gridDim.x / CG;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -62,7 +75,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], kEpiWarps);
+      mbar_init(&tempty[a], kEpiWarps * CG);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -73,11 +86,14 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     prefetch_tmap(&tmB);
   }
   if (warp == 1) {
-    tmem_alloc<1>(tmem_slot, L::kTmemCols);
-    tmem_relinquish<1>();
+    tmem_alloc<CG>(tmem_slot, L::kTmemCols);
+    tmem_relinquish<CG>();
   }
   tc_fence_before();
-  __syncthreads();
+  if (kPair)
+    cluster_sync();
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -87,8 +103,11 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     uint32_t phase = 0;
     uint32_t armed = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < g.tiles; t += gridDim.x) {
+    const uint32_t full_dst = kPair ? mapa_shared(smem_u32(full), 0) : smem_u32(full);
+    for (int t = unit; ok && t < g.tiles; t += num_units) {
       const int mt = t / g.n_tiles, nt = t - (t / g.n_tiles) * g.n_tiles;
+      const int arow = mt * (kBM * CG) + static_cast<int>(rank) * kBM;   // M offset
+      const int bcol = nt * BN + static_cast<int>(rank) * L::kBRows;     // N offset
       for (int kb = 0; kb < g.k_blocks; ++kb) {
         if (lane == 0) ok = mbar_wait(&empty[stage], phase ^ 1u, abort_flag);
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -96,19 +115,26 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
         if (lane == 0) {
           uint8_t *sa = smem + stage * L::kStageBytes;
           uint8_t *sb = sa + L::kABytes;
-          mbar_arrive_expect_tx(&full[stage], L::kStageBytes);
+          if (leader) mbar_arrive_expect_tx(&full[stage], CG * L::kStageBytes);
+          const uint32_t fb = full_dst + stage * 8;
+          auto load = [&](void *dst, const CUtensorMap *m, int c0, int c1) {
+            if (kPair)
+              tma_load_2d_pair(dst, m, fb, c0, c1);
+            else
+              tma_load_2d(dst, m, &full[stage], c0, c1);
+          };
           if (A_MN) {
-            tma_load_2d(sa, &tmA, &full[stage], mt * kBM, kb * kBK);
-            tma_load_2d(sa + 8192, &tmA, &full[stage], mt * kBM + 64, kb * kBK);
+            load(sa, &tmA, arow, kb * kBK);
+            load(sa + 8192, &tmA, arow + 64, kb * kBK);
           } else {
-            tma_load_2d(sa, &tmA, &full[stage], kb * kBK, mt * kBM);
+            load(sa, &tmA, kb * kBK, arow);
           }
           if (B_MN) {
 #pragma unroll
-            for (int i = 0; i < BN / 64; ++i)
-              tma_load_2d(sb + i * 8192, &tmB, &full[stage], nt * BN + i * 64, kb * kBK);
+            for (int i = 0; i < L::kBRows / 64; ++i)
+              load(sb + i * 8192, &tmB, bcol + i * 64, kb * kBK);
           } else {
-            tma_load_2d(sb, &tmB, &full[stage], kb * kBK, nt * BN);
+            load(sb, &tmB, kb * kBK, bcol);
           }
         }
         armed |= 1u << stage;
@@ -119,91 +145,119 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
       }
     }
     if (!ok && lane == 0) {
-      record_timeout(status, abort_flag);
-      for (int s = 0; s < STAGES; ++s) {
-        if (!(armed & (1u << s))) continue;
-        const uint32_t par = (s < stage) ? phase : (phase ^ 1u);
-        int never = 0;
-        mbar_wait(&full[s], par, &never);
+      record_timeout<CG>(status, abort_flag);
+      if (leader) {
+        for (int s = 0; s < STAGES; ++s) {
+          if (!(armed & (1u << s))) continue;
+          const uint32_t par = (s < stage) ? phase : (phase ^ 1u);
+          int never = 0;
+          mbar_wait(&full[s], par, &never);
+        }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    int stage = 0;
-    uint32_t phase = 0;
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    bool ok = true;
-    for (int t = blockIdx.x; ok && t < g.tiles; t += gridDim.x) {
-      if (lane == 0) ok = mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-      for (int kb = 0; kb < g.k_blocks; ++kb) {
-        if (lane == 0) ok = mbar_wait(&full[stage], phase, abort_flag);
+    if (leader) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int t = unit; ok && t < g.tiles; t += num_units) {
+        if (lane == 0) ok = mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         tc_fence_after();
-        if (lane == 0) {
-          const uint32_t a0 = smem_u32(smem + stage * L::kStageBytes);
-          const uint32_t b0 = a0 + L::kABytes;
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < g.k_blocks; ++kb) {
+          if (lane == 0) ok = mbar_wait(&full[stage], phase, abort_flag);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t a0 = smem_u32(smem + stage * L::kStageBytes);
+            const uint32_t b0 = a0 + L::kABytes;
 #pragma unroll
-          for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
-            const uint64_t ad = A_MN ? sdesc_sw128(a0 + kk * 2048, 8192, 1024)
-                                     : sdesc_sw128(a0 + kk * kUmmaK * 2, 16, 1024);
-            const uint64_t bd = B_MN ? sdesc_sw128(b0 + kk * 2048, 8192, 1024)
-                                     : sdesc_sw128(b0 + kk * kUmmaK * 2, 16, 1024);
-            mma_f16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
+              const uint64_t ad = A_MN ? sdesc_sw128(a0 + kk * 2048, 8192, 1024)
+                                       : sdesc_sw128(a0 + kk * kUmmaK * 2, 16, 1024);
+              const uint64_t bd = B_MN ? sdesc_sw128(b0 + kk * 2048, 8192, 1024)
+                                       : sdesc_sw128(b0 + kk * kUmmaK * 2, 16, 1024);
+              if (kPair)
+                mma_f16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+              else
+                mma_f16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            }
+            if (kPair)
+              mma_commit_pair(&empty[stage], 0x3);
+            else
+              mma_commit(&empty[stage]);
           }
-          mma_commit(&empty[stage]);
+          __syncwarp();
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        if (lane == 0) {
+          if (kPair)
+            mma_commit_pair(&tfull[acc], 0x3);
+          else
+            mma_commit(&tfull[acc]);
         }
         __syncwarp();
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
-        }
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
       }
-      if (!ok) break;
-      if (lane == 0) mma_commit(&tfull[acc]);
-      __syncwarp();
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
-    }
-    if (!ok && lane == 0) {
-      record_timeout(status, abort_flag);
-      mma_commit(drain);
-      int never = 0;
-      mbar_wait(drain, 0, &never);
+      if (!ok && lane == 0) {
+        record_timeout<CG>(status, abort_flag);
+        if (kPair)
+          mma_commit_pair_local(drain);
+        else
+          mma_commit(drain);
+        int never = 0;
+        mbar_wait(drain, 0, &never);
+      }
     }
   } else {
     // ------------------------------------------------------------ epilogue
     const int lg = warp & 3;
     const uint32_t lane_off = static_cast<uint32_t>(lg * 32) << 16;
+    const uint32_t tempty_dst = kPair ? mapa_shared(smem_u32(tempty), 0) : smem_u32(tempty);
     Epi epi(ep);
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < g.tiles; t += gridDim.x) {
+    for (int t = unit; t < g.tiles; t += num_units) {
       const int mt = t / g.n_tiles, nt = t - (t / g.n_tiles) * g.n_tiles;
       if (lane == 0) ok = mbar_wait(&tfull[acc], acc_phase, abort_flag);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      epi.tile(tmem_base + lane_off + static_cast<uint32_t>(acc * BN), mt, nt, lg, lane);
+      epi.tile(tmem_base + lane_off + static_cast<uint32_t>(acc * BN),
+               mt * (kBM * CG) + static_cast<int>(rank) * kBM, nt, lg, lane);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (lane == 0) {
+        if (kPair)
+          mbar_arrive_cluster(tempty_dst + acc * 8);
+        else
+          mbar_arrive(&tempty[acc]);
+      }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
-    if (!ok && lane == 0) record_timeout(status, abort_flag);
+    if (!ok && lane == 0) record_timeout<CG>(status, abort_flag);
   }
 
   tc_fence_before();
-  __syncthreads();
+  if (kPair)
+    cluster_sync();
+  else
+    __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc<1>(tmem_base, L::kTmemCols);
+  if (warp == 1) tmem_dealloc<CG>(tmem_base, L::kTmemCols);
 }
 
 }  // namespace flp

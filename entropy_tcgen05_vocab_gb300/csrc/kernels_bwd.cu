@@ -147,8 +147,8 @@ struct DhEpi {
   const Params p;
   __device__ __forceinline__ explicit DhEpi(const Params &pp) : p(pp) {}
 
-  __device__ __forceinline__ void tile(uint32_t taddr, int mt, int nt, int lg, int lane) {
-    const int row = mt * kBM + lg * 32 + lane;
+  __device__ __forceinline__ void tile(uint32_t taddr, int row0, int nt, int lg, int lane) {
+    const int row = row0 + lg * 32 + lane;
     bool valid = row < p.R;
     int64_t orig = 0;
     if (valid) {
@@ -185,8 +185,8 @@ struct DwEpi {
   const Params p;
   __device__ __forceinline__ explicit DwEpi(const Params &pp) : p(pp) {}
 
-  __device__ __forceinline__ void tile(uint32_t taddr, int mt, int nt, int lg, int lane) {
-    const int v = mt * kBM + lg * 32 + lane;
+  __device__ __forceinline__ void tile(uint32_t taddr, int row0, int nt, int lg, int lane) {
+    const int v = row0 + lg * 32 + lane;
     const bool valid = v < p.V;
     float *drow = p.dW + static_cast<int64_t>(valid ? v : 0) * p.ld;
 #pragma unroll 1
@@ -254,12 +254,17 @@ int grad_units(int num_sms) {
   return cached[dev];
 }
 
+constexpr int kGemmCG = 2;
+using GemmL = GemmCfg<kGemmCG>::L;
+#define DH_KERNEL gemm_kernel<false, true, DhEpi, kGemmCG>
+#define DW_KERNEL gemm_kernel<true, true, DwEpi, kGemmCG>
+
 static GemmShape gemm_shape(int M, int N, int K) {
   GemmShape g;
   g.M = M;
   g.N = N;
   g.K = K;
-  g.m_tiles = (M + kBM - 1) / kBM;
+  g.m_tiles = (M + kBM * kGemmCG - 1) / (kBM * kGemmCG);
   g.n_tiles = (N + kGemmBN - 1) / kGemmBN;
   g.tiles = g.m_tiles * g.n_tiles;
   g.k_blocks = (K + kBK - 1) / kBK;
@@ -267,12 +272,18 @@ static GemmShape gemm_shape(int M, int N, int K) {
 }
 
 int gemm_tiles(int M, int N) { return gemm_shape(M, N, 1).tiles; }
+int gemm_cta_group() { return kGemmCG; }
+
+int gemm_units(int num_sms) {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return resident_units(DH_KERNEL, GemmL::kSmemBytes, kGemmCG, num_sms);
+  if (!cached[dev]) cached[dev] = resident_units(DH_KERNEL, GemmL::kSmemBytes, kGemmCG, num_sms);
+  return cached[dev];
+}
 
 cudaError_t launch_dh_gemm(const GemmArgs &a, cudaStream_t stream) {
-  auto kern = gemm_kernel<false, true, DhEpi>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       GemmLayout::kSmemBytes);
-  if (e != cudaSuccess) return e;
   DhEpi::Params p;
   p.R = a.M;
   p.H = a.N;
@@ -282,27 +293,21 @@ cudaError_t launch_dh_gemm(const GemmArgs &a, cudaStream_t stream) {
   p.dh = static_cast<uint16_t *>(a.dh);
   p.ld = a.ld_dh;
   p.bf16 = a.bf16;
-  const uint32_t idesc = idesc_f16(a.bf16, kBM, kGemmBN, false, true);
-  kern<<<a.grid, kPipeThreads, GemmLayout::kSmemBytes, stream>>>(
-      a.tmA, a.tmB, gemm_shape(a.M, a.N, a.K), idesc, p, a.status);
-  return cudaGetLastError();
+  const uint32_t idesc = idesc_f16(a.bf16, kBM * kGemmCG, kGemmBN, false, true);
+  return launch_persistent(DH_KERNEL, a.grid, GemmL::kSmemBytes, kGemmCG, stream, a.tmA, a.tmB,
+                           gemm_shape(a.M, a.N, a.K), idesc, p, a.status);
 }
 
 cudaError_t launch_dw_gemm(const GemmArgs &a, cudaStream_t stream) {
-  auto kern = gemm_kernel<true, true, DwEpi>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       GemmLayout::kSmemBytes);
-  if (e != cudaSuccess) return e;
   DwEpi::Params p;
   p.V = a.M;
   p.H = a.N;
   p.dW = a.dW;
   p.ld = a.ld_dw;
   p.accumulate = a.accumulate;
-  const uint32_t idesc = idesc_f16(a.bf16, kBM, kGemmBN, true, true);
-  kern<<<a.grid, kPipeThreads, GemmLayout::kSmemBytes, stream>>>(
-      a.tmA, a.tmB, gemm_shape(a.M, a.N, a.K), idesc, p, a.status);
-  return cudaGetLastError();
+  const uint32_t idesc = idesc_f16(a.bf16, kBM * kGemmCG, kGemmBN, true, true);
+  return launch_persistent(DW_KERNEL, a.grid, GemmL::kSmemBytes, kGemmCG, stream, a.tmA, a.tmB,
+                           gemm_shape(a.M, a.N, a.K), idesc, p, a.status);
 }
 
 }  // namespace flp

@@ -102,6 +102,8 @@ cudaError_t launch_grad(const GradArgs &a, cudaStream_t stream);
 cudaError_t launch_dh_gemm(const GemmArgs &a, cudaStream_t stream);
 cudaError_t launch_dw_gemm(const GemmArgs &a, cudaStream_t stream);
 int gemm_tiles(int M, int N);
+int gemm_cta_group();
+int gemm_units(int num_sms);
 int fwd_smem_bytes();
 // CTAs or CTA pairs of each pipeline that can be resident at once.
 int fwd_units(int num_sms);
