@@ -223,10 +223,15 @@ def launches_per_call(d):
     w = d["workload"]
     gather = 1 if d["row_idx"] is not None else 0
     if w.kind == "fwd":
-        return gather + 2
+        return gather + 1          # (gather) + the fused scoring kernel
     if w.kind == "kl":
-        return 2 * gather + 2
-    return None
+        return 2 * gather + 1
+    # backward with the statistics supplied: per row chunk, the gradient pass
+    # and the dh and dW GEMMs
+    import entropy_tcgen05_vocab_gb300 as flp
+    shape = flp.make_shape(w.T, w.H, w.V, d["n"], d["h"].dtype)
+    chunk = flp.plan(shape, flp.OP_BACKWARD, 1)["chunk_rows"]
+    return gather + 3 * len(flp.row_chunks(d["n"], chunk))
 
 
 def time_device(flp, d, steps, warmup, world, device, sampler=None):

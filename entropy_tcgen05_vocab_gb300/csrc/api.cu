@@ -87,7 +87,8 @@ int64_t grad_chunk_rows(const flp_shape *s) {
 }
 
 struct Layout {
-  size_t status = 0, zt = 0, pm = 0, ps = 0, pb = 0, pc = 0, pm2 = 0, ps2 = 0;
+  size_t status = 0, cnt = 0, cnt_bytes = 0, zt = 0, pm = 0, ps = 0, pb = 0, pc = 0, pm2 = 0,
+         ps2 = 0;
   size_t hs = 0, hs2 = 0, lse = 0, ez = 0, g = 0, total = 0;
   int64_t grad_rows = 0;
 };
@@ -102,6 +103,10 @@ Layout layout_for(const flp_shape *s, flp_op op) {
     return o;
   };
   L.status = take(kStatusBytes);
+  // one arrival counter per 32-row group (the fused merge), cleared per call;
+  // groups are counted over whole 256-row tiles
+  L.cnt_bytes = static_cast<size_t>(cdiv(s->n_rows, 256) * 8 + 8) * 4;
+  L.cnt = take(L.cnt_bytes);
   const int bn = (op == FLP_OP_KL) ? kKlBN : kFwdBN;
   const size_t sm = static_cast<size_t>(max_splits(s->V, bn));
   L.pm = take(sm * n * 4);
@@ -380,6 +385,7 @@ flp_status flp_plan_scoring(const flp_shape *shape, flp_op op, int32_t num_sms, 
   out->items = p.sch.items;
   out->grid = p.grid * cg;
   out->max_tiles_per_cta = p.max_load;
+  if (op == FLP_OP_BACKWARD) out->chunk_rows = grad_chunk_rows(shape);
   return FLP_OK;
 }
 
@@ -437,13 +443,15 @@ flp_status flp_logprob_entropy(const flp_shape *s, const void *h, const void *W,
   a.ps = at<float>(ws, L.ps);
   a.pb = at<float>(ws, L.pb);
   a.zt = at<float>(ws, L.zt);
+  a.counters = at<uint32_t>(ws, L.cnt);
   a.out_logp = out_logp;
   a.out_ent = out_ent;
   a.out_lse = out_lse;
   a.out_ez = out_ez;
   a.status = at<uint32_t>(ws, L.status);
 
-  cudaError_t e = cudaMemsetAsync(a.status, 0, kStatusBytes, cs);
+  // status words and row-group counters are adjacent: one clear
+  cudaError_t e = cudaMemsetAsync(a.status, 0, L.cnt + L.cnt_bytes - L.status, cs);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(status)");
   if (row_idx) {
     e = launch_gather(h, s->ld_h, row_idx, s->n_rows, s->T, s->H, at<void>(ws, L.hs), dev.sms, cs);
@@ -452,7 +460,6 @@ flp_status flp_logprob_entropy(const flp_shape *s, const void *h, const void *W,
   if ((e = ev.start(cs)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
   if ((e = launch_fwd_scoring(a, cs)) != cudaSuccess) return cuda_fail(e, "scoring launch");
   if ((e = ev.stop(cs)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-  if ((e = launch_fwd_merge(a, cs)) != cudaSuccess) return cuda_fail(e, "merge launch");
   return FLP_OK;
 }
 
@@ -500,10 +507,11 @@ flp_status flp_kl(const flp_shape *s, const void *h_s, const void *W_s, const vo
   a.pct = at<float>(ws, L.pb);
   a.pms = at<float>(ws, L.pm2);
   a.pss = at<float>(ws, L.ps2);
+  a.counters = at<uint32_t>(ws, L.cnt);
   a.out_kl = out_kl;
   a.status = at<uint32_t>(ws, L.status);
 
-  cudaError_t e = cudaMemsetAsync(a.status, 0, kStatusBytes, cs);
+  cudaError_t e = cudaMemsetAsync(a.status, 0, L.cnt + L.cnt_bytes - L.status, cs);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(status)");
   if (row_idx) {
     e = launch_gather(h_s, s->ld_h, row_idx, s->n_rows, s->T, s->H, at<void>(ws, L.hs), dev.sms, cs);
@@ -514,7 +522,6 @@ flp_status flp_kl(const flp_shape *s, const void *h_s, const void *W_s, const vo
   if ((e = ev.start(cs)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
   if ((e = launch_kl(a, cs)) != cudaSuccess) return cuda_fail(e, "KL launch");
   if ((e = ev.stop(cs)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-  if ((e = launch_kl_merge(a, cs)) != cudaSuccess) return cuda_fail(e, "KL merge launch");
   return FLP_OK;
 }
 
@@ -545,7 +552,7 @@ flp_status flp_backward(const flp_shape *s, const void *h, const void *W, const 
   const Layout L = layout_for(s, FLP_OP_BACKWARD);
   uint32_t *status = at<uint32_t>(ws, L.status);
   const size_t esz = 2;
-  cudaError_t e = cudaMemsetAsync(status, 0, kStatusBytes, cs);
+  cudaError_t e = cudaMemsetAsync(status, 0, L.cnt + L.cnt_bytes - L.status, cs);
   // rows that are not scored get a zero gradient
   if (e == cudaSuccess && s->T > 0)
     e = cudaMemset2DAsync(dh, s->ld_h * esz, 0, s->H * esz, s->T, cs);
@@ -585,11 +592,11 @@ flp_status flp_backward(const flp_shape *s, const void *h, const void *W, const 
     a.ps = at<float>(ws, L.ps);
     a.pb = at<float>(ws, L.pb);
     a.zt = at<float>(ws, L.zt);
+    a.counters = at<uint32_t>(ws, L.cnt);
     a.out_lse = at<float>(ws, L.lse);
     a.out_ez = at<float>(ws, L.ez);
     a.status = status;
     if ((e = launch_fwd_scoring(a, cs)) != cudaSuccess) return cuda_fail(e, "stats launch");
-    if ((e = launch_fwd_merge(a, cs)) != cudaSuccess) return cuda_fail(e, "stats merge launch");
     lse = a.out_lse;
     ez = a.out_ez;
   }

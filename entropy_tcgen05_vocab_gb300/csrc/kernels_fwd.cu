@@ -1,6 +1,7 @@
-// kernels_fwd.cu -- forward scoring: response-row gather, the fused
-// logits-tile -> online log-sum-exp/entropy pipeline, and the merge of the
-// per-split partial states into log-prob and entropy.
+// kernels_fwd.cu -- forward scoring: response-row gather and the fused
+// logits-tile -> online log-sum-exp/entropy pipeline, whose epilogue also
+// merges the per-split partial states of a row into log-prob and entropy
+// (the last warp to finish a 32-row group merges it).
 //
 // Arithmetic (miles PR #2764 summary, "Implementation breakdown" item 2:
 // upcast first, temperature in FP32 after the upcast; entropy from the same
@@ -55,6 +56,11 @@ struct LseEpi {
     float sl;                // log2(e) / tau
     float *pm, *ps, *pb;     // [splits][n] partial m, S, B
     float *zt;               // [n] raw FP32 logit of the target
+    uint32_t *counters;      // [ceil(n/32)] items finished per 32-row group
+    int splits;
+    float inv_tau;
+    float *out_logp, *out_ent, *out_lse, *out_ez;  // [n], any may be null
+    uint32_t *status;
   };
   const Params p;
   float m, s0, s1, b0, b1, zt;
@@ -151,61 +157,57 @@ struct LseEpi {
   }
 
   __device__ __forceinline__ void end(int split, int row) {
-    if (row >= p.n) return;
-    const size_t o = static_cast<size_t>(split) * p.n + row;
-    p.pm[o] = m;
-    p.ps[o] = s0 + s1;
-    p.pb[o] = b0 + b1;
-    if (found) p.zt[row] = zt;
+    if (row < p.n) {
+      const size_t o = static_cast<size_t>(split) * p.n + row;
+      p.pm[o] = m;
+      p.ps[o] = s0 + s1;
+      p.pb[o] = b0 + b1;
+      if (found) p.zt[row] = zt;
+    }
+    // The last warp to finish these 32 rows merges them.
+    if (last_arrival(p.counters + (row >> 5), static_cast<uint32_t>(p.splits)) && row < p.n)
+      merge_row(row);
+  }
+
+  // Merge the split partials (m_i, S_i, B_i) of one row:
+  //   M = max m_i,  S = sum S_i 2^(m_i - M),  B = sum 2^(m_i - M) (B_i + (m_i - M) S_i),
+  // then logp = z_tgt / tau - LSE and entropy = ln 2 (log2 S - B / S).
+  __device__ __forceinline__ void merge_row(int i) const {
+    const int n = p.n;
+    float M = -FLT_MAX;
+    for (int s = 0; s < p.splits; ++s) M = fmaxf(M, __ldcg(p.pm + static_cast<size_t>(s) * n + i));
+    float S = 0.f, B = 0.f;
+    for (int s = 0; s < p.splits; ++s) {
+      const size_t o = static_cast<size_t>(s) * n + i;
+      const float d = __ldcg(p.pm + o) - M;
+      const float a = exp2f(d);
+      const float si = __ldcg(p.ps + o);
+      S = fmaf(si, a, S);
+      B = fmaf(a, fmaf(d, si, __ldcg(p.pb + o)), B);
+    }
+    const float l2s = log2f(S);
+    float lse = kLn2 * (M + l2s);
+    float ent = kLn2 * (l2s - B / S);
+    float logp;
+    const int64_t r = p.row_idx ? p.row_idx[i] : i;
+    if (r < 0 || r >= p.T) {
+      atomicAdd(p.status + kStatBadRow, 1u);
+      lse = ent = logp = __int_as_float(0x7fc00000);
+    } else {
+      const int64_t t = p.targets[r];
+      if (t < 0 || t >= p.V) {
+        atomicAdd(p.status + kStatBadTarget, 1u);
+        logp = __int_as_float(0x7fc00000);
+      } else {
+        logp = __ldcg(p.zt + i) * p.inv_tau - lse;
+      }
+    }
+    if (p.out_logp) p.out_logp[i] = logp;
+    if (p.out_ent) p.out_ent[i] = ent;
+    if (p.out_lse) p.out_lse[i] = lse;
+    if (p.out_ez) p.out_ez[i] = lse - ent;
   }
 };
-
-// ---------------------------------------------------------------- merge
-// One thread per scored row: merge the split partials (m_i, S_i, B_i) with
-// M = max m_i, S = sum S_i 2^(m_i-M), B = sum 2^(m_i-M) (B_i + (m_i-M) S_i),
-// then logp = z_tgt/tau - LSE and entropy = ln2 (log2 S - B/S).
-__global__ void merge_kernel(int n, int splits, const float *__restrict__ pm,
-                             const float *__restrict__ ps, const float *__restrict__ pb,
-                             const float *__restrict__ zt, const int64_t *__restrict__ targets,
-                             const int64_t *__restrict__ row_idx, int64_t T, int V,
-                             float inv_tau, float *__restrict__ out_logp,
-                             float *__restrict__ out_ent, float *__restrict__ out_lse,
-                             float *__restrict__ out_ez, uint32_t *status) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n) return;
-  float M = -FLT_MAX;
-  for (int s = 0; s < splits; ++s) M = fmaxf(M, pm[static_cast<size_t>(s) * n + i]);
-  float S = 0.f, B = 0.f;
-  for (int s = 0; s < splits; ++s) {
-    const size_t o = static_cast<size_t>(s) * n + i;
-    const float d = pm[o] - M;
-    const float a = exp2f(d);
-    const float si = ps[o];
-    S = fmaf(si, a, S);
-    B = fmaf(a, fmaf(d, si, pb[o]), B);
-  }
-  const float l2s = log2f(S);
-  float lse = kLn2 * (M + l2s);
-  float ent = kLn2 * (l2s - B / S);
-  float logp;
-  const int64_t r = row_idx ? row_idx[i] : i;
-  if (r < 0 || r >= T) {
-    atomicAdd(status + kStatBadRow, 1u);
-    lse = ent = logp = __int_as_float(0x7fc00000);
-  } else {
-    const int64_t t = targets[r];
-    if (t < 0 || t >= V) {
-      atomicAdd(status + kStatBadTarget, 1u);
-      logp = __int_as_float(0x7fc00000);
-    } else {
-      logp = zt[i] * inv_tau - lse;
-    }
-  }
-  if (out_logp) out_logp[i] = logp;
-  if (out_ent) out_ent[i] = ent;
-  if (out_lse) out_lse[i] = lse;
-  if (out_ez) out_ez[i] = lse - ent;
-}
 
 // ---------------------------------------------------------------- launchers
 cudaError_t launch_gather(const void *h, int64_t ld_h, const int64_t *row_idx, int64_t n,
@@ -235,6 +237,14 @@ cudaError_t launch_fwd_scoring(const FwdArgs &a, cudaStream_t stream) {
   p.ps = a.ps;
   p.pb = a.pb;
   p.zt = a.zt;
+  p.counters = a.counters;
+  p.splits = a.sch.splits;
+  p.inv_tau = a.inv_tau;
+  p.out_logp = a.out_logp;
+  p.out_ent = a.out_ent;
+  p.out_lse = a.out_lse;
+  p.out_ez = a.out_ez;
+  p.status = a.status;
   const uint32_t idesc = idesc_f16(a.bf16, kBM * kFwdCG, kFwdBN, false, false);
   return launch_persistent(FWD_KERNEL, a.grid, FwdLayout::kSmemBytes, kFwdCG, stream, a.tmA,
                            a.tmB, a.tmA, a.tmB, a.sch, idesc, p, a.status);
@@ -247,14 +257,6 @@ int fwd_units(int num_sms) {
   if (dev < 0 || dev >= 64) return resident_units(FWD_KERNEL, FwdLayout::kSmemBytes, kFwdCG, num_sms);
   if (!cached[dev]) cached[dev] = resident_units(FWD_KERNEL, FwdLayout::kSmemBytes, kFwdCG, num_sms);
   return cached[dev];
-}
-
-cudaError_t launch_fwd_merge(const FwdArgs &a, cudaStream_t stream) {
-  const int n = a.sch.n;
-  merge_kernel<<<(n + 255) / 256, 256, 0, stream>>>(
-      n, a.sch.splits, a.pm, a.ps, a.pb, a.zt, a.targets, a.row_idx, a.T, a.sch.V, a.inv_tau,
-      a.out_logp, a.out_ent, a.out_lse, a.out_ez, a.status);
-  return cudaGetLastError();
 }
 
 int fwd_smem_bytes() { return FwdLayout::kSmemBytes; }

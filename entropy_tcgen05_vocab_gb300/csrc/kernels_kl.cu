@@ -10,7 +10,8 @@
 //   teacher  m_t = max y_t,  S_t = sum 2^(y_t - m_t),
 //            C_t = sum 2^(y_t - m_t) (z_t - z_s)      (natural units)
 //   student  m_s = max y_s,  S_s = sum 2^(y_s - m_s)
-// rescaling S and C by 2^(m - m') when a running max grows.  Then
+// rescaling S and C by 2^(m - m') when a running max grows.  The last warp
+// to finish a 32-row group merges the group's split partials and finishes
 //   KL = sum_v p_t (log p_t - log p_s) = C_t / S_t - LSE_t + LSE_s,
 //   LSE = ln 2 (m + log2 S).
 #include <cuda.h>
@@ -32,6 +33,12 @@ struct KlEpi {
     int n;
     int V;
     float *pmt, *pst, *pct, *pms, *pss;  // [splits][n]
+    uint32_t *counters;                   // [ceil(n/32)] items finished per 32-row group
+    int splits;
+    const int64_t *row_idx;
+    int64_t T;
+    float *out_kl;
+    uint32_t *status;
   };
   const Params p;
   float mt, st0, st1, ct0, ct1, ms, ss0, ss1;
@@ -123,48 +130,46 @@ struct KlEpi {
   }
 
   __device__ __forceinline__ void end(int split, int row) {
-    if (row >= p.n) return;
-    const size_t o = static_cast<size_t>(split) * p.n + row;
-    p.pmt[o] = mt;
-    p.pst[o] = st0 + st1;
-    p.pct[o] = ct0 + ct1;
-    p.pms[o] = ms;
-    p.pss[o] = ss0 + ss1;
+    if (row < p.n) {
+      const size_t o = static_cast<size_t>(split) * p.n + row;
+      p.pmt[o] = mt;
+      p.pst[o] = st0 + st1;
+      p.pct[o] = ct0 + ct1;
+      p.pms[o] = ms;
+      p.pss[o] = ss0 + ss1;
+    }
+    if (last_arrival(p.counters + (row >> 5), static_cast<uint32_t>(p.splits)) && row < p.n)
+      merge_row(row);
+  }
+
+  // Merge the split partials of one row and finish the KL.
+  __device__ __forceinline__ void merge_row(int i) const {
+    const int n = p.n;
+    float Mt = -FLT_MAX, Ms = -FLT_MAX;
+    for (int s = 0; s < p.splits; ++s) {
+      const size_t o = static_cast<size_t>(s) * n + i;
+      Mt = fmaxf(Mt, __ldcg(p.pmt + o));
+      Ms = fmaxf(Ms, __ldcg(p.pms + o));
+    }
+    float St = 0.f, Ct = 0.f, Ss = 0.f;
+    for (int s = 0; s < p.splits; ++s) {
+      const size_t o = static_cast<size_t>(s) * n + i;
+      const float at = exp2f(__ldcg(p.pmt + o) - Mt);
+      St = fmaf(__ldcg(p.pst + o), at, St);
+      Ct = fmaf(__ldcg(p.pct + o), at, Ct);
+      Ss = fmaf(__ldcg(p.pss + o), exp2f(__ldcg(p.pms + o) - Ms), Ss);
+    }
+    float kl = Ct / St - kLn2f * ((Mt - Ms) + (log2f(St) - log2f(Ss)));
+    if (p.row_idx) {
+      const int64_t r = p.row_idx[i];
+      if (r < 0 || r >= p.T) {
+        atomicAdd(p.status + kStatBadRow, 1u);
+        kl = __int_as_float(0x7fc00000);
+      }
+    }
+    p.out_kl[i] = kl;
   }
 };
-
-// One thread per scored row: merge the split partials and finish the KL.
-__global__ void kl_merge_kernel(int n, int splits, const float *__restrict__ pmt,
-                                const float *__restrict__ pst, const float *__restrict__ pct,
-                                const float *__restrict__ pms, const float *__restrict__ pss,
-                                const int64_t *__restrict__ row_idx, int64_t T,
-                                float *__restrict__ out_kl, uint32_t *status) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n) return;
-  float Mt = -FLT_MAX, Ms = -FLT_MAX;
-  for (int s = 0; s < splits; ++s) {
-    const size_t o = static_cast<size_t>(s) * n + i;
-    Mt = fmaxf(Mt, pmt[o]);
-    Ms = fmaxf(Ms, pms[o]);
-  }
-  float St = 0.f, Ct = 0.f, Ss = 0.f;
-  for (int s = 0; s < splits; ++s) {
-    const size_t o = static_cast<size_t>(s) * n + i;
-    const float at = exp2f(pmt[o] - Mt);
-    St = fmaf(pst[o], at, St);
-    Ct = fmaf(pct[o], at, Ct);
-    Ss = fmaf(pss[o], exp2f(pms[o] - Ms), Ss);
-  }
-  float kl = Ct / St - kLn2f * ((Mt - Ms) + (log2f(St) - log2f(Ss)));
-  if (row_idx) {
-    const int64_t r = row_idx[i];
-    if (r < 0 || r >= T) {
-      atomicAdd(status + kStatBadRow, 1u);
-      kl = __int_as_float(0x7fc00000);
-    }
-  }
-  out_kl[i] = kl;
-}
 
 using KlLayout = PipeLayout<kKlBN, kKlStages, 2, kKlCG, kKlAcc>;
 #define KL_KERNEL vocab_pipeline_kernel<kKlBN, kKlStages, 2, KlEpi, kKlCG, kKlAcc>
@@ -178,6 +183,12 @@ cudaError_t launch_kl(const KlArgs &a, cudaStream_t stream) {
   p.pct = a.pct;
   p.pms = a.pms;
   p.pss = a.pss;
+  p.counters = a.counters;
+  p.splits = a.sch.splits;
+  p.row_idx = a.row_idx;
+  p.T = a.T;
+  p.out_kl = a.out_kl;
+  p.status = a.status;
   const uint32_t idesc = idesc_f16(a.bf16, kBM * kKlCG, kKlBN, false, false);
   return launch_persistent(KL_KERNEL, a.grid, KlLayout::kSmemBytes, kKlCG, stream, a.tmAs, a.tmBs,
                            a.tmAt, a.tmBt, a.sch, idesc, p, a.status);
@@ -190,14 +201,6 @@ int kl_units(int num_sms) {
   if (dev < 0 || dev >= 64) return resident_units(KL_KERNEL, KlLayout::kSmemBytes, kKlCG, num_sms);
   if (!cached[dev]) cached[dev] = resident_units(KL_KERNEL, KlLayout::kSmemBytes, kKlCG, num_sms);
   return cached[dev];
-}
-
-cudaError_t launch_kl_merge(const KlArgs &a, cudaStream_t stream) {
-  const int n = a.sch.n;
-  kl_merge_kernel<<<(n + 255) / 256, 256, 0, stream>>>(n, a.sch.splits, a.pmt, a.pst, a.pct,
-                                                       a.pms, a.pss, a.row_idx, a.T, a.out_kl,
-                                                       a.status);
-  return cudaGetLastError();
 }
 
 }  // namespace flp

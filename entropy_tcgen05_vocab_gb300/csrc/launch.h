@@ -40,6 +40,7 @@ struct FwdArgs {
   float inv_tau;
   float scale_log2;
   float *pm, *ps, *pb, *zt;
+  uint32_t *counters;  // [ceil(n / 32)] zeroed before the launch
   float *out_logp, *out_ent, *out_lse, *out_ez;
   uint32_t *status;
 };
@@ -53,6 +54,7 @@ struct KlArgs {
   const int64_t *row_idx;
   int64_t T;
   float *pmt, *pst, *pct, *pms, *pss;  // [splits][n] partial states
+  uint32_t *counters;                   // [ceil(n / 32)] zeroed before the launch
   float *out_kl;
   uint32_t *status;
 };
@@ -95,9 +97,7 @@ struct GemmArgs {
 cudaError_t launch_gather(const void *h, int64_t ld_h, const int64_t *row_idx, int64_t n,
                           int64_t T, int64_t H, void *hs, int num_sms, cudaStream_t stream);
 cudaError_t launch_fwd_scoring(const FwdArgs &a, cudaStream_t stream);
-cudaError_t launch_fwd_merge(const FwdArgs &a, cudaStream_t stream);
 cudaError_t launch_kl(const KlArgs &a, cudaStream_t stream);
-cudaError_t launch_kl_merge(const KlArgs &a, cudaStream_t stream);
 cudaError_t launch_grad(const GradArgs &a, cudaStream_t stream);
 cudaError_t launch_dh_gemm(const GemmArgs &a, cudaStream_t stream);
 cudaError_t launch_dw_gemm(const GemmArgs &a, cudaStream_t stream);

@@ -97,6 +97,23 @@ __device__ __forceinline__ void record_timeout(uint32_t *status, volatile int *a
 //                                                          (GEMM op at + op * BN)
 //   __device__ void end(int split, int row);
 // CG = 2 kernels must be launched with a cluster dimension of 2.
+
+// Called by all 32 lanes of a warp after they stored their rows' partial
+// states for one item: returns (to the whole warp) true if this warp is the
+// last of `expected` arrivals for its 32-row group, so every split's partial
+// of these rows is complete and visible to it (fence, count, fence: the last
+// arriver merges).  Warp-local on purpose: no barrier across warps that a
+// timed-out warp could leave waiting.
+__device__ __forceinline__ bool last_arrival(uint32_t *counter, uint32_t expected) {
+  __threadfence();
+  __syncwarp();
+  uint32_t last = 0;
+  if ((threadIdx.x & 31) == 0) last = atomicAdd(counter, 1u) == expected - 1u;
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (last) __threadfence();
+  return last != 0;
+}
+
 template <int BN, int STAGES, int NOPS, class Epi, int CG = 1, int NACC = 2>
 __global__ void __launch_bounds__(kPipeThreads, 1)
     vocab_pipeline_kernel(const __grid_constant__ CUtensorMap tmA0,

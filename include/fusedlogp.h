@@ -242,6 +242,7 @@ typedef struct {
     int32_t items;          /* work items = row_tiles * splits */
     int32_t grid;           /* persistent CTAs launched (a multiple of cta_group) */
     int64_t max_tiles_per_cta; /* load of the busiest CTA (pair), in block_m x block_n tiles */
+    int64_t chunk_rows;     /* FLP_OP_BACKWARD: rows per logit-gradient chunk (else 0) */
 } flp_plan;
 
 flp_status flp_plan_scoring(const flp_shape *shape, flp_op op, int32_t num_sms, flp_plan *out);
