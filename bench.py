@@ -60,6 +60,8 @@ def parse_args():
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     p.add_argument("--no-e2e", action="store_true", help="skip the end-to-end loop")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--T", type=int, default=None,
+                   help="replace the workload's row count (same H, V, recipe): small profiling cases")
     return p.parse_args()
 
 
@@ -345,7 +347,8 @@ def run_ours(args):
     flp.lib()
     P = peaks()
 
-    d = workloads.make(args.workload, device=device)
+    w0 = workloads.WORKLOADS[args.workload]
+    d = workloads.make(w0 if args.T is None else w0.scaled(T=args.T), device=device)
     sampler = ClockSampler(device.index) if rank == 0 else None
     if sampler:
         sampler.start()
