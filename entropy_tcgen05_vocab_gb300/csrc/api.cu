@@ -133,10 +133,10 @@ Layout layout_for(const flp_shape *s, flp_op op) {
 // ------------------------------------------------------------------ planner
 struct PlanKey {
   int64_t n, V, H, band_bytes;
-  int bn, units, bm;
+  int bn, units, bm, a_ops;
   bool operator<(const PlanKey &o) const {
-    return std::tie(n, V, H, band_bytes, bn, units, bm) <
-           std::tie(o.n, o.V, o.H, o.band_bytes, o.bn, o.units, o.bm);
+    return std::tie(n, V, H, band_bytes, bn, units, bm, a_ops) <
+           std::tie(o.n, o.V, o.H, o.band_bytes, o.bn, o.units, o.bm, o.a_ops);
   }
 };
 
@@ -160,7 +160,9 @@ struct Plan {
 std::mutex g_plan_mu;
 std::map<PlanKey, Plan> g_plans;
 
-Plan make_plan(int64_t n, int64_t V, int64_t H, int bn, int num_sms, int bm, int64_t band_bytes) {
+// a_ops = hidden-state operands per row tile (2 for the KL: student and teacher).
+Plan make_plan(int64_t n, int64_t V, int64_t H, int bn, int num_sms, int bm, int64_t band_bytes,
+               int a_ops) {
   Plan best{};
   Schedule s{};
   s.n = static_cast<int>(n);
@@ -168,7 +170,7 @@ Plan make_plan(int64_t n, int64_t V, int64_t H, int bn, int num_sms, int bm, int
   s.row_tiles = static_cast<int>(cdiv(n, bm));
   s.vocab_tiles = vocab_tiles(V, bn);
   s.k_blocks = static_cast<int>(cdiv(H, 64));
-  const int64_t a_tile_bytes = bm * H * 2;
+  const int64_t a_tile_bytes = static_cast<int64_t>(bm) * H * 2 * a_ops;
   s.band = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(s.row_tiles, band_bytes / a_tile_bytes)));
   const int smax = max_splits(V, bn);
   std::vector<int64_t> loads;
@@ -200,14 +202,14 @@ Plan make_plan(int64_t n, int64_t V, int64_t H, int bn, int num_sms, int bm, int
   return best;
 }
 
-Plan plan_cached(int64_t n, int64_t V, int64_t H, int bn, int units, int bm) {
+Plan plan_cached(int64_t n, int64_t V, int64_t H, int bn, int units, int bm, int a_ops = 1) {
   const int64_t band_bytes = band_budget();
-  const PlanKey k{n, V, H, band_bytes, bn, units, bm};
+  const PlanKey k{n, V, H, band_bytes, bn, units, bm, a_ops};
   std::lock_guard<std::mutex> g(g_plan_mu);
   auto it = g_plans.find(k);
   if (it != g_plans.end()) return it->second;
   if (g_plans.size() > 256) g_plans.clear();
-  Plan p = make_plan(n, V, H, bn, units, bm, band_bytes);
+  Plan p = make_plan(n, V, H, bn, units, bm, band_bytes, a_ops);
   g_plans.emplace(k, p);
   return p;
 }
@@ -373,7 +375,8 @@ flp_status flp_plan_scoring(const flp_shape *shape, flp_op op, int32_t num_sms, 
   const int bn = op == FLP_OP_KL ? kKlBN : kFwdBN;
   const int cg = op == FLP_OP_KL ? kKlCG : kFwdCG;
   const int units = std::max(1, num_sms / cg);
-  const Plan p = plan_cached(shape->n_rows, shape->V, shape->H, bn, units, 128 * cg);
+  const Plan p = plan_cached(shape->n_rows, shape->V, shape->H, bn, units, 128 * cg,
+                             op == FLP_OP_KL ? 2 : 1);
   out->row_tiles = p.sch.row_tiles;
   out->vocab_tiles = p.sch.vocab_tiles;
   out->block_m = 128 * cg;
@@ -481,7 +484,7 @@ flp_status flp_kl(const flp_shape *s, const void *h_s, const void *W_s, const vo
   if ((st = device_info(&dev)) != FLP_OK) return st;
 
   const Layout L = layout_for(s, FLP_OP_KL);
-  const Plan p = plan_cached(s->n_rows, s->V, s->H, kKlBN, kl_units(dev.sms), 128 * kKlCG);
+  const Plan p = plan_cached(s->n_rows, s->V, s->H, kKlBN, kl_units(dev.sms), 128 * kKlCG, 2);
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   KlArgs a{};
   const void *As = h_s, *At = h_t;
