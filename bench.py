@@ -181,11 +181,20 @@ def barrier(world):
 
 
 def max_over_ranks(x, world, device):
+    """Max of a per-rank float over the process group (nccl on GPUs, gloo on CPU)."""
     if world == 1:
         return x
+    if torch.distributed.get_backend() != "nccl":
+        device = torch.device("cpu")
     t = torch.tensor([x], dtype=torch.float64, device=device)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(units_per_rank, steps, ms_max, world):
+    """Whole-job units/s: every rank scores its own replica; the job takes as
+    long as its slowest rank."""
+    return world * units_per_rank * steps / (ms_max / 1e3)
 
 
 # ---------------------------------------------------------------- workloads
@@ -356,7 +365,7 @@ def run_ours(args):
     clocks = sampler.stop() if sampler else None
     total_ms = max_over_ranks(total_ms, world, device)
     n = d["n"]
-    value = world * n * args.steps / (total_ms / 1e3)
+    value = job_throughput(n, args.steps, total_ms, world)
     fl = flops_per_call(d)
     achieved = fl / (kernel_ms / 1e3) / 1e12
     traffic, traffic_src = recorded_traffic()

@@ -84,6 +84,8 @@ def lib():
     L.flp_row_chunks.restype = i64
     L.flp_logprob_entropy_noalloc.argtypes = [shp, vp, vp, vp, vp, f32, vp, vp, vp, vp, vp]
     L.flp_logprob_entropy_noalloc.restype = ctypes.c_int
+    L.flp_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp, vp]
+    L.flp_selftest_wait_timeout.restype = ctypes.c_int
     L.flp_set_kernel_events.argtypes = [vp, vp]
     L.flp_set_kernel_events.restype = ctypes.c_int
     for f in (L.flp_logprob_entropy, L.flp_kl, L.flp_backward, L.flp_read_device_status,
@@ -129,6 +131,14 @@ def set_kernel_events(before, after):
     its tensor-core kernels (both must have been recorded once, so that they
     exist)."""
     lib().flp_set_kernel_events(ctypes.c_void_p(before.cuda_event), ctypes.c_void_p(after.cuda_event))
+
+
+def selftest_wait_timeout(limit_ns, device=None):
+    """Run the bounded-wait self-test kernel; returns the device status it left."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    _check(lib().flp_selftest_wait_timeout(int(limit_ns), _ptr(ws), _stream(dev)))
+    return read_device_status(ws, dev)
 
 
 def _ptr(t):

@@ -692,6 +692,20 @@ flp_status flp_logprob_entropy_noalloc(const flp_shape *s, const void *h, const 
                              out_ez, scratch, FLP_NOALLOC_SCRATCH_BYTES, stream);
 }
 
+flp_status flp_selftest_wait_timeout(uint64_t limit_ns, void *ws, flp_stream_t stream) {
+  g_err[0] = 0;
+  if (!ws) return fail(FLP_ERR_WORKSPACE, "workspace is NULL");
+  if (limit_ns < 1000000ull || limit_ns > 1000000000ull)
+    return fail(FLP_ERR_INVALID_ARG, "limit_ns must be within 1 ms .. 1 s");
+  DeviceInfo dev;
+  const flp_status st = device_info(&dev);
+  if (st != FLP_OK) return st;
+  const cudaError_t e =
+      launch_wait_timeout(limit_ns, static_cast<uint32_t *>(ws), reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+  return FLP_OK;
+}
+
 flp_status flp_read_device_status(const void *ws, flp_device_status *out, flp_stream_t stream) {
   g_err[0] = 0;
   if (!ws || !out) return fail(FLP_ERR_INVALID_ARG, "workspace and out are required");

@@ -105,6 +105,7 @@ int gemm_tiles(int M, int N);
 int gemm_cta_group();
 int gemm_units(int num_sms);
 int fwd_smem_bytes();
+cudaError_t launch_wait_timeout(uint64_t limit_ns, uint32_t *status, cudaStream_t stream);
 // CTAs or CTA pairs of each pipeline that can be resident at once.
 int fwd_units(int num_sms);
 int grad_units(int num_sms);

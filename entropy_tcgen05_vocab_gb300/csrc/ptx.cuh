@@ -77,7 +77,8 @@ __device__ __forceinline__ bool mbar_test(uint32_t addr, uint32_t parity) {
 // Wait for the phase with the given parity to complete.  Returns false if
 // *abort becomes non-zero or the wall-clock limit passes first.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
-                                          const volatile int *abort) {
+                                          const volatile int *abort,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   const uint32_t addr = smem_u32(bar);
   if (mbar_test(addr, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
@@ -86,7 +87,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
     for (int i = 0; i < 32; ++i)
       if (mbar_test(addr, parity)) return true;
     if (*abort) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 

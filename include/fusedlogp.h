@@ -220,6 +220,17 @@ flp_status flp_logprob_entropy_noalloc(const flp_shape *shape, const void *h, co
  */
 flp_status flp_set_kernel_events(void *before, void *after);
 
+/*
+ * Self-test of the bounded waits the kernels use on the GPU: launches one
+ * tiny kernel whose thread waits on an mbarrier that nothing arrives on.  The
+ * wait gives up after limit_ns nanoseconds (1 ms .. 1 s), adds one to the
+ * timeout counter of the 256-byte device status block at `workspace` (whose
+ * other words are left alone; clear it first) and the kernel exits normally.
+ * Read the counter with flp_read_device_status().  Used by the tests to show
+ * that a stalled pipeline wait ends in a reported status, not a hung GPU.
+ */
+flp_status flp_selftest_wait_timeout(uint64_t limit_ns, void *workspace, flp_stream_t stream);
+
 /* Static description of a status code. */
 const char *flp_status_string(flp_status status);
 

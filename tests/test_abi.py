@@ -162,3 +162,9 @@ def test_row_chunks_follow_torch_chunk(L, n, c):
     want = [t.numel() for t in torch.arange(n).chunk((n - 1) // c + 1)]
     assert flp.row_chunks(n, c) == want
     assert flp.row_chunks(0, c) == []
+
+
+@pytest.mark.parametrize("limit", [0, 999_999, 2_000_000_000])
+def test_selftest_limit_is_validated_on_host(L, limit):
+    assert L.flp_selftest_wait_timeout(limit, FAKE, None) == 1
+    assert L.flp_selftest_wait_timeout(50_000_000, None, None) == 3

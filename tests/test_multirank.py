@@ -1,0 +1,66 @@
+"""The multi-rank bench path on CPU: two gloo ranks (127.0.0.1).
+
+The path has no exchange step; under torchrun every rank scores its own
+replica and bench.py reduces the timed region with a max over ranks.  These
+tests run that reduction and the whole-job throughput on a real two-process
+gloo group, and check that the reference arm does its work on rank 0 only.
+"""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        ws, r, lr = bench.dist_info()
+        assert (ws, r, lr) == (world, rank, rank)
+        bench.barrier(world)
+        ms = 10.0 + 5.0 * rank                    # rank 1 is the slow one
+        m = bench.max_over_ranks(ms, world, torch.device("cpu"))
+        out[rank] = (m, bench.job_throughput(4096, 20, m, world))
+        bench.barrier(world)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_rank_time_reduction_and_throughput():
+    world = 2
+    mgr = mp.get_context("spawn").Manager()
+    out = mgr.dict()
+    mp.start_processes(_worker, args=(world, _free_port(), out), nprocs=world, join=True,
+                       start_method="spawn")
+    assert out[0] == out[1]
+    m, v = out[0]
+    assert m == 15.0
+    assert v == pytest.approx(2 * 4096 * 20 / 0.015)
+
+
+def test_single_rank_needs_no_group():
+    assert bench.max_over_ranks(3.5, 1, torch.device("cpu")) == 3.5
+    assert bench.job_throughput(10, 2, 1000.0, 1) == 20.0
+
+
+def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("LOCAL_RANK", "1")
+
+    class A:
+        steps, warmup, workload, gpus = 3, 1, 1, 2
+    assert bench.run_reference(A()) is None
+    assert capsys.readouterr().out == ""
