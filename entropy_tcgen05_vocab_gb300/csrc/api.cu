@@ -108,7 +108,8 @@ Layout layout_for(const flp_shape *s, flp_op op) {
   L.cnt_bytes = static_cast<size_t>(cdiv(s->n_rows, 256) * 8 + 8) * 4;
   L.cnt = take(L.cnt_bytes);
   const int bn = (op == FLP_OP_KL) ? kKlBN : kFwdBN;
-  const size_t sm = static_cast<size_t>(max_splits(s->V, bn));
+  const int halves = ((op == FLP_OP_KL) ? kKlEpiWarps : kFwdEpiWarps) / 4;
+  const size_t sm = static_cast<size_t>(max_splits(s->V, bn)) * halves;  // partial slots
   L.pm = take(sm * n * 4);
   L.ps = take(sm * n * 4);
   L.pb = take(sm * n * 4);

@@ -101,9 +101,9 @@ struct GradEpi {
     }
   }
 
-  __device__ __forceinline__ void tile(uint32_t taddr, int col0) {
+  __device__ __forceinline__ void tile(uint32_t taddr, int col0, int nchunks) {
 #pragma unroll 1
-    for (int c = 0; c < kFwdBN / 32; ++c) {
+    for (int c = 0; c < nchunks; ++c) {
       const int cb = col0 + c * 32;
       if (cb >= p.V) break;  // same for the whole warp
       float x[32];
@@ -221,7 +221,8 @@ struct DwEpi {
 
 // ---------------------------------------------------------------- launchers
 using GradLayout = PipeLayout<kFwdBN, kFwdStages, 1, kFwdCG>;
-#define GRAD_KERNEL vocab_pipeline_kernel<kFwdBN, kFwdStages, 1, GradEpi, kFwdCG>
+#define GRAD_KERNEL vocab_pipeline_kernel<kFwdBN, kFwdStages, 1, GradEpi, kFwdCG, 2, kFwdEpiWarps>
+constexpr int kGradThreads = pipe_threads(kFwdEpiWarps);
 
 cudaError_t launch_grad(const GradArgs &a, cudaStream_t stream) {
   GradEpi::Params p;
@@ -241,7 +242,7 @@ cudaError_t launch_grad(const GradArgs &a, cudaStream_t stream) {
   p.ldg = a.ldg;
   p.bf16 = a.bf16;
   const uint32_t idesc = idesc_f16(a.bf16, kBM * kFwdCG, kFwdBN, false, false);
-  return launch_persistent(GRAD_KERNEL, a.grid, GradLayout::kSmemBytes, kFwdCG, stream, a.tmA,
+  return launch_persistent(GRAD_KERNEL, a.grid, kGradThreads, GradLayout::kSmemBytes, kFwdCG, stream, a.tmA,
                            a.tmB, a.tmA, a.tmB, a.sch, idesc, p, a.status);
 }
 
@@ -249,8 +250,8 @@ int grad_units(int num_sms) {
   static int cached[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return resident_units(GRAD_KERNEL, GradLayout::kSmemBytes, kFwdCG, num_sms);
-  if (!cached[dev]) cached[dev] = resident_units(GRAD_KERNEL, GradLayout::kSmemBytes, kFwdCG, num_sms);
+  if (dev < 0 || dev >= 64) return resident_units(GRAD_KERNEL, kGradThreads, GradLayout::kSmemBytes, kFwdCG, num_sms);
+  if (!cached[dev]) cached[dev] = resident_units(GRAD_KERNEL, kGradThreads, GradLayout::kSmemBytes, kFwdCG, num_sms);
   return cached[dev];
 }
 
@@ -278,8 +279,8 @@ int gemm_units(int num_sms) {
   static int cached[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return resident_units(DH_KERNEL, GemmL::kSmemBytes, kGemmCG, num_sms);
-  if (!cached[dev]) cached[dev] = resident_units(DH_KERNEL, GemmL::kSmemBytes, kGemmCG, num_sms);
+  if (dev < 0 || dev >= 64) return resident_units(DH_KERNEL, kPipeThreads, GemmL::kSmemBytes, kGemmCG, num_sms);
+  if (!cached[dev]) cached[dev] = resident_units(DH_KERNEL, kPipeThreads, GemmL::kSmemBytes, kGemmCG, num_sms);
   return cached[dev];
 }
 
@@ -294,7 +295,7 @@ cudaError_t launch_dh_gemm(const GemmArgs &a, cudaStream_t stream) {
   p.ld = a.ld_dh;
   p.bf16 = a.bf16;
   const uint32_t idesc = idesc_f16(a.bf16, kBM * kGemmCG, kGemmBN, false, true);
-  return launch_persistent(DH_KERNEL, a.grid, GemmL::kSmemBytes, kGemmCG, stream, a.tmA, a.tmB,
+  return launch_persistent(DH_KERNEL, a.grid, kPipeThreads, GemmL::kSmemBytes, kGemmCG, stream, a.tmA, a.tmB,
                            gemm_shape(a.M, a.N, a.K), idesc, p, a.status);
 }
 
@@ -306,7 +307,7 @@ cudaError_t launch_dw_gemm(const GemmArgs &a, cudaStream_t stream) {
   p.ld = a.ld_dw;
   p.accumulate = a.accumulate;
   const uint32_t idesc = idesc_f16(a.bf16, kBM * kGemmCG, kGemmBN, true, true);
-  return launch_persistent(DW_KERNEL, a.grid, GemmL::kSmemBytes, kGemmCG, stream, a.tmA, a.tmB,
+  return launch_persistent(DW_KERNEL, a.grid, kPipeThreads, GemmL::kSmemBytes, kGemmCG, stream, a.tmA, a.tmB,
                            gemm_shape(a.M, a.N, a.K), idesc, p, a.status);
 }
 

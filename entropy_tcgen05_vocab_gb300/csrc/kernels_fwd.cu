@@ -134,9 +134,9 @@ struct LseEpi {
     }
   }
 
-  __device__ __forceinline__ void tile(uint32_t taddr, int col0) {
+  __device__ __forceinline__ void tile(uint32_t taddr, int col0, int nchunks) {
 #pragma unroll 1
-    for (int c = 0; c < 8; ++c) {
+    for (int c = 0; c < nchunks; ++c) {
       const int cb = col0 + c * 32;
       if (cb >= p.V) break;  // same for the whole warp
       float x[32];
@@ -223,7 +223,8 @@ cudaError_t launch_gather(const void *h, int64_t ld_h, const int64_t *row_idx, i
 }
 
 using FwdLayout = PipeLayout<kFwdBN, kFwdStages, 1, kFwdCG>;
-#define FWD_KERNEL vocab_pipeline_kernel<kFwdBN, kFwdStages, 1, LseEpi, kFwdCG>
+#define FWD_KERNEL vocab_pipeline_kernel<kFwdBN, kFwdStages, 1, LseEpi, kFwdCG, 2, kFwdEpiWarps>
+constexpr int kFwdThreads = pipe_threads(kFwdEpiWarps);
 
 cudaError_t launch_fwd_scoring(const FwdArgs &a, cudaStream_t stream) {
   LseEpi::Params p;
@@ -238,7 +239,7 @@ cudaError_t launch_fwd_scoring(const FwdArgs &a, cudaStream_t stream) {
   p.pb = a.pb;
   p.zt = a.zt;
   p.counters = a.counters;
-  p.splits = a.sch.splits;
+  p.splits = a.sch.splits * (kFwdEpiWarps / 4);  // partial slots per row
   p.inv_tau = a.inv_tau;
   p.out_logp = a.out_logp;
   p.out_ent = a.out_ent;
@@ -246,7 +247,7 @@ cudaError_t launch_fwd_scoring(const FwdArgs &a, cudaStream_t stream) {
   p.out_ez = a.out_ez;
   p.status = a.status;
   const uint32_t idesc = idesc_f16(a.bf16, kBM * kFwdCG, kFwdBN, false, false);
-  return launch_persistent(FWD_KERNEL, a.grid, FwdLayout::kSmemBytes, kFwdCG, stream, a.tmA,
+  return launch_persistent(FWD_KERNEL, a.grid, kFwdThreads, FwdLayout::kSmemBytes, kFwdCG, stream, a.tmA,
                            a.tmB, a.tmA, a.tmB, a.sch, idesc, p, a.status);
 }
 
@@ -254,8 +255,8 @@ int fwd_units(int num_sms) {
   static int cached[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return resident_units(FWD_KERNEL, FwdLayout::kSmemBytes, kFwdCG, num_sms);
-  if (!cached[dev]) cached[dev] = resident_units(FWD_KERNEL, FwdLayout::kSmemBytes, kFwdCG, num_sms);
+  if (dev < 0 || dev >= 64) return resident_units(FWD_KERNEL, kFwdThreads, FwdLayout::kSmemBytes, kFwdCG, num_sms);
+  if (!cached[dev]) cached[dev] = resident_units(FWD_KERNEL, kFwdThreads, FwdLayout::kSmemBytes, kFwdCG, num_sms);
   return cached[dev];
 }
 

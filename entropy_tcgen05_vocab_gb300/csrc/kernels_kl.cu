@@ -114,9 +114,9 @@ struct KlEpi {
     }
   }
 
-  __device__ __forceinline__ void tile(uint32_t taddr, int col0) {
+  __device__ __forceinline__ void tile(uint32_t taddr, int col0, int nchunks) {
 #pragma unroll 1
-    for (int c = 0; c < kKlBN / 32; ++c) {
+    for (int c = 0; c < nchunks; ++c) {
       const int cb = col0 + c * 32;
       if (cb >= p.V) break;  // same for the whole warp
       float xs[32], xt[32];
@@ -172,7 +172,8 @@ struct KlEpi {
 };
 
 using KlLayout = PipeLayout<kKlBN, kKlStages, 2, kKlCG, kKlAcc>;
-#define KL_KERNEL vocab_pipeline_kernel<kKlBN, kKlStages, 2, KlEpi, kKlCG, kKlAcc>
+#define KL_KERNEL vocab_pipeline_kernel<kKlBN, kKlStages, 2, KlEpi, kKlCG, kKlAcc, kKlEpiWarps>
+constexpr int kKlThreads = pipe_threads(kKlEpiWarps);
 
 cudaError_t launch_kl(const KlArgs &a, cudaStream_t stream) {
   KlEpi::Params p;
@@ -184,13 +185,13 @@ cudaError_t launch_kl(const KlArgs &a, cudaStream_t stream) {
   p.pms = a.pms;
   p.pss = a.pss;
   p.counters = a.counters;
-  p.splits = a.sch.splits;
+  p.splits = a.sch.splits * (kKlEpiWarps / 4);  // partial slots per row
   p.row_idx = a.row_idx;
   p.T = a.T;
   p.out_kl = a.out_kl;
   p.status = a.status;
   const uint32_t idesc = idesc_f16(a.bf16, kBM * kKlCG, kKlBN, false, false);
-  return launch_persistent(KL_KERNEL, a.grid, KlLayout::kSmemBytes, kKlCG, stream, a.tmAs, a.tmBs,
+  return launch_persistent(KL_KERNEL, a.grid, kKlThreads, KlLayout::kSmemBytes, kKlCG, stream, a.tmAs, a.tmBs,
                            a.tmAt, a.tmBt, a.sch, idesc, p, a.status);
 }
 
@@ -198,8 +199,8 @@ int kl_units(int num_sms) {
   static int cached[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return resident_units(KL_KERNEL, KlLayout::kSmemBytes, kKlCG, num_sms);
-  if (!cached[dev]) cached[dev] = resident_units(KL_KERNEL, KlLayout::kSmemBytes, kKlCG, num_sms);
+  if (dev < 0 || dev >= 64) return resident_units(KL_KERNEL, kKlThreads, KlLayout::kSmemBytes, kKlCG, num_sms);
+  if (!cached[dev]) cached[dev] = resident_units(KL_KERNEL, kKlThreads, KlLayout::kSmemBytes, kKlCG, num_sms);
   return cached[dev];
 }
 

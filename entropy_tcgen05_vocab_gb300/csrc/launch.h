@@ -17,6 +17,7 @@ namespace flp {
 constexpr int kFwdBN = 256;
 constexpr int kFwdCG = 2;
 constexpr int kFwdStages = 6;
+constexpr int kFwdEpiWarps = 4;
 // Tile shape of the KL pipeline (student and teacher accumulators per tile):
 // CTA pairs on 256-row x 256-column tiles, 3 stages of 64 KB per CTA, one
 // accumulator buffer (2 x 256 TMEM columns).  Against 128-column tiles with
@@ -26,6 +27,9 @@ constexpr int kKlBN = 256;
 constexpr int kKlCG = 2;
 constexpr int kKlStages = 3;
 constexpr int kKlAcc = 1;
+// Eight epilogue warps (two per TMEM lane quarter, each folding half the
+// columns) halve the epilogue that the single accumulator buffer exposes.
+constexpr int kKlEpiWarps = 8;
 
 
 struct FwdArgs {

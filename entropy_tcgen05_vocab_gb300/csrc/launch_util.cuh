@@ -10,14 +10,14 @@
 namespace flp {
 
 template <typename... KArgs, typename... Args>
-cudaError_t launch_persistent(void (*kern)(KArgs...), int grid, int smem_bytes, int cg,
+cudaError_t launch_persistent(void (*kern)(KArgs...), int grid, int threads, int smem_bytes, int cg,
                               cudaStream_t stream, Args &&...args) {
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
-  cfg.blockDim = dim3(kPipeThreads);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads));
   cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -34,14 +34,14 @@ cudaError_t launch_persistent(void (*kern)(KArgs...), int grid, int smem_bytes, 
 
 // CTAs (cg = 1) or CTA pairs (cg = 2) of `kern` that fit on the device at once.
 template <typename... KArgs>
-int resident_units(void (*kern)(KArgs...), int smem_bytes, int cg, int num_sms) {
+int resident_units(void (*kern)(KArgs...), int threads, int smem_bytes, int cg, int num_sms) {
   if (cg == 1) return num_sms;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) !=
       cudaSuccess)
     return num_sms / cg;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(num_sms));
-  cfg.blockDim = dim3(kPipeThreads);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads));
   cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;

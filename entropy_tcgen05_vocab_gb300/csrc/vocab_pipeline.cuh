@@ -48,8 +48,12 @@ namespace flp {
 constexpr int kBM = 128;         // rows per CTA tile (TMEM lanes)
 constexpr int kBK = 64;          // K elements per stage = one 128-byte swizzle row
 constexpr int kUmmaK = 16;       // K per tcgen05.mma kind::f16
-constexpr int kEpiWarps = 4;
+constexpr int kEpiWarps = 4;                        // epilogue warps of the GEMM kernels
 constexpr int kPipeThreads = 64 + 32 * kEpiWarps;
+
+// Threads of a vocabulary-pipeline CTA with EPIW epilogue warps (4 or 8).
+// With 8, two warps share each 32-lane TMEM quarter and split its columns.
+__host__ __device__ constexpr int pipe_threads(int epiw) { return 64 + 32 * epiw; }
 
 // NOPS independent GEMMs share one tile (the KL pipeline runs the student and
 // the teacher head side by side, NOPS = 2).  Per-CTA stage layout:
@@ -92,10 +96,11 @@ __device__ __forceinline__ void record_timeout(uint32_t *status, volatile int *a
 //   struct Params;
 //   __device__ Epi(const Params&);
 //   __device__ void begin(int mt, int row);               row = global scored row of this thread
-//   __device__ void tile(uint32_t taddr, int col0);       taddr = TMEM address of this warp's
-//                                                          lanes at the tile's first column
-//                                                          (GEMM op at + op * BN)
-//   __device__ void end(int split, int row);
+//   __device__ void tile(uint32_t taddr, int col0, int nchunks);
+//                       taddr = TMEM address of this warp's lanes at its first column (the
+//                       same columns of GEMM op at + op * BN); col0 = first vocabulary column;
+//                       nchunks = 32-column chunks this warp folds
+//   __device__ void end(int slot, int row);               slot = split * (EPIW / 4) + column half
 // CG = 2 kernels must be launched with a cluster dimension of 2.
 
 // Called by all 32 lanes of a warp after they stored their rows' partial
@@ -114,8 +119,8 @@ __device__ __forceinline__ bool last_arrival(uint32_t *counter, uint32_t expecte
   return last != 0;
 }
 
-template <int BN, int STAGES, int NOPS, class Epi, int CG = 1, int NACC = 2>
-__global__ void __launch_bounds__(kPipeThreads, 1)
+template <int BN, int STAGES, int NOPS, class Epi, int CG = 1, int NACC = 2, int EPIW = 4>
+__global__ void __launch_bounds__(pipe_threads(EPIW), 1)
     vocab_pipeline_kernel(const __grid_constant__ CUtensorMap tmA0,
                           const __grid_constant__ CUtensorMap tmB0,
                           const __grid_constant__ CUtensorMap tmA1,
@@ -124,6 +129,9 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                           uint32_t *status) {
   using L = PipeLayout<BN, STAGES, NOPS, CG, NACC>;
   static_assert(NOPS == 1 || NOPS == 2, "one or two GEMMs per tile");
+  static_assert(EPIW == 4 || EPIW == 8, "four or eight epilogue warps");
+  constexpr int kHalves = EPIW / 4;          // warps sharing one TMEM lane quarter
+  constexpr int kWarpCols = BN / kHalves;    // vocabulary columns one epilogue warp folds
   constexpr bool kPair = CG == 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -150,7 +158,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], kEpiWarps * CG);
+      mbar_init(&tempty[a], EPIW * CG);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -316,7 +324,9 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int lg = warp & 3;  // the TMEM lane quarter this warp may access
-    const uint32_t lane_off = static_cast<uint32_t>(lg * 32) << 16;
+    const int half = (warp - 2) / 4;  // which columns of the quarter it folds
+    const uint32_t lane_off = (static_cast<uint32_t>(lg * 32) << 16) +
+                              static_cast<uint32_t>(half * kWarpCols);
     // the pair's "accumulator empty" barriers live in the leader
     const uint32_t tempty_dst = kPair ? mapa_shared(smem_u32(tempty), 0) : smem_u32(tempty);
     Epi epi(ep);
@@ -333,7 +343,8 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         tc_fence_after();
-        epi.tile(tmem_base + lane_off + static_cast<uint32_t>(acc * L::kAccCols), vt * BN);
+        epi.tile(tmem_base + lane_off + static_cast<uint32_t>(acc * L::kAccCols),
+                 vt * BN + half * kWarpCols, kWarpCols / 32);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
@@ -346,7 +357,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
         if (acc == 0) acc_phase ^= 1u;
       }
       if (!ok) break;
-      epi.end(sp, row);
+      epi.end(sp * kHalves + half, row);
     }
     if (!ok && lane == 0) record_timeout<CG>(status, abort_flag);
   }
