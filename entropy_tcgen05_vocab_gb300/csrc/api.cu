@@ -107,7 +107,8 @@ Layout layout_for(const flp_shape *s, flp_op op) {
   // groups are counted over whole 256-row tiles
   L.cnt_bytes = static_cast<size_t>(cdiv(s->n_rows, 256) * 8 + 8) * 4;
   L.cnt = take(L.cnt_bytes);
-  const int bn = (op == FLP_OP_KL) ? kKlBN : kFwdBN;
+  // the backward's statistics pass is the forward kernel
+  const int bn = (op == FLP_OP_KL) ? kKlBN : kFwdTileCols;
   const int halves = ((op == FLP_OP_KL) ? kKlEpiWarps : kFwdEpiWarps) / 4;
   const size_t sm = static_cast<size_t>(max_splits(s->V, bn)) * halves;  // partial slots
   L.pm = take(sm * n * 4);
@@ -373,7 +374,7 @@ flp_status flp_plan_scoring(const flp_shape *shape, flp_op op, int32_t num_sms, 
     return fail(FLP_ERR_INVALID_ARG, "unknown op");
   std::memset(out, 0, sizeof *out);
   if (shape->n_rows == 0) return FLP_OK;
-  const int bn = op == FLP_OP_KL ? kKlBN : kFwdBN;
+  const int bn = op == FLP_OP_KL ? kKlBN : kFwdTileCols;
   const int cg = op == FLP_OP_KL ? kKlCG : kFwdCG;
   const int units = std::max(1, num_sms / cg);
   const Plan p = plan_cached(shape->n_rows, shape->V, shape->H, bn, units, 128 * cg,
@@ -423,7 +424,7 @@ flp_status flp_logprob_entropy(const flp_shape *s, const void *h, const void *W,
   if ((st = device_info(&dev)) != FLP_OK) return st;
 
   const Layout L = layout_for(s, FLP_OP_LOGPROB_ENTROPY);
-  const Plan p = plan_cached(s->n_rows, s->V, s->H, kFwdBN, fwd_units(dev.sms), 128 * kFwdCG);
+  const Plan p = plan_cached(s->n_rows, s->V, s->H, kFwdTileCols, fwd_units(dev.sms), 128 * kFwdCG);
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   FwdArgs a{};
   const void *A = h;
@@ -580,7 +581,7 @@ flp_status flp_backward(const flp_shape *s, const void *h, const void *W, const 
   // Per-row statistics (LSE, E[z']) unless the caller kept them from the forward.
   if (!lse) {
     FwdArgs a{};
-    const Plan p = plan_cached(s->n_rows, s->V, s->H, kFwdBN, fwd_units(dev.sms), 128 * kFwdCG);
+    const Plan p = plan_cached(s->n_rows, s->V, s->H, kFwdTileCols, fwd_units(dev.sms), 128 * kFwdCG);
     if ((st = make_map(&a.tmA, s->dtype, A, s->H, s->n_rows, lda, 64, 128)) != FLP_OK) return st;
     if ((st = make_map(&a.tmB, s->dtype, W, s->H, s->V, s->ld_w, 64, kFwdBN / kFwdCG)) != FLP_OK)
       return st;
@@ -616,12 +617,12 @@ flp_status flp_backward(const flp_shape *s, const void *h, const void *W, const 
     const void *Ar = eb + static_cast<size_t>(r0) * lda * esz;
     // 1. G = d loss / d z for the chunk's rows
     GradArgs ga{};
-    const Plan p = plan_cached(rc, s->V, s->H, kFwdBN, grad_units(dev.sms), 128 * kFwdCG);
+    const Plan p = plan_cached(rc, s->V, s->H, kGradBN, grad_units(dev.sms), 128 * kGradCG);
     if ((st = make_map(&ga.tmA, s->dtype, Ar, s->H, rc, lda, 64, 128)) != FLP_OK) return st;
-    if ((st = make_map(&ga.tmB, s->dtype, W, s->H, s->V, s->ld_w, 64, kFwdBN / kFwdCG)) != FLP_OK)
+    if ((st = make_map(&ga.tmB, s->dtype, W, s->H, s->V, s->ld_w, 64, kGradBN / kGradCG)) != FLP_OK)
       return st;
     ga.sch = p.sch;
-    ga.grid = p.grid * kFwdCG;
+    ga.grid = p.grid * kGradCG;
     ga.bf16 = s->dtype == FLP_BF16;
     ga.r0 = static_cast<int>(r0);
     ga.T = s->T;

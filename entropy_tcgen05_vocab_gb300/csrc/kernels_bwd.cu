@@ -220,9 +220,9 @@ struct DwEpi {
 };
 
 // ---------------------------------------------------------------- launchers
-using GradLayout = PipeLayout<kFwdBN, kFwdStages, 1, kFwdCG>;
-#define GRAD_KERNEL vocab_pipeline_kernel<kFwdBN, kFwdStages, 1, GradEpi, kFwdCG, 2, kFwdEpiWarps>
-constexpr int kGradThreads = pipe_threads(kFwdEpiWarps);
+using GradLayout = PipeLayout<kGradBN, kGradStages, 1, kGradCG>;
+#define GRAD_KERNEL vocab_pipeline_kernel<kGradBN, kGradStages, 1, GradEpi, kGradCG, 2, kGradEpiWarps>
+constexpr int kGradThreads = pipe_threads(kGradEpiWarps);
 
 cudaError_t launch_grad(const GradArgs &a, cudaStream_t stream) {
   GradEpi::Params p;
@@ -241,8 +241,8 @@ cudaError_t launch_grad(const GradArgs &a, cudaStream_t stream) {
   p.G = static_cast<uint16_t *>(a.G);
   p.ldg = a.ldg;
   p.bf16 = a.bf16;
-  const uint32_t idesc = idesc_f16(a.bf16, kBM * kFwdCG, kFwdBN, false, false);
-  return launch_persistent(GRAD_KERNEL, a.grid, kGradThreads, GradLayout::kSmemBytes, kFwdCG, stream, a.tmA,
+  const uint32_t idesc = idesc_f16(a.bf16, kBM * kGradCG, kGradBN, false, false);
+  return launch_persistent(GRAD_KERNEL, a.grid, kGradThreads, GradLayout::kSmemBytes, kGradCG, stream, a.tmA,
                            a.tmB, a.tmA, a.tmB, a.sch, idesc, p, a.status);
 }
 
@@ -250,8 +250,8 @@ int grad_units(int num_sms) {
   static int cached[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return resident_units(GRAD_KERNEL, kGradThreads, GradLayout::kSmemBytes, kFwdCG, num_sms);
-  if (!cached[dev]) cached[dev] = resident_units(GRAD_KERNEL, kGradThreads, GradLayout::kSmemBytes, kFwdCG, num_sms);
+  if (dev < 0 || dev >= 64) return resident_units(GRAD_KERNEL, kGradThreads, GradLayout::kSmemBytes, kGradCG, num_sms);
+  if (!cached[dev]) cached[dev] = resident_units(GRAD_KERNEL, kGradThreads, GradLayout::kSmemBytes, kGradCG, num_sms);
   return cached[dev];
 }
 

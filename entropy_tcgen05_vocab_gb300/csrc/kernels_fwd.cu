@@ -222,8 +222,9 @@ cudaError_t launch_gather(const void *h, int64_t ld_h, const int64_t *row_idx, i
   return cudaGetLastError();
 }
 
-using FwdLayout = PipeLayout<kFwdBN, kFwdStages, 1, kFwdCG>;
-#define FWD_KERNEL vocab_pipeline_kernel<kFwdBN, kFwdStages, 1, LseEpi, kFwdCG, 2, kFwdEpiWarps>
+static_assert(kFwdTileCols == 2 * kFwdBN, "two MMAs per tile");
+using FwdLayout = PipeLayout<kFwdBN, kFwdStages, 2, kFwdCG, 1, true>;
+#define FWD_KERNEL vocab_pipeline_kernel<kFwdBN, kFwdStages, 2, LseEpi, kFwdCG, 1, kFwdEpiWarps, true>
 constexpr int kFwdThreads = pipe_threads(kFwdEpiWarps);
 
 cudaError_t launch_fwd_scoring(const FwdArgs &a, cudaStream_t stream) {

@@ -12,12 +12,24 @@
 
 namespace flp {
 
-// Tile shape of the forward scoring and gradient pipelines: CTA pairs
-// (cta_group::2) on 256-row x 256-column tiles, 6 stages of 32 KB per CTA.
-constexpr int kFwdBN = 256;
+// Forward scoring (and the backward's statistics pass): CTA pairs
+// (cta_group::2) on 256-row x 512-column tiles made of two N = 256 MMAs that
+// share the A operand, one accumulator buffer (512 TMEM columns), eight
+// epilogue warps, 4 stages of 48 KB per CTA.  Against 256-column tiles with
+// double-buffered accumulators this needs a quarter less operand traffic per
+// flop (48 vs 64 B/clk/SM at full rate), which pays for the epilogue no
+// longer overlapping the MMAs.
+constexpr int kFwdBN = 256;        // N of one MMA
+constexpr int kFwdTileCols = 512;  // vocabulary columns per tile
 constexpr int kFwdCG = 2;
-constexpr int kFwdStages = 6;
-constexpr int kFwdEpiWarps = 4;
+constexpr int kFwdStages = 4;
+constexpr int kFwdEpiWarps = 8;
+// Gradient pass of the backward: CTA pairs on 256 x 256 tiles, 6 stages of
+// 32 KB, double-buffered accumulators, four epilogue warps.
+constexpr int kGradBN = 256;
+constexpr int kGradCG = 2;
+constexpr int kGradStages = 6;
+constexpr int kGradEpiWarps = 4;
 // Tile shape of the KL pipeline (student and teacher accumulators per tile):
 // CTA pairs on 256-row x 256-column tiles, 3 stages of 64 KB per CTA, one
 // accumulator buffer (2 x 256 TMEM columns).  Against 128-column tiles with

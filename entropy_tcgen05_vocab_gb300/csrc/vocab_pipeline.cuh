@@ -60,12 +60,17 @@ __host__ __device__ constexpr int pipe_threads(int epiw) { return 64 + 32 * epiw
 // [A_0 .. A_{NOPS-1} | B_0 .. B_{NOPS-1}] with B_i holding BN / CG rows; TMEM:
 // NACC accumulator buffers (2: the epilogue of one tile overlaps the MMAs of
 // the next) of NOPS x BN columns (GEMM op at column offset op * BN).
-template <int BN, int STAGES, int NOPS = 1, int CG = 1, int NACC = 2>
+// SHARED_A: the NOPS GEMMs share one A operand and take their B operands from
+// consecutive BN-row blocks of the same matrix, so the vocabulary tile is
+// NOPS x BN columns wide (one A load feeds NOPS MMAs of N = BN).
+template <int BN, int STAGES, int NOPS = 1, int CG = 1, int NACC = 2, bool SHARED_A = false>
 struct PipeLayout {
   static constexpr int kABytes = kBM * kBK * 2;
+  static constexpr int kAOps = SHARED_A ? 1 : NOPS;
   static constexpr int kBRows = BN / CG;
   static constexpr int kBBytes = kBRows * kBK * 2;
-  static constexpr int kStageBytes = NOPS * (kABytes + kBBytes);
+  static constexpr int kStageBytes = kAOps * kABytes + NOPS * kBBytes;
+  static constexpr int kTileCols = SHARED_A ? NOPS * BN : BN;  // vocabulary columns per tile
   static constexpr int kAccCols = NOPS * BN;
   static constexpr int kTmemCols = NACC * kAccCols;
   static_assert(NACC == 1 || NACC == 2, "one or two accumulator buffers");
@@ -119,7 +124,8 @@ __device__ __forceinline__ bool last_arrival(uint32_t *counter, uint32_t expecte
   return last != 0;
 }
 
-template <int BN, int STAGES, int NOPS, class Epi, int CG = 1, int NACC = 2, int EPIW = 4>
+template <int BN, int STAGES, int NOPS, class Epi, int CG = 1, int NACC = 2, int EPIW = 4,
+          bool SHARED_A = false>
 __global__ void __launch_bounds__(pipe_threads(EPIW), 1)
     vocab_pipeline_kernel(const __grid_constant__ CUtensorMap tmA0,
                           const __grid_constant__ CUtensorMap tmB0,
@@ -127,11 +133,11 @@ __global__ void __launch_bounds__(pipe_threads(EPIW), 1)
                           const __grid_constant__ CUtensorMap tmB1, const Schedule sch,
                           const uint32_t idesc, const typename Epi::Params ep,
                           uint32_t *status) {
-  using L = PipeLayout<BN, STAGES, NOPS, CG, NACC>;
+  using L = PipeLayout<BN, STAGES, NOPS, CG, NACC, SHARED_A>;
   static_assert(NOPS == 1 || NOPS == 2, "one or two GEMMs per tile");
   static_assert(EPIW == 4 || EPIW == 8, "four or eight epilogue warps");
   constexpr int kHalves = EPIW / 4;          // warps sharing one TMEM lane quarter
-  constexpr int kWarpCols = BN / kHalves;    // vocabulary columns one epilogue warp folds
+  constexpr int kWarpCols = L::kTileCols / kHalves;  // vocabulary columns one epilogue warp folds
   constexpr bool kPair = CG == 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -197,29 +203,32 @@ __global__ void __launch_bounds__(pipe_threads(EPIW), 1)
       sch.item(it, mt, sp, vt0, vt1);
       const int arow = mt * (kBM * CG) + static_cast<int>(rank) * kBM;
       for (int vt = vt0; ok && vt < vt1; ++vt) {
-        const int brow = vt * BN + static_cast<int>(rank) * L::kBRows;
+        const int brow = vt * L::kTileCols + static_cast<int>(rank) * L::kBRows;
         for (int kb = 0; kb < sch.k_blocks; ++kb) {
           if (lane == 0) ok = mbar_wait(&empty[stage], phase ^ 1u, abort_flag);
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
           if (lane == 0) {
             uint8_t *sa = smem + stage * L::kStageBytes;
-            uint8_t *sb = sa + NOPS * L::kABytes;
+            uint8_t *sb = sa + L::kAOps * L::kABytes;
             if (leader) mbar_arrive_expect_tx(&full[stage], CG * L::kStageBytes);
+            // second GEMM: its own A and B maps, or (SHARED_A) the next BN rows of B
+            const CUtensorMap *tb1 = SHARED_A ? &tmB0 : &tmB1;
+            const int brow1 = SHARED_A ? brow + BN : brow;
             if (kPair) {
               const uint32_t fb = full_dst + stage * 8;
               tma_load_2d_pair(sa, &tmA0, fb, kb * kBK, arow);
               tma_load_2d_pair(sb, &tmB0, fb, kb * kBK, brow);
               if (NOPS == 2) {
-                tma_load_2d_pair(sa + L::kABytes, &tmA1, fb, kb * kBK, arow);
-                tma_load_2d_pair(sb + L::kBBytes, &tmB1, fb, kb * kBK, brow);
+                if (!SHARED_A) tma_load_2d_pair(sa + L::kABytes, &tmA1, fb, kb * kBK, arow);
+                tma_load_2d_pair(sb + L::kBBytes, tb1, fb, kb * kBK, brow1);
               }
             } else {
               tma_load_2d(sa, &tmA0, &full[stage], kb * kBK, arow);
               tma_load_2d(sb, &tmB0, &full[stage], kb * kBK, brow);
               if (NOPS == 2) {
-                tma_load_2d(sa + L::kABytes, &tmA1, &full[stage], kb * kBK, arow);
-                tma_load_2d(sb + L::kBBytes, &tmB1, &full[stage], kb * kBK, brow);
+                if (!SHARED_A) tma_load_2d(sa + L::kABytes, &tmA1, &full[stage], kb * kBK, arow);
+                tma_load_2d(sb + L::kBBytes, tb1, &full[stage], kb * kBK, brow1);
               }
             }
           }
@@ -271,13 +280,13 @@ __global__ void __launch_bounds__(pipe_threads(EPIW), 1)
             tc_fence_after();
             if (lane == 0) {
               const uint32_t a0 = smem_u32(smem + stage * L::kStageBytes);
-              const uint32_t b0 = a0 + NOPS * L::kABytes;
+              const uint32_t b0 = a0 + L::kAOps * L::kABytes;
 #pragma unroll
               for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
 #pragma unroll
                 for (int op = 0; op < NOPS; ++op) {
-                  const uint64_t ad =
-                      sdesc_sw128(a0 + op * L::kABytes + kk * kUmmaK * 2, 16, 1024);
+                  const uint64_t ad = sdesc_sw128(
+                      a0 + (SHARED_A ? 0 : op) * L::kABytes + kk * kUmmaK * 2, 16, 1024);
                   const uint64_t bd =
                       sdesc_sw128(b0 + op * L::kBBytes + kk * kUmmaK * 2, 16, 1024);
                   if (kPair)
@@ -344,7 +353,7 @@ __global__ void __launch_bounds__(pipe_threads(EPIW), 1)
         if (!ok) break;
         tc_fence_after();
         epi.tile(tmem_base + lane_off + static_cast<uint32_t>(acc * L::kAccCols),
-                 vt * BN + half * kWarpCols, kWarpCols / 32);
+                 vt * L::kTileCols + half * kWarpCols, kWarpCols / 32);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
