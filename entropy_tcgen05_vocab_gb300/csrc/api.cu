@@ -617,7 +617,7 @@ flp_status flp_backward(const flp_shape *s, const void *h, const void *W, const 
     const void *Ar = eb + static_cast<size_t>(r0) * lda * esz;
     // 1. G = d loss / d z for the chunk's rows
     GradArgs ga{};
-    const Plan p = plan_cached(rc, s->V, s->H, kGradBN, grad_units(dev.sms), 128 * kGradCG);
+    const Plan p = plan_cached(rc, s->V, s->H, kGradTileCols, grad_units(dev.sms), 128 * kGradCG);
     if ((st = make_map(&ga.tmA, s->dtype, Ar, s->H, rc, lda, 64, 128)) != FLP_OK) return st;
     if ((st = make_map(&ga.tmB, s->dtype, W, s->H, s->V, s->ld_w, 64, kGradBN / kGradCG)) != FLP_OK)
       return st;

@@ -220,8 +220,9 @@ struct DwEpi {
 };
 
 // ---------------------------------------------------------------- launchers
-using GradLayout = PipeLayout<kGradBN, kGradStages, 1, kGradCG>;
-#define GRAD_KERNEL vocab_pipeline_kernel<kGradBN, kGradStages, 1, GradEpi, kGradCG, 2, kGradEpiWarps>
+static_assert(kGradTileCols == 2 * kGradBN, "two MMAs per tile");
+using GradLayout = PipeLayout<kGradBN, kGradStages, 2, kGradCG, 1, true>;
+#define GRAD_KERNEL vocab_pipeline_kernel<kGradBN, kGradStages, 2, GradEpi, kGradCG, 1, kGradEpiWarps, true>
 constexpr int kGradThreads = pipe_threads(kGradEpiWarps);
 
 cudaError_t launch_grad(const GradArgs &a, cudaStream_t stream) {

@@ -24,12 +24,13 @@ constexpr int kFwdTileCols = 512;  // vocabulary columns per tile
 constexpr int kFwdCG = 2;
 constexpr int kFwdStages = 4;
 constexpr int kFwdEpiWarps = 8;
-// Gradient pass of the backward: CTA pairs on 256 x 256 tiles, 6 stages of
-// 32 KB, double-buffered accumulators, four epilogue warps.
+// Gradient pass of the backward: the same 256 x 512 shared-A tiles, one
+// accumulator buffer, eight epilogue warps, 4 stages of 48 KB.
 constexpr int kGradBN = 256;
+constexpr int kGradTileCols = 512;
 constexpr int kGradCG = 2;
-constexpr int kGradStages = 6;
-constexpr int kGradEpiWarps = 4;
+constexpr int kGradStages = 4;
+constexpr int kGradEpiWarps = 8;
 // Tile shape of the KL pipeline (student and teacher accumulators per tile):
 // CTA pairs on 256-row x 256-column tiles, 3 stages of 64 KB per CTA, one
 // accumulator buffer (2 x 256 TMEM columns).  Against 128-column tiles with
