@@ -645,7 +645,7 @@ flp_status flp_backward(const flp_shape *s, const void *h, const void *W, const 
     da.M = rc;
     da.N = static_cast<int>(s->H);
     da.K = static_cast<int>(s->V);
-    da.grid = gemm_cta_group() * std::min(gemm_tiles(da.M, da.N), gemm_units(dev.sms));
+    da.grid = gemm_cta_group() * std::min(dh_gemm_tiles(da.M, da.N), gemm_units(dev.sms));
     da.bf16 = ga.bf16;
     da.status = status;
     da.r0 = static_cast<int>(r0);
@@ -661,7 +661,7 @@ flp_status flp_backward(const flp_shape *s, const void *h, const void *W, const 
     wa.M = static_cast<int>(s->V);
     wa.N = static_cast<int>(s->H);
     wa.K = rc;
-    wa.grid = gemm_cta_group() * std::min(gemm_tiles(wa.M, wa.N), gemm_units(dev.sms));
+    wa.grid = gemm_cta_group() * std::min(dw_gemm_tiles(wa.M, wa.N), gemm_units(dev.sms));
     wa.bf16 = ga.bf16;
     wa.status = status;
     wa.dW = dW;

@@ -1,6 +1,6 @@
 // gemm_pipeline.cuh -- persistent tcgen05 GEMM D[M,N] = A[M,K] B[N,K]^T with
-// (128 x CG) x 256 output tiles and an epilogue policy, for the two GEMMs of
-// the backward (dh = G W and dW = G^T h).
+// (128 x CG) x 256 or (128 x CG) x 512 output tiles and an epilogue policy,
+// for the two GEMMs of the backward (dh = G W and dW = G^T h).
 //
 // Operands may be K-major (K contiguous) or MN-major (M or N contiguous):
 //   K-major  : one TMA box {64 (K), rows} per stage, 128-byte swizzle rows
@@ -10,12 +10,11 @@
 //              elements; descriptor lbo = 8192 (next 64-element M/N block =
 //              next box), sbo = 1024 (next 8 K-rows), K step of 16 = +2048 B.
 // Roles are those of the vocabulary pipeline: warp 0 TMA producer, warp 1
-// TMEM allocation + MMA issue, warps 2-5 epilogue; double-buffered
-// 256-column TMEM accumulators.  With CG = 2 (cluster of 2) the pair computes
-// a 256 x 256 tile: each CTA loads its 128 rows of A and 128 of the 256
-// columns of B, the leader issues tcgen05.mma.cta_group::2, and each CTA's
-// TMEM holds its 128 output rows (the same protocol as the vocabulary
-// pipeline).
+// TMEM allocation + MMA issue, then the epilogue warps.  With CG = 2 (cluster
+// of 2) the pair computes a 256-row tile: each CTA loads its 128 rows of A and
+// its half of every 256-column block of B, the leader issues
+// tcgen05.mma.cta_group::2, and each CTA's TMEM holds its 128 output rows (the
+// same protocol as the vocabulary pipeline).
 #pragma once
 
 #include <cstdint>
@@ -32,23 +31,35 @@ struct GemmShape {
   int m_tiles, n_tiles, tiles, k_blocks;
 };
 
-template <int CG>
+// WIDE = false: 256-column output tiles, double-buffered accumulators, 4
+// epilogue warps.  WIDE = true: 512-column output tiles made of two N = 256
+// MMAs sharing the A operand, one accumulator buffer (512 TMEM columns), 8
+// epilogue warps each storing 256 columns.
+template <int CG, bool WIDE = false>
 struct GemmCfg {
-  static constexpr int kStages = CG == 2 ? 6 : 4;
-  using L = PipeLayout<kGemmBN, kStages, 1, CG, 2>;
+  static constexpr int kStages = WIDE ? 4 : (CG == 2 ? 6 : 4);
+  static constexpr int kNops = WIDE ? 2 : 1;
+  static constexpr int kNacc = WIDE ? 1 : 2;
+  static constexpr int kEpiw = WIDE ? 8 : 4;
+  static constexpr int kTileN = kNops * kGemmBN;
+  using L = PipeLayout<kGemmBN, kStages, kNops, CG, kNacc, true>;
 };
 
 // Epi must provide: struct Params; Epi(const Params&);
-//   void tile(uint32_t taddr, int row0, int nt, int lg, int lane)
-// where row0 is the first output row held by this CTA's TMEM for the tile.
-template <bool A_MN, bool B_MN, class Epi, int CG = 1>
-__global__ void __launch_bounds__(kPipeThreads, 1)
+//   void tile(uint32_t taddr, int row0, int col0, int ncols)
+// where row0 is this thread's output row and [col0, col0 + ncols) the
+// output columns this warp stores from taddr on.
+template <bool A_MN, bool B_MN, class Epi, int CG = 1, bool WIDE = false>
+__global__ void __launch_bounds__(pipe_threads(GemmCfg<CG, WIDE>::kEpiw), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const GemmShape g, const uint32_t idesc, const typename Epi::Params ep,
                 uint32_t *status) {
-  using L = typename GemmCfg<CG>::L;
-  constexpr int STAGES = GemmCfg<CG>::kStages;
+  using C = GemmCfg<CG, WIDE>;
+  using L = typename C::L;
+  constexpr int STAGES = C::kStages;
   constexpr int BN = kGemmBN;
+  constexpr int NOPS = C::kNops;
+  constexpr int EPIW = C::kEpiw;
   constexpr bool kPair = CG == 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -75,7 +86,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], kEpiWarps * CG);
+      mbar_init(&tempty[a], EPIW * CG);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -107,7 +118,8 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     for (int t = unit; ok && t < g.tiles; t += num_units) {
       const int mt = t / g.n_tiles, nt = t - (t / g.n_tiles) * g.n_tiles;
       const int arow = mt * (kBM * CG) + static_cast<int>(rank) * kBM;   // M offset
-      const int bcol = nt * BN + static_cast<int>(rank) * L::kBRows;     // N offset
+      // N offset of this CTA's share of MMA op 0 (op k adds k * BN)
+      const int bcol = nt * C::kTileN + static_cast<int>(rank) * L::kBRows;
       for (int kb = 0; kb < g.k_blocks; ++kb) {
         if (lane == 0) ok = mbar_wait(&empty[stage], phase ^ 1u, abort_flag);
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -129,12 +141,16 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
           } else {
             load(sa, &tmA, kb * kBK, arow);
           }
-          if (B_MN) {
 #pragma unroll
-            for (int i = 0; i < L::kBRows / 64; ++i)
-              load(sb + i * 8192, &tmB, bcol + i * 64, kb * kBK);
-          } else {
-            load(sb, &tmB, kb * kBK, bcol);
+          for (int op = 0; op < NOPS; ++op) {
+            uint8_t *sbo = sb + op * L::kBBytes;
+            if (B_MN) {
+#pragma unroll
+              for (int i = 0; i < L::kBRows / 64; ++i)
+                load(sbo + i * 8192, &tmB, bcol + op * BN + i * 64, kb * kBK);
+            } else {
+              load(sbo, &tmB, kb * kBK, bcol + op * BN);
+            }
           }
         }
         armed |= 1u << stage;
@@ -168,7 +184,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * L::kAccCols);
         for (int kb = 0; kb < g.k_blocks; ++kb) {
           if (lane == 0) ok = mbar_wait(&full[stage], phase, abort_flag);
           ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -181,12 +197,16 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
               const uint64_t ad = A_MN ? sdesc_sw128(a0 + kk * 2048, 8192, 1024)
                                        : sdesc_sw128(a0 + kk * kUmmaK * 2, 16, 1024);
-              const uint64_t bd = B_MN ? sdesc_sw128(b0 + kk * 2048, 8192, 1024)
-                                       : sdesc_sw128(b0 + kk * kUmmaK * 2, 16, 1024);
-              if (kPair)
-                mma_f16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
-              else
-                mma_f16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+#pragma unroll
+              for (int op = 0; op < NOPS; ++op) {
+                const uint32_t bo = b0 + op * L::kBBytes;
+                const uint64_t bd = B_MN ? sdesc_sw128(bo + kk * 2048, 8192, 1024)
+                                         : sdesc_sw128(bo + kk * kUmmaK * 2, 16, 1024);
+                if (kPair)
+                  mma_f16_pair(d_tmem + op * BN, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                else
+                  mma_f16(d_tmem + op * BN, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+              }
             }
             if (kPair)
               mma_commit_pair(&empty[stage], 0x3);
@@ -207,7 +227,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             mma_commit(&tfull[acc]);
         }
         __syncwarp();
-        acc ^= 1;
+        if (C::kNacc == 2) acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }
       if (!ok && lane == 0) {
@@ -223,7 +243,10 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int lg = warp & 3;
-    const uint32_t lane_off = static_cast<uint32_t>(lg * 32) << 16;
+    const int half = (warp - 2) / 4;                    // column half (8 epilogue warps)
+    constexpr int kWarpCols = C::kTileN / (EPIW / 4);  // output columns per warp
+    const uint32_t lane_off = (static_cast<uint32_t>(lg * 32) << 16) +
+                              static_cast<uint32_t>(half * kWarpCols);
     const uint32_t tempty_dst = kPair ? mapa_shared(smem_u32(tempty), 0) : smem_u32(tempty);
     Epi epi(ep);
     int acc = 0;
@@ -235,8 +258,9 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      epi.tile(tmem_base + lane_off + static_cast<uint32_t>(acc * BN),
-               mt * (kBM * CG) + static_cast<int>(rank) * kBM, nt, lg, lane);
+      epi.tile(tmem_base + lane_off + static_cast<uint32_t>(acc * L::kAccCols),
+               mt * (kBM * CG) + static_cast<int>(rank) * kBM + lg * 32 + lane,
+               nt * C::kTileN + half * kWarpCols, kWarpCols);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -245,7 +269,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
         else
           mbar_arrive(&tempty[acc]);
       }
-      acc ^= 1;
+      if (C::kNacc == 2) acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
     if (!ok && lane == 0) record_timeout<CG>(status, abort_flag);

@@ -118,7 +118,8 @@ cudaError_t launch_kl(const KlArgs &a, cudaStream_t stream);
 cudaError_t launch_grad(const GradArgs &a, cudaStream_t stream);
 cudaError_t launch_dh_gemm(const GemmArgs &a, cudaStream_t stream);
 cudaError_t launch_dw_gemm(const GemmArgs &a, cudaStream_t stream);
-int gemm_tiles(int M, int N);
+int dh_gemm_tiles(int M, int N);
+int dw_gemm_tiles(int M, int N);
 int gemm_cta_group();
 int gemm_units(int num_sms);
 int fwd_smem_bytes();
