@@ -199,3 +199,25 @@ def test_forward_scoring_workload_sampled():
 
 def test_long_packed_workload_sampled():
     _full_size(2)
+
+
+@pytest.mark.parametrize("T,H,V", [
+    (100, 2048, 262144),   # one row tile, 512 vocabulary tiles: the most splits
+    (20000, 128, 512),     # 79 row tiles, one vocabulary tile
+    (3000, 8192, 1000),    # long contraction, V inside two 512-column tiles
+])
+def test_planner_extremes(T, H, V):
+    w = workloads.WORKLOADS[0].scaled(T=T, H=H, V=V, seed=T + V, w_std=0.03)
+    d = workloads.make(w, device="cuda")
+    rows = None
+    if T > 1000:   # oracle on a sample of rows, outputs compared there
+        rows = torch.from_numpy(workloads.sample_rows(T, 300, seed=7)).cuda()
+    _run_and_compare(d["h"], d["W"], d["targets"], rows, 0.8)
+
+
+def test_kl_at_the_planner_extremes():
+    w = workloads.WORKLOADS[3].scaled(T=64, H=1024, V=131072, seed=51)
+    d = workloads.make(w, device="cuda")
+    kl = flp.kl_divergence(d["h_s"], d["W_s"], d["h_t"], d["W_t"])
+    want = coracle.kl(d["h_s"].cpu(), d["W_s"].cpu(), d["h_t"].cpu(), d["W_t"].cpu(), None, "bf16")
+    _check(kl, want, "kl")
