@@ -421,6 +421,35 @@ def run_ours(args):
             except Exception as e:  # a workload whose op is not available is reported, not fatal
                 extra[workloads.WORKLOADS[wid].name] = {"unavailable": str(e).splitlines()[0][:200]}
             torch.cuda.empty_cache()
+        # K-candidate scoring (4 target tokens per row) on the main workload's inputs
+        if d["workload"].kind == "fwd":
+            try:
+                w = d["workload"]
+                K = 4
+                g = torch.Generator(device=device)
+                g.manual_seed(w.seed * 100 + 30)
+                tk = torch.randint(0, w.V, (w.T, K), generator=g, device=device)
+                tk[:, 0] = d["targets"]
+                shape = flp.make_shape(w.T, w.H, w.V, n, d["h"].dtype)
+                wsk = torch.empty(flp.workspace_size(shape, 0), dtype=torch.uint8, device=device)
+                for _ in range(3):
+                    flp.logprob_entropy_k(d["h"], d["W"], tk, d["row_idx"], d["tau"], workspace=wsk)
+                steps = 20
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                torch.cuda.synchronize(device)
+                a.record()
+                for _ in range(steps):
+                    flp.logprob_entropy_k(d["h"], d["W"], tk, d["row_idx"], d["tau"], workspace=wsk)
+                b.record()
+                torch.cuda.synchronize(device)
+                tms = max_over_ranks(a.elapsed_time(b), world, device)
+                extra[w.name + "-k4-candidates"] = {
+                    "config": dict(describe(d), candidates_per_row=K),
+                    "scored_tokens_per_s": job_throughput(n, steps, tms, world),
+                    "ms_per_step": tms / steps,
+                    "tflops": fl / (tms / steps / 1e3) / 1e12}
+            except Exception as e:  # reported, not fatal
+                extra[d["workload"].name + "-k4-candidates"] = {"unavailable": str(e)[:200]}
         out["workloads"] = extra
 
     if rank == 0 and world == 1 and not args.no_cpu:

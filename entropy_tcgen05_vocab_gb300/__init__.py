@@ -18,7 +18,8 @@ import torch
 
 from . import _build
 
-__all__ = ["lib", "build", "workspace_size", "logprob_entropy", "kl_divergence", "backward",
+__all__ = ["lib", "build", "workspace_size", "logprob_entropy", "logprob_entropy_k",
+           "kl_divergence", "backward",
            "read_device_status", "plan", "set_kernel_events", "row_chunks", "FusedLogProbEntropy", "FlpError",
            "OP_LOGPROB_ENTROPY", "OP_KL", "OP_BACKWARD"]
 
@@ -82,6 +83,9 @@ def lib():
     L.flp_plan_scoring.argtypes = [shp, ctypes.c_int, ctypes.c_int32, ctypes.POINTER(FlpPlan)]
     L.flp_row_chunks.argtypes = [i64, i64, ctypes.POINTER(ctypes.c_int64), i64]
     L.flp_row_chunks.restype = i64
+    L.flp_logprob_entropy_k.argtypes = [shp, vp, vp, vp, ctypes.c_int32, vp, f32, vp, vp, vp, vp,
+                                        vp, sz, vp]
+    L.flp_logprob_entropy_k.restype = ctypes.c_int
     L.flp_logprob_entropy_noalloc.argtypes = [shp, vp, vp, vp, vp, f32, vp, vp, vp, vp, vp]
     L.flp_logprob_entropy_noalloc.restype = ctypes.c_int
     L.flp_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp, vp]
@@ -210,6 +214,31 @@ def logprob_entropy(h, W, targets, row_idx=None, temperature=1.0, *, return_stat
                                          _ptr(ez), _ptr(ws), ws.numel(), _stream(dev)))
     if return_stats:
         return logp, ent, lse, ez
+    return logp, ent
+
+
+def logprob_entropy_k(h, W, targets, row_idx=None, temperature=1.0, *, workspace=None):
+    """K target tokens per scored row: targets int64 [T, K] (K <= 8) indexed by
+    h row.  Returns (logp [n, K], ent [n]) float32."""
+    _matrix(h, "h")
+    _matrix(W, "W")
+    dev = h.device
+    if W.device != dev or W.dtype != h.dtype or W.shape[1] != h.shape[1]:
+        raise TypeError("W must match h in device, dtype and hidden size")
+    if not isinstance(targets, torch.Tensor) or targets.dim() != 2 or targets.device != dev:
+        raise TypeError("targets must be a [T, K] tensor on %s" % dev)
+    tg = targets.to(torch.int64).contiguous()
+    K = tg.shape[1]
+    ri = _index(row_idx, "row_idx", dev)
+    n = h.shape[0] if ri is None else ri.numel()
+    shape = make_shape(h.shape[0], h.shape[1], W.shape[0], n, h.dtype, h.stride(0), W.stride(0))
+    logp = torch.empty((n, K), dtype=torch.float32, device=dev)
+    ent = torch.empty(n, dtype=torch.float32, device=dev)
+    ws = _workspace(shape, OP_LOGPROB_ENTROPY, dev, workspace)
+    with torch.cuda.device(dev):
+        _check(lib().flp_logprob_entropy_k(ctypes.byref(shape), _ptr(h), _ptr(W), _ptr(tg), K,
+                                           _ptr(ri), float(temperature), _ptr(logp), _ptr(ent),
+                                           None, None, _ptr(ws), ws.numel(), _stream(dev)))
     return logp, ent
 
 

@@ -118,7 +118,7 @@ Layout layout_for(const flp_shape *s, flp_op op) {
     L.pm2 = take(sm * n * 4);
     L.ps2 = take(sm * n * 4);
   } else {
-    L.zt = take(n * 4);
+    L.zt = take(n * kMaxTargets * 4);  // raw target logits, up to kMaxTargets per row
   }
   L.hs = take(n * static_cast<size_t>(s->H) * 2);
   if (op == FLP_OP_KL) L.hs2 = take(n * static_cast<size_t>(s->H) * 2);
@@ -332,6 +332,73 @@ flp_status noalloc_scratch(void **out) {
   return FLP_OK;
 }
 
+flp_status logprob_impl(const flp_shape *s, const void *h, const void *W, const int64_t *targets,
+                        int K, const int64_t *row_idx, float temperature, float *out_logp,
+                        float *out_ent, float *out_lse, float *out_ez, void *ws, size_t ws_bytes,
+                        flp_stream_t stream) {
+  g_err[0] = 0;
+  const KernelEvents ev;
+  flp_status st = check_common(s, FLP_OP_LOGPROB_ENTROPY, ws, ws_bytes);
+  if (st != FLP_OK) return st;
+  if (!(std::isfinite(temperature) && temperature > 0.f))
+    return fail(FLP_ERR_INVALID_ARG, "temperature must be finite and > 0");
+  if (K < 1 || K > kMaxTargets)
+    return fail(FLP_ERR_INVALID_ARG, "K must be within 1 .. %d", kMaxTargets);
+  if (s->n_rows == 0) return FLP_OK;
+  if (!row_idx && s->n_rows != s->T)
+    return fail(FLP_ERR_INVALID_ARG, "row_idx is NULL but n_rows != T");
+  if (!h || !W || !targets || !out_logp || !out_ent)
+    return fail(FLP_ERR_INVALID_ARG, "h, W, targets, out_logp and out_ent are required");
+  if (!aligned16(h) || !aligned16(W)) return fail(FLP_ERR_INVALID_ARG, "h and W must be 16-byte aligned");
+  DeviceInfo dev;
+  if ((st = device_info(&dev)) != FLP_OK) return st;
+
+  const Layout L = layout_for(s, FLP_OP_LOGPROB_ENTROPY);
+  const Plan p = plan_cached(s->n_rows, s->V, s->H, kFwdTileCols, fwd_units(dev.sms), 128 * kFwdCG);
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  FwdArgs a{};
+  const void *A = h;
+  int64_t lda = s->ld_h;
+  if (row_idx) {
+    A = at<void>(ws, L.hs);
+    lda = s->H;
+  }
+  if ((st = make_map(&a.tmA, s->dtype, A, s->H, s->n_rows, lda, 64, 128)) != FLP_OK) return st;
+  if ((st = make_map(&a.tmB, s->dtype, W, s->H, s->V, s->ld_w, 64, kFwdBN / kFwdCG)) != FLP_OK)
+    return st;
+  a.sch = p.sch;
+  a.grid = p.grid * kFwdCG;
+  a.bf16 = s->dtype == FLP_BF16;
+  a.targets = targets;
+  a.K = K;
+  a.row_idx = row_idx;
+  a.T = s->T;
+  a.inv_tau = 1.0f / temperature;
+  a.scale_log2 = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+  a.pm = at<float>(ws, L.pm);
+  a.ps = at<float>(ws, L.ps);
+  a.pb = at<float>(ws, L.pb);
+  a.zt = at<float>(ws, L.zt);
+  a.counters = at<uint32_t>(ws, L.cnt);
+  a.out_logp = out_logp;
+  a.out_ent = out_ent;
+  a.out_lse = out_lse;
+  a.out_ez = out_ez;
+  a.status = at<uint32_t>(ws, L.status);
+
+  // status words and row-group counters are adjacent: one clear
+  cudaError_t e = cudaMemsetAsync(a.status, 0, L.cnt + L.cnt_bytes - L.status, cs);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(status)");
+  if (row_idx) {
+    e = launch_gather(h, s->ld_h, row_idx, s->n_rows, s->T, s->H, at<void>(ws, L.hs), dev.sms, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "gather launch");
+  }
+  if ((e = ev.start(cs)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+  if ((e = launch_fwd_scoring(a, cs)) != cudaSuccess) return cuda_fail(e, "scoring launch");
+  if ((e = ev.stop(cs)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+  return FLP_OK;
+}
+
 }  // namespace
 }  // namespace flp
 
@@ -408,64 +475,17 @@ flp_status flp_logprob_entropy(const flp_shape *s, const void *h, const void *W,
                                const int64_t *targets, const int64_t *row_idx, float temperature,
                                float *out_logp, float *out_ent, float *out_lse, float *out_ez,
                                void *ws, size_t ws_bytes, flp_stream_t stream) {
-  g_err[0] = 0;
-  const KernelEvents ev;
-  flp_status st = check_common(s, FLP_OP_LOGPROB_ENTROPY, ws, ws_bytes);
-  if (st != FLP_OK) return st;
-  if (!(std::isfinite(temperature) && temperature > 0.f))
-    return fail(FLP_ERR_INVALID_ARG, "temperature must be finite and > 0");
-  if (s->n_rows == 0) return FLP_OK;
-  if (!row_idx && s->n_rows != s->T)
-    return fail(FLP_ERR_INVALID_ARG, "row_idx is NULL but n_rows != T");
-  if (!h || !W || !targets || !out_logp || !out_ent)
-    return fail(FLP_ERR_INVALID_ARG, "h, W, targets, out_logp and out_ent are required");
-  if (!aligned16(h) || !aligned16(W)) return fail(FLP_ERR_INVALID_ARG, "h and W must be 16-byte aligned");
-  DeviceInfo dev;
-  if ((st = device_info(&dev)) != FLP_OK) return st;
+  return logprob_impl(s, h, W, targets, 1, row_idx, temperature, out_logp, out_ent, out_lse, out_ez,
+                      ws, ws_bytes, stream);
+}
 
-  const Layout L = layout_for(s, FLP_OP_LOGPROB_ENTROPY);
-  const Plan p = plan_cached(s->n_rows, s->V, s->H, kFwdTileCols, fwd_units(dev.sms), 128 * kFwdCG);
-  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  FwdArgs a{};
-  const void *A = h;
-  int64_t lda = s->ld_h;
-  if (row_idx) {
-    A = at<void>(ws, L.hs);
-    lda = s->H;
-  }
-  if ((st = make_map(&a.tmA, s->dtype, A, s->H, s->n_rows, lda, 64, 128)) != FLP_OK) return st;
-  if ((st = make_map(&a.tmB, s->dtype, W, s->H, s->V, s->ld_w, 64, kFwdBN / kFwdCG)) != FLP_OK)
-    return st;
-  a.sch = p.sch;
-  a.grid = p.grid * kFwdCG;
-  a.bf16 = s->dtype == FLP_BF16;
-  a.targets = targets;
-  a.row_idx = row_idx;
-  a.T = s->T;
-  a.inv_tau = 1.0f / temperature;
-  a.scale_log2 = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
-  a.pm = at<float>(ws, L.pm);
-  a.ps = at<float>(ws, L.ps);
-  a.pb = at<float>(ws, L.pb);
-  a.zt = at<float>(ws, L.zt);
-  a.counters = at<uint32_t>(ws, L.cnt);
-  a.out_logp = out_logp;
-  a.out_ent = out_ent;
-  a.out_lse = out_lse;
-  a.out_ez = out_ez;
-  a.status = at<uint32_t>(ws, L.status);
-
-  // status words and row-group counters are adjacent: one clear
-  cudaError_t e = cudaMemsetAsync(a.status, 0, L.cnt + L.cnt_bytes - L.status, cs);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(status)");
-  if (row_idx) {
-    e = launch_gather(h, s->ld_h, row_idx, s->n_rows, s->T, s->H, at<void>(ws, L.hs), dev.sms, cs);
-    if (e != cudaSuccess) return cuda_fail(e, "gather launch");
-  }
-  if ((e = ev.start(cs)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-  if ((e = launch_fwd_scoring(a, cs)) != cudaSuccess) return cuda_fail(e, "scoring launch");
-  if ((e = ev.stop(cs)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-  return FLP_OK;
+flp_status flp_logprob_entropy_k(const flp_shape *s, const void *h, const void *W,
+                                 const int64_t *targets, int32_t K, const int64_t *row_idx,
+                                 float temperature, float *out_logp, float *out_ent,
+                                 float *out_lse, float *out_ez, void *ws, size_t ws_bytes,
+                                 flp_stream_t stream) {
+  return logprob_impl(s, h, W, targets, K, row_idx, temperature, out_logp, out_ent, out_lse, out_ez,
+                      ws, ws_bytes, stream);
 }
 
 flp_status flp_kl(const flp_shape *s, const void *h_s, const void *W_s, const void *h_t,
@@ -589,6 +609,7 @@ flp_status flp_backward(const flp_shape *s, const void *h, const void *W, const 
     a.grid = p.grid * kFwdCG;
     a.bf16 = s->dtype == FLP_BF16;
     a.targets = targets;
+    a.K = 1;
     a.row_idx = row_idx;
     a.T = s->T;
     a.inv_tau = inv_tau;

@@ -46,40 +46,50 @@ __global__ void gather_rows_kernel(const uint4 *__restrict__ h, int64_t ld_h16,
 }
 
 // ---------------------------------------------------------------- epilogue
+// KMAX = largest number of target tokens per row the instantiation handles
+// (1 for log-prob + entropy; up to kMaxTargets for K-candidate scoring).
+template <int KMAX>
 struct LseEpi {
   struct Params {
-    const int64_t *targets;  // [T], by h row
+    const int64_t *targets;  // [T, K], by h row
+    int K;                   // targets per row, 1 <= K <= KMAX
     const int64_t *row_idx;  // [n] or null
     int64_t T;
     int n;
     int V;
     float sl;                // log2(e) / tau
-    float *pm, *ps, *pb;     // [splits][n] partial m, S, B
-    float *zt;               // [n] raw FP32 logit of the target
+    float *pm, *ps, *pb;     // [slots][n] partial m, S, B
+    float *zt;               // [n, K] raw FP32 logits of the targets
     uint32_t *counters;      // [ceil(n/32)] items finished per 32-row group
-    int splits;
+    int splits;              // partial slots per row
     float inv_tau;
-    float *out_logp, *out_ent, *out_lse, *out_ez;  // [n], any may be null
+    float *out_logp;         // [n, K]
+    float *out_ent, *out_lse, *out_ez;  // [n], any may be null
     uint32_t *status;
   };
   const Params p;
-  float m, s0, s1, b0, b1, zt;
-  int tgt;
-  bool found;
+  float m, s0, s1, b0, b1;
+  int tgt[KMAX];  // -1: no valid target (never matched)
+  int row_;
 
   __device__ __forceinline__ explicit LseEpi(const Params &pp) : p(pp) {}
 
   __device__ __forceinline__ void begin(int /*mt*/, int row) {
     m = -FLT_MAX;
     s0 = s1 = b0 = b1 = 0.f;
-    zt = 0.f;
-    found = false;
-    tgt = -1;
+    row_ = row;
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) tgt[k] = -1;
     if (row < p.n) {
       const int64_t r = p.row_idx ? p.row_idx[row] : row;
       if (r >= 0 && r < p.T) {
-        const int64_t t = p.targets[r];
-        if (t >= 0 && t < p.V) tgt = static_cast<int>(t);
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k) {
+          if (k < p.K) {
+            const int64_t t = p.targets[r * p.K + k];
+            if (t >= 0 && t < p.V) tgt[k] = static_cast<int>(t);
+          }
+        }
       }
     }
   }
@@ -145,13 +155,16 @@ struct LseEpi {
         fold_full(x);
       else
         fold_masked(x, p.V - cb);
-      const int rel = tgt - cb;
-      if (static_cast<unsigned>(rel) < 32u) {
-        float t = x[0];
+      // each target column lies in exactly one chunk: store its raw logit there
 #pragma unroll
-        for (int j = 1; j < 32; ++j) t = (rel == j) ? x[j] : t;
-        zt = t;
-        found = true;
+      for (int k = 0; k < KMAX; ++k) {
+        const int rel = tgt[k] - cb;
+        if (static_cast<unsigned>(rel) < 32u) {
+          float t = x[0];
+#pragma unroll
+          for (int j = 1; j < 32; ++j) t = (rel == j) ? x[j] : t;
+          p.zt[static_cast<size_t>(row_) * p.K + k] = t;
+        }
       }
     }
   }
@@ -162,7 +175,6 @@ struct LseEpi {
       p.pm[o] = m;
       p.ps[o] = s0 + s1;
       p.pb[o] = b0 + b1;
-      if (found) p.zt[row] = zt;
     }
     // The last warp to finish these 32 rows merges them.
     if (last_arrival(p.counters + (row >> 5), static_cast<uint32_t>(p.splits)) && row < p.n)
@@ -188,21 +200,25 @@ struct LseEpi {
     const float l2s = log2f(S);
     float lse = kLn2 * (M + l2s);
     float ent = kLn2 * (l2s - B / S);
-    float logp;
+    const float qnan = __int_as_float(0x7fc00000);
     const int64_t r = p.row_idx ? p.row_idx[i] : i;
-    if (r < 0 || r >= p.T) {
+    const bool row_ok = r >= 0 && r < p.T;
+    if (!row_ok) {
       atomicAdd(p.status + kStatBadRow, 1u);
-      lse = ent = logp = __int_as_float(0x7fc00000);
-    } else {
-      const int64_t t = p.targets[r];
-      if (t < 0 || t >= p.V) {
-        atomicAdd(p.status + kStatBadTarget, 1u);
-        logp = __int_as_float(0x7fc00000);
-      } else {
-        logp = __ldcg(p.zt + i) * p.inv_tau - lse;
-      }
+      lse = ent = qnan;
     }
-    if (p.out_logp) p.out_logp[i] = logp;
+    for (int k = 0; k < p.K; ++k) {
+      const size_t o = static_cast<size_t>(i) * p.K + k;
+      float logp = qnan;
+      if (row_ok) {
+        const int64_t t = p.targets[r * p.K + k];
+        if (t < 0 || t >= p.V)
+          atomicAdd(p.status + kStatBadTarget, 1u);
+        else
+          logp = __ldcg(p.zt + o) * p.inv_tau - lse;
+      }
+      if (p.out_logp) p.out_logp[o] = logp;
+    }
     if (p.out_ent) p.out_ent[i] = ent;
     if (p.out_lse) p.out_lse[i] = lse;
     if (p.out_ez) p.out_ez[i] = lse - ent;
@@ -224,12 +240,15 @@ cudaError_t launch_gather(const void *h, int64_t ld_h, const int64_t *row_idx, i
 
 static_assert(kFwdTileCols == 2 * kFwdBN, "two MMAs per tile");
 using FwdLayout = PipeLayout<kFwdBN, kFwdStages, 2, kFwdCG, 1, true>;
-#define FWD_KERNEL vocab_pipeline_kernel<kFwdBN, kFwdStages, 2, LseEpi, kFwdCG, 1, kFwdEpiWarps, true>
+#define FWD_KERNEL(KMAX) \
+  vocab_pipeline_kernel<kFwdBN, kFwdStages, 2, LseEpi<KMAX>, kFwdCG, 1, kFwdEpiWarps, true>
 constexpr int kFwdThreads = pipe_threads(kFwdEpiWarps);
 
-cudaError_t launch_fwd_scoring(const FwdArgs &a, cudaStream_t stream) {
-  LseEpi::Params p;
+template <int KMAX>
+static cudaError_t launch_fwd_k(const FwdArgs &a, cudaStream_t stream) {
+  typename LseEpi<KMAX>::Params p;
   p.targets = a.targets;
+  p.K = a.K;
   p.row_idx = a.row_idx;
   p.T = a.T;
   p.n = a.sch.n;
@@ -248,16 +267,22 @@ cudaError_t launch_fwd_scoring(const FwdArgs &a, cudaStream_t stream) {
   p.out_ez = a.out_ez;
   p.status = a.status;
   const uint32_t idesc = idesc_f16(a.bf16, kBM * kFwdCG, kFwdBN, false, false);
-  return launch_persistent(FWD_KERNEL, a.grid, kFwdThreads, FwdLayout::kSmemBytes, kFwdCG, stream, a.tmA,
-                           a.tmB, a.tmA, a.tmB, a.sch, idesc, p, a.status);
+  return launch_persistent(FWD_KERNEL(KMAX), a.grid, kFwdThreads, FwdLayout::kSmemBytes, kFwdCG,
+                           stream, a.tmA, a.tmB, a.tmA, a.tmB, a.sch, idesc, p, a.status);
+}
+
+cudaError_t launch_fwd_scoring(const FwdArgs &a, cudaStream_t stream) {
+  if (a.K == 1) return launch_fwd_k<1>(a, stream);
+  return launch_fwd_k<kMaxTargets>(a, stream);
 }
 
 int fwd_units(int num_sms) {
   static int cached[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return resident_units(FWD_KERNEL, kFwdThreads, FwdLayout::kSmemBytes, kFwdCG, num_sms);
-  if (!cached[dev]) cached[dev] = resident_units(FWD_KERNEL, kFwdThreads, FwdLayout::kSmemBytes, kFwdCG, num_sms);
+  const auto kern = FWD_KERNEL(1);
+  if (dev < 0 || dev >= 64) return resident_units(kern, kFwdThreads, FwdLayout::kSmemBytes, kFwdCG, num_sms);
+  if (!cached[dev]) cached[dev] = resident_units(kern, kFwdThreads, FwdLayout::kSmemBytes, kFwdCG, num_sms);
   return cached[dev];
 }
 

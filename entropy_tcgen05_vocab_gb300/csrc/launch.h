@@ -19,6 +19,9 @@ namespace flp {
 // double-buffered accumulators this needs a quarter less operand traffic per
 // flop (48 vs 64 B/clk/SM at full rate), which pays for the epilogue no
 // longer overlapping the MMAs.
+// Largest number of target tokens per row of the K-candidate forward
+// (FLP_MAX_TARGETS in the public header).
+constexpr int kMaxTargets = 8;
 constexpr int kFwdBN = 256;        // N of one MMA
 constexpr int kFwdTileCols = 512;  // vocabulary columns per tile
 constexpr int kFwdCG = 2;
@@ -51,12 +54,13 @@ struct FwdArgs {
   Schedule sch;
   int grid;
   bool bf16;
-  const int64_t *targets;
+  const int64_t *targets;  // [T, K]
+  int K;                   // targets per row (1 .. kMaxTargets)
   const int64_t *row_idx;
   int64_t T;
   float inv_tau;
   float scale_log2;
-  float *pm, *ps, *pb, *zt;
+  float *pm, *ps, *pb, *zt;  // zt: [n, K]
   uint32_t *counters;  // [ceil(n / 32)] zeroed before the launch
   float *out_logp, *out_ent, *out_lse, *out_ez;
   uint32_t *status;

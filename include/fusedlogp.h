@@ -129,6 +129,25 @@ flp_status flp_logprob_entropy(const flp_shape *shape, const void *h, const void
                                void *workspace, size_t workspace_bytes, flp_stream_t stream);
 
 /*
+ * K target tokens per scored row (score centering's K-candidate scoring,
+ * miles PR #4645, "Scope": a fused log-prob op with K targets per row):
+ * the same pass as flp_logprob_entropy, capturing K target logits per row.
+ *   targets      [T, K] int64, row-major, indexed by h row
+ *   K            1 .. FLP_MAX_TARGETS
+ *   out_logp     [n_rows, K] float: z'_{targets[row, k]} - logsumexp(z')
+ *   out_ent, out_lse, out_ez as in flp_logprob_entropy.
+ * A candidate outside [0, V) gives NaN in its slot and is counted in
+ * bad_targets.  Uses the workspace of FLP_OP_LOGPROB_ENTROPY.
+ */
+#define FLP_MAX_TARGETS 8
+
+flp_status flp_logprob_entropy_k(const flp_shape *shape, const void *h, const void *W,
+                                 const int64_t *targets, int32_t K, const int64_t *row_idx,
+                                 float temperature, float *out_logp, float *out_ent,
+                                 float *out_lse, float *out_ez,
+                                 void *workspace, size_t workspace_bytes, flp_stream_t stream);
+
+/*
  * Full-vocabulary KL(teacher || student) per scored row:
  *   KL = sum_v p_t,v (log p_t,v - log p_s,v),
  *   p_s = softmax(h_s[row] W_s^T),  p_t = softmax(h_t[row] W_t^T),

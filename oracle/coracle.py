@@ -25,6 +25,9 @@ def lib():
         _lib.orc_backward.argtypes = [i64, i64, vp, ip, i64, vp, ip, i64, vp, i64, i64,
                                       vp, dbl, vp, vp, vp, vp, i64, vp]
         _lib.orc_decode_array.argtypes = [vp, ip, i64, vp]
+        _lib.orc_logprob_k.argtypes = [i64, i64, vp, ip, i64, vp, ip, i64, vp, i64, i64, vp, i64,
+                                       dbl, vp, vp, vp]
+        _lib.orc_logprob_k.restype = ip
         _lib.orc_num_threads.restype = ip
         for f in (_lib.orc_logprob_entropy, _lib.orc_kl, _lib.orc_backward):
             f.restype = ip
@@ -142,3 +145,23 @@ def scatter_rows(dh_rows, rows, T):
     np.add.at(out, _i64(rows), dh_rows)
     return out
 
+
+def logprob_k(h, W, targets_tk, rows, tau, dtype):
+    """K targets per scored row: logp [n, K], ent [n], lse [n] (float64).
+    targets_tk is [T, K] (indexed by h row)."""
+    hs, ht, ldh = storage(h, dtype)
+    ws, wt, ldw = storage(W, dtype)
+    T, H, V = hs.shape[0], ldh, ws.shape[0]
+    rows = _i64(rows if rows is not None else np.arange(T))
+    tg = _i64(targets_tk)
+    K = tg.shape[1]
+    n = rows.shape[0]
+    logp = np.empty((n, K))
+    ent = np.empty(n)
+    lse = np.empty(n)
+    rc = lib().orc_logprob_k(H, V, hs.ctypes.data, ht, ldh, ws.ctypes.data, wt, ldw, _ptr(rows), n,
+                             T, _ptr(tg), K, float(tau), logp.ctypes.data, ent.ctypes.data,
+                             lse.ctypes.data)
+    if rc == -2:
+        raise MemoryError("oracle allocation failed")
+    return {"logp": logp, "ent": ent, "lse": lse, "rc": rc}

@@ -338,3 +338,50 @@ int orc_backward(int64_t H, int64_t V,
     free(hd); free(z);
     return 0;
 }
+
+/*
+ * K target tokens per scored row (score centering's K-candidate scoring,
+ * miles PR #4645, "Scope": "K targets per row"): logp[i*K + k] =
+ * z'_{targets[rows[i]*K + k]} - LSE for k < K, with the entropy, LSE and E[z']
+ * of the row as in orc_logprob_entropy.  targets is [T, K] row-major.
+ * Returns 0, or -1 if any row or target is out of range (NaN written there).
+ */
+int orc_logprob_k(int64_t H, int64_t V,
+                  const void *h, int htype, int64_t ld_h,
+                  const void *W, int wtype, int64_t ld_w,
+                  const int64_t *rows, int64_t n, int64_t T,
+                  const int64_t *targets, int64_t K, double tau,
+                  double *logp, double *ent, double *lse_out)
+{
+    int rc = 0;
+    int64_t i0;
+    double *hd = (double *)malloc((size_t)ORC_ROW_BLOCK * H * sizeof(double));
+    double *z = (double *)malloc((size_t)ORC_ROW_BLOCK * V * sizeof(double));
+    if (!hd || !z) { free(hd); free(z); return -2; }
+    for (i0 = 0; i0 < n; i0 += ORC_ROW_BLOCK) {
+        int64_t nb = n - i0 < ORC_ROW_BLOCK ? n - i0 : ORC_ROW_BLOCK;
+        int64_t b, k;
+        for (b = 0; b < nb; ++b)
+            if (rows[i0 + b] < 0 || rows[i0 + b] >= T) { free(hd); free(z); return -1; }
+        orc_gather_h(h, htype, ld_h, rows, i0, nb, H, hd);
+        orc_logits_block(hd, nb, H, V, W, wtype, ld_w, z);
+        for (b = 0; b < nb; ++b) {
+            int64_t i = i0 + b, v;
+            double *zr = z + b * V;
+            double L, ez = 0.0;
+            for (v = 0; v < V; ++v) zr[v] = zr[v] / tau;
+            L = orc_lse(zr, V);
+            for (v = 0; v < V; ++v) ez += exp(zr[v] - L) * zr[v];
+            for (k = 0; k < K; ++k) {
+                int64_t t = targets[rows[i] * K + k];
+                if (t >= 0 && t < V) logp[i * K + k] = zr[t] - L;
+                else { logp[i * K + k] = NAN; rc = -1; }
+            }
+            if (ent) ent[i] = L - ez;
+            if (lse_out) lse_out[i] = L;
+        }
+    }
+    free(hd);
+    free(z);
+    return rc;
+}

@@ -374,3 +374,39 @@ def test_c_and_numpy_agree_kl():
     a = coracle.kl(d["h_s"], d["W_s"], d["h_t"], d["W_t"], None, "bf16")
     b = ref.kl(d["h_s"], d["W_s"], d["h_t"], d["W_t"], None, "bf16")
     np.testing.assert_allclose(a, b, rtol=1e-10, atol=1e-13)
+
+
+# --------------------------------------------------------------------------
+# K targets per row
+
+def test_k_targets_reduce_to_single_targets():
+    d = _random_case(16, T=20, V=700)
+    rng = np.random.default_rng(16)
+    tk = rng.integers(0, 700, size=(20, 5))
+    rows = np.array([3, 19, 0, 7, 7])
+    o = coracle.logprob_k(d["h"], d["W"], tk, rows, 0.7, "bf16")
+    assert o["rc"] == 0
+    for k in range(5):
+        single = coracle.logprob_entropy(d["h"], d["W"], tk[:, k], rows, 0.7, "bf16")
+        np.testing.assert_array_equal(o["logp"][:, k], single["logp"])
+        np.testing.assert_array_equal(o["ent"], single["ent"])
+
+
+def test_k_targets_over_the_whole_vocabulary_sum_to_one():
+    """With every token as a candidate, exp(logp) is the softmax: it sums to 1."""
+    d = _random_case(17, T=6, H=16, V=300)
+    tk = np.tile(np.arange(300), (6, 1))
+    o = coracle.logprob_k(d["h"], d["W"], tk, None, 0.9, "bf16")
+    np.testing.assert_allclose(np.exp(o["logp"]).sum(axis=1), 1.0, atol=1e-12)
+    # the entropy is the entropy of that distribution
+    p = np.exp(o["logp"])
+    np.testing.assert_allclose(-(p * o["logp"]).sum(axis=1), o["ent"], atol=1e-11)
+
+
+def test_k_targets_bad_candidate_is_nan():
+    d = _random_case(18, T=4, V=100)
+    tk = np.array([[1, 2], [3, 100], [5, -1], [7, 8]])
+    o = coracle.logprob_k(d["h"], d["W"], tk, None, 1.0, "bf16")
+    assert o["rc"] == -1
+    assert np.isnan(o["logp"][1, 1]) and np.isnan(o["logp"][2, 1])
+    assert np.isfinite(o["logp"][[0, 3]]).all() and np.isfinite(o["logp"][[1, 2], 0]).all()
