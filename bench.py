@@ -390,7 +390,7 @@ def run_ours(args):
         "kernel_ms": kernel_ms,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": P["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": achieved / P["bf16_tflops"], "traffic": traffic,
-                     "kernel": "vocab_pipeline_kernel<256,4,LseEpi>",
+                     "kernel": "vocab_pipeline_kernel<256,4,2,LseEpi<1>,2,1,8,true>",
                      "peak_kind": "bf16 dense, burst, %s" % P["source"],
                      "frac_of_sustained": achieved / P["bf16_tflops_sustained"],
                      "algorithmic_flops_per_launch": fl,
