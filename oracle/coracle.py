@@ -28,6 +28,12 @@ def lib():
         _lib.orc_logprob_k.argtypes = [i64, i64, vp, ip, i64, vp, ip, i64, vp, i64, i64, vp, i64,
                                        dbl, vp, vp, vp]
         _lib.orc_logprob_k.restype = ip
+        _lib.orc_logprob_entropy_support.argtypes = [i64, i64, vp, ip, i64, vp, ip, i64, vp, i64,
+                                                     i64, vp, vp, i64, dbl, vp, vp, vp, vp]
+        _lib.orc_logprob_entropy_support.restype = ip
+        _lib.orc_backward_support.argtypes = [i64, i64, vp, ip, i64, vp, ip, i64, vp, i64, i64,
+                                              vp, vp, i64, dbl, vp, vp, vp, vp, i64, vp]
+        _lib.orc_backward_support.restype = ip
         _lib.orc_num_threads.restype = ip
         for f in (_lib.orc_logprob_entropy, _lib.orc_kl, _lib.orc_backward):
             f.restype = ip
@@ -165,3 +171,55 @@ def logprob_k(h, W, targets_tk, rows, tau, dtype):
     if rc == -2:
         raise MemoryError("oracle allocation failed")
     return {"logp": logp, "ent": ent, "lse": lse, "rc": rc}
+
+
+def _words(support):
+    w = np.ascontiguousarray(np.asarray(support).view(np.uint32))
+    if w.ndim != 2:
+        raise ValueError("support is a [T, ld] array of uint32 words")
+    return w, w.shape[1]
+
+
+def logprob_entropy_support(h, W, targets, rows, support, tau, dtype):
+    """Per scored row under the row's sampling support (uint32 bitmask [T, ld]
+    by h row): logp (-inf for a target off the support), ent, lse, ez."""
+    hs, ht, ldh = storage(h, dtype)
+    ws, wt, ldw = storage(W, dtype)
+    T, H, V = hs.shape[0], ldh, ws.shape[0]
+    rows = _i64(rows if rows is not None else np.arange(T))
+    sw, lds = _words(support)
+    n = rows.shape[0]
+    out = {k: np.empty(n, dtype=np.float64) for k in ("logp", "ent", "lse", "ez")}
+    rc = lib().orc_logprob_entropy_support(H, V, hs.ctypes.data, ht, ldh, ws.ctypes.data, wt,
+                                           ldw, _ptr(rows), n, T, _ptr(_i64(targets)),
+                                           sw.ctypes.data, lds, float(tau),
+                                           out["logp"].ctypes.data, out["ent"].ctypes.data,
+                                           out["lse"].ctypes.data, out["ez"].ctypes.data)
+    if rc == -2:
+        raise MemoryError("oracle allocation failed")
+    out["rc"] = rc
+    return out
+
+
+def backward_support(h, W, targets, rows, support, tau, g1, g2, dtype, vsel=None):
+    """Gradients of sum(g1*logp + g2*ent) under the sampling support:
+    (dh_rows [n,H], dW_sel [nv,H]) as in :func:`backward`."""
+    hs, ht, ldh = storage(h, dtype)
+    ws, wt, ldw = storage(W, dtype)
+    T, H, V = hs.shape[0], ldh, ws.shape[0]
+    rows = _i64(rows if rows is not None else np.arange(T))
+    sw, lds = _words(support)
+    n = rows.shape[0]
+    g1 = np.ascontiguousarray(g1, dtype=np.float64)
+    g2 = np.ascontiguousarray(g2, dtype=np.float64)
+    vs = None if vsel is None else _i64(vsel)
+    nv = V if vs is None else vs.shape[0]
+    dh = np.zeros((n, H))
+    dW = np.zeros((nv, H))
+    rc = lib().orc_backward_support(H, V, hs.ctypes.data, ht, ldh, ws.ctypes.data, wt, ldw,
+                                    _ptr(rows), n, T, _ptr(_i64(targets)), sw.ctypes.data, lds,
+                                    float(tau), g1.ctypes.data, g2.ctypes.data, dh.ctypes.data,
+                                    _ptr(vs), nv, dW.ctypes.data)
+    if rc:
+        raise RuntimeError("oracle backward_support failed: %d" % rc)
+    return dh, dW

@@ -385,3 +385,157 @@ int orc_logprob_k(int64_t H, int64_t V,
     free(z);
     return rc;
 }
+
+/*
+ * Sampling-support restriction (miles PR #2764 summary, math_utils.py
+ * snippet: calculate_log_probs_and_entropy's sampling_mask, cut into row
+ * chunks together with the logits and the tokens).  Read as: the log-prob
+ * and entropy are those of the sampling distribution, softmax(z') restricted
+ * to the row's support S and renormalised; off S, p_v = 0.
+ *
+ * support is a bitmask of uint32 words, [T, ld_s], indexed by the original h
+ * row like the targets: token v is in row r's support iff bit (v % 32) of
+ * word support[r * ld_s + v / 32] is set.
+ */
+static int orc_in_support(const uint32_t *srow, int64_t v)
+{
+    return (int)((srow[v / 32] >> (v % 32)) & 1u);
+}
+
+/* log sum_{v in S} exp(x_v), two passes; -inf for an empty S. */
+static double orc_lse_support(const double *x, int64_t V, const uint32_t *srow)
+{
+    double m = -INFINITY, s = 0.0;
+    int64_t v;
+    for (v = 0; v < V; ++v)
+        if (orc_in_support(srow, v) && x[v] > m) m = x[v];
+    if (m == -INFINITY) return -INFINITY;
+    for (v = 0; v < V; ++v)
+        if (orc_in_support(srow, v)) s += exp(x[v] - m);
+    return m + log(s);
+}
+
+/*
+ * Per scored row, over the support S:
+ *   LSE_S = log sum_{v in S} exp(z'_v),   p_v = exp(z'_v - LSE_S) on S
+ *   logp  = z'_tgt - LSE_S if tgt is in S, -inf if it is not
+ *   ent   = LSE_S - sum_{v in S} p_v z'_v,  ez = sum_{v in S} p_v z'_v
+ * A row with an empty support, an out-of-range row or an out-of-range target
+ * gives NaN (the target: logp only) and rc -1.
+ */
+int orc_logprob_entropy_support(int64_t H, int64_t V,
+                                const void *h, int htype, int64_t ld_h,
+                                const void *W, int wtype, int64_t ld_w,
+                                const int64_t *rows, int64_t n, int64_t T,
+                                const int64_t *targets, const uint32_t *support,
+                                int64_t ld_s, double tau,
+                                double *logp, double *ent, double *lse_out, double *ez_out)
+{
+    int rc = 0;
+    int64_t i;
+    double *hd = (double *)malloc((size_t)H * sizeof(double));
+    double *z = (double *)malloc((size_t)V * sizeof(double));
+    if (!hd || !z) { free(hd); free(z); return -2; }
+    for (i = 0; i < n; ++i) {
+        int64_t r = rows[i], v, tgt;
+        const uint32_t *srow;
+        double L, ez = 0.0;
+        if (r < 0 || r >= T) {
+            logp[i] = ent[i] = NAN;
+            if (lse_out) lse_out[i] = NAN;
+            if (ez_out) ez_out[i] = NAN;
+            rc = -1;
+            continue;
+        }
+        srow = support + r * ld_s;
+        orc_decode(h, htype, r * ld_h, H, hd);
+        orc_logits_block(hd, 1, H, V, W, wtype, ld_w, z);
+        for (v = 0; v < V; ++v) z[v] = z[v] / tau;
+        L = orc_lse_support(z, V, srow);
+        if (L == -INFINITY) {
+            logp[i] = ent[i] = NAN;
+            if (lse_out) lse_out[i] = NAN;
+            if (ez_out) ez_out[i] = NAN;
+            rc = -1;
+            continue;
+        }
+        for (v = 0; v < V; ++v)
+            if (orc_in_support(srow, v)) ez += exp(z[v] - L) * z[v];
+        tgt = targets[r];
+        if (tgt < 0 || tgt >= V) { logp[i] = NAN; rc = -1; }
+        else logp[i] = orc_in_support(srow, tgt) ? z[tgt] - L : -INFINITY;
+        ent[i] = L - ez;
+        if (lse_out) lse_out[i] = L;
+        if (ez_out) ez_out[i] = ez;
+    }
+    free(hd);
+    free(z);
+    return rc;
+}
+
+/*
+ * Backward of L = sum_i g1[i] logp[i] + g2[i] ent[i] with the support
+ * restriction above.  On S the gradient with respect to z is the unrestricted
+ * formula with p and E z' taken over S; off S it is 0:
+ *   G_v = 1[v in S] (g1 (1[v=tgt] - p_v) - g2 p_v (z'_v - Ez')) / tau
+ * (a target outside S contributes no one-hot term, since G vanishes off S).
+ * Outputs as in orc_backward; rows must be valid with non-empty supports
+ * (rc -1 otherwise).
+ */
+int orc_backward_support(int64_t H, int64_t V,
+                         const void *h, int htype, int64_t ld_h,
+                         const void *W, int wtype, int64_t ld_w,
+                         const int64_t *rows, int64_t n, int64_t T,
+                         const int64_t *targets, const uint32_t *support, int64_t ld_s,
+                         double tau, const double *g1, const double *g2,
+                         double *dh_rows, const int64_t *vsel, int64_t nv, double *dW_sel)
+{
+    int64_t i;
+    double *hd = (double *)malloc((size_t)H * sizeof(double));
+    double *z = (double *)malloc((size_t)V * sizeof(double));
+    double *wd = (double *)malloc((size_t)H * sizeof(double));
+    if (!hd || !z || !wd) { free(hd); free(z); free(wd); return -2; }
+    for (i = 0; i < n; ++i) {
+        int64_t r = rows[i], v, k, j, tgt;
+        const uint32_t *srow;
+        double L, ez = 0.0;
+        if (r < 0 || r >= T) { free(hd); free(z); free(wd); return -1; }
+        tgt = targets[r];
+        if (tgt < 0 || tgt >= V) { free(hd); free(z); free(wd); return -1; }
+        srow = support + r * ld_s;
+        orc_decode(h, htype, r * ld_h, H, hd);
+        orc_logits_block(hd, 1, H, V, W, wtype, ld_w, z);
+        for (v = 0; v < V; ++v) z[v] = z[v] / tau;
+        L = orc_lse_support(z, V, srow);
+        if (L == -INFINITY) { free(hd); free(z); free(wd); return -1; }
+        for (v = 0; v < V; ++v)
+            if (orc_in_support(srow, v)) ez += exp(z[v] - L) * z[v];
+        /* z becomes the gradient row G in place. */
+        for (v = 0; v < V; ++v) {
+            if (orc_in_support(srow, v)) {
+                double p = exp(z[v] - L);
+                double onehot = (v == tgt) ? 1.0 : 0.0;
+                z[v] = (g1[i] * (onehot - p) - g2[i] * p * (z[v] - ez)) / tau;
+            } else {
+                z[v] = 0.0;
+            }
+        }
+        if (dh_rows) {
+            double *d = dh_rows + i * H;
+            for (k = 0; k < H; ++k) d[k] = 0.0;
+            for (v = 0; v < V; ++v) {
+                if (z[v] == 0.0) continue;
+                orc_decode(W, wtype, v * ld_w, H, wd);
+                for (k = 0; k < H; ++k) d[k] += z[v] * wd[k];
+            }
+        }
+        if (dW_sel) {
+            for (j = 0; j < nv; ++j) {
+                double g = z[vsel ? vsel[j] : j];
+                for (k = 0; k < H; ++k) dW_sel[j * H + k] += g * hd[k];
+            }
+        }
+    }
+    free(hd); free(z); free(wd);
+    return 0;
+}

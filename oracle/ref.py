@@ -47,27 +47,63 @@ def _lse(zp):
     return (m + np.log(np.exp(zp - m).sum(axis=1, keepdims=True)))[:, 0]
 
 
-def row_stats(hd, Wd, rows, tau, block=256):
-    """lse and Ez' = sum_v p_v z'_v per scored row, from decoded float64 h, W."""
+def support_bits(support, rows, V):
+    """Boolean [len(rows), V] membership from a uint32 support bitmask [T, ld]
+    indexed by h row: token v is in row r's support iff bit v % 32 of word
+    v // 32 of row r is set."""
+    words = np.ascontiguousarray(np.asarray(support).view(np.uint32)[rows])
+    bits = np.unpackbits(words.view(np.uint8), axis=1, bitorder="little")
+    return bits[:, :V].astype(bool)
+
+
+def _lse_on(zp, keep):
+    """Row-wise log-sum-exp over the entries where keep is True (-inf if none)."""
+    m = np.where(keep, zp, -np.inf).max(axis=1, keepdims=True)
+    safe = np.where(np.isfinite(m), m, 0.0)
+    s = np.where(keep, np.exp(np.where(keep, zp, safe) - safe), 0.0).sum(axis=1, keepdims=True)
+    with np.errstate(divide="ignore"):
+        return np.where(s[:, 0] > 0, safe[:, 0] + np.log(s[:, 0]), -np.inf)
+
+
+def row_stats(hd, Wd, rows, tau, block=256, support=None):
+    """lse and Ez' = sum_v p_v z'_v per scored row, from decoded float64 h, W.
+    With a support bitmask, both are taken over each row's support (p = 0 off
+    it); an empty support gives NaN."""
     rows = _rows(rows, hd.shape[0])
     lse = np.empty(rows.shape[0])
     ez = np.empty(rows.shape[0])
     for i0 in range(0, rows.shape[0], block):
-        zp = (hd[rows[i0:i0 + block]] @ Wd.T) / tau
-        L = _lse(zp)
-        p = np.exp(zp - L[:, None])
+        r = rows[i0:i0 + block]
+        zp = (hd[r] @ Wd.T) / tau
+        if support is None:
+            L = _lse(zp)
+            p = np.exp(zp - L[:, None])
+        else:
+            keep = support_bits(support, r, Wd.shape[0])
+            L = _lse_on(zp, keep)
+            with np.errstate(invalid="ignore"):
+                p = np.where(keep, np.exp(np.where(keep, zp, 0.0) - L[:, None]), 0.0)
+            L = np.where(np.isfinite(L), L, np.nan)
         lse[i0:i0 + block] = L
-        ez[i0:i0 + block] = (p * zp).sum(axis=1)
+        ez[i0:i0 + block] = (p * zp).sum(axis=1) + 0.0 * L
     return lse, ez
 
 
-def logprob_entropy(h, W, targets, rows, tau, dtype, block=256):
+def logprob_entropy(h, W, targets, rows, tau, dtype, block=256, support=None):
+    """logp, ent, lse, ez per scored row.  With ``support`` (uint32 bitmask
+    [T, ld] by h row) the distribution is softmax(z') restricted to the row's
+    support and renormalised (math_utils.py's sampling_mask); a target off
+    the support has logp = -inf."""
     hd, Wd = decode(h, dtype), decode(W, dtype)
     rows = _rows(rows, hd.shape[0])
     tg = np.asarray(targets, dtype=np.int64)[rows]
-    lse, ez = row_stats(hd, Wd, rows, tau, block)
+    lse, ez = row_stats(hd, Wd, rows, tau, block, support)
     zt = np.einsum("ik,ik->i", hd[rows], Wd[tg]) / tau
-    return {"logp": zt - lse, "ent": lse - ez, "lse": lse, "ez": ez}
+    logp = zt - lse
+    if support is not None:
+        on = support_bits(support, rows, Wd.shape[0])[np.arange(rows.shape[0]), tg]
+        logp = np.where(on | np.isnan(lse), logp, -np.inf)
+    return {"logp": logp, "ent": lse - ez, "lse": lse, "ez": ez}
 
 
 def kl(h_s, W_s, h_t, W_t, rows, dtype, block=256):
@@ -84,23 +120,28 @@ def kl(h_s, W_s, h_t, W_t, rows, dtype, block=256):
     return out
 
 
-def grad_logits(zp, tgt, lse, ez, g1, g2, tau):
-    """dL/dz for L = g1 logp + g2 ent, rows of z' = z/tau (float64)."""
+def grad_logits(zp, tgt, lse, ez, g1, g2, tau, keep=None):
+    """dL/dz for L = g1 logp + g2 ent, rows of z' = z/tau (float64).  With a
+    support (keep: boolean [rows, V]) the gradient is the same formula on the
+    support, with p, lse and ez taken over it, and 0 off it."""
+    if keep is not None:
+        zp = np.where(keep, zp, lse[:, None])
     p = np.exp(zp - lse[:, None])
     onehot = np.zeros_like(zp)
     onehot[np.arange(zp.shape[0]), tgt] = 1.0
-    return (g1[:, None] * (onehot - p) - g2[:, None] * p * (zp - ez[:, None])) / tau
+    G = (g1[:, None] * (onehot - p) - g2[:, None] * p * (zp - ez[:, None])) / tau
+    return G if keep is None else np.where(keep, G, 0.0)
 
 
 def backward(h, W, targets, rows, tau, g1, g2, dtype, dh_rows_sel=None, vsel=None,
-             block=256, stats=None):
+             block=256, stats=None, support=None):
     """Gradients of sum(g1 logp + g2 ent).
 
     dh_rows_sel: positions i (into rows) whose dh rows to return (default all).
     vsel: vocabulary rows of dW to return (default all).  dW needs every
     scored row's statistics, which this computes with a float64 matmul pass
     over the full vocabulary unless ``stats=(lse, ez)`` is supplied (each
-    computed by :func:`row_stats`).
+    computed by :func:`row_stats`).  ``support``: as in :func:`logprob_entropy`.
     Returns (dh_rows [len(sel),H], dW_sel [len(vsel),H]).
     """
     hd, Wd = decode(h, dtype), decode(W, dtype)
@@ -117,16 +158,24 @@ def backward(h, W, targets, rows, tau, g1, g2, dtype, dh_rows_sel=None, vsel=Non
     for i0 in range(0, sel.shape[0], block):
         s = sel[i0:i0 + block]
         zp = (hd[rows[s]] @ Wd.T) / tau
-        L = _lse(zp)
-        ez = (np.exp(zp - L[:, None]) * zp).sum(axis=1)
-        G = grad_logits(zp, tg[s], L, ez, g1[s], g2[s], tau)
+        keep = None if support is None else support_bits(support, rows[s], Wd.shape[0])
+        if keep is None:
+            L = _lse(zp)
+            ez = (np.exp(zp - L[:, None]) * zp).sum(axis=1)
+        else:
+            L = _lse_on(zp, keep)
+            ez = np.where(keep, np.exp(np.where(keep, zp, L[:, None]) - L[:, None]) * zp,
+                          0.0).sum(axis=1)
+        G = grad_logits(zp, tg[s], L, ez, g1[s], g2[s], tau, keep)
         dh[i0:i0 + block] = G @ Wd
 
     # dW rows: every scored row contributes to every vocabulary row.
-    lse, ez = stats if stats is not None else row_stats(hd, Wd, rows, tau, block)
+    lse, ez = stats if stats is not None else row_stats(hd, Wd, rows, tau, block, support)
     zp = (hd[rows] @ Wd[vs].T) / tau                       # [n, len(vs)]
     p = np.exp(zp - lse[:, None])
     onehot = (tg[:, None] == vs[None, :]).astype(np.float64)
     G = (g1[:, None] * (onehot - p) - g2[:, None] * p * (zp - ez[:, None])) / tau
+    if support is not None:
+        G = np.where(support_bits(support, rows, Wd.shape[0])[:, vs], G, 0.0)
     dW = G.T @ hd[rows]
     return dh, dW

@@ -410,3 +410,185 @@ def test_k_targets_bad_candidate_is_nan():
     assert o["rc"] == -1
     assert np.isnan(o["logp"][1, 1]) and np.isnan(o["logp"][2, 1])
     assert np.isfinite(o["logp"][[0, 3]]).all() and np.isfinite(o["logp"][[1, 2], 0]).all()
+
+
+# --------------------------------------------------------------------------
+# sampling support (the per-row vocabulary mask of calculate_log_probs_and_entropy)
+
+def _support_case(seed, T=10, H=16, V=150, j=1, force=True, dtype="bf16"):
+    d = _random_case(seed, T=T, H=H, V=V, dtype=dtype)
+    tg = d["targets"].numpy()
+    sup = workloads.support_words(T, V, j, seed, targets=tg if force else None)
+    return d, tg, sup
+
+
+def test_support_of_every_token_is_the_unrestricted_result():
+    d, tg, sup = _support_case(40, j=0)
+    rows = np.array([9, 0, 4, 4])
+    for f, g in ((coracle.logprob_entropy_support, coracle.logprob_entropy),
+                 (lambda *a: ref.logprob_entropy(*a[:4], a[5], a[6], support=a[4]),
+                  ref.logprob_entropy)):
+        a = f(d["h"], d["W"], tg, rows, sup, 0.8, "bf16")
+        b = g(d["h"], d["W"], tg, rows, 0.8, "bf16")
+        for k in ("logp", "ent", "lse", "ez"):
+            np.testing.assert_allclose(a[k], b[k], rtol=1e-13, atol=1e-13)
+
+
+@pytest.mark.parametrize("j", [1, 3])
+def test_support_is_the_problem_on_the_kept_vocabulary(j):
+    """Restricting to S is the unrestricted problem on the vocabulary rows W[S]
+    with the target renumbered: row by row, with the plain oracle."""
+    d, tg, sup = _support_case(41 + j, j=j)
+    Wd = ref.decode(d["W"], "bf16")
+    keep = ref.support_bits(sup, np.arange(10), 150)
+    got = coracle.logprob_entropy_support(d["h"], d["W"], tg, None, sup, 0.7, "bf16")
+    assert got["rc"] == 0
+    for r in range(10):
+        S = np.nonzero(keep[r])[0]
+        t_new = np.full(10, 0)
+        t_new[r] = int(np.searchsorted(S, tg[r]))
+        assert S[t_new[r]] == tg[r]
+        sub = coracle.logprob_entropy(ref.decode(d["h"], "bf16"), Wd[S], t_new, [r], 0.7, "f64")
+        for k in ("logp", "ent", "lse", "ez"):
+            assert got[k][r] == pytest.approx(sub[k][0], rel=1e-13, abs=1e-13), (r, k)
+
+
+def _dec_forward_support(h, W, tg, rows, keep, tau):
+    getcontext().prec = 50
+    out = []
+    for r in rows:
+        S = [v for v in range(W.shape[0]) if keep[r, v]]
+        z = {v: sum(Decimal(float(h[r, k])) * Decimal(float(W[v, k])) for k in range(h.shape[1]))
+             / Decimal(repr(tau)) for v in S}
+        lse = sum((x.exp() for x in z.values()), Decimal(0)).ln()
+        ez = sum(((x - lse).exp() * x for x in z.values()), Decimal(0))
+        out.append((float(z[tg[r]] - lse), float(lse - ez), float(lse), float(ez)))
+    return np.array(out)
+
+
+@pytest.mark.parametrize("tau", [0.7, 1.3])
+def test_support_brute_force(tau):
+    d, tg, sup = _support_case(44, T=6, H=11, V=45, j=1)
+    rows = np.array([5, 2, 0, 2])
+    keep = ref.support_bits(sup, np.arange(6), 45)
+    want = _dec_forward_support(ref.decode(d["h"], "bf16"), ref.decode(d["W"], "bf16"), tg, rows,
+                                keep, tau)
+    c = coracle.logprob_entropy_support(d["h"], d["W"], tg, rows, sup, tau, "bf16")
+    n = ref.logprob_entropy(d["h"], d["W"], tg, rows, tau, "bf16", support=sup)
+    for o in (c, n):
+        got = np.stack([o["logp"], o["ent"], o["lse"], o["ez"]], axis=1)
+        np.testing.assert_allclose(got, want, rtol=1e-13, atol=1e-13)
+
+
+def test_support_singleton_and_pair_closed_forms():
+    rng = np.random.default_rng(45)
+    T, H, V = 4, 6, 70
+    h, W = rng.standard_normal((T, H)), rng.standard_normal((V, H))
+    tg = np.array([3, 40, 69, 0])
+    other = np.array([64, 41, 1, 33])
+    sup = np.zeros((T, 3), dtype=np.uint32)
+    for r in range(T):
+        sup[r, tg[r] // 32] |= np.uint32(1 << (tg[r] % 32))
+    one = coracle.logprob_entropy_support(h, W, tg, None, sup.view(np.int32), 0.9, "f64")
+    assert np.all(one["logp"] == 0.0) and np.all(one["ent"] == 0.0)
+    for r in range(T):
+        sup[r, other[r] // 32] |= np.uint32(1 << (other[r] % 32))
+    two = coracle.logprob_entropy_support(h, W, tg, None, sup.view(np.int32), 0.9, "f64")
+    for r in range(T):
+        dz = (h[r] @ W[other[r]] - h[r] @ W[tg[r]]) / 0.9
+        q = 1 / (1 + math.exp(dz))                  # probability of the target
+        assert two["logp"][r] == pytest.approx(math.log(q), abs=1e-14)
+        assert two["ent"][r] == pytest.approx(-q * math.log(q) - (1 - q) * math.log(1 - q),
+                                              abs=1e-14)
+
+
+def test_support_target_off_support_and_empty_support():
+    d, tg, sup = _support_case(46, T=5, V=100, j=2)
+    words = sup.view(np.uint32).copy()
+    words[1, tg[1] // 32] &= ~np.uint32(1 << (tg[1] % 32))     # target of row 1 off
+    words[3, :] = 0                                             # row 3: empty support
+    s = words.view(np.int32)
+    c = coracle.logprob_entropy_support(d["h"], d["W"], tg, None, s, 1.0, "bf16")
+    n = ref.logprob_entropy(d["h"], d["W"], tg, None, 1.0, "bf16", support=s)
+    assert c["rc"] == -1
+    for o in (c, n):
+        assert o["logp"][1] == -np.inf and np.isfinite(o["ent"][1])
+        assert np.isnan(o["logp"][3]) and np.isnan(o["ent"][3])
+        assert np.isfinite(o["logp"][[0, 2, 4]]).all()
+    np.testing.assert_allclose(c["ent"][[0, 1, 2, 4]], n["ent"][[0, 1, 2, 4]], rtol=1e-12)
+
+
+def _loss_support(h, W, tg, rows, sup, tau, g1, g2):
+    o = coracle.logprob_entropy_support(h, W, tg, rows, sup, tau, "f64")
+    return float(np.sum(g1 * o["logp"] + g2 * o["ent"]))
+
+
+@pytest.mark.parametrize("tau", [0.7, 1.0])
+def test_support_backward_matches_finite_differences(tau):
+    rng = np.random.default_rng(47)
+    T, H, V = 5, 4, 40
+    h = rng.standard_normal((T, H))
+    W = rng.standard_normal((V, H)) * 0.7
+    tg = rng.integers(0, V, size=T)
+    sup = workloads.support_words(T, V, 1, 47, targets=tg)
+    rows = np.array([4, 0, 2])
+    g1, g2 = rng.standard_normal(3), rng.standard_normal(3)
+    dh_rows, dW = coracle.backward_support(h, W, tg, rows, sup, tau, g1, g2, "f64")
+    dh = coracle.scatter_rows(dh_rows, rows, T)
+    eps = 1e-6
+    num_h = np.zeros_like(h)
+    for r in range(T):
+        for k in range(H):
+            hp, hm = h.copy(), h.copy()
+            hp[r, k] += eps
+            hm[r, k] -= eps
+            num_h[r, k] = (_loss_support(hp, W, tg, rows, sup, tau, g1, g2)
+                           - _loss_support(hm, W, tg, rows, sup, tau, g1, g2)) / (2 * eps)
+    num_W = np.zeros_like(W)
+    for v in range(V):
+        for k in range(H):
+            Wp, Wm = W.copy(), W.copy()
+            Wp[v, k] += eps
+            Wm[v, k] -= eps
+            num_W[v, k] = (_loss_support(h, Wp, tg, rows, sup, tau, g1, g2)
+                           - _loss_support(h, Wm, tg, rows, sup, tau, g1, g2)) / (2 * eps)
+    assert np.linalg.norm(dh - num_h) <= 1e-6 * np.linalg.norm(num_h)
+    assert np.linalg.norm(dW - num_W) <= 1e-6 * np.linalg.norm(num_W)
+    # vocabulary rows outside every scored row's support get no gradient
+    keep = ref.support_bits(sup, rows, V).any(axis=0)
+    assert np.all(dW[~keep] == 0.0) and (~keep).any()
+    rdh, rdW = ref.backward(h, W, tg, rows, tau, g1, g2, "f64", support=sup)
+    np.testing.assert_allclose(rdh, dh_rows, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(rdW, dW, rtol=1e-10, atol=1e-12)
+
+
+def test_support_backward_columns_sum_to_zero():
+    """On the support, sum_v G_rv = 0 still holds (targets inside it), so the
+    column sums of dW vanish."""
+    d, tg, sup = _support_case(48, T=12, H=20, V=300, j=2)
+    rows = np.arange(12)
+    rng = np.random.default_rng(48)
+    _, dW = coracle.backward_support(d["h"], d["W"], tg, rows, sup, 0.7, rng.standard_normal(12),
+                                     rng.standard_normal(12), "bf16")
+    scale = np.abs(dW).sum(axis=0)
+    assert np.all(np.abs(dW.sum(axis=0)) <= 1e-12 * scale + 1e-15)
+
+
+def test_support_c_and_numpy_agree_config0():
+    d = workloads.make(0)
+    tg = d["targets"].numpy()
+    sup = workloads.support_words(256, 8192, 2, 0, targets=tg, ld=260)
+    rows = workloads.sample_rows(256, 40, seed=3)
+    c = coracle.logprob_entropy_support(d["h"], d["W"], tg, rows, sup, 1.0, "bf16")
+    n = ref.logprob_entropy(d["h"], d["W"], tg, rows, 1.0, "bf16", support=sup)
+    for k in ("logp", "ent", "lse", "ez"):
+        np.testing.assert_allclose(c[k], n[k], rtol=1e-10, atol=1e-12)
+    g1 = np.linspace(-1, 1, 40)
+    g2 = np.linspace(1, -0.5, 40)
+    vs = np.array([0, 5, 8191, int(tg[rows[0]])])
+    cdh, cdW = coracle.backward_support(d["h"], d["W"], tg, rows[:6], sup, 1.0, g1[:6], g2[:6],
+                                        "bf16", vsel=vs)
+    ndh, ndW = ref.backward(d["h"], d["W"], tg, rows[:6], 1.0, g1[:6], g2[:6], "bf16",
+                            vsel=vs, support=sup)
+    np.testing.assert_allclose(cdh, ndh, rtol=1e-9, atol=1e-12)
+    np.testing.assert_allclose(cdW, ndW, rtol=1e-9, atol=1e-12)

@@ -21,6 +21,11 @@ each (prompt first, response last); workload 4 scores a Bernoulli(0.6) row
 mask; the others score every row.  Workload 4 also draws g1, g2 ~ N(0,1)
 (float32) per scored row.
 
+Sampling supports (the per-row vocabulary masks of the sampling_mask
+argument) are drawn by :func:`support_words`: each bit is Bernoulli(2^-j), the
+AND of j uniform random words, packed 32 tokens per uint32 word (bit v % 32
+of word v // 32), optionally with each row's target forced in.
+
 Random streams: discrete draws (targets, lengths, masks) always come from
 ``numpy.random.Generator(PCG64([seed, k]))`` on the host, so they do not
 depend on the device.  Continuous draws are float32 normals rounded to
@@ -185,6 +190,30 @@ def make(w, device="cpu", generator="auto"):
         out["g1"] = torch.from_numpy(r.standard_normal(n, dtype=np.float32)).to(dev)
         out["g2"] = torch.from_numpy(r.standard_normal(n, dtype=np.float32)).to(dev)
     return out
+
+
+def support_words(T: int, V: int, j: int, seed: int, targets=None, ld: int | None = None,
+                  k: int = 30):
+    """A seeded sampling-support bitmask as int32 storage of uint32 words,
+    [T, ld] with ld >= ceil(V/32) (default equal): token v is in row r's
+    support iff bit v % 32 of word v // 32 of row r is set.  Each bit is set
+    with probability 2^-j (j = 0: every token).  Bits past V and words past
+    ceil(V/32) are random too (consumers must ignore them).  ``targets``
+    (int64 [T], host) are forced into their rows' supports."""
+    nw = (V + 31) // 32
+    ld = nw if ld is None else ld
+    if ld < nw:
+        raise ValueError("ld < ceil(V/32)")
+    rng = _np_rng(seed, k)
+    words = np.full((T, ld), 0xFFFFFFFF, dtype=np.uint32)
+    for _ in range(j):
+        words &= rng.integers(0, 1 << 32, size=(T, ld), dtype=np.uint32)
+    if targets is not None:
+        t = np.asarray(targets, dtype=np.int64)
+        ok = (t >= 0) & (t < V)
+        r = np.nonzero(ok)[0]
+        words[r, t[ok] // 32] |= (np.uint32(1) << (t[ok] % 32).astype(np.uint32))
+    return words.view(np.int32)
 
 
 def sample_rows(n: int, k: int, seed: int = 1234):
