@@ -245,6 +245,20 @@ def launches_per_call(d):
     return gather + 3 * len(flp.row_chunks(d["n"], chunk))
 
 
+def time_calls(fn, steps, device, warmup=3):
+    """Device time (ms, CUDA events on the current stream) of `steps` calls of fn."""
+    for _ in range(warmup):
+        fn()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(device)
+    a.record()
+    for _ in range(steps):
+        fn()
+    b.record()
+    torch.cuda.synchronize(device)
+    return a.elapsed_time(b)
+
+
 def time_device(flp, d, steps, warmup, world, device, sampler=None):
     """Device time of `steps` calls (CUDA events) and of their tensor-core kernels."""
     w = d["workload"]
@@ -421,35 +435,44 @@ def run_ours(args):
             except Exception as e:  # a workload whose op is not available is reported, not fatal
                 extra[workloads.WORKLOADS[wid].name] = {"unavailable": str(e).splitlines()[0][:200]}
             torch.cuda.empty_cache()
-        # K-candidate scoring (4 target tokens per row) on the main workload's inputs
+        # K-candidate scoring (4 target tokens per row) and a sampling support
+        # (about 1/32 of the tokens per row, targets kept) on the main workload's inputs
         if d["workload"].kind == "fwd":
+            w = d["workload"]
+            shape = flp.make_shape(w.T, w.H, w.V, n, d["h"].dtype)
+            wsk = torch.empty(flp.workspace_size(shape, 0), dtype=torch.uint8, device=device)
             try:
-                w = d["workload"]
                 K = 4
                 g = torch.Generator(device=device)
                 g.manual_seed(w.seed * 100 + 30)
                 tk = torch.randint(0, w.V, (w.T, K), generator=g, device=device)
                 tk[:, 0] = d["targets"]
-                shape = flp.make_shape(w.T, w.H, w.V, n, d["h"].dtype)
-                wsk = torch.empty(flp.workspace_size(shape, 0), dtype=torch.uint8, device=device)
-                for _ in range(3):
-                    flp.logprob_entropy_k(d["h"], d["W"], tk, d["row_idx"], d["tau"], workspace=wsk)
-                steps = 20
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                torch.cuda.synchronize(device)
-                a.record()
-                for _ in range(steps):
-                    flp.logprob_entropy_k(d["h"], d["W"], tk, d["row_idx"], d["tau"], workspace=wsk)
-                b.record()
-                torch.cuda.synchronize(device)
-                tms = max_over_ranks(a.elapsed_time(b), world, device)
+                tms = time_calls(lambda: flp.logprob_entropy_k(
+                    d["h"], d["W"], tk, d["row_idx"], d["tau"], workspace=wsk), 20, device)
+                tms = max_over_ranks(tms, world, device)
                 extra[w.name + "-k4-candidates"] = {
-                    "config": dict(describe(d), candidates_per_row=K),
-                    "scored_tokens_per_s": job_throughput(n, steps, tms, world),
-                    "ms_per_step": tms / steps,
-                    "tflops": fl / (tms / steps / 1e3) / 1e12}
+                    "config": dict(describe(d), candidates_per_row=K), "steps": 20,
+                    "scored_tokens_per_s": job_throughput(n, 20, tms, world),
+                    "ms_per_step": tms / 20,
+                    "tflops": fl / (tms / 20 / 1e3) / 1e12}
             except Exception as e:  # reported, not fatal
-                extra[d["workload"].name + "-k4-candidates"] = {"unavailable": str(e)[:200]}
+                extra[w.name + "-k4-candidates"] = {"unavailable": str(e)[:200]}
+            try:
+                sup = torch.from_numpy(workloads.support_words(
+                    w.T, w.V, 5, w.seed, targets=d["targets"].cpu().numpy())).to(device)
+                tms = time_calls(lambda: flp.logprob_entropy(
+                    d["h"], d["W"], d["targets"], d["row_idx"], d["tau"], workspace=wsk,
+                    support=sup), 20, device)
+                tms = max_over_ranks(tms, world, device)
+                extra[w.name + "-sampling-support"] = {
+                    "config": dict(describe(d), support="each token kept with probability 1/32, "
+                                                        "targets kept"), "steps": 20,
+                    "scored_tokens_per_s": job_throughput(n, 20, tms, world),
+                    "ms_per_step": tms / 20,
+                    "tflops": fl / (tms / 20 / 1e3) / 1e12}
+                del sup
+            except Exception as e:  # reported, not fatal
+                extra[w.name + "-sampling-support"] = {"unavailable": str(e)[:200]}
         out["workloads"] = extra
 
     if rank == 0 and world == 1 and not args.no_cpu:

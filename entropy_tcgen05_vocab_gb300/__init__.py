@@ -7,6 +7,8 @@ step of the computation runs in the library's CUDA kernels; there is no CPU
 or PyTorch fallback, and a missing library raises.
 
     logp, ent = logprob_entropy(h, W, targets, row_idx, temperature)
+    logp, ent = logprob_entropy(h, W, targets, row_idx, temperature,
+                                support=pack_support(mask))        # sampling support
     kl = kl_divergence(h_s, W_s, h_t, W_t, row_idx)
     dh, dW = backward(h, W, targets, row_idx, temperature, g1, g2)
     logp, ent = FusedLogProbEntropy.apply(h, W, targets, row_idx, temperature)
@@ -19,7 +21,7 @@ import torch
 from . import _build
 
 __all__ = ["lib", "build", "workspace_size", "logprob_entropy", "logprob_entropy_k",
-           "kl_divergence", "backward",
+           "kl_divergence", "backward", "pack_support",
            "read_device_status", "plan", "set_kernel_events", "row_chunks", "FusedLogProbEntropy", "FlpError",
            "OP_LOGPROB_ENTROPY", "OP_KL", "OP_BACKWARD"]
 
@@ -41,7 +43,7 @@ class FlpShape(ctypes.Structure):
 
 class FlpDeviceStatus(ctypes.Structure):
     _fields_ = [("bad_targets", ctypes.c_uint32), ("bad_rows", ctypes.c_uint32),
-                ("timeouts", ctypes.c_uint32), ("reserved", ctypes.c_uint32)]
+                ("timeouts", ctypes.c_uint32), ("empty_supports", ctypes.c_uint32)]
 
 
 class FlpPlan(ctypes.Structure):
@@ -92,6 +94,14 @@ def lib():
     L.flp_selftest_wait_timeout.restype = ctypes.c_int
     L.flp_set_kernel_events.argtypes = [vp, vp]
     L.flp_set_kernel_events.restype = ctypes.c_int
+    L.flp_logprob_entropy_support.argtypes = [shp, vp, vp, vp, vp, vp, i64, f32, vp, vp, vp, vp,
+                                              vp, sz, vp]
+    L.flp_logprob_entropy_support.restype = ctypes.c_int
+    L.flp_backward_support.argtypes = [shp, vp, vp, vp, vp, vp, i64, f32, vp, vp, vp, vp, vp, vp,
+                                       vp, sz, vp]
+    L.flp_backward_support.restype = ctypes.c_int
+    L.flp_pack_support.argtypes = [vp, i64, i64, i64, vp, i64, vp]
+    L.flp_pack_support.restype = ctypes.c_int
     for f in (L.flp_logprob_entropy, L.flp_kl, L.flp_backward, L.flp_read_device_status,
               L.flp_plan_scoring):
         f.restype = ctypes.c_int
@@ -177,6 +187,34 @@ def _vector(x, name, n, device):
     return x.to(torch.float32).contiguous()
 
 
+def _support(x, T, V, device):
+    """(tensor, row stride in words) of a packed support, or (None, 0)."""
+    if x is None:
+        return None, 0
+    nw = (V + 31) // 32
+    if not isinstance(x, torch.Tensor) or x.device != device or x.dim() != 2 or \
+            x.dtype != torch.int32 or x.stride(1) != 1 or x.shape[0] != T or x.shape[1] < nw:
+        raise TypeError("support must be an int32 [T, >= ceil(V/32)] tensor of packed bits on "
+                        "%s (see pack_support)" % device)
+    return x, x.stride(0)
+
+
+def pack_support(mask, words=None):
+    """Pack a [T, V] bool/uint8 CUDA mask (True = token in the row's sampling
+    support) into int32 words [T, ceil(V/32)] (or ``words`` columns): bit v % 32
+    of word v // 32 is token v.  Runs on the GPU (flp_pack_support)."""
+    if not isinstance(mask, torch.Tensor) or not mask.is_cuda or mask.dim() != 2 or \
+            mask.dtype not in (torch.bool, torch.uint8) or mask.stride(1) != 1:
+        raise TypeError("mask must be a 2-D bool/uint8 CUDA tensor with unit column stride")
+    T, V = mask.shape
+    nw = (V + 31) // 32 if words is None else int(words)
+    out = torch.empty((T, nw), dtype=torch.int32, device=mask.device)
+    with torch.cuda.device(mask.device):
+        _check(lib().flp_pack_support(_ptr(mask), T, V, mask.stride(0), _ptr(out), nw,
+                                      _stream(mask.device)))
+    return out
+
+
 def _workspace(shape, op, device, workspace):
     need = workspace_size(shape, op)
     if need == 0:
@@ -187,12 +225,14 @@ def _workspace(shape, op, device, workspace):
 
 
 def logprob_entropy(h, W, targets, row_idx=None, temperature=1.0, *, return_stats=False,
-                    workspace=None):
+                    workspace=None, support=None):
     """Target log-prob and entropy of softmax(h[row_idx] W^T / temperature).
 
     h [T,H] and W [V,H] bf16/fp16 on the same GPU; targets int64 [T] indexed
     by h row; row_idx int64 [n] (or None: every row).  Returns float32 [n]
-    tensors (logp, ent), plus (lse, ez) if ``return_stats``.
+    tensors (logp, ent), plus (lse, ez) if ``return_stats``.  ``support``
+    (packed by :func:`pack_support`, [T, words] by h row) restricts each row
+    to its sampling support (logp = -inf for a target outside it).
     """
     _matrix(h, "h")
     _matrix(W, "W")
@@ -207,11 +247,19 @@ def logprob_entropy(h, W, targets, row_idx=None, temperature=1.0, *, return_stat
     ent = torch.empty(n, dtype=torch.float32, device=dev)
     lse = torch.empty(n, dtype=torch.float32, device=dev) if return_stats else None
     ez = torch.empty(n, dtype=torch.float32, device=dev) if return_stats else None
+    sup, lds = _support(support, h.shape[0], W.shape[0], dev)
     ws = _workspace(shape, OP_LOGPROB_ENTROPY, dev, workspace)
     with torch.cuda.device(dev):
-        _check(lib().flp_logprob_entropy(ctypes.byref(shape), _ptr(h), _ptr(W), _ptr(tg), _ptr(ri),
-                                         float(temperature), _ptr(logp), _ptr(ent), _ptr(lse),
-                                         _ptr(ez), _ptr(ws), ws.numel(), _stream(dev)))
+        if sup is None:
+            _check(lib().flp_logprob_entropy(ctypes.byref(shape), _ptr(h), _ptr(W), _ptr(tg),
+                                             _ptr(ri), float(temperature), _ptr(logp), _ptr(ent),
+                                             _ptr(lse), _ptr(ez), _ptr(ws), ws.numel(),
+                                             _stream(dev)))
+        else:
+            _check(lib().flp_logprob_entropy_support(
+                ctypes.byref(shape), _ptr(h), _ptr(W), _ptr(tg), _ptr(ri), _ptr(sup), lds,
+                float(temperature), _ptr(logp), _ptr(ent), _ptr(lse), _ptr(ez), _ptr(ws),
+                ws.numel(), _stream(dev)))
     if return_stats:
         return logp, ent, lse, ez
     return logp, ent
@@ -265,9 +313,11 @@ def kl_divergence(h_s, W_s, h_t, W_t, row_idx=None, *, workspace=None):
     return out
 
 
-def backward(h, W, targets, row_idx, temperature, g1, g2, lse=None, ez=None, *, workspace=None):
+def backward(h, W, targets, row_idx, temperature, g1, g2, lse=None, ez=None, *, workspace=None,
+             support=None):
     """dL/dh (dtype of h, [T,H]) and dL/dW (float32 [V,H]) of
-    L = sum g1 * logp + g2 * ent, by tile recompute."""
+    L = sum g1 * logp + g2 * ent, by tile recompute (under each row's
+    sampling support if ``support`` is given, as in :func:`logprob_entropy`)."""
     _matrix(h, "h")
     _matrix(W, "W")
     dev = h.device
@@ -284,11 +334,18 @@ def backward(h, W, targets, row_idx, temperature, g1, g2, lse=None, ez=None, *, 
     if h.stride(0) != h.shape[1] or W.stride(0) != W.shape[1]:
         h = h.contiguous()
         W = W.contiguous()
+    sup, lds = _support(support, h.shape[0], W.shape[0], dev)
     ws = _workspace(shape, OP_BACKWARD, dev, workspace)
     with torch.cuda.device(dev):
-        _check(lib().flp_backward(ctypes.byref(shape), _ptr(h), _ptr(W), _ptr(tg), _ptr(ri),
-                                  float(temperature), _ptr(g1), _ptr(g2), _ptr(lse), _ptr(ez),
-                                  _ptr(dh), _ptr(dW), _ptr(ws), ws.numel(), _stream(dev)))
+        if sup is None:
+            _check(lib().flp_backward(ctypes.byref(shape), _ptr(h), _ptr(W), _ptr(tg), _ptr(ri),
+                                      float(temperature), _ptr(g1), _ptr(g2), _ptr(lse), _ptr(ez),
+                                      _ptr(dh), _ptr(dW), _ptr(ws), ws.numel(), _stream(dev)))
+        else:
+            _check(lib().flp_backward_support(
+                ctypes.byref(shape), _ptr(h), _ptr(W), _ptr(tg), _ptr(ri), _ptr(sup), lds,
+                float(temperature), _ptr(g1), _ptr(g2), _ptr(lse), _ptr(ez), _ptr(dh), _ptr(dW),
+                _ptr(ws), ws.numel(), _stream(dev)))
     return dh, dW
 
 
@@ -299,25 +356,26 @@ def read_device_status(workspace, device=None):
     rc = lib().flp_read_device_status(_ptr(workspace), ctypes.byref(st), _stream(dev))
     if rc not in (0, 5):
         _check(rc)
-    return {k: getattr(st, k) for k, _ in FlpDeviceStatus._fields_[:3]}
+    return {k: getattr(st, k) for k, _ in FlpDeviceStatus._fields_}
 
 
 class FusedLogProbEntropy(torch.autograd.Function):
     """Autograd op: (h, W) -> (logp, ent); backward by tile recompute."""
 
     @staticmethod
-    def forward(ctx, h, W, targets, row_idx=None, temperature=1.0):
+    def forward(ctx, h, W, targets, row_idx=None, temperature=1.0, support=None):
         logp, ent, lse, ez = logprob_entropy(h, W, targets, row_idx, temperature,
-                                             return_stats=True)
-        ctx.save_for_backward(h, W, targets, row_idx, lse, ez)
+                                             return_stats=True, support=support)
+        ctx.save_for_backward(h, W, targets, row_idx, lse, ez, support)
         ctx.temperature = temperature
         return logp, ent
 
     @staticmethod
     def backward(ctx, g_logp, g_ent):
-        h, W, targets, row_idx, lse, ez = ctx.saved_tensors
+        h, W, targets, row_idx, lse, ez, support = ctx.saved_tensors
         n = lse.numel()
         g1 = g_logp if g_logp is not None else torch.zeros(n, device=h.device)
         g2 = g_ent if g_ent is not None else torch.zeros(n, device=h.device)
-        dh, dW = backward(h, W, targets, row_idx, ctx.temperature, g1, g2, lse, ez)
-        return dh, dW.to(W.dtype), None, None, None
+        dh, dW = backward(h, W, targets, row_idx, ctx.temperature, g1, g2, lse, ez,
+                          support=support)
+        return dh, dW.to(W.dtype), None, None, None, None

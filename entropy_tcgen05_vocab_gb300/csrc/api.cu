@@ -332,8 +332,20 @@ flp_status noalloc_scratch(void **out) {
   return FLP_OK;
 }
 
+// Checks of a sampling-support argument (null = no support restriction).
+flp_status check_support(const flp_shape *s, const uint32_t *support, int64_t ld_support) {
+  if (!support) return FLP_OK;
+  if (reinterpret_cast<uintptr_t>(support) % 4 != 0)
+    return fail(FLP_ERR_INVALID_ARG, "support must be 4-byte aligned");
+  if (ld_support < cdiv(s->V, 32))
+    return fail(FLP_ERR_INVALID_ARG, "ld_support (%lld) < ceil(V / 32) (%lld)",
+                static_cast<long long>(ld_support), static_cast<long long>(cdiv(s->V, 32)));
+  return FLP_OK;
+}
+
 flp_status logprob_impl(const flp_shape *s, const void *h, const void *W, const int64_t *targets,
-                        int K, const int64_t *row_idx, float temperature, float *out_logp,
+                        int K, const int64_t *row_idx, const uint32_t *support,
+                        int64_t ld_support, float temperature, float *out_logp,
                         float *out_ent, float *out_lse, float *out_ez, void *ws, size_t ws_bytes,
                         flp_stream_t stream) {
   g_err[0] = 0;
@@ -350,6 +362,7 @@ flp_status logprob_impl(const flp_shape *s, const void *h, const void *W, const 
   if (!h || !W || !targets || !out_logp || !out_ent)
     return fail(FLP_ERR_INVALID_ARG, "h, W, targets, out_logp and out_ent are required");
   if (!aligned16(h) || !aligned16(W)) return fail(FLP_ERR_INVALID_ARG, "h and W must be 16-byte aligned");
+  if ((st = check_support(s, support, ld_support)) != FLP_OK) return st;
   DeviceInfo dev;
   if ((st = device_info(&dev)) != FLP_OK) return st;
 
@@ -385,6 +398,8 @@ flp_status logprob_impl(const flp_shape *s, const void *h, const void *W, const 
   a.out_lse = out_lse;
   a.out_ez = out_ez;
   a.status = at<uint32_t>(ws, L.status);
+  a.support = support;
+  a.ld_support = ld_support;
 
   // status words and row-group counters are adjacent: one clear
   cudaError_t e = cudaMemsetAsync(a.status, 0, L.cnt + L.cnt_bytes - L.status, cs);
@@ -475,8 +490,20 @@ flp_status flp_logprob_entropy(const flp_shape *s, const void *h, const void *W,
                                const int64_t *targets, const int64_t *row_idx, float temperature,
                                float *out_logp, float *out_ent, float *out_lse, float *out_ez,
                                void *ws, size_t ws_bytes, flp_stream_t stream) {
-  return logprob_impl(s, h, W, targets, 1, row_idx, temperature, out_logp, out_ent, out_lse, out_ez,
-                      ws, ws_bytes, stream);
+  return logprob_impl(s, h, W, targets, 1, row_idx, nullptr, 0, temperature, out_logp, out_ent,
+                      out_lse, out_ez, ws, ws_bytes, stream);
+}
+
+flp_status flp_logprob_entropy_support(const flp_shape *s, const void *h, const void *W,
+                                       const int64_t *targets, const int64_t *row_idx,
+                                       const uint32_t *support, int64_t ld_support,
+                                       float temperature, float *out_logp, float *out_ent,
+                                       float *out_lse, float *out_ez, void *ws, size_t ws_bytes,
+                                       flp_stream_t stream) {
+  g_err[0] = 0;
+  if (!support) return fail(FLP_ERR_INVALID_ARG, "support is required");
+  return logprob_impl(s, h, W, targets, 1, row_idx, support, ld_support, temperature, out_logp,
+                      out_ent, out_lse, out_ez, ws, ws_bytes, stream);
 }
 
 flp_status flp_logprob_entropy_k(const flp_shape *s, const void *h, const void *W,
@@ -484,8 +511,8 @@ flp_status flp_logprob_entropy_k(const flp_shape *s, const void *h, const void *
                                  float temperature, float *out_logp, float *out_ent,
                                  float *out_lse, float *out_ez, void *ws, size_t ws_bytes,
                                  flp_stream_t stream) {
-  return logprob_impl(s, h, W, targets, K, row_idx, temperature, out_logp, out_ent, out_lse, out_ez,
-                      ws, ws_bytes, stream);
+  return logprob_impl(s, h, W, targets, K, row_idx, nullptr, 0, temperature, out_logp, out_ent,
+                      out_lse, out_ez, ws, ws_bytes, stream);
 }
 
 flp_status flp_kl(const flp_shape *s, const void *h_s, const void *W_s, const void *h_t,
@@ -550,10 +577,15 @@ flp_status flp_kl(const flp_shape *s, const void *h_s, const void *W_s, const vo
   return FLP_OK;
 }
 
-flp_status flp_backward(const flp_shape *s, const void *h, const void *W, const int64_t *targets,
-                        const int64_t *row_idx, float temperature, const float *g1,
-                        const float *g2, const float *lse, const float *ez, void *dh, float *dW,
-                        void *ws, size_t ws_bytes, flp_stream_t stream) {
+}  // extern "C"
+
+namespace flp {
+namespace {
+flp_status backward_impl(const flp_shape *s, const void *h, const void *W, const int64_t *targets,
+                         const int64_t *row_idx, const uint32_t *support, int64_t ld_support,
+                         float temperature, const float *g1, const float *g2, const float *lse,
+                         const float *ez, void *dh, float *dW, void *ws, size_t ws_bytes,
+                         flp_stream_t stream) {
   g_err[0] = 0;
   const KernelEvents ev;
   flp_status st = check_common(s, FLP_OP_BACKWARD, ws, ws_bytes);
@@ -570,6 +602,7 @@ flp_status flp_backward(const flp_shape *s, const void *h, const void *W, const 
     if (!aligned16(h) || !aligned16(W)) return fail(FLP_ERR_INVALID_ARG, "h and W must be 16-byte aligned");
     if (!row_idx && s->n_rows != s->T)
       return fail(FLP_ERR_INVALID_ARG, "row_idx is NULL but n_rows != T");
+    if ((st = check_support(s, support, ld_support)) != FLP_OK) return st;
   }
   DeviceInfo dev;
   if ((st = device_info(&dev)) != FLP_OK) return st;
@@ -622,6 +655,8 @@ flp_status flp_backward(const flp_shape *s, const void *h, const void *W, const 
     a.out_lse = at<float>(ws, L.lse);
     a.out_ez = at<float>(ws, L.ez);
     a.status = status;
+    a.support = support;
+    a.ld_support = ld_support;
     if ((e = launch_fwd_scoring(a, cs)) != cudaSuccess) return cuda_fail(e, "stats launch");
     lse = a.out_lse;
     ez = a.out_ez;
@@ -658,6 +693,8 @@ flp_status flp_backward(const flp_shape *s, const void *h, const void *W, const 
     ga.G = G;
     ga.ldg = ldg;
     ga.status = status;
+    ga.support = support;
+    ga.ld_support = ld_support;
     if ((e = launch_grad(ga, cs)) != cudaSuccess) return cuda_fail(e, "grad launch");
     // 2. dh[rows] = G W   (M = rc, N = H, K = V; W is MN-major for this product)
     GemmArgs da{};
@@ -691,6 +728,49 @@ flp_status flp_backward(const flp_shape *s, const void *h, const void *W, const 
     if ((e = launch_dw_gemm(wa, cs)) != cudaSuccess) return cuda_fail(e, "dW launch");
   }
   if ((e = ev.stop(cs)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+  return FLP_OK;
+}
+}  // namespace
+}  // namespace flp
+
+extern "C" {
+
+flp_status flp_backward(const flp_shape *s, const void *h, const void *W, const int64_t *targets,
+                        const int64_t *row_idx, float temperature, const float *g1,
+                        const float *g2, const float *lse, const float *ez, void *dh, float *dW,
+                        void *ws, size_t ws_bytes, flp_stream_t stream) {
+  return backward_impl(s, h, W, targets, row_idx, nullptr, 0, temperature, g1, g2, lse, ez, dh, dW,
+                       ws, ws_bytes, stream);
+}
+
+flp_status flp_backward_support(const flp_shape *s, const void *h, const void *W,
+                                const int64_t *targets, const int64_t *row_idx,
+                                const uint32_t *support, int64_t ld_support, float temperature,
+                                const float *g1, const float *g2, const float *lse,
+                                const float *ez, void *dh, float *dW, void *ws, size_t ws_bytes,
+                                flp_stream_t stream) {
+  g_err[0] = 0;
+  if (!support) return fail(FLP_ERR_INVALID_ARG, "support is required");
+  return backward_impl(s, h, W, targets, row_idx, support, ld_support, temperature, g1, g2, lse,
+                       ez, dh, dW, ws, ws_bytes, stream);
+}
+
+flp_status flp_pack_support(const uint8_t *mask, int64_t T, int64_t V, int64_t ld_mask,
+                            uint32_t *support, int64_t ld_support, flp_stream_t stream) {
+  g_err[0] = 0;
+  if (T < 0 || V <= 0) return fail(FLP_ERR_INVALID_ARG, "T must be >= 0 and V > 0");
+  if (ld_mask < V) return fail(FLP_ERR_INVALID_ARG, "ld_mask < V");
+  if (ld_support < cdiv(V, 32)) return fail(FLP_ERR_INVALID_ARG, "ld_support < ceil(V / 32)");
+  if (T == 0) return FLP_OK;
+  if (!mask || !support) return fail(FLP_ERR_INVALID_ARG, "mask and support are required");
+  if (reinterpret_cast<uintptr_t>(support) % 4 != 0)
+    return fail(FLP_ERR_INVALID_ARG, "support must be 4-byte aligned");
+  DeviceInfo dev;
+  const flp_status st = device_info(&dev);
+  if (st != FLP_OK) return st;
+  const cudaError_t e = launch_pack_support(mask, T, V, ld_mask, support, ld_support, dev.sms,
+                                            reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "pack launch");
   return FLP_OK;
 }
 
@@ -741,10 +821,11 @@ flp_status flp_read_device_status(const void *ws, flp_device_status *out, flp_st
   out->bad_targets = w[kStatBadTarget];
   out->bad_rows = w[kStatBadRow];
   out->timeouts = w[kStatTimeout];
-  out->reserved = 0;
-  if (out->bad_targets || out->bad_rows || out->timeouts)
-    return fail(FLP_ERR_DEVICE_STATUS, "device status: %u bad targets, %u bad rows, %u timeouts",
-                out->bad_targets, out->bad_rows, out->timeouts);
+  out->empty_supports = w[kStatEmptySupport];
+  if (out->bad_targets || out->bad_rows || out->timeouts || out->empty_supports)
+    return fail(FLP_ERR_DEVICE_STATUS,
+                "device status: %u bad targets, %u bad rows, %u timeouts, %u empty supports",
+                out->bad_targets, out->bad_rows, out->timeouts, out->empty_supports);
   return FLP_OK;
 }
 

@@ -12,6 +12,8 @@
 //      model dtype into the bounded chunk buffer G [R, V];
 //   2. dh[rows] = G W           (tcgen05 GEMM, K = V, W read MN-major);
 //   3. dW (+)= G^T h[rows]      (tcgen05 GEMM, K = R, both operands MN-major).
+// With a sampling support, LSE and E_p[z'] are taken over the support (the
+// statistics pass restricts them the same way) and G is 0 off the support.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -20,6 +22,7 @@
 #include "gemm_pipeline.cuh"
 #include "launch.h"
 #include "launch_util.cuh"
+#include "support.cuh"
 #include "vocab_pipeline.cuh"
 
 namespace flp {
@@ -61,6 +64,7 @@ __device__ __forceinline__ void store32_16(void *dst, const float (&v)[32], bool
 }  // namespace
 
 // ---------------------------------------------------------------- grad pass
+template <bool SUP>
 struct GradEpi {
   struct Params {
     int n;       // rows in the chunk
@@ -74,12 +78,16 @@ struct GradEpi {
     uint16_t *G;  // [n, ldg]
     int64_t ldg;
     bool bf16;
+    const uint32_t *support;  // SUP: [T, ld_support] words by h row
+    int64_t ld_support;
+    int tile_cols;
   };
   const Params p;
   float lse2, ez, a1, a2;
   int tgt;
   bool valid;
   uint16_t *grow;
+  SupportRow sup;
 
   __device__ __forceinline__ explicit GradEpi(const Params &pp) : p(pp) {}
 
@@ -88,6 +96,7 @@ struct GradEpi {
     tgt = -1;
     lse2 = ez = a1 = a2 = 0.f;
     grow = p.G + static_cast<int64_t>(valid ? row : 0) * p.ldg;
+    if (SUP) sup.reset(nullptr, p.V);
     if (!valid) return;
     const int i = p.r0 + row;
     lse2 = p.lse[i] * kLog2eF;
@@ -98,14 +107,22 @@ struct GradEpi {
     if (r >= 0 && r < p.T) {
       const int64_t t = p.targets[r];
       if (t >= 0 && t < p.V) tgt = static_cast<int>(t);
+      if (SUP) sup.reset(p.support + r * p.ld_support, p.V);
     }
   }
 
   __device__ __forceinline__ void tile(uint32_t taddr, int col0, int nchunks) {
+    uint32_t wn = 0u;
+    if (SUP) wn = sup.first(col0);
 #pragma unroll 1
     for (int c = 0; c < nchunks; ++c) {
       const int cb = col0 + c * 32;
       if (cb >= p.V) break;  // same for the whole warp
+      uint32_t w = 0u;
+      if (SUP) {
+        w = wn;
+        if (c + 1 < nchunks) wn = sup.load(cb + 32);
+      }
       float x[32];
       tmem_ld32(taddr + c * 32, x);
 #pragma unroll
@@ -119,6 +136,10 @@ struct GradEpi {
 #pragma unroll
         for (int j = 0; j < 32; ++j) x[j] += (rel == j) ? a1 : 0.f;
       }
+      if (SUP) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] = ((w >> j) & 1u) ? x[j] : 0.f;
+      }
       if (!valid) continue;
       if (cb + 32 <= p.V) {
         store32_16(grow + cb, x, p.bf16);
@@ -129,6 +150,7 @@ struct GradEpi {
           if (j < nv) grow[cb + j] = pack1(x[j], p.bf16);
       }
     }
+    if (SUP) sup.prefetch(col0 + p.tile_cols);
   }
 
   __device__ __forceinline__ void end(int, int) {}
@@ -220,11 +242,13 @@ struct DwEpi {
 // ---------------------------------------------------------------- launchers
 static_assert(kGradTileCols == 2 * kGradBN, "two MMAs per tile");
 using GradLayout = PipeLayout<kGradBN, kGradStages, 2, kGradCG, 1, true>;
-#define GRAD_KERNEL vocab_pipeline_kernel<kGradBN, kGradStages, 2, GradEpi, kGradCG, 1, kGradEpiWarps, true>
+#define GRAD_KERNEL(SUP) \
+  vocab_pipeline_kernel<kGradBN, kGradStages, 2, GradEpi<SUP>, kGradCG, 1, kGradEpiWarps, true>
 constexpr int kGradThreads = pipe_threads(kGradEpiWarps);
 
-cudaError_t launch_grad(const GradArgs &a, cudaStream_t stream) {
-  GradEpi::Params p;
+template <bool SUP>
+static cudaError_t launch_grad_t(const GradArgs &a, cudaStream_t stream) {
+  typename GradEpi<SUP>::Params p;
   p.n = a.sch.n;
   p.V = a.sch.V;
   p.r0 = a.r0;
@@ -240,17 +264,25 @@ cudaError_t launch_grad(const GradArgs &a, cudaStream_t stream) {
   p.G = static_cast<uint16_t *>(a.G);
   p.ldg = a.ldg;
   p.bf16 = a.bf16;
+  p.support = a.support;
+  p.ld_support = a.ld_support;
+  p.tile_cols = kGradTileCols;
   const uint32_t idesc = idesc_f16(a.bf16, kBM * kGradCG, kGradBN, false, false);
-  return launch_persistent(GRAD_KERNEL, a.grid, kGradThreads, GradLayout::kSmemBytes, kGradCG, stream, a.tmA,
-                           a.tmB, a.tmA, a.tmB, a.sch, idesc, p, a.status);
+  return launch_persistent(GRAD_KERNEL(SUP), a.grid, kGradThreads, GradLayout::kSmemBytes, kGradCG,
+                           stream, a.tmA, a.tmB, a.tmA, a.tmB, a.sch, idesc, p, a.status);
+}
+
+cudaError_t launch_grad(const GradArgs &a, cudaStream_t stream) {
+  return a.support ? launch_grad_t<true>(a, stream) : launch_grad_t<false>(a, stream);
 }
 
 int grad_units(int num_sms) {
   static int cached[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return resident_units(GRAD_KERNEL, kGradThreads, GradLayout::kSmemBytes, kGradCG, num_sms);
-  if (!cached[dev]) cached[dev] = resident_units(GRAD_KERNEL, kGradThreads, GradLayout::kSmemBytes, kGradCG, num_sms);
+  const auto kern = GRAD_KERNEL(false);
+  if (dev < 0 || dev >= 64) return resident_units(kern, kGradThreads, GradLayout::kSmemBytes, kGradCG, num_sms);
+  if (!cached[dev]) cached[dev] = resident_units(kern, kGradThreads, GradLayout::kSmemBytes, kGradCG, num_sms);
   return cached[dev];
 }
 

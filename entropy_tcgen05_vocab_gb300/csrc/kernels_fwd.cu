@@ -13,11 +13,16 @@
 // When m grows to m' the running sums are rescaled with a = 2^(m-m'):
 //   S <- a S,  B <- a (B + (m-m') S).
 // Then ln 2 (m + log2 S) = LSE(z/tau) and ln 2 (log2 S - B/S) = entropy.
+//
+// With a sampling support (SUP) only the support's columns enter m, S and B:
+// the log-prob and entropy are those of softmax(z/tau) restricted to the
+// support and renormalised, and a target outside it has log-prob -inf.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "launch.h"
 #include "launch_util.cuh"
+#include "support.cuh"
 #include "vocab_pipeline.cuh"
 
 namespace flp {
@@ -48,7 +53,8 @@ __global__ void gather_rows_kernel(const uint4 *__restrict__ h, int64_t ld_h16,
 // ---------------------------------------------------------------- epilogue
 // KMAX = largest number of target tokens per row the instantiation handles
 // (1 for log-prob + entropy; up to kMaxTargets for K-candidate scoring).
-template <int KMAX>
+// SUP: restrict each row to its sampling support.
+template <int KMAX, bool SUP = false>
 struct LseEpi {
   struct Params {
     const int64_t *targets;  // [T, K], by h row
@@ -66,11 +72,15 @@ struct LseEpi {
     float *out_logp;         // [n, K]
     float *out_ent, *out_lse, *out_ez;  // [n], any may be null
     uint32_t *status;
+    const uint32_t *support;  // SUP: [T, ld_support] words by h row
+    int64_t ld_support;
+    int tile_cols;            // vocabulary columns per tile
   };
   const Params p;
   float m, s0, s1, b0, b1;
   int tgt[KMAX];  // -1: no valid target (never matched)
   int row_;
+  SupportRow sup;
 
   __device__ __forceinline__ explicit LseEpi(const Params &pp) : p(pp) {}
 
@@ -80,9 +90,11 @@ struct LseEpi {
     row_ = row;
 #pragma unroll
     for (int k = 0; k < KMAX; ++k) tgt[k] = -1;
+    if (SUP) sup.reset(nullptr, p.V);
     if (row < p.n) {
       const int64_t r = p.row_idx ? p.row_idx[row] : row;
       if (r >= 0 && r < p.T) {
+        if (SUP) sup.reset(p.support + r * p.ld_support, p.V);
 #pragma unroll
         for (int k = 0; k < KMAX; ++k) {
           if (k < p.K) {
@@ -144,14 +156,43 @@ struct LseEpi {
     }
   }
 
+  // Fold of the columns whose bit is set in w (w already clipped to V).
+  __device__ __forceinline__ void fold_support(const float (&x)[32], uint32_t w) {
+    float cmax = -FLT_MAX;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) cmax = ((w >> j) & 1u) ? fmaxf(cmax, x[j]) : cmax;
+    rescale(cmax);
+    const float nm = -m;
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+      const float d0 = fmaf(x[j], p.sl, nm);
+      const float d1 = fmaf(x[j + 1], p.sl, nm);
+      const float e0 = ((w >> j) & 1u) ? ex2(d0) : 0.f;
+      const float e1 = ((w >> (j + 1)) & 1u) ? ex2(d1) : 0.f;
+      s0 += e0;
+      s1 += e1;
+      b0 = fmaf(e0, d0, b0);
+      b1 = fmaf(e1, d1, b1);
+    }
+  }
+
   __device__ __forceinline__ void tile(uint32_t taddr, int col0, int nchunks) {
+    uint32_t wn = 0u;
+    if (SUP) wn = sup.first(col0);
 #pragma unroll 1
     for (int c = 0; c < nchunks; ++c) {
       const int cb = col0 + c * 32;
       if (cb >= p.V) break;  // same for the whole warp
+      uint32_t w = 0u;
+      if (SUP) {
+        w = wn;
+        if (c + 1 < nchunks) wn = sup.load(cb + 32);
+      }
       float x[32];
       tmem_ld32(taddr + c * 32, x);
-      if (cb + 32 <= p.V)
+      if (SUP)
+        fold_support(x, sup.clip(w, cb));
+      else if (cb + 32 <= p.V)
         fold_full(x);
       else
         fold_masked(x, p.V - cb);
@@ -167,6 +208,7 @@ struct LseEpi {
         }
       }
     }
+    if (SUP) sup.prefetch(col0 + p.tile_cols);
   }
 
   __device__ __forceinline__ void end(int split, int row) {
@@ -203,9 +245,14 @@ struct LseEpi {
     const float qnan = __int_as_float(0x7fc00000);
     const int64_t r = p.row_idx ? p.row_idx[i] : i;
     const bool row_ok = r >= 0 && r < p.T;
+    bool empty = false;
     if (!row_ok) {
       atomicAdd(p.status + kStatBadRow, 1u);
       lse = ent = qnan;
+    } else if (SUP && !(S > 0.f)) {  // no token of the row is in its support
+      atomicAdd(p.status + kStatEmptySupport, 1u);
+      lse = ent = qnan;
+      empty = true;
     }
     for (int k = 0; k < p.K; ++k) {
       const size_t o = static_cast<size_t>(i) * p.K + k;
@@ -214,6 +261,8 @@ struct LseEpi {
         const int64_t t = p.targets[r * p.K + k];
         if (t < 0 || t >= p.V)
           atomicAdd(p.status + kStatBadTarget, 1u);
+        else if (SUP && !empty && !((__ldg(p.support + r * p.ld_support + (t >> 5)) >> (t & 31)) & 1u))
+          logp = -INFINITY;  // target outside the support
         else
           logp = __ldcg(p.zt + o) * p.inv_tau - lse;
       }
@@ -240,13 +289,13 @@ cudaError_t launch_gather(const void *h, int64_t ld_h, const int64_t *row_idx, i
 
 static_assert(kFwdTileCols == 2 * kFwdBN, "two MMAs per tile");
 using FwdLayout = PipeLayout<kFwdBN, kFwdStages, 2, kFwdCG, 1, true>;
-#define FWD_KERNEL(KMAX) \
-  vocab_pipeline_kernel<kFwdBN, kFwdStages, 2, LseEpi<KMAX>, kFwdCG, 1, kFwdEpiWarps, true>
+#define FWD_KERNEL(KMAX, SUP) \
+  vocab_pipeline_kernel<kFwdBN, kFwdStages, 2, LseEpi<KMAX, SUP>, kFwdCG, 1, kFwdEpiWarps, true>
 constexpr int kFwdThreads = pipe_threads(kFwdEpiWarps);
 
-template <int KMAX>
+template <int KMAX, bool SUP>
 static cudaError_t launch_fwd_k(const FwdArgs &a, cudaStream_t stream) {
-  typename LseEpi<KMAX>::Params p;
+  typename LseEpi<KMAX, SUP>::Params p;
   p.targets = a.targets;
   p.K = a.K;
   p.row_idx = a.row_idx;
@@ -266,21 +315,28 @@ static cudaError_t launch_fwd_k(const FwdArgs &a, cudaStream_t stream) {
   p.out_lse = a.out_lse;
   p.out_ez = a.out_ez;
   p.status = a.status;
+  p.support = a.support;
+  p.ld_support = a.ld_support;
+  p.tile_cols = kFwdTileCols;
   const uint32_t idesc = idesc_f16(a.bf16, kBM * kFwdCG, kFwdBN, false, false);
-  return launch_persistent(FWD_KERNEL(KMAX), a.grid, kFwdThreads, FwdLayout::kSmemBytes, kFwdCG,
+  return launch_persistent(FWD_KERNEL(KMAX, SUP), a.grid, kFwdThreads, FwdLayout::kSmemBytes, kFwdCG,
                            stream, a.tmA, a.tmB, a.tmA, a.tmB, a.sch, idesc, p, a.status);
 }
 
 cudaError_t launch_fwd_scoring(const FwdArgs &a, cudaStream_t stream) {
-  if (a.K == 1) return launch_fwd_k<1>(a, stream);
-  return launch_fwd_k<kMaxTargets>(a, stream);
+  if (a.support) {
+    if (a.K != 1) return cudaErrorInvalidValue;  // the host API never asks for this
+    return launch_fwd_k<1, true>(a, stream);
+  }
+  if (a.K == 1) return launch_fwd_k<1, false>(a, stream);
+  return launch_fwd_k<kMaxTargets, false>(a, stream);
 }
 
 int fwd_units(int num_sms) {
   static int cached[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
-  const auto kern = FWD_KERNEL(1);
+  const auto kern = FWD_KERNEL(1, false);
   if (dev < 0 || dev >= 64) return resident_units(kern, kFwdThreads, FwdLayout::kSmemBytes, kFwdCG, num_sms);
   if (!cached[dev]) cached[dev] = resident_units(kern, kFwdThreads, FwdLayout::kSmemBytes, kFwdCG, num_sms);
   return cached[dev];

@@ -64,6 +64,8 @@ struct FwdArgs {
   uint32_t *counters;  // [ceil(n / 32)] zeroed before the launch
   float *out_logp, *out_ent, *out_lse, *out_ez;
   uint32_t *status;
+  const uint32_t *support;  // [T, ld_support] sampling-support words, or null
+  int64_t ld_support;
 };
 
 struct KlArgs {
@@ -95,6 +97,8 @@ struct GradArgs {
   void *G;          // [R, ldg] model dtype
   int64_t ldg;
   uint32_t *status;
+  const uint32_t *support;  // [T, ld_support] sampling-support words, or null
+  int64_t ld_support;
 };
 
 struct GemmArgs {
@@ -127,6 +131,12 @@ int dw_gemm_tiles(int M, int N);
 int gemm_cta_group();
 int gemm_units(int num_sms);
 int fwd_smem_bytes();
+// support[r, w] (w < ld_support) = bits 32w .. 32w+31 of mask row r (a byte
+// per token, non-zero = in the support); bits past V and words past
+// ceil(V/32) are 0.
+cudaError_t launch_pack_support(const uint8_t *mask, int64_t T, int64_t V, int64_t ld_mask,
+                                uint32_t *support, int64_t ld_support, int num_sms,
+                                cudaStream_t stream);
 cudaError_t launch_wait_timeout(uint64_t limit_ns, uint32_t *status, cudaStream_t stream);
 // CTAs or CTA pairs of each pipeline that can be resident at once.
 int fwd_units(int num_sms);

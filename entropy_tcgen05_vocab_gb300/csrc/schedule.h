@@ -12,6 +12,7 @@ namespace flp {
 constexpr int kStatBadTarget = 0;
 constexpr int kStatBadRow = 1;
 constexpr int kStatTimeout = 2;
+constexpr int kStatEmptySupport = 3;
 
 // Work item = (row tile, vocabulary split).  Items are ordered band by band:
 // within a band of `band` row tiles, all items of split 0 (row tiles

@@ -91,7 +91,7 @@ typedef struct {
     uint32_t bad_targets; /* scored rows whose target was outside [0, V) */
     uint32_t bad_rows;    /* row_idx entries outside [0, T) */
     uint32_t timeouts;    /* pipeline waits that gave up; outputs of that call are invalid */
-    uint32_t reserved;
+    uint32_t empty_supports; /* scored rows whose sampling support held no token */
 } flp_device_status;
 
 /*
@@ -148,6 +148,43 @@ flp_status flp_logprob_entropy_k(const flp_shape *shape, const void *h, const vo
                                  void *workspace, size_t workspace_bytes, flp_stream_t stream);
 
 /*
+ * Log-prob and entropy under each row's sampling support (miles PR #2764
+ * summary, math_utils.py snippet: the sampling_mask argument of
+ * calculate_log_probs_and_entropy, cut into row chunks with the logits and
+ * tokens).  The distribution of row r is softmax(z') restricted to the
+ * tokens of its support S_r and renormalised; tokens off S_r have
+ * probability 0:
+ *   out_logp   z'_tgt - log sum_{v in S} exp(z'_v); -INFINITY if tgt is not in S
+ *   out_ent    entropy (nats) of the restricted distribution
+ *   out_lse    log sum_{v in S} exp(z'_v);   out_ez = sum_{v in S} p_v z'_v
+ *   support    [T, ld_support] uint32 words, DEVICE, indexed by h row (like
+ *              targets): token v is in row r's support iff bit (v % 32) of
+ *              support[r * ld_support + v / 32] is set.  Bits at v >= V are
+ *              ignored.  4-byte aligned; ld_support >= ceil(V / 32).
+ *              flp_pack_support builds it from a byte-per-token mask.
+ * Other arguments as in flp_logprob_entropy; same workspace.  A row whose
+ * support holds no token gets NaN outputs and is counted in empty_supports.
+ */
+flp_status flp_logprob_entropy_support(const flp_shape *shape, const void *h, const void *W,
+                                       const int64_t *targets, const int64_t *row_idx,
+                                       const uint32_t *support, int64_t ld_support,
+                                       float temperature, float *out_logp, float *out_ent,
+                                       float *out_lse, float *out_ez,
+                                       void *workspace, size_t workspace_bytes,
+                                       flp_stream_t stream);
+
+/*
+ * Packs a byte-per-token support mask into the bit words the *_support entry
+ * points read: support[r * ld_support + w] gets bit j set iff
+ * mask[r * ld_mask + 32 w + j] != 0 (and 32 w + j < V).  Bits past V and
+ * words past ceil(V / 32) are written as 0.
+ *   mask      [T, ld_mask] uint8 (e.g. a torch.bool tensor), DEVICE, ld_mask >= V
+ *   support   [T, ld_support] uint32, DEVICE, 4-byte aligned, ld_support >= ceil(V / 32)
+ */
+flp_status flp_pack_support(const uint8_t *mask, int64_t T, int64_t V, int64_t ld_mask,
+                            uint32_t *support, int64_t ld_support, flp_stream_t stream);
+
+/*
  * Full-vocabulary KL(teacher || student) per scored row:
  *   KL = sum_v p_t,v (log p_t,v - log p_s,v),
  *   p_s = softmax(h_s[row] W_s^T),  p_t = softmax(h_t[row] W_t^T),
@@ -185,6 +222,22 @@ flp_status flp_backward(const flp_shape *shape, const void *h, const void *W,
                         float temperature, const float *g1, const float *g2,
                         const float *lse, const float *ez, void *dh, float *dW,
                         void *workspace, size_t workspace_bytes, flp_stream_t stream);
+
+/*
+ * flp_backward under each row's sampling support (as in
+ * flp_logprob_entropy_support): p, lse and E_p[z'] are taken over the row's
+ * support, and
+ *   G_iv = 1[v in S_i] (g1[i] (1[v = tgt_i] - p_iv) - g2[i] p_iv (z'_iv - E_p[z'_i])) / temperature
+ * (a target outside S_i contributes no one-hot term).  lse and ez, if
+ * given, must come from flp_logprob_entropy_support with the same support.
+ * Every scored row's support must hold at least one token.
+ */
+flp_status flp_backward_support(const flp_shape *shape, const void *h, const void *W,
+                                const int64_t *targets, const int64_t *row_idx,
+                                const uint32_t *support, int64_t ld_support, float temperature,
+                                const float *g1, const float *g2, const float *lse,
+                                const float *ez, void *dh, float *dW,
+                                void *workspace, size_t workspace_bytes, flp_stream_t stream);
 
 /*
  * Synchronises `stream` and copies the device status of the last call that

@@ -169,3 +169,34 @@ def test_row_chunks_follow_torch_chunk(L, n, c):
 def test_selftest_limit_is_validated_on_host(L, limit):
     assert L.flp_selftest_wait_timeout(limit, FAKE, None) == 1
     assert L.flp_selftest_wait_timeout(50_000_000, None, None) == 3
+
+
+def test_support_entry_points_validate_on_host(L):
+    s = _shape()                       # V = 8192: 256 words per row
+    sup = ctypes.c_void_p(1 << 21)
+
+    def fwd(support=sup, ld=256, ws_bytes=1 << 40):
+        return L.flp_logprob_entropy_support(ctypes.byref(s), FAKE, FAKE, FAKE, None, support, ld,
+                                             ctypes.c_float(1.0), FAKE, FAKE, None, None, FAKE,
+                                             ctypes.c_size_t(ws_bytes), None)
+
+    assert fwd(support=None) == 1
+    assert fwd(ld=255) == 1
+    assert b"ld_support" in L.flp_last_error()
+    assert fwd(support=ctypes.c_void_p((1 << 21) + 2)) == 1      # 4-byte alignment
+    assert fwd(ws_bytes=10) == 3
+
+    def bwd(support=sup, ld=256):
+        return L.flp_backward_support(ctypes.byref(s), FAKE, FAKE, FAKE, None, support, ld,
+                                      ctypes.c_float(0.7), FAKE, FAKE, None, None, FAKE, FAKE,
+                                      FAKE, ctypes.c_size_t(1 << 40), None)
+
+    assert bwd(support=None) == 1
+    assert bwd(ld=100) == 1
+    i64 = ctypes.c_int64
+    pack = L.flp_pack_support
+    assert pack(FAKE, i64(4), i64(70), i64(69), sup, i64(3), None) == 1       # ld_mask < V
+    assert pack(FAKE, i64(4), i64(70), i64(70), sup, i64(2), None) == 1       # ld_support < 3
+    assert pack(FAKE, i64(4), i64(0), i64(70), sup, i64(3), None) == 1        # V = 0
+    assert pack(None, i64(0), i64(70), i64(70), None, i64(3), None) == 0      # nothing to pack
+    assert pack(None, i64(4), i64(70), i64(70), sup, i64(3), None) == 1

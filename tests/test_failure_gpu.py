@@ -27,7 +27,8 @@ def _lib():
 
 def test_stalled_wait_is_reported_and_the_context_survives():
     st = flp.selftest_wait_timeout(50_000_000)
-    assert st == {"bad_targets": 0, "bad_rows": 0, "timeouts": 1}
+    assert st == {"bad_targets": 0, "bad_rows": 0, "timeouts": 1,
+                  "empty_supports": 0}
     d = workloads.make(0, device="cuda")
     logp, ent = flp.logprob_entropy(d["h"], d["W"], d["targets"], None, 1.0)
     o = coracle.logprob_entropy(d["h"].cpu(), d["W"].cpu(), d["targets"].cpu(), None, 1.0, "bf16")
@@ -40,4 +41,5 @@ def test_normal_calls_report_no_timeouts():
     shape = flp.make_shape(300, 256, 5000, 300, torch.bfloat16)
     ws = torch.empty(flp.workspace_size(shape, flp.OP_KL), dtype=torch.uint8, device="cuda")
     flp.kl_divergence(d["h_s"], d["W_s"], d["h_t"], d["W_t"], None, workspace=ws)
-    assert flp.read_device_status(ws) == {"bad_targets": 0, "bad_rows": 0, "timeouts": 0}
+    assert flp.read_device_status(ws) == {"bad_targets": 0, "bad_rows": 0, "timeouts": 0,
+                                          "empty_supports": 0}

@@ -155,7 +155,7 @@ def test_bad_targets_and_rows_are_nan_and_counted():
                      device="cuda")
     logp, ent = flp.logprob_entropy(d["h"], d["W"], tg, rows, 1.0, workspace=ws)
     st = flp.read_device_status(ws)
-    assert st == {"bad_targets": 2, "bad_rows": 2, "timeouts": 0}
+    assert st == {"bad_targets": 2, "bad_rows": 2, "timeouts": 0, "empty_supports": 0}
     lp, en = logp.cpu().numpy(), ent.cpu().numpy()
     assert np.isnan(lp[[0, 2, 3, 4]]).all() and np.isfinite(lp[[1, 5]]).all()
     assert np.isfinite(en[[0, 1, 2, 5]]).all() and np.isnan(en[[3, 4]]).all()
