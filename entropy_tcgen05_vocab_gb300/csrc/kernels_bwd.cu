@@ -80,7 +80,7 @@ struct GradEpi {
     bool bf16;
     const uint32_t *support;  // SUP: [T, ld_support] words by h row
     int64_t ld_support;
-    int tile_cols;
+    int tile_cols;            // columns from one tile() call of a warp to its next
   };
   const Params p;
   float lse2, ez, a1, a2;
@@ -112,17 +112,12 @@ struct GradEpi {
   }
 
   __device__ __forceinline__ void tile(uint32_t taddr, int col0, int nchunks) {
-    uint32_t wn = 0u;
-    if (SUP) wn = sup.first(col0);
+    if (SUP) sup.start(col0);
 #pragma unroll 1
     for (int c = 0; c < nchunks; ++c) {
       const int cb = col0 + c * 32;
       if (cb >= p.V) break;  // same for the whole warp
-      uint32_t w = 0u;
-      if (SUP) {
-        w = wn;
-        if (c + 1 < nchunks) wn = sup.load(cb + 32);
-      }
+      const uint32_t w = SUP ? sup.next(col0, c) : 0u;
       float x[32];
       tmem_ld32(taddr + c * 32, x);
 #pragma unroll

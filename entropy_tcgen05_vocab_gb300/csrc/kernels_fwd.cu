@@ -16,7 +16,16 @@
 //
 // With a sampling support (SUP) only the support's columns enter m, S and B:
 // the log-prob and entropy are those of softmax(z/tau) restricted to the
-// support and renormalised, and a target outside it has log-prob -inf.
+// support and renormalised, and a target outside it has log-prob -inf.  A
+// column off the support has its logit replaced by a sentinel zs with
+// y_s = zs * log2(e)/tau = -2^120 (finite), and the running max starts at
+// y_s / 2 instead of -FLT_MAX: the sentinel never raises m, and every
+// off-support term is 2^(y_s - m) <= 2^(y_s / 2) = 0 with a finite exponent,
+// so it adds exactly 0 to S and B.  One select per logit; the fold itself is
+// the unrestricted one.
+#include <algorithm>
+#include <cfloat>
+
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -64,6 +73,7 @@ struct LseEpi {
     int n;
     int V;
     float sl;                // log2(e) / tau
+    float zsent;             // SUP: logit given to columns off the support
     float *pm, *ps, *pb;     // [slots][n] partial m, S, B
     float *zt;               // [n, K] raw FP32 logits of the targets
     uint32_t *counters;      // [ceil(n/32)] items finished per 32-row group
@@ -74,7 +84,7 @@ struct LseEpi {
     uint32_t *status;
     const uint32_t *support;  // SUP: [T, ld_support] words by h row
     int64_t ld_support;
-    int tile_cols;            // vocabulary columns per tile
+    int tile_cols;            // columns from one tile() call of a warp to its next
   };
   const Params p;
   float m, s0, s1, b0, b1;
@@ -85,7 +95,7 @@ struct LseEpi {
   __device__ __forceinline__ explicit LseEpi(const Params &pp) : p(pp) {}
 
   __device__ __forceinline__ void begin(int /*mt*/, int row) {
-    m = -FLT_MAX;
+    m = SUP ? 0.5f * (p.zsent * p.sl) : -FLT_MAX;
     s0 = s1 = b0 = b1 = 0.f;
     row_ = row;
 #pragma unroll
@@ -156,46 +166,26 @@ struct LseEpi {
     }
   }
 
-  // Fold of the columns whose bit is set in w (w already clipped to V).
-  __device__ __forceinline__ void fold_support(const float (&x)[32], uint32_t w) {
-    float cmax = -FLT_MAX;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) cmax = ((w >> j) & 1u) ? fmaxf(cmax, x[j]) : cmax;
-    rescale(cmax);
-    const float nm = -m;
-#pragma unroll
-    for (int j = 0; j < 32; j += 2) {
-      const float d0 = fmaf(x[j], p.sl, nm);
-      const float d1 = fmaf(x[j + 1], p.sl, nm);
-      const float e0 = ((w >> j) & 1u) ? ex2(d0) : 0.f;
-      const float e1 = ((w >> (j + 1)) & 1u) ? ex2(d1) : 0.f;
-      s0 += e0;
-      s1 += e1;
-      b0 = fmaf(e0, d0, b0);
-      b1 = fmaf(e1, d1, b1);
-    }
-  }
-
   __device__ __forceinline__ void tile(uint32_t taddr, int col0, int nchunks) {
-    uint32_t wn = 0u;
-    if (SUP) wn = sup.first(col0);
+    if (SUP) sup.start(col0);
 #pragma unroll 1
     for (int c = 0; c < nchunks; ++c) {
       const int cb = col0 + c * 32;
       if (cb >= p.V) break;  // same for the whole warp
-      uint32_t w = 0u;
-      if (SUP) {
-        w = wn;
-        if (c + 1 < nchunks) wn = sup.load(cb + 32);
-      }
+      const uint32_t w = SUP ? sup.next(col0, c) : 0u;
       float x[32];
       tmem_ld32(taddr + c * 32, x);
-      if (SUP)
-        fold_support(x, sup.clip(w, cb));
-      else if (cb + 32 <= p.V)
+      if (SUP) {
+        const uint32_t wc = sup.clip(w, cb);
+        float xs[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) xs[j] = ((wc >> j) & 1u) ? x[j] : p.zsent;
+        fold_full(xs);
+      } else if (cb + 32 <= p.V) {
         fold_full(x);
-      else
+      } else {
         fold_masked(x, p.V - cb);
+      }
       // each target column lies in exactly one chunk: store its raw logit there
 #pragma unroll
       for (int k = 0; k < KMAX; ++k) {
@@ -303,6 +293,9 @@ static cudaError_t launch_fwd_k(const FwdArgs &a, cudaStream_t stream) {
   p.n = a.sch.n;
   p.V = a.sch.V;
   p.sl = a.scale_log2;
+  // y of the sentinel: -2^120, or as close as a finite float logit gets
+  p.zsent = static_cast<float>(
+      std::max(-1.329227995784916e36 / static_cast<double>(a.scale_log2), -0.5 * FLT_MAX));
   p.pm = a.pm;
   p.ps = a.ps;
   p.pb = a.pb;
