@@ -34,6 +34,11 @@ def lib():
         _lib.orc_backward_support.argtypes = [i64, i64, vp, ip, i64, vp, ip, i64, vp, i64, i64,
                                               vp, vp, i64, dbl, vp, vp, vp, vp, i64, vp]
         _lib.orc_backward_support.restype = ip
+        _lib.orc_mxfp4_quantize.argtypes = [vp, ip, i64, i64, i64, i64, vp, vp]
+        _lib.orc_mxfp4_quantize.restype = ip
+        _lib.orc_mxfp4_dequantize.argtypes = [vp, vp, i64, i64, i64, vp]
+        _lib.orc_kl_mxfp4.argtypes = [i64, i64, vp, vp, vp, vp, vp, i64, ip, i64, i64, vp, i64, vp]
+        _lib.orc_kl_mxfp4.restype = ip
         _lib.orc_num_threads.restype = ip
         for f in (_lib.orc_logprob_entropy, _lib.orc_kl, _lib.orc_backward):
             f.restype = ip
@@ -223,3 +228,50 @@ def backward_support(h, W, targets, rows, support, tau, g1, g2, dtype, vsel=None
     if rc:
         raise RuntimeError("oracle backward_support failed: %d" % rc)
     return dh, dW
+
+
+def mxfp4_vpad(V):
+    """Rows of the blocked MXFP4 layout: V rounded up to a multiple of 256."""
+    return -(-V // 256) * 256
+
+
+def mxfp4_quantize(W, dtype):
+    """C quantiser: (packed uint8 [H/64, V_pad, 32], scales uint8 [H/64, V_pad, 2])."""
+    ws, wt, ldw = storage(W, dtype)
+    V, H = ws.shape[0], ldw
+    Vp = mxfp4_vpad(V)
+    packed = np.empty((H // 64, Vp, 32), np.uint8)
+    scales = np.empty((H // 64, Vp, 2), np.uint8)
+    rc = lib().orc_mxfp4_quantize(ws.ctypes.data, wt, V, H, ldw, Vp, packed.ctypes.data,
+                                  scales.ctypes.data)
+    if rc:
+        raise ValueError("H must be a multiple of 64")
+    return packed, scales
+
+
+def mxfp4_dequantize(packed, scales, V):
+    packed = np.ascontiguousarray(packed, np.uint8)
+    scales = np.ascontiguousarray(scales, np.uint8)
+    H = packed.shape[0] * 64
+    out = np.empty((V, H))
+    lib().orc_mxfp4_dequantize(packed.ctypes.data, scales.ctypes.data, V, H, packed.shape[1],
+                               out.ctypes.data)
+    return out
+
+
+def kl_mxfp4(h_s, W_s, h_t, packed, scales, rows, dtype):
+    """Per scored row KL(teacher || student), the teacher head in MXFP4."""
+    a, ty, ldh = storage(h_s, dtype)
+    b, _, ldw = storage(W_s, dtype)
+    c, _, _ = storage(h_t, dtype)
+    packed = np.ascontiguousarray(packed, np.uint8)
+    scales = np.ascontiguousarray(scales, np.uint8)
+    T, V = a.shape[0], b.shape[0]
+    rows = _i64(rows if rows is not None else np.arange(T))
+    out = np.empty(rows.shape[0], dtype=np.float64)
+    rc = lib().orc_kl_mxfp4(ldh, V, a.ctypes.data, b.ctypes.data, c.ctypes.data,
+                            packed.ctypes.data, scales.ctypes.data, packed.shape[1], ty, ldh,
+                            ldw, _ptr(rows), rows.shape[0], out.ctypes.data)
+    if rc:
+        raise RuntimeError("oracle kl_mxfp4 failed: %d" % rc)
+    return out

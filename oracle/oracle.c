@@ -42,7 +42,36 @@
 #endif
 
 /* Element types of the matrices handed to the oracle. */
-enum { ORC_BF16 = 0, ORC_FP16 = 1, ORC_F64 = 2 };
+enum { ORC_BF16 = 0, ORC_FP16 = 1, ORC_F64 = 2, ORC_MXFP4 = 3 };
+
+/*
+ * A matrix [V, H] stored in MXFP4 (OCP Microscaling: E2M1 elements, one
+ * E8M0 power-of-two scale per 32 consecutive elements of a row), in the
+ * blocked layout the library uses: for each 64-wide column block kb and each
+ * row v < V_pad, 32 bytes of elements (byte b: element 2b in the low nibble,
+ * 2b+1 in the high nibble) at packed[(kb * V_pad + v) * 32] and two scale
+ * codes at scales[(kb * V_pad + v) * 2] (elements 0..31 and 32..63 of the
+ * block).  Handed to orc_decode as a pointer to this struct.
+ */
+typedef struct {
+    const uint8_t *packed;
+    const uint8_t *scales;
+    int64_t V_pad;
+    int64_t H;
+} orc_mx_matrix;
+
+/* E2M1 magnitudes by code (sign in bit 3): 1 sign, 2 exponent (bias 1), 1 mantissa bit. */
+static const double orc_e2m1_mag[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+
+static double orc_mx_element(const orc_mx_matrix *m, int64_t v, int64_t k)
+{
+    int64_t blk = (k / 64) * m->V_pad + v;
+    uint8_t byte = m->packed[blk * 32 + (k % 64) / 2];
+    int code = (k % 2) ? (byte >> 4) : (byte & 15);
+    int sc = m->scales[blk * 2 + (k % 64) / 32];
+    double mag = ldexp(orc_e2m1_mag[code & 7], sc - 127);
+    return (code & 8) ? -mag : mag;
+}
 
 /* Rows of h whose logits are held at once. */
 #define ORC_ROW_BLOCK 32
@@ -82,6 +111,9 @@ static void orc_decode(const void *p, int type, int64_t off, int64_t n, double *
     } else if (type == ORC_FP16) {
         const uint16_t *q = (const uint16_t *)p + off;
         for (i = 0; i < n; ++i) out[i] = orc_fp16(q[i]);
+    } else if (type == ORC_MXFP4) {
+        const orc_mx_matrix *m = (const orc_mx_matrix *)p;
+        for (i = 0; i < n; ++i) out[i] = orc_mx_element(m, (off + i) / m->H, (off + i) % m->H);
     } else {
         const double *q = (const double *)p + off;
         for (i = 0; i < n; ++i) out[i] = q[i];
@@ -537,5 +569,111 @@ int orc_backward_support(int64_t H, int64_t V,
         }
     }
     free(hd); free(z); free(wd);
+    return 0;
+}
+
+/*
+ * MXFP4 quantisation of W [V, H] (bf16/fp16/f64), OCP Microscaling rule, per
+ * 32 consecutive elements x_0..x_31 of a row:
+ *   e = floor(log2(max |x_i|)) - 2   (2 = exponent of E2M1's largest value, 6)
+ *   scale code = e + 127, clamped to [0, 254]; all-zero block: code 0
+ *   element = the E2M1 value nearest to x_i / 2^(code - 127), ties to the
+ *             even code (mantissa bit 0), magnitudes above 6 saturated to 6;
+ *             a zero magnitude is stored as +0 (code 0).
+ * Output in the blocked layout of orc_mx_matrix, V_pad >= V rows (rows past V
+ * are zero).  H must be a multiple of 64.
+ */
+int orc_mxfp4_quantize(const void *W, int wtype, int64_t V, int64_t H, int64_t ld_w,
+                       int64_t V_pad, uint8_t *packed, uint8_t *scales)
+{
+    int64_t v, k0, i;
+    double x[32];
+    if (H % 64 != 0 || V_pad < V) return -1;
+    memset(packed, 0, (size_t)(H / 64) * V_pad * 32);
+    memset(scales, 0, (size_t)(H / 64) * V_pad * 2);
+    for (v = 0; v < V; ++v) {
+        for (k0 = 0; k0 < H; k0 += 32) {
+            double amax = 0.0, unit;
+            int code = 0, fe;
+            int64_t blk = (k0 / 64) * V_pad + v;
+            orc_decode(W, wtype, v * ld_w + k0, 32, x);
+            for (i = 0; i < 32; ++i)
+                if (fabs(x[i]) > amax) amax = fabs(x[i]);
+            if (amax > 0.0) {
+                frexp(amax, &fe);          /* amax = f 2^fe, f in [0.5, 1) */
+                code = (fe - 1) - 2 + 127;
+                if (code < 0) code = 0;
+                if (code > 254) code = 254;
+            }
+            scales[blk * 2 + (k0 % 64) / 32] = (uint8_t)code;
+            unit = ldexp(1.0, code - 127);
+            for (i = 0; i < 32; ++i) {
+                double a = fabs(x[i]) / unit, best = 1e300;
+                int c, q = 0;
+                for (c = 0; c < 8; ++c) {   /* nearest magnitude, ties to the even code */
+                    double d = fabs(a - orc_e2m1_mag[c]);
+                    if (d < best || (d == best && (c % 2) == 0)) { best = d; q = c; }
+                }
+                if (a > 6.0) q = 7;
+                if (q != 0 && x[i] < 0) q |= 8;
+                {
+                    int64_t byte = blk * 32 + ((k0 % 64) + i) / 2;
+                    packed[byte] |= (uint8_t)(((k0 + i) % 2) ? (q << 4) : q);
+                }
+            }
+        }
+    }
+    return 0;
+}
+
+/* Decoded values of an MXFP4 matrix: out [V, H] float64. */
+void orc_mxfp4_dequantize(const uint8_t *packed, const uint8_t *scales, int64_t V, int64_t H,
+                          int64_t V_pad, double *out)
+{
+    orc_mx_matrix m;
+    int64_t v;
+    m.packed = packed; m.scales = scales; m.V_pad = V_pad; m.H = H;
+    for (v = 0; v < V; ++v) orc_decode(&m, ORC_MXFP4, v * H, H, out + v * H);
+}
+
+/*
+ * KL(teacher || student) with the teacher head in MXFP4 (DeepSeek-V4 book
+ * ch. 19, "1. FP4 in OPD": inference-only teacher forwards use 4-bit MXFP4
+ * weights): exactly orc_kl with W_t replaced by its decoded values.
+ * h_s, W_s, h_t share `type` and strides; W_t is the MXFP4 matrix.
+ */
+int orc_kl_mxfp4(int64_t H, int64_t V,
+                 const void *h_s, const void *W_s, const void *h_t,
+                 const uint8_t *Wt_packed, const uint8_t *Wt_scales, int64_t V_pad,
+                 int type, int64_t ld_h, int64_t ld_w,
+                 const int64_t *rows, int64_t n, double *kl)
+{
+    int64_t i0;
+    orc_mx_matrix wt;
+    double *hds = (double *)malloc((size_t)ORC_ROW_BLOCK * H * sizeof(double));
+    double *hdt = (double *)malloc((size_t)ORC_ROW_BLOCK * H * sizeof(double));
+    double *zs = (double *)malloc((size_t)ORC_ROW_BLOCK * V * sizeof(double));
+    double *zt = (double *)malloc((size_t)ORC_ROW_BLOCK * V * sizeof(double));
+    if (!hds || !hdt || !zs || !zt) { free(hds); free(hdt); free(zs); free(zt); return -2; }
+    wt.packed = Wt_packed; wt.scales = Wt_scales; wt.V_pad = V_pad; wt.H = H;
+    for (i0 = 0; i0 < n; i0 += ORC_ROW_BLOCK) {
+        int64_t nb = n - i0 < ORC_ROW_BLOCK ? n - i0 : ORC_ROW_BLOCK;
+        int64_t b;
+        orc_gather_h(h_s, type, ld_h, rows, i0, nb, H, hds);
+        orc_gather_h(h_t, type, ld_h, rows, i0, nb, H, hdt);
+        orc_logits_block(hds, nb, H, V, W_s, type, ld_w, zs);
+        orc_logits_block(hdt, nb, H, V, &wt, ORC_MXFP4, H, zt);
+        for (b = 0; b < nb; ++b) {
+            const double *s = zs + b * V, *t = zt + b * V;
+            double Ls = orc_lse(s, V), Lt = orc_lse(t, V), acc = 0.0;
+            int64_t v;
+            for (v = 0; v < V; ++v) {
+                double lpt = t[v] - Lt, lps = s[v] - Ls;
+                acc += exp(lpt) * (lpt - lps);
+            }
+            kl[i0 + b] = acc;
+        }
+    }
+    free(hds); free(hdt); free(zs); free(zt);
     return 0;
 }

@@ -179,3 +179,75 @@ def backward(h, W, targets, rows, tau, g1, g2, dtype, dh_rows_sel=None, vsel=Non
         G = np.where(support_bits(support, rows, Wd.shape[0])[:, vs], G, 0.0)
     dW = G.T @ hd[rows]
     return dh, dW
+
+
+# ---------------------------------------------------------------- MXFP4
+# OCP Microscaling FP4: E2M1 elements (1 sign, 2 exponent bits with bias 1, 1
+# mantissa bit) with one E8M0 power-of-two scale per 32 consecutive elements
+# of a row.  Blocked layout: for column block kb (64 wide) and row v < V_pad,
+# packed[kb, v, b] holds elements 2b (low nibble) and 2b+1 (high nibble),
+# scales[kb, v, j] the code of elements 32j .. 32j+31 of the block.
+
+def mxfp4_vpad(V):
+    return -(-V // 256) * 256
+
+
+def mxfp4_quantize(W, dtype):
+    """(packed uint8 [H/64, V_pad, 32], scales uint8 [H/64, V_pad, 2]).
+
+    Restated independently of the C quantiser: the scale exponent from
+    numpy.frexp, the rounding as numpy.rint (ties to even) in units of the
+    grid spacing of the octave the value falls in (0.5 below 2, 1 in [2, 4),
+    2 from 4), saturation at 6."""
+    x = decode(W, dtype)
+    V, H = x.shape
+    assert H % 64 == 0
+    Vp = mxfp4_vpad(V)
+    blocks = x.reshape(V, H // 32, 32)
+    amax = np.abs(blocks).max(axis=2)
+    _, fe = np.frexp(amax)
+    code = np.where(amax > 0, np.clip(fe - 1 - 2 + 127, 0, 254), 0).astype(np.int64)
+    a = np.abs(blocks) / np.ldexp(1.0, code - 127)[:, :, None]
+    spacing = np.where(a < 2, 0.5, np.where(a < 4, 1.0, 2.0))
+    q = np.minimum(np.rint(a / spacing) * spacing, 6.0)
+    mags = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    idx = np.searchsorted(mags, q)
+    assert np.all(mags[idx] == q)
+    nib = np.where((blocks < 0) & (idx > 0), idx | 8, idx).reshape(V, H)
+    packed = np.zeros((H // 64, Vp, 32), np.uint8)
+    pairs = (nib[:, 0::2] | (nib[:, 1::2] << 4)).astype(np.uint8).reshape(V, H // 64, 32)
+    packed[:, :V, :] = pairs.transpose(1, 0, 2)
+    scales = np.zeros((H // 64, Vp, 2), np.uint8)
+    scales[:, :V, :] = code.reshape(V, H // 64, 2).transpose(1, 0, 2)
+    return packed, scales
+
+
+def mxfp4_dequantize(packed, scales, V):
+    """Decoded float64 [V, H] of a blocked MXFP4 matrix."""
+    packed = np.asarray(packed, np.uint8)
+    scales = np.asarray(scales, np.uint8)
+    nkb = packed.shape[0]
+    lo = (packed[:, :V, :] & 15).astype(np.int64)
+    hi = (packed[:, :V, :] >> 4).astype(np.int64)
+    nib = np.stack([lo, hi], axis=3).reshape(nkb, V, 64)       # element order within the block
+    mags = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    val = np.where(nib & 8, -1.0, 1.0) * mags[nib & 7]
+    sc = np.repeat(scales[:, :V, :].astype(np.int64), 32, axis=2)  # [nkb, V, 64]
+    val = np.ldexp(val, sc - 127)
+    return val.transpose(1, 0, 2).reshape(V, nkb * 64)
+
+
+def kl_mxfp4(h_s, W_s, h_t, packed, scales, rows, dtype, block=256):
+    """KL(teacher || student) with the teacher head given in MXFP4."""
+    hs, Ws, ht = (decode(a, dtype) for a in (h_s, W_s, h_t))
+    Wt = mxfp4_dequantize(packed, scales, Ws.shape[0])
+    rows = _rows(rows, hs.shape[0])
+    out = np.empty(rows.shape[0])
+    for i0 in range(0, rows.shape[0], block):
+        r = rows[i0:i0 + block]
+        ls = hs[r] @ Ws.T
+        lt = ht[r] @ Wt.T
+        ls = ls - _lse(ls)[:, None]
+        lt = lt - _lse(lt)[:, None]
+        out[i0:i0 + block] = (np.exp(lt) * (lt - ls)).sum(axis=1)
+    return out

@@ -592,3 +592,102 @@ def test_support_c_and_numpy_agree_config0():
                             vsel=vs, support=sup)
     np.testing.assert_allclose(cdh, ndh, rtol=1e-9, atol=1e-12)
     np.testing.assert_allclose(cdW, ndW, rtol=1e-9, atol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# MXFP4 teacher head (OCP Microscaling FP4: E2M1 elements, E8M0 block scales)
+
+E2M1 = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def test_mxfp4_decoding_is_the_e2m1_table_times_the_block_scale():
+    V, H = 3, 64
+    packed = np.zeros((1, 256, 32), np.uint8)
+    scales = np.zeros((1, 256, 2), np.uint8)
+    codes = np.arange(64) % 16                      # every nibble, twice per row
+    for v in range(V):
+        packed[0, v] = (codes[0::2] | (codes[1::2] << 4)).astype(np.uint8)
+        scales[0, v] = (127 + v - 1, 127 + 3 * v)    # 2^(v-1) and 2^(3v)
+    for deq in (coracle.mxfp4_dequantize(packed, scales, V),
+                ref.mxfp4_dequantize(packed, scales, V)):
+        for v in range(V):
+            for k in range(64):
+                c = codes[k]
+                want = (-1.0 if c & 8 else 1.0) * E2M1[c & 7] * 2.0 ** (
+                    (v - 1) if k < 32 else 3 * v)
+                assert deq[v, k] == want, (v, k)
+
+
+def test_mxfp4_grid_values_round_trip_exactly():
+    """A block of grid values whose largest magnitude is 4 or 6 (times 2^e)
+    gets scale code e + 127 and is stored exactly."""
+    rng = np.random.default_rng(70)
+    V, H = 40, 128
+    mags = np.array(E2M1)
+    e = rng.integers(-20, 10, size=(V, H // 32))
+    top = rng.choice([4.0, 6.0], size=(V, H // 32))
+    x = rng.choice(mags, size=(V, H // 32, 32)) * rng.choice([-1.0, 1.0], size=(V, H // 32, 32))
+    x[:, :, 0] = top
+    W = (x * np.ldexp(1.0, e)[:, :, None]).reshape(V, H)
+    for q in (coracle.mxfp4_quantize(W, "f64"), ref.mxfp4_quantize(W, "f64")):
+        assert np.array_equal(q[1][:, :V, :].transpose(1, 0, 2).reshape(V, -1), e + 127)
+        assert np.array_equal(coracle.mxfp4_dequantize(*q, V), W)
+
+
+def test_mxfp4_rounding_is_nearest_with_ties_to_even_and_saturation():
+    rng = np.random.default_rng(71)
+    V, H = 64, 256
+    W = rng.standard_normal((V, H)) * np.exp(rng.uniform(-3, 3, size=(V, 1)))
+    W[0, :32] = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 5.5, 7.0] + [0.0] * 22 + [7.9])
+    W[1, :32] = 0.0
+    packed, scales = coracle.mxfp4_quantize(W, "f64")
+    deq = coracle.mxfp4_dequantize(packed, scales, V)
+    code = scales[:, :V, :].transpose(1, 0, 2).reshape(V, H // 32).astype(np.int64)
+    # the block scale: 2^(floor(log2 max|x|) - 2)
+    amax = np.abs(W.reshape(V, H // 32, 32)).max(axis=2)
+    want_code = np.where(amax > 0, np.floor(np.log2(np.where(amax > 0, amax, 1))) - 2 + 127, 0)
+    assert np.array_equal(code, want_code)
+    unit = np.repeat(np.ldexp(1.0, code - 127), 32, axis=1)
+    a = np.abs(W) / unit
+    grid = np.array(E2M1)
+    for v in range(V):
+        for k in range(H):
+            got = abs(deq[v, k]) / unit[v, k]
+            d = np.abs(grid - min(a[v, k], 6.0))
+            best = d.min()
+            ties = np.nonzero(d == best)[0]
+            want = grid[ties[0]] if len(ties) == 1 else grid[[t for t in ties if t % 2 == 0][0]]
+            assert got == want, (v, k, a[v, k], got)
+            if got != 0:
+                assert np.sign(deq[v, k]) == np.sign(W[v, k])
+    # the printed tie cases, in units of the block scale (max 7.9 -> scale 1)
+    assert code[0, 0] == 127
+    assert deq[0, :9].tolist() == [0.0, 1.0, 1.0, 2.0, 2.0, 4.0, 4.0, 6.0, 6.0]
+    assert np.all(deq[1, :32] == 0.0) and code[1, 0] == 0
+
+
+def test_mxfp4_c_and_numpy_quantisers_agree():
+    w = workloads.WORKLOADS[3].scaled(T=4, H=256, V=700, seed=72)
+    d = workloads.make(w)
+    for m in (d["W_t"], d["W_s"]):
+        pc, sc = coracle.mxfp4_quantize(m, "bf16")
+        pn, sn = ref.mxfp4_quantize(m, "bf16")
+        assert np.array_equal(pc, pn) and np.array_equal(sc, sn)
+        assert np.all(pc[:, 700:, :] == 0) and np.all(sc[:, 700:, :] == 0)   # padding rows
+
+
+def test_kl_with_mxfp4_teacher_is_kl_on_the_decoded_weights():
+    w = workloads.WORKLOADS[3].scaled(T=10, H=128, V=400, seed=73)
+    d = workloads.make(w)
+    packed, scales = coracle.mxfp4_quantize(d["W_t"], "bf16")
+    Wt = coracle.mxfp4_dequantize(packed, scales, 400)
+    rows = np.array([9, 0, 4])
+    got = coracle.kl_mxfp4(d["h_s"], d["W_s"], d["h_t"], packed, scales, rows, "bf16")
+    dec = [ref.decode(d[k], "bf16") for k in ("h_s", "W_s", "h_t")]
+    want = coracle.kl(dec[0], dec[1], dec[2], Wt, rows, "f64")
+    np.testing.assert_allclose(got, want, rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(ref.kl_mxfp4(d["h_s"], d["W_s"], d["h_t"], packed, scales, rows,
+                                            "bf16"), want, rtol=1e-10, atol=1e-13)
+    # the teacher's quantisation moves the KL, but not by much at these sizes
+    plain = coracle.kl(d["h_s"], d["W_s"], d["h_t"], d["W_t"], rows, "bf16")
+    assert np.all(np.abs(got - plain) < 0.1 * plain)
