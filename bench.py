@@ -481,6 +481,35 @@ def run_ours(args):
                                                      d["tau"], workspace=wsk, support=sup),
                          {"support": "each token kept with probability 1/32, targets kept"})
             del sup, tk
+        # distillation KL with the teacher head in MXFP4 (4.25 bits per weight),
+        # alternating with the bf16 teacher head on the same inputs
+        try:
+            dk = workloads.make(3, device=device)
+            wk = dk["workload"]
+            packed, scales = flp.mxfp4_quantize(dk["W_t"])
+            shape = flp.make_shape(wk.T, wk.H, wk.V, dk["n"], dk["h"].dtype)
+            wsk = torch.empty(flp.workspace_size(shape, 1), dtype=torch.uint8, device=device)
+            t_mx = t_bf = 0.0
+            for _ in range(2):
+                t_bf += time_calls(lambda: flp.kl_divergence(
+                    dk["h_s"], dk["W_s"], dk["h_t"], dk["W_t"], None, workspace=wsk), 10, device)
+                t_mx += time_calls(lambda: flp.kl_divergence_mxfp4(
+                    dk["h_s"], dk["W_s"], dk["h_t"], packed, scales, None, workspace=wsk), 10,
+                    device)
+            t_mx = max_over_ranks(t_mx, world, device)
+            t_bf = max_over_ranks(t_bf, world, device)
+            flk = flops_per_call(dk)
+            extra[wk.name + "-mxfp4-teacher"] = {
+                "config": dict(describe(dk), teacher_head="MXFP4 (E2M1, E8M0 per 32), %.3f GB "
+                               "against %.3f GB in bf16" % (packed.numel() / 1e9 + scales.numel() / 1e9,
+                                                            wk.V * wk.H * 2 / 1e9)),
+                "steps": 20, "scored_tokens_per_s": job_throughput(dk["n"], 20, t_mx, world),
+                "ms_per_step": t_mx / 20, "tflops": flk / (t_mx / 20 / 1e3) / 1e12,
+                "bf16_teacher_ms_per_step_same_clocks": t_bf / 20}
+            del dk, packed, scales, wsk
+        except Exception as e:  # reported, not fatal
+            extra[workloads.WORKLOADS[3].name + "-mxfp4-teacher"] = {"unavailable": str(e)[:200]}
+        torch.cuda.empty_cache()
         out["workloads"] = extra
 
     if rank == 0 and world == 1 and not args.no_cpu:

@@ -10,6 +10,7 @@ or PyTorch fallback, and a missing library raises.
     logp, ent = logprob_entropy(h, W, targets, row_idx, temperature,
                                 support=pack_support(mask))        # sampling support
     kl = kl_divergence(h_s, W_s, h_t, W_t, row_idx)
+    kl = kl_divergence_mxfp4(h_s, W_s, h_t, *mxfp4_quantize(W_t), row_idx)
     dh, dW = backward(h, W, targets, row_idx, temperature, g1, g2)
     logp, ent = FusedLogProbEntropy.apply(h, W, targets, row_idx, temperature)
 """
@@ -21,7 +22,8 @@ import torch
 from . import _build
 
 __all__ = ["lib", "build", "workspace_size", "logprob_entropy", "logprob_entropy_k",
-           "kl_divergence", "backward", "pack_support",
+           "kl_divergence", "backward", "pack_support", "mxfp4_quantize",
+           "kl_divergence_mxfp4",
            "read_device_status", "plan", "set_kernel_events", "row_chunks", "FusedLogProbEntropy", "FlpError",
            "OP_LOGPROB_ENTROPY", "OP_KL", "OP_BACKWARD"]
 
@@ -102,6 +104,14 @@ def lib():
     L.flp_backward_support.restype = ctypes.c_int
     L.flp_pack_support.argtypes = [vp, i64, i64, i64, vp, i64, vp]
     L.flp_pack_support.restype = ctypes.c_int
+    L.flp_mxfp4_rows.argtypes = [i64]
+    L.flp_mxfp4_rows.restype = i64
+    L.flp_mxfp4_bytes.argtypes = [i64, i64, ctypes.POINTER(sz), ctypes.POINTER(sz)]
+    L.flp_mxfp4_bytes.restype = sz
+    L.flp_mxfp4_quantize.argtypes = [vp, ctypes.c_int, i64, i64, i64, vp, vp, vp]
+    L.flp_mxfp4_quantize.restype = ctypes.c_int
+    L.flp_kl_mxfp4.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.flp_kl_mxfp4.restype = ctypes.c_int
     for f in (L.flp_logprob_entropy, L.flp_kl, L.flp_backward, L.flp_read_device_status,
               L.flp_plan_scoring):
         f.restype = ctypes.c_int
@@ -347,6 +357,50 @@ def backward(h, W, targets, row_idx, temperature, g1, g2, lse=None, ez=None, *, 
                 float(temperature), _ptr(g1), _ptr(g2), _ptr(lse), _ptr(ez), _ptr(dh), _ptr(dW),
                 _ptr(ws), ws.numel(), _stream(dev)))
     return dh, dW
+
+
+def mxfp4_quantize(W):
+    """Quantise W [V, H] (bf16/fp16 CUDA, H a multiple of 64) to MXFP4 on the
+    GPU.  Returns (packed uint8 [H/64, V_pad, 32], scales uint8 [H/64, V_pad, 2])
+    in the library's blocked layout (see include/fusedlogp.h)."""
+    _matrix(W, "W")
+    V, H = W.shape
+    if H % 64:
+        raise TypeError("H must be a multiple of 64")
+    Vp = int(lib().flp_mxfp4_rows(V))
+    packed = torch.empty((H // 64, Vp, 32), dtype=torch.uint8, device=W.device)
+    scales = torch.empty((H // 64, Vp, 2), dtype=torch.uint8, device=W.device)
+    with torch.cuda.device(W.device):
+        _check(lib().flp_mxfp4_quantize(_ptr(W), _DTYPES[W.dtype], V, H, W.stride(0), _ptr(packed),
+                                        _ptr(scales), _stream(W.device)))
+    return packed, scales
+
+
+def kl_divergence_mxfp4(h_s, W_s, h_t, Wt_packed, Wt_scales, row_idx=None, *, workspace=None):
+    """KL(teacher || student) per scored row with the teacher head in MXFP4
+    (from :func:`mxfp4_quantize`); bf16 rows and student head."""
+    for x, nm in ((h_s, "h_s"), (W_s, "W_s"), (h_t, "h_t")):
+        _matrix(x, nm)
+    dev = h_s.device
+    if h_s.shape != h_t.shape or h_s.shape[1] != W_s.shape[1] or h_t.stride(0) != h_s.stride(0):
+        raise TypeError("student and teacher rows must share shape and stride with W_s's H")
+    V, H = W_s.shape
+    Vp = int(lib().flp_mxfp4_rows(V))
+    for x, nm, last in ((Wt_packed, "Wt_packed", 32), (Wt_scales, "Wt_scales", 2)):
+        if not isinstance(x, torch.Tensor) or x.device != dev or x.dtype != torch.uint8 or \
+                tuple(x.shape) != (H // 64, Vp, last) or not x.is_contiguous():
+            raise TypeError("%s must be a contiguous uint8 [%d, %d, %d] tensor on %s"
+                            % (nm, H // 64, Vp, last, dev))
+    ri = _index(row_idx, "row_idx", dev)
+    n = h_s.shape[0] if ri is None else ri.numel()
+    shape = make_shape(h_s.shape[0], H, V, n, h_s.dtype, h_s.stride(0), W_s.stride(0))
+    out = torch.empty(n, dtype=torch.float32, device=dev)
+    ws = _workspace(shape, OP_KL, dev, workspace)
+    with torch.cuda.device(dev):
+        _check(lib().flp_kl_mxfp4(ctypes.byref(shape), _ptr(h_s), _ptr(W_s), _ptr(h_t),
+                                  _ptr(Wt_packed), _ptr(Wt_scales), _ptr(ri), _ptr(out), _ptr(ws),
+                                  ws.numel(), _stream(dev)))
+    return out
 
 
 def read_device_status(workspace, device=None):

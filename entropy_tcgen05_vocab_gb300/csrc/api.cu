@@ -515,25 +515,31 @@ flp_status flp_logprob_entropy_k(const flp_shape *s, const void *h, const void *
                       out_lse, out_ez, ws, ws_bytes, stream);
 }
 
-flp_status flp_kl(const flp_shape *s, const void *h_s, const void *W_s, const void *h_t,
-                  const void *W_t, const int64_t *row_idx, float *out_kl, void *ws,
-                  size_t ws_bytes, flp_stream_t stream) {
-  g_err[0] = 0;
+}  // extern "C"
+
+namespace flp {
+namespace {
+// KL(teacher || student); the teacher head is W_t, or (mx.packed != null)
+// the blocked MXFP4 operand mx.
+flp_status kl_impl(const flp_shape *s, const void *h_s, const void *W_s, const void *h_t,
+                   const void *W_t, const MxOperand &mx, const int64_t *row_idx, float *out_kl,
+                   void *ws, size_t ws_bytes, flp_stream_t stream) {
   const KernelEvents ev;
   flp_status st = check_common(s, FLP_OP_KL, ws, ws_bytes);
   if (st != FLP_OK) return st;
   if (s->n_rows == 0) return FLP_OK;
   if (!row_idx && s->n_rows != s->T)
     return fail(FLP_ERR_INVALID_ARG, "row_idx is NULL but n_rows != T");
-  if (!h_s || !W_s || !h_t || !W_t || !out_kl)
-    return fail(FLP_ERR_INVALID_ARG, "h_s, W_s, h_t, W_t and out_kl are required");
-  if (!aligned16(h_s) || !aligned16(W_s) || !aligned16(h_t) || !aligned16(W_t))
+  if (!h_s || !W_s || !h_t || !(W_t || mx.packed) || !out_kl)
+    return fail(FLP_ERR_INVALID_ARG, "h_s, W_s, h_t, the teacher head and out_kl are required");
+  if (!aligned16(h_s) || !aligned16(W_s) || !aligned16(h_t) || (W_t && !aligned16(W_t)))
     return fail(FLP_ERR_INVALID_ARG, "h_s, W_s, h_t and W_t must be 16-byte aligned");
   DeviceInfo dev;
   if ((st = device_info(&dev)) != FLP_OK) return st;
 
   const Layout L = layout_for(s, FLP_OP_KL);
-  const Plan p = plan_cached(s->n_rows, s->V, s->H, kKlBN, kl_units(dev.sms), 128 * kKlCG, 2);
+  const int units = mx.packed ? kl_mx_units(dev.sms) : kl_units(dev.sms);
+  const Plan p = plan_cached(s->n_rows, s->V, s->H, kKlBN, units, 128 * kKlCG, 2);
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   KlArgs a{};
   const void *As = h_s, *At = h_t;
@@ -547,8 +553,10 @@ flp_status flp_kl(const flp_shape *s, const void *h_s, const void *W_s, const vo
   if ((st = make_map(&a.tmAt, s->dtype, At, s->H, s->n_rows, lda, 64, 128)) != FLP_OK) return st;
   if ((st = make_map(&a.tmBs, s->dtype, W_s, s->H, s->V, s->ld_w, 64, kKlBN / kKlCG)) != FLP_OK)
     return st;
-  if ((st = make_map(&a.tmBt, s->dtype, W_t, s->H, s->V, s->ld_w, 64, kKlBN / kKlCG)) != FLP_OK)
+  if (W_t && (st = make_map(&a.tmBt, s->dtype, W_t, s->H, s->V, s->ld_w, 64, kKlBN / kKlCG)) !=
+                 FLP_OK)
     return st;
+  a.mx = mx;
   a.sch = p.sch;
   a.grid = p.grid * kKlCG;
   a.bf16 = s->dtype == FLP_BF16;
@@ -575,6 +583,69 @@ flp_status flp_kl(const flp_shape *s, const void *h_s, const void *W_s, const vo
   if ((e = launch_kl(a, cs)) != cudaSuccess) return cuda_fail(e, "KL launch");
   if ((e = ev.stop(cs)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
   return FLP_OK;
+}
+}  // namespace
+}  // namespace flp
+
+extern "C" {
+
+flp_status flp_kl(const flp_shape *s, const void *h_s, const void *W_s, const void *h_t,
+                  const void *W_t, const int64_t *row_idx, float *out_kl, void *ws,
+                  size_t ws_bytes, flp_stream_t stream) {
+  g_err[0] = 0;
+  if (!W_t && s && s->n_rows > 0) return fail(FLP_ERR_INVALID_ARG, "W_t is required");
+  return kl_impl(s, h_s, W_s, h_t, W_t, MxOperand{nullptr, nullptr, 0}, row_idx, out_kl, ws,
+                 ws_bytes, stream);
+}
+
+int64_t flp_mxfp4_rows(int64_t V) { return V <= 0 ? 0 : cdiv(V, 256) * 256; }
+
+size_t flp_mxfp4_bytes(int64_t V, int64_t H, size_t *packed_bytes, size_t *scale_bytes) {
+  if (V <= 0 || H <= 0 || H % 64 != 0) return 0;
+  const size_t rows = static_cast<size_t>(flp_mxfp4_rows(V));
+  const size_t blocks = static_cast<size_t>(H / 64);
+  if (packed_bytes) *packed_bytes = blocks * rows * 32;
+  if (scale_bytes) *scale_bytes = blocks * rows * 2;
+  return blocks * rows * 34;
+}
+
+flp_status flp_mxfp4_quantize(const void *W, flp_dtype dtype, int64_t V, int64_t H,
+                              int64_t ld_w, uint8_t *packed, uint8_t *scales,
+                              flp_stream_t stream) {
+  g_err[0] = 0;
+  if (V <= 0 || H <= 0 || H % 64 != 0)
+    return fail(FLP_ERR_INVALID_ARG, "V must be > 0 and H a positive multiple of 64");
+  if (dtype != FLP_BF16 && dtype != FLP_FP16) return fail(FLP_ERR_INVALID_ARG, "bad dtype");
+  if (ld_w < H) return fail(FLP_ERR_INVALID_ARG, "ld_w < H");
+  if (!W || !packed || !scales) return fail(FLP_ERR_INVALID_ARG, "W, packed and scales are required");
+  if (reinterpret_cast<uintptr_t>(W) % 2 != 0 || !aligned16(packed))
+    return fail(FLP_ERR_INVALID_ARG, "W must be 2-byte and packed 16-byte aligned");
+  DeviceInfo dev;
+  const flp_status st = device_info(&dev);
+  if (st != FLP_OK) return st;
+  const cudaError_t e =
+      launch_mxfp4_quantize(W, dtype == FLP_BF16, V, H, ld_w, flp_mxfp4_rows(V), packed, scales,
+                            dev.sms, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+  return FLP_OK;
+}
+
+flp_status flp_kl_mxfp4(const flp_shape *s, const void *h_s, const void *W_s, const void *h_t,
+                        const uint8_t *Wt_packed, const uint8_t *Wt_scales,
+                        const int64_t *row_idx, float *out_kl, void *ws, size_t ws_bytes,
+                        flp_stream_t stream) {
+  g_err[0] = 0;
+  const char *why = nullptr;
+  if (!shape_ok(s, &why)) return fail(FLP_ERR_INVALID_ARG, "%s", why);
+  if (s->dtype != FLP_BF16)
+    return fail(FLP_ERR_UNSUPPORTED, "the MXFP4 teacher head needs bf16 student and teacher rows");
+  if (s->H % 64 != 0) return fail(FLP_ERR_INVALID_ARG, "H must be a multiple of 64");
+  if (s->n_rows > 0 && (!Wt_packed || !Wt_scales))
+    return fail(FLP_ERR_INVALID_ARG, "Wt_packed and Wt_scales are required");
+  if ((Wt_packed && !aligned16(Wt_packed)) || (Wt_scales && !aligned16(Wt_scales)))
+    return fail(FLP_ERR_INVALID_ARG, "Wt_packed and Wt_scales must be 16-byte aligned");
+  const MxOperand mx{Wt_packed, Wt_scales, static_cast<long long>(flp_mxfp4_rows(s->V))};
+  return kl_impl(s, h_s, W_s, h_t, nullptr, mx, row_idx, out_kl, ws, ws_bytes, stream);
 }
 
 }  // extern "C"

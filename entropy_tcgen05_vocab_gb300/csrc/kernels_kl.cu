@@ -39,6 +39,7 @@ struct KlEpi {
     int64_t T;
     float *out_kl;
     uint32_t *status;
+    MxOperand mx;  // teacher head in MXFP4 (read by the MX pipeline's producer)
   };
   const Params p;
   float mt, st0, st1, ct0, ct1, ms, ss0, ss1;
@@ -172,8 +173,13 @@ struct KlEpi {
 };
 
 using KlLayout = PipeLayout<kKlBN, kKlStages, 2, kKlCG, kKlAcc>;
+using KlMxLayout = PipeLayout<kKlBN, kKlStages, 2, kKlCG, kKlAcc, false, true>;
 #define KL_KERNEL vocab_pipeline_kernel<kKlBN, kKlStages, 2, KlEpi, kKlCG, kKlAcc, kKlEpiWarps>
+// the teacher head's B operand decoded from MXFP4 in shared memory
+#define KL_MX_KERNEL \
+  vocab_pipeline_kernel<kKlBN, kKlStages, 2, KlEpi, kKlCG, kKlAcc, kKlEpiWarps, false, true>
 constexpr int kKlThreads = pipe_threads(kKlEpiWarps);
+constexpr int kKlMxThreads = pipe_threads(kKlEpiWarps, true);
 
 cudaError_t launch_kl(const KlArgs &a, cudaStream_t stream) {
   KlEpi::Params p;
@@ -190,9 +196,24 @@ cudaError_t launch_kl(const KlArgs &a, cudaStream_t stream) {
   p.T = a.T;
   p.out_kl = a.out_kl;
   p.status = a.status;
+  p.mx = a.mx;
   const uint32_t idesc = idesc_f16(a.bf16, kBM * kKlCG, kKlBN, false, false);
+  if (a.mx.packed)  // tmBt is unused: the teacher's B comes from the MXFP4 operand
+    return launch_persistent(KL_MX_KERNEL, a.grid, kKlMxThreads, KlMxLayout::kSmemBytes, kKlCG,
+                             stream, a.tmAs, a.tmBs, a.tmAt, a.tmBs, a.sch, idesc, p, a.status);
   return launch_persistent(KL_KERNEL, a.grid, kKlThreads, KlLayout::kSmemBytes, kKlCG, stream, a.tmAs, a.tmBs,
                            a.tmAt, a.tmBt, a.sch, idesc, p, a.status);
+}
+
+int kl_mx_units(int num_sms) {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64)
+    return resident_units(KL_MX_KERNEL, kKlMxThreads, KlMxLayout::kSmemBytes, kKlCG, num_sms);
+  if (!cached[dev])
+    cached[dev] = resident_units(KL_MX_KERNEL, kKlMxThreads, KlMxLayout::kSmemBytes, kKlCG, num_sms);
+  return cached[dev];
 }
 
 int kl_units(int num_sms) {

@@ -80,6 +80,7 @@ struct KlArgs {
   uint32_t *counters;                   // [ceil(n / 32)] zeroed before the launch
   float *out_kl;
   uint32_t *status;
+  MxOperand mx;  // teacher head in MXFP4 (packed == null: W_t through tmBt)
 };
 
 struct GradArgs {
@@ -142,5 +143,11 @@ cudaError_t launch_wait_timeout(uint64_t limit_ns, uint32_t *status, cudaStream_
 int fwd_units(int num_sms);
 int grad_units(int num_sms);
 int kl_units(int num_sms);
+int kl_mx_units(int num_sms);
+// MXFP4 quantisation of W [V, ld_w] (bf16/fp16) into the blocked layout of
+// MxOperand with v_pad rows (rows past V zero); H a multiple of 64.
+cudaError_t launch_mxfp4_quantize(const void *W, bool bf16, int64_t V, int64_t H, int64_t ld_w,
+                                  int64_t v_pad, uint8_t *packed, uint8_t *scales, int num_sms,
+                                  cudaStream_t stream);
 
 }  // namespace flp

@@ -14,6 +14,16 @@ constexpr int kStatBadRow = 1;
 constexpr int kStatTimeout = 2;
 constexpr int kStatEmptySupport = 3;
 
+// MXFP4 operand in the blocked layout: for column block kb (64 wide) and row
+// v < v_pad, 32 bytes of E2M1 codes at packed + (kb * v_pad + v) * 32 (byte b:
+// element 2b in the low nibble, 2b + 1 in the high one) and two E8M0 scale
+// codes at scales + (kb * v_pad + v) * 2 (elements 0..31, 32..63).
+struct MxOperand {
+  const unsigned char *packed;
+  const unsigned char *scales;
+  long long v_pad;
+};
+
 // Work item = (row tile, vocabulary split).  Items are ordered band by band:
 // within a band of `band` row tiles, all items of split 0 (row tiles
 // fastest), then split 1, ...  The last band may hold fewer row tiles.

@@ -27,6 +27,16 @@
 //   warps 2-5  epilogue: tcgen05.ld of their 32 TMEM lanes (= 32 rows),
 //              32 columns at a time, folded by the Epi policy.
 //
+// MX: the second GEMM's B operand (a teacher head) is stored in MXFP4 (E2M1
+// elements with an E8M0 scale per 32, in the blocked layout of MxOperand).
+// Each CTA's producer bulk-copies its rows' packed codes and scales into a
+// small staging buffer per stage; four converter warps decode them exactly
+// into bf16 in the 128B-swizzled layout a TMA copy would have written, fence
+// them into the async proxy and arrive on the leader's "converted" barrier,
+// which the MMA issuer waits on with the "full" one.  Every E2M1 value times
+// a power of two is a bf16 value, so the bf16 MMA computes exactly the
+// product with the decoded weights.
+//
 // CTA pairs (CG = 2, cluster of 2): each CTA loads its own 128 rows of A and
 // its half (BN/2 rows) of B; the leader (rank 0) issues tcgen05.mma.cta_group::2
 // for the 256 x BN tile, which reads both CTAs' shared memory and writes
@@ -54,6 +64,10 @@ constexpr int kPipeThreads = 64 + 32 * kEpiWarps;
 // Threads of a vocabulary-pipeline CTA with EPIW epilogue warps (4 or 8).
 // With 8, two warps share each 32-lane TMEM quarter and split its columns.
 __host__ __device__ constexpr int pipe_threads(int epiw) { return 64 + 32 * epiw; }
+// Four more warps decode an MX operand.
+__host__ __device__ constexpr int pipe_threads(int epiw, bool mx) {
+  return pipe_threads(epiw) + (mx ? 128 : 0);
+}
 
 // NOPS independent GEMMs share one tile (the KL pipeline runs the student and
 // the teacher head side by side, NOPS = 2).  Per-CTA stage layout:
@@ -63,7 +77,48 @@ __host__ __device__ constexpr int pipe_threads(int epiw) { return 64 + 32 * epiw
 // SHARED_A: the NOPS GEMMs share one A operand and take their B operands from
 // consecutive BN-row blocks of the same matrix, so the vocabulary tile is
 // NOPS x BN columns wide (one A load feeds NOPS MMAs of N = BN).
-template <int BN, int STAGES, int NOPS = 1, int CG = 1, int NACC = 2, bool SHARED_A = false>
+// One row of 64 MXFP4 elements -> 64 bf16 written as the row of a
+// 128B-swizzled K-major tile: 16-byte chunk c (elements 8c .. 8c+7) goes to
+// chunk position c ^ (row % 8) of the row's 128 bytes.  An element with code
+// (sign, e, m) and block scale code s is (-1)^sign (e ? 1 + m/2 : m/2)
+// 2^(e - 1 + s - 127): bf16 exponent field s + e - 1, mantissa bit m when
+// e > 0.  Exponent fields below 1 (scale codes 0 and 1) flush to zero.
+__device__ __forceinline__ uint32_t mx_bf16_pair(uint32_t byte, uint32_t scale) {
+  uint32_t out = 0;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t code = (byte >> (4 * h)) & 15u;
+    const uint32_t mag = code & 7u;
+    const uint32_t e = mag >> 1;
+    const int32_t ex = static_cast<int32_t>(scale + e) - 1;
+    const uint32_t mant = (e != 0u) ? (mag & 1u) : 0u;
+    uint32_t bits = ((code & 8u) << 12) | (static_cast<uint32_t>(ex) << 7) | (mant << 6);
+    bits = (mag != 0u && ex > 0) ? bits : 0u;
+    out |= bits << (16 * h);
+  }
+  return out;
+}
+
+__device__ __forceinline__ void mx_decode_row(const uint8_t *codes, const uint8_t *sc,
+                                              uint8_t *row_base, int row) {
+  const uint4 q0 = *reinterpret_cast<const uint4 *>(codes);
+  const uint4 q1 = *reinterpret_cast<const uint4 *>(codes + 16);
+  const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+  const uint32_t s0 = sc[0], s1 = sc[1];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {  // chunk c: code bytes 4c .. 4c+3 = one word
+    const uint32_t s = c < 4 ? s0 : s1;
+    uint4 o;
+    o.x = mx_bf16_pair(w[c] & 0xffu, s);
+    o.y = mx_bf16_pair((w[c] >> 8) & 0xffu, s);
+    o.z = mx_bf16_pair((w[c] >> 16) & 0xffu, s);
+    o.w = mx_bf16_pair(w[c] >> 24, s);
+    *reinterpret_cast<uint4 *>(row_base + ((c ^ (row & 7)) << 4)) = o;
+  }
+}
+
+template <int BN, int STAGES, int NOPS = 1, int CG = 1, int NACC = 2, bool SHARED_A = false,
+          bool MX = false>
 struct PipeLayout {
   static constexpr int kABytes = kBM * kBK * 2;
   static constexpr int kAOps = SHARED_A ? 1 : NOPS;
@@ -75,8 +130,17 @@ struct PipeLayout {
   static constexpr int kTmemCols = NACC * kAccCols;
   static_assert(NACC == 1 || NACC == 2, "one or two accumulator buffers");
   static constexpr int kBarrierBytes = 8 * (2 * STAGES + 5) + 16;
+  // MX: "staged" and "converted" barriers per stage, then per stage the
+  // CTA's B rows' codes (32 bytes each) and scale codes (2 bytes each).
+  static constexpr int kMxBarrierBytes = MX ? 16 * STAGES : 0;
+  static constexpr int kQCodeBytes = kBRows * 32;
+  static constexpr int kQBytes = MX ? kBRows * 34 : 0;
+  static constexpr int kQOffset =
+      (STAGES * kStageBytes + kBarrierBytes + kMxBarrierBytes + 127) / 128 * 128;
   // + 1024 so the stage ring can be aligned to a swizzle atom.
-  static constexpr int kSmemBytes = STAGES * kStageBytes + kBarrierBytes + 1024;
+  static constexpr int kSmemBytes = kQOffset + STAGES * kQBytes + 1024;
+  static_assert(!MX || (NOPS == 2 && !SHARED_A), "the MX operand is the second GEMM's B");
+  static_assert(kQBytes % 16 == 0, "staging buffers stay 16-byte aligned");
   static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM columns must be a power of two");
   static_assert(CG == 1 || CG == 2, "one CTA or a CTA pair");
 };
@@ -125,15 +189,15 @@ __device__ __forceinline__ bool last_arrival(uint32_t *counter, uint32_t expecte
 }
 
 template <int BN, int STAGES, int NOPS, class Epi, int CG = 1, int NACC = 2, int EPIW = 4,
-          bool SHARED_A = false>
-__global__ void __launch_bounds__(pipe_threads(EPIW), 1)
+          bool SHARED_A = false, bool MX = false>
+__global__ void __launch_bounds__(pipe_threads(EPIW, MX), 1)
     vocab_pipeline_kernel(const __grid_constant__ CUtensorMap tmA0,
                           const __grid_constant__ CUtensorMap tmB0,
                           const __grid_constant__ CUtensorMap tmA1,
                           const __grid_constant__ CUtensorMap tmB1, const Schedule sch,
                           const uint32_t idesc, const typename Epi::Params ep,
                           uint32_t *status) {
-  using L = PipeLayout<BN, STAGES, NOPS, CG, NACC, SHARED_A>;
+  using L = PipeLayout<BN, STAGES, NOPS, CG, NACC, SHARED_A, MX>;
   static_assert(NOPS == 1 || NOPS == 2, "one or two GEMMs per tile");
   static_assert(EPIW == 4 || EPIW == 8, "four or eight epilogue warps");
   constexpr int kHalves = EPIW / 4;          // warps sharing one TMEM lane quarter
@@ -149,6 +213,9 @@ __global__ void __launch_bounds__(pipe_threads(EPIW), 1)
   uint64_t *drain = tempty + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  uint64_t *qfull = reinterpret_cast<uint64_t *>(smem + STAGES * L::kStageBytes + L::kBarrierBytes);
+  uint64_t *cvt = qfull + STAGES;
+  uint8_t *qbuf = smem + L::kQOffset;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -167,6 +234,12 @@ __global__ void __launch_bounds__(pipe_threads(EPIW), 1)
       mbar_init(&tempty[a], EPIW * CG);
     }
     mbar_init(drain, 1);
+    if (MX) {
+      for (int st = 0; st < STAGES; ++st) {
+        mbar_init(&qfull[st], 1);
+        mbar_init(&cvt[st], 4 * CG);  // four converter warps per CTA
+      }
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -211,7 +284,17 @@ __global__ void __launch_bounds__(pipe_threads(EPIW), 1)
           if (lane == 0) {
             uint8_t *sa = smem + stage * L::kStageBytes;
             uint8_t *sb = sa + L::kAOps * L::kABytes;
-            if (leader) mbar_arrive_expect_tx(&full[stage], CG * L::kStageBytes);
+            if (leader)
+              mbar_arrive_expect_tx(&full[stage],
+                                    CG * (MX ? L::kStageBytes - L::kBBytes : L::kStageBytes));
+            if constexpr (MX) {  // this CTA's B rows of the MX operand, to its staging buffer
+              const MxOperand &mx = ep.mx;
+              const int64_t blk = static_cast<int64_t>(kb) * mx.v_pad + brow;
+              uint8_t *q = qbuf + stage * L::kQBytes;
+              mbar_arrive_expect_tx(&qfull[stage], L::kQBytes);
+              bulk_load(q, mx.packed + blk * 32, L::kQCodeBytes, &qfull[stage]);
+              bulk_load(q + L::kQCodeBytes, mx.scales + blk * 2, L::kBRows * 2, &qfull[stage]);
+            }
             // second GEMM: its own A and B maps, or (SHARED_A) the next BN rows of B
             const CUtensorMap *tb1 = SHARED_A ? &tmB0 : &tmB1;
             const int brow1 = SHARED_A ? brow + BN : brow;
@@ -221,14 +304,14 @@ __global__ void __launch_bounds__(pipe_threads(EPIW), 1)
               tma_load_2d_pair(sb, &tmB0, fb, kb * kBK, brow);
               if (NOPS == 2) {
                 if (!SHARED_A) tma_load_2d_pair(sa + L::kABytes, &tmA1, fb, kb * kBK, arow);
-                tma_load_2d_pair(sb + L::kBBytes, tb1, fb, kb * kBK, brow1);
+                if (!MX) tma_load_2d_pair(sb + L::kBBytes, tb1, fb, kb * kBK, brow1);
               }
             } else {
               tma_load_2d(sa, &tmA0, &full[stage], kb * kBK, arow);
               tma_load_2d(sb, &tmB0, &full[stage], kb * kBK, brow);
               if (NOPS == 2) {
                 if (!SHARED_A) tma_load_2d(sa + L::kABytes, &tmA1, &full[stage], kb * kBK, arow);
-                tma_load_2d(sb + L::kBBytes, tb1, &full[stage], kb * kBK, brow1);
+                if (!MX) tma_load_2d(sb + L::kBBytes, tb1, &full[stage], kb * kBK, brow1);
               }
             }
           }
@@ -254,6 +337,14 @@ __global__ void __launch_bounds__(pipe_threads(EPIW), 1)
             mbar_wait(&full[s], par, &never);
           }
         }
+        if (MX) {  // and this CTA's own staging copies
+          for (int s = 0; s < STAGES; ++s) {
+            if (!(armed & (1u << s))) continue;
+            const uint32_t par = (s < stage) ? phase : (phase ^ 1u);
+            int never = 0;
+            mbar_wait(&qfull[s], par, &never);
+          }
+        }
       }
     }
   } else if (warp == 1) {
@@ -274,7 +365,10 @@ __global__ void __launch_bounds__(pipe_threads(EPIW), 1)
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * L::kAccCols);
           for (int kb = 0; kb < sch.k_blocks; ++kb) {
-            if (lane == 0) ok = mbar_wait(&full[stage], phase, abort_flag);
+            if (lane == 0) {
+              ok = mbar_wait(&full[stage], phase, abort_flag);
+              if (MX && ok) ok = mbar_wait_cluster(&cvt[stage], phase, abort_flag);
+            }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after();
@@ -330,6 +424,44 @@ __global__ void __launch_bounds__(pipe_threads(EPIW), 1)
         mbar_wait(drain, 0, &never);
       }
     }
+  } else if (MX && warp >= 2 + EPIW) {
+    // ------------------------------------------------------------ MX converters
+    // Thread t of the four warps decodes B row t of this CTA's half, stage by
+    // stage in the producer's order.
+    const int crow = (warp - 2 - EPIW) * 32 + lane;
+    const uint32_t cvt_dst = kPair ? mapa_shared(smem_u32(cvt), 0) : smem_u32(cvt);
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int it = unit; ok && it < sch.items; it += num_units) {
+      int mt, sp, vt0, vt1;
+      sch.item(it, mt, sp, vt0, vt1);
+      for (int vt = vt0; ok && vt < vt1; ++vt) {
+        for (int kb = 0; kb < sch.k_blocks; ++kb) {
+          ok = mbar_wait(&qfull[stage], phase, abort_flag);
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+          }
+          const uint8_t *q = qbuf + stage * L::kQBytes;
+          uint8_t *b1 = smem + stage * L::kStageBytes + L::kAOps * L::kABytes + L::kBBytes;
+          mx_decode_row(q + crow * 32, q + L::kQCodeBytes + crow * 2, b1 + crow * 128, crow);
+          fence_async_smem();  // the MMAs read these bytes through the async proxy
+          __syncwarp();
+          if (lane == 0) {
+            if (kPair)
+              mbar_arrive_cluster(cvt_dst + stage * 8);
+            else
+              mbar_arrive(&cvt[stage]);
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+    if (!ok && lane == 0) record_timeout<CG>(status, abort_flag);
   } else {
     // ------------------------------------------------------------ epilogue
     const int lg = warp & 3;  // the TMEM lane quarter this warp may access

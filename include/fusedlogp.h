@@ -200,6 +200,55 @@ flp_status flp_kl(const flp_shape *shape, const void *h_s, const void *W_s,
                   flp_stream_t stream);
 
 /*
+ * Teacher head in MXFP4 (DeepSeek-V4 book ch. 19, "1. FP4 in OPD": the
+ * inference-only teacher forwards run on 4-bit MXFP4 weights, which cuts the
+ * teacher head's memory and read traffic about 4x against bf16).
+ *
+ * Format (OCP Microscaling FP4): E2M1 elements (1 sign, 2 exponent bits with
+ * bias 1, 1 mantissa bit; magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6) with one
+ * E8M0 scale code s (value 2^(s - 127)) per 32 consecutive elements of a row.
+ * Layout (blocked, so that a tile of rows is contiguous): with
+ * V_pad = flp_mxfp4_rows(V) and for each 64-wide column block kb < H/64 and
+ * row v < V_pad,
+ *   packed[(kb * V_pad + v) * 32 + b]  elements kb*64 + 2b (low nibble) and
+ *                                      kb*64 + 2b + 1 (high nibble) of row v
+ *   scales[(kb * V_pad + v) * 2 + j]   scale code of elements kb*64 + 32j ..
+ *                                      kb*64 + 32j + 31
+ * Rows v >= V are zero.  Sizes: flp_mxfp4_bytes.  H must be a multiple of 64.
+ */
+int64_t flp_mxfp4_rows(int64_t V);  /* V rounded up to a multiple of 256 (0 if V <= 0) */
+
+/* Bytes of the packed codes and the scales; returns their sum (0 if V <= 0 or
+ * H is not a positive multiple of 64).  Either out pointer may be NULL. */
+size_t flp_mxfp4_bytes(int64_t V, int64_t H, size_t *packed_bytes, size_t *scale_bytes);
+
+/*
+ * Quantises W [V, ld_w] (bf16/fp16, DEVICE, finite values) to MXFP4:
+ *   s = floor(log2 max |x|) - 2 + 127 over each 32-element block, clamped to
+ *       [0, 254] (0 for an all-zero block);
+ *   each element = the E2M1 value nearest to x / 2^(s - 127), ties to the
+ *       even code, magnitudes above 6 saturated to 6; zero is stored as +0.
+ * packed and scales are DEVICE buffers of flp_mxfp4_bytes' sizes; packed
+ * 16-byte aligned.  Enqueued on `stream`.
+ */
+flp_status flp_mxfp4_quantize(const void *W, flp_dtype dtype, int64_t V, int64_t H,
+                              int64_t ld_w, uint8_t *packed, uint8_t *scales,
+                              flp_stream_t stream);
+
+/*
+ * flp_kl with the teacher head given in MXFP4 (Wt_packed, Wt_scales as
+ * produced by flp_mxfp4_quantize for V rows of H columns): the teacher logits
+ * are h_t[row] times the decoded weights, exactly (every MXFP4 value is a
+ * bf16 value, decoded in shared memory next to the tensor cores; scale codes
+ * 0 and 1 flush to zero).  bf16 only (FLP_ERR_UNSUPPORTED for fp16); H a
+ * multiple of 64; both buffers 16-byte aligned.  Same workspace as FLP_OP_KL.
+ */
+flp_status flp_kl_mxfp4(const flp_shape *shape, const void *h_s, const void *W_s,
+                        const void *h_t, const uint8_t *Wt_packed, const uint8_t *Wt_scales,
+                        const int64_t *row_idx, float *out_kl,
+                        void *workspace, size_t workspace_bytes, flp_stream_t stream);
+
+/*
  * Gradients of L = sum_i g1[i] logp_i + g2[i] ent_i (logp, ent as in
  * flp_logprob_entropy) by tile recompute:
  *   G_iv = (g1[i] (1[v = tgt_i] - p_iv) - g2[i] p_iv (z'_iv - E_p[z'_i])) / temperature

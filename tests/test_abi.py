@@ -200,3 +200,33 @@ def test_support_entry_points_validate_on_host(L):
     assert pack(FAKE, i64(4), i64(0), i64(70), sup, i64(3), None) == 1        # V = 0
     assert pack(None, i64(0), i64(70), i64(70), None, i64(3), None) == 0      # nothing to pack
     assert pack(None, i64(4), i64(70), i64(70), sup, i64(3), None) == 1
+
+
+def test_mxfp4_layout_sizes(L):
+    assert L.flp_mxfp4_rows(1) == 256 and L.flp_mxfp4_rows(256) == 256
+    assert L.flp_mxfp4_rows(257) == 512 and L.flp_mxfp4_rows(0) == 0
+    assert L.flp_mxfp4_rows(129280) == 129280
+    pb, sb = ctypes.c_size_t(), ctypes.c_size_t()
+    tot = L.flp_mxfp4_bytes(1000, 128, ctypes.byref(pb), ctypes.byref(sb))
+    assert pb.value == 2 * 1024 * 32 and sb.value == 2 * 1024 * 2 and tot == pb.value + sb.value
+    assert L.flp_mxfp4_bytes(1000, 100, None, None) == 0
+    # 4.25 bits per weight plus the row padding, against 16 for bf16
+    assert L.flp_mxfp4_bytes(129280, 4096, None, None) == 129280 * 4096 * 17 // 32
+
+
+def test_mxfp4_entry_points_validate_on_host(L):
+    s = _shape()
+    assert L.flp_kl_mxfp4(ctypes.byref(s), FAKE, FAKE, FAKE, None, FAKE, None, FAKE, FAKE,
+                          ctypes.c_size_t(1 << 40), None) == 1          # packed missing
+    assert L.flp_kl_mxfp4(ctypes.byref(s), FAKE, FAKE, FAKE, ctypes.c_void_p((1 << 20) + 8), FAKE,
+                          None, FAKE, FAKE, ctypes.c_size_t(1 << 40), None) == 1   # alignment
+    half = _shape(dtype=1)
+    assert L.flp_kl_mxfp4(ctypes.byref(half), FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE,
+                          ctypes.c_size_t(1 << 40), None) == 2          # fp16: unsupported
+    odd = _shape(H=520, ld_h=520, ld_w=520)
+    assert L.flp_kl_mxfp4(ctypes.byref(odd), FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE,
+                          ctypes.c_size_t(1 << 40), None) == 1          # H % 64
+    i64 = ctypes.c_int64
+    assert L.flp_mxfp4_quantize(FAKE, 0, i64(100), i64(96), i64(96), FAKE, FAKE, None) == 1
+    assert L.flp_mxfp4_quantize(FAKE, 0, i64(100), i64(128), i64(64), FAKE, FAKE, None) == 1
+    assert L.flp_mxfp4_quantize(None, 0, i64(100), i64(128), i64(128), FAKE, FAKE, None) == 1
