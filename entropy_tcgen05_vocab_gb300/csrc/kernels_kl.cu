@@ -174,12 +174,15 @@ struct KlEpi {
 
 using KlLayout = PipeLayout<kKlBN, kKlStages, 2, kKlCG, kKlAcc>;
 using KlMxLayout = PipeLayout<kKlBN, kKlStages, 2, kKlCG, kKlAcc, false, true>;
+// With the MX teacher head, four epilogue warps (the eight converter warps
+// take the place of the other four).
+constexpr int kKlMxEpiWarps = 4;
 #define KL_KERNEL vocab_pipeline_kernel<kKlBN, kKlStages, 2, KlEpi, kKlCG, kKlAcc, kKlEpiWarps>
 // the teacher head's B operand decoded from MXFP4 in shared memory
 #define KL_MX_KERNEL \
-  vocab_pipeline_kernel<kKlBN, kKlStages, 2, KlEpi, kKlCG, kKlAcc, kKlEpiWarps, false, true>
+  vocab_pipeline_kernel<kKlBN, kKlStages, 2, KlEpi, kKlCG, kKlAcc, kKlMxEpiWarps, false, true>
 constexpr int kKlThreads = pipe_threads(kKlEpiWarps);
-constexpr int kKlMxThreads = pipe_threads(kKlEpiWarps, true);
+constexpr int kKlMxThreads = pipe_threads(kKlMxEpiWarps, true);
 
 cudaError_t launch_kl(const KlArgs &a, cudaStream_t stream) {
   KlEpi::Params p;
@@ -191,7 +194,8 @@ cudaError_t launch_kl(const KlArgs &a, cudaStream_t stream) {
   p.pms = a.pms;
   p.pss = a.pss;
   p.counters = a.counters;
-  p.splits = a.sch.splits * (kKlEpiWarps / 4);  // partial slots per row
+  // partial slots per row
+  p.splits = a.sch.splits * ((a.mx.packed ? kKlMxEpiWarps : kKlEpiWarps) / 4);
   p.row_idx = a.row_idx;
   p.T = a.T;
   p.out_kl = a.out_kl;

@@ -29,13 +29,15 @@
 //
 // MX: the second GEMM's B operand (a teacher head) is stored in MXFP4 (E2M1
 // elements with an E8M0 scale per 32, in the blocked layout of MxOperand).
-// Each CTA's producer bulk-copies its rows' packed codes and scales into a
-// small staging buffer per stage; four converter warps decode them exactly
-// into bf16 in the 128B-swizzled layout a TMA copy would have written, fence
-// them into the async proxy and arrive on the leader's "converted" barrier,
-// which the MMA issuer waits on with the "full" one.  Every E2M1 value times
-// a power of two is a bf16 value, so the bf16 MMA computes exactly the
-// product with the decoded weights.
+// Four converter warps per CTA own it.  They keep a ring of kQStages small
+// staging buffers filled with bulk copies of their CTA's rows' codes and
+// scales, kQStages k-blocks ahead of the MMAs.  For each k-block they wait
+// until the MMAs have released the stage's B slot ("empty"), decode the codes
+// exactly into bf16 in the 128B-swizzled layout a TMA copy would have
+// written, fence them into the async proxy and arrive on the leader's
+// "converted" barrier, which the MMA issuer waits on with the "full" one.
+// Every E2M1 value times a power of two is a bf16 value, so the bf16 MMA
+// computes exactly the product with the decoded weights.
 //
 // CTA pairs (CG = 2, cluster of 2): each CTA loads its own 128 rows of A and
 // its half (BN/2 rows) of B; the leader (rank 0) issues tcgen05.mma.cta_group::2
@@ -64,9 +66,9 @@ constexpr int kPipeThreads = 64 + 32 * kEpiWarps;
 // Threads of a vocabulary-pipeline CTA with EPIW epilogue warps (4 or 8).
 // With 8, two warps share each 32-lane TMEM quarter and split its columns.
 __host__ __device__ constexpr int pipe_threads(int epiw) { return 64 + 32 * epiw; }
-// Four more warps decode an MX operand.
+// Eight more warps decode an MX operand.
 __host__ __device__ constexpr int pipe_threads(int epiw, bool mx) {
-  return pipe_threads(epiw) + (mx ? 128 : 0);
+  return pipe_threads(epiw) + (mx ? 256 : 0);
 }
 
 // NOPS independent GEMMs share one tile (the KL pipeline runs the student and
@@ -77,45 +79,118 @@ __host__ __device__ constexpr int pipe_threads(int epiw, bool mx) {
 // SHARED_A: the NOPS GEMMs share one A operand and take their B operands from
 // consecutive BN-row blocks of the same matrix, so the vocabulary tile is
 // NOPS x BN columns wide (one A load feeds NOPS MMAs of N = BN).
-// One row of 64 MXFP4 elements -> 64 bf16 written as the row of a
-// 128B-swizzled K-major tile: 16-byte chunk c (elements 8c .. 8c+7) goes to
-// chunk position c ^ (row % 8) of the row's 128 bytes.  An element with code
-// (sign, e, m) and block scale code s is (-1)^sign (e ? 1 + m/2 : m/2)
-// 2^(e - 1 + s - 127): bf16 exponent field s + e - 1, mantissa bit m when
-// e > 0.  Exponent fields below 1 (scale codes 0 and 1) flush to zero.
-__device__ __forceinline__ uint32_t mx_bf16_pair(uint32_t byte, uint32_t scale) {
-  uint32_t out = 0;
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const uint32_t code = (byte >> (4 * h)) & 15u;
-    const uint32_t mag = code & 7u;
-    const uint32_t e = mag >> 1;
-    const int32_t ex = static_cast<int32_t>(scale + e) - 1;
-    const uint32_t mant = (e != 0u) ? (mag & 1u) : 0u;
-    uint32_t bits = ((code & 8u) << 12) | (static_cast<uint32_t>(ex) << 7) | (mant << 6);
-    bits = (mag != 0u && ex > 0) ? bits : 0u;
-    out |= bits << (16 * h);
-  }
-  return out;
+// MXFP4 -> bf16.  A code (sign, e, m) with block scale code s is
+// (-1)^sign (e ? 1 + m/2 : m/2) 2^(e - 1 + s - 127), so for s in [2, 252] the
+// seven non-zero magnitudes have bf16 exponent fields s-1, s, s, s+1, s+1,
+// s+2, s+2 and mantissa 0x40 for the odd magnitude codes from 3.  Per block
+// the high and low bytes of the eight bf16 patterns form two 8-entry byte
+// tables, and one byte permute looks four elements up at once.  Other scale
+// codes (never produced from bf16 weights) take the field-by-field path.
+struct MxTable {
+  uint32_t hlo, hhi, llo, lhi;
+};
+
+__device__ __forceinline__ MxTable mx_table(uint32_t s) {
+  const uint32_t f1 = s - 1, f2 = s, f4 = s + 1, f6 = s + 2;  // exponent fields
+  MxTable t;
+  t.hlo = ((f1 >> 1) << 8) | ((f2 >> 1) << 16) | ((f2 >> 1) << 24);
+  t.hhi = (f4 >> 1) | ((f4 >> 1) << 8) | ((f6 >> 1) << 16) | ((f6 >> 1) << 24);
+  const uint32_t l1 = (f1 & 1u) << 7, l2 = (f2 & 1u) << 7, l4 = (f4 & 1u) << 7,
+                 l6 = (f6 & 1u) << 7;
+  t.llo = (l1 << 8) | (l2 << 16) | ((l2 | 0x40u) << 24);
+  t.lhi = l4 | ((l4 | 0x40u) << 8) | (l6 << 16) | ((l6 | 0x40u) << 24);
+  return t;
 }
 
+// Field-by-field decode of one code (any scale code; exponent fields below 1
+// flush to zero).
+__device__ __forceinline__ uint32_t mx_bf16_slow(uint32_t code, uint32_t s) {
+  const uint32_t mag = code & 7u, e = mag >> 1;
+  const int32_t ex = static_cast<int32_t>(s + e) - 1;
+  const uint32_t mant = (e != 0u) ? (mag & 1u) : 0u;
+  const uint32_t bits = ((code & 8u) << 12) | (static_cast<uint32_t>(ex) << 7) | (mant << 6);
+  return (mag != 0u && ex > 0 && ex < 255) ? bits : ((code & 8u) << 12);
+}
+
+// PTX prmt in its default mode: selector nibble i picks byte (nibble & 7) of
+// {a, b} for result byte i, replicated from that byte's top bit when the
+// nibble's top bit is set.
+__device__ __forceinline__ uint32_t prmt_sign(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+
+// Eight codes (one word, element i in nibble i) -> four bf16 pairs.
+__device__ __forceinline__ void mx_word(uint32_t w, const MxTable &t, uint32_t s, bool fast,
+                                        uint32_t (&o)[4]) {
+  if (fast) {
+    const uint32_t sel0 = w & 0x7777u, sel1 = (w >> 16) & 0x7777u;
+    const uint32_t h0 = __byte_perm(t.hlo, t.hhi, sel0), l0 = __byte_perm(t.llo, t.lhi, sel0);
+    const uint32_t h1 = __byte_perm(t.hlo, t.hhi, sel1), l1 = __byte_perm(t.llo, t.lhi, sel1);
+    // Signs: the top bit of byte k of w is the sign of element 2k+1, of w << 4
+    // the sign of element 2k; a permute in sign-replicating mode spreads them
+    // to the top bytes of each bf16 pair.
+    const uint32_t w4 = w << 4;
+    o[0] = __byte_perm(l0, h0, 0x5140) | (prmt_sign(w4, w, 0xC080u) & 0x80008000u);
+    o[1] = __byte_perm(l0, h0, 0x7362) | (prmt_sign(w4, w, 0xD090u) & 0x80008000u);
+    o[2] = __byte_perm(l1, h1, 0x5140) | (prmt_sign(w4, w, 0xE0A0u) & 0x80008000u);
+    o[3] = __byte_perm(l1, h1, 0x7362) | (prmt_sign(w4, w, 0xF0B0u) & 0x80008000u);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      o[i] = mx_bf16_slow((w >> (8 * i)) & 15u, s) | (mx_bf16_slow((w >> (8 * i + 4)) & 15u, s) << 16);
+  }
+}
+
+// One row of 64 MXFP4 elements -> 64 bf16 written as the row of a
+// 128B-swizzled K-major tile: 16-byte chunk c (elements 8c .. 8c+7) goes to
+// chunk position c ^ (row % 8) of the row's 128 bytes.
 __device__ __forceinline__ void mx_decode_row(const uint8_t *codes, const uint8_t *sc,
                                               uint8_t *row_base, int row) {
   const uint4 q0 = *reinterpret_cast<const uint4 *>(codes);
   const uint4 q1 = *reinterpret_cast<const uint4 *>(codes + 16);
   const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
   const uint32_t s0 = sc[0], s1 = sc[1];
+  const MxTable t0 = mx_table(s0), t1 = mx_table(s1);
+  const bool f0 = s0 >= 2u && s0 <= 252u, f1 = s1 >= 2u && s1 <= 252u;
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {  // chunk c: code bytes 4c .. 4c+3 = one word
-    const uint32_t s = c < 4 ? s0 : s1;
-    uint4 o;
-    o.x = mx_bf16_pair(w[c] & 0xffu, s);
-    o.y = mx_bf16_pair((w[c] >> 8) & 0xffu, s);
-    o.z = mx_bf16_pair((w[c] >> 16) & 0xffu, s);
-    o.w = mx_bf16_pair(w[c] >> 24, s);
-    *reinterpret_cast<uint4 *>(row_base + ((c ^ (row & 7)) << 4)) = o;
+  for (int c = 0; c < 8; ++c) {  // chunk c: elements 8c .. 8c+7 = code word c
+    uint32_t o[4];
+    if (c < 4)
+      mx_word(w[c], t0, s0, f0, o);
+    else
+      mx_word(w[c], t1, s1, f1, o);
+    *reinterpret_cast<uint4 *>(row_base + ((c ^ (row & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
+
+// The (vocabulary tile, k-block) sequence a CTA (pair) works through, in the
+// order of its items; used to run ahead of the MMAs.
+struct KSeq {
+  int it, vt, vt1, kb;
+  bool valid;
+  __device__ __forceinline__ void load(const Schedule &s) {
+    valid = it < s.items;
+    if (valid) {
+      int mt, sp, vt0;
+      s.item(it, mt, sp, vt0, vt1);
+      vt = vt0;
+    }
+  }
+  __device__ __forceinline__ void first(const Schedule &s, int unit) {
+    it = unit;
+    kb = 0;
+    load(s);
+  }
+  __device__ __forceinline__ void next(const Schedule &s, int num_units) {
+    if (++kb < s.k_blocks) return;
+    kb = 0;
+    if (++vt < vt1) return;
+    it += num_units;
+    load(s);
+  }
+};
 
 template <int BN, int STAGES, int NOPS = 1, int CG = 1, int NACC = 2, bool SHARED_A = false,
           bool MX = false>
@@ -130,16 +205,21 @@ struct PipeLayout {
   static constexpr int kTmemCols = NACC * kAccCols;
   static_assert(NACC == 1 || NACC == 2, "one or two accumulator buffers");
   static constexpr int kBarrierBytes = 8 * (2 * STAGES + 5) + 16;
-  // MX: "staged" and "converted" barriers per stage, then per stage the
-  // CTA's B rows' codes (32 bytes each) and scale codes (2 bytes each).
-  static constexpr int kMxBarrierBytes = MX ? 16 * STAGES : 0;
-  static constexpr int kQCodeBytes = kBRows * 32;
-  static constexpr int kQBytes = MX ? kBRows * 34 : 0;
+  // MX: a "converted" barrier per stage, then for each of the eight
+  // converter warps (two groups of four, taking alternate k-blocks) a ring of
+  // kQStages staging buffers (a "staged" barrier each) holding its 32 B rows'
+  // codes (32 bytes each) and scale codes (2 bytes each) of one k-block.
+  static constexpr int kCvtWarps = 8;
+  static constexpr int kQStages = 3;
+  static constexpr int kMxBarrierBytes = MX ? 8 * (STAGES + kCvtWarps * kQStages) : 0;
+  static constexpr int kQCodeBytes = 32 * 32;
+  static constexpr int kQBytes = MX ? 32 * 34 : 0;  // one warp's slot
   static constexpr int kQOffset =
       (STAGES * kStageBytes + kBarrierBytes + kMxBarrierBytes + 127) / 128 * 128;
   // + 1024 so the stage ring can be aligned to a swizzle atom.
-  static constexpr int kSmemBytes = kQOffset + STAGES * kQBytes + 1024;
-  static_assert(!MX || (NOPS == 2 && !SHARED_A), "the MX operand is the second GEMM's B");
+  static constexpr int kSmemBytes = kQOffset + kCvtWarps * kQStages * kQBytes + 1024;
+  static_assert(!MX || (NOPS == 2 && !SHARED_A && kBRows == 128),
+                "the MX operand is the second GEMM's B, 128 rows per CTA");
   static_assert(kQBytes % 16 == 0, "staging buffers stay 16-byte aligned");
   static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM columns must be a power of two");
   static_assert(CG == 1 || CG == 2, "one CTA or a CTA pair");
@@ -213,8 +293,8 @@ __global__ void __launch_bounds__(pipe_threads(EPIW, MX), 1)
   uint64_t *drain = tempty + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-  uint64_t *qfull = reinterpret_cast<uint64_t *>(smem + STAGES * L::kStageBytes + L::kBarrierBytes);
-  uint64_t *cvt = qfull + STAGES;
+  uint64_t *cvt = reinterpret_cast<uint64_t *>(smem + STAGES * L::kStageBytes + L::kBarrierBytes);
+  uint64_t *qfull = cvt + STAGES;  // [8 warps][kQStages]
   uint8_t *qbuf = smem + L::kQOffset;
 
   const int warp = threadIdx.x >> 5;
@@ -235,10 +315,8 @@ __global__ void __launch_bounds__(pipe_threads(EPIW, MX), 1)
     }
     mbar_init(drain, 1);
     if (MX) {
-      for (int st = 0; st < STAGES; ++st) {
-        mbar_init(&qfull[st], 1);
-        mbar_init(&cvt[st], 4 * CG);  // four converter warps per CTA
-      }
+      for (int st = 0; st < STAGES; ++st) mbar_init(&cvt[st], 4 * CG);  // 4 converter warps per CTA
+      for (int q = 0; q < L::kCvtWarps * L::kQStages; ++q) mbar_init(&qfull[q], 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -287,14 +365,7 @@ __global__ void __launch_bounds__(pipe_threads(EPIW, MX), 1)
             if (leader)
               mbar_arrive_expect_tx(&full[stage],
                                     CG * (MX ? L::kStageBytes - L::kBBytes : L::kStageBytes));
-            if constexpr (MX) {  // this CTA's B rows of the MX operand, to its staging buffer
-              const MxOperand &mx = ep.mx;
-              const int64_t blk = static_cast<int64_t>(kb) * mx.v_pad + brow;
-              uint8_t *q = qbuf + stage * L::kQBytes;
-              mbar_arrive_expect_tx(&qfull[stage], L::kQBytes);
-              bulk_load(q, mx.packed + blk * 32, L::kQCodeBytes, &qfull[stage]);
-              bulk_load(q + L::kQCodeBytes, mx.scales + blk * 2, L::kBRows * 2, &qfull[stage]);
-            }
+
             // second GEMM: its own A and B maps, or (SHARED_A) the next BN rows of B
             const CUtensorMap *tb1 = SHARED_A ? &tmB0 : &tmB1;
             const int brow1 = SHARED_A ? brow + BN : brow;
@@ -335,14 +406,6 @@ __global__ void __launch_bounds__(pipe_threads(EPIW, MX), 1)
             const uint32_t par = (s < stage) ? phase : (phase ^ 1u);
             int never = 0;
             mbar_wait(&full[s], par, &never);
-          }
-        }
-        if (MX) {  // and this CTA's own staging copies
-          for (int s = 0; s < STAGES; ++s) {
-            if (!(armed & (1u << s))) continue;
-            const uint32_t par = (s < stage) ? phase : (phase ^ 1u);
-            int never = 0;
-            mbar_wait(&qfull[s], par, &never);
           }
         }
       }
@@ -426,42 +489,85 @@ __global__ void __launch_bounds__(pipe_threads(EPIW, MX), 1)
     }
   } else if (MX && warp >= 2 + EPIW) {
     // ------------------------------------------------------------ MX converters
-    // Thread t of the four warps decodes B row t of this CTA's half, stage by
-    // stage in the producer's order.
-    const int crow = (warp - 2 - EPIW) * 32 + lane;
-    const uint32_t cvt_dst = kPair ? mapa_shared(smem_u32(cvt), 0) : smem_u32(cvt);
-    int stage = 0;
-    uint32_t phase = 0;
-    bool ok = true;
-    for (int it = unit; ok && it < sch.items; it += num_units) {
-      int mt, sp, vt0, vt1;
-      sch.item(it, mt, sp, vt0, vt1);
-      for (int vt = vt0; ok && vt < vt1; ++vt) {
-        for (int kb = 0; kb < sch.k_blocks; ++kb) {
-          ok = mbar_wait(&qfull[stage], phase, abort_flag);
-          if (!__all_sync(0xffffffffu, ok)) {
-            ok = false;
-            break;
-          }
-          const uint8_t *q = qbuf + stage * L::kQBytes;
-          uint8_t *b1 = smem + stage * L::kStageBytes + L::kAOps * L::kABytes + L::kBBytes;
-          mx_decode_row(q + crow * 32, q + L::kQCodeBytes + crow * 2, b1 + crow * 128, crow);
-          fence_async_smem();  // the MMAs read these bytes through the async proxy
-          __syncwarp();
-          if (lane == 0) {
-            if (kPair)
-              mbar_arrive_cluster(cvt_dst + stage * 8);
-            else
-              mbar_arrive(&cvt[stage]);
-          }
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
+    // Two groups of four warps take alternate k-blocks (group 0 the even
+    // ones of this CTA's sequence), so each has two k-blocks of MMA time per
+    // decode.  Thread t of warp cw decodes B row 32 (cw % 4) + t of this CTA's
+    // half.  Lane 0 keeps the warp's own staging ring kQStages of its
+    // k-blocks ahead; a slot is refilled right after the warp decoded it.
+    if constexpr (MX) {
+      constexpr int QS = L::kQStages;
+      const int cw = warp - 2 - EPIW;
+      const int group = cw >> 2;
+      const int crow = (cw & 3) * 32 + lane;
+      const MxOperand &mx = ep.mx;
+      const uint32_t cvt_dst = kPair ? mapa_shared(smem_u32(cvt), 0) : smem_u32(cvt);
+      uint64_t *wfull = qfull + cw * QS;
+      uint8_t *wbuf = qbuf + cw * QS * L::kQBytes;
+      KSeq ahead, cur;
+      ahead.first(sch, unit);
+      cur.first(sch, unit);
+      if (group == 1) {
+        ahead.next(sch, num_units);
+        cur.next(sch, num_units);
+      }
+      uint32_t issued = 0, consumed = 0;
+      // lane 0: stage the k-block `ahead` points at into slot issued % QS
+      auto stage_next = [&]() {
+        const int q = static_cast<int>(issued % QS);
+        const int64_t brow = static_cast<int64_t>(ahead.vt) * L::kTileCols +
+                             static_cast<int64_t>(rank) * L::kBRows + (cw & 3) * 32;
+        const int64_t blk = static_cast<int64_t>(ahead.kb) * mx.v_pad + brow;
+        uint8_t *dst = wbuf + q * L::kQBytes;
+        mbar_arrive_expect_tx(&wfull[q], L::kQBytes);
+        bulk_load(dst, mx.packed + blk * 32, L::kQCodeBytes, &wfull[q]);
+        bulk_load(dst + L::kQCodeBytes, mx.scales + blk * 2, 64, &wfull[q]);
+        ++issued;
+        ahead.next(sch, num_units);
+        ahead.next(sch, num_units);
+      };
+      if (lane == 0)
+        for (int i = 0; i < QS && ahead.valid; ++i) stage_next();
+      bool ok = true;
+      uint32_t g = static_cast<uint32_t>(group);  // index of `cur` in the CTA's k-block sequence
+      while (ok && cur.valid) {
+        const int stage = static_cast<int>(g % STAGES);
+        const uint32_t phase = (g / STAGES) & 1u;
+        const int q = static_cast<int>(consumed % QS);
+        // the MMAs are done with this stage's B slot, and the codes have landed
+        if (lane == 0) ok = mbar_wait(&empty[stage], phase ^ 1u, abort_flag);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (ok) ok = mbar_wait(&wfull[q], (consumed / QS) & 1u, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        const uint8_t *src = wbuf + q * L::kQBytes;
+        uint8_t *b1 = smem + stage * L::kStageBytes + L::kAOps * L::kABytes + L::kBBytes;
+        mx_decode_row(src + lane * 32, src + L::kQCodeBytes + lane * 2, b1 + crow * 128, crow);
+        // the MMAs read the rows, and the next bulk copy rewrites the slot,
+        // through the async proxy
+        fence_async_smem();
+        __syncwarp();
+        ++consumed;
+        if (lane == 0) {
+          if (kPair)
+            mbar_arrive_cluster(cvt_dst + stage * 8);
+          else
+            mbar_arrive(&cvt[stage]);
+          if (ahead.valid) stage_next();
+        }
+        g += 2;
+        cur.next(sch, num_units);
+        cur.next(sch, num_units);
+      }
+      if (lane == 0) {
+        if (!ok) record_timeout<CG>(status, abort_flag);
+        for (uint32_t c = consumed; c < issued; ++c) {  // let the copies in flight land
+          int never = 0;
+          mbar_wait(&wfull[c % QS], (c / QS) & 1u, &never);
         }
       }
     }
-    if (!ok && lane == 0) record_timeout<CG>(status, abort_flag);
   } else {
     // ------------------------------------------------------------ epilogue
     const int lg = warp & 3;  // the TMEM lane quarter this warp may access
