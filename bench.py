@@ -62,6 +62,11 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--T", type=int, default=None,
                    help="replace the workload's row count (same H, V, recipe): small profiling cases")
+    p.add_argument("--teacher", choices=["bf16", "mxfp4"], default="bf16",
+                   help="KL workloads: the teacher head in bf16 or in MXFP4 (quantised before timing)")
+    p.add_argument("--support-j", type=int, default=None,
+                   help="forward workloads: restrict each row to a sampling support keeping each "
+                        "token with probability 2^-J (targets kept)")
     return p.parse_args()
 
 
@@ -217,8 +222,11 @@ def call_once(flp, d, ws, stats=None):
     w = d["workload"]
     if w.kind == "fwd":
         return flp.logprob_entropy(d["h"], d["W"], d["targets"], d["row_idx"], d["tau"],
-                                   workspace=ws)
+                                   workspace=ws, support=d.get("support"))
     if w.kind == "kl":
+        if d.get("mx") is not None:
+            return flp.kl_divergence_mxfp4(d["h_s"], d["W_s"], d["h_t"], *d["mx"], d["row_idx"],
+                                           workspace=ws)
         return flp.kl_divergence(d["h_s"], d["W_s"], d["h_t"], d["W_t"], d["row_idx"],
                                  workspace=ws)
     lse, ez = stats
@@ -372,6 +380,16 @@ def run_ours(args):
 
     w0 = workloads.WORKLOADS[args.workload]
     d = workloads.make(w0 if args.T is None else w0.scaled(T=args.T), device=device)
+    variant = {}
+    if args.teacher == "mxfp4" and w0.kind == "kl":
+        d["mx"] = flp.mxfp4_quantize(d["W_t"])
+        variant["teacher_head"] = "MXFP4 (E2M1 + E8M0 per 32), quantised before timing"
+    if args.support_j is not None and w0.kind == "fwd":
+        d["support"] = torch.from_numpy(workloads.support_words(
+            d["workload"].T, d["workload"].V, args.support_j, d["workload"].seed,
+            targets=d["targets"].cpu().numpy())).to(device)
+        variant["support"] = "each token kept with probability 2^-%d, targets kept" % args.support_j
+    headline = w0.kind == "fwd" and args.workload == 1 and args.T is None and not variant
     sampler = ClockSampler(device.index) if rank == 0 else None
     if sampler:
         sampler.start()
@@ -382,10 +400,10 @@ def run_ours(args):
     value = job_throughput(n, args.steps, total_ms, world)
     fl = flops_per_call(d)
     achieved = fl / (kernel_ms / 1e3) / 1e12
-    traffic, traffic_src = recorded_traffic()
+    traffic, traffic_src = recorded_traffic() if headline else (None, "not the headline kernel")
 
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and w0.kind == "fwd":
         e2e_steps = min(args.steps, 100)
         e2e_ms, h2d, d2h = time_e2e(flp, d, ws, e2e_steps, world, device)
         e2e_ms = max_over_ranks(e2e_ms, world, device)
@@ -398,13 +416,18 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": d["workload"].dtype,
         "data": "synthetic (seeded; shapes and distributions of the pages' workloads)",
-        "config": dict(describe(d), parallelism="replicas" if world > 1 else "single GPU"),
+        "config": dict(describe(d), parallelism="replicas" if world > 1 else "single GPU",
+                       **variant),
         "tflops": world * fl * args.steps / (total_ms / 1e3) / 1e12,
         "pct_of_bf16_peak": 100.0 * fl * args.steps / (total_ms / 1e3) / 1e12 / P["bf16_tflops"],
         "kernel_ms": kernel_ms,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": P["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": achieved / P["bf16_tflops"], "traffic": traffic,
-                     "kernel": "vocab_pipeline_kernel<256,4,2,LseEpi<1>,2,1,8,true>",
+                     "kernel": {"fwd": "vocab_pipeline_kernel<256,4,2,LseEpi<1,%s>,2,1,8,true>"
+                                       % ("true" if "support" in variant else "false"),
+                                "kl": "vocab_pipeline_kernel<256,3,2,KlEpi,2,1,%s>"
+                                      % ("4,false,true" if "teacher_head" in variant else "8"),
+                                "bwd": "grad pass + dh and dW GEMMs"}[w0.kind],
                      "peak_kind": "bf16 dense, burst, %s" % P["source"],
                      "frac_of_sustained": achieved / P["bf16_tflops_sustained"],
                      "algorithmic_flops_per_launch": fl,
