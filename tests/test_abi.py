@@ -230,3 +230,30 @@ def test_mxfp4_entry_points_validate_on_host(L):
     assert L.flp_mxfp4_quantize(FAKE, 0, i64(100), i64(96), i64(96), FAKE, FAKE, None) == 1
     assert L.flp_mxfp4_quantize(FAKE, 0, i64(100), i64(128), i64(64), FAKE, FAKE, None) == 1
     assert L.flp_mxfp4_quantize(None, 0, i64(100), i64(128), i64(128), FAKE, FAKE, None) == 1
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """Without the built .so every entry point raises: there is no CPU or
+    PyTorch fallback for the product path."""
+    monkeypatch.setattr(flp._build, "LIB", str(tmp_path / "absent.so"))
+    monkeypatch.setattr(flp, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        flp.lib()
+    h = torch.zeros(4, 64, dtype=torch.bfloat16)
+    with pytest.raises((RuntimeError, TypeError)):
+        flp.logprob_entropy(h, h, torch.zeros(4, dtype=torch.int64))
+
+
+def test_product_package_does_not_import_the_oracle():
+    import ast
+    pkg = os.path.join(ROOT, "entropy_tcgen05_vocab_gb300")
+    for fn in os.listdir(pkg):
+        if fn.endswith(".py"):
+            tree = ast.parse(open(os.path.join(pkg, fn)).read())
+            for node in ast.walk(tree):
+                mods = []
+                if isinstance(node, ast.Import):
+                    mods = [a.name for a in node.names]
+                elif isinstance(node, ast.ImportFrom):
+                    mods = [node.module or ""]
+                assert not any(m == "oracle" or m.startswith("oracle.") for m in mods), fn
