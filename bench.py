@@ -109,7 +109,7 @@ def recorded_traffic():
     if kv.get("kernel_sources_sha256") != kernel_sources_sha():
         return None, "kernel changed since the ncu capture"
     try:
-        return int(kv["dram_bytes_per_launch"]), TRAFFIC_FILE
+        return int(kv["dram_bytes_per_launch"]), os.path.relpath(TRAFFIC_FILE, ROOT)
     except (KeyError, ValueError):
         return None, "no dram_bytes_per_launch"
 
