@@ -161,3 +161,10 @@ def test_backward_dw_rows_exact_at_full_vocabulary():
                            d["g1"].cpu().numpy(), d["g2"].cpu().numpy(), "bf16",
                            dh_rows_sel=np.zeros(0, np.int64), vsel=vsel)
     _rel(dW[torch.from_numpy(vsel).cuda()], want, "dW (sampled vocabulary rows)")
+
+
+def test_backward_repeated_calls_are_bitwise_identical():
+    d = _case(300, 256, 3000)
+    a = flp.backward(d["h"], d["W"], d["targets"], d["row_idx"], d["tau"], d["g1"], d["g2"])
+    b = flp.backward(d["h"], d["W"], d["targets"], d["row_idx"], d["tau"], d["g1"], d["g2"])
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])

@@ -221,3 +221,29 @@ def test_kl_at_the_planner_extremes():
     kl = flp.kl_divergence(d["h_s"], d["W_s"], d["h_t"], d["W_t"])
     want = coracle.kl(d["h_s"].cpu(), d["W_s"].cpu(), d["h_t"].cpu(), d["W_t"].cpu(), None, "bf16")
     _check(kl, want, "kl")
+
+
+def test_no_vocabulary_sized_buffer_is_allocated():
+    """The call allocates nothing beyond its outputs: the peak of torch's
+    allocator over the call, with the workspace passed in, is the two [n]
+    outputs, and the device's free memory is unchanged afterwards (the
+    library itself never allocates).  The workspace is far below the [T, V]
+    FP32 logits (2.5 GB at this size)."""
+    d = workloads.make(1, device="cuda")
+    w = d["workload"]
+    shape = flp.make_shape(w.T, w.H, w.V, d["n"], torch.bfloat16)
+    ws = torch.empty(flp.workspace_size(shape, flp.OP_LOGPROB_ENTROPY), dtype=torch.uint8,
+                     device="cuda")
+    flp.logprob_entropy(d["h"], d["W"], d["targets"], None, d["tau"], workspace=ws)
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    torch.cuda.reset_peak_memory_stats()
+    base = torch.cuda.memory_allocated()
+    logp, ent = flp.logprob_entropy(d["h"], d["W"], d["targets"], None, d["tau"], workspace=ws)
+    torch.cuda.synchronize()
+    peak = torch.cuda.max_memory_allocated() - base
+    assert peak <= 2 * 4 * w.T + (1 << 20), peak
+    assert torch.cuda.mem_get_info()[0] >= free0 - (2 << 20)
+    logits_bytes = w.T * w.V * 4
+    assert ws.numel() * 20 < logits_bytes, (ws.numel(), logits_bytes)
+    del logp, ent

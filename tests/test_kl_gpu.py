@@ -108,3 +108,11 @@ def test_distillation_workload_sampled():
     k = kl.cpu().numpy()
     assert np.all(np.isfinite(k)) and np.all(k >= -1e-4)
     print("distillation workload: %d sampled rows, max|dKL| %.2e, mean KL %.3f" % (len(pos), e, k.mean()))
+
+
+def test_kl_repeated_calls_are_bitwise_identical():
+    w = workloads.WORKLOADS[3].scaled(T=700, H=256, V=9000, seed=81)
+    d = workloads.make(w, device="cuda")
+    a = flp.kl_divergence(d["h_s"], d["W_s"], d["h_t"], d["W_t"])
+    b = flp.kl_divergence(d["h_s"], d["W_s"], d["h_t"], d["W_t"])
+    assert torch.equal(a, b)

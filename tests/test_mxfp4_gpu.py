@@ -117,3 +117,10 @@ def test_distill_workload_with_mxfp4_teacher_sampled():
     assert np.abs(got - want).max() <= TOL
     allkl = kl.cpu().numpy()
     assert np.all(np.isfinite(allkl)) and np.all(allkl >= -1e-4)
+
+
+def test_kl_mxfp4_repeated_calls_are_bitwise_identical():
+    d = _kl_case(300, 256, 3000, seed=82)
+    a = flp.kl_divergence_mxfp4(d["h_s"], d["W_s"], d["h_t"], d["packed"], d["scales"])
+    b = flp.kl_divergence_mxfp4(d["h_s"], d["W_s"], d["h_t"], d["packed"], d["scales"])
+    assert torch.equal(a, b)

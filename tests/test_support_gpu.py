@@ -251,3 +251,10 @@ def test_autograd_with_support():
     assert torch.allclose(h.grad.float(), dh.float(), rtol=0, atol=1e-3 * dh.float().abs().max())
     assert torch.allclose(W.grad.float(), dW.to(W.dtype).float(), rtol=0,
                           atol=1e-2 * dW.abs().max())
+
+
+def test_support_repeated_calls_are_bitwise_identical():
+    d = _case(300, 256, 5000, 2, seed=83)
+    a = flp.logprob_entropy(d["h"], d["W"], d["targets"], None, 0.7, support=d["support"])
+    b = flp.logprob_entropy(d["h"], d["W"], d["targets"], None, 0.7, support=d["support"])
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
