@@ -29,13 +29,17 @@
 //
 // MX: the second GEMM's B operand (a teacher head) is stored in MXFP4 (E2M1
 // elements with an E8M0 scale per 32, in the blocked layout of MxOperand).
-// Four converter warps per CTA own it.  They keep a ring of kQStages small
-// staging buffers filled with bulk copies of their CTA's rows' codes and
-// scales, kQStages k-blocks ahead of the MMAs.  For each k-block they wait
-// until the MMAs have released the stage's B slot ("empty"), decode the codes
-// exactly into bf16 in the 128B-swizzled layout a TMA copy would have
-// written, fence them into the async proxy and arrive on the leader's
-// "converted" barrier, which the MMA issuer waits on with the "full" one.
+// Eight converter warps per CTA own it, in two groups of four that take
+// alternate k-blocks, and a ring of kDSlots decoded slots, one deeper than
+// the stage ring.  Each warp keeps a ring of kQStages small staging buffers
+// filled with bulk copies of its 32 rows' codes and scales, ahead of the
+// MMAs.  For each of its k-blocks a warp waits until the MMAs have released
+// the decoded slot ("released"), decodes the codes exactly into bf16 in the
+// 128B-swizzled layout a TMA copy would have written, fences them into the
+// async proxy and arrives on a CTA-local barrier.  A relay warp per group
+// turns the four local arrivals into one arrival on the leader's "converted"
+// barrier, which the MMA issuer waits on with the "full" one (the
+// cluster-scope release that arrival needs costs about a microsecond).
 // Every E2M1 value times a power of two is a bf16 value, so the bf16 MMA
 // computes exactly the product with the decoded weights.
 //
@@ -66,9 +70,9 @@ constexpr int kPipeThreads = 64 + 32 * kEpiWarps;
 // Threads of a vocabulary-pipeline CTA with EPIW epilogue warps (4 or 8).
 // With 8, two warps share each 32-lane TMEM quarter and split its columns.
 __host__ __device__ constexpr int pipe_threads(int epiw) { return 64 + 32 * epiw; }
-// Eight more warps decode an MX operand.
+// Eight more warps decode an MX operand and two relay their completion.
 __host__ __device__ constexpr int pipe_threads(int epiw, bool mx) {
-  return pipe_threads(epiw) + (mx ? 256 : 0);
+  return pipe_threads(epiw) + (mx ? 320 : 0);
 }
 
 // NOPS independent GEMMs share one tile (the KL pipeline runs the student and
@@ -199,7 +203,12 @@ struct PipeLayout {
   static constexpr int kAOps = SHARED_A ? 1 : NOPS;
   static constexpr int kBRows = BN / CG;
   static constexpr int kBBytes = kBRows * kBK * 2;
-  static constexpr int kStageBytes = kAOps * kABytes + NOPS * kBBytes;
+  // MX: the second GEMM's B lives in a ring of kDSlots decoded slots of its
+  // own, one deeper than the stage ring (the decode handshake needs the slack).
+  static constexpr int kDSlots = MX ? STAGES + 1 : 0;
+  static constexpr int kDMod = MX ? kDSlots : 1;  // index arithmetic MX = false never uses
+  static constexpr int kStageBytes = kAOps * kABytes + (MX ? NOPS - 1 : NOPS) * kBBytes;
+  static constexpr int kRingBytes = STAGES * kStageBytes + kDSlots * kBBytes;
   static constexpr int kTileCols = SHARED_A ? NOPS * BN : BN;  // vocabulary columns per tile
   static constexpr int kAccCols = NOPS * BN;
   static constexpr int kTmemCols = NACC * kAccCols;
@@ -210,12 +219,12 @@ struct PipeLayout {
   // kQStages staging buffers (a "staged" barrier each) holding its 32 B rows'
   // codes (32 bytes each) and scale codes (2 bytes each) of one k-block.
   static constexpr int kCvtWarps = 8;
-  static constexpr int kQStages = 3;
-  static constexpr int kMxBarrierBytes = MX ? 8 * (STAGES + kCvtWarps * kQStages) : 0;
+  static constexpr int kQStages = 2;
+  static constexpr int kMxBarrierBytes = MX ? 8 * (3 * kDSlots + kCvtWarps * kQStages) : 0;
   static constexpr int kQCodeBytes = 32 * 32;
   static constexpr int kQBytes = MX ? 32 * 34 : 0;  // one warp's slot
   static constexpr int kQOffset =
-      (STAGES * kStageBytes + kBarrierBytes + kMxBarrierBytes + 127) / 128 * 128;
+      (kRingBytes + kBarrierBytes + kMxBarrierBytes + 127) / 128 * 128;
   // + 1024 so the stage ring can be aligned to a swizzle atom.
   static constexpr int kSmemBytes = kQOffset + kCvtWarps * kQStages * kQBytes + 1024;
   static_assert(!MX || (NOPS == 2 && !SHARED_A && kBRows == 128),
@@ -286,15 +295,20 @@ __global__ void __launch_bounds__(pipe_threads(EPIW, MX), 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * L::kStageBytes);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::kRingBytes);
   uint64_t *empty = full + STAGES;
   uint64_t *tfull = empty + STAGES;
   uint64_t *tempty = tfull + 2;
   uint64_t *drain = tempty + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-  uint64_t *cvt = reinterpret_cast<uint64_t *>(smem + STAGES * L::kStageBytes + L::kBarrierBytes);
-  uint64_t *qfull = cvt + STAGES;  // [8 warps][kQStages]
+  // MX barriers per decoded slot: "converted" (leader; one relay arrival per
+  // CTA), "released" (the MMAs' commit), and this CTA's four decode warps done
+  uint64_t *dfull = reinterpret_cast<uint64_t *>(smem + L::kRingBytes + L::kBarrierBytes);
+  uint64_t *dempty = dfull + L::kDSlots;
+  uint64_t *ldec = dempty + L::kDSlots;
+  uint64_t *qfull = ldec + L::kDSlots;  // [8 warps][kQStages]
+  uint8_t *dring = smem + STAGES * L::kStageBytes;  // decoded B slots
   uint8_t *qbuf = smem + L::kQOffset;
 
   const int warp = threadIdx.x >> 5;
@@ -315,7 +329,11 @@ __global__ void __launch_bounds__(pipe_threads(EPIW, MX), 1)
     }
     mbar_init(drain, 1);
     if (MX) {
-      for (int st = 0; st < STAGES; ++st) mbar_init(&cvt[st], 4 * CG);  // 4 converter warps per CTA
+      for (int d = 0; d < L::kDSlots; ++d) {
+        mbar_init(&dfull[d], CG);   // one relay arrival per CTA
+        mbar_init(&dempty[d], 1);   // the MMAs' commit
+        mbar_init(&ldec[d], 4);     // the four decode warps of the k-block's group
+      }
       for (int q = 0; q < L::kCvtWarps * L::kQStages; ++q) mbar_init(&qfull[q], 1);
     }
     *abort_flag = 0;
@@ -362,9 +380,7 @@ __global__ void __launch_bounds__(pipe_threads(EPIW, MX), 1)
           if (lane == 0) {
             uint8_t *sa = smem + stage * L::kStageBytes;
             uint8_t *sb = sa + L::kAOps * L::kABytes;
-            if (leader)
-              mbar_arrive_expect_tx(&full[stage],
-                                    CG * (MX ? L::kStageBytes - L::kBBytes : L::kStageBytes));
+            if (leader) mbar_arrive_expect_tx(&full[stage], CG * L::kStageBytes);
 
             // second GEMM: its own A and B maps, or (SHARED_A) the next BN rows of B
             const CUtensorMap *tb1 = SHARED_A ? &tmB0 : &tmB1;
@@ -417,6 +433,7 @@ __global__ void __launch_bounds__(pipe_threads(EPIW, MX), 1)
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
+      uint32_t g = 0;  // k-blocks issued (MX: decoded slot g % kDSlots)
       bool ok = true;
       for (int it = unit; ok && it < sch.items; it += num_units) {
         int mt, sp, vt0, vt1;
@@ -428,9 +445,11 @@ __global__ void __launch_bounds__(pipe_threads(EPIW, MX), 1)
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * L::kAccCols);
           for (int kb = 0; kb < sch.k_blocks; ++kb) {
+            const int dslot = static_cast<int>(g % L::kDMod);
             if (lane == 0) {
               ok = mbar_wait(&full[stage], phase, abort_flag);
-              if (MX && ok) ok = mbar_wait_cluster(&cvt[stage], phase, abort_flag);
+              if (MX && ok)
+                ok = mbar_wait_cluster(&dfull[dslot], (g / L::kDMod) & 1u, abort_flag);
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
@@ -444,8 +463,10 @@ __global__ void __launch_bounds__(pipe_threads(EPIW, MX), 1)
                 for (int op = 0; op < NOPS; ++op) {
                   const uint64_t ad = sdesc_sw128(
                       a0 + (SHARED_A ? 0 : op) * L::kABytes + kk * kUmmaK * 2, 16, 1024);
-                  const uint64_t bd =
-                      sdesc_sw128(b0 + op * L::kBBytes + kk * kUmmaK * 2, 16, 1024);
+                  const uint32_t bop = (MX && op == 1)
+                                           ? smem_u32(dring + dslot * L::kBBytes)
+                                           : b0 + op * L::kBBytes;
+                  const uint64_t bd = sdesc_sw128(bop + kk * kUmmaK * 2, 16, 1024);
                   if (kPair)
                     mma_f16_pair(d_tmem + op * BN, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
                   else
@@ -457,8 +478,15 @@ __global__ void __launch_bounds__(pipe_threads(EPIW, MX), 1)
                 mma_commit_pair(&empty[stage], 0x3);
               else
                 mma_commit(&empty[stage]);
+              if (MX) {  // and the decoded slot
+                if (kPair)
+                  mma_commit_pair(&dempty[dslot], 0x3);
+                else
+                  mma_commit(&dempty[dslot]);
+              }
             }
             __syncwarp();
+            ++g;
             if (++stage == STAGES) {
               stage = 0;
               phase ^= 1u;
@@ -487,6 +515,39 @@ __global__ void __launch_bounds__(pipe_threads(EPIW, MX), 1)
         mbar_wait(drain, 0, &never);
       }
     }
+  } else if (MX && warp >= 2 + EPIW + L::kCvtWarps) {
+    // ------------------------------------------------------------ MX relays
+    // Relay warp r forwards group r's "this CTA decoded the stage" (a local
+    // barrier the group's four warps arrive on) to the leader's "converted"
+    // barrier.  That remote arrive needs a cluster-scope release, which costs
+    // about a microsecond; doing it here keeps it off the decode warps.
+    if constexpr (MX) {
+      const int group = warp - 2 - EPIW - L::kCvtWarps;
+      const uint32_t dfull_dst = kPair ? mapa_shared(smem_u32(dfull), 0) : smem_u32(dfull);
+      KSeq cur;
+      cur.first(sch, unit);
+      if (group == 1) cur.next(sch, num_units);
+      bool ok = true;
+      uint32_t g = static_cast<uint32_t>(group);
+      while (cur.valid) {
+        const int d = static_cast<int>(g % L::kDMod);
+        if (lane == 0) {
+          ok = mbar_wait(&ldec[d], (g / L::kDMod) & 1u, abort_flag);
+          if (ok) {
+            if (kPair)
+              mbar_arrive_cluster(dfull_dst + d * 8);
+            else
+              mbar_arrive(&dfull[d]);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        g += 2;
+        cur.next(sch, num_units);
+        cur.next(sch, num_units);
+      }
+      if (!ok && lane == 0) record_timeout<CG>(status, abort_flag);
+    }
   } else if (MX && warp >= 2 + EPIW) {
     // ------------------------------------------------------------ MX converters
     // Two groups of four warps take alternate k-blocks (group 0 the even
@@ -500,7 +561,6 @@ __global__ void __launch_bounds__(pipe_threads(EPIW, MX), 1)
       const int group = cw >> 2;
       const int crow = (cw & 3) * 32 + lane;
       const MxOperand &mx = ep.mx;
-      const uint32_t cvt_dst = kPair ? mapa_shared(smem_u32(cvt), 0) : smem_u32(cvt);
       uint64_t *wfull = qfull + cw * QS;
       uint8_t *wbuf = qbuf + cw * QS * L::kQBytes;
       KSeq ahead, cur;
@@ -530,11 +590,10 @@ __global__ void __launch_bounds__(pipe_threads(EPIW, MX), 1)
       bool ok = true;
       uint32_t g = static_cast<uint32_t>(group);  // index of `cur` in the CTA's k-block sequence
       while (ok && cur.valid) {
-        const int stage = static_cast<int>(g % STAGES);
-        const uint32_t phase = (g / STAGES) & 1u;
+        const int d = static_cast<int>(g % L::kDMod);
         const int q = static_cast<int>(consumed % QS);
-        // the MMAs are done with this stage's B slot, and the codes have landed
-        if (lane == 0) ok = mbar_wait(&empty[stage], phase ^ 1u, abort_flag);
+        // the MMAs are done with the decoded slot, and the codes have landed
+        if (lane == 0) ok = mbar_wait(&dempty[d], ((g / L::kDMod) & 1u) ^ 1u, abort_flag);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (ok) ok = mbar_wait(&wfull[q], (consumed / QS) & 1u, abort_flag);
         if (!__all_sync(0xffffffffu, ok)) {
@@ -542,7 +601,7 @@ __global__ void __launch_bounds__(pipe_threads(EPIW, MX), 1)
           break;
         }
         const uint8_t *src = wbuf + q * L::kQBytes;
-        uint8_t *b1 = smem + stage * L::kStageBytes + L::kAOps * L::kABytes + L::kBBytes;
+        uint8_t *b1 = dring + d * L::kBBytes;
         mx_decode_row(src + lane * 32, src + L::kQCodeBytes + lane * 2, b1 + crow * 128, crow);
         // the MMAs read the rows, and the next bulk copy rewrites the slot,
         // through the async proxy
@@ -550,10 +609,7 @@ __global__ void __launch_bounds__(pipe_threads(EPIW, MX), 1)
         __syncwarp();
         ++consumed;
         if (lane == 0) {
-          if (kPair)
-            mbar_arrive_cluster(cvt_dst + stage * 8);
-          else
-            mbar_arrive(&cvt[stage]);
+          mbar_arrive(&ldec[d]);  // CTA-scope release; the relay warp forwards it
           if (ahead.valid) stage_next();
         }
         g += 2;
