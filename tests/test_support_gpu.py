@@ -258,3 +258,32 @@ def test_support_repeated_calls_are_bitwise_identical():
     a = flp.logprob_entropy(d["h"], d["W"], d["targets"], None, 0.7, support=d["support"])
     b = flp.logprob_entropy(d["h"], d["W"], d["targets"], None, 0.7, support=d["support"])
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_support_backward_full_backward_workload():
+    """The backward workload (16,384 rows, 60 % scored, H 4096, V 151,936,
+    tau 0.7) restricted to 1/32-dense supports: dh on sampled scored rows
+    against the oracle, unscored rows zero, and the columns of dW summing to
+    zero (each row of G sums to zero over its support)."""
+    d = workloads.make(4, device="cuda")
+    w = d["workload"]
+    tg = d["targets"].cpu().numpy()
+    sup = workloads.support_words(w.T, w.V, 5, 4, targets=tg)
+    dh, dW = flp.backward(d["h"], d["W"], d["targets"], d["row_idx"], d["tau"], d["g1"], d["g2"],
+                          support=torch.from_numpy(sup).cuda())
+    torch.cuda.synchronize()
+    n = d["n"]
+    rows = d["row_idx"].cpu().numpy()
+    sel = workloads.sample_rows(n, 64, seed=84)
+    want, _ = ref.backward(d["h"].cpu(), d["W"].cpu(), tg, rows, d["tau"], d["g1"].cpu().numpy(),
+                           d["g2"].cpu().numpy(), "bf16", dh_rows_sel=sel,
+                           vsel=np.zeros(0, np.int64), stats=(np.zeros(n), np.zeros(n)),
+                           support=sup)
+    _rel(dh[torch.from_numpy(rows[sel]).cuda()], want, "dh (sampled rows)")
+    scored = torch.zeros(w.T, dtype=torch.bool, device="cuda")
+    scored[d["row_idx"]] = True
+    assert torch.count_nonzero(dh[~scored]) == 0
+    colsum = dW.double().sum(0)
+    scale = dW.double().abs().sum(0)
+    assert torch.all(colsum.abs() <= 2e-3 * scale), (colsum.abs() / scale).max()
+    assert torch.isfinite(dW).all()
