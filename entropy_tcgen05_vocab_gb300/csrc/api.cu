@@ -414,111 +414,6 @@ flp_status logprob_impl(const flp_shape *s, const void *h, const void *W, const 
   return FLP_OK;
 }
 
-}  // namespace
-}  // namespace flp
-
-using namespace flp;
-
-extern "C" {
-
-size_t flp_workspace_size(const flp_shape *shape, flp_op op) {
-  const char *why = nullptr;
-  if (!shape_ok(shape, &why)) return 0;
-  if (op != FLP_OP_LOGPROB_ENTROPY && op != FLP_OP_KL && op != FLP_OP_BACKWARD) return 0;
-  return layout_for(shape, op).total;
-}
-
-const char *flp_status_string(flp_status s) {
-  switch (s) {
-    case FLP_OK: return "ok";
-    case FLP_ERR_INVALID_ARG: return "invalid argument";
-    case FLP_ERR_UNSUPPORTED: return "unsupported device or size";
-    case FLP_ERR_WORKSPACE: return "workspace missing or too small";
-    case FLP_ERR_CUDA: return "CUDA error";
-    case FLP_ERR_DEVICE_STATUS: return "the device recorded a problem";
-  }
-  return "unknown status";
-}
-
-const char *flp_last_error(void) { return g_err; }
-
-flp_status flp_set_kernel_events(void *before, void *after) {
-  g_ev_before = static_cast<cudaEvent_t>(before);
-  g_ev_after = static_cast<cudaEvent_t>(after);
-  return FLP_OK;
-}
-
-flp_status flp_plan_scoring(const flp_shape *shape, flp_op op, int32_t num_sms, flp_plan *out) {
-  const char *why = nullptr;
-  if (!shape_ok(shape, &why)) return fail(FLP_ERR_INVALID_ARG, "%s", why);
-  if (!out || num_sms <= 0) return fail(FLP_ERR_INVALID_ARG, "out is NULL or num_sms <= 0");
-  if (op != FLP_OP_LOGPROB_ENTROPY && op != FLP_OP_KL && op != FLP_OP_BACKWARD)
-    return fail(FLP_ERR_INVALID_ARG, "unknown op");
-  std::memset(out, 0, sizeof *out);
-  if (shape->n_rows == 0) return FLP_OK;
-  const int bn = op == FLP_OP_KL ? kKlBN : kFwdTileCols;
-  const int cg = op == FLP_OP_KL ? kKlCG : kFwdCG;
-  const int units = std::max(1, num_sms / cg);
-  const Plan p = plan_cached(shape->n_rows, shape->V, shape->H, bn, units, 128 * cg,
-                             op == FLP_OP_KL ? 2 : 1);
-  out->row_tiles = p.sch.row_tiles;
-  out->vocab_tiles = p.sch.vocab_tiles;
-  out->block_m = 128 * cg;
-  out->block_n = bn;
-  out->cta_group = cg;
-  out->splits = p.sch.splits;
-  out->tiles_per_split = p.sch.tiles_per_split;
-  out->band = p.sch.band;
-  out->items = p.sch.items;
-  out->grid = p.grid * cg;
-  out->max_tiles_per_cta = p.max_load;
-  if (op == FLP_OP_BACKWARD) out->chunk_rows = grad_chunk_rows(shape);
-  return FLP_OK;
-}
-
-int64_t flp_row_chunks(int64_t n_rows, int64_t chunk_rows, int64_t *out_lengths, int64_t max_out) {
-  if (n_rows <= 0 || chunk_rows <= 0) return 0;
-  const int64_t num = (n_rows - 1) / chunk_rows + 1;
-  const int64_t each = cdiv(n_rows, num);
-  int64_t k = 0;
-  for (int64_t start = 0; start < n_rows; start += each, ++k)
-    if (out_lengths && k < max_out) out_lengths[k] = std::min(each, n_rows - start);
-  return k;
-}
-
-flp_status flp_logprob_entropy(const flp_shape *s, const void *h, const void *W,
-                               const int64_t *targets, const int64_t *row_idx, float temperature,
-                               float *out_logp, float *out_ent, float *out_lse, float *out_ez,
-                               void *ws, size_t ws_bytes, flp_stream_t stream) {
-  return logprob_impl(s, h, W, targets, 1, row_idx, nullptr, 0, temperature, out_logp, out_ent,
-                      out_lse, out_ez, ws, ws_bytes, stream);
-}
-
-flp_status flp_logprob_entropy_support(const flp_shape *s, const void *h, const void *W,
-                                       const int64_t *targets, const int64_t *row_idx,
-                                       const uint32_t *support, int64_t ld_support,
-                                       float temperature, float *out_logp, float *out_ent,
-                                       float *out_lse, float *out_ez, void *ws, size_t ws_bytes,
-                                       flp_stream_t stream) {
-  g_err[0] = 0;
-  if (!support) return fail(FLP_ERR_INVALID_ARG, "support is required");
-  return logprob_impl(s, h, W, targets, 1, row_idx, support, ld_support, temperature, out_logp,
-                      out_ent, out_lse, out_ez, ws, ws_bytes, stream);
-}
-
-flp_status flp_logprob_entropy_k(const flp_shape *s, const void *h, const void *W,
-                                 const int64_t *targets, int32_t K, const int64_t *row_idx,
-                                 float temperature, float *out_logp, float *out_ent,
-                                 float *out_lse, float *out_ez, void *ws, size_t ws_bytes,
-                                 flp_stream_t stream) {
-  return logprob_impl(s, h, W, targets, K, row_idx, nullptr, 0, temperature, out_logp, out_ent,
-                      out_lse, out_ez, ws, ws_bytes, stream);
-}
-
-}  // extern "C"
-
-namespace flp {
-namespace {
 // KL(teacher || student); the teacher head is W_t, or (mx.packed != null)
 // the blocked MXFP4 operand mx.
 flp_status kl_impl(const flp_shape *s, const void *h_s, const void *W_s, const void *h_t,
@@ -584,74 +479,7 @@ flp_status kl_impl(const flp_shape *s, const void *h_s, const void *W_s, const v
   if ((e = ev.stop(cs)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
   return FLP_OK;
 }
-}  // namespace
-}  // namespace flp
 
-extern "C" {
-
-flp_status flp_kl(const flp_shape *s, const void *h_s, const void *W_s, const void *h_t,
-                  const void *W_t, const int64_t *row_idx, float *out_kl, void *ws,
-                  size_t ws_bytes, flp_stream_t stream) {
-  g_err[0] = 0;
-  if (!W_t && s && s->n_rows > 0) return fail(FLP_ERR_INVALID_ARG, "W_t is required");
-  return kl_impl(s, h_s, W_s, h_t, W_t, MxOperand{nullptr, nullptr, 0}, row_idx, out_kl, ws,
-                 ws_bytes, stream);
-}
-
-int64_t flp_mxfp4_rows(int64_t V) { return V <= 0 ? 0 : cdiv(V, 256) * 256; }
-
-size_t flp_mxfp4_bytes(int64_t V, int64_t H, size_t *packed_bytes, size_t *scale_bytes) {
-  if (V <= 0 || H <= 0 || H % 64 != 0) return 0;
-  const size_t rows = static_cast<size_t>(flp_mxfp4_rows(V));
-  const size_t blocks = static_cast<size_t>(H / 64);
-  if (packed_bytes) *packed_bytes = blocks * rows * 32;
-  if (scale_bytes) *scale_bytes = blocks * rows * 2;
-  return blocks * rows * 34;
-}
-
-flp_status flp_mxfp4_quantize(const void *W, flp_dtype dtype, int64_t V, int64_t H,
-                              int64_t ld_w, uint8_t *packed, uint8_t *scales,
-                              flp_stream_t stream) {
-  g_err[0] = 0;
-  if (V <= 0 || H <= 0 || H % 64 != 0)
-    return fail(FLP_ERR_INVALID_ARG, "V must be > 0 and H a positive multiple of 64");
-  if (dtype != FLP_BF16 && dtype != FLP_FP16) return fail(FLP_ERR_INVALID_ARG, "bad dtype");
-  if (ld_w < H) return fail(FLP_ERR_INVALID_ARG, "ld_w < H");
-  if (!W || !packed || !scales) return fail(FLP_ERR_INVALID_ARG, "W, packed and scales are required");
-  if (reinterpret_cast<uintptr_t>(W) % 2 != 0 || !aligned16(packed))
-    return fail(FLP_ERR_INVALID_ARG, "W must be 2-byte and packed 16-byte aligned");
-  DeviceInfo dev;
-  const flp_status st = device_info(&dev);
-  if (st != FLP_OK) return st;
-  const cudaError_t e =
-      launch_mxfp4_quantize(W, dtype == FLP_BF16, V, H, ld_w, flp_mxfp4_rows(V), packed, scales,
-                            dev.sms, reinterpret_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
-  return FLP_OK;
-}
-
-flp_status flp_kl_mxfp4(const flp_shape *s, const void *h_s, const void *W_s, const void *h_t,
-                        const uint8_t *Wt_packed, const uint8_t *Wt_scales,
-                        const int64_t *row_idx, float *out_kl, void *ws, size_t ws_bytes,
-                        flp_stream_t stream) {
-  g_err[0] = 0;
-  const char *why = nullptr;
-  if (!shape_ok(s, &why)) return fail(FLP_ERR_INVALID_ARG, "%s", why);
-  if (s->dtype != FLP_BF16)
-    return fail(FLP_ERR_UNSUPPORTED, "the MXFP4 teacher head needs bf16 student and teacher rows");
-  if (s->H % 64 != 0) return fail(FLP_ERR_INVALID_ARG, "H must be a multiple of 64");
-  if (s->n_rows > 0 && (!Wt_packed || !Wt_scales))
-    return fail(FLP_ERR_INVALID_ARG, "Wt_packed and Wt_scales are required");
-  if ((Wt_packed && !aligned16(Wt_packed)) || (Wt_scales && !aligned16(Wt_scales)))
-    return fail(FLP_ERR_INVALID_ARG, "Wt_packed and Wt_scales must be 16-byte aligned");
-  const MxOperand mx{Wt_packed, Wt_scales, static_cast<long long>(flp_mxfp4_rows(s->V))};
-  return kl_impl(s, h_s, W_s, h_t, nullptr, mx, row_idx, out_kl, ws, ws_bytes, stream);
-}
-
-}  // extern "C"
-
-namespace flp {
-namespace {
 flp_status backward_impl(const flp_shape *s, const void *h, const void *W, const int64_t *targets,
                          const int64_t *row_idx, const uint32_t *support, int64_t ld_support,
                          float temperature, const float *g1, const float *g2, const float *lse,
@@ -801,10 +629,168 @@ flp_status backward_impl(const flp_shape *s, const void *h, const void *W, const
   if ((e = ev.stop(cs)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
   return FLP_OK;
 }
+
 }  // namespace
 }  // namespace flp
 
+using namespace flp;
+
 extern "C" {
+
+size_t flp_workspace_size(const flp_shape *shape, flp_op op) {
+  const char *why = nullptr;
+  if (!shape_ok(shape, &why)) return 0;
+  if (op != FLP_OP_LOGPROB_ENTROPY && op != FLP_OP_KL && op != FLP_OP_BACKWARD) return 0;
+  return layout_for(shape, op).total;
+}
+
+const char *flp_status_string(flp_status s) {
+  switch (s) {
+    case FLP_OK: return "ok";
+    case FLP_ERR_INVALID_ARG: return "invalid argument";
+    case FLP_ERR_UNSUPPORTED: return "unsupported device or size";
+    case FLP_ERR_WORKSPACE: return "workspace missing or too small";
+    case FLP_ERR_CUDA: return "CUDA error";
+    case FLP_ERR_DEVICE_STATUS: return "the device recorded a problem";
+  }
+  return "unknown status";
+}
+
+const char *flp_last_error(void) { return g_err; }
+
+flp_status flp_set_kernel_events(void *before, void *after) {
+  g_ev_before = static_cast<cudaEvent_t>(before);
+  g_ev_after = static_cast<cudaEvent_t>(after);
+  return FLP_OK;
+}
+
+flp_status flp_plan_scoring(const flp_shape *shape, flp_op op, int32_t num_sms, flp_plan *out) {
+  const char *why = nullptr;
+  if (!shape_ok(shape, &why)) return fail(FLP_ERR_INVALID_ARG, "%s", why);
+  if (!out || num_sms <= 0) return fail(FLP_ERR_INVALID_ARG, "out is NULL or num_sms <= 0");
+  if (op != FLP_OP_LOGPROB_ENTROPY && op != FLP_OP_KL && op != FLP_OP_BACKWARD)
+    return fail(FLP_ERR_INVALID_ARG, "unknown op");
+  std::memset(out, 0, sizeof *out);
+  if (shape->n_rows == 0) return FLP_OK;
+  const int bn = op == FLP_OP_KL ? kKlBN : kFwdTileCols;
+  const int cg = op == FLP_OP_KL ? kKlCG : kFwdCG;
+  const int units = std::max(1, num_sms / cg);
+  const Plan p = plan_cached(shape->n_rows, shape->V, shape->H, bn, units, 128 * cg,
+                             op == FLP_OP_KL ? 2 : 1);
+  out->row_tiles = p.sch.row_tiles;
+  out->vocab_tiles = p.sch.vocab_tiles;
+  out->block_m = 128 * cg;
+  out->block_n = bn;
+  out->cta_group = cg;
+  out->splits = p.sch.splits;
+  out->tiles_per_split = p.sch.tiles_per_split;
+  out->band = p.sch.band;
+  out->items = p.sch.items;
+  out->grid = p.grid * cg;
+  out->max_tiles_per_cta = p.max_load;
+  if (op == FLP_OP_BACKWARD) out->chunk_rows = grad_chunk_rows(shape);
+  return FLP_OK;
+}
+
+int64_t flp_row_chunks(int64_t n_rows, int64_t chunk_rows, int64_t *out_lengths, int64_t max_out) {
+  if (n_rows <= 0 || chunk_rows <= 0) return 0;
+  const int64_t num = (n_rows - 1) / chunk_rows + 1;
+  const int64_t each = cdiv(n_rows, num);
+  int64_t k = 0;
+  for (int64_t start = 0; start < n_rows; start += each, ++k)
+    if (out_lengths && k < max_out) out_lengths[k] = std::min(each, n_rows - start);
+  return k;
+}
+
+flp_status flp_logprob_entropy(const flp_shape *s, const void *h, const void *W,
+                               const int64_t *targets, const int64_t *row_idx, float temperature,
+                               float *out_logp, float *out_ent, float *out_lse, float *out_ez,
+                               void *ws, size_t ws_bytes, flp_stream_t stream) {
+  return logprob_impl(s, h, W, targets, 1, row_idx, nullptr, 0, temperature, out_logp, out_ent,
+                      out_lse, out_ez, ws, ws_bytes, stream);
+}
+
+flp_status flp_logprob_entropy_support(const flp_shape *s, const void *h, const void *W,
+                                       const int64_t *targets, const int64_t *row_idx,
+                                       const uint32_t *support, int64_t ld_support,
+                                       float temperature, float *out_logp, float *out_ent,
+                                       float *out_lse, float *out_ez, void *ws, size_t ws_bytes,
+                                       flp_stream_t stream) {
+  g_err[0] = 0;
+  if (!support) return fail(FLP_ERR_INVALID_ARG, "support is required");
+  return logprob_impl(s, h, W, targets, 1, row_idx, support, ld_support, temperature, out_logp,
+                      out_ent, out_lse, out_ez, ws, ws_bytes, stream);
+}
+
+flp_status flp_logprob_entropy_k(const flp_shape *s, const void *h, const void *W,
+                                 const int64_t *targets, int32_t K, const int64_t *row_idx,
+                                 float temperature, float *out_logp, float *out_ent,
+                                 float *out_lse, float *out_ez, void *ws, size_t ws_bytes,
+                                 flp_stream_t stream) {
+  return logprob_impl(s, h, W, targets, K, row_idx, nullptr, 0, temperature, out_logp, out_ent,
+                      out_lse, out_ez, ws, ws_bytes, stream);
+}
+
+
+flp_status flp_kl(const flp_shape *s, const void *h_s, const void *W_s, const void *h_t,
+                  const void *W_t, const int64_t *row_idx, float *out_kl, void *ws,
+                  size_t ws_bytes, flp_stream_t stream) {
+  g_err[0] = 0;
+  if (!W_t && s && s->n_rows > 0) return fail(FLP_ERR_INVALID_ARG, "W_t is required");
+  return kl_impl(s, h_s, W_s, h_t, W_t, MxOperand{nullptr, nullptr, 0}, row_idx, out_kl, ws,
+                 ws_bytes, stream);
+}
+
+int64_t flp_mxfp4_rows(int64_t V) { return V <= 0 ? 0 : cdiv(V, 256) * 256; }
+
+size_t flp_mxfp4_bytes(int64_t V, int64_t H, size_t *packed_bytes, size_t *scale_bytes) {
+  if (V <= 0 || H <= 0 || H % 64 != 0) return 0;
+  const size_t rows = static_cast<size_t>(flp_mxfp4_rows(V));
+  const size_t blocks = static_cast<size_t>(H / 64);
+  if (packed_bytes) *packed_bytes = blocks * rows * 32;
+  if (scale_bytes) *scale_bytes = blocks * rows * 2;
+  return blocks * rows * 34;
+}
+
+flp_status flp_mxfp4_quantize(const void *W, flp_dtype dtype, int64_t V, int64_t H,
+                              int64_t ld_w, uint8_t *packed, uint8_t *scales,
+                              flp_stream_t stream) {
+  g_err[0] = 0;
+  if (V <= 0 || H <= 0 || H % 64 != 0)
+    return fail(FLP_ERR_INVALID_ARG, "V must be > 0 and H a positive multiple of 64");
+  if (dtype != FLP_BF16 && dtype != FLP_FP16) return fail(FLP_ERR_INVALID_ARG, "bad dtype");
+  if (ld_w < H) return fail(FLP_ERR_INVALID_ARG, "ld_w < H");
+  if (!W || !packed || !scales) return fail(FLP_ERR_INVALID_ARG, "W, packed and scales are required");
+  if (reinterpret_cast<uintptr_t>(W) % 2 != 0 || !aligned16(packed))
+    return fail(FLP_ERR_INVALID_ARG, "W must be 2-byte and packed 16-byte aligned");
+  DeviceInfo dev;
+  const flp_status st = device_info(&dev);
+  if (st != FLP_OK) return st;
+  const cudaError_t e =
+      launch_mxfp4_quantize(W, dtype == FLP_BF16, V, H, ld_w, flp_mxfp4_rows(V), packed, scales,
+                            dev.sms, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+  return FLP_OK;
+}
+
+flp_status flp_kl_mxfp4(const flp_shape *s, const void *h_s, const void *W_s, const void *h_t,
+                        const uint8_t *Wt_packed, const uint8_t *Wt_scales,
+                        const int64_t *row_idx, float *out_kl, void *ws, size_t ws_bytes,
+                        flp_stream_t stream) {
+  g_err[0] = 0;
+  const char *why = nullptr;
+  if (!shape_ok(s, &why)) return fail(FLP_ERR_INVALID_ARG, "%s", why);
+  if (s->dtype != FLP_BF16)
+    return fail(FLP_ERR_UNSUPPORTED, "the MXFP4 teacher head needs bf16 student and teacher rows");
+  if (s->H % 64 != 0) return fail(FLP_ERR_INVALID_ARG, "H must be a multiple of 64");
+  if (s->n_rows > 0 && (!Wt_packed || !Wt_scales))
+    return fail(FLP_ERR_INVALID_ARG, "Wt_packed and Wt_scales are required");
+  if ((Wt_packed && !aligned16(Wt_packed)) || (Wt_scales && !aligned16(Wt_scales)))
+    return fail(FLP_ERR_INVALID_ARG, "Wt_packed and Wt_scales must be 16-byte aligned");
+  const MxOperand mx{Wt_packed, Wt_scales, static_cast<long long>(flp_mxfp4_rows(s->V))};
+  return kl_impl(s, h_s, W_s, h_t, nullptr, mx, row_idx, out_kl, ws, ws_bytes, stream);
+}
+
 
 flp_status flp_backward(const flp_shape *s, const void *h, const void *W, const int64_t *targets,
                         const int64_t *row_idx, float temperature, const float *g1,
