@@ -1,4 +1,4 @@
-// launch.h -- internal interface between the host API (api.cpp) and the
+// launch.h -- internal interface between the host API (api.cu) and the
 // kernel translation units.  Not installed; the public interface is
 // include/fusedlogp.h.
 #pragma once

@@ -7,25 +7,30 @@
 // of a [tile, vocab] buffer: no logit ever reaches global memory.
 //
 // Work decomposition.  Rows are cut into row tiles of 128 x CG rows, the
-// vocabulary into BN-column tiles.  A work item is (row tile, vocabulary
-// split): one CTA (CG = 1) or one CTA pair (CG = 2) sweeps the split's
-// vocabulary tiles for its row tile, keeping per-row running state in
-// registers, and emits one partial state per row and item.  Items are ordered
-// band by band (a band = `band` consecutive row tiles, all splits of the
-// band, row tiles fastest) so the CTAs resident at one time share the same
-// weight tiles and each W tile is read from HBM about once per band while
-// the band's hidden rows stay in L2.  Persistent CTAs (pairs) take items
-// round robin.
+// vocabulary into tiles of BN columns (NOPS x BN with SHARED_A).  A work
+// item is (row tile, vocabulary split): one CTA (CG = 1) or one CTA pair
+// (CG = 2) sweeps the split's vocabulary tiles for its row tile, keeping
+// per-row running state in registers, and emits one partial state per row
+// and item.  Items are ordered band by band (a band = `band` consecutive row
+// tiles, all splits of the band, row tiles fastest) so the CTAs resident at
+// one time share the same weight tiles and each W tile is read from HBM
+// about once per band while the band's hidden rows stay in L2.  Persistent
+// CTAs (pairs) take items round robin.
 //
-// Roles (192 threads per CTA):
+// Roles (64 + 32 x EPIW threads per CTA, plus 320 with MX):
 //   warp 0     TMA producer: A (hidden rows, K-major) and B (W rows, K-major)
 //              per 64-wide K block into a STAGES-deep ring of 128B-swizzled
 //              shared-memory stages.
 //   warp 1     TMEM allocation + tcgen05.mma issue (one elected lane),
 //              M = 128 x CG, N = BN, K = 16 per instruction, FP32 accumulators
-//              in a double-buffered TMEM region.
-//   warps 2-5  epilogue: tcgen05.ld of their 32 TMEM lanes (= 32 rows),
-//              32 columns at a time, folded by the Epi policy.
+//              in NACC TMEM buffers (2: the epilogue of one tile overlaps the
+//              MMAs of the next; 1: the producer keeps filling stages while
+//              the epilogue drains the single buffer).
+//   warps 2..  EPIW epilogue warps: tcgen05.ld of their 32 TMEM lanes (= 32
+//              rows), 32 columns at a time, folded by the Epi policy; with
+//              EPIW = 8 two warps share each lane quarter and split its
+//              columns.
+//   MX only    eight converter warps and two relay warps (below).
 //
 // MX: the second GEMM's B operand (a teacher head) is stored in MXFP4 (E2M1
 // elements with an E8M0 scale per 32, in the blocked layout of MxOperand).
