@@ -89,7 +89,7 @@ int64_t grad_chunk_rows(const flp_shape *s) {
 struct Layout {
   size_t status = 0, cnt = 0, cnt_bytes = 0, zt = 0, pm = 0, ps = 0, pb = 0, pc = 0, pm2 = 0,
          ps2 = 0;
-  size_t hs = 0, hs2 = 0, lse = 0, ez = 0, g = 0, total = 0;
+  size_t hs = 0, hs2 = 0, lse = 0, ez = 0, g = 0, rowcnt = 0, total = 0;
   int64_t grad_rows = 0;
 };
 
@@ -127,6 +127,7 @@ Layout layout_for(const flp_shape *s, flp_op op) {
     L.ez = take(n * 4);
     L.grad_rows = grad_chunk_rows(s);
     L.g = take(static_cast<size_t>(L.grad_rows) * static_cast<size_t>(cdiv(s->V, 8) * 8) * 2);
+    L.rowcnt = take(static_cast<size_t>(s->T) * 4);  // scored rows per h row
   }
   L.total = off;
   return L;
@@ -520,11 +521,17 @@ flp_status backward_impl(const flp_shape *s, const void *h, const void *W, const
 
   const void *A = h;
   int64_t lda = s->ld_h;
+  uint32_t *rowcnt = nullptr;
   if (row_idx) {
     A = at<void>(ws, L.hs);
     lda = s->H;
     e = launch_gather(h, s->ld_h, row_idx, s->n_rows, s->T, s->H, at<void>(ws, L.hs), dev.sms, cs);
     if (e != cudaSuccess) return cuda_fail(e, "gather launch");
+    // rows named more than once have their dh contributions summed
+    rowcnt = at<uint32_t>(ws, L.rowcnt);
+    e = cudaMemsetAsync(rowcnt, 0, static_cast<size_t>(s->T) * 4, cs);
+    if (e == cudaSuccess) e = launch_count_rows(row_idx, s->n_rows, s->T, rowcnt, dev.sms, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "row count");
   }
   const float inv_tau = 1.0f / temperature;
   const float sl = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
@@ -608,6 +615,7 @@ flp_status backward_impl(const flp_shape *s, const void *h, const void *W, const
     da.r0 = static_cast<int>(r0);
     da.T = s->T;
     da.row_idx = row_idx;
+    da.rowcnt = rowcnt;
     da.dh = dh;
     da.ld_dh = s->ld_h;
     if ((e = launch_dh_gemm(da, cs)) != cudaSuccess) return cuda_fail(e, "dh launch");

@@ -61,6 +61,15 @@ __device__ __forceinline__ void store32_16(void *dst, const float (&v)[32], bool
     d[q] = u;
   }
 }
+// Scored rows per h row (row_idx may name a row more than once).
+__global__ void count_rows_kernel(const int64_t *__restrict__ row_idx, int64_t n, int64_t T,
+                                  uint32_t *__restrict__ cnt) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const int64_t r = row_idx[i];
+    if (r >= 0 && r < T) atomicAdd(cnt + r, 1u);
+  }
+}
 }  // namespace
 
 // ---------------------------------------------------------------- grad pass
@@ -157,6 +166,7 @@ struct DhEpi {
     int R, H, r0;
     int64_t T;
     const int64_t *row_idx;
+    const uint32_t *rowcnt;  // scored rows per h row, or null (row_idx null: all distinct)
     uint16_t *dh;
     int64_t ld;
     bool bf16;
@@ -171,6 +181,9 @@ struct DhEpi {
       orig = p.row_idx ? p.row_idx[p.r0 + row] : p.r0 + row;
       valid = orig >= 0 && orig < p.T;
     }
+    // A row scored more than once gets the sum of its contributions: added
+    // with packed 16-bit atomics onto the zeroed dh row (in any chunk order).
+    const bool repeated = valid && p.rowcnt && p.rowcnt[orig] > 1u;
     uint16_t *drow = p.dh + (valid ? orig : 0) * p.ld;
 #pragma unroll 1
     for (int c = 0; c < ncols / 32; ++c) {
@@ -179,7 +192,18 @@ struct DhEpi {
       float x[32];
       tmem_ld32(taddr + c * 32, x);
       if (!valid) continue;
-      if (col + 32 <= p.H) {
+      if (repeated) {
+        // H is a multiple of 8, so the valid columns of a chunk come in pairs
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          if (col + j >= p.H) break;
+          if (p.bf16)
+            atomicAdd(reinterpret_cast<__nv_bfloat162 *>(drow + col + j),
+                      __floats2bfloat162_rn(x[j], x[j + 1]));
+          else
+            atomicAdd(reinterpret_cast<__half2 *>(drow + col + j), __floats2half2_rn(x[j], x[j + 1]));
+        }
+      } else if (col + 32 <= p.H) {
         store32_16(drow + col, x, p.bf16);
       } else {
 #pragma unroll
@@ -324,6 +348,7 @@ cudaError_t launch_dh_gemm(const GemmArgs &a, cudaStream_t stream) {
   p.r0 = a.r0;
   p.T = a.T;
   p.row_idx = a.row_idx;
+  p.rowcnt = a.rowcnt;
   p.dh = static_cast<uint16_t *>(a.dh);
   p.ld = a.ld_dh;
   p.bf16 = a.bf16;
@@ -331,6 +356,16 @@ cudaError_t launch_dh_gemm(const GemmArgs &a, cudaStream_t stream) {
   return launch_persistent(DH_KERNEL, a.grid, pipe_threads(DhCfg::kEpiw), DhCfg::L::kSmemBytes,
                            kGemmCG, stream, a.tmA, a.tmB, gemm_shape(a.M, a.N, a.K, DhCfg::kTileN),
                            idesc, p, a.status);
+}
+
+cudaError_t launch_count_rows(const int64_t *row_idx, int64_t n, int64_t T, uint32_t *cnt,
+                              int num_sms, cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  int64_t blocks = (n + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 4;
+  if (blocks > cap) blocks = cap;
+  count_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(row_idx, n, T, cnt);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_dw_gemm(const GemmArgs &a, cudaStream_t stream) {

@@ -112,6 +112,7 @@ struct GemmArgs {
   int r0;
   int64_t T;
   const int64_t *row_idx;
+  const uint32_t *rowcnt;  // scored rows per h row (null when row_idx is null)
   void *dh;
   int64_t ld_dh;
   // dW epilogue
@@ -127,6 +128,9 @@ cudaError_t launch_kl(const KlArgs &a, cudaStream_t stream);
 cudaError_t launch_grad(const GradArgs &a, cudaStream_t stream);
 cudaError_t launch_dh_gemm(const GemmArgs &a, cudaStream_t stream);
 cudaError_t launch_dw_gemm(const GemmArgs &a, cudaStream_t stream);
+// cnt[r] += 1 for every row_idx entry r in [0, T) (cnt zeroed by the caller).
+cudaError_t launch_count_rows(const int64_t *row_idx, int64_t n, int64_t T, uint32_t *cnt,
+                              int num_sms, cudaStream_t stream);
 int dh_gemm_tiles(int M, int N);
 int dw_gemm_tiles(int M, int N);
 int gemm_cta_group();

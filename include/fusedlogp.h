@@ -100,7 +100,8 @@ typedef struct {
  * whether row_idx is given); it is about n_rows*H*2 bytes for the gathered
  * rows, plus O(n_rows * 64) bytes of per-row partial state, plus, for the
  * backward, one bounded chunk of the bf16/fp16 logit gradient (at most
- * 4 GiB; never a [T,V] buffer for the forward or KL).
+ * 4 GiB; never a [T,V] buffer for the forward or KL) and 4*T bytes of
+ * per-row counts.
  */
 size_t flp_workspace_size(const flp_shape *shape, flp_op op);
 
@@ -259,8 +260,11 @@ flp_status flp_kl_mxfp4(const flp_shape *shape, const void *h_s, const void *W_s
  *                the same inputs (out_lse, out_ez), or both NULL: the
  *                statistics are then recomputed (one extra forward pass)
  *   dh           [T, ld_h] dtype; dW [V, ld_w] float32
- * row_idx entries must be distinct (a row scored twice would need its dh
- * contributions summed; that is a precondition, not checked).
+ * row_idx may name a row more than once: that row's dh is the sum of its
+ * contributions, added onto the zeroed row with packed 16-bit atomics (so
+ * for a row named three or more times the low bits depend on the order of
+ * the additions; every other row is written once and is bitwise
+ * reproducible).
  * n_rows == 0 writes zeros to dh and dW.  The scored rows are processed in
  * chunks of at most flp's chunk size (as many rows as keep the chunk's
  * logit gradient within 4 GiB; the environment variable FLP_GRAD_CHUNK_ROWS,

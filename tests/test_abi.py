@@ -116,7 +116,7 @@ def test_workspace_formula(L):
                 if w.V >= 38016:
                     assert b < n * w.V * 4
             else:
-                assert b <= gathered + n * 128 * 4 * 4 + (4 << 30) + (1 << 20)
+                assert b <= gathered + n * 128 * 4 * 4 + (4 << 30) + 4 * w.T + (1 << 20)
     # monotone in the number of scored rows
     a = L.flp_workspace_size(ctypes.byref(_shape(T=4096, H=4096, V=151936, n=1000)), 0)
     b = L.flp_workspace_size(ctypes.byref(_shape(T=4096, H=4096, V=151936, n=2000)), 0)

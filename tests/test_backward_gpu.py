@@ -105,6 +105,35 @@ def test_backward_several_row_chunks(monkeypatch):
     _rel(dW, ref_dW, "dW")
 
 
+@pytest.mark.parametrize("dtype,chunk", [("bf16", None), ("fp16", None), ("bf16", "128")])
+def test_backward_repeated_rows_sum_their_contributions(monkeypatch, dtype, chunk):
+    """row_idx naming rows 2, 3 and 5 times, scattered through the list (and,
+    with 128-row chunks, across chunks): each such dh row is the sum of its
+    contributions, as the oracle's scatter-add gives; dW takes every
+    position."""
+    d = _case(700, 256, 3000, dtype=dtype, seed=45)
+    rows = d["row_idx"].cpu().numpy()
+    extra = np.concatenate([rows[:5], rows[10:13], rows[10:13], np.repeat(rows[20:21], 4)])
+    allrows = np.concatenate([rows, extra])[::-1].copy()
+    allrows = np.roll(allrows, len(allrows) // 3)
+    n = len(allrows)
+    d["row_idx"] = torch.from_numpy(allrows).cuda()
+    d["n"] = n
+    d["g1"] = workloads.normal((n,), 1.0, 46, 1, "f32", "cpu").cuda()
+    d["g2"] = workloads.normal((n,), 1.0, 46, 2, "f32", "cpu").cuda()
+    if chunk:
+        monkeypatch.setenv("FLP_GRAD_CHUNK_ROWS", chunk)
+        assert len(flp.row_chunks(n, int(chunk))) >= 3
+    dh, dW = flp.backward(d["h"], d["W"], d["targets"], d["row_idx"], d["tau"], d["g1"], d["g2"])
+    torch.cuda.synchronize()
+    ref_dh, ref_dW = _oracle(d, dtype)
+    _rel(dh, ref_dh, "dh")
+    _rel(dW, ref_dW, "dW")
+    # the repeated rows themselves, on their own
+    rep = np.unique(extra)
+    _rel(dh[torch.from_numpy(rep).cuda()], ref_dh[rep], "dh (repeated rows)")
+
+
 def test_backward_no_scored_rows_gives_zeros():
     d = _case(64, 128, 512)
     rows = torch.zeros(0, dtype=torch.int64, device="cuda")
