@@ -30,6 +30,7 @@ import hashlib
 import json
 import math
 import os
+import platform
 import subprocess
 import sys
 import tempfile
@@ -390,6 +391,37 @@ def cpu_oracle_rate(d, seconds, calib_rows=2):
     return k / dt, k, dt, coracle.num_threads()
 
 
+def numpy_oracle_rate(d, seconds):
+    """Rows per second of the NumPy float64 restatement (BLAS matmul) on a
+    row sample, inputs decoded to float64 beforehand: an optimistic CPU
+    figure beside the C oracle's."""
+    from oracle import ref
+    w = d["workload"]
+    rows_all = np.arange(w.T) if d["row_idx"] is None else d["row_idx"].cpu().numpy()
+    Wd = ref.decode(d["W"].cpu(), w.dtype)
+    k = 256
+    hd = ref.decode(d["h"][torch.from_numpy(rows_all[:k]).to(d["h"].device)].cpu(), w.dtype)
+    t = time.perf_counter()
+    ref.row_stats(hd[:32], Wd, None, d["tau"])
+    per_row = max((time.perf_counter() - t) / 32, 1e-6)
+    k = int(max(32, min(k, seconds / per_row)))
+    t = time.perf_counter()
+    ref.row_stats(hd[:k], Wd, None, d["tau"])
+    dt = time.perf_counter() - t
+    return k / dt, k, dt
+
+
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.startswith("Model name:"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.machine()
+
+
 # ---------------------------------------------------------------- arms
 def run_ours(args):
     import entropy_tcgen05_vocab_gb300 as flp
@@ -566,7 +598,16 @@ def run_ours(args):
         rate, k, dt, cores = cpu_oracle_rate(d, args.cpu_seconds)
         out["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
                                "sample": "%d of %d rows of the same workload (float64 C oracle, "
-                                         "%.1f s)" % (k, n, dt)}
+                                         "%.1f s)" % (k, n, dt),
+                               "host_cpus": len(os.sched_getaffinity(0)), "cpu_model": cpu_model()}
+        try:
+            nrate, nk, ndt = numpy_oracle_rate(d, args.cpu_seconds / 2)
+            out["cpu_baseline"]["numpy_blas"] = {
+                "value": nrate, "unit": UNIT,
+                "sample": "%d rows, per-row statistics by the NumPy float64 oracle (BLAS matmul) "
+                          "on inputs decoded beforehand, %.1f s" % (nk, ndt)}
+        except MemoryError as e:  # reported, not fatal
+            out["cpu_baseline"]["numpy_blas"] = {"unavailable": str(e)[:200]}
     if world > 1:
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()
@@ -613,7 +654,8 @@ def run_reference(args):
         "data": "synthetic (seeded; shapes and distributions of the pages' workloads)",
         "config": describe(d),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": "%d random rows of %d per step (float64 C oracle)" % (k, d["n"])},
+                         "sample": "%d random rows of %d per step (float64 C oracle)" % (k, d["n"]),
+                         "host_cpus": len(os.sched_getaffinity(0)), "cpu_model": cpu_model()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
