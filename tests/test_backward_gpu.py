@@ -5,10 +5,12 @@ Tolerance (per tensor): ||d - ref||_F <= 1e-2 ||ref||_F, and every element
 within 1e-2 max|ref|.  Small cases compare dh and dW in full, across several
 row and vocabulary tiles, ragged hidden and vocabulary sizes, fp16, several
 row chunks and caller-supplied statistics.  At the full backward workload
-(16,384 rows, 60 % scored, H 4096, V 151,936) dh is compared on sampled rows,
+(16,384 rows, 60 % scored, H 4096, V 151,936) dh is compared on 512 sampled
+rows and the rows with the most negative log-probs,
 dW is checked through a property that holds at any size (its columns sum to
 zero because every row of G sums to zero), and dW is compared exactly on
-sampled vocabulary rows at the same H and V with fewer scored rows.
+256 sampled vocabulary rows (plus target rows and the last row) at the same
+H and V with fewer scored rows.
 """
 import os
 
@@ -159,8 +161,11 @@ def test_backward_workload_full_size():
     torch.cuda.synchronize()
     n = d["n"]
     rows = d["row_idx"].cpu().numpy()
-    # dh on sampled scored rows (each needs only its own row statistics)
-    sel = workloads.sample_rows(n, 96, seed=4)
+    # dh on 512 sampled scored rows and the 8 with the most negative log-prob
+    # (each needs only its own row statistics)
+    logp, _ = flp.logprob_entropy(d["h"], d["W"], d["targets"], d["row_idx"], d["tau"])
+    worst = np.argsort(logp.cpu().numpy())[:8]
+    sel = np.unique(np.concatenate([workloads.sample_rows(n, 512, seed=4), worst]))
     want, _ = ref.backward(d["h"].cpu(), d["W"].cpu(), d["targets"].cpu().numpy(), rows, d["tau"],
                            d["g1"].cpu().numpy(), d["g2"].cpu().numpy(), "bf16",
                            dh_rows_sel=sel, vsel=np.zeros(0, np.int64),
@@ -184,7 +189,7 @@ def test_backward_dw_rows_exact_at_full_vocabulary():
     rows = d["row_idx"].cpu().numpy()
     dh, dW = flp.backward(d["h"], d["W"], d["targets"], d["row_idx"], d["tau"], d["g1"], d["g2"])
     torch.cuda.synchronize()
-    vsel = np.concatenate([workloads.sample_rows(w.V, 64, seed=44),
+    vsel = np.concatenate([workloads.sample_rows(w.V, 256, seed=44),
                            d["targets"].cpu().numpy()[rows[:8]], [w.V - 1]])
     _, want = ref.backward(d["h"].cpu(), d["W"].cpu(), d["targets"].cpu().numpy(), rows, d["tau"],
                            d["g1"].cpu().numpy(), d["g2"].cpu().numpy(), "bf16",

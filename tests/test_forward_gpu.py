@@ -4,7 +4,9 @@ Element by element on small cases that still span several 128-row tiles,
 several 256-column vocabulary tiles and ragged tails in rows, vocabulary and
 hidden size; on seeded row samples at the full sizes of the forward-scoring
 (4096 x 4096 x 151,936, tau 0.7) and long-packed (49,152 packed, H 5120,
-V 38,016, fp16) workloads, in the same launch configuration the bench times.
+V 38,016, fp16) workloads, in the same launch configuration the bench times:
+512 seeded rows plus the first and last rows, the rows with the most negative
+log-probs and those with the lowest and highest entropies.
 Tolerance: |d logp|, |d ent| <= 1e-3 absolute on every checked row.
 """
 import math
@@ -174,13 +176,21 @@ def test_repeated_calls_are_deterministic():
 
 # ---------------------------------------------------------------- full sizes
 
-def _full_size(wid, k=256):
+def _extreme_rows(logp, ent, k=8):
+    """Positions of the rows with the most negative log-prob (the target's
+    logit furthest below the row's maximum) and the lowest and highest
+    entropies: where the fold's precision is tested hardest."""
+    lp, en = logp.detach().cpu().numpy(), ent.detach().cpu().numpy()
+    return np.concatenate([np.argsort(lp)[:k], np.argsort(en)[:k // 2], np.argsort(en)[-(k // 2):]])
+
+
+def _full_size(wid, k=512):
     d = workloads.make(wid, device="cuda")
     logp, ent = flp.logprob_entropy(d["h"], d["W"], d["targets"], d["row_idx"], d["tau"])
     torch.cuda.synchronize()
     n = d["n"]
     pos = workloads.sample_rows(n, k, seed=wid)
-    pos = np.unique(np.concatenate([pos, [0, n - 1]]))
+    pos = np.unique(np.concatenate([pos, [0, n - 1], _extreme_rows(logp, ent)]))
     rows = pos if d["row_idx"] is None else d["row_idx"].cpu().numpy()[pos]
     o = ref.logprob_entropy(d["h"].cpu(), d["W"].cpu(), d["targets"].cpu().numpy(), rows,
                             d["tau"], d["workload"].dtype)

@@ -102,7 +102,10 @@ def test_distillation_workload_sampled():
     kl = flp.kl_divergence(d["h_s"], d["W_s"], d["h_t"], d["W_t"])
     torch.cuda.synchronize()
     n = d["n"]
-    pos = np.unique(np.concatenate([workloads.sample_rows(n, 192, seed=3), [0, n - 1]]))
+    k_gpu = kl.detach().cpu().numpy()
+    # 512 seeded rows, the ends, and the rows with the largest and smallest KL
+    extreme = np.concatenate([np.argsort(k_gpu)[-8:], np.argsort(k_gpu)[:4]])
+    pos = np.unique(np.concatenate([workloads.sample_rows(n, 512, seed=3), [0, n - 1], extreme]))
     want = ref.kl(d["h_s"].cpu(), d["W_s"].cpu(), d["h_t"].cpu(), d["W_t"].cpu(), pos, "bf16")
     e = _check(kl[torch.from_numpy(pos).cuda()], want)
     k = kl.cpu().numpy()
