@@ -282,15 +282,19 @@ def _loss(h, W, tg, rows, tau, g1, g2):
     return float(np.sum(g1 * o["logp"] + g2 * o["ent"]))
 
 
-@pytest.mark.parametrize("tau", [0.7, 1.0])
-def test_backward_matches_finite_differences(tau):
+@pytest.mark.parametrize("tau,rows", [
+    (0.7, [5, 0, 2, 3]),
+    (1.0, [5, 0, 2, 3]),
+    (0.7, [5, 0, 2, 5, 3, 0, 5]),   # rows scored more than once: their terms add up
+])
+def test_backward_matches_finite_differences(tau, rows):
     rng = np.random.default_rng(13)
     T, H, V = 6, 5, 7
     h = rng.standard_normal((T, H))
     W = rng.standard_normal((V, H)) * 0.7
     tg = rng.integers(0, V, size=T)
-    rows = np.array([5, 0, 2, 3])
-    g1, g2 = rng.standard_normal(4), rng.standard_normal(4)
+    rows = np.array(rows)
+    g1, g2 = rng.standard_normal(len(rows)), rng.standard_normal(len(rows))
     dh_rows, dW = coracle.backward(h, W, tg, rows, tau, g1, g2, "f64")
     dh = coracle.scatter_rows(dh_rows, rows, T)
     eps = 1e-6
