@@ -324,10 +324,14 @@ def kl_divergence(h_s, W_s, h_t, W_t, row_idx=None, *, workspace=None):
 
 
 def backward(h, W, targets, row_idx, temperature, g1, g2, lse=None, ez=None, *, workspace=None,
-             support=None):
+             support=None, need_dh=True, need_dW=True):
     """dL/dh (dtype of h, [T,H]) and dL/dW (float32 [V,H]) of
     L = sum g1 * logp + g2 * ent, by tile recompute (under each row's
-    sampling support if ``support`` is given, as in :func:`logprob_entropy`)."""
+    sampling support if ``support`` is given, as in :func:`logprob_entropy`).
+    ``need_dh`` / ``need_dW`` False skips that gradient (returned as None),
+    e.g. for a frozen output layer."""
+    if not (need_dh or need_dW):
+        raise ValueError("need_dh and need_dW are both False")
     _matrix(h, "h")
     _matrix(W, "W")
     dev = h.device
@@ -339,8 +343,9 @@ def backward(h, W, targets, row_idx, temperature, g1, g2, lse=None, ez=None, *, 
     lse = _vector(lse, "lse", n, dev)
     ez = _vector(ez, "ez", n, dev)
     shape = make_shape(h.shape[0], h.shape[1], W.shape[0], n, h.dtype, h.shape[1], W.shape[1])
-    dh = torch.empty((h.shape[0], h.shape[1]), dtype=h.dtype, device=dev)
-    dW = torch.empty((W.shape[0], W.shape[1]), dtype=torch.float32, device=dev)
+    dh = torch.empty((h.shape[0], h.shape[1]), dtype=h.dtype, device=dev) if need_dh else None
+    dW = (torch.empty((W.shape[0], W.shape[1]), dtype=torch.float32, device=dev)
+          if need_dW else None)
     if h.stride(0) != h.shape[1] or W.stride(0) != W.shape[1]:
         h = h.contiguous()
         W = W.contiguous()
@@ -430,6 +435,9 @@ class FusedLogProbEntropy(torch.autograd.Function):
         n = lse.numel()
         g1 = g_logp if g_logp is not None else torch.zeros(n, device=h.device)
         g2 = g_ent if g_ent is not None else torch.zeros(n, device=h.device)
+        need_dh, need_dW = ctx.needs_input_grad[0], ctx.needs_input_grad[1]
+        if not (need_dh or need_dW):
+            return None, None, None, None, None, None
         dh, dW = backward(h, W, targets, row_idx, ctx.temperature, g1, g2, lse, ez,
-                          support=support)
-        return dh, dW.to(W.dtype), None, None, None, None
+                          support=support, need_dh=need_dh, need_dW=need_dW)
+        return dh, (dW.to(W.dtype) if dW is not None else None), None, None, None, None

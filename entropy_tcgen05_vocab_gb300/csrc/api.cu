@@ -492,8 +492,9 @@ flp_status backward_impl(const flp_shape *s, const void *h, const void *W, const
   if (st != FLP_OK) return st;
   if (!(std::isfinite(temperature) && temperature > 0.f))
     return fail(FLP_ERR_INVALID_ARG, "temperature must be finite and > 0");
-  if (!dh || !dW) return fail(FLP_ERR_INVALID_ARG, "dh and dW are required");
-  if (!aligned16(dh) || !aligned16(dW)) return fail(FLP_ERR_INVALID_ARG, "dh and dW must be 16-byte aligned");
+  if (!dh && !dW) return fail(FLP_ERR_INVALID_ARG, "dh and dW are both NULL: nothing to compute");
+  if ((dh && !aligned16(dh)) || (dW && !aligned16(dW)))
+    return fail(FLP_ERR_INVALID_ARG, "dh and dW must be 16-byte aligned");
   if ((lse == nullptr) != (ez == nullptr))
     return fail(FLP_ERR_INVALID_ARG, "lse and ez must both be given or both be NULL");
   if (s->n_rows > 0) {
@@ -512,9 +513,9 @@ flp_status backward_impl(const flp_shape *s, const void *h, const void *W, const
   const size_t esz = 2;
   cudaError_t e = cudaMemsetAsync(status, 0, L.cnt + L.cnt_bytes - L.status, cs);
   // rows that are not scored get a zero gradient
-  if (e == cudaSuccess && s->T > 0)
+  if (e == cudaSuccess && dh && s->T > 0)
     e = cudaMemset2DAsync(dh, s->ld_h * esz, 0, s->H * esz, s->T, cs);
-  if (e == cudaSuccess && s->n_rows == 0)
+  if (e == cudaSuccess && dW && s->n_rows == 0)
     e = cudaMemset2DAsync(dW, s->ld_w * 4, 0, s->H * 4, s->V, cs);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemset");
   if (s->n_rows == 0) return FLP_OK;
@@ -527,11 +528,13 @@ flp_status backward_impl(const flp_shape *s, const void *h, const void *W, const
     lda = s->H;
     e = launch_gather(h, s->ld_h, row_idx, s->n_rows, s->T, s->H, at<void>(ws, L.hs), dev.sms, cs);
     if (e != cudaSuccess) return cuda_fail(e, "gather launch");
-    // rows named more than once have their dh contributions summed
-    rowcnt = at<uint32_t>(ws, L.rowcnt);
-    e = cudaMemsetAsync(rowcnt, 0, static_cast<size_t>(s->T) * 4, cs);
-    if (e == cudaSuccess) e = launch_count_rows(row_idx, s->n_rows, s->T, rowcnt, dev.sms, cs);
-    if (e != cudaSuccess) return cuda_fail(e, "row count");
+    if (dh) {
+        // rows named more than once have their dh contributions summed
+        rowcnt = at<uint32_t>(ws, L.rowcnt);
+        e = cudaMemsetAsync(rowcnt, 0, static_cast<size_t>(s->T) * 4, cs);
+        if (e == cudaSuccess) e = launch_count_rows(row_idx, s->n_rows, s->T, rowcnt, dev.sms, cs);
+        if (e != cudaSuccess) return cuda_fail(e, "row count");
+    }
   }
   const float inv_tau = 1.0f / temperature;
   const float sl = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
@@ -603,36 +606,40 @@ flp_status backward_impl(const flp_shape *s, const void *h, const void *W, const
     ga.ld_support = ld_support;
     if ((e = launch_grad(ga, cs)) != cudaSuccess) return cuda_fail(e, "grad launch");
     // 2. dh[rows] = G W   (M = rc, N = H, K = V; W is MN-major for this product)
-    GemmArgs da{};
-    if ((st = make_map(&da.tmA, s->dtype, G, s->V, rc, ldg, 64, 128)) != FLP_OK) return st;
-    if ((st = make_map(&da.tmB, s->dtype, W, s->H, s->V, s->ld_w, 64, 64)) != FLP_OK) return st;
-    da.M = rc;
-    da.N = static_cast<int>(s->H);
-    da.K = static_cast<int>(s->V);
-    da.grid = gemm_cta_group() * std::min(dh_gemm_tiles(da.M, da.N), gemm_units(dev.sms));
-    da.bf16 = ga.bf16;
-    da.status = status;
-    da.r0 = static_cast<int>(r0);
-    da.T = s->T;
-    da.row_idx = row_idx;
-    da.rowcnt = rowcnt;
-    da.dh = dh;
-    da.ld_dh = s->ld_h;
-    if ((e = launch_dh_gemm(da, cs)) != cudaSuccess) return cuda_fail(e, "dh launch");
+    if (dh) {
+      GemmArgs da{};
+      if ((st = make_map(&da.tmA, s->dtype, G, s->V, rc, ldg, 64, 128)) != FLP_OK) return st;
+      if ((st = make_map(&da.tmB, s->dtype, W, s->H, s->V, s->ld_w, 64, 64)) != FLP_OK) return st;
+      da.M = rc;
+      da.N = static_cast<int>(s->H);
+      da.K = static_cast<int>(s->V);
+      da.grid = gemm_cta_group() * std::min(dh_gemm_tiles(da.M, da.N), gemm_units(dev.sms));
+      da.bf16 = ga.bf16;
+      da.status = status;
+      da.r0 = static_cast<int>(r0);
+      da.T = s->T;
+      da.row_idx = row_idx;
+      da.rowcnt = rowcnt;
+      da.dh = dh;
+      da.ld_dh = s->ld_h;
+      if ((e = launch_dh_gemm(da, cs)) != cudaSuccess) return cuda_fail(e, "dh launch");
+    }
     // 3. dW (+)= G^T h[rows]   (M = V, N = H, K = rc; both operands MN-major)
-    GemmArgs wa{};
-    if ((st = make_map(&wa.tmA, s->dtype, G, s->V, rc, ldg, 64, 64)) != FLP_OK) return st;
-    if ((st = make_map(&wa.tmB, s->dtype, Ar, s->H, rc, lda, 64, 64)) != FLP_OK) return st;
-    wa.M = static_cast<int>(s->V);
-    wa.N = static_cast<int>(s->H);
-    wa.K = rc;
-    wa.grid = gemm_cta_group() * std::min(dw_gemm_tiles(wa.M, wa.N), gemm_units(dev.sms));
-    wa.bf16 = ga.bf16;
-    wa.status = status;
-    wa.dW = dW;
-    wa.ld_dw = s->ld_w;
-    wa.accumulate = r0 > 0;
-    if ((e = launch_dw_gemm(wa, cs)) != cudaSuccess) return cuda_fail(e, "dW launch");
+    if (dW) {
+      GemmArgs wa{};
+      if ((st = make_map(&wa.tmA, s->dtype, G, s->V, rc, ldg, 64, 64)) != FLP_OK) return st;
+      if ((st = make_map(&wa.tmB, s->dtype, Ar, s->H, rc, lda, 64, 64)) != FLP_OK) return st;
+      wa.M = static_cast<int>(s->V);
+      wa.N = static_cast<int>(s->H);
+      wa.K = rc;
+      wa.grid = gemm_cta_group() * std::min(dw_gemm_tiles(wa.M, wa.N), gemm_units(dev.sms));
+      wa.bf16 = ga.bf16;
+      wa.status = status;
+      wa.dW = dW;
+      wa.ld_dw = s->ld_w;
+      wa.accumulate = r0 > 0;
+      if ((e = launch_dw_gemm(wa, cs)) != cudaSuccess) return cuda_fail(e, "dW launch");
+    }
   }
   if ((e = ev.stop(cs)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
   return FLP_OK;

@@ -259,13 +259,15 @@ flp_status flp_kl_mxfp4(const flp_shape *shape, const void *h_s, const void *W_s
  *   lse, ez      [n_rows] float from a previous flp_logprob_entropy with
  *                the same inputs (out_lse, out_ez), or both NULL: the
  *                statistics are then recomputed (one extra forward pass)
- *   dh           [T, ld_h] dtype; dW [V, ld_w] float32
+ *   dh           [T, ld_h] dtype; dW [V, ld_w] float32.  Either may be NULL
+ *                (not both) to skip that gradient, e.g. for a frozen output
+ *                layer: a NULL dW skips the dW GEMM, a third of the work.
  * row_idx may name a row more than once: that row's dh is the sum of its
  * contributions, added onto the zeroed row with packed 16-bit atomics (so
  * for a row named three or more times the low bits depend on the order of
  * the additions; every other row is written once and is bitwise
  * reproducible).
- * n_rows == 0 writes zeros to dh and dW.  The scored rows are processed in
+ * n_rows == 0 writes zeros to dh and dW (those given).  The scored rows are processed in
  * chunks of at most flp's chunk size (as many rows as keep the chunk's
  * logit gradient within 4 GiB; the environment variable FLP_GRAD_CHUNK_ROWS,
  * read at each call, can lower it); chunk lengths follow flp_row_chunks.

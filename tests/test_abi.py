@@ -98,6 +98,11 @@ def test_kl_and_backward_validate_on_host(L):
     bad = _shape(H=12)
     assert L.flp_kl(ctypes.byref(bad), FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, 1 << 40,
                     None) == 1
+    # dh and dW may each be NULL (that gradient skipped), not both
+    ws = 1 << 40
+    assert L.flp_backward(ctypes.byref(s), FAKE, FAKE, FAKE, None, ctypes.c_float(1.0), FAKE,
+                          FAKE, None, None, None, None, FAKE, ws, None) == 1
+    assert b"both NULL" in L.flp_last_error()
 
 
 def test_workspace_formula(L):

@@ -136,6 +136,30 @@ def test_backward_repeated_rows_sum_their_contributions(monkeypatch, dtype, chun
     _rel(dh[torch.from_numpy(rep).cuda()], ref_dh[rep], "dh (repeated rows)")
 
 
+def test_backward_frozen_weight_or_input_skips_that_gradient():
+    """need_dW=False (a frozen output layer) or need_dh=False runs only the
+    other GEMM; the gradient that is computed is bitwise the full call's."""
+    d = _case(300, 256, 3000)
+    args = (d["h"], d["W"], d["targets"], d["row_idx"], d["tau"], d["g1"], d["g2"])
+    dh, dW = flp.backward(*args)
+    dh_only, none_w = flp.backward(*args, need_dW=False)
+    none_h, dW_only = flp.backward(*args, need_dh=False)
+    assert none_w is None and none_h is None
+    assert torch.equal(dh, dh_only) and torch.equal(dW, dW_only)
+    with pytest.raises(ValueError):
+        flp.backward(*args, need_dh=False, need_dW=False)
+
+
+def test_autograd_with_a_frozen_weight():
+    d = _case(300, 256, 3000)
+    h = d["h"].clone().requires_grad_(True)
+    logp, ent = flp.FusedLogProbEntropy.apply(h, d["W"], d["targets"], d["row_idx"], d["tau"])
+    (logp * d["g1"] + ent * d["g2"]).sum().backward()
+    dh, _ = flp.backward(d["h"], d["W"], d["targets"], d["row_idx"], d["tau"], d["g1"], d["g2"])
+    assert d["W"].grad is None
+    assert torch.equal(h.grad, dh)
+
+
 def test_backward_no_scored_rows_gives_zeros():
     d = _case(64, 128, 512)
     rows = torch.zeros(0, dtype=torch.int64, device="cuda")
