@@ -168,6 +168,17 @@ struct LseEpi {
 
   __device__ __forceinline__ void tile(uint32_t taddr, int col0, int nchunks) {
     if (SUP) sup.start(col0);
+    // With several targets, bit c marks the chunks that hold one, so a chunk
+    // without any costs one test instead of KMAX.
+    uint32_t hit = 0xffffffffu;
+    if (KMAX > 1) {
+      hit = 0u;
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k) {
+        const int rel = tgt[k] - col0;
+        if (static_cast<unsigned>(rel) < static_cast<unsigned>(nchunks * 32)) hit |= 1u << (rel >> 5);
+      }
+    }
 #pragma unroll 1
     for (int c = 0; c < nchunks; ++c) {
       const int cb = col0 + c * 32;
@@ -187,6 +198,7 @@ struct LseEpi {
         fold_masked(x, p.V - cb);
       }
       // each target column lies in exactly one chunk: store its raw logit there
+      if (!((hit >> c) & 1u)) continue;
 #pragma unroll
       for (int k = 0; k < KMAX; ++k) {
         const int rel = tgt[k] - cb;
