@@ -519,8 +519,8 @@ def run_ours(args):
             torch.cuda.empty_cache()
         # K-candidate scoring (4 target tokens per row) and a sampling support
         # (about 1/32 of the tokens per row, targets kept) on the main workload's
-        # inputs, each timed in blocks of 20 calls alternating with blocks of the
-        # plain call, so both see the same clocks.
+        # inputs, each timed in blocks of 10 calls interleaved (ABBA) with blocks
+        # of the plain call, so both see the same clocks.
         if d["workload"].kind == "fwd":
             w = d["workload"]
             shape = flp.make_shape(w.T, w.H, w.V, n, d["h"].dtype)
@@ -532,10 +532,16 @@ def run_ours(args):
 
             def variant_line(name, fn, note):
                 try:
+                    # blocks of 10 calls in ABBA order, so a drift of the clock over
+                    # the run (heating towards the power cap) weighs on both alike
                     t_var = t_plain = 0.0
-                    for _ in range(2):
-                        t_plain += time_calls(plain, 20, device)
-                        t_var += time_calls(fn, 20, device)
+                    for order in ((plain, fn), (fn, plain), (plain, fn), (fn, plain)):
+                        for f in order:
+                            t = time_calls(f, 10, device)
+                            if f is fn:
+                                t_var += t
+                            else:
+                                t_plain += t
                     t_var = max_over_ranks(t_var, world, device)
                     t_plain = max_over_ranks(t_plain, world, device)
                     extra[name] = {
@@ -564,20 +570,28 @@ def run_ours(args):
                          {"support": "each token kept with probability 1/32, targets kept"})
             del sup, tk
         # distillation KL with the teacher head in MXFP4 (4.25 bits per weight),
-        # alternating with the bf16 teacher head on the same inputs
+        # interleaved (ABBA) with the bf16 teacher head on the same inputs
         try:
             dk = workloads.make(3, device=device)
             wk = dk["workload"]
             packed, scales = flp.mxfp4_quantize(dk["W_t"])
             shape = flp.make_shape(wk.T, wk.H, wk.V, dk["n"], dk["h"].dtype)
             wsk = torch.empty(flp.workspace_size(shape, 1), dtype=torch.uint8, device=device)
+            def bf16_teacher():
+                flp.kl_divergence(dk["h_s"], dk["W_s"], dk["h_t"], dk["W_t"], None, workspace=wsk)
+
+            def mx_teacher():
+                flp.kl_divergence_mxfp4(dk["h_s"], dk["W_s"], dk["h_t"], packed, scales, None,
+                                        workspace=wsk)
+
             t_mx = t_bf = 0.0
-            for _ in range(2):
-                t_bf += time_calls(lambda: flp.kl_divergence(
-                    dk["h_s"], dk["W_s"], dk["h_t"], dk["W_t"], None, workspace=wsk), 10, device)
-                t_mx += time_calls(lambda: flp.kl_divergence_mxfp4(
-                    dk["h_s"], dk["W_s"], dk["h_t"], packed, scales, None, workspace=wsk), 10,
-                    device)
+            for order in ((bf16_teacher, mx_teacher), (mx_teacher, bf16_teacher)):  # ABBA
+                for f in order:
+                    t = time_calls(f, 10, device)
+                    if f is mx_teacher:
+                        t_mx += t
+                    else:
+                        t_bf += t
             t_mx = max_over_ranks(t_mx, world, device)
             t_bf = max_over_ranks(t_bf, world, device)
             flk = flops_per_call(dk)
