@@ -64,3 +64,25 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
         steps, warmup, workload, gpus = 3, 1, 1, 2
     assert bench.run_reference(A()) is None
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_prints_the_contract_line(monkeypatch, capsys):
+    """The reference arm (the float64 oracle on the host cores) prints one
+    JSON line with the contract's keys, on the tiny workload here."""
+    import json
+    for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+
+    class A:
+        steps, warmup, workload, gpus = 2, 3, 0, 1
+    bench.run_reference(A())
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+              "cpu_baseline", "e2e"):
+        assert k in line, k
+    assert line["impl"] == "reference" and line["value"] > 0 and line["steps"] == 2
+    assert line["config"]["workload"].startswith("tiny")
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
