@@ -138,6 +138,36 @@ def test_one_hot_dominant_rows():
     _check(ent, o["ent"], "ent")
 
 
+@pytest.mark.parametrize("tau", [0.1, 10.0, 50.0])
+def test_extreme_temperatures(tau):
+    """Sharp (logits / 0.1 spread over tens of nats) and nearly flat (entropy
+    close to ln V) distributions."""
+    w = workloads.WORKLOADS[0].scaled(T=300, V=5000, seed=26, w_std=0.05)
+    d = workloads.make(w, device="cuda")
+    logp, ent = _run_and_compare(d["h"], d["W"], d["targets"], None, tau)
+    if tau >= 10.0:
+        assert np.all(ent.cpu().numpy() > math.log(5000) - 0.1)
+
+
+def test_large_logits():
+    """Hidden states 30x the recipe's scale: logits in the hundreds, so the
+    running max moves by large steps and almost all the mass sits on a few
+    tokens per row."""
+    w = workloads.WORKLOADS[0].scaled(T=260, V=7000, seed=27, w_std=0.05, h_std=30.0)
+    d = workloads.make(w, device="cuda")
+    _run_and_compare(d["h"], d["W"], d["targets"], None, 1.0)
+
+
+def test_single_token_vocabulary():
+    """V = 1: every row's distribution is the one token, logp = 0, entropy 0
+    (up to FP32 rounding: the fold works in base 2, so z/tau and the LSE
+    reach the same value by different roundings)."""
+    w = workloads.WORKLOADS[0].scaled(T=200, H=64, V=1, seed=28)
+    d = workloads.make(w, device="cuda")
+    logp, ent = _run_and_compare(d["h"], d["W"], d["targets"], None, 0.7)
+    assert logp.abs().max().item() <= 1e-6 and ent.abs().max().item() <= 1e-6
+
+
 def test_no_scored_rows():
     d = workloads.make(workloads.WORKLOADS[0].scaled(T=64, V=512), device="cuda")
     rows = torch.zeros(0, dtype=torch.int64, device="cuda")
