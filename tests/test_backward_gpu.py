@@ -160,6 +160,23 @@ def test_autograd_with_a_frozen_weight():
     assert torch.equal(h.grad, dh)
 
 
+@pytest.mark.parametrize("tau", [0.1, 20.0])
+def test_backward_extreme_temperatures(tau):
+    d = _case(260, 128, 2500, seed=47, tau=tau)
+    dh, dW = flp.backward(d["h"], d["W"], d["targets"], d["row_idx"], d["tau"], d["g1"], d["g2"])
+    torch.cuda.synchronize()
+    ref_dh, ref_dW = _oracle(d, "bf16")
+    _rel(dh, ref_dh, "dh")
+    _rel(dW, ref_dW, "dW")
+
+
+def test_backward_single_token_vocabulary_is_zero():
+    """V = 1: p = 1 = the one-hot, z' = E z', so G and both gradients vanish."""
+    d = _case(130, 64, 1, seed=48)
+    dh, dW = flp.backward(d["h"], d["W"], d["targets"], d["row_idx"], d["tau"], d["g1"], d["g2"])
+    assert dh.float().abs().max().item() <= 1e-5 and dW.abs().max().item() <= 1e-5
+
+
 def test_backward_no_scored_rows_gives_zeros():
     d = _case(64, 128, 512)
     rows = torch.zeros(0, dtype=torch.int64, device="cuda")

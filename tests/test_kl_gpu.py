@@ -54,6 +54,26 @@ def test_kl_small(T, H, V):
     _check(kl, want)
 
 
+def test_kl_large_logits():
+    """Hidden states 10x the recipe's scale (teacher noise scaled alike):
+    logits in the tens to hundreds, peaked distributions, KL of tens of
+    nats on some rows."""
+    w = workloads.WORKLOADS[3].scaled(T=260, H=256, V=6000, seed=35, h_std=10.0,
+                                      teacher_noise=3.0)
+    d = workloads.make(w, device="cuda")
+    kl = flp.kl_divergence(d["h_s"], d["W_s"], d["h_t"], d["W_t"])
+    want = coracle.kl(d["h_s"].cpu(), d["W_s"].cpu(), d["h_t"].cpu(), d["W_t"].cpu(), None, "bf16")
+    assert want.max() > 10.0
+    _check(kl, want)
+
+
+def test_kl_single_token_vocabulary_is_zero():
+    w = workloads.WORKLOADS[3].scaled(T=100, H=64, V=1, seed=36)
+    d = workloads.make(w, device="cuda")
+    kl = flp.kl_divergence(d["h_s"], d["W_s"], d["h_t"], d["W_t"])
+    assert kl.abs().max().item() <= 1e-6
+
+
 def test_kl_fp16_with_row_idx():
     rows = torch.tensor([5, 0, 299, 5, 128, 127, 200], device="cuda")
     kl, want, _ = _case(300, 256, 4000, dtype="fp16", seed=32, rows=rows)
