@@ -549,6 +549,7 @@ def run_ours(args):
                         "scored_tokens_per_s": job_throughput(n, 40, t_var, world),
                         "ms_per_step": t_var / 40,
                         "tflops": fl / (t_var / 40 / 1e3) / 1e12,
+                        "pct_of_bf16_peak": 100 * fl / (t_var / 40 / 1e3) / 1e12 / P["bf16_tflops"],
                         "plain_ms_per_step_same_clocks": t_plain / 40}
                 except Exception as e:  # reported, not fatal
                     extra[name] = {"unavailable": str(e)[:200]}
@@ -601,6 +602,7 @@ def run_ours(args):
                                                             wk.V * wk.H * 2 / 1e9)),
                 "steps": 20, "scored_tokens_per_s": job_throughput(dk["n"], 20, t_mx, world),
                 "ms_per_step": t_mx / 20, "tflops": flk / (t_mx / 20 / 1e3) / 1e12,
+                "pct_of_bf16_peak": 100 * flk / (t_mx / 20 / 1e3) / 1e12 / P["bf16_tflops"],
                 "bf16_teacher_ms_per_step_same_clocks": t_bf / 20}
             del dk, packed, scales, wsk
         except Exception as e:  # reported, not fatal
