@@ -663,7 +663,7 @@ const char *flp_status_string(flp_status s) {
   switch (s) {
     case FLP_OK: return "ok";
     case FLP_ERR_INVALID_ARG: return "invalid argument";
-    case FLP_ERR_UNSUPPORTED: return "unsupported device or size";
+    case FLP_ERR_UNSUPPORTED: return "unsupported device or input combination";
     case FLP_ERR_WORKSPACE: return "workspace missing or too small";
     case FLP_ERR_CUDA: return "CUDA error";
     case FLP_ERR_DEVICE_STATUS: return "the device recorded a problem";

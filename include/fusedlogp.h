@@ -39,7 +39,8 @@
  *   - Matrices are row-major.  h is [T, ld_h] with H <= ld_h used columns;
  *     W is [V, ld_w].  H, ld_h and ld_w must be multiples of 8 and h, W
  *     16-byte aligned (tensor-memory-access copies move 16-byte units).
- *   - n_rows == 0 is valid and enqueues nothing (the "no scored rows" case).
+ *   - n_rows == 0 is valid (the "no scored rows" case): the scoring and KL
+ *     calls enqueue nothing, the backward only zeroes dh and dW.
  */
 #ifndef FUSEDLOGP_H
 #define FUSEDLOGP_H
@@ -56,8 +57,10 @@ typedef struct CUstream_st *flp_stream_t;
 
 typedef enum {
     FLP_OK = 0,
-    FLP_ERR_INVALID_ARG = 1,   /* null pointer, bad size, stride, alignment or temperature */
-    FLP_ERR_UNSUPPORTED = 2,   /* no usable sm_103a device, or a size beyond int32 tiling */
+    FLP_ERR_INVALID_ARG = 1,   /* null pointer, bad size (also one beyond the 32-bit tiling
+                                  range), stride, alignment or temperature */
+    FLP_ERR_UNSUPPORTED = 2,   /* no usable sm_103a device, or an unsupported combination
+                                  (the MXFP4 teacher with fp16 rows) */
     FLP_ERR_WORKSPACE = 3,     /* workspace null or smaller than flp_workspace_size() */
     FLP_ERR_CUDA = 4,          /* a CUDA runtime/driver call or a launch failed */
     FLP_ERR_DEVICE_STATUS = 5  /* flp_read_device_status(): the device recorded a problem */
@@ -240,8 +243,9 @@ flp_status flp_mxfp4_quantize(const void *W, flp_dtype dtype, int64_t V, int64_t
  * flp_kl with the teacher head given in MXFP4 (Wt_packed, Wt_scales as
  * produced by flp_mxfp4_quantize for V rows of H columns): the teacher logits
  * are h_t[row] times the decoded weights, exactly (every MXFP4 value is a
- * bf16 value, decoded in shared memory next to the tensor cores; scale codes
- * 0 and 1 flush to zero).  bf16 only (FLP_ERR_UNSUPPORTED for fp16); H a
+ * bf16 value, decoded in shared memory next to the tensor cores; decoded
+ * values below bf16's normal range, 2^-126, which only scale codes 0 and 1
+ * can give, flush to zero).  bf16 only (FLP_ERR_UNSUPPORTED for fp16); H a
  * multiple of 64; both buffers 16-byte aligned.  Same workspace as FLP_OP_KL.
  */
 flp_status flp_kl_mxfp4(const flp_shape *shape, const void *h_s, const void *W_s,
