@@ -1,7 +1,8 @@
 """Compile ``oracle.c`` into ``oracle/_build/liboracle.so`` with gcc.
 
-Test infrastructure: building the checker is not using it.  Portable flags
-only (no -march), so the same source builds on x86_64 and aarch64 hosts.
+Test infrastructure: compiling the oracle does not put it on the product
+path, which never loads it.  Portable flags only (no -march), so the same
+source builds on x86_64 and aarch64 hosts.
 """
 import os
 import subprocess
