@@ -44,7 +44,11 @@ flp_status cuda_fail(cudaError_t e, const char *what) {
   return fail(FLP_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+// Vocabulary splits per row tile: at most 64, or as many as give about
+// kSplitItems work items when there are few row tiles (with one row tile,
+// 64 splits would leave 12 of 76 CTA pairs idle in the HBM-bound regime).
 constexpr int64_t kMaxSplits = 64;
+constexpr int64_t kSplitItems = 320;
 constexpr size_t kAlign = 1024;
 constexpr size_t kStatusBytes = 256;
 // Upper bound of the backward's logit-gradient chunk.
@@ -69,8 +73,10 @@ bool shape_ok(const flp_shape *s, const char **why) {
 
 int vocab_tiles(int64_t V, int bn) { return static_cast<int>(cdiv(V, bn)); }
 
-int max_splits(int64_t V, int bn) {
-  return static_cast<int>(std::min<int64_t>(vocab_tiles(V, bn), kMaxSplits));
+int max_splits(int64_t V, int bn, int64_t n_rows, int bm) {
+  const int64_t row_tiles = std::max<int64_t>(1, cdiv(n_rows, bm));
+  const int64_t cap = std::max<int64_t>(kMaxSplits, cdiv(kSplitItems, row_tiles));
+  return static_cast<int>(std::min<int64_t>(vocab_tiles(V, bn), cap));
 }
 
 // Rows of the backward's logit-gradient chunk: as many as fit in 4 GiB, or
@@ -110,7 +116,7 @@ Layout layout_for(const flp_shape *s, flp_op op) {
   // the backward's statistics pass is the forward kernel
   const int bn = (op == FLP_OP_KL) ? kKlBN : kFwdTileCols;
   const int halves = ((op == FLP_OP_KL) ? kKlEpiWarps : kFwdEpiWarps) / 4;
-  const size_t sm = static_cast<size_t>(max_splits(s->V, bn)) * halves;  // partial slots
+  const size_t sm = static_cast<size_t>(max_splits(s->V, bn, s->n_rows, 128 * kFwdCG)) * halves;  // partial slots
   L.pm = take(sm * n * 4);
   L.ps = take(sm * n * 4);
   L.pb = take(sm * n * 4);
@@ -175,7 +181,7 @@ Plan make_plan(int64_t n, int64_t V, int64_t H, int bn, int num_sms, int bm, int
   s.k_blocks = static_cast<int>(cdiv(H, 64));
   const int64_t a_tile_bytes = static_cast<int64_t>(bm) * H * 2 * a_ops;
   s.band = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(s.row_tiles, band_bytes / a_tile_bytes)));
-  const int smax = max_splits(V, bn);
+  const int smax = max_splits(V, bn, n, bm);
   std::vector<int64_t> loads;
   int64_t best_load = -1;
   for (int S = 1; S <= smax; ++S) {
