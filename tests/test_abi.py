@@ -262,3 +262,25 @@ def test_product_package_does_not_import_the_oracle():
                 elif isinstance(node, ast.ImportFrom):
                     mods = [node.module or ""]
                 assert not any(m == "oracle" or m.startswith("oracle.") for m in mods), fn
+
+
+def test_plain_c_caller_compiles_against_the_header(L, tmp_path):
+    """The public header is plain C: a C11 caller (tests/c_caller) compiles
+    and links against the library with gcc -Wall -Werror.  Running it needs a
+    GPU (tests/test_c_abi_gpu.py)."""
+    import shutil
+    import subprocess
+    cuda = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+    if shutil.which("gcc") is None or not os.path.exists(os.path.join(cuda, "include", "cuda_runtime.h")):
+        pytest.skip("gcc or the CUDA headers are missing")
+    libdirs = [os.path.join(cuda, d) for d in ("lib64", "targets/sbsa-linux/lib",
+                                                "targets/x86_64-linux/lib")]
+    cudalib = next((p for p in libdirs if os.path.exists(os.path.join(p, "libcudart.so"))), None)
+    if cudalib is None:
+        pytest.skip("libcudart.so not found")
+    libdir = os.path.dirname(flp._build.LIB)
+    subprocess.run(["gcc", "-O2", "-std=c11", "-Wall", "-Werror",
+                    "-I", os.path.join(ROOT, "include"), "-I", os.path.join(cuda, "include"),
+                    os.path.join(ROOT, "tests", "c_caller", "flp_c_caller.c"),
+                    "-o", str(tmp_path / "caller"), "-L", libdir, "-lfusedlogp",
+                    "-L", cudalib, "-lcudart"], check=True)
