@@ -374,7 +374,12 @@ flp_status logprob_impl(const flp_shape *s, const void *h, const void *W, const 
   if ((st = device_info(&dev)) != FLP_OK) return st;
 
   const Layout L = layout_for(s, FLP_OP_LOGPROB_ENTROPY);
-  const Plan p = plan_cached(s->n_rows, s->V, s->H, kFwdTileCols, fwd_units(dev.sms), 128 * kFwdCG);
+  // few rows: single CTAs on 128-row tiles (the workspace's partial slots
+  // cover this plan too: twice the columns' worth of splits per row)
+  const bool few = s->n_rows <= kSmallRows && K == 1 && !support;
+  const int cg = few ? 1 : kFwdCG;
+  const Plan p = few ? plan_cached(s->n_rows, s->V, s->H, kFwdBN, fwd1_units(dev.sms), 128)
+                     : plan_cached(s->n_rows, s->V, s->H, kFwdTileCols, fwd_units(dev.sms), 128 * kFwdCG);
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   FwdArgs a{};
   const void *A = h;
@@ -384,10 +389,10 @@ flp_status logprob_impl(const flp_shape *s, const void *h, const void *W, const 
     lda = s->H;
   }
   if ((st = make_map(&a.tmA, s->dtype, A, s->H, s->n_rows, lda, 64, 128)) != FLP_OK) return st;
-  if ((st = make_map(&a.tmB, s->dtype, W, s->H, s->V, s->ld_w, 64, kFwdBN / kFwdCG)) != FLP_OK)
+  if ((st = make_map(&a.tmB, s->dtype, W, s->H, s->V, s->ld_w, 64, kFwdBN / cg)) != FLP_OK)
     return st;
   a.sch = p.sch;
-  a.grid = p.grid * kFwdCG;
+  a.grid = p.grid * cg;
   a.bf16 = s->dtype == FLP_BF16;
   a.targets = targets;
   a.K = K;
@@ -416,7 +421,8 @@ flp_status logprob_impl(const flp_shape *s, const void *h, const void *W, const 
     if (e != cudaSuccess) return cuda_fail(e, "gather launch");
   }
   if ((e = ev.start(cs)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-  if ((e = launch_fwd_scoring(a, cs)) != cudaSuccess) return cuda_fail(e, "scoring launch");
+  e = few ? launch_fwd_scoring_1cta(a, cs) : launch_fwd_scoring(a, cs);
+  if (e != cudaSuccess) return cuda_fail(e, "scoring launch");
   if ((e = ev.stop(cs)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
   return FLP_OK;
 }
@@ -693,8 +699,10 @@ flp_status flp_plan_scoring(const flp_shape *shape, flp_op op, int32_t num_sms, 
     return fail(FLP_ERR_INVALID_ARG, "unknown op");
   std::memset(out, 0, sizeof *out);
   if (shape->n_rows == 0) return FLP_OK;
-  const int bn = op == FLP_OP_KL ? kKlBN : kFwdTileCols;
-  const int cg = op == FLP_OP_KL ? kKlCG : kFwdCG;
+  // the forward's few-rows path (one target, no support) runs single CTAs
+  const bool few = op == FLP_OP_LOGPROB_ENTROPY && shape->n_rows <= kSmallRows;
+  const int bn = op == FLP_OP_KL ? kKlBN : (few ? kFwdBN : kFwdTileCols);
+  const int cg = op == FLP_OP_KL ? kKlCG : (few ? 1 : kFwdCG);
   const int units = std::max(1, num_sms / cg);
   const Plan p = plan_cached(shape->n_rows, shape->V, shape->H, bn, units, 128 * cg,
                              op == FLP_OP_KL ? 2 : 1);

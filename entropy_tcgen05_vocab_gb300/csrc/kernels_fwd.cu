@@ -349,4 +349,43 @@ int fwd_units(int num_sms) {
 
 int fwd_smem_bytes() { return FwdLayout::kSmemBytes; }
 
+// ---------------------------------------------------------------- few rows
+using Fwd1Layout = PipeLayout<kFwdBN, kFwd1Stages, 1, 1, 2, false>;
+#define FWD1_KERNEL \
+  vocab_pipeline_kernel<kFwdBN, kFwd1Stages, 1, LseEpi<1, false>, 1, 2, kFwd1EpiWarps, false>
+constexpr int kFwd1Threads = pipe_threads(kFwd1EpiWarps);
+
+cudaError_t launch_fwd_scoring_1cta(const FwdArgs &a, cudaStream_t stream) {
+  if (a.K != 1 || a.support) return cudaErrorInvalidValue;  // the host API never asks for this
+  LseEpi<1, false>::Params p;
+  p.targets = a.targets;
+  p.K = 1;
+  p.row_idx = a.row_idx;
+  p.T = a.T;
+  p.n = a.sch.n;
+  p.V = a.sch.V;
+  p.sl = a.scale_log2;
+  p.zsent = 0.f;  // no support on this path
+  p.pm = a.pm;
+  p.ps = a.ps;
+  p.pb = a.pb;
+  p.zt = a.zt;
+  p.counters = a.counters;
+  p.splits = a.sch.splits * (kFwd1EpiWarps / 4);
+  p.inv_tau = a.inv_tau;
+  p.out_logp = a.out_logp;
+  p.out_ent = a.out_ent;
+  p.out_lse = a.out_lse;
+  p.out_ez = a.out_ez;
+  p.status = a.status;
+  p.support = nullptr;
+  p.ld_support = 0;
+  p.tile_cols = kFwdBN;
+  const uint32_t idesc = idesc_f16(a.bf16, kBM, kFwdBN, false, false);
+  return launch_persistent(FWD1_KERNEL, a.grid, kFwd1Threads, Fwd1Layout::kSmemBytes, 1, stream,
+                           a.tmA, a.tmB, a.tmA, a.tmB, a.sch, idesc, p, a.status);
+}
+
+int fwd1_units(int num_sms) { return num_sms; }
+
 }  // namespace flp

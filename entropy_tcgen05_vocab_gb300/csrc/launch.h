@@ -27,6 +27,13 @@ constexpr int kFwdTileCols = 512;  // vocabulary columns per tile
 constexpr int kFwdCG = 2;
 constexpr int kFwdStages = 4;
 constexpr int kFwdEpiWarps = 8;
+// Few scored rows (n <= kSmallRows, one target, no support): single CTAs on
+// 128-row x 256-column tiles with double-buffered accumulators.  A pair tile
+// would be at least half padding there, and the call is bound by the
+// weight stream, not by the tensor cores.
+constexpr int kSmallRows = 128;
+constexpr int kFwd1Stages = 4;
+constexpr int kFwd1EpiWarps = 4;
 // Gradient pass of the backward: the same 256 x 512 shared-A tiles, one
 // accumulator buffer, eight epilogue warps, 4 stages of 48 KB.
 constexpr int kGradBN = 256;
@@ -124,6 +131,10 @@ struct GemmArgs {
 cudaError_t launch_gather(const void *h, int64_t ld_h, const int64_t *row_idx, int64_t n,
                           int64_t T, int64_t H, void *hs, int num_sms, cudaStream_t stream);
 cudaError_t launch_fwd_scoring(const FwdArgs &a, cudaStream_t stream);
+// The single-CTA variant (tmB box 64 x kFwdBN rows; plan with 128-row tiles
+// of kFwdBN columns, in CTAs).
+cudaError_t launch_fwd_scoring_1cta(const FwdArgs &a, cudaStream_t stream);
+int fwd1_units(int num_sms);
 cudaError_t launch_kl(const KlArgs &a, cudaStream_t stream);
 cudaError_t launch_grad(const GradArgs &a, cudaStream_t stream);
 cudaError_t launch_dh_gemm(const GemmArgs &a, cudaStream_t stream);
