@@ -255,6 +255,18 @@ def test_planner_extremes(T, H, V):
     _run_and_compare(d["h"], d["W"], d["targets"], rows, 0.8)
 
 
+@pytest.mark.parametrize("n", [1, 127, 128, 129])
+def test_few_rows_path_boundary(n):
+    """n <= 128 scored rows run single CTAs on 128 x 256 tiles, n > 128 CTA
+    pairs; both sides of the switch, with a gather, against the oracle."""
+    w = workloads.WORKLOADS[0].scaled(T=400, H=320, V=33000, seed=n, w_std=0.05)
+    d = workloads.make(w, device="cuda")
+    rows = torch.from_numpy(workloads.sample_rows(400, n, seed=n + 1)).cuda()
+    plan = flp.plan(flp.make_shape(400, 320, 33000, n, torch.bfloat16), flp.OP_LOGPROB_ENTROPY, 152)
+    assert plan["cta_group"] == (1 if n <= 128 else 2)
+    _run_and_compare(d["h"], d["W"], d["targets"], rows, 0.8)
+
+
 def test_kl_at_the_planner_extremes():
     w = workloads.WORKLOADS[3].scaled(T=64, H=1024, V=131072, seed=51)
     d = workloads.make(w, device="cuda")
