@@ -376,7 +376,7 @@ flp_status logprob_impl(const flp_shape *s, const void *h, const void *W, const 
   const Layout L = layout_for(s, FLP_OP_LOGPROB_ENTROPY);
   // few rows: single CTAs on 128-row tiles (the workspace's partial slots
   // cover this plan too: twice the columns' worth of splits per row)
-  const bool few = s->n_rows <= kSmallRows && K == 1 && !support;
+  const bool few = s->n_rows <= kSmallRows;
   const int cg = few ? 1 : kFwdCG;
   const Plan p = few ? plan_cached(s->n_rows, s->V, s->H, kFwdBN, fwd1_units(dev.sms), 128)
                      : plan_cached(s->n_rows, s->V, s->H, kFwdTileCols, fwd_units(dev.sms), 128 * kFwdCG);
@@ -699,7 +699,7 @@ flp_status flp_plan_scoring(const flp_shape *shape, flp_op op, int32_t num_sms, 
     return fail(FLP_ERR_INVALID_ARG, "unknown op");
   std::memset(out, 0, sizeof *out);
   if (shape->n_rows == 0) return FLP_OK;
-  // the forward's few-rows path (one target, no support) runs single CTAs
+  // the forward's few-rows path runs single CTAs
   const bool few = op == FLP_OP_LOGPROB_ENTROPY && shape->n_rows <= kSmallRows;
   const int bn = op == FLP_OP_KL ? kKlBN : (few ? kFwdBN : kFwdTileCols);
   const int cg = op == FLP_OP_KL ? kKlCG : (few ? 1 : kFwdCG);

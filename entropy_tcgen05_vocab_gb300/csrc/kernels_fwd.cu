@@ -295,7 +295,15 @@ using FwdLayout = PipeLayout<kFwdBN, kFwdStages, 2, kFwdCG, 1, true>;
   vocab_pipeline_kernel<kFwdBN, kFwdStages, 2, LseEpi<KMAX, SUP>, kFwdCG, 1, kFwdEpiWarps, true>
 constexpr int kFwdThreads = pipe_threads(kFwdEpiWarps);
 
-template <int KMAX, bool SUP>
+// Few scored rows: single CTAs on 128-row x kFwdBN-column tiles, two
+// accumulator buffers, four epilogue warps.
+using Fwd1Layout = PipeLayout<kFwdBN, kFwd1Stages, 1, 1, 2, false>;
+#define FWD1_KERNEL(KMAX, SUP) \
+  vocab_pipeline_kernel<kFwdBN, kFwd1Stages, 1, LseEpi<KMAX, SUP>, 1, 2, kFwd1EpiWarps, false>
+constexpr int kFwd1Threads = pipe_threads(kFwd1EpiWarps);
+
+// FEW: the single-CTA kernel, else the CTA-pair one.
+template <int KMAX, bool SUP, bool FEW>
 static cudaError_t launch_fwd_k(const FwdArgs &a, cudaStream_t stream) {
   typename LseEpi<KMAX, SUP>::Params p;
   p.targets = a.targets;
@@ -313,7 +321,8 @@ static cudaError_t launch_fwd_k(const FwdArgs &a, cudaStream_t stream) {
   p.pb = a.pb;
   p.zt = a.zt;
   p.counters = a.counters;
-  p.splits = a.sch.splits * (kFwdEpiWarps / 4);  // partial slots per row
+  // partial slots per row
+  p.splits = a.sch.splits * ((FEW ? kFwd1EpiWarps : kFwdEpiWarps) / 4);
   p.inv_tau = a.inv_tau;
   p.out_logp = a.out_logp;
   p.out_ent = a.out_ent;
@@ -322,19 +331,34 @@ static cudaError_t launch_fwd_k(const FwdArgs &a, cudaStream_t stream) {
   p.status = a.status;
   p.support = a.support;
   p.ld_support = a.ld_support;
-  p.tile_cols = kFwdTileCols;
-  const uint32_t idesc = idesc_f16(a.bf16, kBM * kFwdCG, kFwdBN, false, false);
-  return launch_persistent(FWD_KERNEL(KMAX, SUP), a.grid, kFwdThreads, FwdLayout::kSmemBytes, kFwdCG,
-                           stream, a.tmA, a.tmB, a.tmA, a.tmB, a.sch, idesc, p, a.status);
+  p.tile_cols = FEW ? kFwdBN : kFwdTileCols;
+  if constexpr (FEW) {
+    const uint32_t idesc = idesc_f16(a.bf16, kBM, kFwdBN, false, false);
+    return launch_persistent(FWD1_KERNEL(KMAX, SUP), a.grid, kFwd1Threads, Fwd1Layout::kSmemBytes,
+                             1, stream, a.tmA, a.tmB, a.tmA, a.tmB, a.sch, idesc, p, a.status);
+  } else {
+    const uint32_t idesc = idesc_f16(a.bf16, kBM * kFwdCG, kFwdBN, false, false);
+    return launch_persistent(FWD_KERNEL(KMAX, SUP), a.grid, kFwdThreads, FwdLayout::kSmemBytes,
+                             kFwdCG, stream, a.tmA, a.tmB, a.tmA, a.tmB, a.sch, idesc, p, a.status);
+  }
+}
+
+template <bool FEW>
+static cudaError_t launch_fwd_any(const FwdArgs &a, cudaStream_t stream) {
+  if (a.support) {
+    if (a.K != 1) return cudaErrorInvalidValue;  // the host API never asks for this
+    return launch_fwd_k<1, true, FEW>(a, stream);
+  }
+  if (a.K == 1) return launch_fwd_k<1, false, FEW>(a, stream);
+  return launch_fwd_k<kMaxTargets, false, FEW>(a, stream);
 }
 
 cudaError_t launch_fwd_scoring(const FwdArgs &a, cudaStream_t stream) {
-  if (a.support) {
-    if (a.K != 1) return cudaErrorInvalidValue;  // the host API never asks for this
-    return launch_fwd_k<1, true>(a, stream);
-  }
-  if (a.K == 1) return launch_fwd_k<1, false>(a, stream);
-  return launch_fwd_k<kMaxTargets, false>(a, stream);
+  return launch_fwd_any<false>(a, stream);
+}
+
+cudaError_t launch_fwd_scoring_1cta(const FwdArgs &a, cudaStream_t stream) {
+  return launch_fwd_any<true>(a, stream);
 }
 
 int fwd_units(int num_sms) {
@@ -348,43 +372,6 @@ int fwd_units(int num_sms) {
 }
 
 int fwd_smem_bytes() { return FwdLayout::kSmemBytes; }
-
-// ---------------------------------------------------------------- few rows
-using Fwd1Layout = PipeLayout<kFwdBN, kFwd1Stages, 1, 1, 2, false>;
-#define FWD1_KERNEL \
-  vocab_pipeline_kernel<kFwdBN, kFwd1Stages, 1, LseEpi<1, false>, 1, 2, kFwd1EpiWarps, false>
-constexpr int kFwd1Threads = pipe_threads(kFwd1EpiWarps);
-
-cudaError_t launch_fwd_scoring_1cta(const FwdArgs &a, cudaStream_t stream) {
-  if (a.K != 1 || a.support) return cudaErrorInvalidValue;  // the host API never asks for this
-  LseEpi<1, false>::Params p;
-  p.targets = a.targets;
-  p.K = 1;
-  p.row_idx = a.row_idx;
-  p.T = a.T;
-  p.n = a.sch.n;
-  p.V = a.sch.V;
-  p.sl = a.scale_log2;
-  p.zsent = 0.f;  // no support on this path
-  p.pm = a.pm;
-  p.ps = a.ps;
-  p.pb = a.pb;
-  p.zt = a.zt;
-  p.counters = a.counters;
-  p.splits = a.sch.splits * (kFwd1EpiWarps / 4);
-  p.inv_tau = a.inv_tau;
-  p.out_logp = a.out_logp;
-  p.out_ent = a.out_ent;
-  p.out_lse = a.out_lse;
-  p.out_ez = a.out_ez;
-  p.status = a.status;
-  p.support = nullptr;
-  p.ld_support = 0;
-  p.tile_cols = kFwdBN;
-  const uint32_t idesc = idesc_f16(a.bf16, kBM, kFwdBN, false, false);
-  return launch_persistent(FWD1_KERNEL, a.grid, kFwd1Threads, Fwd1Layout::kSmemBytes, 1, stream,
-                           a.tmA, a.tmB, a.tmA, a.tmB, a.sch, idesc, p, a.status);
-}
 
 int fwd1_units(int num_sms) { return num_sms; }
 

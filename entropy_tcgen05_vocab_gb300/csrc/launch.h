@@ -27,7 +27,7 @@ constexpr int kFwdTileCols = 512;  // vocabulary columns per tile
 constexpr int kFwdCG = 2;
 constexpr int kFwdStages = 4;
 constexpr int kFwdEpiWarps = 8;
-// Few scored rows (n <= kSmallRows, one target, no support): single CTAs on
+// Few scored rows (n <= kSmallRows): single CTAs on
 // 128-row x 256-column tiles with double-buffered accumulators.  A pair tile
 // would be at least half padding there, and the call is bound by the
 // weight stream, not by the tensor cores.

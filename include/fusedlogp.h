@@ -372,8 +372,8 @@ const char *flp_last_error(void);
  * Tiling plan of the scoring kernels, for inspection and tests (pure host
  * function; no GPU needed).  num_sms is the number of SMs to plan for.
  * FLP_OP_LOGPROB_ENTROPY with n_rows <= 128 reports the few-rows plan that
- * flp_logprob_entropy uses for one target per row without a support: single
- * CTAs (cta_group 1) on 128-row x 256-column tiles.
+ * the scoring calls (flp_logprob_entropy and its _k and _support forms) use:
+ * single CTAs (cta_group 1) on 128-row x 256-column tiles.
  */
 typedef struct {
     int32_t row_tiles;      /* ceil(n_rows / block_m) */

@@ -43,6 +43,15 @@ def test_k_targets_small(K):
     _compare(d, _candidates(300, 5001, K, K), None, 0.7)
 
 
+@pytest.mark.parametrize("n", [100, 128, 129])
+def test_k_targets_both_sides_of_the_few_rows_switch(n):
+    """n <= 128 scored rows run the single-CTA kernel, more the CTA pairs."""
+    w = workloads.WORKLOADS[0].scaled(T=400, H=320, V=33000, seed=n + 3, w_std=0.05)
+    d = workloads.make(w, device="cuda")
+    rows = torch.from_numpy(workloads.sample_rows(400, n, seed=n)).cuda()
+    _compare(d, _candidates(400, 33000, 6, n), rows, 0.8)
+
+
 def test_k_targets_fp16_row_idx():
     w = workloads.WORKLOADS[2].scaled(T=2000, H=256, V=3000)
     d = workloads.make(w, device="cuda")

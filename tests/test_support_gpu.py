@@ -84,6 +84,14 @@ def test_support_small(T, H, V, j, rows):
     _compare(_case(T, H, V, j, seed=T + V + j, rows=rows), 0.7)
 
 
+@pytest.mark.parametrize("n", [100, 128, 129])
+def test_support_both_sides_of_the_few_rows_switch(n):
+    """n <= 128 scored rows run the single-CTA kernel, more the CTA pairs."""
+    d = _case(400, 256, 33000, 4, seed=n + 7)
+    d["rows"] = torch.from_numpy(workloads.sample_rows(400, n, seed=n)).cuda()
+    _compare(d, 0.7)
+
+
 def test_support_fp16():
     _compare(_case(200, 256, 6000, 2, seed=61, dtype="fp16"), 1.0, dt="fp16")
 
