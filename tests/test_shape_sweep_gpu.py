@@ -1,0 +1,140 @@
+"""Seeded sweep of random shapes through the forward, the KL and the
+backward, each compared with the float64 oracle.
+
+The fixed-shape parity tests pick their ragged cases by hand.  This sweep
+draws 48 more from one seeded generator: rows T in [1, 700], hidden size H a
+multiple of 8 in [8, 1024], vocabulary V from 1 to 40,000 (log-uniform),
+bf16 or fp16, a temperature in [0.3, 3], and either all rows or a random
+row selection (unsorted, with repeats).  So tails of every kind fall at
+random places: a part of a 128-row tile, of a 64-wide K block, of a
+32-column chunk and of a 512-column vocabulary tile, and the few-rows path
+(n <= 128) against the pair path.  Each case is small enough for the C
+oracle to finish in about a second.
+
+Tolerances are those of the fixed-shape tests: |d logp|, |d ent|, |d KL|
+<= 1e-3 absolute; gradients within 1e-2 relative (Frobenius, and every
+element within 1e-2 of the largest).
+"""
+import numpy as np
+import pytest
+import torch
+
+import entropy_tcgen05_vocab_gb300 as flp
+import workloads
+from oracle import coracle
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-3
+RTOL = 1e-2
+N_CASES = 48
+MAX_WORK = 6e8   # n * V * H per case, so the oracle stays near a second
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    flp.build()
+    flp.lib()
+
+
+def _draw(case):
+    """Shape, dtype, temperature and row selection of sweep case ``case``."""
+    r = np.random.Generator(np.random.PCG64([2026, case]))
+    while True:
+        T = int(r.integers(1, 701))
+        H = 8 * int(r.integers(1, 129))
+        V = int(np.exp(r.uniform(0.0, np.log(40000.0)))) + 1
+        if T * V * H <= MAX_WORK:
+            break
+    dtype = "bf16" if r.random() < 0.6 else "fp16"
+    tau = float(np.round(r.uniform(0.3, 3.0), 3))
+    if r.random() < 0.4:
+        rows = None
+    else:
+        n = int(r.integers(1, 2 * T + 1))
+        rows = r.integers(0, T, size=n).astype(np.int64)
+    return T, H, V, dtype, tau, rows, int(r.integers(0, 2**31))
+
+
+def _scaled(kind, T, H, V, dtype, tau, seed):
+    base = {"fwd": 0, "kl": 3, "bwd": 4}[kind]
+    w = workloads.WORKLOADS[base].scaled(T=T, H=H, V=V, dtype=dtype, tau=tau, seed=seed,
+                                         w_std=0.06, rows="all", targets="uniform")
+    return workloads.make(w, device="cuda")
+
+
+def _abs(got, want, what):
+    g = got.detach().cpu().double().numpy()
+    assert np.all(np.isfinite(g)), what + ": non-finite output"
+    err = np.abs(g - want)
+    assert err.max() <= TOL, "%s: max |diff| %.3e at %d" % (what, err.max(), int(err.argmax()))
+
+
+def _rel(got, want, what):
+    g = got.detach().cpu().double().numpy()
+    assert np.all(np.isfinite(g)), what + ": non-finite"
+    fro = np.linalg.norm(g - want) / max(np.linalg.norm(want), 1e-30)
+    ele = np.abs(g - want).max() / max(np.abs(want).max(), 1e-30)
+    assert fro <= RTOL and ele <= RTOL, "%s: rel Frobenius %.2e, rel max %.2e" % (what, fro, ele)
+
+
+def _rel_or_zero(got, want, what):
+    if np.abs(want).max() < 1e-6:   # e.g. a one-token vocabulary: every gradient is zero
+        g = got.detach().cpu().double().numpy()
+        assert np.all(np.isfinite(g)) and np.abs(g).max() <= 1e-5, what + ": expected zeros"
+        return
+    _rel(got, want, what)
+
+
+CASES = [_draw(c) for c in range(N_CASES)]
+
+
+def _id(c):
+    T, H, V, dtype, tau, rows, _ = c
+    return "T%d-H%d-V%d-%s-tau%g-%s" % (T, H, V, dtype, tau,
+                                        "all" if rows is None else "n%d" % len(rows))
+
+
+@pytest.mark.parametrize("case", CASES, ids=[_id(c) for c in CASES])
+def test_forward_sweep(case):
+    T, H, V, dtype, tau, rows, seed = case
+    d = _scaled("fwd", T, H, V, dtype, tau, seed)
+    ri = None if rows is None else torch.from_numpy(rows).cuda()
+    logp, ent, lse, ez = flp.logprob_entropy(d["h"], d["W"], d["targets"], ri, tau,
+                                             return_stats=True)
+    torch.cuda.synchronize()
+    o = coracle.logprob_entropy(d["h"].cpu(), d["W"].cpu(), d["targets"].cpu().numpy(), rows,
+                                tau, dtype)
+    _abs(logp, o["logp"], "logp")
+    _abs(ent, o["ent"], "ent")
+    _abs(lse, o["lse"], "lse")
+
+
+@pytest.mark.parametrize("case", CASES[::2], ids=[_id(c) for c in CASES[::2]])
+def test_kl_sweep(case):
+    T, H, V, dtype, _, rows, seed = case
+    d = _scaled("kl", T, H, V, dtype, 1.0, seed)
+    ri = None if rows is None else torch.from_numpy(rows).cuda()
+    kl = flp.kl_divergence(d["h_s"], d["W_s"], d["h_t"], d["W_t"], ri)
+    torch.cuda.synchronize()
+    want = coracle.kl(d["h_s"].cpu(), d["W_s"].cpu(), d["h_t"].cpu(), d["W_t"].cpu(), rows, dtype)
+    _abs(kl, want, "kl")
+
+
+@pytest.mark.parametrize("case", CASES[1::2], ids=[_id(c) for c in CASES[1::2]])
+def test_backward_sweep(case):
+    T, H, V, dtype, tau, rows, seed = case
+    d = _scaled("bwd", T, H, V, dtype, tau, seed)
+    n = T if rows is None else len(rows)
+    g = np.random.Generator(np.random.PCG64([seed, 7]))
+    g1 = torch.from_numpy(g.standard_normal(n, dtype=np.float32)).cuda()
+    g2 = torch.from_numpy(g.standard_normal(n, dtype=np.float32)).cuda()
+    ri = None if rows is None else torch.from_numpy(rows).cuda()
+    dh, dW = flp.backward(d["h"], d["W"], d["targets"], ri, tau, g1, g2)
+    torch.cuda.synchronize()
+    dh_rows, ref_dW = coracle.backward(d["h"].cpu(), d["W"].cpu(), d["targets"].cpu().numpy(),
+                                       rows, tau, g1.cpu().numpy(), g2.cpu().numpy(), dtype)
+    ref_dh = coracle.scatter_rows(dh_rows, np.arange(T) if rows is None else rows, T)
+    _rel_or_zero(dh, ref_dh, "dh")
+    _rel_or_zero(dW, ref_dW, "dW")
