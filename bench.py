@@ -16,6 +16,8 @@ Prints ONE JSON line (rank 0):
   e2e         the same metric through the public API with the step's inputs
               copied from pinned host memory and the results read back
   cpu_baseline the float64 oracle on a bounded row sample on the host cores
+  memory      the allocator's peak over one call beside the workspace and
+              the [n, V] FP32 logits the fused path never forms
   workloads   the other workloads (long packed fp16, KL, backward) measured
               the same way, when available
 
@@ -233,6 +235,33 @@ def call_once(flp, d, ws, stats=None):
     lse, ez = stats
     return flp.backward(d["h"], d["W"], d["targets"], d["row_idx"], d["tau"], d["g1"], d["g2"],
                         lse, ez, workspace=ws)
+
+
+def memory_footprint(flp, d, ws, device):
+    """Peak of torch's allocator over one call with the workspace passed in
+    (outside the timed region), beside the workspace and the [n, V] FP32
+    logits that the fused path never forms."""
+    w = d["workload"]
+    stats = None
+    if w.kind == "bwd":
+        _, _, lse, ez = flp.logprob_entropy(d["h"], d["W"], d["targets"], d["row_idx"], d["tau"],
+                                            return_stats=True)
+        stats = (lse, ez)
+    torch.cuda.synchronize(device)
+    free0 = torch.cuda.mem_get_info(device)[0]
+    torch.cuda.reset_peak_memory_stats(device)
+    base = torch.cuda.memory_allocated(device)
+    out = call_once(flp, d, ws, stats)
+    torch.cuda.synchronize(device)
+    peak = torch.cuda.max_memory_allocated(device) - base
+    outs = out if isinstance(out, tuple) else (out,)
+    out_bytes = sum(t.numel() * t.element_size() for t in outs if t is not None)
+    del out, outs
+    torch.cuda.synchronize(device)
+    return {"peak_alloc_delta_bytes": int(peak), "output_bytes": int(out_bytes),
+            "workspace_bytes": int(ws.numel()),
+            "logits_fp32_bytes_not_formed": int(d["n"]) * int(w.V) * 4,
+            "free_memory_unchanged": bool(torch.cuda.mem_get_info(device)[0] >= free0 - (2 << 20))}
 
 
 def op_of(d):
@@ -494,6 +523,7 @@ def run_ours(args):
         "e2e": e2e,
         "clocks": clocks,
         "gpu_launches": launches_per_call(d) * args.steps,
+        "memory": memory_footprint(flp, d, ws, device),
     }
 
     if not args.no_extra:

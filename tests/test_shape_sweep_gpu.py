@@ -9,7 +9,9 @@ row selection (unsorted, with repeats).  So tails of every kind fall at
 random places: a part of a 128-row tile, of a 64-wide K block, of a
 32-column chunk and of a 512-column vocabulary tile, and the few-rows path
 (n <= 128) against the pair path.  Each case is small enough for the C
-oracle to finish in about a second.
+oracle to finish in about a second.  The same cases also run the K-target
+forward, the forward and backward under a sampling support, and the KL with
+an MXFP4 teacher head.
 
 Tolerances are those of the fixed-shape tests: |d logp|, |d ent|, |d KL|
 <= 1e-3 absolute; gradients within 1e-2 relative (Frobenius, and every
@@ -138,3 +140,82 @@ def test_backward_sweep(case):
     ref_dh = coracle.scatter_rows(dh_rows, np.arange(T) if rows is None else rows, T)
     _rel_or_zero(dh, ref_dh, "dh")
     _rel_or_zero(dW, ref_dW, "dW")
+
+
+def _extra(case, k):
+    """A second seeded draw per case for the widened calls (K, support density)."""
+    return np.random.Generator(np.random.PCG64([2027, case[-1] % (2**31), k]))
+
+
+@pytest.mark.parametrize("case", CASES[::3], ids=[_id(c) for c in CASES[::3]])
+def test_k_targets_sweep(case):
+    T, H, V, dtype, tau, rows, seed = case
+    d = _scaled("fwd", T, H, V, dtype, tau, seed)
+    r = _extra(case, 1)
+    K = int(r.integers(1, 9))
+    tk = torch.from_numpy(r.integers(0, V, size=(T, K)).astype(np.int64))
+    ri = None if rows is None else torch.from_numpy(rows).cuda()
+    logp, ent = flp.logprob_entropy_k(d["h"], d["W"], tk.cuda(), ri, tau)
+    torch.cuda.synchronize()
+    o = coracle.logprob_k(d["h"].cpu(), d["W"].cpu(), tk.numpy(), rows, tau, dtype)
+    _abs(logp, o["logp"], "logp[K=%d]" % K)
+    _abs(ent, o["ent"], "ent")
+
+
+@pytest.mark.parametrize("case", CASES[1::3], ids=[_id(c) for c in CASES[1::3]])
+def test_support_forward_sweep(case):
+    T, H, V, dtype, tau, rows, seed = case
+    d = _scaled("fwd", T, H, V, dtype, tau, seed)
+    j = int(_extra(case, 2).integers(0, 4))
+    sup = workloads.support_words(T, V, j, seed % (2**31), targets=d["targets"].cpu().numpy())
+    ri = None if rows is None else torch.from_numpy(rows).cuda()
+    logp, ent = flp.logprob_entropy(d["h"], d["W"], d["targets"], ri, tau,
+                                    support=torch.from_numpy(sup).cuda())
+    torch.cuda.synchronize()
+    o = coracle.logprob_entropy_support(d["h"].cpu(), d["W"].cpu(), d["targets"].cpu().numpy(),
+                                        rows, sup, tau, dtype)
+    _abs(logp, o["logp"], "logp (support 2^-%d)" % j)
+    _abs(ent, o["ent"], "ent (support 2^-%d)" % j)
+
+
+@pytest.mark.parametrize("case", CASES[2::3], ids=[_id(c) for c in CASES[2::3]])
+def test_support_backward_sweep(case):
+    T, H, V, dtype, tau, rows, seed = case
+    d = _scaled("bwd", T, H, V, dtype, tau, seed)
+    j = int(_extra(case, 3).integers(0, 4))
+    sup = workloads.support_words(T, V, j, seed % (2**31), targets=d["targets"].cpu().numpy())
+    n = T if rows is None else len(rows)
+    g = np.random.Generator(np.random.PCG64([seed, 8]))
+    g1 = torch.from_numpy(g.standard_normal(n, dtype=np.float32)).cuda()
+    g2 = torch.from_numpy(g.standard_normal(n, dtype=np.float32)).cuda()
+    ri = None if rows is None else torch.from_numpy(rows).cuda()
+    dh, dW = flp.backward(d["h"], d["W"], d["targets"], ri, tau, g1, g2,
+                          support=torch.from_numpy(sup).cuda())
+    torch.cuda.synchronize()
+    dh_rows, ref_dW = coracle.backward_support(d["h"].cpu(), d["W"].cpu(),
+                                               d["targets"].cpu().numpy(), rows, sup, tau,
+                                               g1.cpu().numpy(), g2.cpu().numpy(), dtype)
+    ref_dh = coracle.scatter_rows(dh_rows, np.arange(T) if rows is None else rows, T)
+    _rel_or_zero(dh, ref_dh, "dh (support 2^-%d)" % j)
+    _rel_or_zero(dW, ref_dW, "dW (support 2^-%d)" % j)
+
+
+MX_CASES = [c for c in CASES if c[3] == "bf16"][::2]
+
+
+@pytest.mark.parametrize("case", MX_CASES, ids=[_id(c) for c in MX_CASES])
+def test_kl_mxfp4_sweep(case):
+    """The teacher head quantised to MXFP4 (bf16 workloads: the decoded
+    teacher weights meet bf16 hidden states in the MMA).  The MXFP4 layout
+    takes whole 64-wide column blocks, so H is rounded up to a multiple of
+    64."""
+    T, H, V, _, _, rows, seed = case
+    H = 64 * ((H + 63) // 64)
+    d = _scaled("kl", T, H, V, "bf16", 1.0, seed)
+    packed, scales = flp.mxfp4_quantize(d["W_t"])
+    ri = None if rows is None else torch.from_numpy(rows).cuda()
+    kl = flp.kl_divergence_mxfp4(d["h_s"], d["W_s"], d["h_t"], packed, scales, ri)
+    torch.cuda.synchronize()
+    want = coracle.kl_mxfp4(d["h_s"].cpu(), d["W_s"].cpu(), d["h_t"].cpu(),
+                            packed.cpu().numpy(), scales.cpu().numpy(), rows, "bf16")
+    _abs(kl, want, "kl (MXFP4 teacher)")
