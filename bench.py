@@ -276,11 +276,14 @@ def launches_per_call(d):
     if w.kind == "kl":
         return 2 * gather + 1
     # backward with the statistics supplied: per row chunk, the gradient pass
-    # and the dh and dW GEMMs
+    # and the dh and dW GEMMs, plus the sum of the dh GEMM's split tail tiles
+    # when its last wave is split (counted as planned for the first chunk)
     import entropy_tcgen05_vocab_gb300 as flp
     shape = flp.make_shape(w.T, w.H, w.V, d["n"], d["h"].dtype)
-    chunk = flp.plan(shape, flp.OP_BACKWARD, 1)["chunk_rows"]
-    return gather + 3 * len(flp.row_chunks(d["n"], chunk))
+    sms = torch.cuda.get_device_properties(d["h"].device).multi_processor_count
+    pl = flp.plan(shape, flp.OP_BACKWARD, sms)
+    per_chunk = 3 + (1 if pl["dh_split"] > 1 else 0)
+    return gather + per_chunk * len(flp.row_chunks(d["n"], pl["chunk_rows"]))
 
 
 def time_calls(fn, steps, device, warmup=3):

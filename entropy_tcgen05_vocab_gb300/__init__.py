@@ -54,7 +54,8 @@ class FlpPlan(ctypes.Structure):
                 ("cta_group", ctypes.c_int32), ("splits", ctypes.c_int32),
                 ("tiles_per_split", ctypes.c_int32), ("band", ctypes.c_int32),
                 ("items", ctypes.c_int32), ("grid", ctypes.c_int32),
-                ("max_tiles_per_cta", ctypes.c_int64), ("chunk_rows", ctypes.c_int64)]
+                ("max_tiles_per_cta", ctypes.c_int64), ("chunk_rows", ctypes.c_int64),
+                ("dh_split", ctypes.c_int32), ("dh_tail_tiles", ctypes.c_int32)]
 
 
 _lib = None

@@ -95,9 +95,28 @@ int64_t grad_chunk_rows(const flp_shape *s) {
 struct Layout {
   size_t status = 0, cnt = 0, cnt_bytes = 0, zt = 0, pm = 0, ps = 0, pb = 0, pc = 0, pm2 = 0,
          ps2 = 0;
-  size_t hs = 0, hs2 = 0, lse = 0, ez = 0, g = 0, rowcnt = 0, total = 0;
+  size_t hs = 0, hs2 = 0, lse = 0, ez = 0, g = 0, rowcnt = 0, part = 0, total = 0;
   int64_t grad_rows = 0;
+  int part_slots = 0;  // backward: 512 KB FP32 partial tiles of the dh GEMM's split tail
 };
+
+// Partial-tile slots the backward's workspace holds for the dh GEMM's split
+// tail: none if V is too short to split (fewer than two segments of
+// kDhSplitMinKb k-blocks), else as many as the chunk's tiles could use,
+// at most kDhSplitSlots.
+int dh_part_slots(const flp_shape *s, int64_t grad_rows) {
+  const int64_t kb = cdiv(s->V, 64);
+  if (kb < 2 * kDhSplitMinKb) return 0;
+  const int64_t tiles = dh_gemm_tiles(static_cast<int>(grad_rows), static_cast<int>(s->H));
+  return static_cast<int>(std::min<int64_t>(kDhSplitSlots, tiles * (kb / kDhSplitMinKb)));
+}
+
+// The dh GEMM's tail split is on unless FLP_DH_SPLIT=0 (a tuning knob, read
+// at each call).
+bool dh_split_enabled() {
+  const char *env = std::getenv("FLP_DH_SPLIT");
+  return !(env && env[0] == '0' && env[1] == '\0');
+}
 
 Layout layout_for(const flp_shape *s, flp_op op) {
   Layout L;
@@ -134,6 +153,8 @@ Layout layout_for(const flp_shape *s, flp_op op) {
     L.grad_rows = grad_chunk_rows(s);
     L.g = take(static_cast<size_t>(L.grad_rows) * static_cast<size_t>(cdiv(s->V, 8) * 8) * 2);
     L.rowcnt = take(static_cast<size_t>(s->T) * 4);  // scored rows per h row
+    L.part_slots = dh_part_slots(s, L.grad_rows);
+    L.part = take(static_cast<size_t>(L.part_slots) * kDhSlotBytes);
   }
   L.total = off;
   return L;
@@ -625,7 +646,10 @@ flp_status backward_impl(const flp_shape *s, const void *h, const void *W, const
       da.M = rc;
       da.N = static_cast<int>(s->H);
       da.K = static_cast<int>(s->V);
-      da.grid = gemm_cta_group() * std::min(dh_gemm_tiles(da.M, da.N), gemm_units(dev.sms));
+      const int units = gemm_units(dev.sms);
+      da.dh_split = dh_split_plan(da.M, da.N, da.K, units, dh_split_enabled() ? L.part_slots : 0);
+      da.part = at<float>(ws, L.part);
+      da.grid = gemm_cta_group() * std::min(da.dh_split.items, units);
       da.bf16 = ga.bf16;
       da.status = status;
       da.r0 = static_cast<int>(r0);
@@ -717,7 +741,17 @@ flp_status flp_plan_scoring(const flp_shape *shape, flp_op op, int32_t num_sms, 
   out->items = p.sch.items;
   out->grid = p.grid * cg;
   out->max_tiles_per_cta = p.max_load;
-  if (op == FLP_OP_BACKWARD) out->chunk_rows = grad_chunk_rows(shape);
+  out->dh_split = 1;
+  if (op == FLP_OP_BACKWARD) {
+    out->chunk_rows = grad_chunk_rows(shape);
+    // rows of the first chunk (the chunk rule of flp_row_chunks)
+    const int64_t first = cdiv(shape->n_rows, (shape->n_rows - 1) / out->chunk_rows + 1);
+    const DhSplit d = dh_split_plan(static_cast<int>(first), static_cast<int>(shape->H),
+                                    static_cast<int>(shape->V), std::max(1, num_sms / gemm_cta_group()),
+                                    dh_split_enabled() ? dh_part_slots(shape, out->chunk_rows) : 0);
+    out->dh_split = d.split;
+    out->dh_tail_tiles = d.split > 1 ? d.tail : 0;
+  }
   return FLP_OK;
 }
 

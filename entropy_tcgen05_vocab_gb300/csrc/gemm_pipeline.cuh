@@ -26,9 +26,35 @@ namespace flp {
 
 constexpr int kGemmBN = 256;
 
+// Work items: tiles [0, full_tiles) are computed whole and go through the
+// epilogue policy; each of the remaining tiles (the last, partial wave of a
+// persistent launch) is split into `split` K segments of kb_per_seg k-blocks,
+// one item each, whose FP32 partial tiles are stored to `part` (segment s of
+// tail tile j at slot j * split + s, (128 CG) x kTileN row-major floats) and
+// summed by a separate pass.  Without a split: full_tiles = tiles, split = 1.
 struct GemmShape {
   int M, N, K;
   int m_tiles, n_tiles, tiles, k_blocks;
+  int items, full_tiles, split, kb_per_seg;
+  float *part;
+
+  // Item `i` -> output tile, its k-block range [kb0, kb1), and the partial
+  // slot (-1: a whole tile).
+  __device__ __forceinline__ void item(int i, int &t, int &kb0, int &kb1, int &slot) const {
+    if (i < full_tiles) {
+      t = i;
+      kb0 = 0;
+      kb1 = k_blocks;
+      slot = -1;
+      return;
+    }
+    const int j = i - full_tiles;
+    const int seg = j % split;
+    t = full_tiles + j / split;
+    kb0 = seg * kb_per_seg;
+    kb1 = min(k_blocks, kb0 + kb_per_seg);
+    slot = j;
+  }
 };
 
 // WIDE = false: 256-column output tiles, double-buffered accumulators, 4
@@ -115,12 +141,14 @@ __global__ void __launch_bounds__(pipe_threads(GemmCfg<CG, WIDE>::kEpiw), 1)
     uint32_t armed = 0;
     bool ok = true;
     const uint32_t full_dst = kPair ? mapa_shared(smem_u32(full), 0) : smem_u32(full);
-    for (int t = unit; ok && t < g.tiles; t += num_units) {
+    for (int it = unit; ok && it < g.items; it += num_units) {
+      int t, kb0, kb1, slot;
+      g.item(it, t, kb0, kb1, slot);
       const int mt = t / g.n_tiles, nt = t - (t / g.n_tiles) * g.n_tiles;
       const int arow = mt * (kBM * CG) + static_cast<int>(rank) * kBM;   // M offset
       // N offset of this CTA's share of MMA op 0 (op k adds k * BN)
       const int bcol = nt * C::kTileN + static_cast<int>(rank) * L::kBRows;
-      for (int kb = 0; kb < g.k_blocks; ++kb) {
+      for (int kb = kb0; kb < kb1; ++kb) {
         if (lane == 0) ok = mbar_wait(&empty[stage], phase ^ 1u, abort_flag);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
@@ -179,13 +207,15 @@ __global__ void __launch_bounds__(pipe_threads(GemmCfg<CG, WIDE>::kEpiw), 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int t = unit; ok && t < g.tiles; t += num_units) {
+      for (int it = unit; ok && it < g.items; it += num_units) {
+        int t, kb0, kb1, slot;
+        g.item(it, t, kb0, kb1, slot);
         if (lane == 0) ok = mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * L::kAccCols);
-        for (int kb = 0; kb < g.k_blocks; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (lane == 0) ok = mbar_wait(&full[stage], phase, abort_flag);
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
@@ -203,9 +233,9 @@ __global__ void __launch_bounds__(pipe_threads(GemmCfg<CG, WIDE>::kEpiw), 1)
                 const uint64_t bd = B_MN ? sdesc_sw128(bo + kk * 2048, 8192, 1024)
                                          : sdesc_sw128(bo + kk * kUmmaK * 2, 16, 1024);
                 if (kPair)
-                  mma_f16_pair(d_tmem + op * BN, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                  mma_f16_pair(d_tmem + op * BN, ad, bd, idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
                 else
-                  mma_f16(d_tmem + op * BN, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                  mma_f16(d_tmem + op * BN, ad, bd, idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
               }
             }
             if (kPair)
@@ -252,15 +282,33 @@ __global__ void __launch_bounds__(pipe_threads(GemmCfg<CG, WIDE>::kEpiw), 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int t = unit; t < g.tiles; t += num_units) {
+    for (int it = unit; it < g.items; it += num_units) {
+      int t, kb0, kb1, slot;
+      g.item(it, t, kb0, kb1, slot);
       const int mt = t / g.n_tiles, nt = t - (t / g.n_tiles) * g.n_tiles;
       if (lane == 0) ok = mbar_wait(&tfull[acc], acc_phase, abort_flag);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      epi.tile(tmem_base + lane_off + static_cast<uint32_t>(acc * L::kAccCols),
-               mt * (kBM * CG) + static_cast<int>(rank) * kBM + lg * 32 + lane,
-               nt * C::kTileN + half * kWarpCols, kWarpCols);
+      const uint32_t taddr = tmem_base + lane_off + static_cast<uint32_t>(acc * L::kAccCols);
+      if (slot < 0) {
+        epi.tile(taddr, mt * (kBM * CG) + static_cast<int>(rank) * kBM + lg * 32 + lane,
+                 nt * C::kTileN + half * kWarpCols, kWarpCols);
+      } else {
+        // a K segment of a tail tile: the FP32 partial tile, row-major
+        float *prow = g.part + static_cast<size_t>(slot) * (kBM * CG) * C::kTileN +
+                      static_cast<size_t>(static_cast<int>(rank) * kBM + lg * 32 + lane) * C::kTileN +
+                      half * kWarpCols;
+#pragma unroll 1
+        for (int c = 0; c < kWarpCols / 32; ++c) {
+          float x[32];
+          tmem_ld32(taddr + c * 32, x);
+          float4 *d = reinterpret_cast<float4 *>(prow + c * 32);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            d[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+        }
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {

@@ -14,6 +14,8 @@
 //   3. dW (+)= G^T h[rows]      (tcgen05 GEMM, K = R, both operands MN-major).
 // With a sampling support, LSE and E_p[z'] are taken over the support (the
 // statistics pass restricts them the same way) and G is 0 off the support.
+#include <algorithm>
+
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -174,45 +176,104 @@ struct DhEpi {
   const Params p;
   __device__ __forceinline__ explicit DhEpi(const Params &pp) : p(pp) {}
 
-  __device__ __forceinline__ void tile(uint32_t taddr, int row, int col0, int ncols) {
+  // Destination of product row `row` (chunk-local): the dh row, whether it
+  // is valid, and whether that h row is scored more than once.
+  struct Dest {
+    uint16_t *drow;
+    bool valid, repeated;
+  };
+  __device__ __forceinline__ static Dest dest(const Params &p, int row) {
     bool valid = row < p.R;
     int64_t orig = 0;
     if (valid) {
       orig = p.row_idx ? p.row_idx[p.r0 + row] : p.r0 + row;
       valid = orig >= 0 && orig < p.T;
     }
-    // A row scored more than once gets the sum of its contributions: added
-    // with packed 16-bit atomics onto the zeroed dh row (in any chunk order).
     const bool repeated = valid && p.rowcnt && p.rowcnt[orig] > 1u;
-    uint16_t *drow = p.dh + (valid ? orig : 0) * p.ld;
+    return Dest{p.dh + (valid ? orig : 0) * p.ld, valid, repeated};
+  }
+
+  // Store 32 columns [col, col + 32) of one product row (those below H).
+  // A row scored more than once gets the sum of its contributions: added
+  // with packed 16-bit atomics onto the zeroed dh row (in any chunk order).
+  __device__ __forceinline__ static void store(const Params &p, const Dest &d, int col,
+                                               const float (&x)[32]) {
+    if (d.repeated) {
+      // H is a multiple of 8, so the valid columns of a chunk come in pairs
+#pragma unroll
+      for (int j = 0; j < 32; j += 2) {
+        if (col + j >= p.H) break;
+        if (p.bf16)
+          atomicAdd(reinterpret_cast<__nv_bfloat162 *>(d.drow + col + j),
+                    __floats2bfloat162_rn(x[j], x[j + 1]));
+        else
+          atomicAdd(reinterpret_cast<__half2 *>(d.drow + col + j), __floats2half2_rn(x[j], x[j + 1]));
+      }
+    } else if (col + 32 <= p.H) {
+      store32_16(d.drow + col, x, p.bf16);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (col + j < p.H) d.drow[col + j] = pack1(x[j], p.bf16);
+    }
+  }
+
+  __device__ __forceinline__ void tile(uint32_t taddr, int row, int col0, int ncols) {
+    const Dest d = dest(p, row);
 #pragma unroll 1
     for (int c = 0; c < ncols / 32; ++c) {
       const int col = col0 + c * 32;
       if (col >= p.H) break;
       float x[32];
       tmem_ld32(taddr + c * 32, x);
-      if (!valid) continue;
-      if (repeated) {
-        // H is a multiple of 8, so the valid columns of a chunk come in pairs
-#pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          if (col + j >= p.H) break;
-          if (p.bf16)
-            atomicAdd(reinterpret_cast<__nv_bfloat162 *>(drow + col + j),
-                      __floats2bfloat162_rn(x[j], x[j + 1]));
-          else
-            atomicAdd(reinterpret_cast<__half2 *>(drow + col + j), __floats2half2_rn(x[j], x[j + 1]));
-        }
-      } else if (col + 32 <= p.H) {
-        store32_16(drow + col, x, p.bf16);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (col + j < p.H) drow[col + j] = pack1(x[j], p.bf16);
-      }
+      if (d.valid) store(p, d, col, x);
     }
   }
 };
+
+// The tail tiles of the dh GEMM were split into K segments whose FP32
+// partial tiles sit in `part` (slot j * split + s for segment s of tail tile
+// j, tile_m x tile_n row-major).  One thread per (row, 32-column chunk) of
+// a tail tile adds the segments in order (so the result does not depend on
+// which CTA finished first) and stores the sum as DhEpi does.
+__global__ void __launch_bounds__(256) dh_tail_sum_kernel(const float *__restrict__ part,
+                                                           int tail_tiles, int split,
+                                                           int full_tiles, int n_tiles,
+                                                           int tile_m, int tile_n,
+                                                           DhEpi::Params p) {
+  const int chunks = tile_n / 32;
+  const int64_t total = static_cast<int64_t>(tail_tiles) * tile_m * chunks;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int c = static_cast<int>(i % chunks);
+    const int r = static_cast<int>((i / chunks) % tile_m);
+    const int j = static_cast<int>(i / (static_cast<int64_t>(chunks) * tile_m));
+    const int t = full_tiles + j;
+    const int mt = t / n_tiles, nt = t - (t / n_tiles) * n_tiles;
+    const int row = mt * tile_m + r;
+    const int col = nt * tile_n + c * 32;
+    if (row >= p.R || col >= p.H) continue;
+    const DhEpi::Dest d = DhEpi::dest(p, row);
+    if (!d.valid) continue;
+    float x[32];
+#pragma unroll
+    for (int q = 0; q < 32; ++q) x[q] = 0.f;
+    for (int sgm = 0; sgm < split; ++sgm) {
+      const float4 *src = reinterpret_cast<const float4 *>(
+          part + (static_cast<size_t>(j) * split + sgm) * tile_m * tile_n +
+          static_cast<size_t>(r) * tile_n + c * 32);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 v = __ldcg(src + q);
+        x[4 * q] += v.x;
+        x[4 * q + 1] += v.y;
+        x[4 * q + 2] += v.z;
+        x[4 * q + 3] += v.w;
+      }
+    }
+    DhEpi::store(p, d, col, x);
+  }
+}
 
 // ---------------------------------------------------------------- dW = G^T h
 struct DwEpi {
@@ -324,7 +385,34 @@ static GemmShape gemm_shape(int M, int N, int K, int tile_n) {
   g.n_tiles = (N + tile_n - 1) / tile_n;
   g.tiles = g.m_tiles * g.n_tiles;
   g.k_blocks = (K + kBK - 1) / kBK;
+  g.items = g.tiles;
+  g.full_tiles = g.tiles;
+  g.split = 1;
+  g.kb_per_seg = g.k_blocks;
+  g.part = nullptr;
   return g;
+}
+
+DhSplit dh_split_plan(int M, int N, int K, int units, int max_slots) {
+  const GemmShape g = gemm_shape(M, N, K, DhCfg::kTileN);
+  DhSplit d{g.tiles, g.tiles, 0, 1, g.k_blocks, g.tiles};
+  if (g.tiles <= 0 || units <= 0) return d;
+  const int rem = g.tiles % units;
+  // split only a last wave that leaves at least half of the pairs idle
+  if (rem == 0 || 2 * rem > units) return d;
+  int s = units / rem;
+  s = std::min(s, g.k_blocks / kDhSplitMinKb);
+  s = std::min(s, max_slots / rem);
+  if (s < 2) return d;
+  const int per = (g.k_blocks + s - 1) / s;
+  s = (g.k_blocks + per - 1) / per;  // every segment non-empty
+  if (s < 2) return d;
+  d.full_tiles = g.tiles - rem;
+  d.tail = rem;
+  d.split = s;
+  d.kb_per_seg = per;
+  d.items = d.full_tiles + rem * s;
+  return d;
 }
 
 int dh_gemm_tiles(int M, int N) { return gemm_shape(M, N, 1, DhCfg::kTileN).tiles; }
@@ -352,10 +440,29 @@ cudaError_t launch_dh_gemm(const GemmArgs &a, cudaStream_t stream) {
   p.dh = static_cast<uint16_t *>(a.dh);
   p.ld = a.ld_dh;
   p.bf16 = a.bf16;
+  GemmShape g = gemm_shape(a.M, a.N, a.K, DhCfg::kTileN);
+  const DhSplit &d = a.dh_split;
+  const bool split = d.split > 1;
+  if (split) {
+    if (!a.part || d.tiles != g.tiles || d.full_tiles + d.tail != g.tiles) return cudaErrorInvalidValue;
+    g.full_tiles = d.full_tiles;
+    g.split = d.split;
+    g.kb_per_seg = d.kb_per_seg;
+    g.items = d.items;
+    g.part = a.part;
+  }
   const uint32_t idesc = idesc_f16(a.bf16, kBM * kGemmCG, kGemmBN, false, true);
-  return launch_persistent(DH_KERNEL, a.grid, pipe_threads(DhCfg::kEpiw), DhCfg::L::kSmemBytes,
-                           kGemmCG, stream, a.tmA, a.tmB, gemm_shape(a.M, a.N, a.K, DhCfg::kTileN),
-                           idesc, p, a.status);
+  cudaError_t e = launch_persistent(DH_KERNEL, a.grid, pipe_threads(DhCfg::kEpiw),
+                                    DhCfg::L::kSmemBytes, kGemmCG, stream, a.tmA, a.tmB, g, idesc,
+                                    p, a.status);
+  if (e != cudaSuccess || !split) return e;
+  // add up the tail tiles' K segments and store them
+  const int tile_m = kBM * kGemmCG;
+  const int64_t threads = static_cast<int64_t>(d.tail) * tile_m * (DhCfg::kTileN / 32);
+  const int blocks = static_cast<int>(std::min<int64_t>((threads + 255) / 256, 4096));
+  dh_tail_sum_kernel<<<blocks, 256, 0, stream>>>(a.part, d.tail, d.split, d.full_tiles, g.n_tiles,
+                                                 tile_m, DhCfg::kTileN, p);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_count_rows(const int64_t *row_idx, int64_t n, int64_t T, uint32_t *cnt,

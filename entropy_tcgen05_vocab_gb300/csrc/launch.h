@@ -3,6 +3,7 @@
 // include/fusedlogp.h.
 #pragma once
 
+#include <cstddef>
 #include <cstdint>
 
 #include <cuda.h>
@@ -109,10 +110,33 @@ struct GradArgs {
   int64_t ld_support;
 };
 
+// The dh GEMM's split of its last, partial wave (see dh_split_plan).
+struct DhSplit {
+  int tiles;       // output tiles of the product
+  int full_tiles;  // tiles computed whole
+  int tail;        // tiles split along K (tiles - full_tiles)
+  int split;       // K segments per tail tile (1: no split)
+  int kb_per_seg;  // 64-wide k-blocks per segment
+  int items;       // work items of the persistent launch
+};
+// Minimum k-blocks per K segment, and the 512 KB partial-tile slots the
+// backward's workspace holds at most.
+constexpr int kDhSplitMinKb = 16;
+constexpr int kDhSplitSlots = 80;
+constexpr size_t kDhSlotBytes = static_cast<size_t>(256) * 512 * 4;
+
+// Plan of the dh GEMM (M x N output, K contraction) on `units` CTA pairs: if
+// its last wave would leave at least half of the pairs idle, its tiles are
+// each split into up to units / tail K segments of >= kDhSplitMinKb
+// k-blocks, using at most max_slots partial tiles.
+DhSplit dh_split_plan(int M, int N, int K, int units, int max_slots);
+
 struct GemmArgs {
   CUtensorMap tmA, tmB;
   int M, N, K;
   int grid;
+  DhSplit dh_split;  // dh GEMM only; split 1 (or zero-initialised) = no split
+  float *part;       // dh GEMM with a split: dh_split.tail * split slots of kDhSlotBytes
   bool bf16;
   uint32_t *status;
   // dh epilogue: row i of the product goes to dh[row_idx[r0 + i]]

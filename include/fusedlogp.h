@@ -103,8 +103,10 @@ typedef struct {
  * whether row_idx is given); it is about n_rows*H*2 bytes for the gathered
  * rows, plus O(n_rows * 64) bytes of per-row partial state, plus, for the
  * backward, one bounded chunk of the bf16/fp16 logit gradient (at most
- * 4 GiB; never a [T,V] buffer for the forward or KL) and 4*T bytes of
- * per-row counts.
+ * 4 GiB; never a [T,V] buffer for the forward or KL), 4*T bytes of per-row
+ * counts and at most 40 MiB of FP32 partial tiles for the dh GEMM (when
+ * the last wave of its output tiles would leave most CTA pairs idle, those
+ * tiles are split along V and their partial sums added in a fixed order).
  */
 size_t flp_workspace_size(const flp_shape *shape, flp_op op);
 
@@ -275,6 +277,8 @@ flp_status flp_kl_mxfp4(const flp_shape *shape, const void *h_s, const void *W_s
  * chunks of at most flp's chunk size (as many rows as keep the chunk's
  * logit gradient within 4 GiB; the environment variable FLP_GRAD_CHUNK_ROWS,
  * read at each call, can lower it); chunk lengths follow flp_row_chunks.
+ * FLP_DH_SPLIT=0 (read at each call) turns off the split of the dh GEMM's
+ * last wave (flp_plan's dh_split); the results agree to FP32 rounding.
  */
 flp_status flp_backward(const flp_shape *shape, const void *h, const void *W,
                         const int64_t *targets, const int64_t *row_idx,
@@ -388,6 +392,9 @@ typedef struct {
     int32_t grid;           /* persistent CTAs launched (a multiple of cta_group) */
     int64_t max_tiles_per_cta; /* load of the busiest CTA (pair), in block_m x block_n tiles */
     int64_t chunk_rows;     /* FLP_OP_BACKWARD: rows per logit-gradient chunk (else 0) */
+    int32_t dh_split;       /* FLP_OP_BACKWARD, first chunk: K segments into which each tile
+                               of the dh GEMM's last, partial wave is split (1: none) */
+    int32_t dh_tail_tiles;  /* FLP_OP_BACKWARD, first chunk: the tiles so split */
 } flp_plan;
 
 flp_status flp_plan_scoring(const flp_shape *shape, flp_op op, int32_t num_sms, flp_plan *out);

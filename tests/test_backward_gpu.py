@@ -107,6 +107,39 @@ def test_backward_several_row_chunks(monkeypatch):
     _rel(dW, ref_dW, "dW")
 
 
+@pytest.mark.parametrize("T,H,V", [
+    (600, 1024, 8192),    # 348 scored rows: 4 output tiles of dh, each in 8 K segments
+    (2000, 512, 4100),    # 1205 rows: 5 tiles in K segments of 17, 17, 17, 14 k-blocks
+])
+def test_backward_dh_split_tail(monkeypatch, T, H, V):
+    """When the dh GEMM's last wave of output tiles would leave most CTA
+    pairs idle, those tiles are split along V into K segments whose FP32
+    partials are added in a fixed order.  Against the oracle, against the
+    unsplit GEMM (FLP_DH_SPLIT=0), and bitwise across repeated calls."""
+    d = _case(T, H, V, seed=T + V)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    shape = flp.make_shape(T, H, V, d["n"], torch.bfloat16)
+    pl = flp.plan(shape, flp.OP_BACKWARD, sms)
+    assert pl["dh_split"] > 1 and pl["dh_tail_tiles"] > 0, pl
+    args = (d["h"], d["W"], d["targets"], d["row_idx"], d["tau"], d["g1"], d["g2"])
+    dh, dW = flp.backward(*args)
+    dh2, _ = flp.backward(*args)
+    monkeypatch.setenv("FLP_DH_SPLIT", "0")
+    assert flp.plan(shape, flp.OP_BACKWARD, sms)["dh_split"] == 1
+    dh_whole, dW_whole = flp.backward(*args)
+    torch.cuda.synchronize()
+    assert torch.equal(dh, dh2)
+    assert torch.equal(dW, dW_whole)          # the dW GEMM does not change
+    ref_dh, ref_dW = _oracle(d, "bf16")
+    _rel(dh, ref_dh, "dh (split tail)")
+    _rel(dh_whole, ref_dh, "dh (whole tiles)")
+    _rel(dW, ref_dW, "dW")
+    # the split changes only the FP32 summation order, so the two bf16
+    # results differ by at most an ulp or so of the largest element
+    diff = (dh.float() - dh_whole.float()).abs()
+    assert diff.max().item() <= 2.0 ** -7 * dh_whole.float().abs().max().item()
+
+
 @pytest.mark.parametrize("dtype,chunk", [("bf16", None), ("fp16", None), ("bf16", "128")])
 def test_backward_repeated_rows_sum_their_contributions(monkeypatch, dtype, chunk):
     """row_idx naming rows 2, 3 and 5 times, scattered through the list (and,
