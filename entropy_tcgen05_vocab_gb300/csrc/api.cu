@@ -82,7 +82,7 @@ int max_splits(int64_t V, int bn, int64_t n_rows, int bm) {
 // Rows of the backward's logit-gradient chunk: as many as fit in 4 GiB, or
 // fewer if FLP_GRAD_CHUNK_ROWS asks for it (a memory/tuning knob).
 int64_t grad_chunk_rows(const flp_shape *s) {
-  const int64_t ldg = cdiv(s->V, 8) * 8;
+  const int64_t ldg = cdiv(s->V, 16) * 16;
   int64_t r = kGradChunkBytes / (ldg * 2);
   r = std::max<int64_t>(128, r / 128 * 128);
   if (const char *env = std::getenv("FLP_GRAD_CHUNK_ROWS")) {
@@ -151,7 +151,7 @@ Layout layout_for(const flp_shape *s, flp_op op) {
     L.lse = take(n * 4);
     L.ez = take(n * 4);
     L.grad_rows = grad_chunk_rows(s);
-    L.g = take(static_cast<size_t>(L.grad_rows) * static_cast<size_t>(cdiv(s->V, 8) * 8) * 2);
+    L.g = take(static_cast<size_t>(L.grad_rows) * static_cast<size_t>(cdiv(s->V, 16) * 16) * 2);
     L.rowcnt = take(static_cast<size_t>(s->T) * 4);  // scored rows per h row
     L.part_slots = dh_part_slots(s, L.grad_rows);
     L.part = take(static_cast<size_t>(L.part_slots) * kDhSlotBytes);
@@ -604,7 +604,7 @@ flp_status backward_impl(const flp_shape *s, const void *h, const void *W, const
     ez = a.out_ez;
   }
 
-  const int64_t ldg = cdiv(s->V, 8) * 8;
+  const int64_t ldg = cdiv(s->V, 16) * 16;
   void *G = at<void>(ws, L.g);
   const int64_t n = s->n_rows;
   const int64_t num = (n - 1) / L.grad_rows + 1;

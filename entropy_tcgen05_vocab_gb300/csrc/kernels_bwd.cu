@@ -63,6 +63,30 @@ __device__ __forceinline__ void store32_16(void *dst, const float (&v)[32], bool
     d[q] = u;
   }
 }
+// One 256-bit global store (8 words; dst 32-byte aligned).  A warp whose
+// lanes each write a different row touches one line per lane per store, so
+// storing a row's 64 or 128 bytes in 32-byte pieces halves the store
+// instructions (and the lines the L1 processes) against 16-byte pieces.
+__device__ __forceinline__ void st_global_v8(void *dst, uint32_t a0, uint32_t a1, uint32_t a2,
+                                             uint32_t a3, uint32_t a4, uint32_t a5, uint32_t a6,
+                                             uint32_t a7) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(a0),
+               "r"(a1), "r"(a2), "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
+               : "memory");
+}
+
+// store32_16 with 32-byte stores (dst 32-byte aligned).
+__device__ __forceinline__ void store32_16_v8(void *dst, const float (&v)[32], bool bf16) {
+  uint8_t *d = static_cast<uint8_t *>(dst);
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const float *w = v + 16 * q;
+    st_global_v8(d + 32 * q, pack2(w[0], w[1], bf16), pack2(w[2], w[3], bf16),
+                 pack2(w[4], w[5], bf16), pack2(w[6], w[7], bf16), pack2(w[8], w[9], bf16),
+                 pack2(w[10], w[11], bf16), pack2(w[12], w[13], bf16), pack2(w[14], w[15], bf16));
+  }
+}
+
 // Scored rows per h row (row_idx may name a row more than once).
 __global__ void count_rows_kernel(const int64_t *__restrict__ row_idx, int64_t n, int64_t T,
                                   uint32_t *__restrict__ cnt) {
@@ -89,6 +113,7 @@ struct GradEpi {
     uint16_t *G;  // [n, ldg]
     int64_t ldg;
     bool bf16;
+    bool v8;      // G and its rows 32-byte aligned: 32-byte stores
     const uint32_t *support;  // SUP: [T, ld_support] words by h row
     int64_t ld_support;
     int tile_cols;            // columns from one tile() call of a warp to its next
@@ -148,7 +173,10 @@ struct GradEpi {
       }
       if (!valid) continue;
       if (cb + 32 <= p.V) {
-        store32_16(grow + cb, x, p.bf16);
+        if (p.v8)
+          store32_16_v8(grow + cb, x, p.bf16);
+        else
+          store32_16(grow + cb, x, p.bf16);
       } else {
         const int nv = p.V - cb;
 #pragma unroll
@@ -282,6 +310,7 @@ struct DwEpi {
     float *dW;
     int64_t ld;
     int accumulate;
+    bool v8;  // dW 32-byte aligned (its rows are, ld being a multiple of 8): 32-byte stores
   };
   const Params p;
   __device__ __forceinline__ explicit DwEpi(const Params &pp) : p(pp) {}
@@ -296,7 +325,15 @@ struct DwEpi {
       float x[32];
       tmem_ld32(taddr + c * 32, x);
       if (!valid) continue;
-      if (col + 32 <= p.H) {
+      if (col + 32 <= p.H && p.v8 && !p.accumulate) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float *w = x + 8 * q;
+          st_global_v8(drow + col + 8 * q, __float_as_uint(w[0]), __float_as_uint(w[1]),
+                       __float_as_uint(w[2]), __float_as_uint(w[3]), __float_as_uint(w[4]),
+                       __float_as_uint(w[5]), __float_as_uint(w[6]), __float_as_uint(w[7]));
+        }
+      } else if (col + 32 <= p.H) {
         float4 *d = reinterpret_cast<float4 *>(drow + col);
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
@@ -344,6 +381,7 @@ static cudaError_t launch_grad_t(const GradArgs &a, cudaStream_t stream) {
   p.G = static_cast<uint16_t *>(a.G);
   p.ldg = a.ldg;
   p.bf16 = a.bf16;
+  p.v8 = (reinterpret_cast<uintptr_t>(a.G) & 31u) == 0 && (a.ldg * 2) % 32 == 0;
   p.support = a.support;
   p.ld_support = a.ld_support;
   p.tile_cols = kGradTileCols;
@@ -482,6 +520,7 @@ cudaError_t launch_dw_gemm(const GemmArgs &a, cudaStream_t stream) {
   p.dW = a.dW;
   p.ld = a.ld_dw;
   p.accumulate = a.accumulate;
+  p.v8 = (reinterpret_cast<uintptr_t>(a.dW) & 31u) == 0 && (a.ld_dw * 4) % 32 == 0;
   const uint32_t idesc = idesc_f16(a.bf16, kBM * kGemmCG, kGemmBN, true, true);
   return launch_persistent(DW_KERNEL, a.grid, pipe_threads(DwCfg::kEpiw), DwCfg::L::kSmemBytes,
                            kGemmCG, stream, a.tmA, a.tmB, gemm_shape(a.M, a.N, a.K, DwCfg::kTileN),
