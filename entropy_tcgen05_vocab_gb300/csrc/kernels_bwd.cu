@@ -119,7 +119,10 @@ struct GradEpi {
     int tile_cols;            // columns from one tile() call of a warp to its next
   };
   const Params p;
-  float lse2, ez, a1, a2;
+  // G_v = a1 1[v = tgt] - p_v (a1 + a2 (z_v / tau - E z')), a1 = g1 / tau,
+  // a2 = g2 / tau, folded per row into -p_v (c1 z_v + c0) with
+  // c1 = a2 / tau and c0 = a1 - a2 E z' (z_v the raw FP32 logit).
+  float lse2, a1, c1, c0;
   int tgt;
   bool valid;
   uint16_t *grow;
@@ -130,15 +133,16 @@ struct GradEpi {
   __device__ __forceinline__ void begin(int /*mt*/, int row) {
     valid = row < p.n;
     tgt = -1;
-    lse2 = ez = a1 = a2 = 0.f;
+    lse2 = a1 = c1 = c0 = 0.f;
     grow = p.G + static_cast<int64_t>(valid ? row : 0) * p.ldg;
     if (SUP) sup.reset(nullptr, p.V);
     if (!valid) return;
     const int i = p.r0 + row;
     lse2 = p.lse[i] * kLog2eF;
-    ez = p.ez[i];
     a1 = p.g1[i] * p.inv_tau;
-    a2 = p.g2[i] * p.inv_tau;
+    const float a2 = p.g2[i] * p.inv_tau;
+    c1 = a2 * p.inv_tau;
+    c0 = fmaf(-a2, p.ez[i], a1);
     const int64_t r = p.row_idx ? p.row_idx[i] : i;
     if (r >= 0 && r < p.T) {
       const int64_t t = p.targets[r];
@@ -159,8 +163,7 @@ struct GradEpi {
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         const float pr = ex2(fmaf(x[j], p.sl, -lse2));
-        const float zp = x[j] * p.inv_tau;
-        x[j] = -pr * fmaf(a2, zp - ez, a1);
+        x[j] = -pr * fmaf(x[j], c1, c0);
       }
       const int rel = tgt - cb;
       if (static_cast<unsigned>(rel) < 32u) {
