@@ -75,6 +75,14 @@ __device__ __forceinline__ void st_global_v8(void *dst, uint32_t a0, uint32_t a1
                : "memory");
 }
 
+// One 256-bit global load (8 words; src 32-byte aligned).
+__device__ __forceinline__ void ld_global_v8(const void *src, uint32_t (&a)[8]) {
+  asm volatile("ld.global.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]),
+                 "=r"(a[6]), "=r"(a[7])
+               : "l"(src));
+}
+
 // store32_16 with 32-byte stores (dst 32-byte aligned).
 __device__ __forceinline__ void store32_16_v8(void *dst, const float (&v)[32], bool bf16) {
   uint8_t *d = static_cast<uint8_t *>(dst);
@@ -328,10 +336,18 @@ struct DwEpi {
       float x[32];
       tmem_ld32(taddr + c * 32, x);
       if (!valid) continue;
-      if (col + 32 <= p.H && p.v8 && !p.accumulate) {
+      if (col + 32 <= p.H && p.v8) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const float *w = x + 8 * q;
+          float w[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) w[e] = x[8 * q + e];
+          if (p.accumulate) {  // a later row chunk adds onto dW
+            uint32_t prev[8];
+            ld_global_v8(drow + col + 8 * q, prev);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) w[e] += __uint_as_float(prev[e]);
+          }
           st_global_v8(drow + col + 8 * q, __float_as_uint(w[0]), __float_as_uint(w[1]),
                        __float_as_uint(w[2]), __float_as_uint(w[3]), __float_as_uint(w[4]),
                        __float_as_uint(w[5]), __float_as_uint(w[6]), __float_as_uint(w[7]));
