@@ -284,3 +284,37 @@ def test_plain_c_caller_compiles_against_the_header(L, tmp_path):
                     os.path.join(ROOT, "tests", "c_caller", "flp_c_caller.c"),
                     "-o", str(tmp_path / "caller"), "-L", libdir, "-lfusedlogp",
                     "-L", cudalib, "-lcudart"], check=True)
+
+
+@pytest.mark.parametrize("sms,split,tail", [
+    (152, 9, 8),     # 312 dh tiles on 76 pairs: 304 whole, the last 8 in 9 K segments
+    (148, 4, 16),    # 74 pairs: 16 left over, at most 80 partial slots -> 4 segments
+    (200, 6, 12),    # 100 pairs: 12 left over -> 6 segments (80 slots)
+    (80, 1, 0),      # 40 pairs: a last wave of 32 is more than half full, no split
+])
+def test_dh_split_plan(L, monkeypatch, sms, split, tail):
+    """The dh GEMM's last, partial wave (workload 4: 9,843 scored rows, one
+    chunk, 39 x 8 output tiles of 256 x 512, K = V = 151,936) is split along
+    K when it would leave at least half of the CTA pairs idle, into as many
+    segments as idle pairs, partial-tile slots (80) and 16-k-block segments
+    allow."""
+    monkeypatch.delenv("FLP_DH_SPLIT", raising=False)
+    p = flp.plan(_shape(T=16384, H=4096, V=151936, n=9843), 2, sms)
+    assert p["chunk_rows"] == 9843
+    assert (p["dh_split"], p["dh_tail_tiles"]) == (split, tail)
+    assert tail * split <= 80 and tail * split <= sms // 2
+
+
+def test_dh_split_off_and_short_vocabularies(L, monkeypatch):
+    monkeypatch.delenv("FLP_DH_SPLIT", raising=False)
+    # V <= 1984: fewer than 32 k-blocks of 64, i.e. than two 16-k-block
+    # segments, so no split and no slots
+    short = _shape(T=300, H=256, V=1984, n=300)
+    assert flp.plan(short, 2, 152)["dh_split"] == 1
+    longer = _shape(T=300, H=256, V=3000, n=300)
+    assert flp.plan(longer, 2, 152)["dh_split"] == 2
+    assert L.flp_workspace_size(ctypes.byref(longer), 2) > L.flp_workspace_size(ctypes.byref(short), 2)
+    monkeypatch.setenv("FLP_DH_SPLIT", "0")
+    assert flp.plan(longer, 2, 152)["dh_split"] == 1
+    # the forward and the KL have no dh GEMM
+    assert flp.plan(longer, 0, 152)["dh_split"] == 1
