@@ -199,6 +199,11 @@ def max_over_ranks(x, world, device):
     return float(t.item())
 
 
+def compact(**kv):
+    """A workload's figures, rounded to 4 significant digits."""
+    return {k: (float("%.4g" % v) if isinstance(v, float) else v) for k, v in kv.items()}
+
+
 def job_throughput(units_per_rank, steps, ms_max, world):
     """Whole-job units/s: every rank scores its own replica; the job takes as
     long as its slowest rank."""
@@ -529,6 +534,7 @@ def run_ours(args):
         "memory": memory_footprint(flp, d, ws, device),
     }
 
+    configs = {}   # each extra workload's configuration, reported apart from its figures
     if not args.no_extra:
         extra = {}
         for wid in (2, 3, 4):
@@ -540,12 +546,13 @@ def run_ours(args):
                 tms, kms, _ = time_device(flp, dx, steps, 3, world, device)
                 tms = max_over_ranks(tms, world, device)
                 flx = flops_per_call(dx)
-                extra[dx["workload"].name] = {
-                    "config": describe(dx), "steps": steps, "scored_tokens_per_s": world * dx["n"] * steps / (tms / 1e3),
-                    "ms_per_step": tms / steps, "kernel_ms": kms,
-                    "tflops": flx / (tms / steps / 1e3) / 1e12,
-                    "pct_of_bf16_peak": 100 * flx / (tms / steps / 1e3) / 1e12 / P["bf16_tflops"],
-                    "algorithmic_flops_per_call": flx}
+                configs[dx["workload"].name] = dict(describe(dx), steps=steps,
+                                                    algorithmic_flops_per_call=flx)
+                extra[dx["workload"].name] = compact(
+                    n_rows=dx["n"], scored_tokens_per_s=world * dx["n"] * steps / (tms / 1e3),
+                    ms_per_step=tms / steps, kernel_ms=kms,
+                    tflops=flx / (tms / steps / 1e3) / 1e12,
+                    pct_of_bf16_peak=100 * flx / (tms / steps / 1e3) / 1e12 / P["bf16_tflops"])
                 del dx
             except Exception as e:  # a workload whose op is not available is reported, not fatal
                 extra[workloads.WORKLOADS[wid].name] = {"unavailable": str(e).splitlines()[0][:200]}
@@ -577,13 +584,12 @@ def run_ours(args):
                                 t_plain += t
                     t_var = max_over_ranks(t_var, world, device)
                     t_plain = max_over_ranks(t_plain, world, device)
-                    extra[name] = {
-                        "config": dict(describe(d), **note), "steps": 40,
-                        "scored_tokens_per_s": job_throughput(n, 40, t_var, world),
-                        "ms_per_step": t_var / 40,
-                        "tflops": fl / (t_var / 40 / 1e3) / 1e12,
-                        "pct_of_bf16_peak": 100 * fl / (t_var / 40 / 1e3) / 1e12 / P["bf16_tflops"],
-                        "plain_ms_per_step_same_clocks": t_plain / 40}
+                    configs[name] = dict(describe(d), steps=40, **note)
+                    extra[name] = compact(
+                        n_rows=n, scored_tokens_per_s=job_throughput(n, 40, t_var, world),
+                        ms_per_step=t_var / 40, tflops=fl / (t_var / 40 / 1e3) / 1e12,
+                        pct_of_bf16_peak=100 * fl / (t_var / 40 / 1e3) / 1e12 / P["bf16_tflops"],
+                        plain_ms_same_clocks=t_plain / 40)
                 except Exception as e:  # reported, not fatal
                     extra[name] = {"unavailable": str(e)[:200]}
 
@@ -629,19 +635,20 @@ def run_ours(args):
             t_mx = max_over_ranks(t_mx, world, device)
             t_bf = max_over_ranks(t_bf, world, device)
             flk = flops_per_call(dk)
-            extra[wk.name + "-mxfp4-teacher"] = {
-                "config": dict(describe(dk), teacher_head="MXFP4 (E2M1, E8M0 per 32), %.3f GB "
-                               "against %.3f GB in bf16" % (packed.numel() / 1e9 + scales.numel() / 1e9,
-                                                            wk.V * wk.H * 2 / 1e9)),
-                "steps": 20, "scored_tokens_per_s": job_throughput(dk["n"], 20, t_mx, world),
-                "ms_per_step": t_mx / 20, "tflops": flk / (t_mx / 20 / 1e3) / 1e12,
-                "pct_of_bf16_peak": 100 * flk / (t_mx / 20 / 1e3) / 1e12 / P["bf16_tflops"],
-                "bf16_teacher_ms_per_step_same_clocks": t_bf / 20}
+            configs[wk.name + "-mxfp4-teacher"] = dict(
+                describe(dk), steps=20,
+                teacher_head="MXFP4 (E2M1, E8M0 per 32), %.3f GB against %.3f GB in bf16"
+                             % (packed.numel() / 1e9 + scales.numel() / 1e9, wk.V * wk.H * 2 / 1e9))
+            extra[wk.name + "-mxfp4-teacher"] = compact(
+                n_rows=dk["n"], scored_tokens_per_s=job_throughput(dk["n"], 20, t_mx, world),
+                ms_per_step=t_mx / 20, tflops=flk / (t_mx / 20 / 1e3) / 1e12,
+                pct_of_bf16_peak=100 * flk / (t_mx / 20 / 1e3) / 1e12 / P["bf16_tflops"],
+                plain_ms_same_clocks=t_bf / 20)
             del dk, packed, scales, wsk
         except Exception as e:  # reported, not fatal
             extra[workloads.WORKLOADS[3].name + "-mxfp4-teacher"] = {"unavailable": str(e)[:200]}
         torch.cuda.empty_cache()
-        out["workloads"] = extra
+        out["workload_configs"] = configs
 
     if rank == 0 and world == 1 and not args.no_cpu:
         rate, k, dt, cores = cpu_oracle_rate(d, args.cpu_seconds)
@@ -657,6 +664,10 @@ def run_ours(args):
                           "on inputs decoded beforehand, %.1f s" % (nk, ndt)}
         except MemoryError as e:  # reported, not fatal
             out["cpu_baseline"]["numpy_blas"] = {"unavailable": str(e)[:200]}
+    if not args.no_extra:
+        # last on the line, short entries: the figures of every workload stay
+        # in view when only the end of the output is kept
+        out["workloads"] = extra
     if world > 1:
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()

@@ -24,7 +24,8 @@ from . import _build
 __all__ = ["lib", "build", "workspace_size", "logprob_entropy", "logprob_entropy_k",
            "kl_divergence", "backward", "pack_support", "mxfp4_quantize",
            "kl_divergence_mxfp4",
-           "read_device_status", "plan", "set_kernel_events", "row_chunks", "FusedLogProbEntropy", "FlpError",
+           "read_device_status", "plan", "set_kernel_events", "set_wait_limit", "row_chunks",
+           "FusedLogProbEntropy", "FlpError",
            "OP_LOGPROB_ENTROPY", "OP_KL", "OP_BACKWARD"]
 
 OP_LOGPROB_ENTROPY, OP_KL, OP_BACKWARD = 0, 1, 2
@@ -97,6 +98,8 @@ def lib():
     L.flp_selftest_wait_timeout.restype = ctypes.c_int
     L.flp_set_kernel_events.argtypes = [vp, vp]
     L.flp_set_kernel_events.restype = ctypes.c_int
+    L.flp_set_wait_limit.argtypes = [ctypes.c_uint64]
+    L.flp_set_wait_limit.restype = ctypes.c_int
     L.flp_logprob_entropy_support.argtypes = [shp, vp, vp, vp, vp, vp, i64, f32, vp, vp, vp, vp,
                                               vp, sz, vp]
     L.flp_logprob_entropy_support.restype = ctypes.c_int
@@ -156,6 +159,13 @@ def set_kernel_events(before, after):
     its tensor-core kernels (both must have been recorded once, so that they
     exist)."""
     lib().flp_set_kernel_events(ctypes.c_void_p(before.cuda_event), ctypes.c_void_p(after.cuda_event))
+
+
+def set_wait_limit(limit_ns):
+    """Wall-clock limit (ns) of the kernels' barrier waits for later calls from
+    this thread; 0 restores the default (4 s).  A wait that runs out ends its
+    kernel with a timeout counted in the call's device status."""
+    _check(lib().flp_set_wait_limit(int(limit_ns)))
 
 
 def selftest_wait_timeout(limit_ns, device=None):

@@ -23,6 +23,9 @@ namespace {
 
 thread_local char g_err[512] = "";
 thread_local cudaEvent_t g_ev_before = nullptr, g_ev_after = nullptr;
+// Limit of the kernels' barrier waits for calls from this thread (0: the
+// kernels' default); set by flp_set_wait_limit.
+thread_local uint64_t g_wait_ns = 0;
 
 // Records the measurement-hook events (if set) around the tensor-core work.
 struct KernelEvents {
@@ -55,6 +58,9 @@ constexpr size_t kStatusBytes = 256;
 constexpr int64_t kGradChunkBytes = int64_t(4) << 30;
 // L2 budget of one band's hidden rows.
 constexpr int64_t kBandBytes = int64_t(48) << 20;
+// Range of flp_set_wait_limit.
+constexpr uint64_t kMinWaitNs = 100;
+constexpr uint64_t kMaxWaitNs = 60000000000ull;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -118,8 +124,12 @@ bool dh_split_enabled() {
   return !(env && env[0] == '0' && env[1] == '\0');
 }
 
-Layout layout_for(const flp_shape *s, flp_op op) {
+// gather = false: the scoring or KL call scores rows 0..T-1 in place
+// (row_idx NULL) and needs no gathered rows; they are the layout's last
+// blocks for those ops, so the other offsets do not move.
+Layout layout_for(const flp_shape *s, flp_op op, bool gather = true) {
   Layout L;
+  if (op == FLP_OP_BACKWARD) gather = true;
   const size_t n = static_cast<size_t>(s->n_rows);
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -145,8 +155,10 @@ Layout layout_for(const flp_shape *s, flp_op op) {
   } else {
     L.zt = take(n * kMaxTargets * 4);  // raw target logits, up to kMaxTargets per row
   }
-  L.hs = take(n * static_cast<size_t>(s->H) * 2);
-  if (op == FLP_OP_KL) L.hs2 = take(n * static_cast<size_t>(s->H) * 2);
+  if (gather) {
+    L.hs = take(n * static_cast<size_t>(s->H) * 2);
+    if (op == FLP_OP_KL) L.hs2 = take(n * static_cast<size_t>(s->H) * 2);
+  }
   if (op == FLP_OP_BACKWARD) {
     L.lse = take(n * 4);
     L.ez = take(n * 4);
@@ -316,11 +328,12 @@ flp_status make_map(CUtensorMap *m, flp_dtype dt, const void *base, int64_t inne
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-flp_status check_common(const flp_shape *s, flp_op op, const void *ws, size_t ws_bytes) {
+flp_status check_common(const flp_shape *s, flp_op op, const void *ws, size_t ws_bytes,
+                        bool gather = true) {
   const char *why = nullptr;
   if (!shape_ok(s, &why)) return fail(FLP_ERR_INVALID_ARG, "%s", why);
   if (!ws) return fail(FLP_ERR_WORKSPACE, "workspace is NULL");
-  const size_t need = layout_for(s, op).total;
+  const size_t need = layout_for(s, op, gather).total;
   if (ws_bytes < need)
     return fail(FLP_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, need);
   if (reinterpret_cast<uintptr_t>(ws) % 256)
@@ -340,23 +353,59 @@ static_assert(FLP_NOALLOC_SCRATCH_BYTES % kAlign == 0, "scratch size");
 static __device__ __align__(256) unsigned char g_noalloc_scratch[FLP_NOALLOC_SCRATCH_BYTES];
 
 std::mutex g_scratch_mu;
-std::map<int, void *> g_scratch_addr;
+std::map<unsigned long long, void *> g_scratch_addr;  // by CUDA context id
 
-// Device address of the array on the current device; looked up once per
-// device with that device current.
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+
+// Id of the CUDA context current on this thread (unique for the life of the
+// process, so a context made after a reset gets a new one); false if there
+// is none yet or the driver does not provide the query.
+bool current_context_id(unsigned long long *id) {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  CUcontext ctx = nullptr;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of the array in the current device's context.  It is
+// looked up (cudaGetSymbolAddress, with that device current) once per
+// context: normally once per device, and again after the device's context
+// was reset, when the library's module is loaded anew and the array may sit
+// elsewhere.
 flp_status noalloc_scratch(void **out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  unsigned long long ctx = 0;
+  const bool keyed = current_context_id(&ctx);
   std::lock_guard<std::mutex> g(g_scratch_mu);
-  auto it = g_scratch_addr.find(dev);
-  if (it == g_scratch_addr.end()) {
-    void *p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
-    it = g_scratch_addr.emplace(dev, p).first;
+  if (keyed) {
+    auto it = g_scratch_addr.find(ctx);
+    if (it != g_scratch_addr.end()) {
+      *out = it->second;
+      return FLP_OK;
+    }
   }
-  *out = it->second;
+  void *p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+  // the look-up makes the device's context current if it was not yet
+  if (keyed || current_context_id(&ctx)) g_scratch_addr[ctx] = p;
+  *out = p;
   return FLP_OK;
 }
 
@@ -378,7 +427,7 @@ flp_status logprob_impl(const flp_shape *s, const void *h, const void *W, const 
                         flp_stream_t stream) {
   g_err[0] = 0;
   const KernelEvents ev;
-  flp_status st = check_common(s, FLP_OP_LOGPROB_ENTROPY, ws, ws_bytes);
+  flp_status st = check_common(s, FLP_OP_LOGPROB_ENTROPY, ws, ws_bytes, row_idx != nullptr);
   if (st != FLP_OK) return st;
   if (!(std::isfinite(temperature) && temperature > 0.f))
     return fail(FLP_ERR_INVALID_ARG, "temperature must be finite and > 0");
@@ -394,7 +443,7 @@ flp_status logprob_impl(const flp_shape *s, const void *h, const void *W, const 
   DeviceInfo dev;
   if ((st = device_info(&dev)) != FLP_OK) return st;
 
-  const Layout L = layout_for(s, FLP_OP_LOGPROB_ENTROPY);
+  const Layout L = layout_for(s, FLP_OP_LOGPROB_ENTROPY, row_idx != nullptr);
   // few rows: single CTAs on 128-row tiles (the workspace's partial slots
   // cover this plan too: twice the columns' worth of splits per row)
   const bool few = s->n_rows <= kSmallRows;
@@ -413,6 +462,7 @@ flp_status logprob_impl(const flp_shape *s, const void *h, const void *W, const 
   if ((st = make_map(&a.tmB, s->dtype, W, s->H, s->V, s->ld_w, 64, kFwdBN / cg)) != FLP_OK)
     return st;
   a.sch = p.sch;
+  a.sch.wait_ns = g_wait_ns;
   a.grid = p.grid * cg;
   a.bf16 = s->dtype == FLP_BF16;
   a.targets = targets;
@@ -454,7 +504,7 @@ flp_status kl_impl(const flp_shape *s, const void *h_s, const void *W_s, const v
                    const void *W_t, const MxOperand &mx, const int64_t *row_idx, float *out_kl,
                    void *ws, size_t ws_bytes, flp_stream_t stream) {
   const KernelEvents ev;
-  flp_status st = check_common(s, FLP_OP_KL, ws, ws_bytes);
+  flp_status st = check_common(s, FLP_OP_KL, ws, ws_bytes, row_idx != nullptr);
   if (st != FLP_OK) return st;
   if (s->n_rows == 0) return FLP_OK;
   if (!row_idx && s->n_rows != s->T)
@@ -466,7 +516,7 @@ flp_status kl_impl(const flp_shape *s, const void *h_s, const void *W_s, const v
   DeviceInfo dev;
   if ((st = device_info(&dev)) != FLP_OK) return st;
 
-  const Layout L = layout_for(s, FLP_OP_KL);
+  const Layout L = layout_for(s, FLP_OP_KL, row_idx != nullptr);
   const int units = mx.packed ? kl_mx_units(dev.sms) : kl_units(dev.sms);
   const Plan p = plan_cached(s->n_rows, s->V, s->H, kKlBN, units, 128 * kKlCG, 2);
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
@@ -487,6 +537,7 @@ flp_status kl_impl(const flp_shape *s, const void *h_s, const void *W_s, const v
     return st;
   a.mx = mx;
   a.sch = p.sch;
+  a.sch.wait_ns = g_wait_ns;
   a.grid = p.grid * kKlCG;
   a.bf16 = s->dtype == FLP_BF16;
   a.row_idx = row_idx;
@@ -581,6 +632,7 @@ flp_status backward_impl(const flp_shape *s, const void *h, const void *W, const
     if ((st = make_map(&a.tmB, s->dtype, W, s->H, s->V, s->ld_w, 64, kFwdBN / kFwdCG)) != FLP_OK)
       return st;
     a.sch = p.sch;
+    a.sch.wait_ns = g_wait_ns;
     a.grid = p.grid * kFwdCG;
     a.bf16 = s->dtype == FLP_BF16;
     a.targets = targets;
@@ -620,6 +672,7 @@ flp_status backward_impl(const flp_shape *s, const void *h, const void *W, const
     if ((st = make_map(&ga.tmB, s->dtype, W, s->H, s->V, s->ld_w, 64, kGradBN / kGradCG)) != FLP_OK)
       return st;
     ga.sch = p.sch;
+    ga.sch.wait_ns = g_wait_ns;
     ga.grid = p.grid * kGradCG;
     ga.bf16 = s->dtype == FLP_BF16;
     ga.r0 = static_cast<int>(r0);
@@ -658,6 +711,7 @@ flp_status backward_impl(const flp_shape *s, const void *h, const void *W, const
       da.rowcnt = rowcnt;
       da.dh = dh;
       da.ld_dh = s->ld_h;
+      da.wait_ns = g_wait_ns;
       if ((e = launch_dh_gemm(da, cs)) != cudaSuccess) return cuda_fail(e, "dh launch");
     }
     // 3. dW (+)= G^T h[rows]   (M = V, N = H, K = rc; both operands MN-major)
@@ -674,6 +728,7 @@ flp_status backward_impl(const flp_shape *s, const void *h, const void *W, const
       wa.dW = dW;
       wa.ld_dw = s->ld_w;
       wa.accumulate = r0 > 0;
+      wa.wait_ns = g_wait_ns;
       if ((e = launch_dw_gemm(wa, cs)) != cudaSuccess) return cuda_fail(e, "dW launch");
     }
   }
@@ -708,6 +763,16 @@ const char *flp_status_string(flp_status s) {
 }
 
 const char *flp_last_error(void) { return g_err; }
+
+flp_status flp_set_wait_limit(uint64_t limit_ns) {
+  g_err[0] = 0;
+  if (limit_ns != 0 && (limit_ns < kMinWaitNs || limit_ns > kMaxWaitNs))
+    return fail(FLP_ERR_INVALID_ARG, "limit_ns must be 0 or within %llu .. %llu",
+                static_cast<unsigned long long>(kMinWaitNs),
+                static_cast<unsigned long long>(kMaxWaitNs));
+  g_wait_ns = limit_ns;
+  return FLP_OK;
+}
 
 flp_status flp_set_kernel_events(void *before, void *after) {
   g_ev_before = static_cast<cudaEvent_t>(before);
@@ -901,7 +966,8 @@ flp_status flp_logprob_entropy_noalloc(const flp_shape *s, const void *h, const 
   g_err[0] = 0;
   const char *why = nullptr;
   if (!shape_ok(s, &why)) return fail(FLP_ERR_INVALID_ARG, "%s", why);
-  const size_t need = layout_for(s, FLP_OP_LOGPROB_ENTROPY).total;
+  // without row_idx no rows are gathered, so no room is needed for them
+  const size_t need = layout_for(s, FLP_OP_LOGPROB_ENTROPY, row_idx != nullptr).total;
   if (need > FLP_NOALLOC_SCRATCH_BYTES)
     return fail(FLP_ERR_WORKSPACE,
                 "problem needs %zu bytes of scratch; the static scratch holds %zu "

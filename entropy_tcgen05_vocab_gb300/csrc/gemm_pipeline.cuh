@@ -37,6 +37,7 @@ struct GemmShape {
   int m_tiles, n_tiles, tiles, k_blocks;
   int items, full_tiles, split, kb_per_seg;
   float *part;
+  unsigned long long wait_ns;  // limit of the main loops' barrier waits (0: the default)
 
   // Item `i` -> output tile, its k-block range [kb0, kb1), and the partial
   // slot (-1: a whole tile).
@@ -97,6 +98,8 @@ __global__ void __launch_bounds__(pipe_threads(GemmCfg<CG, WIDE>::kEpiw), 1)
   uint64_t *drain = tempty + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  // k-block iterations the peer's producer issued (written there at teardown)
+  volatile uint32_t *peer_issued = reinterpret_cast<volatile uint32_t *>(tmem_slot + 2);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -104,6 +107,8 @@ __global__ void __launch_bounds__(pipe_threads(GemmCfg<CG, WIDE>::kEpiw), 1)
   const bool leader = rank == 0;
   const int unit = blockIdx.x / CG;
   const int num_units = gridDim.x / CG;
+  const uint64_t lim = wait_limit(g.wait_ns);  // limit of the main loops' waits
+  uint32_t issued = 0;  // producer: k-block iterations whose copies were issued
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -116,6 +121,7 @@ __global__ void __launch_bounds__(pipe_threads(GemmCfg<CG, WIDE>::kEpiw), 1)
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
+    *peer_issued = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -138,7 +144,6 @@ __global__ void __launch_bounds__(pipe_threads(GemmCfg<CG, WIDE>::kEpiw), 1)
     // ------------------------------------------------------------ producer
     int stage = 0;
     uint32_t phase = 0;
-    uint32_t armed = 0;
     bool ok = true;
     const uint32_t full_dst = kPair ? mapa_shared(smem_u32(full), 0) : smem_u32(full);
     for (int it = unit; ok && it < g.items; it += num_units) {
@@ -149,7 +154,7 @@ __global__ void __launch_bounds__(pipe_threads(GemmCfg<CG, WIDE>::kEpiw), 1)
       // N offset of this CTA's share of MMA op 0 (op k adds k * BN)
       const int bcol = nt * C::kTileN + static_cast<int>(rank) * L::kBRows;
       for (int kb = kb0; kb < kb1; ++kb) {
-        if (lane == 0) ok = mbar_wait(&empty[stage], phase ^ 1u, abort_flag);
+        if (lane == 0) ok = mbar_wait(&empty[stage], phase ^ 1u, abort_flag, lim);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         if (lane == 0) {
@@ -181,24 +186,14 @@ __global__ void __launch_bounds__(pipe_threads(GemmCfg<CG, WIDE>::kEpiw), 1)
             }
           }
         }
-        armed |= 1u << stage;
+        ++issued;
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
         }
       }
     }
-    if (!ok && lane == 0) {
-      record_timeout<CG>(status, abort_flag);
-      if (leader) {
-        for (int s = 0; s < STAGES; ++s) {
-          if (!(armed & (1u << s))) continue;
-          const uint32_t par = (s < stage) ? phase : (phase ^ 1u);
-          int never = 0;
-          mbar_wait(&full[s], par, &never);
-        }
-      }
-    }
+    if (!ok && lane == 0) record_timeout<CG>(status, abort_flag);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (leader) {
@@ -210,13 +205,13 @@ __global__ void __launch_bounds__(pipe_threads(GemmCfg<CG, WIDE>::kEpiw), 1)
       for (int it = unit; ok && it < g.items; it += num_units) {
         int t, kb0, kb1, slot;
         g.item(it, t, kb0, kb1, slot);
-        if (lane == 0) ok = mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag);
+        if (lane == 0) ok = mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, lim);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * L::kAccCols);
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (lane == 0) ok = mbar_wait(&full[stage], phase, abort_flag);
+          if (lane == 0) ok = mbar_wait(&full[stage], phase, abort_flag, lim);
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
           tc_fence_after();
@@ -260,15 +255,7 @@ __global__ void __launch_bounds__(pipe_threads(GemmCfg<CG, WIDE>::kEpiw), 1)
         if (C::kNacc == 2) acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }
-      if (!ok && lane == 0) {
-        record_timeout<CG>(status, abort_flag);
-        if (kPair)
-          mma_commit_pair_local(drain);
-        else
-          mma_commit(drain);
-        int never = 0;
-        mbar_wait(drain, 0, &never);
-      }
+      if (!ok && lane == 0) record_timeout<CG>(status, abort_flag);
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -286,7 +273,7 @@ __global__ void __launch_bounds__(pipe_threads(GemmCfg<CG, WIDE>::kEpiw), 1)
       int t, kb0, kb1, slot;
       g.item(it, t, kb0, kb1, slot);
       const int mt = t / g.n_tiles, nt = t - (t / g.n_tiles) * g.n_tiles;
-      if (lane == 0) ok = mbar_wait(&tfull[acc], acc_phase, abort_flag);
+      if (lane == 0) ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, lim);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
@@ -323,12 +310,20 @@ __global__ void __launch_bounds__(pipe_threads(GemmCfg<CG, WIDE>::kEpiw), 1)
     if (!ok && lane == 0) record_timeout<CG>(status, abort_flag);
   }
 
-  tc_fence_before();
-  if (kPair)
-    cluster_sync();
-  else
-    __syncthreads();
-  tc_fence_after();
+  // Teardown, as in the vocabulary pipeline: in-flight copies and MMAs are
+  // drained after a wait gave up, before TMEM is freed and the CTAs exit.
+  if (kPair && warp == 0 && lane == 0 && !leader)
+    st_cluster_u32(mapa_shared(smem_u32(const_cast<uint32_t *>(peer_issued)), 0), issued);
+  pipe_sync<CG>();
+  if (*abort_flag) {
+    if (leader && lane == 0) {
+      if (warp == 0)
+        drain_copies<STAGES, CG>(full, issued, kPair ? *peer_issued : issued, L::kStageBytes);
+      else if (warp == 1)
+        drain_mmas<CG>(drain);
+    }
+    pipe_sync<CG>();
+  }
   if (warp == 1) tmem_dealloc<CG>(tmem_base, L::kTmemCols);
 }
 

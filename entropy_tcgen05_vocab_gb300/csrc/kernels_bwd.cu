@@ -447,6 +447,7 @@ static GemmShape gemm_shape(int M, int N, int K, int tile_n) {
   g.split = 1;
   g.kb_per_seg = g.k_blocks;
   g.part = nullptr;
+  g.wait_ns = 0;
   return g;
 }
 
@@ -508,6 +509,7 @@ cudaError_t launch_dh_gemm(const GemmArgs &a, cudaStream_t stream) {
     g.items = d.items;
     g.part = a.part;
   }
+  g.wait_ns = a.wait_ns;
   const uint32_t idesc = idesc_f16(a.bf16, kBM * kGemmCG, kGemmBN, false, true);
   cudaError_t e = launch_persistent(DH_KERNEL, a.grid, pipe_threads(DhCfg::kEpiw),
                                     DhCfg::L::kSmemBytes, kGemmCG, stream, a.tmA, a.tmB, g, idesc,
@@ -541,9 +543,10 @@ cudaError_t launch_dw_gemm(const GemmArgs &a, cudaStream_t stream) {
   p.accumulate = a.accumulate;
   p.v8 = (reinterpret_cast<uintptr_t>(a.dW) & 31u) == 0 && (a.ld_dw * 4) % 32 == 0;
   const uint32_t idesc = idesc_f16(a.bf16, kBM * kGemmCG, kGemmBN, true, true);
+  GemmShape g = gemm_shape(a.M, a.N, a.K, DwCfg::kTileN);
+  g.wait_ns = a.wait_ns;
   return launch_persistent(DW_KERNEL, a.grid, pipe_threads(DwCfg::kEpiw), DwCfg::L::kSmemBytes,
-                           kGemmCG, stream, a.tmA, a.tmB, gemm_shape(a.M, a.N, a.K, DwCfg::kTileN),
-                           idesc, p, a.status);
+                           kGemmCG, stream, a.tmA, a.tmB, g, idesc, p, a.status);
 }
 
 }  // namespace flp

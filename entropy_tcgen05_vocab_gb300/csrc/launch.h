@@ -150,6 +150,7 @@ struct GemmArgs {
   float *dW;
   int64_t ld_dw;
   int accumulate;
+  unsigned long long wait_ns;  // limit of the kernel's barrier waits (0: the default)
 };
 
 cudaError_t launch_gather(const void *h, int64_t ld_h, const int64_t *row_idx, int64_t n,

@@ -13,8 +13,14 @@
 
 namespace flp {
 
-// Wall-clock limit of one barrier wait.
+// Wall-clock limit of one barrier wait (the default; a call can lower it for
+// the waits of its kernels' main loops, see flp_set_wait_limit).
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
+
+// The limit a kernel uses: `ns`, or the default when `ns` is 0.
+__host__ __device__ __forceinline__ uint64_t wait_limit(uint64_t ns) {
+  return ns ? ns : kWaitLimitNs;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -58,6 +64,14 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// Counts `bytes` of the current phase's expected transaction bytes as
+// arrived without a copy (used to settle a phase whose copy was never issued).
+__device__ __forceinline__ void mbar_complete_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)),
                "r"(bytes)
                : "memory");
 }

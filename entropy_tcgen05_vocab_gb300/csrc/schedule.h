@@ -37,6 +37,7 @@ struct Schedule {
   int band;             // row tiles per band
   int items;            // row_tiles * splits
   int k_blocks;         // ceil(H / 64)
+  unsigned long long wait_ns;  // limit of the kernels' barrier waits (0: the default, 4 s)
 
   __host__ __device__ __forceinline__ void item(int L, int &mt, int &s, int &vt0,
                                                 int &vt1) const {

@@ -255,6 +255,62 @@ __device__ __forceinline__ void record_timeout(uint32_t *status, volatile int *a
   record_timeout<1>(status, abort_flag);
 }
 
+// Teardown after a wait gave up (the abort flag is set once every role has
+// left its loop).  The producers may have left operand copies in flight and
+// the MMA issuer MMAs that still read shared memory and write TMEM; both are
+// waited for before TMEM is freed and before a CTA exits.
+//
+// drain_copies runs in the thread that arms the "full" barriers (the
+// leader's producer lane).  `own` and `peer` are the k-block iterations the
+// leader's and (pair) the peer's producer issued.  Every iteration that may
+// still be in flight lies in the last STAGES of max(own, peer): a producer
+// issues iteration i only after the MMAs released iteration i - STAGES, so
+// neither runs more than STAGES ahead of the MMAs, and each of those stages
+// holds one of them.  In a pair the two producers may have stopped at
+// different iterations.  An iteration the leader never armed but the peer
+// issued is armed now for the peer's bytes alone; one the leader armed but
+// the peer never issued has the peer's missing bytes counted as arrived.
+// Then each phase completes once the copies really issued have landed.
+template <int STAGES, int CG>
+__device__ __forceinline__ void drain_copies(uint64_t *full, uint32_t own, uint32_t peer,
+                                             uint32_t cta_stage_bytes) {
+  const uint32_t hi = own > peer ? own : peer;
+  const uint32_t lo = hi > static_cast<uint32_t>(STAGES) ? hi - STAGES : 0u;
+  for (uint32_t i = lo; i < hi; ++i) {
+    uint64_t *bar = &full[i % STAGES];
+    if (CG == 2) {
+      if (i >= own)
+        mbar_arrive_expect_tx(bar, cta_stage_bytes);
+      else if (i >= peer)
+        mbar_complete_tx(bar, cta_stage_bytes);
+    }
+    int never = 0;
+    mbar_wait(bar, (i / STAGES) & 1u, &never);
+  }
+}
+
+// Run by the MMA-issuing thread: waits until every MMA it issued has
+// completed (a commit tracks all of the thread's earlier tcgen05 operations).
+template <int CG>
+__device__ __forceinline__ void drain_mmas(uint64_t *drain) {
+  if (CG == 2)
+    mma_commit_pair_local(drain);
+  else
+    mma_commit(drain);
+  int never = 0;
+  mbar_wait(drain, 0, &never);
+}
+
+template <int CG>
+__device__ __forceinline__ void pipe_sync() {
+  tc_fence_before();
+  if (CG == 2)
+    cluster_sync();
+  else
+    __syncthreads();
+  tc_fence_after();
+}
+
 // Epi must provide:
 //   struct Params;
 //   __device__ Epi(const Params&);
@@ -307,6 +363,8 @@ __global__ void __launch_bounds__(pipe_threads(EPIW, MX), 1)
   uint64_t *drain = tempty + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  // k-block iterations the peer's producer issued (written there at teardown)
+  volatile uint32_t *peer_issued = reinterpret_cast<volatile uint32_t *>(tmem_slot + 2);
   // MX barriers per decoded slot: "converted" (leader; one relay arrival per
   // CTA), "released" (the MMAs' commit), and this CTA's four decode warps done
   uint64_t *dfull = reinterpret_cast<uint64_t *>(smem + L::kRingBytes + L::kBarrierBytes);
@@ -322,6 +380,8 @@ __global__ void __launch_bounds__(pipe_threads(EPIW, MX), 1)
   const bool leader = rank == 0;
   const int unit = blockIdx.x / CG;          // CTA (pair) index
   const int num_units = gridDim.x / CG;
+  const uint64_t lim = wait_limit(sch.wait_ns);  // limit of the main loops' waits
+  uint32_t issued = 0;  // producer: k-block iterations whose copies were issued
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -342,6 +402,7 @@ __global__ void __launch_bounds__(pipe_threads(EPIW, MX), 1)
       for (int q = 0; q < L::kCvtWarps * L::kQStages; ++q) mbar_init(&qfull[q], 1);
     }
     *abort_flag = 0;
+    *peer_issued = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -368,7 +429,6 @@ __global__ void __launch_bounds__(pipe_threads(EPIW, MX), 1)
     // ------------------------------------------------------------ producer
     int stage = 0;
     uint32_t phase = 0;
-    uint32_t armed = 0;  // bit s: stage s has been armed at least once
     bool ok = true;
     // the pair's bytes all complete on the leader's "full" barriers
     const uint32_t full_dst = kPair ? mapa_shared(smem_u32(full), 0) : smem_u32(full);
@@ -379,7 +439,7 @@ __global__ void __launch_bounds__(pipe_threads(EPIW, MX), 1)
       for (int vt = vt0; ok && vt < vt1; ++vt) {
         const int brow = vt * L::kTileCols + static_cast<int>(rank) * L::kBRows;
         for (int kb = 0; kb < sch.k_blocks; ++kb) {
-          if (lane == 0) ok = mbar_wait(&empty[stage], phase ^ 1u, abort_flag);
+          if (lane == 0) ok = mbar_wait(&empty[stage], phase ^ 1u, abort_flag, lim);
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
           if (lane == 0) {
@@ -407,7 +467,7 @@ __global__ void __launch_bounds__(pipe_threads(EPIW, MX), 1)
               }
             }
           }
-          armed |= 1u << stage;
+          ++issued;
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -415,22 +475,7 @@ __global__ void __launch_bounds__(pipe_threads(EPIW, MX), 1)
         }
       }
     }
-    if (!ok) {
-      if (lane == 0) {
-        record_timeout<CG>(status, abort_flag);
-        if (leader) {
-          // Let the copies already in flight land before the CTA leaves.
-          for (int s = 0; s < STAGES; ++s) {
-            if (!(armed & (1u << s))) continue;
-            // Stage s was last armed in the current phase for stages behind
-            // `stage`, in the previous one otherwise.
-            const uint32_t par = (s < stage) ? phase : (phase ^ 1u);
-            int never = 0;
-            mbar_wait(&full[s], par, &never);
-          }
-        }
-      }
-    }
+    if (!ok && lane == 0) record_timeout<CG>(status, abort_flag);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (leader) {
@@ -444,7 +489,7 @@ __global__ void __launch_bounds__(pipe_threads(EPIW, MX), 1)
         int mt, sp, vt0, vt1;
         sch.item(it, mt, sp, vt0, vt1);
         for (int vt = vt0; ok && vt < vt1; ++vt) {
-          if (lane == 0) ok = mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag);
+          if (lane == 0) ok = mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, lim);
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
           tc_fence_after();
@@ -452,9 +497,9 @@ __global__ void __launch_bounds__(pipe_threads(EPIW, MX), 1)
           for (int kb = 0; kb < sch.k_blocks; ++kb) {
             const int dslot = static_cast<int>(g % L::kDMod);
             if (lane == 0) {
-              ok = mbar_wait(&full[stage], phase, abort_flag);
+              ok = mbar_wait(&full[stage], phase, abort_flag, lim);
               if (MX && ok)
-                ok = mbar_wait_cluster(&dfull[dslot], (g / L::kDMod) & 1u, abort_flag);
+                ok = mbar_wait_cluster(&dfull[dslot], (g / L::kDMod) & 1u, abort_flag, lim);
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
@@ -509,16 +554,7 @@ __global__ void __launch_bounds__(pipe_threads(EPIW, MX), 1)
           if (acc == 0) acc_phase ^= 1u;
         }
       }
-      if (!ok && lane == 0) {
-        record_timeout<CG>(status, abort_flag);
-        // Wait for the MMAs already issued before TMEM is released.
-        if (kPair)
-          mma_commit_pair_local(drain);
-        else
-          mma_commit(drain);
-        int never = 0;
-        mbar_wait(drain, 0, &never);
-      }
+      if (!ok && lane == 0) record_timeout<CG>(status, abort_flag);
     }
   } else if (MX && warp >= 2 + EPIW + L::kCvtWarps) {
     // ------------------------------------------------------------ MX relays
@@ -537,7 +573,7 @@ __global__ void __launch_bounds__(pipe_threads(EPIW, MX), 1)
       while (cur.valid) {
         const int d = static_cast<int>(g % L::kDMod);
         if (lane == 0) {
-          ok = mbar_wait(&ldec[d], (g / L::kDMod) & 1u, abort_flag);
+          ok = mbar_wait(&ldec[d], (g / L::kDMod) & 1u, abort_flag, lim);
           if (ok) {
             if (kPair)
               mbar_arrive_cluster(dfull_dst + d * 8);
@@ -598,9 +634,9 @@ __global__ void __launch_bounds__(pipe_threads(EPIW, MX), 1)
         const int d = static_cast<int>(g % L::kDMod);
         const int q = static_cast<int>(consumed % QS);
         // the MMAs are done with the decoded slot, and the codes have landed
-        if (lane == 0) ok = mbar_wait(&dempty[d], ((g / L::kDMod) & 1u) ^ 1u, abort_flag);
+        if (lane == 0) ok = mbar_wait(&dempty[d], ((g / L::kDMod) & 1u) ^ 1u, abort_flag, lim);
         ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (ok) ok = mbar_wait(&wfull[q], (consumed / QS) & 1u, abort_flag);
+        if (ok) ok = mbar_wait(&wfull[q], (consumed / QS) & 1u, abort_flag, lim);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;
@@ -647,7 +683,7 @@ __global__ void __launch_bounds__(pipe_threads(EPIW, MX), 1)
       const int row = mt * (kBM * CG) + static_cast<int>(rank) * kBM + lg * 32 + lane;
       epi.begin(mt, row);
       for (int vt = vt0; vt < vt1; ++vt) {
-        if (lane == 0) ok = mbar_wait(&tfull[acc], acc_phase, abort_flag);
+        if (lane == 0) ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, lim);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         tc_fence_after();
@@ -670,12 +706,22 @@ __global__ void __launch_bounds__(pipe_threads(EPIW, MX), 1)
     if (!ok && lane == 0) record_timeout<CG>(status, abort_flag);
   }
 
-  tc_fence_before();
-  if (kPair)
-    cluster_sync();
-  else
-    __syncthreads();
-  tc_fence_after();
+  // Teardown.  The peer's producer tells the leader how far it got; after
+  // the sync every role has left its loop and the abort flag (set in both
+  // CTAs of a pair by record_timeout) is final, so all threads of the pair
+  // take the same branch.
+  if (kPair && warp == 0 && lane == 0 && !leader)
+    st_cluster_u32(mapa_shared(smem_u32(const_cast<uint32_t *>(peer_issued)), 0), issued);
+  pipe_sync<CG>();
+  if (*abort_flag) {
+    if (leader && lane == 0) {
+      if (warp == 0)
+        drain_copies<STAGES, CG>(full, issued, kPair ? *peer_issued : issued, L::kStageBytes);
+      else if (warp == 1)
+        drain_mmas<CG>(drain);
+    }
+    pipe_sync<CG>();
+  }
   if (warp == 1) tmem_dealloc<CG>(tmem_base, L::kTmemCols);
 }
 

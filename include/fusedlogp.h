@@ -101,18 +101,26 @@ typedef struct {
  * Bytes of workspace `op` needs for `shape` (0 if the shape is invalid).
  * The size is a function of the shape alone (not of the device or of
  * whether row_idx is given); it is about n_rows*H*2 bytes for the gathered
- * rows, plus O(n_rows * 64) bytes of per-row partial state, plus, for the
- * backward, one bounded chunk of the bf16/fp16 logit gradient (at most
- * 4 GiB; never a [T,V] buffer for the forward or KL), 4*T bytes of per-row
- * counts and at most 40 MiB of FP32 partial tiles for the dh GEMM (when
- * the last wave of its output tiles would leave most CTA pairs idle, those
- * tiles are split along V and their partial sums added in a fixed order).
+ * rows (twice that for the KL's two heads), plus O(n_rows * 64) bytes of
+ * per-row partial state, plus, for the backward, one bounded chunk of the
+ * bf16/fp16 logit gradient (at most 4 GiB; never a [T,V] buffer for the
+ * forward or KL), 4*T bytes of per-row counts and at most 40 MiB of FP32
+ * partial tiles for the dh GEMM (when the last wave of its output tiles
+ * would leave most CTA pairs idle, those tiles are split along V and their
+ * partial sums added in a fixed order).
+ * The size returned is always enough.  The scoring and KL calls made with
+ * row_idx == NULL gather no rows and accept a workspace smaller by the
+ * gathered rows' bytes (n_rows*H*2 per head, rounded up to 1 KiB).
  */
 size_t flp_workspace_size(const flp_shape *shape, flp_op op);
 
 /*
  * Target log-probability and entropy of softmax(z / temperature) per
- * scored row, z = h[row] W^T.
+ * scored row, z = h[row] W^T (miles PR #2764 summary, "Implementation
+ * breakdown" items 2-3: each chunk of logits is upcast to FP32, divided by
+ * the temperature in FP32, and the log-prob and entropy are both taken from
+ * those values; miles PR #4645, "How it works": the output layer runs on the
+ * scored rows only, a tile at a time).
  *
  *   h            [T, ld_h] bf16/fp16 hidden states
  *   W            [V, ld_w] bf16/fp16 output-layer (LM head) weight
@@ -191,7 +199,10 @@ flp_status flp_pack_support(const uint8_t *mask, int64_t T, int64_t V, int64_t l
                             uint32_t *support, int64_t ld_support, flp_stream_t stream);
 
 /*
- * Full-vocabulary KL(teacher || student) per scored row:
+ * Full-vocabulary KL(teacher || student) per scored row (DeepSeek-V4 book
+ * ch. 19, "TileLang KL kernel": the exact KL over the whole vocabulary from
+ * the two heads' logits, rebuilt from the cached hidden states, in a static
+ * memory layout, with neither logit tensor in memory):
  *   KL = sum_v p_t,v (log p_t,v - log p_s,v),
  *   p_s = softmax(h_s[row] W_s^T),  p_t = softmax(h_t[row] W_t^T),
  * temperature 1, neither logit tensor materialised.  Student and teacher
@@ -257,7 +268,9 @@ flp_status flp_kl_mxfp4(const flp_shape *shape, const void *h_s, const void *W_s
 
 /*
  * Gradients of L = sum_i g1[i] logp_i + g2[i] ent_i (logp, ent as in
- * flp_logprob_entropy) by tile recompute:
+ * flp_logprob_entropy) by tile recompute (miles PR #4645, "How it works": the
+ * backward replays each logit tile instead of keeping the [tokens x vocab]
+ * logits or their gradient from the forward):
  *   G_iv = (g1[i] (1[v = tgt_i] - p_iv) - g2[i] p_iv (z'_iv - E_p[z'_i])) / temperature
  *   dh[row_idx[i], :] = sum_v G_iv W[v, :]      (dtype of h; rows not scored are 0)
  *   dW[v, :]          = sum_i G_iv h[row_idx[i], :]   (float32, overwritten)
@@ -323,21 +336,29 @@ flp_status flp_read_device_status(const void *workspace, flp_device_status *out,
  * FLP_NOALLOC_SCRATCH_BYTES (16 MiB), which every GPU that loads the library
  * holds until the process exits.
  *
- *   - A problem whose workspace (flp_workspace_size(shape,
- *     FLP_OP_LOGPROB_ENTROPY)) exceeds FLP_NOALLOC_SCRATCH_BYTES is rejected
- *     with FLP_ERR_WORKSPACE before anything is enqueued.  For example
- *     4,096 rows x H 4,096 x V 151,936 without row_idx fits; with row_idx the
- *     gathered rows alone need n_rows * H * 2 bytes.
+ *   - The scratch a problem needs is flp_workspace_size(shape,
+ *     FLP_OP_LOGPROB_ENTROPY) with row_idx given; with row_idx == NULL no
+ *     rows are gathered and the n_rows * H * 2 bytes of gathered rows are
+ *     not needed.  A problem that needs more than FLP_NOALLOC_SCRATCH_BYTES
+ *     is rejected with FLP_ERR_WORKSPACE before anything is enqueued.  For
+ *     example, 4,096 rows x H 4,096 x V 151,936 need 6.1 MiB without row_idx
+ *     and fit; with row_idx the gathered rows add 32 MiB and the call is
+ *     rejected (at that H and V, up to 1,718 gathered rows fit).
  *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     (cudaGetSymbolAddress) with that device current, and so does the first
+ *     call after the device's context was reset (the library's module, and
+ *     the array with it, is then loaded anew).  That first call may also be
+ *     the one that makes CUDA load the library's module, which places the
+ *     array in device memory.  Make it before any stream capture.
  *   - All calls in the process share the one array, and it keeps the last
  *     call's contents (the status words are cleared at the start of every
  *     call).  Calls whose GPU work overlaps -- on two streams, or from two
  *     host threads -- race on it and give wrong results: serialise them.
  *   - The device status counters of these calls live inside the shared
- *     array and are not exposed; a bad target or row still shows up as NaN
- *     in that row's outputs.
+ *     array and are not exposed.  A row_idx entry outside [0, T) gives NaN
+ *     in every output of that row; a target outside [0, V) gives NaN in that
+ *     row's out_logp only (its entropy, log-sum-exp and E[z'] stay finite),
+ *     so check out_logp to catch bad targets.
  */
 #define FLP_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 
@@ -365,6 +386,20 @@ flp_status flp_set_kernel_events(void *before, void *after);
  * that a stalled pipeline wait ends in a reported status, not a hung GPU.
  */
 flp_status flp_selftest_wait_timeout(uint64_t limit_ns, void *workspace, flp_stream_t stream);
+
+/*
+ * Lowers (or restores) the wall-clock limit of the barrier waits inside the
+ * kernels of later calls made from the calling host thread: 0 restores the
+ * default of 4 s; otherwise limit_ns must lie within 100 ns .. 60 s.  The
+ * setting stays until it is changed.  Every pipeline wait is bounded by
+ * this limit; a wait that runs out sets the pipeline's abort flag, lets the
+ * copies and tensor-core operations already in flight finish, frees its
+ * tensor memory, adds one to the `timeouts` counter of the call's device
+ * status and ends the kernel normally.  That call's outputs are then
+ * invalid, and the context stays usable.  The tests use a limit shorter
+ * than a pipeline stage to drive that path on purpose.
+ */
+flp_status flp_set_wait_limit(uint64_t limit_ns);
 
 /* Static description of a status code. */
 const char *flp_status_string(flp_status status);

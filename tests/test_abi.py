@@ -176,6 +176,54 @@ def test_selftest_limit_is_validated_on_host(L, limit):
     assert L.flp_selftest_wait_timeout(50_000_000, None, None) == 3
 
 
+@pytest.mark.parametrize("limit,ok", [(0, True), (99, False), (100, True), (60_000_000_000, True),
+                                      (60_000_000_001, False)])
+def test_wait_limit_is_validated_on_host(L, limit, ok):
+    try:
+        assert (L.flp_set_wait_limit(limit) == 0) == ok
+    finally:
+        assert L.flp_set_wait_limit(0) == 0
+
+
+def test_scoring_without_row_idx_needs_no_room_for_gathered_rows(L):
+    """The scoring and KL calls gather no rows when row_idx is NULL, so a
+    workspace smaller by the gathered rows' bytes passes the workspace check
+    (the call then fails later, on the device query, since there is no GPU
+    here); with row_idx the same workspace is rejected as too small."""
+    T, H, V = 4096, 4096, 151936
+    s = _shape(T=T, H=H, V=V, n=T)
+    for op, heads in ((0, 1), (1, 2)):
+        full = L.flp_workspace_size(ctypes.byref(s), op)
+        small = full - heads * T * H * 2
+        if op == 0:
+            assert _fwd(L, s, ws_bytes=small) != 3
+            assert _fwd(L, s, ws_bytes=small, row_idx=FAKE) == 3
+        else:
+            kl = lambda ri: L.flp_kl(ctypes.byref(s), FAKE, FAKE, FAKE, FAKE, ri, FAKE, FAKE,
+                                     small, None)
+            assert kl(None) != 3
+            assert kl(FAKE) == 3
+        assert L.flp_workspace_size(ctypes.byref(s), op) == full
+
+
+def test_noalloc_scratch_limit_on_host(L):
+    """flp_logprob_entropy_noalloc's 16 MiB static scratch holds the forward
+    of 4096 x 4096 x 151,936 without row_idx, and of up to 1,718 gathered
+    rows at that H and V; more gathered rows are rejected before any device
+    call."""
+    lim = 16 << 20
+    nofit = _shape(T=4096, H=4096, V=151936, n=1719)
+    assert L.flp_workspace_size(ctypes.byref(nofit), 0) > lim
+    fit = _shape(T=4096, H=4096, V=151936, n=1718)
+    assert L.flp_workspace_size(ctypes.byref(fit), 0) <= lim
+    call = lambda s, ri: L.flp_logprob_entropy_noalloc(ctypes.byref(s), FAKE, FAKE, FAKE, ri, 1.0,
+                                                       FAKE, FAKE, None, None, None)
+    assert call(nofit, FAKE) == 3
+    assert b"static scratch" in L.flp_last_error()
+    assert call(fit, FAKE) != 3                              # fails later: no GPU here
+    assert call(_shape(T=4096, H=4096, V=151936, n=4096), None) != 3
+
+
 def test_support_entry_points_validate_on_host(L):
     s = _shape()                       # V = 8192: 256 words per row
     sup = ctypes.c_void_p(1 << 21)

@@ -5,12 +5,14 @@ Tolerance (per tensor): ||d - ref||_F <= 1e-2 ||ref||_F, and every element
 within 1e-2 max|ref|.  Small cases compare dh and dW in full, across several
 row and vocabulary tiles, ragged hidden and vocabulary sizes, fp16, several
 row chunks and caller-supplied statistics.  At the full backward workload
-(16,384 rows, 60 % scored, H 4096, V 151,936) dh is compared on 512 sampled
-rows and the rows with the most negative log-probs,
-dW is checked through a property that holds at any size (its columns sum to
-zero because every row of G sums to zero), and dW is compared exactly on
-256 sampled vocabulary rows (plus target rows and the last row) at the same
-H and V with fewer scored rows.
+(16,384 rows, 60 % scored, H 4096, V 151,936) the oracle first computes
+every scored row's statistics (log-sum-exp and E[z'], a float64 pass over
+the whole vocabulary, which every element of dW depends on); then dh is
+compared on 512 sampled rows and the rows with the most negative log-probs,
+and dW element by element on 256 sampled vocabulary rows plus the targets of
+those worst rows and the last row.  dW is also checked through a property
+that holds at any size (its columns sum to zero because every row of G sums
+to zero).
 """
 import os
 
@@ -232,19 +234,30 @@ def test_autograd_function_matches_backward():
 def test_backward_workload_full_size():
     d = workloads.make(4, device="cuda")
     dh, dW = flp.backward(d["h"], d["W"], d["targets"], d["row_idx"], d["tau"], d["g1"], d["g2"])
+    logp, _, lse, ez = flp.logprob_entropy(d["h"], d["W"], d["targets"], d["row_idx"], d["tau"],
+                                           return_stats=True)
     torch.cuda.synchronize()
     n = d["n"]
     rows = d["row_idx"].cpu().numpy()
-    # dh on 512 sampled scored rows and the 8 with the most negative log-prob
-    # (each needs only its own row statistics)
-    logp, _ = flp.logprob_entropy(d["h"], d["W"], d["targets"], d["row_idx"], d["tau"])
+    tg = d["targets"].cpu().numpy()
+    # every scored row's statistics in float64 (dW[v] sums over all of them);
+    # the kernels' own statistics are checked against them on the way
+    hd, Wd = ref.decode(d["h"].cpu(), "bf16"), ref.decode(d["W"].cpu(), "bf16")
+    lse_ref, ez_ref = ref.row_stats(hd, Wd, rows, d["tau"])
+    del hd, Wd
+    assert np.abs(lse.cpu().double().numpy() - lse_ref).max() <= 1e-3
+    assert np.abs(ez.cpu().double().numpy() - ez_ref).max() <= 1e-3
+    # dh on 512 sampled scored rows and the 8 with the most negative log-prob;
+    # dW on 256 sampled vocabulary rows, those rows' targets and the last row
     worst = np.argsort(logp.cpu().numpy())[:8]
     sel = np.unique(np.concatenate([workloads.sample_rows(n, 512, seed=4), worst]))
-    want, _ = ref.backward(d["h"].cpu(), d["W"].cpu(), d["targets"].cpu().numpy(), rows, d["tau"],
-                           d["g1"].cpu().numpy(), d["g2"].cpu().numpy(), "bf16",
-                           dh_rows_sel=sel, vsel=np.zeros(0, np.int64),
-                           stats=(np.zeros(n), np.zeros(n)))
-    _rel(dh[torch.from_numpy(rows[sel]).cuda()], want, "dh (sampled rows)")
+    vsel = np.unique(np.concatenate([workloads.sample_rows(d["workload"].V, 256, seed=44),
+                                     tg[rows[worst]], [d["workload"].V - 1]]))
+    want_dh, want_dW = ref.backward(d["h"].cpu(), d["W"].cpu(), tg, rows, d["tau"],
+                                    d["g1"].cpu().numpy(), d["g2"].cpu().numpy(), "bf16",
+                                    dh_rows_sel=sel, vsel=vsel, stats=(lse_ref, ez_ref))
+    _rel(dh[torch.from_numpy(rows[sel]).cuda()], want_dh, "dh (sampled rows)")
+    _rel(dW[torch.from_numpy(vsel).cuda()], want_dW, "dW (sampled vocabulary rows)")
     # unscored rows are zero
     scored = torch.zeros(d["h"].shape[0], dtype=torch.bool, device="cuda")
     scored[d["row_idx"]] = True
