@@ -53,7 +53,11 @@ def test_normal_calls_report_no_timeouts():
                                           "empty_supports": 0}
 
 
-SHORT_NS = 1000     # 1 us: less than one tile of MMAs at these sizes
+SHORT_NS = 1000     # 1 us
+# H = 2048 (32 k-blocks): a CTA's first accumulator tile takes well over
+# 1 us of MMAs whatever the granularity of the GPU's global timer, so the
+# epilogue's wait for it runs out in every pipeline.
+ABORT_H = 2048
 
 
 class _ShortWaits:
@@ -71,6 +75,10 @@ def _ws(T, H, V, n, op):
     return torch.empty(flp.workspace_size(shape, op), dtype=torch.uint8, device="cuda")
 
 
+def _fwd_case():
+    return workloads.make(workloads.WORKLOADS[0].scaled(H=ABORT_H), device="cuda")
+
+
 def _forward_matches_oracle(d, rows=None):
     logp, ent = flp.logprob_entropy(d["h"], d["W"], d["targets"], rows, 1.0)
     o = coracle.logprob_entropy(d["h"].cpu(), d["W"].cpu(), d["targets"].cpu(),
@@ -81,9 +89,9 @@ def _forward_matches_oracle(d, rows=None):
 
 @pytest.mark.parametrize("n", [256, 100])       # CTA pairs; the single-CTA few-rows path
 def test_forward_pipeline_wait_that_runs_out_unwinds(n):
-    d = workloads.make(0, device="cuda")
+    d = _fwd_case()
     rows = None if n == 256 else torch.arange(n, device="cuda") * 2
-    ws = _ws(256, 512, 8192, n, flp.OP_LOGPROB_ENTROPY)
+    ws = _ws(256, ABORT_H, 8192, n, flp.OP_LOGPROB_ENTROPY)
     with _ShortWaits():
         flp.logprob_entropy(d["h"], d["W"], d["targets"], rows, 1.0, workspace=ws)
         st = flp.read_device_status(ws)
@@ -96,8 +104,9 @@ def test_forward_pipeline_wait_that_runs_out_unwinds(n):
 
 @pytest.mark.parametrize("teacher", ["bf16", "mxfp4"])
 def test_kl_pipeline_wait_that_runs_out_unwinds(teacher):
-    k = workloads.make(workloads.WORKLOADS[3].scaled(T=256, H=512, V=8192, seed=5), device="cuda")
-    ws = _ws(256, 512, 8192, 256, flp.OP_KL)
+    k = workloads.make(workloads.WORKLOADS[3].scaled(T=256, H=ABORT_H, V=8192, seed=5),
+                       device="cuda")
+    ws = _ws(256, ABORT_H, 8192, 256, flp.OP_KL)
     if teacher == "mxfp4":
         packed, scales = flp.mxfp4_quantize(k["W_t"])
         run = lambda: flp.kl_divergence_mxfp4(k["h_s"], k["W_s"], k["h_t"], packed, scales,
@@ -120,8 +129,9 @@ def test_kl_pipeline_wait_that_runs_out_unwinds(teacher):
 def test_backward_pipelines_wait_that_runs_out_unwinds():
     """The statistics pass, the gradient pass and the dh and dW GEMMs all run
     with 1 us waits; each gives up and unwinds."""
-    b = workloads.make(workloads.WORKLOADS[4].scaled(T=200, H=128, V=3000, seed=6), device="cuda")
-    shape = flp.make_shape(200, 128, 3000, b["n"], torch.bfloat16)
+    b = workloads.make(workloads.WORKLOADS[4].scaled(T=300, H=ABORT_H, V=4000, seed=6),
+                       device="cuda")
+    shape = flp.make_shape(300, ABORT_H, 4000, b["n"], torch.bfloat16)
     ws = torch.empty(flp.workspace_size(shape, flp.OP_BACKWARD), dtype=torch.uint8,
                      device="cuda")
     args = (b["h"], b["W"], b["targets"], b["row_idx"], b["tau"], b["g1"], b["g2"])
