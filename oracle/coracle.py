@@ -39,6 +39,13 @@ def lib():
         _lib.orc_mxfp4_dequantize.argtypes = [vp, vp, i64, i64, i64, vp]
         _lib.orc_kl_mxfp4.argtypes = [i64, i64, vp, vp, vp, vp, vp, i64, ip, i64, i64, vp, i64, vp]
         _lib.orc_kl_mxfp4.restype = ip
+        _lib.orc_mxfp8_quantize.argtypes = [vp, ip, i64, i64, i64, vp, vp]
+        _lib.orc_mxfp8_quantize.restype = ip
+        _lib.orc_mxfp8_dequantize.argtypes = [vp, vp, i64, i64, vp]
+        _lib.orc_e4m3_value.argtypes = [ip]
+        _lib.orc_e4m3_value.restype = dbl
+        _lib.orc_kl_mx.argtypes = [i64, i64, vp, vp, vp, vp, vp, i64, ip, i64, i64, vp, i64, vp]
+        _lib.orc_kl_mx.restype = ip
         _lib.orc_num_threads.restype = ip
         for f in (_lib.orc_logprob_entropy, _lib.orc_kl, _lib.orc_backward):
             f.restype = ip
@@ -274,4 +281,50 @@ def kl_mxfp4(h_s, W_s, h_t, packed, scales, rows, dtype):
                             ldw, _ptr(rows), rows.shape[0], out.ctypes.data)
     if rc:
         raise RuntimeError("oracle kl_mxfp4 failed: %d" % rc)
+    return out
+
+
+def e4m3_value(code):
+    """Value of one E4M3 code (0..255) by the C oracle's decoder."""
+    return float(lib().orc_e4m3_value(int(code)))
+
+
+def mxfp8_quantize(X, dtype):
+    """C quantiser: (codes uint8 [R, H] E4M3, scales uint8 [R, H/32] E8M0)."""
+    xs, xt, ld = storage(X, dtype)
+    R, H = xs.shape[0], ld
+    codes = np.empty((R, H), np.uint8)
+    scales = np.empty((R, H // 32), np.uint8)
+    rc = lib().orc_mxfp8_quantize(xs.ctypes.data, xt, R, H, ld, codes.ctypes.data,
+                                  scales.ctypes.data)
+    if rc:
+        raise ValueError("H must be a multiple of 32")
+    return codes, scales
+
+
+def mxfp8_dequantize(codes, scales):
+    codes = np.ascontiguousarray(codes, np.uint8)
+    scales = np.ascontiguousarray(scales, np.uint8)
+    R, H = codes.shape
+    out = np.empty((R, H))
+    lib().orc_mxfp8_dequantize(codes.ctypes.data, scales.ctypes.data, R, H, out.ctypes.data)
+    return out
+
+
+def kl_mx(h_s, W_s, h_t, packed, scales, rows, dtype):
+    """Per scored row KL(teacher || student) on the block-scaled teacher path:
+    h_t rows quantised to MXFP8, the teacher head in MXFP4 (blocked layout)."""
+    a, ty, ldh = storage(h_s, dtype)
+    b, _, ldw = storage(W_s, dtype)
+    c, _, _ = storage(h_t, dtype)
+    packed = np.ascontiguousarray(packed, np.uint8)
+    scales = np.ascontiguousarray(scales, np.uint8)
+    T, V = a.shape[0], b.shape[0]
+    rows = _i64(rows if rows is not None else np.arange(T))
+    out = np.empty(rows.shape[0], dtype=np.float64)
+    rc = lib().orc_kl_mx(ldh, V, a.ctypes.data, b.ctypes.data, c.ctypes.data,
+                         packed.ctypes.data, scales.ctypes.data, packed.shape[1], ty, ldh, ldw,
+                         _ptr(rows), rows.shape[0], out.ctypes.data)
+    if rc:
+        raise RuntimeError("oracle kl_mx failed: %d" % rc)
     return out

@@ -677,3 +677,137 @@ int orc_kl_mxfp4(int64_t H, int64_t V,
     free(hds); free(hdt); free(zs); free(zt);
     return 0;
 }
+
+
+/*
+ * OCP Microscaling MXFP8 with E4M3 elements: the format the teacher hidden
+ * states take on the block-scaled tensor-core path, beside the MXFP4
+ * teacher head (DeepSeek-V4 book ch. 19, "1. FP4 in OPD": the teacher's
+ * inference-only forward runs in native low precision; the block-scaled
+ * MMA needs both of its operands in a microscaling format).
+ *   E4M3: 1 sign, 4 exponent bits (bias 7), 3 mantissa bits.  Exponent field
+ *   0 is subnormal: (m / 8) 2^-6.  Codes 0x7F and 0xFF are NaN, so the
+ *   largest finite value is 0x7E = 1.75 * 2^8 = 448.
+ * Per 32 consecutive elements x_0..x_31 of a row:
+ *   scale code = floor(log2(max |x_i|)) - 8 + 127 (8 = exponent of 448),
+ *                clamped to [0, 254]; all-zero block: code 0
+ *   element    = the finite E4M3 value nearest to x_i / 2^(code - 127), ties
+ *                to the even code (mantissa bit 0 clear), magnitudes above 448
+ *                saturated to 448; a zero result is stored as +0 (code 0).
+ */
+static double orc_e4m3(int c)
+{
+    int e = (c >> 3) & 15, m = c & 7;
+    double v = e ? ldexp(1.0 + m / 8.0, e - 7) : ldexp(m / 8.0, -6);
+    if ((c & 0x7F) == 0x7F) return NAN;
+    return (c & 0x80) ? -v : v;
+}
+
+double orc_e4m3_value(int code) { return orc_e4m3(code & 0xFF); }
+
+/* One block of 32 values -> 32 E4M3 codes and the scale code. */
+static void orc_mxfp8_block(const double *x, uint8_t *codes, uint8_t *scale)
+{
+    double amax = 0.0, unit;
+    int code = 0, fe, i;
+    for (i = 0; i < 32; ++i)
+        if (fabs(x[i]) > amax) amax = fabs(x[i]);
+    if (amax > 0.0) {
+        frexp(amax, &fe);                  /* amax = f 2^fe, f in [0.5, 1) */
+        code = (fe - 1) - 8 + 127;
+        if (code < 0) code = 0;
+        if (code > 254) code = 254;
+    }
+    *scale = (uint8_t)code;
+    unit = ldexp(1.0, code - 127);
+    for (i = 0; i < 32; ++i) {
+        double a = fabs(x[i]) / unit, best = 1e300;
+        int c, q = 0;
+        for (c = 0; c <= 0x7E; ++c) {     /* nearest finite magnitude, ties to the even code */
+            double d = fabs(a - orc_e4m3(c));
+            if (d < best || (d == best && (c % 2) == 0)) { best = d; q = c; }
+        }
+        if (a > 448.0) q = 0x7E;
+        if (q != 0 && x[i] < 0) q |= 0x80;
+        codes[i] = (uint8_t)q;
+    }
+}
+
+/*
+ * MXFP8 quantisation of X [R, H] (bf16/fp16/f64, row stride ld), H a
+ * multiple of 32: codes [R, H] row-major, scales [R, H / 32].
+ */
+int orc_mxfp8_quantize(const void *X, int xtype, int64_t R, int64_t H, int64_t ld,
+                       uint8_t *codes, uint8_t *scales)
+{
+    int64_t r, k0;
+    double x[32];
+    if (H % 32 != 0) return -1;
+    for (r = 0; r < R; ++r)
+        for (k0 = 0; k0 < H; k0 += 32) {
+            orc_decode(X, xtype, r * ld + k0, 32, x);
+            orc_mxfp8_block(x, codes + r * H + k0, scales + r * (H / 32) + k0 / 32);
+        }
+    return 0;
+}
+
+/* Decoded values of an MXFP8 matrix: out [R, H] float64. */
+void orc_mxfp8_dequantize(const uint8_t *codes, const uint8_t *scales, int64_t R, int64_t H,
+                          double *out)
+{
+    int64_t r, k;
+    for (r = 0; r < R; ++r)
+        for (k = 0; k < H; ++k)
+            out[r * H + k] = ldexp(orc_e4m3(codes[r * H + k]), (int)scales[r * (H / 32) + k / 32] - 127);
+}
+
+/*
+ * KL(teacher || student) on the block-scaled teacher path: as orc_kl_mxfp4
+ * (teacher head W_t in MXFP4, blocked layout), with each teacher hidden row
+ * h_t[r] first quantised to MXFP8 by the rule above; the teacher logits are
+ * the float64 products of the two decoded operands.  The student is exact
+ * (bf16 h_s and W_s).  H a multiple of 64.
+ */
+int orc_kl_mx(int64_t H, int64_t V,
+              const void *h_s, const void *W_s, const void *h_t,
+              const uint8_t *Wt_packed, const uint8_t *Wt_scales, int64_t V_pad,
+              int type, int64_t ld_h, int64_t ld_w,
+              const int64_t *rows, int64_t n, double *kl)
+{
+    int64_t i0;
+    orc_mx_matrix wt;
+    double *hds = (double *)malloc((size_t)ORC_ROW_BLOCK * H * sizeof(double));
+    double *hdt = (double *)malloc((size_t)ORC_ROW_BLOCK * H * sizeof(double));
+    double *zs = (double *)malloc((size_t)ORC_ROW_BLOCK * V * sizeof(double));
+    double *zt = (double *)malloc((size_t)ORC_ROW_BLOCK * V * sizeof(double));
+    if (!hds || !hdt || !zs || !zt) { free(hds); free(hdt); free(zs); free(zt); return -2; }
+    wt.packed = Wt_packed; wt.scales = Wt_scales; wt.V_pad = V_pad; wt.H = H;
+    for (i0 = 0; i0 < n; i0 += ORC_ROW_BLOCK) {
+        int64_t nb = n - i0 < ORC_ROW_BLOCK ? n - i0 : ORC_ROW_BLOCK;
+        int64_t b, k0;
+        orc_gather_h(h_s, type, ld_h, rows, i0, nb, H, hds);
+        orc_gather_h(h_t, type, ld_h, rows, i0, nb, H, hdt);
+        for (b = 0; b < nb; ++b)            /* h_t rows -> their MXFP8 values */
+            for (k0 = 0; k0 < H; k0 += 32) {
+                uint8_t c[32], sc;
+                int i;
+                double *x = hdt + b * H + k0;
+                orc_mxfp8_block(x, c, &sc);
+                for (i = 0; i < 32; ++i) x[i] = ldexp(orc_e4m3(c[i]), (int)sc - 127);
+            }
+        orc_logits_block(hds, nb, H, V, W_s, type, ld_w, zs);
+        orc_logits_block(hdt, nb, H, V, &wt, ORC_MXFP4, H, zt);
+        for (b = 0; b < nb; ++b) {
+            const double *s = zs + b * V, *t = zt + b * V;
+            double Ls = orc_lse(s, V), Lt = orc_lse(t, V), acc = 0.0;
+            int64_t v;
+            for (v = 0; v < V; ++v) {
+                double lpt = t[v] - Lt, lps = s[v] - Ls;
+                acc += exp(lpt) * (lpt - lps);
+            }
+            kl[i0 + b] = acc;
+        }
+    }
+    free(hds); free(hdt); free(zs); free(zt);
+    return 0;
+}

@@ -251,3 +251,72 @@ def kl_mxfp4(h_s, W_s, h_t, packed, scales, rows, dtype, block=256):
         lt = lt - _lse(lt)[:, None]
         out[i0:i0 + block] = (np.exp(lt) * (lt - ls)).sum(axis=1)
     return out
+
+
+# ---------------------------------------------------------------- MXFP8
+# OCP Microscaling MXFP8 with E4M3 elements (1 sign, 4 exponent bits with
+# bias 7, 3 mantissa bits; exponent field 0 subnormal; 0x7F NaN, largest
+# finite 448) and one E8M0 scale per 32 consecutive elements of a row: the
+# teacher hidden states' format on the block-scaled tensor-core path.
+
+def e4m3_values():
+    """Float64 values of the 256 E4M3 codes (NaN for 0x7F and 0xFF)."""
+    c = np.arange(256)
+    e, m = (c >> 3) & 15, c & 7
+    v = np.where(e > 0, np.ldexp(1.0 + m / 8.0, e - 7), np.ldexp(m / 8.0, -6))
+    v = np.where(c & 0x80, -v, v)
+    v[[0x7F, 0xFF]] = np.nan
+    return v
+
+
+def mxfp8_quantize(X, dtype):
+    """(codes uint8 [R, H], scales uint8 [R, H/32]).
+
+    Restated independently of the C quantiser: the scale from numpy.frexp;
+    the element rounding as numpy.rint (ties to even) in units of the grid
+    spacing of the value's octave (2^(e - 3) for a value in [2^e, 2^(e+1)),
+    e >= -6, and the subnormal spacing 2^-9 below 2^-6), saturated at 448."""
+    x = decode(X, dtype)
+    R, H = x.shape
+    assert H % 32 == 0
+    blocks = x.reshape(R, H // 32, 32)
+    amax = np.abs(blocks).max(axis=2)
+    _, fe = np.frexp(amax)
+    code = np.where(amax > 0, np.clip(fe - 1 - 8 + 127, 0, 254), 0).astype(np.int64)
+    a = np.abs(blocks) / np.ldexp(1.0, code - 127)[:, :, None]
+    with np.errstate(divide="ignore"):
+        oct_e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    spacing = np.where(a >= 2.0 ** -6, np.ldexp(1.0, (np.maximum(oct_e, -6) - 3).astype(np.int64)),
+                       2.0 ** -9)
+    q = np.minimum(np.rint(a / spacing) * spacing, 448.0)
+    vals = e4m3_values()[:0x7F]                       # the non-negative finite codes, ascending
+    idx = np.searchsorted(vals, q)
+    assert np.all(vals[idx] == q)
+    codes = np.where((blocks < 0) & (idx > 0), idx | 0x80, idx).astype(np.uint8).reshape(R, H)
+    return codes, code.astype(np.uint8)
+
+
+def mxfp8_dequantize(codes, scales):
+    codes = np.asarray(codes, np.uint8)
+    R, H = codes.shape
+    sc = np.repeat(np.asarray(scales, np.int64), 32, axis=1)
+    return np.ldexp(e4m3_values()[codes], sc - 127)
+
+
+def kl_mx(h_s, W_s, h_t, packed, scales, rows, dtype, block=256):
+    """KL(teacher || student) on the block-scaled teacher path: the teacher
+    hidden rows quantised to MXFP8 and the teacher head in MXFP4 (blocked
+    layout); the student exact."""
+    hs, Ws = decode(h_s, dtype), decode(W_s, dtype)
+    Wt = mxfp4_dequantize(packed, scales, Ws.shape[0])
+    rows = _rows(rows, hs.shape[0])
+    out = np.empty(rows.shape[0])
+    for i0 in range(0, rows.shape[0], block):
+        r = rows[i0:i0 + block]
+        ht = mxfp8_dequantize(*mxfp8_quantize(np.asarray(decode(h_t, dtype))[r], "f64"))
+        ls = hs[r] @ Ws.T
+        lt = ht @ Wt.T
+        ls = ls - _lse(ls)[:, None]
+        lt = lt - _lse(lt)[:, None]
+        out[i0:i0 + block] = (np.exp(lt) * (lt - ls)).sum(axis=1)
+    return out

@@ -695,3 +695,135 @@ def test_kl_with_mxfp4_teacher_is_kl_on_the_decoded_weights():
     # the teacher's quantisation moves the KL, but not by much at these sizes
     plain = coracle.kl(d["h_s"], d["W_s"], d["h_t"], d["W_t"], rows, "bf16")
     assert np.all(np.abs(got - plain) < 0.1 * plain)
+
+
+# --------------------------------------------------------------------------
+# MXFP8 teacher rows (OCP Microscaling FP8: E4M3 elements, E8M0 block scales),
+# the hidden-state side of the block-scaled teacher path
+
+def test_e4m3_decoding_every_code():
+    """Both oracle decoders give the E4M3 value of every code: 1 sign, 4
+    exponent bits (bias 7), 3 mantissa bits, subnormals below exponent field
+    1, NaN at 0x7F / 0xFF, 448 the largest finite value.  Checked against the
+    format's definition written out here and against torch.float8_e4m3fn."""
+    want = []
+    for c in range(256):
+        s, e, m = c >> 7, (c >> 3) & 15, c & 7
+        if e == 15 and m == 7:
+            want.append(float("nan"))
+            continue
+        v = (1 + m / 8) * 2.0 ** (e - 7) if e else (m / 8) * 2.0 ** -6
+        want.append(-v if s else v)
+    want = np.array(want)
+    lib_vals = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    nan = np.isnan(want)
+    for got in (np.array([coracle.e4m3_value(c) for c in range(256)]), ref.e4m3_values(), lib_vals):
+        assert np.array_equal(np.isnan(got), nan)
+        assert np.array_equal(got[~nan], want[~nan])
+    assert want[0x38] == 1.0 and want[0x7E] == 448.0 and want[0x01] == 2.0 ** -9
+    assert want[0x08] == 2.0 ** -6 and want[0xB8] == -1.0 and want[0x77] == 240.0
+
+
+def test_mxfp8_scale_is_the_block_maximum_exponent_minus_8():
+    rng = np.random.default_rng(80)
+    R, H = 32, 256
+    X = rng.standard_normal((R, H)) * np.exp(rng.uniform(-20, 20, size=(R, 1)))
+    X[3, 32:64] = 0.0
+    for codes, scales in (coracle.mxfp8_quantize(X, "f64"), ref.mxfp8_quantize(X, "f64")):
+        amax = np.abs(X.reshape(R, H // 32, 32)).max(axis=2)
+        want = np.where(amax > 0, np.floor(np.log2(np.where(amax > 0, amax, 1))) - 8 + 127, 0)
+        assert np.array_equal(scales.astype(np.int64), want)
+        assert scales[3, 1] == 0 and np.all(codes[3, 32:64] == 0)
+
+
+def test_mxfp8_rounding_matches_torch_e4m3_below_saturation():
+    """Inside the block's scale unit the element is the E4M3 value nearest to
+    x / 2^(scale - 127), ties to even; torch's float8_e4m3fn conversion, an
+    independent round-to-nearest-even, agrees wherever it does not overflow
+    (x / unit <= 464).  Above that the oracle saturates at 448."""
+    rng = np.random.default_rng(81)
+    R, H = 64, 256
+    X = rng.standard_normal((R, H))
+    # exact midpoints between neighbouring codes, in units of the scale
+    vals = ref.e4m3_values()[:0x7F]
+    mids = (vals[:-1] + vals[1:]) / 2
+    X[0, :32] = 0.0
+    X[0, 0] = 448.0                                 # scale 2^0
+    X[0, 1:32] = mids[rng.choice(len(mids), 31)]
+    X[1, :32] = [500.0] + [470.0, 464.0, 463.0, 449.0] + [1.0] * 27   # scale 2^0, saturation
+    codes, scales = coracle.mxfp8_quantize(X, "f64")
+    deq = coracle.mxfp8_dequantize(codes, scales)
+    unit = np.repeat(np.ldexp(1.0, scales.astype(np.int64) - 127), 32, axis=1)
+    a = X / unit
+    ok = np.abs(a) <= 464.0
+    lib = torch.from_numpy(a[ok]).float().to(torch.float8_e4m3fn).double().numpy()
+    assert np.array_equal(deq[ok] / unit[ok], lib)
+    assert deq[1, :5].tolist() == [448.0, 448.0, 448.0, 448.0, 448.0]
+    assert np.array_equal(codes, ref.mxfp8_quantize(X, "f64")[0])
+
+
+def test_mxfp8_grid_values_round_trip_exactly():
+    """A block of E4M3 values whose largest is 448 (times 2^k) gets scale
+    code k + 127 and is stored exactly."""
+    rng = np.random.default_rng(82)
+    R, H = 24, 128
+    vals = ref.e4m3_values()[:0x7F]
+    k = rng.integers(-60, 40, size=(R, H // 32))
+    x = rng.choice(vals, size=(R, H // 32, 32)) * rng.choice([-1.0, 1.0], size=(R, H // 32, 32))
+    x[:, :, 0] = 448.0
+    X = (x * np.ldexp(1.0, k)[:, :, None]).reshape(R, H)
+    for codes, scales in (coracle.mxfp8_quantize(X, "f64"), ref.mxfp8_quantize(X, "f64")):
+        assert np.array_equal(scales.astype(np.int64), k + 127)
+        assert np.array_equal(coracle.mxfp8_dequantize(codes, scales), X)
+
+
+def test_mxfp8_c_and_numpy_quantisers_agree():
+    w = workloads.WORKLOADS[3].scaled(T=200, H=256, V=64, seed=83)
+    d = workloads.make(w)
+    for m in (d["h_t"], d["h_s"]):
+        cc, sc = coracle.mxfp8_quantize(m, "bf16")
+        cn, sn = ref.mxfp8_quantize(m, "bf16")
+        assert np.array_equal(cc, cn) and np.array_equal(sc, sn)
+    # signs, zeros (stored as +0) and values far below the block maximum
+    x = np.array([[-0.0, 0.0, -1e-30, 1e-30, 3.0, -3.0, 2.0 ** -140, -7.5] * 4])
+    cc, sc = coracle.mxfp8_quantize(x, "f64")
+    assert np.array_equal(cc, ref.mxfp8_quantize(x, "f64")[0])
+    assert cc[0, 0] == 0 and cc[0, 2] == 0 and cc[0, 6] == 0
+
+
+def test_kl_block_scaled_teacher_on_the_grid_is_the_mxfp4_kl():
+    """Teacher rows already on the MXFP8 grid are not changed by the
+    quantisation, so the block-scaled KL equals the MXFP4-teacher KL on the
+    same (decoded) inputs; with the student equal to the teacher it is 0."""
+    w = workloads.WORKLOADS[3].scaled(T=12, H=128, V=300, seed=84)
+    d = workloads.make(w)
+    ht = coracle.mxfp8_dequantize(*coracle.mxfp8_quantize(d["h_t"], "bf16"))
+    ht_bits = _bits(ht, "bf16").reshape(ht.shape)                 # exact in bf16
+    assert np.array_equal(ref.decode(ht_bits, "bf16"), ht)
+    packed, scales = coracle.mxfp4_quantize(d["W_t"], "bf16")
+    rows = np.array([11, 0, 5, 5])
+    hs = _bits(ref.decode(d["h_s"], "bf16"), "bf16").reshape(ht.shape)
+    got = coracle.kl_mx(hs, d["W_s"], ht_bits, packed, scales, rows, "bf16")
+    want = coracle.kl_mxfp4(hs, d["W_s"], ht_bits, packed, scales, rows, "bf16")
+    np.testing.assert_allclose(got, want, rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(ref.kl_mx(hs, d["W_s"], ht_bits, packed, scales, rows, "bf16"),
+                               want, rtol=1e-10, atol=1e-13)
+    # student = teacher: h_s on the MXFP8 grid, W_s the decoded MXFP4 head
+    Wt = coracle.mxfp4_dequantize(packed, scales, 300)
+    Ws_bits = _bits(Wt, "bf16").reshape(Wt.shape)
+    same = coracle.kl_mx(ht_bits, Ws_bits, ht_bits, packed, scales, rows, "bf16")
+    assert np.all(np.abs(same) <= 1e-13)
+
+
+def test_kl_block_scaled_teacher_c_and_numpy_agree():
+    w = workloads.WORKLOADS[3].scaled(T=20, H=256, V=500, seed=85)
+    d = workloads.make(w)
+    packed, scales = coracle.mxfp4_quantize(d["W_t"], "bf16")
+    rows = np.array([19, 3, 7, 0])
+    got = coracle.kl_mx(d["h_s"], d["W_s"], d["h_t"], packed, scales, rows, "bf16")
+    np.testing.assert_allclose(ref.kl_mx(d["h_s"], d["W_s"], d["h_t"], packed, scales, rows,
+                                         "bf16"), got, rtol=1e-10, atol=1e-13)
+    assert np.all(got >= 0)
+    # the teacher rows' quantisation moves the KL, but not by much
+    base = coracle.kl_mxfp4(d["h_s"], d["W_s"], d["h_t"], packed, scales, rows, "bf16")
+    assert np.all(np.abs(got - base) < 0.2 * base)
