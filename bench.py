@@ -65,8 +65,10 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--T", type=int, default=None,
                    help="replace the workload's row count (same H, V, recipe): small profiling cases")
-    p.add_argument("--teacher", choices=["bf16", "mxfp4"], default="bf16",
-                   help="KL workloads: the teacher head in bf16 or in MXFP4 (quantised before timing)")
+    p.add_argument("--teacher", choices=["bf16", "mxfp4", "mx"], default="bf16",
+                   help="KL workloads: the teacher head in bf16, in MXFP4 decoded to bf16 next to "
+                        "the tensor cores, or (mx) MXFP4 on the block-scaled tensor cores with the "
+                        "teacher rows in MXFP8 (heads quantised before timing)")
     p.add_argument("--support-j", type=int, default=None,
                    help="forward workloads: restrict each row to a sampling support keeping each "
                         "token with probability 2^-J (targets kept)")
@@ -235,6 +237,9 @@ def call_once(flp, d, ws, stats=None):
         if d.get("mx") is not None:
             return flp.kl_divergence_mxfp4(d["h_s"], d["W_s"], d["h_t"], *d["mx"], d["row_idx"],
                                            workspace=ws)
+        if d.get("mx_head") is not None:
+            return flp.kl_divergence_mx(d["h_s"], d["W_s"], d["h_t"], d["mx_head"], d["row_idx"],
+                                        workspace=ws)
         return flp.kl_divergence(d["h_s"], d["W_s"], d["h_t"], d["W_t"], d["row_idx"],
                                  workspace=ws)
     lse, ez = stats
@@ -270,6 +275,8 @@ def memory_footprint(flp, d, ws, device):
 
 
 def op_of(d):
+    if d["workload"].kind == "kl" and d.get("mx_head") is not None:
+        return 3     # the block-scaled KL's workspace (it holds the MXFP8 teacher rows)
     return {"fwd": 0, "kl": 1, "bwd": 2}[d["workload"].kind]
 
 
@@ -279,6 +286,8 @@ def launches_per_call(d):
     if w.kind == "fwd":
         return gather + 1          # (gather) + the fused scoring kernel
     if w.kind == "kl":
+        if d.get("mx_head") is not None:   # (gather of h_s) + MXFP8 quantiser + pipeline
+            return gather + 2
         return 2 * gather + 1
     # backward with the statistics supplied: per row chunk, the gradient pass
     # and the dh and dW GEMMs, plus the sum of the dh GEMM's split tail tiles
@@ -479,6 +488,11 @@ def run_ours(args):
     if args.teacher == "mxfp4" and w0.kind == "kl":
         d["mx"] = flp.mxfp4_quantize(d["W_t"])
         variant["teacher_head"] = "MXFP4 (E2M1 + E8M0 per 32), quantised before timing"
+    if args.teacher == "mx" and w0.kind == "kl":
+        d["mx_head"] = flp.mx_head_quantize(d["W_t"])
+        variant["teacher_head"] = ("MXFP4 (E2M1 + E8M0 per 32), quantised before timing, on the "
+                                   "block-scaled tensor cores; teacher rows quantised to MXFP8 "
+                                   "inside each call")
     if args.support_j is not None and w0.kind == "fwd":
         d["support"] = torch.from_numpy(workloads.support_words(
             d["workload"].T, d["workload"].V, args.support_j, d["workload"].seed,
@@ -521,8 +535,10 @@ def run_ours(args):
                      "unit": "TFLOP/s", "frac": achieved / P["bf16_tflops"], "traffic": traffic,
                      "kernel": {"fwd": "vocab_pipeline_kernel<256,4,2,LseEpi<1,%s>,2,1,8,true>"
                                        % ("true" if "support" in variant else "false"),
-                                "kl": "vocab_pipeline_kernel<256,3,2,KlEpi,2,1,%s>"
-                                      % ("4,false,true" if "teacher_head" in variant else "8"),
+                                "kl": ("mx_kl_pipeline_kernel<KlEpiT<224,16>>"
+                                       if args.teacher == "mx" else
+                                       "vocab_pipeline_kernel<256,3,2,KlEpi,2,1,%s>"
+                                       % ("4,false,true" if "teacher_head" in variant else "8")),
                                 "bwd": "grad pass + dh and dW GEMMs"}[w0.kind],
                      "peak_kind": "bf16 dense, burst, %s" % P["source"],
                      "frac_of_sustained": achieved / P["bf16_tflops_sustained"],
@@ -609,44 +625,58 @@ def run_ours(args):
                                                      d["tau"], workspace=wsk, support=sup),
                          {"support": "each token kept with probability 1/32, targets kept"})
             del sup, tk
-        # distillation KL with the teacher head in MXFP4 (4.25 bits per weight),
-        # interleaved (ABBA) with the bf16 teacher head on the same inputs
+        # distillation KL with the teacher head in MXFP4 (4.25 bits per weight):
+        # decoded to bf16 next to the tensor cores, and on the block-scaled
+        # tensor cores with the teacher rows in MXFP8; each interleaved (ABBA)
+        # with the bf16 teacher head on the same inputs
         try:
             dk = workloads.make(3, device=device)
             wk = dk["workload"]
             packed, scales = flp.mxfp4_quantize(dk["W_t"])
+            head = flp.mx_head_quantize(dk["W_t"])
             shape = flp.make_shape(wk.T, wk.H, wk.V, dk["n"], dk["h"].dtype)
-            wsk = torch.empty(flp.workspace_size(shape, 1), dtype=torch.uint8, device=device)
+            wsk = torch.empty(max(flp.workspace_size(shape, flp.OP_KL),
+                                  flp.workspace_size(shape, flp.OP_KL_MX)),
+                              dtype=torch.uint8, device=device)
+            flk = flops_per_call(dk)
+            bf16_gb = wk.V * wk.H * 2 / 1e9
+
             def bf16_teacher():
                 flp.kl_divergence(dk["h_s"], dk["W_s"], dk["h_t"], dk["W_t"], None, workspace=wsk)
 
-            def mx_teacher():
-                flp.kl_divergence_mxfp4(dk["h_s"], dk["W_s"], dk["h_t"], packed, scales, None,
-                                        workspace=wsk)
-
-            t_mx = t_bf = 0.0
-            for order in ((bf16_teacher, mx_teacher), (mx_teacher, bf16_teacher)):  # ABBA
-                for f in order:
-                    t = time_calls(f, 10, device)
-                    if f is mx_teacher:
-                        t_mx += t
-                    else:
-                        t_bf += t
-            t_mx = max_over_ranks(t_mx, world, device)
-            t_bf = max_over_ranks(t_bf, world, device)
-            flk = flops_per_call(dk)
-            configs[wk.name + "-mxfp4-teacher"] = dict(
-                describe(dk), steps=20,
-                teacher_head="MXFP4 (E2M1, E8M0 per 32), %.3f GB against %.3f GB in bf16"
-                             % (packed.numel() / 1e9 + scales.numel() / 1e9, wk.V * wk.H * 2 / 1e9))
-            extra[wk.name + "-mxfp4-teacher"] = compact(
-                n_rows=dk["n"], scored_tokens_per_s=job_throughput(dk["n"], 20, t_mx, world),
-                ms_per_step=t_mx / 20, tflops=flk / (t_mx / 20 / 1e3) / 1e12,
-                pct_of_bf16_peak=100 * flk / (t_mx / 20 / 1e3) / 1e12 / P["bf16_tflops"],
-                plain_ms_same_clocks=t_bf / 20)
-            del dk, packed, scales, wsk
+            variants = (
+                ("-mxfp4-teacher",
+                 lambda: flp.kl_divergence_mxfp4(dk["h_s"], dk["W_s"], dk["h_t"], packed, scales,
+                                                 None, workspace=wsk),
+                 "MXFP4 (E2M1, E8M0 per 32) decoded to bf16 in shared memory, %.3f GB against "
+                 "%.3f GB in bf16" % (packed.numel() / 1e9 + scales.numel() / 1e9, bf16_gb)),
+                ("-mx-teacher",
+                 lambda: flp.kl_divergence_mx(dk["h_s"], dk["W_s"], dk["h_t"], head, None,
+                                              workspace=wsk),
+                 "MXFP4 head (%.3f GB against %.3f GB in bf16) x MXFP8 teacher rows on the "
+                 "block-scaled tensor cores (tcgen05.mma kind::mxf8f6f4)"
+                 % (head.numel() / 1e9, bf16_gb)),
+            )
+            for suffix, fn, note in variants:
+                t_mx = t_bf = 0.0
+                for order in ((bf16_teacher, fn), (fn, bf16_teacher)):  # ABBA
+                    for f in order:
+                        t = time_calls(f, 10, device)
+                        if f is fn:
+                            t_mx += t
+                        else:
+                            t_bf += t
+                t_mx = max_over_ranks(t_mx, world, device)
+                t_bf = max_over_ranks(t_bf, world, device)
+                configs[wk.name + suffix] = dict(describe(dk), steps=20, teacher_head=note)
+                extra[wk.name + suffix] = compact(
+                    n_rows=dk["n"], scored_tokens_per_s=job_throughput(dk["n"], 20, t_mx, world),
+                    ms_per_step=t_mx / 20, tflops=flk / (t_mx / 20 / 1e3) / 1e12,
+                    pct_of_bf16_peak=100 * flk / (t_mx / 20 / 1e3) / 1e12 / P["bf16_tflops"],
+                    plain_ms_same_clocks=t_bf / 20)
+            del dk, packed, scales, head, wsk
         except Exception as e:  # reported, not fatal
-            extra[workloads.WORKLOADS[3].name + "-mxfp4-teacher"] = {"unavailable": str(e)[:200]}
+            extra[workloads.WORKLOADS[3].name + "-mx-teacher"] = {"unavailable": str(e)[:200]}
         torch.cuda.empty_cache()
         out["workload_configs"] = configs
 

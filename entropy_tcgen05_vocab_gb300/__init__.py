@@ -11,6 +11,7 @@ or PyTorch fallback, and a missing library raises.
                                 support=pack_support(mask))        # sampling support
     kl = kl_divergence(h_s, W_s, h_t, W_t, row_idx)
     kl = kl_divergence_mxfp4(h_s, W_s, h_t, *mxfp4_quantize(W_t), row_idx)
+    kl = kl_divergence_mx(h_s, W_s, h_t, mx_head_quantize(W_t), row_idx)  # block-scaled MMA
     dh, dW = backward(h, W, targets, row_idx, temperature, g1, g2)
     logp, ent = FusedLogProbEntropy.apply(h, W, targets, row_idx, temperature)
 """
@@ -23,12 +24,12 @@ from . import _build
 
 __all__ = ["lib", "build", "workspace_size", "logprob_entropy", "logprob_entropy_k",
            "kl_divergence", "backward", "pack_support", "mxfp4_quantize",
-           "kl_divergence_mxfp4",
+           "kl_divergence_mxfp4", "mx_head_quantize", "mxfp8_quantize", "kl_divergence_mx",
            "read_device_status", "plan", "set_kernel_events", "set_wait_limit", "row_chunks",
            "FusedLogProbEntropy", "FlpError",
-           "OP_LOGPROB_ENTROPY", "OP_KL", "OP_BACKWARD"]
+           "OP_LOGPROB_ENTROPY", "OP_KL", "OP_BACKWARD", "OP_KL_MX"]
 
-OP_LOGPROB_ENTROPY, OP_KL, OP_BACKWARD = 0, 1, 2
+OP_LOGPROB_ENTROPY, OP_KL, OP_BACKWARD, OP_KL_MX = 0, 1, 2, 3
 _DTYPES = {torch.bfloat16: 0, torch.float16: 1}
 
 
@@ -116,6 +117,14 @@ def lib():
     L.flp_mxfp4_quantize.restype = ctypes.c_int
     L.flp_kl_mxfp4.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.flp_kl_mxfp4.restype = ctypes.c_int
+    L.flp_mx_head_bytes.argtypes = [i64, i64]
+    L.flp_mx_head_bytes.restype = sz
+    L.flp_mx_head_quantize.argtypes = [vp, ctypes.c_int, i64, i64, i64, vp, vp]
+    L.flp_mx_head_quantize.restype = ctypes.c_int
+    L.flp_mxfp8_quantize.argtypes = [vp, ctypes.c_int, i64, i64, i64, vp, vp, vp]
+    L.flp_mxfp8_quantize.restype = ctypes.c_int
+    L.flp_kl_mx.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.flp_kl_mx.restype = ctypes.c_int
     for f in (L.flp_logprob_entropy, L.flp_kl, L.flp_backward, L.flp_read_device_status,
               L.flp_plan_scoring):
         f.restype = ctypes.c_int
@@ -416,6 +425,64 @@ def kl_divergence_mxfp4(h_s, W_s, h_t, Wt_packed, Wt_scales, row_idx=None, *, wo
         _check(lib().flp_kl_mxfp4(ctypes.byref(shape), _ptr(h_s), _ptr(W_s), _ptr(h_t),
                                   _ptr(Wt_packed), _ptr(Wt_scales), _ptr(ri), _ptr(out), _ptr(ws),
                                   ws.numel(), _stream(dev)))
+    return out
+
+
+def mx_head_quantize(W):
+    """Quantise W [V, H] (bf16/fp16 CUDA, H a multiple of 128) to MXFP4 in the
+    layout of the block-scaled KL (E2M1 codes [V, H/2] then the scale atoms;
+    see include/fusedlogp.h).  Returns a flat uint8 tensor of
+    flp_mx_head_bytes(V, H) bytes."""
+    _matrix(W, "W")
+    V, H = W.shape
+    nbytes = int(lib().flp_mx_head_bytes(V, H))
+    if nbytes == 0:
+        raise TypeError("H must be a positive multiple of 128")
+    head = torch.empty(nbytes, dtype=torch.uint8, device=W.device)
+    with torch.cuda.device(W.device):
+        _check(lib().flp_mx_head_quantize(_ptr(W), _DTYPES[W.dtype], V, H, W.stride(0), _ptr(head),
+                                          _stream(W.device)))
+    return head
+
+
+def mxfp8_quantize(X):
+    """OCP MXFP8 (E4M3 codes, an E8M0 scale per 32) of X [R, H] (bf16/fp16
+    CUDA, H a multiple of 32), on the GPU: (codes uint8 [R, H], scales uint8
+    [R, H/32])."""
+    _matrix(X, "X")
+    R, H = X.shape
+    codes = torch.empty((R, H), dtype=torch.uint8, device=X.device)
+    scales = torch.empty((R, H // 32), dtype=torch.uint8, device=X.device)
+    with torch.cuda.device(X.device):
+        _check(lib().flp_mxfp8_quantize(_ptr(X), _DTYPES[X.dtype], R, H, X.stride(0), _ptr(codes),
+                                        _ptr(scales), _stream(X.device)))
+    return codes, scales
+
+
+def kl_divergence_mx(h_s, W_s, h_t, Wt_head, row_idx=None, *, workspace=None):
+    """KL(teacher || student) per scored row with the teacher forward on the
+    block-scaled tensor cores: h_t quantised to MXFP8 per call, the teacher
+    head in MXFP4 (from :func:`mx_head_quantize`).  Float32 [n]."""
+    for x, nm in ((h_s, "h_s"), (W_s, "W_s"), (h_t, "h_t")):
+        _matrix(x, nm)
+    dev = h_s.device
+    if h_s.shape != h_t.shape or h_s.shape[1] != W_s.shape[1] or h_t.stride(0) != h_s.stride(0) \
+            or h_t.dtype != h_s.dtype or W_s.dtype != h_s.dtype:
+        raise TypeError("student and teacher rows must share shape, stride and dtype with W_s")
+    V, H = W_s.shape
+    nbytes = int(lib().flp_mx_head_bytes(V, H))
+    if not isinstance(Wt_head, torch.Tensor) or Wt_head.device != dev or \
+            Wt_head.dtype != torch.uint8 or Wt_head.numel() < nbytes or not Wt_head.is_contiguous():
+        raise TypeError("Wt_head must be a contiguous uint8 tensor of >= %d bytes on %s "
+                        "(see mx_head_quantize)" % (nbytes, dev))
+    ri = _index(row_idx, "row_idx", dev)
+    n = h_s.shape[0] if ri is None else ri.numel()
+    shape = make_shape(h_s.shape[0], H, V, n, h_s.dtype, h_s.stride(0), W_s.stride(0))
+    out = torch.empty(n, dtype=torch.float32, device=dev)
+    ws = _workspace(shape, OP_KL_MX, dev, workspace)
+    with torch.cuda.device(dev):
+        _check(lib().flp_kl_mx(ctypes.byref(shape), _ptr(h_s), _ptr(W_s), _ptr(h_t), _ptr(Wt_head),
+                               _ptr(ri), _ptr(out), _ptr(ws), ws.numel(), _stream(dev)))
     return out
 
 

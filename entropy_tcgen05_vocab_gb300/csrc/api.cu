@@ -102,6 +102,7 @@ struct Layout {
   size_t status = 0, cnt = 0, cnt_bytes = 0, zt = 0, pm = 0, ps = 0, pb = 0, pc = 0, pm2 = 0,
          ps2 = 0;
   size_t hs = 0, hs2 = 0, lse = 0, ez = 0, g = 0, rowcnt = 0, part = 0, total = 0;
+  size_t q8 = 0, sfa = 0;  // block-scaled KL: teacher rows in MXFP8 and their scale atoms
   int64_t grad_rows = 0;
   int part_slots = 0;  // backward: 512 KB FP32 partial tiles of the dh GEMM's split tail
 };
@@ -143,17 +144,24 @@ Layout layout_for(const flp_shape *s, flp_op op, bool gather = true) {
   L.cnt_bytes = static_cast<size_t>(cdiv(s->n_rows, 256) * 8 + 8) * 4;
   L.cnt = take(L.cnt_bytes);
   // the backward's statistics pass is the forward kernel
-  const int bn = (op == FLP_OP_KL) ? kKlBN : kFwdTileCols;
-  const int halves = ((op == FLP_OP_KL) ? kKlEpiWarps : kFwdEpiWarps) / 4;
-  const size_t sm = static_cast<size_t>(max_splits(s->V, bn, s->n_rows, 128 * kFwdCG)) * halves;  // partial slots
+  const bool kl = op == FLP_OP_KL || op == FLP_OP_KL_MX;
+  const int bn = op == FLP_OP_KL ? kKlBN : (op == FLP_OP_KL_MX ? kMxBN : kFwdTileCols);
+  const int epiw = op == FLP_OP_KL ? kKlEpiWarps : (op == FLP_OP_KL_MX ? kMxEpiWarps : kFwdEpiWarps);
+  const size_t sm = static_cast<size_t>(max_splits(s->V, bn, s->n_rows, 128 * kFwdCG)) * (epiw / 4);  // partial slots
   L.pm = take(sm * n * 4);
   L.ps = take(sm * n * 4);
   L.pb = take(sm * n * 4);
-  if (op == FLP_OP_KL) {
+  if (kl) {
     L.pm2 = take(sm * n * 4);
     L.ps2 = take(sm * n * 4);
   } else {
     L.zt = take(n * kMaxTargets * 4);  // raw target logits, up to kMaxTargets per row
+  }
+  if (op == FLP_OP_KL_MX) {
+    // the teacher's rows quantised per call: E4M3 codes and 512-byte scale
+    // atoms per 128 rows and 128-wide k-chunk
+    L.q8 = take(n * static_cast<size_t>(s->H));
+    L.sfa = take(static_cast<size_t>(cdiv(s->n_rows, 128) * cdiv(s->H, kMxChunk)) * 512);
   }
   if (gather) {
     L.hs = take(n * static_cast<size_t>(s->H) * 2);
@@ -326,7 +334,38 @@ flp_status make_map(CUtensorMap *m, flp_dtype dt, const void *base, int64_t inne
   return FLP_OK;
 }
 
+// 2-D map of any element type over `outer` rows of `inner` elements,
+// `stride` bytes apart.
+flp_status make_map_typed(CUtensorMap *m, CUtensorMapDataType type, const void *base, int64_t inner,
+                          int64_t outer, int64_t stride, int box_inner, int box_outer,
+                          CUtensorMapSwizzle swizzle) {
+  EncodeTiledFn enc;
+  flp_status st = get_encoder(&enc);
+  if (st != FLP_OK) return st;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(stride)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_outer)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(m, type, 2, const_cast<void *>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(FLP_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d, type %d)", static_cast<int>(r),
+                static_cast<int>(type));
+  return FLP_OK;
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Block-scaled teacher head: the E2M1 codes [V, H/2], then (1 KiB aligned)
+// the scale atoms, two of 512 B per 224-row vocabulary tile and 128-wide
+// k-chunk.
+size_t mx_head_code_bytes(int64_t V, int64_t H) {
+  return align_up(static_cast<size_t>(V) * static_cast<size_t>(H / 2));
+}
+size_t mx_head_atom_bytes(int64_t V, int64_t H) {
+  return static_cast<size_t>(cdiv(V, kMxBN)) * static_cast<size_t>(H / kMxChunk) * 1024;
+}
 
 flp_status check_common(const flp_shape *s, flp_op op, const void *ws, size_t ws_bytes,
                         bool gather = true) {
@@ -565,6 +604,91 @@ flp_status kl_impl(const flp_shape *s, const void *h_s, const void *W_s, const v
   return FLP_OK;
 }
 
+// KL(teacher || student) with the teacher on the block-scaled tensor cores:
+// the scored teacher rows are quantised to MXFP8 in the workspace, then one
+// persistent launch forms both heads' logit tiles and folds them.
+flp_status kl_bs_impl(const flp_shape *s, const void *h_s, const void *W_s, const void *h_t,
+                      const void *head, const int64_t *row_idx, float *out_kl, void *ws,
+                      size_t ws_bytes, flp_stream_t stream) {
+  const KernelEvents ev;
+  flp_status st = check_common(s, FLP_OP_KL_MX, ws, ws_bytes, row_idx != nullptr);
+  if (st != FLP_OK) return st;
+  if (s->H % kMxChunk != 0)
+    return fail(FLP_ERR_INVALID_ARG, "H must be a multiple of 128 for the block-scaled teacher");
+  if (s->n_rows == 0) return FLP_OK;
+  if (!row_idx && s->n_rows != s->T)
+    return fail(FLP_ERR_INVALID_ARG, "row_idx is NULL but n_rows != T");
+  if (!h_s || !W_s || !h_t || !head || !out_kl)
+    return fail(FLP_ERR_INVALID_ARG, "h_s, W_s, h_t, the teacher head and out_kl are required");
+  if (!aligned16(h_s) || !aligned16(W_s) || !aligned16(h_t))
+    return fail(FLP_ERR_INVALID_ARG, "h_s, W_s and h_t must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(head) % 256 != 0)
+    return fail(FLP_ERR_INVALID_ARG, "the teacher head must be 256-byte aligned");
+  DeviceInfo dev;
+  if ((st = device_info(&dev)) != FLP_OK) return st;
+
+  const Layout L = layout_for(s, FLP_OP_KL_MX, row_idx != nullptr);
+  const Plan p = plan_cached(s->n_rows, s->V, s->H, kMxBN, kl_bs_units(dev.sms), 256, 2);
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t kc = s->H / kMxChunk;
+  KlBsArgs a{};
+  const void *As = h_s;
+  int64_t lda = s->ld_h;
+  if (row_idx) {
+    As = at<void>(ws, L.hs);
+    lda = s->H;
+  }
+  uint8_t *q8 = at<uint8_t>(ws, L.q8), *sfa = at<uint8_t>(ws, L.sfa);
+  const uint8_t *codes = static_cast<const uint8_t *>(head);
+  const uint8_t *atoms = codes + mx_head_code_bytes(s->V, s->H);
+  if ((st = make_map(&a.tmAs, s->dtype, As, s->H, s->n_rows, lda, 64, 128)) != FLP_OK) return st;
+  if ((st = make_map(&a.tmBs, s->dtype, W_s, s->H, s->V, s->ld_w, 64, kMxBN / 2)) != FLP_OK)
+    return st;
+  if ((st = make_map_typed(&a.tmAt, CU_TENSOR_MAP_DATA_TYPE_UINT8, q8, s->H, s->n_rows, s->H,
+                           kMxChunk, 128, CU_TENSOR_MAP_SWIZZLE_128B)) != FLP_OK)
+    return st;
+  if ((st = make_map_typed(&a.tmBt, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, codes, s->H, s->V,
+                           s->H / 2, kMxChunk, kMxBN / 2, CU_TENSOR_MAP_SWIZZLE_128B)) != FLP_OK)
+    return st;
+  if ((st = make_map_typed(&a.tmSfa, CU_TENSOR_MAP_DATA_TYPE_UINT8, sfa, 16,
+                           cdiv(s->n_rows, 128) * kc * 32, 16, 16, 32,
+                           CU_TENSOR_MAP_SWIZZLE_NONE)) != FLP_OK)
+    return st;
+  if ((st = make_map_typed(&a.tmSfb, CU_TENSOR_MAP_DATA_TYPE_UINT8, atoms, 16,
+                           cdiv(s->V, kMxBN) * kc * 64, 16, 16, 64, CU_TENSOR_MAP_SWIZZLE_NONE)) !=
+      FLP_OK)
+    return st;
+  a.sch = p.sch;
+  a.sch.k_blocks = static_cast<int>(kc);
+  a.sch.wait_ns = g_wait_ns;
+  a.grid = p.grid * 2;
+  a.bf16 = s->dtype == FLP_BF16;
+  a.row_idx = row_idx;
+  a.T = s->T;
+  a.pmt = at<float>(ws, L.pm);
+  a.pst = at<float>(ws, L.ps);
+  a.pct = at<float>(ws, L.pb);
+  a.pms = at<float>(ws, L.pm2);
+  a.pss = at<float>(ws, L.ps2);
+  a.counters = at<uint32_t>(ws, L.cnt);
+  a.out_kl = out_kl;
+  a.status = at<uint32_t>(ws, L.status);
+
+  cudaError_t e = cudaMemsetAsync(a.status, 0, L.cnt + L.cnt_bytes - L.status, cs);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(status)");
+  if (row_idx &&
+      (e = launch_gather(h_s, s->ld_h, row_idx, s->n_rows, s->T, s->H, at<void>(ws, L.hs), dev.sms,
+                         cs)) != cudaSuccess)
+    return cuda_fail(e, "gather launch");
+  if ((e = launch_mxfp8_quantize(h_t, a.bf16, s->n_rows, s->H, s->ld_h, row_idx, s->T, q8, sfa,
+                                 true, dev.sms, cs)) != cudaSuccess)
+    return cuda_fail(e, "MXFP8 quantize launch");
+  if ((e = ev.start(cs)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+  if ((e = launch_kl_blockscaled(a, cs)) != cudaSuccess) return cuda_fail(e, "block-scaled KL launch");
+  if ((e = ev.stop(cs)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+  return FLP_OK;
+}
+
 flp_status backward_impl(const flp_shape *s, const void *h, const void *W, const int64_t *targets,
                          const int64_t *row_idx, const uint32_t *support, int64_t ld_support,
                          float temperature, const float *g1, const float *g2, const float *lse,
@@ -746,7 +870,10 @@ extern "C" {
 size_t flp_workspace_size(const flp_shape *shape, flp_op op) {
   const char *why = nullptr;
   if (!shape_ok(shape, &why)) return 0;
-  if (op != FLP_OP_LOGPROB_ENTROPY && op != FLP_OP_KL && op != FLP_OP_BACKWARD) return 0;
+  if (op != FLP_OP_LOGPROB_ENTROPY && op != FLP_OP_KL && op != FLP_OP_BACKWARD &&
+      op != FLP_OP_KL_MX)
+    return 0;
+  if (op == FLP_OP_KL_MX && shape->H % kMxChunk != 0) return 0;
   return layout_for(shape, op).total;
 }
 
@@ -784,17 +911,18 @@ flp_status flp_plan_scoring(const flp_shape *shape, flp_op op, int32_t num_sms, 
   const char *why = nullptr;
   if (!shape_ok(shape, &why)) return fail(FLP_ERR_INVALID_ARG, "%s", why);
   if (!out || num_sms <= 0) return fail(FLP_ERR_INVALID_ARG, "out is NULL or num_sms <= 0");
-  if (op != FLP_OP_LOGPROB_ENTROPY && op != FLP_OP_KL && op != FLP_OP_BACKWARD)
+  if (op != FLP_OP_LOGPROB_ENTROPY && op != FLP_OP_KL && op != FLP_OP_BACKWARD &&
+      op != FLP_OP_KL_MX)
     return fail(FLP_ERR_INVALID_ARG, "unknown op");
   std::memset(out, 0, sizeof *out);
   if (shape->n_rows == 0) return FLP_OK;
   // the forward's few-rows path runs single CTAs
   const bool few = op == FLP_OP_LOGPROB_ENTROPY && shape->n_rows <= kSmallRows;
-  const int bn = op == FLP_OP_KL ? kKlBN : (few ? kFwdBN : kFwdTileCols);
-  const int cg = op == FLP_OP_KL ? kKlCG : (few ? 1 : kFwdCG);
+  const bool kl = op == FLP_OP_KL || op == FLP_OP_KL_MX;
+  const int bn = op == FLP_OP_KL ? kKlBN : (op == FLP_OP_KL_MX ? kMxBN : (few ? kFwdBN : kFwdTileCols));
+  const int cg = kl ? 2 : (few ? 1 : kFwdCG);
   const int units = std::max(1, num_sms / cg);
-  const Plan p = plan_cached(shape->n_rows, shape->V, shape->H, bn, units, 128 * cg,
-                             op == FLP_OP_KL ? 2 : 1);
+  const Plan p = plan_cached(shape->n_rows, shape->V, shape->H, bn, units, 128 * cg, kl ? 2 : 1);
   out->row_tiles = p.sch.row_tiles;
   out->vocab_tiles = p.sch.vocab_tiles;
   out->block_m = 128 * cg;
@@ -919,6 +1047,65 @@ flp_status flp_kl_mxfp4(const flp_shape *s, const void *h_s, const void *W_s, co
   return kl_impl(s, h_s, W_s, h_t, nullptr, mx, row_idx, out_kl, ws, ws_bytes, stream);
 }
 
+
+size_t flp_mx_head_bytes(int64_t V, int64_t H) {
+  if (V <= 0 || H <= 0 || H % kMxChunk != 0 || V > (int64_t(1) << 30) || H > (int64_t(1) << 24))
+    return 0;
+  return mx_head_code_bytes(V, H) + mx_head_atom_bytes(V, H);
+}
+
+flp_status flp_mx_head_quantize(const void *W, flp_dtype dtype, int64_t V, int64_t H, int64_t ld_w,
+                                void *head, flp_stream_t stream) {
+  g_err[0] = 0;
+  if (flp_mx_head_bytes(V, H) == 0)
+    return fail(FLP_ERR_INVALID_ARG, "V must be > 0 and H a positive multiple of 128");
+  if (dtype != FLP_BF16 && dtype != FLP_FP16) return fail(FLP_ERR_INVALID_ARG, "bad dtype");
+  if (ld_w < H) return fail(FLP_ERR_INVALID_ARG, "ld_w < H");
+  if (!W || !head) return fail(FLP_ERR_INVALID_ARG, "W and head are required");
+  if (reinterpret_cast<uintptr_t>(W) % 2 != 0 || reinterpret_cast<uintptr_t>(head) % 256 != 0)
+    return fail(FLP_ERR_INVALID_ARG, "W must be 2-byte and head 256-byte aligned");
+  DeviceInfo dev;
+  const flp_status st = device_info(&dev);
+  if (st != FLP_OK) return st;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t *codes = static_cast<uint8_t *>(head);
+  const size_t used = static_cast<size_t>(V) * static_cast<size_t>(H / 2);
+  uint8_t *atoms = codes + mx_head_code_bytes(V, H);
+  // the kernel writes neither the padding after the codes nor the atom bytes
+  // of the rows past each tile's 224
+  cudaError_t e = cudaMemsetAsync(codes + used, 0, flp_mx_head_bytes(V, H) - used, cs);
+  if (e == cudaSuccess)
+    e = launch_mx_head_quantize(W, dtype == FLP_BF16, V, H, ld_w, codes, atoms, dev.sms, cs);
+  if (e != cudaSuccess) return cuda_fail(e, "head quantize launch");
+  return FLP_OK;
+}
+
+flp_status flp_mxfp8_quantize(const void *X, flp_dtype dtype, int64_t R, int64_t H, int64_t ld,
+                              uint8_t *codes, uint8_t *scales, flp_stream_t stream) {
+  g_err[0] = 0;
+  if (R < 0 || H <= 0 || H % 32 != 0 || ld < H || ld % 8 != 0)
+    return fail(FLP_ERR_INVALID_ARG, "need R >= 0, H a positive multiple of 32, ld >= H and a multiple of 8");
+  if (dtype != FLP_BF16 && dtype != FLP_FP16) return fail(FLP_ERR_INVALID_ARG, "bad dtype");
+  if (R == 0) return FLP_OK;
+  if (!X || !codes || !scales) return fail(FLP_ERR_INVALID_ARG, "X, codes and scales are required");
+  if (!aligned16(X) || !aligned16(codes))
+    return fail(FLP_ERR_INVALID_ARG, "X and codes must be 16-byte aligned");
+  DeviceInfo dev;
+  const flp_status st = device_info(&dev);
+  if (st != FLP_OK) return st;
+  const cudaError_t e = launch_mxfp8_quantize(X, dtype == FLP_BF16, R, H, ld, nullptr, R, codes,
+                                              scales, false, dev.sms,
+                                              reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "MXFP8 quantize launch");
+  return FLP_OK;
+}
+
+flp_status flp_kl_mx(const flp_shape *s, const void *h_s, const void *W_s, const void *h_t,
+                     const void *Wt_head, const int64_t *row_idx, float *out_kl, void *ws,
+                     size_t ws_bytes, flp_stream_t stream) {
+  g_err[0] = 0;
+  return kl_bs_impl(s, h_s, W_s, h_t, Wt_head, row_idx, out_kl, ws, ws_bytes, stream);
+}
 
 flp_status flp_backward(const flp_shape *s, const void *h, const void *W, const int64_t *targets,
                         const int64_t *row_idx, float temperature, const float *g1,

@@ -56,6 +56,16 @@ constexpr int kKlAcc = 1;
 constexpr int kKlEpiWarps = 8;
 
 
+// Block-scaled KL (the teacher GEMM on tcgen05.mma kind::mxf8f6f4, E4M3
+// hidden rows x E2M1 head, one E8M0 scale per 32): CTA pairs on 256-row x
+// 224-column tiles (224 = 512 TMEM columns minus room for the scale factors
+// beside the student and teacher accumulators), 128-wide teacher k-chunks,
+// eight epilogue warps.  The head's scale atoms are laid out per 224-row
+// vocabulary tile (see flp_mx_head_quantize).
+constexpr int kMxBN = 224;
+constexpr int kMxChunk = 128;
+constexpr int kMxEpiWarps = 8;
+
 struct FwdArgs {
   CUtensorMap tmA;  // scored hidden rows [n, H], box 64 x 128
   CUtensorMap tmB;  // W [V, H], box 64 x kFwdBN
@@ -89,6 +99,22 @@ struct KlArgs {
   float *out_kl;
   uint32_t *status;
   MxOperand mx;  // teacher head in MXFP4 (packed == null: W_t through tmBt)
+};
+
+struct KlBsArgs {
+  CUtensorMap tmAs, tmBs;    // student rows [n, H] (box 64 x 128) and head [V, H] (box 64 x 112)
+  CUtensorMap tmAt, tmBt;    // teacher MXFP8 codes [n, H] uint8 (box 128 x 128), head codes
+                             // [V, H] 16U4_ALIGN16B (box 128 x 112)
+  CUtensorMap tmSfa, tmSfb;  // scale atoms as rows of 16 bytes (boxes 16 x 32, 16 x 64)
+  Schedule sch;              // k_blocks = H / 128
+  int grid;
+  bool bf16;
+  const int64_t *row_idx;
+  int64_t T;
+  float *pmt, *pst, *pct, *pms, *pss;
+  uint32_t *counters;
+  float *out_kl;
+  uint32_t *status;
 };
 
 struct GradArgs {
@@ -179,6 +205,21 @@ cudaError_t launch_pack_support(const uint8_t *mask, int64_t T, int64_t V, int64
                                 uint32_t *support, int64_t ld_support, int num_sms,
                                 cudaStream_t stream);
 cudaError_t launch_wait_timeout(uint64_t limit_ns, uint32_t *status, cudaStream_t stream);
+cudaError_t launch_kl_blockscaled(const KlBsArgs &a, cudaStream_t stream);
+int kl_bs_units(int num_sms);
+// MXFP8 quantisation of R rows (row_idx[i], or i, of X [*, ld] bf16/fp16;
+// rows outside [0, T) read as zeros) into codes [R, H] and scales: the
+// pipeline's 512-byte atoms (atoms = true, rows up to the next multiple of
+// 128 get scale 0) or a plain [R, H / 32] array.  H a multiple of 128
+// (atoms) or 32.
+cudaError_t launch_mxfp8_quantize(const void *X, bool bf16, int64_t R, int64_t H, int64_t ld,
+                                  const int64_t *row_idx, int64_t T, uint8_t *codes,
+                                  uint8_t *scales, bool atoms, int num_sms, cudaStream_t stream);
+// MXFP4 quantisation of W [V, ld_w] into the block-scaled head: codes [V, H/2]
+// row-major, scale atoms per 224-row vocabulary tile.
+cudaError_t launch_mx_head_quantize(const void *W, bool bf16, int64_t V, int64_t H, int64_t ld_w,
+                                    uint8_t *codes, uint8_t *atoms, int num_sms,
+                                    cudaStream_t stream);
 // CTAs or CTA pairs of each pipeline that can be resident at once.
 int fwd_units(int num_sms);
 int grad_units(int num_sms);

@@ -1,0 +1,342 @@
+// mx_pipeline.cuh -- the KL pipeline with the teacher GEMM on the
+// block-scaled tensor-core path (tcgen05.mma kind::mxf8f6f4).
+//
+// DeepSeek-V4 book ch. 19, "1. FP4 in OPD": the inference-only teacher
+// forward runs in native 4-bit precision.  Here the teacher head is MXFP4
+// (E2M1 codes, one E8M0 scale per 32) and the teacher's hidden rows are
+// quantised to MXFP8 (E4M3 codes, one E8M0 scale per 32) per call, so the
+// teacher logits come out of the tensor cores' block-scaled MMA at twice the
+// bf16 rate, with the scales applied inside the MMA.  The student stays on
+// the bf16/fp16 path, and the epilogue is the KL fold of the bf16 pipeline.
+//
+// CTA pairs (cluster of 2) on 256-row x 224-column tiles, persistent, one
+// item = (256-row tile, vocabulary split) as in vocab_pipeline.cuh.  Two
+// operand rings per CTA, filled by one producer warp in the order the MMA
+// issuer consumes them:
+//   student ring  kMxSStages stages of one 64-wide k-block: A_s (128 x 64
+//                 bf16) and B_s (112 x 64 bf16), 128B-swizzled;
+//   teacher ring  kMxTStages stages of one 128-wide k-chunk: A_t (128 x 128
+//                 E4M3), B_t (112 x 128 E2M1 in the padded layout the MMA
+//                 reads: each 16 elements as 8 bytes of codes and an 8-byte
+//                 gap, written so by the tensor-map copy of type
+//                 16U4_ALIGN16B), 128B-swizzled, and the scale atoms of A_t's
+//                 128 rows (512 B) and of the whole 224-row B_t tile (1 KB:
+//                 every CTA of the pair needs the scales of all N columns).
+// A scale atom holds the scales of 128 rows for the four 32-element steps
+// of a k-chunk: byte (r % 32) * 16 + (r / 32) * 4 + j for row r, step j.
+// One tcgen05.cp (32 rows x 16 bytes, to every lane quarter) moves an atom
+// into four TMEM columns, which is the layout the block-scaled MMA reads
+// (row m's scale at lane m, column m / 32; column n's at lane n % 32 of the
+// row's lane quarter, column n / 32; step j in byte j).
+// TMEM (512 columns): student accumulator [0, 224), teacher accumulator
+// [224, 448), and 12 scale columns per teacher stage from 448 (4 for A, 8 for
+// B).  Per 128-wide k-chunk the MMA issuer copies the chunk's scales into
+// its stage's columns, issues four block-scaled MMAs (K = 32, scale id =
+// step) into the teacher accumulator and eight bf16 MMAs (K = 16, two
+// student k-blocks) into the student accumulator.  The copies and MMAs of
+// one thread execute in issue order, and a stage's scale columns are
+// rewritten only after the MMAs that read them released that stage.
+// Eight epilogue warps (two per TMEM lane quarter, 112 columns each) fold
+// the two accumulators 16 columns at a time with the KL epilogue.
+#pragma once
+
+#include "launch.h"
+#include "vocab_pipeline.cuh"
+
+namespace flp {
+
+constexpr int kMxBRows = kMxBN / 2;   // B rows per CTA
+constexpr int kMxSStages = 4;
+constexpr int kMxTStages = 3;
+constexpr int kMxThreads = 64 + 32 * kMxEpiWarps;
+constexpr int kMxUmmaK = 32;          // K per block-scaled MMA
+
+struct MxPipeLayout {
+  static constexpr int kSA = kBM * kBK * 2;             // 16384
+  static constexpr int kSB = kMxBRows * kBK * 2;        // 14336
+  static constexpr int kSStage = kSA + kSB;             // 30720
+  static constexpr int kTA = kBM * kMxChunk;            // 16384: 128 rows x 128 E4M3
+  static constexpr int kTB = kMxBRows * kMxChunk;       // 14336: padded E2M1 in shared memory
+  static constexpr int kTBTx = kMxBRows * kMxChunk / 2; // 7168: code bytes the copy counts
+  static constexpr int kSfa = 512;
+  static constexpr int kSfb = 1024;
+  static constexpr int kTStage = 32768;
+  static constexpr int kTTx = kTA + kTBTx + kSfa + kSfb;  // bytes one CTA's teacher copies count
+  static constexpr int kTRing = kMxSStages * kSStage;
+  static constexpr int kRingBytes = kTRing + kMxTStages * kTStage;
+  static constexpr int kBarrierBytes = 8 * (2 * kMxSStages + 2 * kMxTStages + 3) + 32;
+  static constexpr int kSmemBytes = kRingBytes + kBarrierBytes + 1024;
+  static constexpr int kTmemCols = 512;
+  static constexpr int kSfCol0 = 2 * kMxBN;
+  static constexpr int kSfCols = 12;
+};
+static_assert(MxPipeLayout::kSStage % 1024 == 0 && MxPipeLayout::kTStage % 1024 == 0,
+              "stages stay aligned to swizzle atoms");
+static_assert(MxPipeLayout::kTA + MxPipeLayout::kTB + MxPipeLayout::kSfa + MxPipeLayout::kSfb <=
+                  MxPipeLayout::kTStage,
+              "teacher stage fits");
+static_assert(MxPipeLayout::kSfCol0 + kMxTStages * MxPipeLayout::kSfCols <= MxPipeLayout::kTmemCols,
+              "scale columns fit beside the accumulators");
+static_assert(MxPipeLayout::kSmemBytes <= 227 * 1024, "shared memory per CTA");
+
+// Epi as in vocab_pipeline.cuh (tile() gets nchunks in units of Epi::kChunk).
+// Maps: tmAs / tmBs the student rows and head (bf16/fp16, boxes 64 x 128 and
+// 64 x 112), tmAt the teacher's MXFP8 codes (uint8, box 128 x 128), tmBt the
+// teacher head's codes (16U4_ALIGN16B, box 128 x 112), tmSfa / tmSfb the
+// scale atoms (uint8 rows of 16 bytes, boxes 16 x 32 and 16 x 64).
+// sch.k_blocks counts 128-wide k-chunks.  Launched with a cluster dimension
+// of 2 and kMxThreads threads.
+template <class Epi>
+__global__ void __launch_bounds__(kMxThreads, 1)
+    mx_kl_pipeline_kernel(const __grid_constant__ CUtensorMap tmAs,
+                          const __grid_constant__ CUtensorMap tmBs,
+                          const __grid_constant__ CUtensorMap tmAt,
+                          const __grid_constant__ CUtensorMap tmBt,
+                          const __grid_constant__ CUtensorMap tmSfa,
+                          const __grid_constant__ CUtensorMap tmSfb, const Schedule sch,
+                          const uint32_t idesc_s, const uint32_t idesc_t,
+                          const typename Epi::Params ep, uint32_t *status) {
+  using L = MxPipeLayout;
+  constexpr int CG = 2;
+  constexpr int kHalves = kMxEpiWarps / 4;
+  constexpr int kWarpCols = kMxBN / kHalves;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t *sfull = reinterpret_cast<uint64_t *>(smem + L::kRingBytes);
+  uint64_t *sempty = sfull + kMxSStages;
+  uint64_t *tfull = sempty + kMxSStages;
+  uint64_t *tempty = tfull + kMxTStages;
+  uint64_t *afull = tempty + kMxTStages;  // accumulators ready for the epilogue
+  uint64_t *aempty = afull + 1;           // accumulators drained
+  uint64_t *drain = aempty + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  // iterations of the two rings the peer's producer issued (written at teardown)
+  volatile uint32_t *peer_issued = reinterpret_cast<volatile uint32_t *>(tmem_slot + 2);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int unit = blockIdx.x / CG;
+  const int num_units = gridDim.x / CG;
+  const int kc_n = sch.k_blocks;  // 128-wide k-chunks
+  const uint64_t lim = wait_limit(sch.wait_ns);
+  uint32_t s_issued = 0, t_issued = 0;  // producer: iterations issued per ring
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kMxSStages; ++s) {
+      mbar_init(&sfull[s], 1);
+      mbar_init(&sempty[s], 1);
+    }
+    for (int s = 0; s < kMxTStages; ++s) {
+      mbar_init(&tfull[s], 1);
+      mbar_init(&tempty[s], 1);
+    }
+    mbar_init(afull, 1);
+    mbar_init(aempty, kMxEpiWarps * CG);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    peer_issued[0] = 0;
+    peer_issued[1] = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmAs);
+    prefetch_tmap(&tmBs);
+    prefetch_tmap(&tmAt);
+    prefetch_tmap(&tmBt);
+    prefetch_tmap(&tmSfa);
+    prefetch_tmap(&tmSfb);
+  }
+  if (warp == 1) {
+    tmem_alloc<CG>(tmem_slot, L::kTmemCols);
+    tmem_relinquish<CG>();
+  }
+  pipe_sync<CG>();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    int ss = 0, ts = 0;
+    uint32_t sph = 0, tph = 0;
+    bool ok = true;
+    const uint32_t sfull_dst = mapa_shared(smem_u32(sfull), 0);
+    const uint32_t tfull_dst = mapa_shared(smem_u32(tfull), 0);
+    for (int it = unit; ok && it < sch.items; it += num_units) {
+      int mt, sp, vt0, vt1;
+      sch.item(it, mt, sp, vt0, vt1);
+      const int arow = mt * (kBM * CG) + static_cast<int>(rank) * kBM;
+      const int ablk = mt * CG + static_cast<int>(rank);  // 128-row block of the scale atoms
+      for (int vt = vt0; ok && vt < vt1; ++vt) {
+        const int brow = vt * kMxBN + static_cast<int>(rank) * kMxBRows;
+        for (int c = 0; c < kc_n; ++c) {
+          // teacher k-chunk c
+          if (lane == 0) ok = mbar_wait(&tempty[ts], tph ^ 1u, abort_flag, lim);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          if (lane == 0) {
+            uint8_t *base = smem + L::kTRing + ts * L::kTStage;
+            if (leader) mbar_arrive_expect_tx(&tfull[ts], CG * L::kTTx);
+            const uint32_t fb = tfull_dst + ts * 8;
+            tma_load_2d_pair(base, &tmAt, fb, c * kMxChunk, arow);
+            tma_load_2d_pair(base + L::kTA, &tmBt, fb, c * kMxChunk, brow);
+            tma_load_2d_pair(base + L::kTA + L::kTB, &tmSfa, fb, 0, (ablk * kc_n + c) * 32);
+            tma_load_2d_pair(base + L::kTA + L::kTB + L::kSfa, &tmSfb, fb, 0, (vt * kc_n + c) * 64);
+          }
+          ++t_issued;
+          if (++ts == kMxTStages) {
+            ts = 0;
+            tph ^= 1u;
+          }
+          // student k-blocks 2c and 2c + 1
+          for (int h = 0; h < 2; ++h) {
+            if (lane == 0) ok = mbar_wait(&sempty[ss], sph ^ 1u, abort_flag, lim);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            if (lane == 0) {
+              uint8_t *sa = smem + ss * L::kSStage;
+              if (leader) mbar_arrive_expect_tx(&sfull[ss], CG * L::kSStage);
+              const uint32_t fb = sfull_dst + ss * 8;
+              const int kb = 2 * c + h;
+              tma_load_2d_pair(sa, &tmAs, fb, kb * kBK, arow);
+              tma_load_2d_pair(sa + L::kSA, &tmBs, fb, kb * kBK, brow);
+            }
+            ++s_issued;
+            if (++ss == kMxSStages) {
+              ss = 0;
+              sph ^= 1u;
+            }
+          }
+          if (!ok) break;
+        }
+      }
+    }
+    if (!ok && lane == 0) record_timeout<CG>(status, abort_flag);
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (leader) {
+      int ss = 0, ts = 0;
+      uint32_t sph = 0, tph = 0, aph = 0;
+      bool ok = true;
+      const uint32_t d_student = tmem_base;
+      const uint32_t d_teacher = tmem_base + kMxBN;
+      for (int it = unit; ok && it < sch.items; it += num_units) {
+        int mt, sp, vt0, vt1;
+        sch.item(it, mt, sp, vt0, vt1);
+        for (int vt = vt0; ok && vt < vt1; ++vt) {
+          if (lane == 0) ok = mbar_wait(aempty, aph ^ 1u, abort_flag, lim);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          tc_fence_after();
+          for (int c = 0; c < kc_n; ++c) {
+            if (lane == 0) ok = mbar_wait(&tfull[ts], tph, abort_flag, lim);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            if (lane == 0) {
+              const uint32_t tb = smem_u32(smem + L::kTRing + ts * L::kTStage);
+              const uint32_t sf = tmem_base + static_cast<uint32_t>(L::kSfCol0 + ts * L::kSfCols);
+              tmem_cp_32x128b_x4_pair(sf, sdesc_rows16(tb + L::kTA + L::kTB));
+              tmem_cp_32x128b_x4_pair(sf + 4, sdesc_rows16(tb + L::kTA + L::kTB + L::kSfa));
+              tmem_cp_32x128b_x4_pair(sf + 8, sdesc_rows16(tb + L::kTA + L::kTB + L::kSfa + 512));
+#pragma unroll
+              for (int j = 0; j < kMxChunk / kMxUmmaK; ++j) {
+                const uint64_t ad = sdesc_sw128(tb + j * kMxUmmaK, 16, 1024);
+                const uint64_t bd = sdesc_sw128(tb + L::kTA + j * kMxUmmaK, 16, 1024);
+                mma_mx_pair(d_teacher, ad, bd, idesc_mx_sf(idesc_t, static_cast<uint32_t>(j)), sf,
+                            sf + 4, (c | j) != 0 ? 1u : 0u);
+              }
+              mma_commit_pair(&tempty[ts], 0x3);
+            }
+            __syncwarp();
+            if (++ts == kMxTStages) {
+              ts = 0;
+              tph ^= 1u;
+            }
+            for (int h = 0; h < 2; ++h) {
+              if (lane == 0) ok = mbar_wait(&sfull[ss], sph, abort_flag, lim);
+              ok = __shfl_sync(0xffffffffu, ok, 0);
+              if (!ok) break;
+              tc_fence_after();
+              if (lane == 0) {
+                const uint32_t sa = smem_u32(smem + ss * L::kSStage);
+#pragma unroll
+                for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
+                  const uint64_t ad = sdesc_sw128(sa + kk * kUmmaK * 2, 16, 1024);
+                  const uint64_t bd = sdesc_sw128(sa + L::kSA + kk * kUmmaK * 2, 16, 1024);
+                  mma_f16_pair(d_student, ad, bd, idesc_s, (c | h | kk) != 0 ? 1u : 0u);
+                }
+                mma_commit_pair(&sempty[ss], 0x3);
+              }
+              __syncwarp();
+              if (++ss == kMxSStages) {
+                ss = 0;
+                sph ^= 1u;
+              }
+            }
+            if (!ok) break;
+          }
+          if (!ok) break;
+          if (lane == 0) mma_commit_pair(afull, 0x3);  // both accumulators ready
+          __syncwarp();
+          aph ^= 1u;
+        }
+      }
+      if (!ok && lane == 0) record_timeout<CG>(status, abort_flag);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int lg = warp & 3;
+    const int half = (warp - 2) / 4;
+    const uint32_t lane_off = (static_cast<uint32_t>(lg * 32) << 16) +
+                              static_cast<uint32_t>(half * kWarpCols);
+    const uint32_t aempty_dst = mapa_shared(smem_u32(aempty), 0);
+    Epi epi(ep);
+    uint32_t aph = 0;
+    bool ok = true;
+    for (int it = unit; ok && it < sch.items; it += num_units) {
+      int mt, sp, vt0, vt1;
+      sch.item(it, mt, sp, vt0, vt1);
+      const int row = mt * (kBM * CG) + static_cast<int>(rank) * kBM + lg * 32 + lane;
+      epi.begin(mt, row);
+      for (int vt = vt0; vt < vt1; ++vt) {
+        if (lane == 0) ok = mbar_wait(afull, aph, abort_flag, lim);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        tc_fence_after();
+        epi.tile(tmem_base + lane_off, vt * kMxBN + half * kWarpCols, kWarpCols / Epi::kChunk);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(aempty_dst);
+        aph ^= 1u;
+      }
+      if (!ok) break;
+      epi.end(sp * kHalves + half, row);
+    }
+    if (!ok && lane == 0) record_timeout<CG>(status, abort_flag);
+  }
+
+  // Teardown (as in vocab_pipeline_kernel, for both rings).
+  if (warp == 0 && lane == 0 && !leader) {
+    const uint32_t pi = mapa_shared(smem_u32(const_cast<uint32_t *>(peer_issued)), 0);
+    st_cluster_u32(pi, s_issued);
+    st_cluster_u32(pi + 4, t_issued);
+  }
+  pipe_sync<CG>();
+  if (*abort_flag) {
+    if (leader && lane == 0) {
+      if (warp == 0) {
+        drain_copies<kMxSStages, CG>(sfull, s_issued, peer_issued[0], L::kSStage);
+        drain_copies<kMxTStages, CG>(tfull, t_issued, peer_issued[1], L::kTTx);
+      } else if (warp == 1) {
+        drain_mmas<CG>(drain);
+      }
+    }
+    pipe_sync<CG>();
+  }
+  if (warp == 1) tmem_dealloc<CG>(tmem_base, L::kTmemCols);
+}
+
+}  // namespace flp

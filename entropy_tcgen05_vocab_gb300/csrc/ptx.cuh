@@ -318,6 +318,52 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 32 lanes x 16 consecutive 32-bit columns (as tmem_ld32, half the width).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// CTA-pair block-scaled MMA, kind::mxf8f6f4 with one E8M0 scale per 32
+// elements of K (scale_vec::1X), K = 32 per instruction, FP32 accumulation.
+// Issued by one thread of the leader; A, B and D are split between the CTAs
+// as in mma_f16_pair.  The scale factors are read from each CTA's own TMEM:
+// the scale of A row m from lane m, column sfa + m/32; that of B column n
+// (all N of them, in both CTAs) from lane n % 32 of the lane quarter that
+// holds the D row being formed, column sfb + n/32; the byte of the 32-bit
+// cell is the scale-factor id of the instruction descriptor.
+__device__ __forceinline__ void mma_mx_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X "
+      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// CTA-pair copy of a 32-row x 16-byte shared-memory block into TMEM, issued
+// by one thread of the leader: each CTA copies the block at the same offset
+// of its own shared memory into its own TMEM, row r to lane r of every lane
+// quarter (4 columns from `taddr`).  Executes in order with the issuing
+// thread's MMAs.
+__device__ __forceinline__ void tmem_cp_32x128b_x4_pair(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
 // Shared-memory matrix descriptor of tcgen05.mma for a 128-byte-swizzled
 // operand tile (the layout a TMA copy with CU_TENSOR_MAP_SWIZZLE_128B
 // writes: rows of 128 bytes, swizzle atoms of 8 rows = 1024 bytes, atoms
@@ -339,6 +385,18 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// Shared-memory descriptor of a plain (unswizzled) block of 16-byte rows,
+// the source of a tcgen05.cp: rows 16 bytes apart, 8-row groups 128 bytes
+// apart (layout type SWIZZLE_NONE, 0).
+__device__ __forceinline__ uint64_t sdesc_rows16(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(128u >> 4) << 16;
+  d |= static_cast<uint64_t>(128u >> 4) << 32;
+  d |= 1ull << 46;
+  return d;
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16 with FP32 accumulation:
 // D format F32 (bit 4), A/B format (bits [7,10) and [10,13): 0 = F16,
 // 1 = BF16), A/B major (bit 15 / 16: 0 = K-major, 1 = MN-major), N >> 3 in
@@ -347,6 +405,21 @@ __host__ __device__ constexpr uint32_t idesc_f16(bool bf16, int M, int N, bool a
   return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
          ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Instruction descriptor of tcgen05.mma kind::mxf8f6f4 (block-scaled, FP32
+// accumulation), A E4M3 and B E2M1, both K-major: A format in bits [7,10)
+// (E4M3 = 0), B format in [10,13) (E2M1 = 5), N >> 3 in [17,23), scale type
+// UE8M0 (bit 23 = 1), M >> 4 in [24,29); the scale-factor ids (which byte of
+// the 32-bit TMEM cell holds this instruction's scales) go to bits [4,6)
+// for B and [29,31) for A, see idesc_mx_sf.
+__host__ __device__ constexpr uint32_t idesc_mx_e4m3_e2m1(int M, int N) {
+  return (0u << 7) | (5u << 10) | (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__host__ __device__ constexpr uint32_t idesc_mx_sf(uint32_t idesc, uint32_t sf_id) {
+  return idesc | (sf_id << 4) | (sf_id << 29);
 }
 
 // 2^x on the special-function unit (PTX ex2.approx, subnormals flushed).

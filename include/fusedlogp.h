@@ -71,7 +71,8 @@ typedef enum { FLP_BF16 = 0, FLP_FP16 = 1 } flp_dtype;
 typedef enum {
     FLP_OP_LOGPROB_ENTROPY = 0,
     FLP_OP_KL = 1,
-    FLP_OP_BACKWARD = 2
+    FLP_OP_BACKWARD = 2,
+    FLP_OP_KL_MX = 3   /* flp_kl_mx: the teacher on the block-scaled tensor cores */
 } flp_op;
 
 /*
@@ -265,6 +266,72 @@ flp_status flp_kl_mxfp4(const flp_shape *shape, const void *h_s, const void *W_s
                         const void *h_t, const uint8_t *Wt_packed, const uint8_t *Wt_scales,
                         const int64_t *row_idx, float *out_kl,
                         void *workspace, size_t workspace_bytes, flp_stream_t stream);
+
+/*
+ * The teacher forward on the block-scaled tensor cores (DeepSeek-V4 book
+ * ch. 19, "1. FP4 in OPD": the inference-only teacher forwards run in native
+ * FP4, which cuts the teacher head's memory and read traffic; the MMA that
+ * takes FP4 weights natively takes the other operand in a microscaling
+ * format too).  The teacher head is MXFP4 as for flp_mxfp4_quantize (same
+ * rounding), in the layout the block-scaled MMA reads; the teacher's hidden
+ * rows are quantised to MXFP8 per call (flp_mxfp8_quantize's rule); the
+ * teacher logits are the exact products of the two quantised operands,
+ * accumulated in FP32 by tcgen05.mma kind::mxf8f6f4 at twice the bf16 rate.
+ * The student is computed as in flp_kl.
+ *
+ * Head layout (`head`, flp_mx_head_bytes bytes, 256-byte aligned DEVICE
+ * buffer):
+ *   codes   [V, H/2] bytes at head: byte b of row v holds elements 2b (low
+ *           nibble) and 2b + 1 (high nibble), E2M1 codes
+ *   atoms   at head + (V * H/2 rounded up to 1024): for vocabulary tile
+ *           t = v / 224, row i = v % 224, 128-wide k-chunk c = k / 128 and
+ *           step j = (k % 128) / 32, the E8M0 scale of elements
+ *           c*128 + 32j .. + 31 of row v sits in the 512-byte atom
+ *           (t * (H/128) + c) * 2 + i / 128, at byte
+ *           (i % 128 % 32) * 16 + (i % 128 / 32) * 4 + j.  The padding after
+ *           the codes and the atom bytes of rows past V (and past each
+ *           tile's 224 rows) are 0.
+ */
+/* Bytes of a block-scaled teacher head (0 if V <= 0 or H is not a positive
+ * multiple of 128). */
+size_t flp_mx_head_bytes(int64_t V, int64_t H);
+
+/*
+ * Quantises W [V, ld_w] (bf16/fp16, DEVICE, finite) to MXFP4 in the head
+ * layout above: per 32-element block s = floor(log2 max|x|) - 2 + 127
+ * clamped to [0, 254] (0 for an all-zero block), elements the E2M1 value
+ * nearest to x / 2^(s - 127), ties to the even code, saturated at 6, zero as
+ * +0 (the rule of flp_mxfp4_quantize).  H a multiple of 128.
+ */
+flp_status flp_mx_head_quantize(const void *W, flp_dtype dtype, int64_t V, int64_t H,
+                                int64_t ld_w, void *head, flp_stream_t stream);
+
+/*
+ * OCP MXFP8 (E4M3 elements: 1 sign, 4 exponent bits with bias 7, 3 mantissa
+ * bits, largest finite 448; one E8M0 scale per 32 elements) of X [R, ld]
+ * (bf16/fp16, DEVICE, finite, 16-byte aligned, ld a multiple of 8):
+ *   s = floor(log2 max|x|) - 8 + 127 over each 32-element block, clamped to
+ *       [0, 254] (0 for an all-zero block);
+ *   each element = the E4M3 value nearest to x / 2^(s - 127), ties to the
+ *       even code, magnitudes above 448 saturated to 448, zero as +0.
+ *   codes   [R, H] uint8 row-major (16-byte aligned); scales [R, H/32] uint8.
+ * This is the quantisation flp_kl_mx applies to the teacher's hidden rows.
+ */
+flp_status flp_mxfp8_quantize(const void *X, flp_dtype dtype, int64_t R, int64_t H, int64_t ld,
+                              uint8_t *codes, uint8_t *scales, flp_stream_t stream);
+
+/*
+ * KL(teacher || student) per scored row as flp_kl, with the teacher's logits
+ * h_t[row]^MXFP8 times the MXFP4 head `Wt_head` (from flp_mx_head_quantize,
+ * V rows of H columns) on the block-scaled tensor cores.  bf16 or fp16 rows
+ * and student head; H a multiple of 128.  Workspace: flp_workspace_size(shape,
+ * FLP_OP_KL_MX) (it holds the quantised teacher rows: n_rows * H bytes plus
+ * their scales).
+ */
+flp_status flp_kl_mx(const flp_shape *shape, const void *h_s, const void *W_s,
+                     const void *h_t, const void *Wt_head, const int64_t *row_idx,
+                     float *out_kl, void *workspace, size_t workspace_bytes,
+                     flp_stream_t stream);
 
 /*
  * Gradients of L = sum_i g1[i] logp_i + g2[i] ent_i (logp, ent as in

@@ -149,3 +149,23 @@ def test_backward_pipelines_wait_that_runs_out_unwinds():
     for got, want in ((dh, dh_ref), (dW, dW_ref)):
         g = got.cpu().double().numpy()
         assert np.linalg.norm(g - want) <= 1e-2 * np.linalg.norm(want)
+
+
+def test_block_scaled_kl_pipeline_wait_that_runs_out_unwinds():
+    """The two-ring pipeline of flp_kl_mx (student and teacher rings, scale
+    copies into TMEM) gives up, drains and frees its TMEM the same way."""
+    k = workloads.make(workloads.WORKLOADS[3].scaled(T=256, H=ABORT_H, V=8192, seed=5),
+                       device="cuda")
+    ws = _ws(256, ABORT_H, 8192, 256, flp.OP_KL_MX)
+    head = flp.mx_head_quantize(k["W_t"])
+    run = lambda: flp.kl_divergence_mx(k["h_s"], k["W_s"], k["h_t"], head, workspace=ws)
+    packed, scales = coracle.mxfp4_quantize(k["W_t"].cpu(), "bf16")
+    want = coracle.kl_mx(k["h_s"].cpu(), k["W_s"].cpu(), k["h_t"].cpu(), packed, scales, None,
+                         "bf16")
+    with _ShortWaits():
+        run()
+        st = flp.read_device_status(ws)
+    assert st["timeouts"] > 0, st
+    kl = run()
+    assert flp.read_device_status(ws)["timeouts"] == 0
+    assert np.abs(kl.cpu().double().numpy() - want).max() <= 1e-3
