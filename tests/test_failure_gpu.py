@@ -111,8 +111,9 @@ def test_kl_pipeline_wait_that_runs_out_unwinds(teacher):
         packed, scales = flp.mxfp4_quantize(k["W_t"])
         run = lambda: flp.kl_divergence_mxfp4(k["h_s"], k["W_s"], k["h_t"], packed, scales,
                                               workspace=ws)
-        want = ref.kl_mxfp4(k["h_s"].cpu(), k["W_s"].cpu(), k["h_t"].cpu(), packed.cpu().numpy(),
-                            scales.cpu().numpy(), None, "bf16")
+        opacked, oscales = coracle.mxfp4_quantize(k["W_t"].cpu(), "bf16")
+        want = ref.kl_mxfp4(k["h_s"].cpu(), k["W_s"].cpu(), k["h_t"].cpu(), opacked, oscales, None,
+                            "bf16")
     else:
         run = lambda: flp.kl_divergence(k["h_s"], k["W_s"], k["h_t"], k["W_t"], workspace=ws)
         want = coracle.kl(k["h_s"].cpu(), k["W_s"].cpu(), k["h_t"].cpu(), k["W_t"].cpu(), None,

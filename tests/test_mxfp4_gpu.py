@@ -66,6 +66,11 @@ def _kl_case(T, H, V, seed, rows=False):
     if rows:
         d["rows"] = torch.from_numpy(workloads.sample_rows(T, T // 2, seed=seed)).cuda()
     d["packed"], d["scales"] = flp.mxfp4_quantize(d["W_t"])
+    # the oracle's own quantisation of the teacher head (the oracle takes no
+    # input from the GPU); the two agree bit for bit
+    d["opacked"], d["oscales"] = coracle.mxfp4_quantize(d["W_t"].cpu(), "bf16")
+    assert np.array_equal(d["packed"].cpu().numpy(), d["opacked"])
+    assert np.array_equal(d["scales"].cpu().numpy(), d["oscales"])
     return d
 
 
@@ -81,14 +86,13 @@ def test_kl_mxfp4_matches_the_oracle(T, H, V, rows):
     torch.cuda.synchronize()
     r = None if d["rows"] is None else d["rows"].cpu().numpy()
     want = coracle.kl_mxfp4(d["h_s"].cpu(), d["W_s"].cpu(), d["h_t"].cpu(),
-                            d["packed"].cpu().numpy(), d["scales"].cpu().numpy(), r, "bf16")
+                            d["opacked"], d["oscales"], r, "bf16")
     got = kl.cpu().double().numpy()
     assert np.all(np.isfinite(got))
     err = np.abs(got - want).max()
     assert err <= TOL, err
     # the same numbers through the bf16 KL path, with the decoded weights as bf16
-    Wt_dec = torch.from_numpy(ref.mxfp4_dequantize(d["packed"].cpu().numpy(),
-                                                   d["scales"].cpu().numpy(), V))
+    Wt_dec = torch.from_numpy(ref.mxfp4_dequantize(d["opacked"], d["oscales"], V))
     Wt_bf = Wt_dec.to(torch.bfloat16)
     assert torch.equal(Wt_bf.double(), Wt_dec)      # every decoded value is a bf16 value
     kl2 = flp.kl_divergence(d["h_s"], d["W_s"], d["h_t"], Wt_bf.cuda(), d["rows"])
@@ -111,8 +115,9 @@ def test_distill_workload_with_mxfp4_teacher_sampled():
     kl = flp.kl_divergence_mxfp4(d["h_s"], d["W_s"], d["h_t"], packed, scales)
     torch.cuda.synchronize()
     pos = np.unique(np.concatenate([workloads.sample_rows(8192, 48, seed=74), [0, 8191]]))
-    want = coracle.kl_mxfp4(d["h_s"].cpu(), d["W_s"].cpu(), d["h_t"].cpu(), packed.cpu().numpy(),
-                            scales.cpu().numpy(), pos, "bf16")
+    opacked, oscales = coracle.mxfp4_quantize(d["W_t"].cpu(), "bf16")
+    want = coracle.kl_mxfp4(d["h_s"].cpu(), d["W_s"].cpu(), d["h_t"].cpu(), opacked, oscales, pos,
+                            "bf16")
     got = kl[torch.from_numpy(pos).cuda()].cpu().double().numpy()
     assert np.abs(got - want).max() <= TOL
     allkl = kl.cpu().numpy()
