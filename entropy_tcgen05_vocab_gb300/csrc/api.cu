@@ -615,6 +615,10 @@ flp_status kl_bs_impl(const flp_shape *s, const void *h_s, const void *W_s, cons
   if (st != FLP_OK) return st;
   if (s->H % kMxChunk != 0)
     return fail(FLP_ERR_INVALID_ARG, "H must be a multiple of 128 for the block-scaled teacher");
+  // the scale atoms are addressed by 32-bit tensor-map row coordinates
+  if (cdiv(s->V, kMxBN) * (s->H / kMxChunk) * 64 > (int64_t(1) << 31) - 64 ||
+      cdiv(s->n_rows, 128) * (s->H / kMxChunk) * 32 > (int64_t(1) << 31) - 32)
+    return fail(FLP_ERR_INVALID_ARG, "size beyond the block-scaled tiling range");
   if (s->n_rows == 0) return FLP_OK;
   if (!row_idx && s->n_rows != s->T)
     return fail(FLP_ERR_INVALID_ARG, "row_idx is NULL but n_rows != T");

@@ -122,10 +122,34 @@ def test_workspace_formula(L):
                     assert b < n * w.V * 4
             else:
                 assert b <= gathered + n * 128 * 4 * 4 + (4 << 30) + 4 * w.T + (1 << 20)
+    # the block-scaled KL: gathered student rows, the teacher rows in MXFP8
+    # (n*H bytes) and their scale atoms (n*H/32 bytes, whole 128-row blocks),
+    # plus the same per-row state; 0 when H is not a multiple of 128
+    w = workloads.WORKLOADS[3]
+    s = _shape(T=w.T, H=w.H, V=w.V, n=w.T)
+    b = L.flp_workspace_size(ctypes.byref(s), 3)
+    q8 = w.T * w.H + (w.T + 127) // 128 * (w.H // 128) * 512
+    assert q8 + w.T * w.H * 2 <= b <= q8 + w.T * w.H * 2 + w.T * 128 * 4 * 5 + (1 << 20)
+    assert L.flp_workspace_size(ctypes.byref(_shape(T=64, H=192, V=1000, n=64)), 3) == 0
     # monotone in the number of scored rows
     a = L.flp_workspace_size(ctypes.byref(_shape(T=4096, H=4096, V=151936, n=1000)), 0)
     b = L.flp_workspace_size(ctypes.byref(_shape(T=4096, H=4096, V=151936, n=2000)), 0)
     assert b > a
+
+
+def test_mx_head_layout_sizes(L):
+    """flp_mx_head_bytes: the E2M1 codes (V*H/2, rounded up to 1 KiB) and two
+    512-byte scale atoms per 224-row vocabulary tile and 128-wide k-chunk."""
+    L.flp_mx_head_bytes.argtypes = [ctypes.c_int64, ctypes.c_int64]
+    L.flp_mx_head_bytes.restype = ctypes.c_size_t
+    for V, H in ((129280, 4096), (224, 128), (225, 256), (1, 128)):
+        codes = -(-V * H // 2 // 1024) * 1024
+        assert L.flp_mx_head_bytes(V, H) == codes + -(-V // 224) * (H // 128) * 1024
+    assert L.flp_mx_head_bytes(1000, 192) == 0 and L.flp_mx_head_bytes(0, 128) == 0
+    # the workload-3 teacher head: 4 bits per weight plus a scale byte per 32
+    # weights, in atoms of 256 row slots per 224-row tile
+    bits = 8 * L.flp_mx_head_bytes(129280, 4096) / (129280 * 4096)
+    assert abs(bits - (4 + 8 / 32 * 256 / 224)) < 1e-3
 
 
 @pytest.mark.parametrize("wid", [0, 1, 2, 3, 4])
