@@ -8,8 +8,9 @@
  *
  * DIR holds h.bin (T x H bf16 bits), W.bin (V x H), ht.bin, Wt.bin (the
  * teacher's), targets.bin (T int64), rows.bin (N int64), g1.bin, g2.bin
- * (N float32).  Writes logp.bin, ent.bin, kl.bin (N float32), dh.bin
- * (T x H bf16 bits) and dW.bin (V x H float32).  Exit status 0 on success,
+ * (N float32).  Writes logp.bin, ent.bin, kl.bin, klmx.bin (N float32; the
+ * last with the teacher on the block-scaled tensor cores), dh.bin (T x H bf16
+ * bits) and dW.bin (V x H float32).  Exit status 0 on success,
  * 2 on a library or CUDA error (the reason is printed).
  */
 #include <stdint.h>
@@ -109,14 +110,24 @@ int main(int argc, char **argv) {
   }
   size_t ws_bytes = flp_workspace_size(&s, FLP_OP_LOGPROB_ENTROPY);
   const size_t ws_kl = flp_workspace_size(&s, FLP_OP_KL), ws_bw = flp_workspace_size(&s, FLP_OP_BACKWARD);
+  const size_t ws_klmx = flp_workspace_size(&s, FLP_OP_KL_MX);
   if (ws_kl > ws_bytes) ws_bytes = ws_kl;
   if (ws_bw > ws_bytes) ws_bytes = ws_bw;
+  if (ws_klmx > ws_bytes) ws_bytes = ws_klmx;
+  const size_t head_bytes = flp_mx_head_bytes(V, H);
+  if (ws_klmx == 0 || head_bytes == 0) {
+    fprintf(stderr, "H must be a multiple of 128 for the block-scaled teacher\n");
+    return 2;
+  }
   if (ws_bytes == 0) {
     fprintf(stderr, "flp_workspace_size rejected the shape\n");
     return 2;
   }
   void *ws = NULL, *d_logp = NULL, *d_ent = NULL, *d_kl = NULL, *d_dh = NULL, *d_dW = NULL;
+  void *d_head = NULL, *d_klmx = NULL;
   CUDA_OK(cudaMalloc(&ws, ws_bytes));
+  CUDA_OK(cudaMalloc(&d_head, head_bytes));
+  CUDA_OK(cudaMalloc(&d_klmx, (size_t)N * 4 + 16));
   CUDA_OK(cudaMalloc(&d_logp, (size_t)N * 4 + 16));
   CUDA_OK(cudaMalloc(&d_ent, (size_t)N * 4 + 16));
   CUDA_OK(cudaMalloc(&d_kl, (size_t)N * 4 + 16));
@@ -129,6 +140,10 @@ int main(int argc, char **argv) {
   flp_device_status st;
   FLP_OK_(flp_read_device_status(ws, &st, NULL));
   FLP_OK_(flp_kl(&s, d_h, d_W, d_ht, d_Wt, (const int64_t *)d_rows, (float *)d_kl, ws, ws_bytes, NULL));
+  FLP_OK_(flp_read_device_status(ws, &st, NULL));
+  FLP_OK_(flp_mx_head_quantize(d_Wt, FLP_BF16, V, H, H, d_head, NULL));
+  FLP_OK_(flp_kl_mx(&s, d_h, d_W, d_ht, d_head, (const int64_t *)d_rows, (float *)d_klmx, ws, ws_bytes,
+                    NULL));
   FLP_OK_(flp_read_device_status(ws, &st, NULL));
   FLP_OK_(flp_backward(&s, d_h, d_W, (const int64_t *)d_tg, (const int64_t *)d_rows, tau,
                        (const float *)d_g1, (const float *)d_g2, NULL, NULL, d_dh, (float *)d_dW, ws,
@@ -145,16 +160,19 @@ int main(int argc, char **argv) {
   CUDA_OK(cudaDeviceSynchronize());
 
   float *logp = malloc((size_t)N * 4 + 4), *ent = malloc((size_t)N * 4 + 4), *kl = malloc((size_t)N * 4 + 4);
+  float *klmx = malloc((size_t)N * 4 + 4);
   void *dh = malloc(hb);
   float *dW = malloc((size_t)V * H * 4);
-  if (!logp || !ent || !kl || !dh || !dW) return 2;
+  if (!logp || !ent || !kl || !klmx || !dh || !dW) return 2;
+  CUDA_OK(cudaMemcpy(klmx, d_klmx, (size_t)N * 4, cudaMemcpyDeviceToHost));
   CUDA_OK(cudaMemcpy(logp, d_logp, (size_t)N * 4, cudaMemcpyDeviceToHost));
   CUDA_OK(cudaMemcpy(ent, d_ent, (size_t)N * 4, cudaMemcpyDeviceToHost));
   CUDA_OK(cudaMemcpy(kl, d_kl, (size_t)N * 4, cudaMemcpyDeviceToHost));
   CUDA_OK(cudaMemcpy(dh, d_dh, hb, cudaMemcpyDeviceToHost));
   CUDA_OK(cudaMemcpy(dW, d_dW, (size_t)V * H * 4, cudaMemcpyDeviceToHost));
   if (write_file(dir, "logp.bin", logp, (size_t)N * 4) || write_file(dir, "ent.bin", ent, (size_t)N * 4) ||
-      write_file(dir, "kl.bin", kl, (size_t)N * 4) || write_file(dir, "dh.bin", dh, hb) ||
+      write_file(dir, "kl.bin", kl, (size_t)N * 4) || write_file(dir, "klmx.bin", klmx, (size_t)N * 4) ||
+      write_file(dir, "dh.bin", dh, hb) ||
       write_file(dir, "dW.bin", dW, (size_t)V * H * 4)) {
     fprintf(stderr, "writing the outputs failed\n");
     return 1;

@@ -1,8 +1,8 @@
 """The C ABI from a plain C program: no Python binding and no torch in the
 caller.  tests/c_caller/flp_c_caller.c is compiled with gcc against
 include/fusedlogp.h and the built libfusedlogp.so, fed seeded inputs from
-workloads.py through raw files, and its outputs (log-prob, entropy, KL, dh,
-dW) are compared with the float64 oracle: 1e-3 absolute for the per-row
+workloads.py through raw files, and its outputs (log-prob, entropy, KL with
+a bf16 and with a block-scaled teacher, dh, dW) are compared with the float64 oracle: 1e-3 absolute for the per-row
 values, 1e-2 relative (Frobenius) for the gradients.
 """
 import os
@@ -71,6 +71,9 @@ def test_plain_c_caller(tmp_path):
     assert np.abs(out("ent.bin", np.float32, (n,)) - o["ent"]).max() <= 1e-3
     want_kl = coracle.kl(d["h"], d["W"], k["h_t"], k["W_t"], rows, "bf16")
     assert np.abs(out("kl.bin", np.float32, (n,)) - want_kl).max() <= 1e-3
+    packed, scales = coracle.mxfp4_quantize(k["W_t"], "bf16")
+    want_klmx = coracle.kl_mx(d["h"], d["W"], k["h_t"], packed, scales, rows, "bf16")
+    assert np.abs(out("klmx.bin", np.float32, (n,)) - want_klmx).max() <= 1e-3
     dh_rows, dW = coracle.backward(d["h"], d["W"], d["targets"].numpy(), rows, tau,
                                    d["g1"].numpy(), d["g2"].numpy(), "bf16")
     dh = coracle.scatter_rows(dh_rows, rows, T)

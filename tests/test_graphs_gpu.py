@@ -75,3 +75,20 @@ def test_kl_replay():
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(out, flp.kl_divergence(d["h_s"], d["W_s"], d["h_t"], d["W_t"], workspace=ws))
+
+
+def test_block_scaled_kl_replay():
+    """The block-scaled KL (MXFP8 quantisation of the teacher rows, then the
+    pipeline) captured and replayed on new teacher rows."""
+    w = workloads.WORKLOADS[3].scaled(T=500, H=256, V=6000, seed=93)
+    d = workloads.make(w, device="cuda")
+    shape = flp.make_shape(w.T, w.H, w.V, w.T, torch.bfloat16)
+    ws = torch.empty(flp.workspace_size(shape, flp.OP_KL_MX), dtype=torch.uint8, device="cuda")
+    head = flp.mx_head_quantize(d["W_t"])
+    h_t = d["h_t"].clone()
+    g, out = _capture(lambda: flp.kl_divergence_mx(d["h_s"], d["W_s"], h_t, head, workspace=ws))
+    for scale in (1.0, 0.5):
+        h_t.copy_((d["h_t"].float() * scale).to(torch.bfloat16))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, flp.kl_divergence_mx(d["h_s"], d["W_s"], h_t, head, workspace=ws))

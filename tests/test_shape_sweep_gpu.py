@@ -11,7 +11,7 @@ random places: a part of a 128-row tile, of a 64-wide K block, of a
 (n <= 128) against the pair path.  Each case is small enough for the C
 oracle to finish in about a second.  The same cases also run the K-target
 forward, the forward and backward under a sampling support, and the KL with
-an MXFP4 teacher head.
+an MXFP4 teacher head, decoded and on the block-scaled tensor cores.
 
 Tolerances are those of the fixed-shape tests: |d logp|, |d ent|, |d KL|
 <= 1e-3 absolute; gradients within 1e-2 relative (Frobenius, and every
@@ -216,6 +216,28 @@ def test_kl_mxfp4_sweep(case):
     ri = None if rows is None else torch.from_numpy(rows).cuda()
     kl = flp.kl_divergence_mxfp4(d["h_s"], d["W_s"], d["h_t"], packed, scales, ri)
     torch.cuda.synchronize()
-    want = coracle.kl_mxfp4(d["h_s"].cpu(), d["W_s"].cpu(), d["h_t"].cpu(),
-                            packed.cpu().numpy(), scales.cpu().numpy(), rows, "bf16")
+    opacked, oscales = coracle.mxfp4_quantize(d["W_t"].cpu(), "bf16")   # the oracle's own
+    want = coracle.kl_mxfp4(d["h_s"].cpu(), d["W_s"].cpu(), d["h_t"].cpu(), opacked, oscales,
+                            rows, "bf16")
     _abs(kl, want, "kl (MXFP4 teacher)")
+
+
+BS_CASES = CASES[1::3]
+
+
+@pytest.mark.parametrize("case", BS_CASES, ids=[_id(c) for c in BS_CASES])
+def test_kl_block_scaled_sweep(case):
+    """The teacher on the block-scaled tensor cores (MXFP8 rows, MXFP4 head),
+    bf16 and fp16; the layout takes whole 128-wide k-chunks, so H is rounded
+    up to a multiple of 128."""
+    T, H, V, dtype, _, rows, seed = case
+    H = 128 * ((H + 127) // 128)
+    d = _scaled("kl", T, H, V, dtype, 1.0, seed)
+    head = flp.mx_head_quantize(d["W_t"])
+    ri = None if rows is None else torch.from_numpy(rows).cuda()
+    kl = flp.kl_divergence_mx(d["h_s"], d["W_s"], d["h_t"], head, ri)
+    torch.cuda.synchronize()
+    packed, scales = coracle.mxfp4_quantize(d["W_t"].cpu(), dtype)
+    want = coracle.kl_mx(d["h_s"].cpu(), d["W_s"].cpu(), d["h_t"].cpu(), packed, scales, rows,
+                         dtype)
+    _abs(kl, want, "kl (block-scaled teacher)")
