@@ -13,8 +13,9 @@
 // item = (256-row tile, vocabulary split) as in vocab_pipeline.cuh.  Two
 // operand rings per CTA, filled by one producer warp in the order the MMA
 // issuer consumes them:
-//   student ring  kMxSStages stages of one 64-wide k-block: A_s (128 x 64
-//                 bf16) and B_s (112 x 64 bf16), 128B-swizzled;
+//   student ring  kMxSStages stages of one 128-wide k-chunk: A_s (128 x 128
+//                 bf16, two 64-wide k-blocks) and B_s (112 x 128 bf16),
+//                 128B-swizzled, four tensor-map copies;
 //   teacher ring  kMxTStages stages of one 128-wide k-chunk: A_t (128 x 128
 //                 E4M3), B_t (112 x 128 E2M1 in the padded layout the MMA
 //                 reads: each 16 elements as 8 bytes of codes and an 8-byte
@@ -32,10 +33,17 @@
 // [224, 448), and 12 scale columns per teacher stage from 448 (4 for A, 8 for
 // B).  Per 128-wide k-chunk the MMA issuer copies the chunk's scales into
 // its stage's columns, issues four block-scaled MMAs (K = 32, scale id =
-// step) into the teacher accumulator and eight bf16 MMAs (K = 16, two
-// student k-blocks) into the student accumulator.  The copies and MMAs of
-// one thread execute in issue order, and a stage's scale columns are
-// rewritten only after the MMAs that read them released that stage.
+// step) into the teacher accumulator and eight bf16 MMAs (K = 16) into the
+// student accumulator, and commits twice (one release per ring).  Issuing
+// an MMA blocks the thread for about the MMA's own execution time (the
+// tensor pipe's queue is shallow), so every other operation the issuing
+// thread adds between MMAs -- a commit, a wait -- lengthens the pipe's
+// critical path: hence one student stage per k-chunk rather than one per
+// 64-wide k-block (a third fewer commits and waits).  A single ring of
+// whole k-chunks for both heads (one commit per k-chunk) fits only two
+// stages and was slower.  The copies and MMAs of one thread execute in
+// issue order, and a stage's scale columns are rewritten only after the
+// MMAs that read them released that stage.
 // Eight epilogue warps (two per TMEM lane quarter, 112 columns each) fold
 // the two accumulators 16 columns at a time with the KL epilogue.
 #pragma once
@@ -46,15 +54,15 @@
 namespace flp {
 
 constexpr int kMxBRows = kMxBN / 2;   // B rows per CTA
-constexpr int kMxSStages = 4;
+constexpr int kMxSStages = 2;
 constexpr int kMxTStages = 3;
 constexpr int kMxThreads = 64 + 32 * kMxEpiWarps;
 constexpr int kMxUmmaK = 32;          // K per block-scaled MMA
 
 struct MxPipeLayout {
-  static constexpr int kSA = kBM * kBK * 2;             // 16384
-  static constexpr int kSB = kMxBRows * kBK * 2;        // 14336
-  static constexpr int kSStage = kSA + kSB;             // 30720
+  static constexpr int kSA = kBM * kBK * 2;             // 16384: one 64-wide k-block of A_s
+  static constexpr int kSB = kMxBRows * kBK * 2;        // 14336: one k-block of B_s
+  static constexpr int kSStage = 2 * (kSA + kSB);       // 61440: A_s kb 0, 1 then B_s kb 0, 1
   static constexpr int kTA = kBM * kMxChunk;            // 16384: 128 rows x 128 E4M3
   static constexpr int kTB = kMxBRows * kMxChunk;       // 14336: padded E2M1 in shared memory
   static constexpr int kTBTx = kMxBRows * kMxChunk / 2; // 7168: code bytes the copy counts
@@ -191,25 +199,23 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             tph ^= 1u;
           }
           // student k-blocks 2c and 2c + 1
-          for (int h = 0; h < 2; ++h) {
-            if (lane == 0) ok = mbar_wait(&sempty[ss], sph ^ 1u, abort_flag, lim);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            if (lane == 0) {
-              uint8_t *sa = smem + ss * L::kSStage;
-              if (leader) mbar_arrive_expect_tx(&sfull[ss], CG * L::kSStage);
-              const uint32_t fb = sfull_dst + ss * 8;
-              const int kb = 2 * c + h;
-              tma_load_2d_pair(sa, &tmAs, fb, kb * kBK, arow);
-              tma_load_2d_pair(sa + L::kSA, &tmBs, fb, kb * kBK, brow);
-            }
-            ++s_issued;
-            if (++ss == kMxSStages) {
-              ss = 0;
-              sph ^= 1u;
-            }
-          }
+          if (lane == 0) ok = mbar_wait(&sempty[ss], sph ^ 1u, abort_flag, lim);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
+          if (lane == 0) {
+            uint8_t *sa = smem + ss * L::kSStage;
+            if (leader) mbar_arrive_expect_tx(&sfull[ss], CG * L::kSStage);
+            const uint32_t fb = sfull_dst + ss * 8;
+            tma_load_2d_pair(sa, &tmAs, fb, 2 * c * kBK, arow);
+            tma_load_2d_pair(sa + L::kSA, &tmAs, fb, (2 * c + 1) * kBK, arow);
+            tma_load_2d_pair(sa + 2 * L::kSA, &tmBs, fb, 2 * c * kBK, brow);
+            tma_load_2d_pair(sa + 2 * L::kSA + L::kSB, &tmBs, fb, (2 * c + 1) * kBK, brow);
+          }
+          ++s_issued;
+          if (++ss == kMxSStages) {
+            ss = 0;
+            sph ^= 1u;
+          }
         }
       }
     }
@@ -255,28 +261,28 @@ __global__ void __launch_bounds__(kMxThreads, 1)
               ts = 0;
               tph ^= 1u;
             }
-            for (int h = 0; h < 2; ++h) {
-              if (lane == 0) ok = mbar_wait(&sfull[ss], sph, abort_flag, lim);
-              ok = __shfl_sync(0xffffffffu, ok, 0);
-              if (!ok) break;
-              tc_fence_after();
-              if (lane == 0) {
-                const uint32_t sa = smem_u32(smem + ss * L::kSStage);
+            if (lane == 0) ok = mbar_wait(&sfull[ss], sph, abort_flag, lim);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            if (lane == 0) {
+              const uint32_t sa = smem_u32(smem + ss * L::kSStage);
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
 #pragma unroll
                 for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
-                  const uint64_t ad = sdesc_sw128(sa + kk * kUmmaK * 2, 16, 1024);
-                  const uint64_t bd = sdesc_sw128(sa + L::kSA + kk * kUmmaK * 2, 16, 1024);
+                  const uint64_t ad = sdesc_sw128(sa + h * L::kSA + kk * kUmmaK * 2, 16, 1024);
+                  const uint64_t bd =
+                      sdesc_sw128(sa + 2 * L::kSA + h * L::kSB + kk * kUmmaK * 2, 16, 1024);
                   mma_f16_pair(d_student, ad, bd, idesc_s, (c | h | kk) != 0 ? 1u : 0u);
                 }
-                mma_commit_pair(&sempty[ss], 0x3);
-              }
-              __syncwarp();
-              if (++ss == kMxSStages) {
-                ss = 0;
-                sph ^= 1u;
-              }
+              mma_commit_pair(&sempty[ss], 0x3);
             }
-            if (!ok) break;
+            __syncwarp();
+            if (++ss == kMxSStages) {
+              ss = 0;
+              sph ^= 1u;
+            }
           }
           if (!ok) break;
           if (lane == 0) mma_commit_pair(afull, 0x3);  // both accumulators ready
