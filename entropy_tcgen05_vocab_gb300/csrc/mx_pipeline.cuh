@@ -11,8 +11,8 @@
 //
 // CTA pairs (cluster of 2) on 256-row x 224-column tiles, persistent, one
 // item = (256-row tile, vocabulary split) as in vocab_pipeline.cuh.  Two
-// operand rings per CTA, filled by one producer warp in the order the MMA
-// issuer consumes them:
+// operand rings per CTA, each with its own producer warp and (in the leader
+// CTA) its own MMA-issuing thread:
 //   student ring  kMxSStages stages of one 128-wide k-chunk: A_s (128 x 128
 //                 bf16, two 64-wide k-blocks) and B_s (112 x 128 bf16),
 //                 128B-swizzled, four tensor-map copies;
@@ -31,19 +31,21 @@
 // row's lane quarter, column n / 32; step j in byte j).
 // TMEM (512 columns): student accumulator [0, 224), teacher accumulator
 // [224, 448), and 12 scale columns per teacher stage from 448 (4 for A, 8 for
-// B).  Per 128-wide k-chunk the MMA issuer copies the chunk's scales into
-// its stage's columns, issues four block-scaled MMAs (K = 32, scale id =
-// step) into the teacher accumulator and eight bf16 MMAs (K = 16) into the
-// student accumulator, and commits twice (one release per ring).  Issuing
-// an MMA blocks the thread for about the MMA's own execution time (the
-// tensor pipe's queue is shallow), so every other operation the issuing
-// thread adds between MMAs -- a commit, a wait -- lengthens the pipe's
-// critical path: hence one student stage per k-chunk rather than one per
-// 64-wide k-block (a third fewer commits and waits).  A single ring of
-// whole k-chunks for both heads (one commit per k-chunk) fits only two
-// stages and was slower.  The copies and MMAs of one thread execute in
-// issue order, and a stage's scale columns are rewritten only after the
-// MMAs that read them released that stage.
+// B).  Per 128-wide k-chunk the teacher's issuer copies the chunk's scales
+// into its stage's columns and issues four block-scaled MMAs (K = 32, scale
+// id = step) into the teacher accumulator; the student's issuer issues
+// eight bf16 MMAs (K = 16) into the student accumulator; each commits once
+// to release its stage.  Issuing an MMA blocks the thread for about the
+// MMA's own execution time (the tensor pipe's queue is shallow), so every
+// other operation an issuing thread adds between MMAs -- a commit, a wait
+// -- would stretch the pipe's critical path if one thread issued both
+// heads; with two issuers one keeps the pipe fed while the other waits or
+// commits.  For the same reason a student stage is a whole 128-wide k-chunk
+// (one commit and one wait per eight MMAs).  The copies and MMAs of one
+// thread execute in issue order, and a stage's scale columns are rewritten
+// only after the MMAs that read them released that stage.  Each issuer
+// commits to the accumulators' "full" barrier once per tile (two arrivals)
+// and both wait for the epilogue to hand the accumulators back.
 // Eight epilogue warps (two per TMEM lane quarter, 112 columns each) fold
 // the two accumulators 16 columns at a time with the KL epilogue.
 #pragma once
@@ -56,7 +58,11 @@ namespace flp {
 constexpr int kMxBRows = kMxBN / 2;   // B rows per CTA
 constexpr int kMxSStages = 2;
 constexpr int kMxTStages = 3;
-constexpr int kMxThreads = 64 + 32 * kMxEpiWarps;
+// warps: 0 student producer, 1 TMEM allocation + student MMA issuer, 2..9
+// epilogue, 10 teacher producer, 11 teacher MMA issuer
+constexpr int kMxTProdWarp = 2 + kMxEpiWarps;
+constexpr int kMxTMmaWarp = kMxTProdWarp + 1;
+constexpr int kMxThreads = 32 * (kMxTMmaWarp + 1);
 constexpr int kMxUmmaK = 32;          // K per block-scaled MMA
 
 struct MxPipeLayout {
@@ -72,7 +78,7 @@ struct MxPipeLayout {
   static constexpr int kTTx = kTA + kTBTx + kSfa + kSfb;  // bytes one CTA's teacher copies count
   static constexpr int kTRing = kMxSStages * kSStage;
   static constexpr int kRingBytes = kTRing + kMxTStages * kTStage;
-  static constexpr int kBarrierBytes = 8 * (2 * kMxSStages + 2 * kMxTStages + 3) + 32;
+  static constexpr int kBarrierBytes = 8 * (2 * kMxSStages + 2 * kMxTStages + 4) + 32;
   static constexpr int kSmemBytes = kRingBytes + kBarrierBytes + 1024;
   static constexpr int kTmemCols = 512;
   static constexpr int kSfCol0 = 2 * kMxBN;
@@ -117,8 +123,9 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   uint64_t *tempty = tfull + kMxTStages;
   uint64_t *afull = tempty + kMxTStages;  // accumulators ready for the epilogue
   uint64_t *aempty = afull + 1;           // accumulators drained
-  uint64_t *drain = aempty + 1;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  uint64_t *drain = aempty + 1;           // student issuer's teardown
+  uint64_t *tdrain = drain + 1;           // teacher issuer's teardown
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tdrain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   // iterations of the two rings the peer's producer issued (written at teardown)
   volatile uint32_t *peer_issued = reinterpret_cast<volatile uint32_t *>(tmem_slot + 2);
@@ -142,9 +149,10 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       mbar_init(&tfull[s], 1);
       mbar_init(&tempty[s], 1);
     }
-    mbar_init(afull, 1);
+    mbar_init(afull, 2);  // one commit per issuer
     mbar_init(aempty, kMxEpiWarps * CG);
     mbar_init(drain, 1);
+    mbar_init(tdrain, 1);
     *abort_flag = 0;
     peer_issued[0] = 0;
     peer_issued[1] = 0;
@@ -165,13 +173,16 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   pipe_sync<CG>();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    int ss = 0, ts = 0;
-    uint32_t sph = 0, tph = 0;
+  if (warp == 0 || warp == kMxTProdWarp) {
+    // ----------------------------------------------------------- producers
+    // Warp 0 fills the student ring, warp kMxTProdWarp the teacher ring.
+    const bool teacher = warp == kMxTProdWarp;
+    int st = 0;
+    uint32_t ph = 0, issued = 0;
     bool ok = true;
-    const uint32_t sfull_dst = mapa_shared(smem_u32(sfull), 0);
-    const uint32_t tfull_dst = mapa_shared(smem_u32(tfull), 0);
+    const uint32_t full_dst = mapa_shared(smem_u32(teacher ? tfull : sfull), 0);
+    uint64_t *empty = teacher ? tempty : sempty;
+    const int stages = teacher ? kMxTStages : kMxSStages;
     for (int it = unit; ok && it < sch.items; it += num_units) {
       int mt, sp, vt0, vt1;
       sch.item(it, mt, sp, vt0, vt1);
@@ -180,52 +191,58 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       for (int vt = vt0; ok && vt < vt1; ++vt) {
         const int brow = vt * kMxBN + static_cast<int>(rank) * kMxBRows;
         for (int c = 0; c < kc_n; ++c) {
-          // teacher k-chunk c
-          if (lane == 0) ok = mbar_wait(&tempty[ts], tph ^ 1u, abort_flag, lim);
+          if (lane == 0) ok = mbar_wait(&empty[st], ph ^ 1u, abort_flag, lim);
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
           if (lane == 0) {
-            uint8_t *base = smem + L::kTRing + ts * L::kTStage;
-            if (leader) mbar_arrive_expect_tx(&tfull[ts], CG * L::kTTx);
-            const uint32_t fb = tfull_dst + ts * 8;
-            tma_load_2d_pair(base, &tmAt, fb, c * kMxChunk, arow);
-            tma_load_2d_pair(base + L::kTA, &tmBt, fb, c * kMxChunk, brow);
-            tma_load_2d_pair(base + L::kTA + L::kTB, &tmSfa, fb, 0, (ablk * kc_n + c) * 32);
-            tma_load_2d_pair(base + L::kTA + L::kTB + L::kSfa, &tmSfb, fb, 0, (vt * kc_n + c) * 64);
+            const uint32_t fb = full_dst + st * 8;
+            if (teacher) {
+              // teacher k-chunk c: codes of A_t and B_t, then the scale atoms
+              uint8_t *base = smem + L::kTRing + st * L::kTStage;
+              if (leader) mbar_arrive_expect_tx(&tfull[st], CG * L::kTTx);
+              tma_load_2d_pair(base, &tmAt, fb, c * kMxChunk, arow);
+              tma_load_2d_pair(base + L::kTA, &tmBt, fb, c * kMxChunk, brow);
+              tma_load_2d_pair(base + L::kTA + L::kTB, &tmSfa, fb, 0, (ablk * kc_n + c) * 32);
+              tma_load_2d_pair(base + L::kTA + L::kTB + L::kSfa, &tmSfb, fb, 0,
+                               (vt * kc_n + c) * 64);
+            } else {
+              // student k-blocks 2c and 2c + 1
+              uint8_t *sa = smem + st * L::kSStage;
+              if (leader) mbar_arrive_expect_tx(&sfull[st], CG * L::kSStage);
+              tma_load_2d_pair(sa, &tmAs, fb, 2 * c * kBK, arow);
+              tma_load_2d_pair(sa + L::kSA, &tmAs, fb, (2 * c + 1) * kBK, arow);
+              tma_load_2d_pair(sa + 2 * L::kSA, &tmBs, fb, 2 * c * kBK, brow);
+              tma_load_2d_pair(sa + 2 * L::kSA + L::kSB, &tmBs, fb, (2 * c + 1) * kBK, brow);
+            }
           }
-          ++t_issued;
-          if (++ts == kMxTStages) {
-            ts = 0;
-            tph ^= 1u;
-          }
-          // student k-blocks 2c and 2c + 1
-          if (lane == 0) ok = mbar_wait(&sempty[ss], sph ^ 1u, abort_flag, lim);
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) break;
-          if (lane == 0) {
-            uint8_t *sa = smem + ss * L::kSStage;
-            if (leader) mbar_arrive_expect_tx(&sfull[ss], CG * L::kSStage);
-            const uint32_t fb = sfull_dst + ss * 8;
-            tma_load_2d_pair(sa, &tmAs, fb, 2 * c * kBK, arow);
-            tma_load_2d_pair(sa + L::kSA, &tmAs, fb, (2 * c + 1) * kBK, arow);
-            tma_load_2d_pair(sa + 2 * L::kSA, &tmBs, fb, 2 * c * kBK, brow);
-            tma_load_2d_pair(sa + 2 * L::kSA + L::kSB, &tmBs, fb, (2 * c + 1) * kBK, brow);
-          }
-          ++s_issued;
-          if (++ss == kMxSStages) {
-            ss = 0;
-            sph ^= 1u;
+          ++issued;
+          if (++st == stages) {
+            st = 0;
+            ph ^= 1u;
           }
         }
       }
     }
+    if (teacher)
+      t_issued = issued;
+    else
+      s_issued = issued;
     if (!ok && lane == 0) record_timeout<CG>(status, abort_flag);
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == kMxTMmaWarp) {
+    // --------------------------------------------------------- MMA issuers
+    // Warp 1 issues the student's bf16 MMAs, warp kMxTMmaWarp the teacher's
+    // scale copies and block-scaled MMAs.  Each thread's commits track only
+    // its own tcgen05 operations, so while one issuer waits for a stage or
+    // commits, the other keeps the tensor pipe fed.  Both commit to "afull"
+    // (two arrivals per tile) and both wait for the epilogue's "aempty".
     if (leader) {
-      int ss = 0, ts = 0;
-      uint32_t sph = 0, tph = 0, aph = 0;
+      const bool teacher = warp == kMxTMmaWarp;
+      int st = 0;
+      uint32_t ph = 0, aph = 0;
       bool ok = true;
+      uint64_t *full = teacher ? tfull : sfull;
+      uint64_t *empty = teacher ? tempty : sempty;
+      const int stages = teacher ? kMxTStages : kMxSStages;
       const uint32_t d_student = tmem_base;
       const uint32_t d_teacher = tmem_base + kMxBN;
       for (int it = unit; ok && it < sch.items; it += num_units) {
@@ -237,55 +254,47 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           if (!ok) break;
           tc_fence_after();
           for (int c = 0; c < kc_n; ++c) {
-            if (lane == 0) ok = mbar_wait(&tfull[ts], tph, abort_flag, lim);
+            if (lane == 0) ok = mbar_wait(&full[st], ph, abort_flag, lim);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after();
             if (lane == 0) {
-              const uint32_t tb = smem_u32(smem + L::kTRing + ts * L::kTStage);
-              const uint32_t sf = tmem_base + static_cast<uint32_t>(L::kSfCol0 + ts * L::kSfCols);
-              tmem_cp_32x128b_x4_pair(sf, sdesc_rows16(tb + L::kTA + L::kTB));
-              tmem_cp_32x128b_x4_pair(sf + 4, sdesc_rows16(tb + L::kTA + L::kTB + L::kSfa));
-              tmem_cp_32x128b_x4_pair(sf + 8, sdesc_rows16(tb + L::kTA + L::kTB + L::kSfa + 512));
+              if (teacher) {
+                const uint32_t tb = smem_u32(smem + L::kTRing + st * L::kTStage);
+                const uint32_t sf = tmem_base + static_cast<uint32_t>(L::kSfCol0 + st * L::kSfCols);
+                tmem_cp_32x128b_x4_pair(sf, sdesc_rows16(tb + L::kTA + L::kTB));
+                tmem_cp_32x128b_x4_pair(sf + 4, sdesc_rows16(tb + L::kTA + L::kTB + L::kSfa));
+                tmem_cp_32x128b_x4_pair(sf + 8,
+                                        sdesc_rows16(tb + L::kTA + L::kTB + L::kSfa + 512));
 #pragma unroll
-              for (int j = 0; j < kMxChunk / kMxUmmaK; ++j) {
-                const uint64_t ad = sdesc_sw128(tb + j * kMxUmmaK, 16, 1024);
-                const uint64_t bd = sdesc_sw128(tb + L::kTA + j * kMxUmmaK, 16, 1024);
-                mma_mx_pair(d_teacher, ad, bd, idesc_mx_sf(idesc_t, static_cast<uint32_t>(j)), sf,
-                            sf + 4, (c | j) != 0 ? 1u : 0u);
-              }
-              mma_commit_pair(&tempty[ts], 0x3);
-            }
-            __syncwarp();
-            if (++ts == kMxTStages) {
-              ts = 0;
-              tph ^= 1u;
-            }
-            if (lane == 0) ok = mbar_wait(&sfull[ss], sph, abort_flag, lim);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            tc_fence_after();
-            if (lane == 0) {
-              const uint32_t sa = smem_u32(smem + ss * L::kSStage);
-#pragma unroll
-              for (int h = 0; h < 2; ++h)
-#pragma unroll
-                for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
-                  const uint64_t ad = sdesc_sw128(sa + h * L::kSA + kk * kUmmaK * 2, 16, 1024);
-                  const uint64_t bd =
-                      sdesc_sw128(sa + 2 * L::kSA + h * L::kSB + kk * kUmmaK * 2, 16, 1024);
-                  mma_f16_pair(d_student, ad, bd, idesc_s, (c | h | kk) != 0 ? 1u : 0u);
+                for (int j = 0; j < kMxChunk / kMxUmmaK; ++j) {
+                  const uint64_t ad = sdesc_sw128(tb + j * kMxUmmaK, 16, 1024);
+                  const uint64_t bd = sdesc_sw128(tb + L::kTA + j * kMxUmmaK, 16, 1024);
+                  mma_mx_pair(d_teacher, ad, bd, idesc_mx_sf(idesc_t, static_cast<uint32_t>(j)),
+                              sf, sf + 4, (c | j) != 0 ? 1u : 0u);
                 }
-              mma_commit_pair(&sempty[ss], 0x3);
+              } else {
+                const uint32_t sa = smem_u32(smem + st * L::kSStage);
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                  for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
+                    const uint64_t ad = sdesc_sw128(sa + h * L::kSA + kk * kUmmaK * 2, 16, 1024);
+                    const uint64_t bd =
+                        sdesc_sw128(sa + 2 * L::kSA + h * L::kSB + kk * kUmmaK * 2, 16, 1024);
+                    mma_f16_pair(d_student, ad, bd, idesc_s, (c | h | kk) != 0 ? 1u : 0u);
+                  }
+              }
+              mma_commit_pair(&empty[st], 0x3);
             }
             __syncwarp();
-            if (++ss == kMxSStages) {
-              ss = 0;
-              sph ^= 1u;
+            if (++st == stages) {
+              st = 0;
+              ph ^= 1u;
             }
           }
           if (!ok) break;
-          if (lane == 0) mma_commit_pair(afull, 0x3);  // both accumulators ready
+          if (lane == 0) mma_commit_pair(afull, 0x3);  // this issuer's accumulator is ready
           __syncwarp();
           aph ^= 1u;
         }
@@ -324,21 +333,25 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     if (!ok && lane == 0) record_timeout<CG>(status, abort_flag);
   }
 
-  // Teardown (as in vocab_pipeline_kernel, for both rings).
-  if (warp == 0 && lane == 0 && !leader) {
+  // Teardown (as in vocab_pipeline_kernel, for both rings and both issuers).
+  if (lane == 0 && !leader && (warp == 0 || warp == kMxTProdWarp)) {
     const uint32_t pi = mapa_shared(smem_u32(const_cast<uint32_t *>(peer_issued)), 0);
-    st_cluster_u32(pi, s_issued);
-    st_cluster_u32(pi + 4, t_issued);
+    if (warp == 0)
+      st_cluster_u32(pi, s_issued);
+    else
+      st_cluster_u32(pi + 4, t_issued);
   }
   pipe_sync<CG>();
   if (*abort_flag) {
     if (leader && lane == 0) {
-      if (warp == 0) {
+      if (warp == 0)
         drain_copies<kMxSStages, CG>(sfull, s_issued, peer_issued[0], L::kSStage);
+      else if (warp == kMxTProdWarp)
         drain_copies<kMxTStages, CG>(tfull, t_issued, peer_issued[1], L::kTTx);
-      } else if (warp == 1) {
+      else if (warp == 1)
         drain_mmas<CG>(drain);
-      }
+      else if (warp == kMxTMmaWarp)
+        drain_mmas<CG>(tdrain);
     }
     pipe_sync<CG>();
   }
