@@ -46,6 +46,9 @@ def lib():
         _lib.orc_e4m3_value.restype = dbl
         _lib.orc_kl_mx.argtypes = [i64, i64, vp, vp, vp, vp, vp, i64, ip, i64, i64, vp, i64, vp]
         _lib.orc_kl_mx.restype = ip
+        _lib.orc_logprob_entropy_mx.argtypes = [i64, i64, vp, ip, i64, vp, vp, i64, vp, i64,
+                                                i64, vp, dbl, vp, vp, vp, vp]
+        _lib.orc_logprob_entropy_mx.restype = ip
         _lib.orc_num_threads.restype = ip
         for f in (_lib.orc_logprob_entropy, _lib.orc_kl, _lib.orc_backward):
             f.restype = ip
@@ -327,4 +330,26 @@ def kl_mx(h_s, W_s, h_t, packed, scales, rows, dtype):
                          _ptr(rows), rows.shape[0], out.ctypes.data)
     if rc:
         raise RuntimeError("oracle kl_mx failed: %d" % rc)
+    return out
+
+
+def logprob_entropy_mx(h, packed, scales, V, targets, rows, tau, dtype):
+    """Per scored row logp, ent, lse, ez on the block-scaled path: the rows
+    h[rows] quantised to MXFP8, the head in MXFP4 (blocked layout, V rows)."""
+    hs, ht, ldh = storage(h, dtype)
+    packed = np.ascontiguousarray(packed, np.uint8)
+    scales = np.ascontiguousarray(scales, np.uint8)
+    T, H = hs.shape[0], ldh
+    rows = _i64(rows if rows is not None else np.arange(T))
+    tg = _i64(targets)
+    n = rows.shape[0]
+    out = {k: np.empty(n, dtype=np.float64) for k in ("logp", "ent", "lse", "ez")}
+    rc = lib().orc_logprob_entropy_mx(H, int(V), hs.ctypes.data, ht, ldh, packed.ctypes.data,
+                                      scales.ctypes.data, packed.shape[1], _ptr(rows), n, T,
+                                      _ptr(tg), float(tau), out["logp"].ctypes.data,
+                                      out["ent"].ctypes.data, out["lse"].ctypes.data,
+                                      out["ez"].ctypes.data)
+    if rc == -2:
+        raise MemoryError("oracle allocation failed")
+    out["rc"] = rc
     return out

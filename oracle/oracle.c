@@ -811,3 +811,48 @@ int orc_kl_mx(int64_t H, int64_t V,
     free(hds); free(hdt); free(zs); free(zt);
     return 0;
 }
+
+/*
+ * Log-prob and entropy on the block-scaled path (DeepSeek-V4 book ch. 19,
+ * "1. FP4 in OPD": every forward that needs no backward -- among them the
+ * reference model's log-probs for the KL baseline -- runs in native 4-bit
+ * precision).  The head W is MXFP4 in the blocked layout of orc_kl_mxfp4,
+ * and each scored row h[rows[i]] is first quantised to MXFP8 by
+ * orc_mxfp8_block; z is the float64 product of the two decoded operands,
+ * and logp, entropy, LSE and E[z'] follow as in orc_logprob_entropy.
+ * H a multiple of 64.  Bad rows and targets give NaN as there (return -1).
+ */
+int orc_logprob_entropy_mx(int64_t H, int64_t V,
+                           const void *h, int htype, int64_t ld_h,
+                           const uint8_t *W_packed, const uint8_t *W_scales, int64_t V_pad,
+                           const int64_t *rows, int64_t n, int64_t T,
+                           const int64_t *targets, double tau,
+                           double *logp, double *ent, double *lse_out, double *ez_out)
+{
+    int64_t i, k0;
+    int rc;
+    orc_mx_matrix w;
+    double *hq = (double *)malloc((size_t)(n > 0 ? n : 1) * H * sizeof(double));
+    int64_t *r2 = (int64_t *)malloc((size_t)(n > 0 ? n : 1) * sizeof(int64_t));
+    int64_t *tg = (int64_t *)malloc((size_t)(n > 0 ? n : 1) * sizeof(int64_t));
+    if (!hq || !r2 || !tg) { free(hq); free(r2); free(tg); return -2; }
+    /* the scored rows, quantised, become rows 0..n-1 of hq; a bad index stays bad */
+    for (i = 0; i < n; ++i) {
+        if (rows[i] < 0 || rows[i] >= T) { r2[i] = -1; tg[i] = 0; continue; }
+        r2[i] = i;
+        tg[i] = targets[rows[i]];
+        orc_decode(h, htype, rows[i] * ld_h, H, hq + i * H);
+        for (k0 = 0; k0 < H; k0 += 32) {
+            uint8_t c[32], sc;
+            int j;
+            double *x = hq + i * H + k0;
+            orc_mxfp8_block(x, c, &sc);
+            for (j = 0; j < 32; ++j) x[j] = ldexp(orc_e4m3(c[j]), (int)sc - 127);
+        }
+    }
+    w.packed = W_packed; w.scales = W_scales; w.V_pad = V_pad; w.H = H;
+    rc = orc_logprob_entropy(H, V, hq, ORC_F64, H, &w, ORC_MXFP4, H, r2, n, n, tg, tau,
+                             logp, ent, lse_out, ez_out);
+    free(hq); free(r2); free(tg);
+    return rc;
+}

@@ -320,3 +320,17 @@ def kl_mx(h_s, W_s, h_t, packed, scales, rows, dtype, block=256):
         lt = lt - _lse(lt)[:, None]
         out[i0:i0 + block] = (np.exp(lt) * (lt - ls)).sum(axis=1)
     return out
+
+
+def logprob_entropy_mx(h, packed, scales, V, targets, rows, tau, dtype, block=256):
+    """logp, ent, lse, ez per scored row on the block-scaled path: each scored
+    row of h quantised to MXFP8 (mxfp8_quantize above), the head in MXFP4
+    (blocked layout, decoded by mxfp4_dequantize)."""
+    hd = np.asarray(decode(h, dtype))
+    Wd = mxfp4_dequantize(packed, scales, V)
+    rows = _rows(rows, hd.shape[0])
+    tg = np.asarray(targets, dtype=np.int64)[rows]
+    hq = mxfp8_dequantize(*mxfp8_quantize(hd[rows], "f64")) if rows.shape[0] else hd[rows]
+    lse, ez = row_stats(hq, Wd, np.arange(rows.shape[0]), tau, block)
+    logp = np.einsum("ik,ik->i", hq, Wd[tg]) / tau - lse
+    return {"logp": logp, "ent": lse - ez, "lse": lse, "ez": ez}

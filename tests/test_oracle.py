@@ -827,3 +827,70 @@ def test_kl_block_scaled_teacher_c_and_numpy_agree():
     # the teacher rows' quantisation moves the KL, but not by much
     base = coracle.kl_mxfp4(d["h_s"], d["W_s"], d["h_t"], packed, scales, rows, "bf16")
     assert np.all(np.abs(got - base) < 0.2 * base)
+
+
+# --------------------------------------------------------------------------
+# Log-prob and entropy on the block-scaled path (an inference-only forward,
+# e.g. the reference model's log-probs): MXFP8 rows x MXFP4 head
+
+def test_logprob_entropy_block_scaled_is_the_plain_forward_on_the_decoded_operands():
+    """Rows on the MXFP8 grid are left alone by the quantisation and the head
+    is its decoded MXFP4 values, so the block-scaled forward equals the plain
+    forward on those values; rows off the grid score as their MXFP8 values."""
+    w = workloads.WORKLOADS[1].scaled(T=14, H=128, V=300, seed=86)
+    d = workloads.make(w)
+    packed, scales = coracle.mxfp4_quantize(d["W"], "bf16")
+    Wd = coracle.mxfp4_dequantize(packed, scales, 300)
+    Wd_bits = _bits(Wd, "bf16").reshape(Wd.shape)                  # exact in bf16
+    assert np.array_equal(ref.decode(Wd_bits, "bf16"), Wd)
+    hq = coracle.mxfp8_dequantize(*coracle.mxfp8_quantize(d["h"], "bf16"))
+    hq_bits = _bits(hq, "bf16").reshape(hq.shape)
+    assert np.array_equal(ref.decode(hq_bits, "bf16"), hq)
+    rows = np.array([13, 0, 6, 6, 2])
+    tg = d["targets"]
+    for h in (hq_bits, d["h"]):   # on the grid, then the raw rows
+        got = coracle.logprob_entropy_mx(h, packed, scales, 300, tg, rows, 0.7, "bf16")
+        want = coracle.logprob_entropy(hq_bits, Wd_bits, tg, rows, 0.7, "bf16")
+        for k in ("logp", "ent", "lse", "ez"):
+            np.testing.assert_allclose(got[k], want[k], rtol=1e-13, atol=1e-13)
+        assert got["rc"] == 0
+    # the quantisation moves the scores, but not by much at these sizes
+    plain = coracle.logprob_entropy(d["h"], d["W"], tg, rows, 0.7, "bf16")
+    assert np.all(np.abs(got["ent"] - plain["ent"]) < 0.05 * plain["ent"])
+
+
+def test_logprob_entropy_block_scaled_closed_forms_and_bounds():
+    """A zero head gives logp = -ln V and entropy = ln V; every row keeps
+    logp <= 0 and 0 <= entropy <= ln V; a bad row index gives NaN."""
+    w = workloads.WORKLOADS[1].scaled(T=9, H=64, V=257, seed=87)
+    d = workloads.make(w)
+    zero = np.zeros((257, 64))
+    packed, scales = coracle.mxfp4_quantize(zero, "f64")
+    assert not packed.any() and not scales.any()
+    out = coracle.logprob_entropy_mx(d["h"], packed, scales, 257, d["targets"], None, 1.3, "bf16")
+    np.testing.assert_allclose(out["logp"], -LN(257), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(out["ent"], LN(257), rtol=0, atol=1e-12)
+    packed, scales = coracle.mxfp4_quantize(d["W"], "bf16")
+    rows = np.array([8, -1, 3, 9])
+    out = coracle.logprob_entropy_mx(d["h"], packed, scales, 257, d["targets"], rows, 0.7, "bf16")
+    assert out["rc"] == -1
+    ok = np.array([True, False, True, False])
+    assert np.all(np.isnan(out["logp"][~ok])) and np.all(np.isnan(out["ent"][~ok]))
+    assert np.all(out["logp"][ok] <= 0)
+    assert np.all((out["ent"][ok] >= 0) & (out["ent"][ok] <= LN(257)))
+
+
+def test_logprob_entropy_block_scaled_c_and_numpy_agree():
+    w = workloads.WORKLOADS[1].scaled(T=40, H=256, V=700, seed=88)
+    d = workloads.make(w)
+    packed, scales = coracle.mxfp4_quantize(d["W"], "bf16")
+    rows = np.array([39, 3, 7, 0, 3, 22])
+    got = coracle.logprob_entropy_mx(d["h"], packed, scales, 700, d["targets"], rows, 0.7, "bf16")
+    want = ref.logprob_entropy_mx(d["h"], packed, scales, 700, d["targets"], rows, 0.7, "bf16")
+    for k in ("logp", "ent", "lse", "ez"):
+        np.testing.assert_allclose(got[k], want[k], rtol=1e-10, atol=1e-11)
+    got16 = coracle.logprob_entropy_mx(_bits(ref.decode(d["h"], "bf16"), "fp16").reshape(40, 256),
+                                       packed, scales, 700, d["targets"], rows, 1.0, "fp16")
+    want16 = ref.logprob_entropy_mx(_bits(ref.decode(d["h"], "bf16"), "fp16").reshape(40, 256),
+                                    packed, scales, 700, d["targets"], rows, 1.0, "fp16")
+    np.testing.assert_allclose(got16["logp"], want16["logp"], rtol=1e-10, atol=1e-11)
