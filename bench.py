@@ -48,7 +48,8 @@ import torch  # noqa: E402
 METRIC = "scored tokens/s and TFLOP/s (% of GB300 dense BF16 peak), fused logp+entropy"
 UNIT = "scored tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-FWD_KERNEL_SOURCES = ["ptx.cuh", "schedule.h", "vocab_pipeline.cuh", "kernels_fwd.cu", "launch.h"]
+FWD_KERNEL_SOURCES = ["ptx.cuh", "schedule.h", "vocab_pipeline.cuh", "kernels_fwd.cu", "launch.h",
+                      "lse_epilogue.cuh", "support.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "vocab_pipeline_forward-scoring.txt")
 
 
@@ -65,6 +66,9 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--T", type=int, default=None,
                    help="replace the workload's row count (same H, V, recipe): small profiling cases")
+    p.add_argument("--head", choices=["bf16", "mx"], default="bf16",
+                   help="forward workloads: the head in bf16, or in MXFP4 on the block-scaled "
+                        "tensor cores with the scored rows in MXFP8 (head quantised before timing)")
     p.add_argument("--teacher", choices=["bf16", "mxfp4", "mx"], default="bf16",
                    help="KL workloads: the teacher head in bf16, in MXFP4 decoded to bf16 next to "
                         "the tensor cores, or (mx) MXFP4 on the block-scaled tensor cores with the "
@@ -231,6 +235,9 @@ def flops_per_call(d):
 def call_once(flp, d, ws, stats=None):
     w = d["workload"]
     if w.kind == "fwd":
+        if d.get("mx_head") is not None:
+            return flp.logprob_entropy_mx(d["h"], d["mx_head"], w.V, d["targets"], d["row_idx"],
+                                          d["tau"], workspace=ws)
         return flp.logprob_entropy(d["h"], d["W"], d["targets"], d["row_idx"], d["tau"],
                                    workspace=ws, support=d.get("support"))
     if w.kind == "kl":
@@ -277,6 +284,8 @@ def memory_footprint(flp, d, ws, device):
 def op_of(d):
     if d["workload"].kind == "kl" and d.get("mx_head") is not None:
         return 3     # the block-scaled KL's workspace (it holds the MXFP8 teacher rows)
+    if d["workload"].kind == "fwd" and d.get("mx_head") is not None:
+        return 4     # the block-scaled forward's (it holds the MXFP8 scored rows)
     return {"fwd": 0, "kl": 1, "bwd": 2}[d["workload"].kind]
 
 
@@ -284,6 +293,8 @@ def launches_per_call(d):
     w = d["workload"]
     gather = 1 if d["row_idx"] is not None else 0
     if w.kind == "fwd":
+        if d.get("mx_head") is not None:
+            return 2               # MXFP8 quantiser (it gathers) + the block-scaled pipeline
         return gather + 1          # (gather) + the fused scoring kernel
     if w.kind == "kl":
         if d.get("mx_head") is not None:   # (gather of h_s) + MXFP8 quantiser + pipeline
@@ -392,7 +403,11 @@ def time_e2e(flp, d, ws, steps, world, device):
         compute.wait_event(ready[i % 2])
         if not last:
             load(i + 1)
-        logp, ent = flp.logprob_entropy(hb, d["W"], tb, rb, d["tau"], workspace=ws)
+        if d.get("mx_head") is not None:
+            logp, ent = flp.logprob_entropy_mx(hb, d["mx_head"], d["workload"].V, tb, rb,
+                                               d["tau"], workspace=ws)
+        else:
+            logp, ent = flp.logprob_entropy(hb, d["W"], tb, rb, d["tau"], workspace=ws)
         free[i % 2].record(compute)
         lp_pin.copy_(logp, non_blocking=True)
         en_pin.copy_(ent, non_blocking=True)
@@ -493,6 +508,11 @@ def run_ours(args):
         variant["teacher_head"] = ("MXFP4 (E2M1 + E8M0 per 32), quantised before timing, on the "
                                    "block-scaled tensor cores; teacher rows quantised to MXFP8 "
                                    "inside each call")
+    if args.head == "mx" and w0.kind == "fwd":
+        d["mx_head"] = flp.mx_head_quantize(d["W"])
+        variant["head"] = ("MXFP4 (E2M1 + E8M0 per 32), quantised before timing, on the "
+                           "block-scaled tensor cores; scored rows quantised to MXFP8 inside "
+                           "each call")
     if args.support_j is not None and w0.kind == "fwd":
         d["support"] = torch.from_numpy(workloads.support_words(
             d["workload"].T, d["workload"].V, args.support_j, d["workload"].seed,
@@ -533,8 +553,10 @@ def run_ours(args):
         "kernel_ms": kernel_ms,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": P["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": achieved / P["bf16_tflops"], "traffic": traffic,
-                     "kernel": {"fwd": "vocab_pipeline_kernel<256,4,2,LseEpi<1,%s>,2,1,8,true>"
-                                       % ("true" if "support" in variant else "false"),
+                     "kernel": {"fwd": ("mx_fwd_pipeline_kernel<LseEpi<1,false>>"
+                                        if "head" in variant else
+                                        "vocab_pipeline_kernel<256,4,2,LseEpi<1,%s>,2,1,8,true>"
+                                        % ("true" if "support" in variant else "false")),
                                 "kl": ("mx_kl_pipeline_kernel<KlEpiT<224,16>>"
                                        if args.teacher == "mx" else
                                        "vocab_pipeline_kernel<256,3,2,KlEpi,2,1,%s>"
@@ -625,6 +647,23 @@ def run_ours(args):
                                                      d["tau"], workspace=wsk, support=sup),
                          {"support": "each token kept with probability 1/32, targets kept"})
             del sup, tk
+            # scoring with the head in MXFP4 and the rows in MXFP8 on the
+            # block-scaled tensor cores (the forward of a model that needs no
+            # backward, e.g. the reference policy's log-probs)
+            try:
+                mxh = flp.mx_head_quantize(d["W"])
+                wsm = torch.empty(flp.workspace_size(shape, flp.OP_LOGPROB_ENTROPY_MX),
+                                  dtype=torch.uint8, device=device)
+                variant_line(w.name + "-mx-head",
+                             lambda: flp.logprob_entropy_mx(d["h"], mxh, w.V, d["targets"],
+                                                            d["row_idx"], d["tau"], workspace=wsm),
+                             {"head": "MXFP4 head (%.3f GB against %.3f GB in bf16) x MXFP8 rows "
+                                      "on the block-scaled tensor cores (tcgen05.mma "
+                                      "kind::mxf8f6f4)"
+                                      % (mxh.numel() / 1e9, w.V * w.H * 2 / 1e9)})
+                del mxh, wsm
+            except Exception as e:  # reported, not fatal
+                extra[w.name + "-mx-head"] = {"unavailable": str(e)[:200]}
         # distillation KL with the teacher head in MXFP4 (4.25 bits per weight):
         # decoded to bf16 next to the tensor cores, and on the block-scaled
         # tensor cores with the teacher rows in MXFP8; each interleaved (ABBA)

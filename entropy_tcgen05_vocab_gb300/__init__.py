@@ -12,6 +12,7 @@ or PyTorch fallback, and a missing library raises.
     kl = kl_divergence(h_s, W_s, h_t, W_t, row_idx)
     kl = kl_divergence_mxfp4(h_s, W_s, h_t, *mxfp4_quantize(W_t), row_idx)
     kl = kl_divergence_mx(h_s, W_s, h_t, mx_head_quantize(W_t), row_idx)  # block-scaled MMA
+    logp, ent = logprob_entropy_mx(h, mx_head_quantize(W), V, targets, row_idx, temperature)
     dh, dW = backward(h, W, targets, row_idx, temperature, g1, g2)
     logp, ent = FusedLogProbEntropy.apply(h, W, targets, row_idx, temperature)
 """
@@ -25,11 +26,12 @@ from . import _build
 __all__ = ["lib", "build", "workspace_size", "logprob_entropy", "logprob_entropy_k",
            "kl_divergence", "backward", "pack_support", "mxfp4_quantize",
            "kl_divergence_mxfp4", "mx_head_quantize", "mxfp8_quantize", "kl_divergence_mx",
+           "logprob_entropy_mx",
            "read_device_status", "plan", "set_kernel_events", "set_wait_limit", "row_chunks",
            "FusedLogProbEntropy", "FlpError",
-           "OP_LOGPROB_ENTROPY", "OP_KL", "OP_BACKWARD", "OP_KL_MX"]
+           "OP_LOGPROB_ENTROPY", "OP_KL", "OP_BACKWARD", "OP_KL_MX", "OP_LOGPROB_ENTROPY_MX"]
 
-OP_LOGPROB_ENTROPY, OP_KL, OP_BACKWARD, OP_KL_MX = 0, 1, 2, 3
+OP_LOGPROB_ENTROPY, OP_KL, OP_BACKWARD, OP_KL_MX, OP_LOGPROB_ENTROPY_MX = 0, 1, 2, 3, 4
 _DTYPES = {torch.bfloat16: 0, torch.float16: 1}
 
 
@@ -125,6 +127,9 @@ def lib():
     L.flp_mxfp8_quantize.restype = ctypes.c_int
     L.flp_kl_mx.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.flp_kl_mx.restype = ctypes.c_int
+    L.flp_logprob_entropy_mx.argtypes = [shp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp, vp,
+                                         sz, vp]
+    L.flp_logprob_entropy_mx.restype = ctypes.c_int
     for f in (L.flp_logprob_entropy, L.flp_kl, L.flp_backward, L.flp_read_device_status,
               L.flp_plan_scoring):
         f.restype = ctypes.c_int
@@ -484,6 +489,44 @@ def kl_divergence_mx(h_s, W_s, h_t, Wt_head, row_idx=None, *, workspace=None):
         _check(lib().flp_kl_mx(ctypes.byref(shape), _ptr(h_s), _ptr(W_s), _ptr(h_t), _ptr(Wt_head),
                                _ptr(ri), _ptr(out), _ptr(ws), ws.numel(), _stream(dev)))
     return out
+
+
+def logprob_entropy_mx(h, head, V, targets, row_idx=None, temperature=1.0, *,
+                       return_stats=False, workspace=None):
+    """Target log-prob and entropy with the logits on the block-scaled tensor
+    cores, for scoring that needs no backward (e.g. the reference model's
+    log-probs): the scored rows of h [T, H] (bf16/fp16, H a multiple of 128)
+    quantised to MXFP8 per call, times the MXFP4 head of V rows (from
+    :func:`mx_head_quantize`).  targets int64 [T] by h row, row_idx int64 [n]
+    or None.  Returns float32 [n] (logp, ent), plus (lse, ez) if
+    ``return_stats``."""
+    _matrix(h, "h")
+    dev = h.device
+    H = h.shape[1]
+    nbytes = int(lib().flp_mx_head_bytes(int(V), H))
+    if nbytes == 0:
+        raise TypeError("V must be > 0 and H a positive multiple of 128")
+    if not isinstance(head, torch.Tensor) or head.device != dev or head.dtype != torch.uint8 \
+            or head.numel() < nbytes or not head.is_contiguous():
+        raise TypeError("head must be a contiguous uint8 tensor of >= %d bytes on %s "
+                        "(see mx_head_quantize)" % (nbytes, dev))
+    tg = _index(targets, "targets", dev)
+    ri = _index(row_idx, "row_idx", dev)
+    n = h.shape[0] if ri is None else ri.numel()
+    shape = make_shape(h.shape[0], H, int(V), n, h.dtype, h.stride(0), H)
+    logp = torch.empty(n, dtype=torch.float32, device=dev)
+    ent = torch.empty(n, dtype=torch.float32, device=dev)
+    lse = torch.empty(n, dtype=torch.float32, device=dev) if return_stats else None
+    ez = torch.empty(n, dtype=torch.float32, device=dev) if return_stats else None
+    ws = _workspace(shape, OP_LOGPROB_ENTROPY_MX, dev, workspace)
+    with torch.cuda.device(dev):
+        _check(lib().flp_logprob_entropy_mx(ctypes.byref(shape), _ptr(h), _ptr(head), _ptr(tg),
+                                            _ptr(ri), float(temperature), _ptr(logp), _ptr(ent),
+                                            _ptr(lse), _ptr(ez), _ptr(ws), ws.numel(),
+                                            _stream(dev)))
+    if return_stats:
+        return logp, ent, lse, ez
+    return logp, ent
 
 
 def read_device_status(workspace, device=None):

@@ -145,8 +145,15 @@ Layout layout_for(const flp_shape *s, flp_op op, bool gather = true) {
   L.cnt = take(L.cnt_bytes);
   // the backward's statistics pass is the forward kernel
   const bool kl = op == FLP_OP_KL || op == FLP_OP_KL_MX;
-  const int bn = op == FLP_OP_KL ? kKlBN : (op == FLP_OP_KL_MX ? kMxBN : kFwdTileCols);
-  const int epiw = op == FLP_OP_KL ? kKlEpiWarps : (op == FLP_OP_KL_MX ? kMxEpiWarps : kFwdEpiWarps);
+  const bool mx = op == FLP_OP_KL_MX || op == FLP_OP_LOGPROB_ENTROPY_MX;
+  const int bn = op == FLP_OP_KL ? kKlBN
+                 : op == FLP_OP_KL_MX ? kMxBN
+                 : op == FLP_OP_LOGPROB_ENTROPY_MX ? kMxFwdTileCols
+                 : kFwdTileCols;
+  const int epiw = op == FLP_OP_KL ? kKlEpiWarps
+                   : op == FLP_OP_KL_MX ? kMxEpiWarps
+                   : op == FLP_OP_LOGPROB_ENTROPY_MX ? kMxFEpiWarps
+                   : kFwdEpiWarps;
   const size_t sm = static_cast<size_t>(max_splits(s->V, bn, s->n_rows, 128 * kFwdCG)) * (epiw / 4);  // partial slots
   L.pm = take(sm * n * 4);
   L.ps = take(sm * n * 4);
@@ -157,13 +164,14 @@ Layout layout_for(const flp_shape *s, flp_op op, bool gather = true) {
   } else {
     L.zt = take(n * kMaxTargets * 4);  // raw target logits, up to kMaxTargets per row
   }
-  if (op == FLP_OP_KL_MX) {
-    // the teacher's rows quantised per call: E4M3 codes and 512-byte scale
-    // atoms per 128 rows and 128-wide k-chunk
+  if (mx) {
+    // the teacher's (KL) or the scored (forward) rows quantised per call:
+    // E4M3 codes and 512-byte scale atoms per 128 rows and 128-wide k-chunk
     L.q8 = take(n * static_cast<size_t>(s->H));
     L.sfa = take(static_cast<size_t>(cdiv(s->n_rows, 128) * cdiv(s->H, kMxChunk)) * 512);
   }
-  if (gather) {
+  // the block-scaled forward has no bf16/fp16 operand: its quantiser gathers
+  if (gather && op != FLP_OP_LOGPROB_ENTROPY_MX) {
     L.hs = take(n * static_cast<size_t>(s->H) * 2);
     if (op == FLP_OP_KL) L.hs2 = take(n * static_cast<size_t>(s->H) * 2);
   }
@@ -693,6 +701,91 @@ flp_status kl_bs_impl(const flp_shape *s, const void *h_s, const void *W_s, cons
   return FLP_OK;
 }
 
+// Log-prob and entropy with the logits on the block-scaled tensor cores: the
+// scored rows are quantised to MXFP8 in the workspace (gathered on the way),
+// then one persistent launch forms the logit tiles against the MXFP4 head
+// and folds them.
+flp_status fwd_bs_impl(const flp_shape *s, const void *h, const void *head,
+                       const int64_t *targets, const int64_t *row_idx, float temperature,
+                       float *out_logp, float *out_ent, float *out_lse, float *out_ez, void *ws,
+                       size_t ws_bytes, flp_stream_t stream) {
+  const KernelEvents ev;
+  flp_status st = check_common(s, FLP_OP_LOGPROB_ENTROPY_MX, ws, ws_bytes, false);
+  if (st != FLP_OK) return st;
+  if (s->H % kMxChunk != 0)
+    return fail(FLP_ERR_INVALID_ARG, "H must be a multiple of 128 for the block-scaled forward");
+  if (!(std::isfinite(temperature) && temperature > 0.f))
+    return fail(FLP_ERR_INVALID_ARG, "temperature must be finite and > 0");
+  // the scale atoms are addressed by 32-bit tensor-map row coordinates (the
+  // last tile may name one head tile past the end)
+  if ((cdiv(s->V, kMxBN) + 1) * (s->H / kMxChunk) * 64 > (int64_t(1) << 31) - 64 ||
+      cdiv(s->n_rows, 128) * (s->H / kMxChunk) * 32 > (int64_t(1) << 31) - 32)
+    return fail(FLP_ERR_INVALID_ARG, "size beyond the block-scaled tiling range");
+  if (s->n_rows == 0) return FLP_OK;
+  if (!row_idx && s->n_rows != s->T)
+    return fail(FLP_ERR_INVALID_ARG, "row_idx is NULL but n_rows != T");
+  if (!h || !head || !targets || !out_logp || !out_ent)
+    return fail(FLP_ERR_INVALID_ARG, "h, head, targets, out_logp and out_ent are required");
+  if (!aligned16(h)) return fail(FLP_ERR_INVALID_ARG, "h must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(head) % 256 != 0)
+    return fail(FLP_ERR_INVALID_ARG, "the head must be 256-byte aligned");
+  DeviceInfo dev;
+  if ((st = device_info(&dev)) != FLP_OK) return st;
+
+  const Layout L = layout_for(s, FLP_OP_LOGPROB_ENTROPY_MX, false);
+  const Plan p = plan_cached(s->n_rows, s->V, s->H, kMxFwdTileCols, fwd_bs_units(dev.sms), 256);
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t kc = s->H / kMxChunk;
+  FwdBsArgs a{};
+  uint8_t *q8 = at<uint8_t>(ws, L.q8), *sfa = at<uint8_t>(ws, L.sfa);
+  const uint8_t *codes = static_cast<const uint8_t *>(head);
+  const uint8_t *atoms = codes + mx_head_code_bytes(s->V, s->H);
+  if ((st = make_map_typed(&a.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, q8, s->H, s->n_rows, s->H,
+                           kMxChunk, 128, CU_TENSOR_MAP_SWIZZLE_128B)) != FLP_OK)
+    return st;
+  if ((st = make_map_typed(&a.tmB, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, codes, s->H, s->V,
+                           s->H / 2, kMxChunk, kMxBN / 2, CU_TENSOR_MAP_SWIZZLE_128B)) != FLP_OK)
+    return st;
+  if ((st = make_map_typed(&a.tmSfa, CU_TENSOR_MAP_DATA_TYPE_UINT8, sfa, 16,
+                           cdiv(s->n_rows, 128) * kc * 32, 16, 16, 32,
+                           CU_TENSOR_MAP_SWIZZLE_NONE)) != FLP_OK)
+    return st;
+  if ((st = make_map_typed(&a.tmSfb, CU_TENSOR_MAP_DATA_TYPE_UINT8, atoms, 16,
+                           cdiv(s->V, kMxBN) * kc * 64, 16, 16, 64, CU_TENSOR_MAP_SWIZZLE_NONE)) !=
+      FLP_OK)
+    return st;
+  a.sch = p.sch;
+  a.sch.k_blocks = static_cast<int>(kc);
+  a.sch.wait_ns = g_wait_ns;
+  a.grid = p.grid * 2;
+  a.targets = targets;
+  a.row_idx = row_idx;
+  a.T = s->T;
+  a.inv_tau = 1.0f / temperature;
+  a.scale_log2 = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+  a.pm = at<float>(ws, L.pm);
+  a.ps = at<float>(ws, L.ps);
+  a.pb = at<float>(ws, L.pb);
+  a.zt = at<float>(ws, L.zt);
+  a.counters = at<uint32_t>(ws, L.cnt);
+  a.out_logp = out_logp;
+  a.out_ent = out_ent;
+  a.out_lse = out_lse;
+  a.out_ez = out_ez;
+  a.status = at<uint32_t>(ws, L.status);
+
+  cudaError_t e = cudaMemsetAsync(a.status, 0, L.cnt + L.cnt_bytes - L.status, cs);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(status)");
+  if ((e = launch_mxfp8_quantize(h, s->dtype == FLP_BF16, s->n_rows, s->H, s->ld_h, row_idx, s->T,
+                                 q8, sfa, true, dev.sms, cs)) != cudaSuccess)
+    return cuda_fail(e, "MXFP8 quantize launch");
+  if ((e = ev.start(cs)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+  if ((e = launch_fwd_blockscaled(a, cs)) != cudaSuccess)
+    return cuda_fail(e, "block-scaled scoring launch");
+  if ((e = ev.stop(cs)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+  return FLP_OK;
+}
+
 flp_status backward_impl(const flp_shape *s, const void *h, const void *W, const int64_t *targets,
                          const int64_t *row_idx, const uint32_t *support, int64_t ld_support,
                          float temperature, const float *g1, const float *g2, const float *lse,
@@ -875,9 +968,9 @@ size_t flp_workspace_size(const flp_shape *shape, flp_op op) {
   const char *why = nullptr;
   if (!shape_ok(shape, &why)) return 0;
   if (op != FLP_OP_LOGPROB_ENTROPY && op != FLP_OP_KL && op != FLP_OP_BACKWARD &&
-      op != FLP_OP_KL_MX)
+      op != FLP_OP_KL_MX && op != FLP_OP_LOGPROB_ENTROPY_MX)
     return 0;
-  if (op == FLP_OP_KL_MX && shape->H % kMxChunk != 0) return 0;
+  if ((op == FLP_OP_KL_MX || op == FLP_OP_LOGPROB_ENTROPY_MX) && shape->H % kMxChunk != 0) return 0;
   return layout_for(shape, op).total;
 }
 
@@ -916,15 +1009,19 @@ flp_status flp_plan_scoring(const flp_shape *shape, flp_op op, int32_t num_sms, 
   if (!shape_ok(shape, &why)) return fail(FLP_ERR_INVALID_ARG, "%s", why);
   if (!out || num_sms <= 0) return fail(FLP_ERR_INVALID_ARG, "out is NULL or num_sms <= 0");
   if (op != FLP_OP_LOGPROB_ENTROPY && op != FLP_OP_KL && op != FLP_OP_BACKWARD &&
-      op != FLP_OP_KL_MX)
+      op != FLP_OP_KL_MX && op != FLP_OP_LOGPROB_ENTROPY_MX)
     return fail(FLP_ERR_INVALID_ARG, "unknown op");
   std::memset(out, 0, sizeof *out);
   if (shape->n_rows == 0) return FLP_OK;
   // the forward's few-rows path runs single CTAs
   const bool few = op == FLP_OP_LOGPROB_ENTROPY && shape->n_rows <= kSmallRows;
   const bool kl = op == FLP_OP_KL || op == FLP_OP_KL_MX;
-  const int bn = op == FLP_OP_KL ? kKlBN : (op == FLP_OP_KL_MX ? kMxBN : (few ? kFwdBN : kFwdTileCols));
-  const int cg = kl ? 2 : (few ? 1 : kFwdCG);
+  const int bn = op == FLP_OP_KL                    ? kKlBN
+                 : op == FLP_OP_KL_MX               ? kMxBN
+                 : op == FLP_OP_LOGPROB_ENTROPY_MX  ? kMxFwdTileCols
+                 : few                              ? kFwdBN
+                                                    : kFwdTileCols;
+  const int cg = kl || op == FLP_OP_LOGPROB_ENTROPY_MX ? 2 : (few ? 1 : kFwdCG);
   const int units = std::max(1, num_sms / cg);
   const Plan p = plan_cached(shape->n_rows, shape->V, shape->H, bn, units, 128 * cg, kl ? 2 : 1);
   out->row_tiles = p.sch.row_tiles;
@@ -1109,6 +1206,16 @@ flp_status flp_kl_mx(const flp_shape *s, const void *h_s, const void *W_s, const
                      size_t ws_bytes, flp_stream_t stream) {
   g_err[0] = 0;
   return kl_bs_impl(s, h_s, W_s, h_t, Wt_head, row_idx, out_kl, ws, ws_bytes, stream);
+}
+
+flp_status flp_logprob_entropy_mx(const flp_shape *s, const void *h, const void *head,
+                                  const int64_t *targets, const int64_t *row_idx,
+                                  float temperature, float *out_logp, float *out_ent,
+                                  float *out_lse, float *out_ez, void *ws, size_t ws_bytes,
+                                  flp_stream_t stream) {
+  g_err[0] = 0;
+  return fwd_bs_impl(s, h, head, targets, row_idx, temperature, out_logp, out_ent, out_lse, out_ez,
+                     ws, ws_bytes, stream);
 }
 
 flp_status flp_backward(const flp_shape *s, const void *h, const void *W, const int64_t *targets,

@@ -65,6 +65,11 @@ constexpr int kKlEpiWarps = 8;
 constexpr int kMxBN = 224;
 constexpr int kMxChunk = 128;
 constexpr int kMxEpiWarps = 8;
+// Block-scaled forward (E4M3 scored rows x the same E2M1 head): CTA pairs on
+// 256-row x 448-column tiles, two N = 224 MMAs (two head tiles) sharing A,
+// one accumulator buffer, eight epilogue warps.
+constexpr int kMxFwdTileCols = 2 * kMxBN;
+constexpr int kMxFEpiWarps = 8;
 
 struct FwdArgs {
   CUtensorMap tmA;  // scored hidden rows [n, H], box 64 x 128
@@ -114,6 +119,23 @@ struct KlBsArgs {
   float *pmt, *pst, *pct, *pms, *pss;
   uint32_t *counters;
   float *out_kl;
+  uint32_t *status;
+};
+
+struct FwdBsArgs {
+  CUtensorMap tmA;           // MXFP8 codes of the scored rows [n, H] uint8, box 128 x 128
+  CUtensorMap tmB;           // head codes [V, H] 16U4_ALIGN16B, box 128 x 112
+  CUtensorMap tmSfa, tmSfb;  // scale atoms as rows of 16 bytes (boxes 16 x 32, 16 x 64)
+  Schedule sch;              // k_blocks = H / 128, vocabulary tiles of kMxFwdTileCols
+  int grid;
+  const int64_t *targets;    // [T]
+  const int64_t *row_idx;
+  int64_t T;
+  float inv_tau;
+  float scale_log2;
+  float *pm, *ps, *pb, *zt;
+  uint32_t *counters;        // [ceil(n / 32)] zeroed before the launch
+  float *out_logp, *out_ent, *out_lse, *out_ez;
   uint32_t *status;
 };
 
@@ -207,6 +229,8 @@ cudaError_t launch_pack_support(const uint8_t *mask, int64_t T, int64_t V, int64
 cudaError_t launch_wait_timeout(uint64_t limit_ns, uint32_t *status, cudaStream_t stream);
 cudaError_t launch_kl_blockscaled(const KlBsArgs &a, cudaStream_t stream);
 int kl_bs_units(int num_sms);
+cudaError_t launch_fwd_blockscaled(const FwdBsArgs &a, cudaStream_t stream);
+int fwd_bs_units(int num_sms);
 // MXFP8 quantisation of R rows (row_idx[i], or i, of X [*, ld] bf16/fp16;
 // rows outside [0, T) read as zeros) into codes [R, H] and scales: the
 // pipeline's 512-byte atoms (atoms = true, rows up to the next multiple of

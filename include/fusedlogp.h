@@ -72,7 +72,9 @@ typedef enum {
     FLP_OP_LOGPROB_ENTROPY = 0,
     FLP_OP_KL = 1,
     FLP_OP_BACKWARD = 2,
-    FLP_OP_KL_MX = 3   /* flp_kl_mx: the teacher on the block-scaled tensor cores */
+    FLP_OP_KL_MX = 3,  /* flp_kl_mx: the teacher on the block-scaled tensor cores */
+    FLP_OP_LOGPROB_ENTROPY_MX = 4  /* flp_logprob_entropy_mx: scoring on the block-scaled
+                                      tensor cores */
 } flp_op;
 
 /*
@@ -332,6 +334,31 @@ flp_status flp_kl_mx(const flp_shape *shape, const void *h_s, const void *W_s,
                      const void *h_t, const void *Wt_head, const int64_t *row_idx,
                      float *out_kl, void *workspace, size_t workspace_bytes,
                      flp_stream_t stream);
+
+/*
+ * flp_logprob_entropy with the logits on the block-scaled tensor cores, for
+ * scoring that needs no backward (DeepSeek-V4 book ch. 19, "1. FP4 in OPD":
+ * rollout, the teachers and the reference model that gives the KL baseline
+ * run their forwards in native 4-bit precision): each scored row h[row] is
+ * quantised to MXFP8 (flp_mxfp8_quantize's rule) inside the call and the
+ * logits are h[row]^MXFP8 times the MXFP4 head `head` (from
+ * flp_mx_head_quantize, V rows of H columns), FP32-accumulated with the
+ * scales applied inside the MMA; then, as in flp_logprob_entropy (temperature
+ * in FP32 after the upcast), per scored position i:
+ *   out_logp[i] = z'[tgt] - LSE,  out_ent[i] = entropy,  out_lse / out_ez
+ *   optional (NULL to skip).
+ * h bf16 or fp16 [T, ld_h], 16-byte aligned; H a multiple of 128; head
+ * 256-byte aligned.  targets [T] by h row; row_idx [n_rows] or NULL (then
+ * n_rows == T).  Bad rows and targets are handled as in flp_logprob_entropy.
+ * Workspace: flp_workspace_size(shape, FLP_OP_LOGPROB_ENTROPY_MX) (it holds
+ * the quantised rows: n_rows * H bytes plus their scales).  shape->ld_w is
+ * not used but must pass the shape checks (set it to H).
+ */
+flp_status flp_logprob_entropy_mx(const flp_shape *shape, const void *h, const void *head,
+                                  const int64_t *targets, const int64_t *row_idx,
+                                  float temperature, float *out_logp, float *out_ent,
+                                  float *out_lse, float *out_ez, void *workspace,
+                                  size_t workspace_bytes, flp_stream_t stream);
 
 /*
  * Gradients of L = sum_i g1[i] logp_i + g2[i] ent_i (logp, ent as in

@@ -131,6 +131,17 @@ def test_workspace_formula(L):
     q8 = w.T * w.H + (w.T + 127) // 128 * (w.H // 128) * 512
     assert q8 + w.T * w.H * 2 <= b <= q8 + w.T * w.H * 2 + w.T * 128 * 4 * 5 + (1 << 20)
     assert L.flp_workspace_size(ctypes.byref(_shape(T=64, H=192, V=1000, n=64)), 3) == 0
+    # the block-scaled forward: the scored rows in MXFP8 and their atoms (no
+    # gathered bf16 rows: the quantiser gathers), plus the forward's per-row
+    # state and target logits
+    w = workloads.WORKLOADS[1]
+    s = _shape(T=w.T, H=w.H, V=w.V, n=w.T)
+    b = L.flp_workspace_size(ctypes.byref(s), 4)
+    q8 = w.T * w.H + (w.T + 127) // 128 * (w.H // 128) * 512
+    assert q8 <= b <= q8 + w.T * 128 * 4 * 5 + (1 << 20)
+    assert b < L.flp_workspace_size(ctypes.byref(s), 0)
+    assert L.flp_workspace_size(ctypes.byref(_shape(T=64, H=192, V=1000, n=64)), 4) == 0
+    assert L.flp_workspace_size(ctypes.byref(s), 5) == 0
     # monotone in the number of scored rows
     a = L.flp_workspace_size(ctypes.byref(_shape(T=4096, H=4096, V=151936, n=1000)), 0)
     b = L.flp_workspace_size(ctypes.byref(_shape(T=4096, H=4096, V=151936, n=2000)), 0)
@@ -307,6 +318,27 @@ def test_mxfp4_entry_points_validate_on_host(L):
     assert L.flp_mxfp4_quantize(FAKE, 0, i64(100), i64(96), i64(96), FAKE, FAKE, None) == 1
     assert L.flp_mxfp4_quantize(FAKE, 0, i64(100), i64(128), i64(64), FAKE, FAKE, None) == 1
     assert L.flp_mxfp4_quantize(None, 0, i64(100), i64(128), i64(128), FAKE, FAKE, None) == 1
+
+
+def test_block_scaled_forward_validates_on_host(L):
+    f = L.flp_logprob_entropy_mx
+    f.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_float] + [ctypes.c_void_p] * 5 + \
+        [ctypes.c_size_t, ctypes.c_void_p]
+    s = _shape(H=512, ld_h=512, ld_w=512)
+    big = ctypes.c_size_t(1 << 40)
+    ok = [FAKE, FAKE, FAKE, None, 0.7, FAKE, FAKE, None, None, FAKE, big, None]
+    def call(shape, **kw):
+        a = list(ok)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return f(ctypes.byref(shape), *a)
+    assert call(_shape(H=520, ld_h=520, ld_w=520)) == 1                  # H % 128
+    assert call(s, a4=0.0) == 1 and call(s, a4=float("nan")) == 1        # temperature
+    assert call(s, a1=None) == 1                                         # head missing
+    assert call(s, a1=ctypes.c_void_p((1 << 20) + 16)) == 1              # head alignment
+    assert call(s, a0=ctypes.c_void_p((1 << 20) + 8)) == 1               # h alignment
+    assert call(s, a9=None) == 3                                         # workspace
+    assert call(s, a10=ctypes.c_size_t(16)) == 3
 
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):

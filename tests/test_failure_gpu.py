@@ -170,3 +170,24 @@ def test_block_scaled_kl_pipeline_wait_that_runs_out_unwinds():
     kl = run()
     assert flp.read_device_status(ws)["timeouts"] == 0
     assert np.abs(kl.cpu().double().numpy() - want).max() <= 1e-3
+
+
+def test_block_scaled_forward_pipeline_wait_that_runs_out_unwinds():
+    """The block-scaled forward (one ring, scale slots fewer than its stages)
+    gives up, drains and frees its TMEM the same way."""
+    d = _fwd_case()
+    V = 8192
+    ws = _ws(256, ABORT_H, V, 256, flp.OP_LOGPROB_ENTROPY_MX)
+    head = flp.mx_head_quantize(d["W"])
+    run = lambda: flp.logprob_entropy_mx(d["h"], head, V, d["targets"], None, 1.0, workspace=ws)
+    packed, scales = coracle.mxfp4_quantize(d["W"].cpu(), "bf16")
+    want = coracle.logprob_entropy_mx(d["h"].cpu(), packed, scales, V, d["targets"].cpu().numpy(),
+                                      None, 1.0, "bf16")
+    with _ShortWaits():
+        run()
+        st = flp.read_device_status(ws)
+    assert st["timeouts"] > 0, st
+    logp, ent = run()
+    assert flp.read_device_status(ws)["timeouts"] == 0
+    assert np.abs(logp.cpu().double().numpy() - want["logp"]).max() <= 1e-3
+    assert np.abs(ent.cpu().double().numpy() - want["ent"]).max() <= 1e-3

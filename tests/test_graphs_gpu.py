@@ -92,3 +92,24 @@ def test_block_scaled_kl_replay():
         g.replay()
         torch.cuda.synchronize()
         assert torch.equal(out, flp.kl_divergence_mx(d["h_s"], d["W_s"], h_t, head, workspace=ws))
+
+
+def test_block_scaled_forward_replay():
+    """The block-scaled forward (MXFP8 quantisation of the scored rows, then
+    the pipeline) captured and replayed on new hidden rows."""
+    w = workloads.WORKLOADS[1].scaled(T=600, H=256, V=7000, seed=94, targets="uniform")
+    d = workloads.make(w, device="cuda")
+    rows = torch.arange(0, 600, 3, device="cuda")
+    shape = flp.make_shape(w.T, w.H, w.V, rows.numel(), torch.bfloat16)
+    ws = torch.empty(flp.workspace_size(shape, flp.OP_LOGPROB_ENTROPY_MX), dtype=torch.uint8,
+                     device="cuda")
+    head = flp.mx_head_quantize(d["W"])
+    h = d["h"].clone()
+    g, out = _capture(lambda: flp.logprob_entropy_mx(h, head, w.V, d["targets"], rows, 0.7,
+                                                     workspace=ws))
+    for scale in (1.0, 0.5):
+        h.copy_((d["h"].float() * scale).to(torch.bfloat16))
+        g.replay()
+        torch.cuda.synchronize()
+        ref_out = flp.logprob_entropy_mx(h, head, w.V, d["targets"], rows, 0.7, workspace=ws)
+        assert torch.equal(out[0], ref_out[0]) and torch.equal(out[1], ref_out[1])
