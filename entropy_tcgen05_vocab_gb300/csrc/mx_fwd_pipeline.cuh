@@ -27,15 +27,18 @@
 // TMEM: the accumulator at [0, 448) (MMA 0 at columns [0, 224), MMA 1 at
 // [224, 448), so tile column c is vocabulary column 448 vt + c), then
 // kMxFSlots slots of 20 scale columns (4 for A, 8 per head tile).  Per
-// k-chunk the MMA issuer copies the chunk's five atoms into the chunk's slot
-// with tcgen05.cp (the layout the block-scaled MMA reads; see mx_pipeline.cuh),
-// issues the four K = 32 steps of both MMAs with scale id = step, and
-// commits once to release the stage.  The slots are fewer than the stages:
-// before it rewrites slot g % kMxFSlots for k-chunk g, the issuer waits for
-// the release of k-chunk g - kMxFSlots, whose MMAs were that slot's last
-// readers (long finished by then: the issue of each MMA takes about its
-// execution time).  Eight epilogue warps (two per TMEM lane quarter, 224
-// columns each) fold the accumulator 32 columns at a time.
+// k-chunk a scale-copier warp copies the chunk's five atoms into the chunk's
+// slot with tcgen05.cp (the layout the block-scaled MMA reads; see
+// mx_pipeline.cuh) and commits that to the slot's "ready" barrier; the MMA
+// issuer waits for it, issues the four K = 32 steps of both MMAs with scale
+// id = step, and commits once to release the stage.  The slots are fewer
+// than the stages, so before it rewrites slot g % kMxFSlots for k-chunk g
+// the copier waits for the release of k-chunk g - kMxFSlots, whose MMAs were
+// that slot's last readers.  (With the copies and that wait on the issuer's
+// own thread, the issuer spent about 12 % of its time in that wait, with
+// the tensor pipe idle.)  Eight epilogue warps
+// (two per TMEM lane quarter, 224 columns each) fold the accumulator 32
+// columns at a time.
 #pragma once
 
 #include "launch.h"
@@ -46,7 +49,10 @@ namespace flp {
 
 constexpr int kMxFStages = 4;
 constexpr int kMxFSlots = 3;
-constexpr int kMxFThreads = 64 + 32 * kMxFEpiWarps;
+// warps: 0 producer, 1 TMEM allocation + MMA issuer, 2..9 epilogue, 10 scale
+// copier (leader CTA)
+constexpr int kMxFScaleWarp = 2 + kMxFEpiWarps;
+constexpr int kMxFThreads = 32 * (kMxFScaleWarp + 1);
 static_assert(kMxFStages > kMxFSlots, "a slot's last readers are released before the issuer "
                                       "can reach the chunk after next in their stage");
 
@@ -64,7 +70,7 @@ struct MxFwdLayout {
   static constexpr int kStage = 48 * 1024;
   static constexpr int kTx = kA + 2 * kBTx + kSfa + 2 * kSfb;  // bytes one CTA's copies count
   static constexpr int kRingBytes = kMxFStages * kStage;
-  static constexpr int kBarrierBytes = 8 * (2 * kMxFStages + 3) + 32;
+  static constexpr int kBarrierBytes = 8 * (2 * kMxFStages + kMxFSlots + 4) + 32;
   static constexpr int kSmemBytes = kRingBytes + kBarrierBytes + 1024;
   static constexpr int kTmemCols = 512;
   static constexpr int kAccCols = kMxFwdTileCols;        // 448
@@ -105,8 +111,10 @@ __global__ void __launch_bounds__(kMxFThreads, 1)
   uint64_t *empty = full + kMxFStages;
   uint64_t *afull = empty + kMxFStages;  // accumulator ready for the epilogue
   uint64_t *aempty = afull + 1;          // accumulator drained
-  uint64_t *drain = aempty + 1;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  uint64_t *drain = aempty + 1;          // MMA issuer's teardown
+  uint64_t *sready = drain + 1;          // [kMxFSlots] a k-chunk's scales are in TMEM
+  uint64_t *sdrain = sready + kMxFSlots;  // scale copier's teardown
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sdrain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   // k-chunks the peer's producer issued (written at teardown)
   volatile uint32_t *peer_issued = reinterpret_cast<volatile uint32_t *>(tmem_slot + 2);
@@ -129,6 +137,8 @@ __global__ void __launch_bounds__(kMxFThreads, 1)
     mbar_init(afull, 1);
     mbar_init(aempty, kMxFEpiWarps * CG);
     mbar_init(drain, 1);
+    for (int s = 0; s < kMxFSlots; ++s) mbar_init(&sready[s], 1);
+    mbar_init(sdrain, 1);
     *abort_flag = 0;
     peer_issued[0] = 0;
     fence_mbar_init();
@@ -202,11 +212,8 @@ __global__ void __launch_bounds__(kMxFThreads, 1)
           for (int c = 0; c < kc_n; ++c) {
             if (lane == 0) {
               ok = mbar_wait(&full[st], ph, abort_flag, lim);
-              if (ok && g >= static_cast<uint32_t>(kMxFSlots)) {
-                // the MMAs of k-chunk g - kMxFSlots last read this chunk's scale slot
-                const uint32_t gp = g - kMxFSlots;
-                ok = mbar_wait(&empty[gp % kMxFStages], (gp / kMxFStages) & 1u, abort_flag, lim);
-              }
+              if (ok)  // the scale copier put this k-chunk's scales into its slot
+                ok = mbar_wait(&sready[g % kMxFSlots], (g / kMxFSlots) & 1u, abort_flag, lim);
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
@@ -215,11 +222,6 @@ __global__ void __launch_bounds__(kMxFThreads, 1)
               const uint32_t tb = smem_u32(smem + st * L::kStage);
               const uint32_t sf =
                   tmem_base + static_cast<uint32_t>(L::kAccCols + (g % kMxFSlots) * L::kSfCols);
-              tmem_cp_32x128b_x4_pair(sf, sdesc_rows16(tb + L::kOffSfa));
-              tmem_cp_32x128b_x4_pair(sf + 4, sdesc_rows16(tb + L::kOffSfb0));
-              tmem_cp_32x128b_x4_pair(sf + 8, sdesc_rows16(tb + L::kOffSfb0 + 512));
-              tmem_cp_32x128b_x4_pair(sf + 12, sdesc_rows16(tb + L::kOffSfb1));
-              tmem_cp_32x128b_x4_pair(sf + 16, sdesc_rows16(tb + L::kOffSfb1 + 512));
 #pragma unroll
               for (int j = 0; j < kMxChunk / kMxUmmaK; ++j) {
                 const uint64_t ad = sdesc_sw128(tb + j * kMxUmmaK, 16, 1024);
@@ -243,6 +245,55 @@ __global__ void __launch_bounds__(kMxFThreads, 1)
           if (lane == 0) mma_commit_pair(afull, 0x3);  // the accumulator is ready
           __syncwarp();
           aph ^= 1u;
+        }
+      }
+      if (!ok && lane == 0) record_timeout<CG>(status, abort_flag);
+    }
+  } else if (warp == kMxFScaleWarp) {
+    // ------------------------------------------------------- scale copier
+    // Copies each k-chunk's five scale atoms from its stage into the chunk's
+    // TMEM slot and commits that to the slot's "ready" barrier.  A slot is
+    // rewritten only after the MMAs of the chunk kMxFSlots earlier, its last
+    // readers, were released; waiting for that here, off the MMA issuer,
+    // keeps the issuer's thread on MMAs (its copies and MMAs would otherwise
+    // wait on the same release).
+    if (leader) {
+      int st = 0;
+      uint32_t ph = 0, g = 0;
+      bool ok = true;
+      for (int it = unit; ok && it < sch.items; it += num_units) {
+        int mt, sp, vt0, vt1;
+        sch.item(it, mt, sp, vt0, vt1);
+        for (int vt = vt0; ok && vt < vt1; ++vt) {
+          for (int c = 0; c < kc_n; ++c) {
+            if (lane == 0) {
+              ok = mbar_wait(&full[st], ph, abort_flag, lim);
+              if (ok && g >= static_cast<uint32_t>(kMxFSlots)) {
+                const uint32_t gp = g - kMxFSlots;
+                ok = mbar_wait(&empty[gp % kMxFStages], (gp / kMxFStages) & 1u, abort_flag, lim);
+              }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            if (lane == 0) {
+              const uint32_t tb = smem_u32(smem + st * L::kStage);
+              const uint32_t sf =
+                  tmem_base + static_cast<uint32_t>(L::kAccCols + (g % kMxFSlots) * L::kSfCols);
+              tmem_cp_32x128b_x4_pair(sf, sdesc_rows16(tb + L::kOffSfa));
+              tmem_cp_32x128b_x4_pair(sf + 4, sdesc_rows16(tb + L::kOffSfb0));
+              tmem_cp_32x128b_x4_pair(sf + 8, sdesc_rows16(tb + L::kOffSfb0 + 512));
+              tmem_cp_32x128b_x4_pair(sf + 12, sdesc_rows16(tb + L::kOffSfb1));
+              tmem_cp_32x128b_x4_pair(sf + 16, sdesc_rows16(tb + L::kOffSfb1 + 512));
+              mma_commit_pair_local(&sready[g % kMxFSlots]);
+            }
+            __syncwarp();
+            ++g;
+            if (++st == kMxFStages) {
+              st = 0;
+              ph ^= 1u;
+            }
+          }
         }
       }
       if (!ok && lane == 0) record_timeout<CG>(status, abort_flag);
@@ -291,6 +342,8 @@ __global__ void __launch_bounds__(kMxFThreads, 1)
         drain_copies<kMxFStages, CG>(full, issued, peer_issued[0], L::kTx);
       else if (warp == 1)
         drain_mmas<CG>(drain);
+      else if (warp == kMxFScaleWarp)
+        drain_mmas<CG>(sdrain);  // the scale copies
     }
     pipe_sync<CG>();
   }
