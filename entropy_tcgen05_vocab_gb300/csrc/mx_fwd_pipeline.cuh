@@ -156,26 +156,28 @@ __global__ void __launch_bounds__(kMxFThreads, 1)
   pipe_sync<CG>();
   const uint32_t tmem_base = *tmem_slot;
 
+  // The producer, the MMA issuer and the scale copier run on one lane each
+  // (the other lanes of their warps wait at the end): no warp-wide exchange
+  // sits between one k-chunk's MMAs and the next's.
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    int st = 0;
-    uint32_t ph = 0;
-    bool ok = true;
-    const uint32_t full_dst = mapa_shared(smem_u32(full), 0);
-    for (int it = unit; ok && it < sch.items; it += num_units) {
-      int mt, sp, vt0, vt1;
-      sch.item(it, mt, sp, vt0, vt1);
-      const int arow = mt * (kBM * CG) + static_cast<int>(rank) * kBM;
-      const int ablk = mt * CG + static_cast<int>(rank);  // 128-row block of the scale atoms
-      for (int vt = vt0; ok && vt < vt1; ++vt) {
-        const int t0 = 2 * vt, t1 = 2 * vt + 1;  // the tile's two 224-row head tiles
-        const int brow0 = t0 * kMxBN + static_cast<int>(rank) * kMxBRows;
-        const int brow1 = t1 * kMxBN + static_cast<int>(rank) * kMxBRows;
-        for (int c = 0; c < kc_n; ++c) {
-          if (lane == 0) ok = mbar_wait(&empty[st], ph ^ 1u, abort_flag, lim);
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) break;
-          if (lane == 0) {
+    if (lane == 0) {
+      int st = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      const uint32_t full_dst = mapa_shared(smem_u32(full), 0);
+      for (int it = unit; ok && it < sch.items; it += num_units) {
+        int mt, sp, vt0, vt1;
+        sch.item(it, mt, sp, vt0, vt1);
+        const int arow = mt * (kBM * CG) + static_cast<int>(rank) * kBM;
+        const int ablk = mt * CG + static_cast<int>(rank);  // 128-row block of the scale atoms
+        for (int vt = vt0; ok && vt < vt1; ++vt) {
+          const int t0 = 2 * vt, t1 = 2 * vt + 1;  // the tile's two 224-row head tiles
+          const int brow0 = t0 * kMxBN + static_cast<int>(rank) * kMxBRows;
+          const int brow1 = t1 * kMxBN + static_cast<int>(rank) * kMxBRows;
+          for (int c = 0; c < kc_n; ++c) {
+            ok = mbar_wait(&empty[st], ph ^ 1u, abort_flag, lim);
+            if (!ok) break;
             uint8_t *base = smem + st * L::kStage;
             if (leader) mbar_arrive_expect_tx(&full[st], CG * L::kTx);
             const uint32_t fb = full_dst + st * 8;
@@ -185,19 +187,20 @@ __global__ void __launch_bounds__(kMxFThreads, 1)
             tma_load_2d_pair(base + L::kOffSfa, &tmSfa, fb, 0, (ablk * kc_n + c) * 32);
             tma_load_2d_pair(base + L::kOffSfb0, &tmSfb, fb, 0, (t0 * kc_n + c) * 64);
             tma_load_2d_pair(base + L::kOffSfb1, &tmSfb, fb, 0, (t1 * kc_n + c) * 64);
-          }
-          ++issued;
-          if (++st == kMxFStages) {
-            st = 0;
-            ph ^= 1u;
+            ++issued;
+            if (++st == kMxFStages) {
+              st = 0;
+              ph ^= 1u;
+            }
           }
         }
       }
+      if (!ok) record_timeout<CG>(status, abort_flag);
     }
-    if (!ok && lane == 0) record_timeout<CG>(status, abort_flag);
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (leader) {
+    if (leader && lane == 0) {
       int st = 0;
       uint32_t ph = 0, aph = 0, g = 0;  // g: k-chunks consumed
       bool ok = true;
@@ -205,36 +208,30 @@ __global__ void __launch_bounds__(kMxFThreads, 1)
         int mt, sp, vt0, vt1;
         sch.item(it, mt, sp, vt0, vt1);
         for (int vt = vt0; ok && vt < vt1; ++vt) {
-          if (lane == 0) ok = mbar_wait(aempty, aph ^ 1u, abort_flag, lim);
-          ok = __shfl_sync(0xffffffffu, ok, 0);
+          ok = mbar_wait(aempty, aph ^ 1u, abort_flag, lim);
           if (!ok) break;
           tc_fence_after();
           for (int c = 0; c < kc_n; ++c) {
-            if (lane == 0) {
-              ok = mbar_wait(&full[st], ph, abort_flag, lim);
-              if (ok)  // the scale copier put this k-chunk's scales into its slot
-                ok = mbar_wait(&sready[g % kMxFSlots], (g / kMxFSlots) & 1u, abort_flag, lim);
-            }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
+            // the scale copier put this k-chunk's scales into its slot (after
+            // it saw the stage land), then the stage itself
+            ok = mbar_wait(&sready[g % kMxFSlots], (g / kMxFSlots) & 1u, abort_flag, lim) &&
+                 mbar_wait(&full[st], ph, abort_flag, lim);
             if (!ok) break;
             tc_fence_after();
-            if (lane == 0) {
-              const uint32_t tb = smem_u32(smem + st * L::kStage);
-              const uint32_t sf =
-                  tmem_base + static_cast<uint32_t>(L::kAccCols + (g % kMxFSlots) * L::kSfCols);
+            const uint32_t tb = smem_u32(smem + st * L::kStage);
+            const uint32_t sf =
+                tmem_base + static_cast<uint32_t>(L::kAccCols + (g % kMxFSlots) * L::kSfCols);
 #pragma unroll
-              for (int j = 0; j < kMxChunk / kMxUmmaK; ++j) {
-                const uint64_t ad = sdesc_sw128(tb + j * kMxUmmaK, 16, 1024);
-                const uint64_t bd0 = sdesc_sw128(tb + L::kOffB0 + j * kMxUmmaK, 16, 1024);
-                const uint64_t bd1 = sdesc_sw128(tb + L::kOffB1 + j * kMxUmmaK, 16, 1024);
-                const uint32_t id = idesc_mx_sf(idesc, static_cast<uint32_t>(j));
-                const uint32_t acc = (c | j) != 0 ? 1u : 0u;
-                mma_mx_pair(tmem_base, ad, bd0, id, sf, sf + 4, acc);
-                mma_mx_pair(tmem_base + kMxBN, ad, bd1, id, sf, sf + 12, acc);
-              }
-              mma_commit_pair(&empty[st], 0x3);
+            for (int j = 0; j < kMxChunk / kMxUmmaK; ++j) {
+              const uint64_t ad = sdesc_sw128(tb + j * kMxUmmaK, 16, 1024);
+              const uint64_t bd0 = sdesc_sw128(tb + L::kOffB0 + j * kMxUmmaK, 16, 1024);
+              const uint64_t bd1 = sdesc_sw128(tb + L::kOffB1 + j * kMxUmmaK, 16, 1024);
+              const uint32_t id = idesc_mx_sf(idesc, static_cast<uint32_t>(j));
+              const uint32_t acc = (c | j) != 0 ? 1u : 0u;
+              mma_mx_pair(tmem_base, ad, bd0, id, sf, sf + 4, acc);
+              mma_mx_pair(tmem_base + kMxBN, ad, bd1, id, sf, sf + 12, acc);
             }
-            __syncwarp();
+            mma_commit_pair(&empty[st], 0x3);
             ++g;
             if (++st == kMxFStages) {
               st = 0;
@@ -242,22 +239,23 @@ __global__ void __launch_bounds__(kMxFThreads, 1)
             }
           }
           if (!ok) break;
-          if (lane == 0) mma_commit_pair(afull, 0x3);  // the accumulator is ready
-          __syncwarp();
+          mma_commit_pair(afull, 0x3);  // the accumulator is ready
           aph ^= 1u;
         }
       }
-      if (!ok && lane == 0) record_timeout<CG>(status, abort_flag);
+      if (!ok) record_timeout<CG>(status, abort_flag);
     }
+    __syncwarp();
   } else if (warp == kMxFScaleWarp) {
     // ------------------------------------------------------- scale copier
     // Copies each k-chunk's five scale atoms from its stage into the chunk's
     // TMEM slot and commits that to the slot's "ready" barrier.  A slot is
     // rewritten only after the MMAs of the chunk kMxFSlots earlier, its last
     // readers, were released; waiting for that here, off the MMA issuer,
-    // keeps the issuer's thread on MMAs (its copies and MMAs would otherwise
-    // wait on the same release).
-    if (leader) {
+    // keeps the issuer's thread on MMAs.  The release also paces this warp:
+    // it never runs more than kMxFSlots chunks ahead, so each "ready" phase
+    // is consumed before the slot's next one.
+    if (leader && lane == 0) {
       int st = 0;
       uint32_t ph = 0, g = 0;
       bool ok = true;
@@ -266,28 +264,22 @@ __global__ void __launch_bounds__(kMxFThreads, 1)
         sch.item(it, mt, sp, vt0, vt1);
         for (int vt = vt0; ok && vt < vt1; ++vt) {
           for (int c = 0; c < kc_n; ++c) {
-            if (lane == 0) {
-              ok = mbar_wait(&full[st], ph, abort_flag, lim);
-              if (ok && g >= static_cast<uint32_t>(kMxFSlots)) {
-                const uint32_t gp = g - kMxFSlots;
-                ok = mbar_wait(&empty[gp % kMxFStages], (gp / kMxFStages) & 1u, abort_flag, lim);
-              }
+            ok = mbar_wait(&full[st], ph, abort_flag, lim);
+            if (ok && g >= static_cast<uint32_t>(kMxFSlots)) {
+              const uint32_t gp = g - kMxFSlots;
+              ok = mbar_wait(&empty[gp % kMxFStages], (gp / kMxFStages) & 1u, abort_flag, lim);
             }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after();
-            if (lane == 0) {
-              const uint32_t tb = smem_u32(smem + st * L::kStage);
-              const uint32_t sf =
-                  tmem_base + static_cast<uint32_t>(L::kAccCols + (g % kMxFSlots) * L::kSfCols);
-              tmem_cp_32x128b_x4_pair(sf, sdesc_rows16(tb + L::kOffSfa));
-              tmem_cp_32x128b_x4_pair(sf + 4, sdesc_rows16(tb + L::kOffSfb0));
-              tmem_cp_32x128b_x4_pair(sf + 8, sdesc_rows16(tb + L::kOffSfb0 + 512));
-              tmem_cp_32x128b_x4_pair(sf + 12, sdesc_rows16(tb + L::kOffSfb1));
-              tmem_cp_32x128b_x4_pair(sf + 16, sdesc_rows16(tb + L::kOffSfb1 + 512));
-              mma_commit_pair_local(&sready[g % kMxFSlots]);
-            }
-            __syncwarp();
+            const uint32_t tb = smem_u32(smem + st * L::kStage);
+            const uint32_t sf =
+                tmem_base + static_cast<uint32_t>(L::kAccCols + (g % kMxFSlots) * L::kSfCols);
+            tmem_cp_32x128b_x4_pair(sf, sdesc_rows16(tb + L::kOffSfa));
+            tmem_cp_32x128b_x4_pair(sf + 4, sdesc_rows16(tb + L::kOffSfb0));
+            tmem_cp_32x128b_x4_pair(sf + 8, sdesc_rows16(tb + L::kOffSfb0 + 512));
+            tmem_cp_32x128b_x4_pair(sf + 12, sdesc_rows16(tb + L::kOffSfb1));
+            tmem_cp_32x128b_x4_pair(sf + 16, sdesc_rows16(tb + L::kOffSfb1 + 512));
+            mma_commit_pair_local(&sready[g % kMxFSlots]);
             ++g;
             if (++st == kMxFStages) {
               st = 0;
@@ -296,8 +288,9 @@ __global__ void __launch_bounds__(kMxFThreads, 1)
           }
         }
       }
-      if (!ok && lane == 0) record_timeout<CG>(status, abort_flag);
+      if (!ok) record_timeout<CG>(status, abort_flag);
     }
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
     const int lg = warp & 3;
