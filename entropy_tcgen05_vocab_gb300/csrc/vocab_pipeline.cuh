@@ -425,24 +425,26 @@ __global__ void __launch_bounds__(pipe_threads(EPIW, MX), 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
+  // The producer and the MMA issuer run on one lane each (the other lanes of
+  // their warps wait at the end): no warp-wide exchange sits between one
+  // k-block's MMAs and the next's.
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    int stage = 0;
-    uint32_t phase = 0;
-    bool ok = true;
-    // the pair's bytes all complete on the leader's "full" barriers
-    const uint32_t full_dst = kPair ? mapa_shared(smem_u32(full), 0) : smem_u32(full);
-    for (int it = unit; ok && it < sch.items; it += num_units) {
-      int mt, sp, vt0, vt1;
-      sch.item(it, mt, sp, vt0, vt1);
-      const int arow = mt * (kBM * CG) + static_cast<int>(rank) * kBM;
-      for (int vt = vt0; ok && vt < vt1; ++vt) {
-        const int brow = vt * L::kTileCols + static_cast<int>(rank) * L::kBRows;
-        for (int kb = 0; kb < sch.k_blocks; ++kb) {
-          if (lane == 0) ok = mbar_wait(&empty[stage], phase ^ 1u, abort_flag, lim);
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) break;
-          if (lane == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      // the pair's bytes all complete on the leader's "full" barriers
+      const uint32_t full_dst = kPair ? mapa_shared(smem_u32(full), 0) : smem_u32(full);
+      for (int it = unit; ok && it < sch.items; it += num_units) {
+        int mt, sp, vt0, vt1;
+        sch.item(it, mt, sp, vt0, vt1);
+        const int arow = mt * (kBM * CG) + static_cast<int>(rank) * kBM;
+        for (int vt = vt0; ok && vt < vt1; ++vt) {
+          const int brow = vt * L::kTileCols + static_cast<int>(rank) * L::kBRows;
+          for (int kb = 0; kb < sch.k_blocks; ++kb) {
+            ok = mbar_wait(&empty[stage], phase ^ 1u, abort_flag, lim);
+            if (!ok) break;
             uint8_t *sa = smem + stage * L::kStageBytes;
             uint8_t *sb = sa + L::kAOps * L::kABytes;
             if (leader) mbar_arrive_expect_tx(&full[stage], CG * L::kStageBytes);
@@ -466,19 +468,20 @@ __global__ void __launch_bounds__(pipe_threads(EPIW, MX), 1)
                 if (!MX) tma_load_2d(sb + L::kBBytes, tb1, &full[stage], kb * kBK, brow1);
               }
             }
-          }
-          ++issued;
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
+            ++issued;
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
         }
       }
+      if (!ok) record_timeout<CG>(status, abort_flag);
     }
-    if (!ok && lane == 0) record_timeout<CG>(status, abort_flag);
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (leader) {
+    if (leader && lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -489,53 +492,46 @@ __global__ void __launch_bounds__(pipe_threads(EPIW, MX), 1)
         int mt, sp, vt0, vt1;
         sch.item(it, mt, sp, vt0, vt1);
         for (int vt = vt0; ok && vt < vt1; ++vt) {
-          if (lane == 0) ok = mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, lim);
-          ok = __shfl_sync(0xffffffffu, ok, 0);
+          ok = mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, lim);
           if (!ok) break;
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * L::kAccCols);
           for (int kb = 0; kb < sch.k_blocks; ++kb) {
             const int dslot = static_cast<int>(g % L::kDMod);
-            if (lane == 0) {
-              ok = mbar_wait(&full[stage], phase, abort_flag, lim);
-              if (MX && ok)
-                ok = mbar_wait_cluster(&dfull[dslot], (g / L::kDMod) & 1u, abort_flag, lim);
-            }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
+            ok = mbar_wait(&full[stage], phase, abort_flag, lim);
+            if (MX && ok)
+              ok = mbar_wait_cluster(&dfull[dslot], (g / L::kDMod) & 1u, abort_flag, lim);
             if (!ok) break;
             tc_fence_after();
-            if (lane == 0) {
-              const uint32_t a0 = smem_u32(smem + stage * L::kStageBytes);
-              const uint32_t b0 = a0 + L::kAOps * L::kABytes;
+            const uint32_t a0 = smem_u32(smem + stage * L::kStageBytes);
+            const uint32_t b0 = a0 + L::kAOps * L::kABytes;
 #pragma unroll
-              for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
+            for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
 #pragma unroll
-                for (int op = 0; op < NOPS; ++op) {
-                  const uint64_t ad = sdesc_sw128(
-                      a0 + (SHARED_A ? 0 : op) * L::kABytes + kk * kUmmaK * 2, 16, 1024);
-                  const uint32_t bop = (MX && op == 1)
-                                           ? smem_u32(dring + dslot * L::kBBytes)
-                                           : b0 + op * L::kBBytes;
-                  const uint64_t bd = sdesc_sw128(bop + kk * kUmmaK * 2, 16, 1024);
-                  if (kPair)
-                    mma_f16_pair(d_tmem + op * BN, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
-                  else
-                    mma_f16(d_tmem + op * BN, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
-                }
-              }
-              // frees the stage (in both CTAs of a pair) when these MMAs finish
-              if (kPair)
-                mma_commit_pair(&empty[stage], 0x3);
-              else
-                mma_commit(&empty[stage]);
-              if (MX) {  // and the decoded slot
+              for (int op = 0; op < NOPS; ++op) {
+                const uint64_t ad = sdesc_sw128(
+                    a0 + (SHARED_A ? 0 : op) * L::kABytes + kk * kUmmaK * 2, 16, 1024);
+                const uint32_t bop = (MX && op == 1)
+                                         ? smem_u32(dring + dslot * L::kBBytes)
+                                         : b0 + op * L::kBBytes;
+                const uint64_t bd = sdesc_sw128(bop + kk * kUmmaK * 2, 16, 1024);
                 if (kPair)
-                  mma_commit_pair(&dempty[dslot], 0x3);
+                  mma_f16_pair(d_tmem + op * BN, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
                 else
-                  mma_commit(&dempty[dslot]);
+                  mma_f16(d_tmem + op * BN, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
               }
             }
-            __syncwarp();
+            // frees the stage (in both CTAs of a pair) when these MMAs finish
+            if (kPair)
+              mma_commit_pair(&empty[stage], 0x3);
+            else
+              mma_commit(&empty[stage]);
+            if (MX) {  // and the decoded slot
+              if (kPair)
+                mma_commit_pair(&dempty[dslot], 0x3);
+              else
+                mma_commit(&dempty[dslot]);
+            }
             ++g;
             if (++stage == STAGES) {
               stage = 0;
@@ -543,19 +539,18 @@ __global__ void __launch_bounds__(pipe_threads(EPIW, MX), 1)
             }
           }
           if (!ok) break;
-          if (lane == 0) {  // accumulator ready for the epilogue(s)
-            if (kPair)
-              mma_commit_pair(&tfull[acc], 0x3);
-            else
-              mma_commit(&tfull[acc]);
-          }
-          __syncwarp();
+          // accumulator ready for the epilogue(s)
+          if (kPair)
+            mma_commit_pair(&tfull[acc], 0x3);
+          else
+            mma_commit(&tfull[acc]);
           if (NACC == 2) acc ^= 1;
           if (acc == 0) acc_phase ^= 1u;
         }
       }
-      if (!ok && lane == 0) record_timeout<CG>(status, abort_flag);
+      if (!ok) record_timeout<CG>(status, abort_flag);
     }
+    __syncwarp();
   } else if (MX && warp >= 2 + EPIW + L::kCvtWarps) {
     // ------------------------------------------------------------ MX relays
     // Relay warp r forwards group r's "this CTA decoded the stage" (a local
