@@ -140,24 +140,26 @@ __global__ void __launch_bounds__(pipe_threads(GemmCfg<CG, WIDE>::kEpiw), 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
+  // The producer and the MMA issuer run on one lane each (the other lanes of
+  // their warps wait at the end): no warp-wide exchange sits between one
+  // k-block's MMAs and the next's.
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    int stage = 0;
-    uint32_t phase = 0;
-    bool ok = true;
-    const uint32_t full_dst = kPair ? mapa_shared(smem_u32(full), 0) : smem_u32(full);
-    for (int it = unit; ok && it < g.items; it += num_units) {
-      int t, kb0, kb1, slot;
-      g.item(it, t, kb0, kb1, slot);
-      const int mt = t / g.n_tiles, nt = t - (t / g.n_tiles) * g.n_tiles;
-      const int arow = mt * (kBM * CG) + static_cast<int>(rank) * kBM;   // M offset
-      // N offset of this CTA's share of MMA op 0 (op k adds k * BN)
-      const int bcol = nt * C::kTileN + static_cast<int>(rank) * L::kBRows;
-      for (int kb = kb0; kb < kb1; ++kb) {
-        if (lane == 0) ok = mbar_wait(&empty[stage], phase ^ 1u, abort_flag, lim);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        if (lane == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      const uint32_t full_dst = kPair ? mapa_shared(smem_u32(full), 0) : smem_u32(full);
+      for (int it = unit; ok && it < g.items; it += num_units) {
+        int t, kb0, kb1, slot;
+        g.item(it, t, kb0, kb1, slot);
+        const int mt = t / g.n_tiles, nt = t - (t / g.n_tiles) * g.n_tiles;
+        const int arow = mt * (kBM * CG) + static_cast<int>(rank) * kBM;   // M offset
+        // N offset of this CTA's share of MMA op 0 (op k adds k * BN)
+        const int bcol = nt * C::kTileN + static_cast<int>(rank) * L::kBRows;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          ok = mbar_wait(&empty[stage], phase ^ 1u, abort_flag, lim);
+          if (!ok) break;
           uint8_t *sa = smem + stage * L::kStageBytes;
           uint8_t *sb = sa + L::kABytes;
           if (leader) mbar_arrive_expect_tx(&full[stage], CG * L::kStageBytes);
@@ -185,18 +187,19 @@ __global__ void __launch_bounds__(pipe_threads(GemmCfg<CG, WIDE>::kEpiw), 1)
               load(sbo, &tmB, kb * kBK, bcol + op * BN);
             }
           }
-        }
-        ++issued;
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
       }
+      if (!ok) record_timeout<CG>(status, abort_flag);
     }
-    if (!ok && lane == 0) record_timeout<CG>(status, abort_flag);
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (leader) {
+    if (leader && lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -205,58 +208,51 @@ __global__ void __launch_bounds__(pipe_threads(GemmCfg<CG, WIDE>::kEpiw), 1)
       for (int it = unit; ok && it < g.items; it += num_units) {
         int t, kb0, kb1, slot;
         g.item(it, t, kb0, kb1, slot);
-        if (lane == 0) ok = mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, lim);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
+        ok = mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, lim);
         if (!ok) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * L::kAccCols);
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (lane == 0) ok = mbar_wait(&full[stage], phase, abort_flag, lim);
-          ok = __shfl_sync(0xffffffffu, ok, 0);
+          ok = mbar_wait(&full[stage], phase, abort_flag, lim);
           if (!ok) break;
           tc_fence_after();
-          if (lane == 0) {
-            const uint32_t a0 = smem_u32(smem + stage * L::kStageBytes);
-            const uint32_t b0 = a0 + L::kABytes;
+          const uint32_t a0 = smem_u32(smem + stage * L::kStageBytes);
+          const uint32_t b0 = a0 + L::kABytes;
 #pragma unroll
-            for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
-              const uint64_t ad = A_MN ? sdesc_sw128(a0 + kk * 2048, 8192, 1024)
-                                       : sdesc_sw128(a0 + kk * kUmmaK * 2, 16, 1024);
+          for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
+            const uint64_t ad = A_MN ? sdesc_sw128(a0 + kk * 2048, 8192, 1024)
+                                     : sdesc_sw128(a0 + kk * kUmmaK * 2, 16, 1024);
 #pragma unroll
-              for (int op = 0; op < NOPS; ++op) {
-                const uint32_t bo = b0 + op * L::kBBytes;
-                const uint64_t bd = B_MN ? sdesc_sw128(bo + kk * 2048, 8192, 1024)
-                                         : sdesc_sw128(bo + kk * kUmmaK * 2, 16, 1024);
-                if (kPair)
-                  mma_f16_pair(d_tmem + op * BN, ad, bd, idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
-                else
-                  mma_f16(d_tmem + op * BN, ad, bd, idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
-              }
+            for (int op = 0; op < NOPS; ++op) {
+              const uint32_t bo = b0 + op * L::kBBytes;
+              const uint64_t bd = B_MN ? sdesc_sw128(bo + kk * 2048, 8192, 1024)
+                                       : sdesc_sw128(bo + kk * kUmmaK * 2, 16, 1024);
+              if (kPair)
+                mma_f16_pair(d_tmem + op * BN, ad, bd, idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
+              else
+                mma_f16(d_tmem + op * BN, ad, bd, idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
             }
-            if (kPair)
-              mma_commit_pair(&empty[stage], 0x3);
-            else
-              mma_commit(&empty[stage]);
           }
-          __syncwarp();
+          if (kPair)
+            mma_commit_pair(&empty[stage], 0x3);
+          else
+            mma_commit(&empty[stage]);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        if (lane == 0) {
-          if (kPair)
-            mma_commit_pair(&tfull[acc], 0x3);
-          else
-            mma_commit(&tfull[acc]);
-        }
-        __syncwarp();
+        if (kPair)
+          mma_commit_pair(&tfull[acc], 0x3);
+        else
+          mma_commit(&tfull[acc]);
         if (C::kNacc == 2) acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }
-      if (!ok && lane == 0) record_timeout<CG>(status, abort_flag);
+      if (!ok) record_timeout<CG>(status, abort_flag);
     }
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
     const int lg = warp & 3;

@@ -173,28 +173,30 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   pipe_sync<CG>();
   const uint32_t tmem_base = *tmem_slot;
 
+  // Producers and MMA issuers run on one lane each (the other lanes of their
+  // warps wait at the end): no warp-wide exchange sits between one k-chunk's
+  // MMAs and the next's.
   if (warp == 0 || warp == kMxTProdWarp) {
     // ----------------------------------------------------------- producers
     // Warp 0 fills the student ring, warp kMxTProdWarp the teacher ring.
     const bool teacher = warp == kMxTProdWarp;
-    int st = 0;
-    uint32_t ph = 0, issued = 0;
-    bool ok = true;
-    const uint32_t full_dst = mapa_shared(smem_u32(teacher ? tfull : sfull), 0);
-    uint64_t *empty = teacher ? tempty : sempty;
-    const int stages = teacher ? kMxTStages : kMxSStages;
-    for (int it = unit; ok && it < sch.items; it += num_units) {
-      int mt, sp, vt0, vt1;
-      sch.item(it, mt, sp, vt0, vt1);
-      const int arow = mt * (kBM * CG) + static_cast<int>(rank) * kBM;
-      const int ablk = mt * CG + static_cast<int>(rank);  // 128-row block of the scale atoms
-      for (int vt = vt0; ok && vt < vt1; ++vt) {
-        const int brow = vt * kMxBN + static_cast<int>(rank) * kMxBRows;
-        for (int c = 0; c < kc_n; ++c) {
-          if (lane == 0) ok = mbar_wait(&empty[st], ph ^ 1u, abort_flag, lim);
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) break;
-          if (lane == 0) {
+    if (lane == 0) {
+      int st = 0;
+      uint32_t ph = 0, issued = 0;
+      bool ok = true;
+      const uint32_t full_dst = mapa_shared(smem_u32(teacher ? tfull : sfull), 0);
+      uint64_t *empty = teacher ? tempty : sempty;
+      const int stages = teacher ? kMxTStages : kMxSStages;
+      for (int it = unit; ok && it < sch.items; it += num_units) {
+        int mt, sp, vt0, vt1;
+        sch.item(it, mt, sp, vt0, vt1);
+        const int arow = mt * (kBM * CG) + static_cast<int>(rank) * kBM;
+        const int ablk = mt * CG + static_cast<int>(rank);  // 128-row block of the scale atoms
+        for (int vt = vt0; ok && vt < vt1; ++vt) {
+          const int brow = vt * kMxBN + static_cast<int>(rank) * kMxBRows;
+          for (int c = 0; c < kc_n; ++c) {
+            ok = mbar_wait(&empty[st], ph ^ 1u, abort_flag, lim);
+            if (!ok) break;
             const uint32_t fb = full_dst + st * 8;
             if (teacher) {
               // teacher k-chunk c: codes of A_t and B_t, then the scale atoms
@@ -214,20 +216,21 @@ __global__ void __launch_bounds__(kMxThreads, 1)
               tma_load_2d_pair(sa + 2 * L::kSA, &tmBs, fb, 2 * c * kBK, brow);
               tma_load_2d_pair(sa + 2 * L::kSA + L::kSB, &tmBs, fb, (2 * c + 1) * kBK, brow);
             }
-          }
-          ++issued;
-          if (++st == stages) {
-            st = 0;
-            ph ^= 1u;
+            ++issued;
+            if (++st == stages) {
+              st = 0;
+              ph ^= 1u;
+            }
           }
         }
       }
+      if (teacher)
+        t_issued = issued;
+      else
+        s_issued = issued;
+      if (!ok) record_timeout<CG>(status, abort_flag);
     }
-    if (teacher)
-      t_issued = issued;
-    else
-      s_issued = issued;
-    if (!ok && lane == 0) record_timeout<CG>(status, abort_flag);
+    __syncwarp();
   } else if (warp == 1 || warp == kMxTMmaWarp) {
     // --------------------------------------------------------- MMA issuers
     // Warp 1 issues the student's bf16 MMAs, warp kMxTMmaWarp the teacher's
@@ -235,7 +238,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     // its own tcgen05 operations, so while one issuer waits for a stage or
     // commits, the other keeps the tensor pipe fed.  Both commit to "afull"
     // (two arrivals per tile) and both wait for the epilogue's "aempty".
-    if (leader) {
+    if (leader && lane == 0) {
       const bool teacher = warp == kMxTMmaWarp;
       int st = 0;
       uint32_t ph = 0, aph = 0;
@@ -249,58 +252,52 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         int mt, sp, vt0, vt1;
         sch.item(it, mt, sp, vt0, vt1);
         for (int vt = vt0; ok && vt < vt1; ++vt) {
-          if (lane == 0) ok = mbar_wait(aempty, aph ^ 1u, abort_flag, lim);
-          ok = __shfl_sync(0xffffffffu, ok, 0);
+          ok = mbar_wait(aempty, aph ^ 1u, abort_flag, lim);
           if (!ok) break;
           tc_fence_after();
           for (int c = 0; c < kc_n; ++c) {
-            if (lane == 0) ok = mbar_wait(&full[st], ph, abort_flag, lim);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
+            ok = mbar_wait(&full[st], ph, abort_flag, lim);
             if (!ok) break;
             tc_fence_after();
-            if (lane == 0) {
-              if (teacher) {
-                const uint32_t tb = smem_u32(smem + L::kTRing + st * L::kTStage);
-                const uint32_t sf = tmem_base + static_cast<uint32_t>(L::kSfCol0 + st * L::kSfCols);
-                tmem_cp_32x128b_x4_pair(sf, sdesc_rows16(tb + L::kTA + L::kTB));
-                tmem_cp_32x128b_x4_pair(sf + 4, sdesc_rows16(tb + L::kTA + L::kTB + L::kSfa));
-                tmem_cp_32x128b_x4_pair(sf + 8,
-                                        sdesc_rows16(tb + L::kTA + L::kTB + L::kSfa + 512));
+            if (teacher) {
+              const uint32_t tb = smem_u32(smem + L::kTRing + st * L::kTStage);
+              const uint32_t sf = tmem_base + static_cast<uint32_t>(L::kSfCol0 + st * L::kSfCols);
+              tmem_cp_32x128b_x4_pair(sf, sdesc_rows16(tb + L::kTA + L::kTB));
+              tmem_cp_32x128b_x4_pair(sf + 4, sdesc_rows16(tb + L::kTA + L::kTB + L::kSfa));
+              tmem_cp_32x128b_x4_pair(sf + 8, sdesc_rows16(tb + L::kTA + L::kTB + L::kSfa + 512));
 #pragma unroll
-                for (int j = 0; j < kMxChunk / kMxUmmaK; ++j) {
-                  const uint64_t ad = sdesc_sw128(tb + j * kMxUmmaK, 16, 1024);
-                  const uint64_t bd = sdesc_sw128(tb + L::kTA + j * kMxUmmaK, 16, 1024);
-                  mma_mx_pair(d_teacher, ad, bd, idesc_mx_sf(idesc_t, static_cast<uint32_t>(j)),
-                              sf, sf + 4, (c | j) != 0 ? 1u : 0u);
-                }
-              } else {
-                const uint32_t sa = smem_u32(smem + st * L::kSStage);
-#pragma unroll
-                for (int h = 0; h < 2; ++h)
-#pragma unroll
-                  for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
-                    const uint64_t ad = sdesc_sw128(sa + h * L::kSA + kk * kUmmaK * 2, 16, 1024);
-                    const uint64_t bd =
-                        sdesc_sw128(sa + 2 * L::kSA + h * L::kSB + kk * kUmmaK * 2, 16, 1024);
-                    mma_f16_pair(d_student, ad, bd, idesc_s, (c | h | kk) != 0 ? 1u : 0u);
-                  }
+              for (int j = 0; j < kMxChunk / kMxUmmaK; ++j) {
+                const uint64_t ad = sdesc_sw128(tb + j * kMxUmmaK, 16, 1024);
+                const uint64_t bd = sdesc_sw128(tb + L::kTA + j * kMxUmmaK, 16, 1024);
+                mma_mx_pair(d_teacher, ad, bd, idesc_mx_sf(idesc_t, static_cast<uint32_t>(j)), sf,
+                            sf + 4, (c | j) != 0 ? 1u : 0u);
               }
-              mma_commit_pair(&empty[st], 0x3);
+            } else {
+              const uint32_t sa = smem_u32(smem + st * L::kSStage);
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
+                  const uint64_t ad = sdesc_sw128(sa + h * L::kSA + kk * kUmmaK * 2, 16, 1024);
+                  const uint64_t bd =
+                      sdesc_sw128(sa + 2 * L::kSA + h * L::kSB + kk * kUmmaK * 2, 16, 1024);
+                  mma_f16_pair(d_student, ad, bd, idesc_s, (c | h | kk) != 0 ? 1u : 0u);
+                }
             }
-            __syncwarp();
+            mma_commit_pair(&empty[st], 0x3);
             if (++st == stages) {
               st = 0;
               ph ^= 1u;
             }
           }
           if (!ok) break;
-          if (lane == 0) mma_commit_pair(afull, 0x3);  // this issuer's accumulator is ready
-          __syncwarp();
+          mma_commit_pair(afull, 0x3);  // this issuer's accumulator is ready
           aph ^= 1u;
         }
       }
-      if (!ok && lane == 0) record_timeout<CG>(status, abort_flag);
+      if (!ok) record_timeout<CG>(status, abort_flag);
     }
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
     const int lg = warp & 3;
