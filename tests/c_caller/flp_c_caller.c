@@ -9,8 +9,10 @@
  * DIR holds h.bin (T x H bf16 bits), W.bin (V x H), ht.bin, Wt.bin (the
  * teacher's), targets.bin (T int64), rows.bin (N int64), g1.bin, g2.bin
  * (N float32).  Writes logp.bin, ent.bin, kl.bin, klmx.bin (N float32; the
- * last with the teacher on the block-scaled tensor cores), dh.bin (T x H bf16
- * bits) and dW.bin (V x H float32).  Exit status 0 on success,
+ * last with the teacher on the block-scaled tensor cores), logpmx.bin and
+ * entmx.bin (N float32: h scored against the teacher's head, in MXFP4, on the
+ * block-scaled tensor cores), dh.bin (T x H bf16 bits) and dW.bin (V x H
+ * float32).  Exit status 0 on success,
  * 2 on a library or CUDA error (the reason is printed).
  */
 #include <stdint.h>
@@ -111,6 +113,8 @@ int main(int argc, char **argv) {
   size_t ws_bytes = flp_workspace_size(&s, FLP_OP_LOGPROB_ENTROPY);
   const size_t ws_kl = flp_workspace_size(&s, FLP_OP_KL), ws_bw = flp_workspace_size(&s, FLP_OP_BACKWARD);
   const size_t ws_klmx = flp_workspace_size(&s, FLP_OP_KL_MX);
+  const size_t ws_fmx = flp_workspace_size(&s, FLP_OP_LOGPROB_ENTROPY_MX);
+  if (ws_fmx > ws_bytes) ws_bytes = ws_fmx;
   if (ws_kl > ws_bytes) ws_bytes = ws_kl;
   if (ws_bw > ws_bytes) ws_bytes = ws_bw;
   if (ws_klmx > ws_bytes) ws_bytes = ws_klmx;
@@ -124,10 +128,12 @@ int main(int argc, char **argv) {
     return 2;
   }
   void *ws = NULL, *d_logp = NULL, *d_ent = NULL, *d_kl = NULL, *d_dh = NULL, *d_dW = NULL;
-  void *d_head = NULL, *d_klmx = NULL;
+  void *d_head = NULL, *d_klmx = NULL, *d_lpmx = NULL, *d_enmx = NULL;
   CUDA_OK(cudaMalloc(&ws, ws_bytes));
   CUDA_OK(cudaMalloc(&d_head, head_bytes));
   CUDA_OK(cudaMalloc(&d_klmx, (size_t)N * 4 + 16));
+  CUDA_OK(cudaMalloc(&d_lpmx, (size_t)N * 4 + 16));
+  CUDA_OK(cudaMalloc(&d_enmx, (size_t)N * 4 + 16));
   CUDA_OK(cudaMalloc(&d_logp, (size_t)N * 4 + 16));
   CUDA_OK(cudaMalloc(&d_ent, (size_t)N * 4 + 16));
   CUDA_OK(cudaMalloc(&d_kl, (size_t)N * 4 + 16));
@@ -145,6 +151,9 @@ int main(int argc, char **argv) {
   FLP_OK_(flp_kl_mx(&s, d_h, d_W, d_ht, d_head, (const int64_t *)d_rows, (float *)d_klmx, ws, ws_bytes,
                     NULL));
   FLP_OK_(flp_read_device_status(ws, &st, NULL));
+  FLP_OK_(flp_logprob_entropy_mx(&s, d_h, d_head, (const int64_t *)d_tg, (const int64_t *)d_rows, tau,
+                                 (float *)d_lpmx, (float *)d_enmx, NULL, NULL, ws, ws_bytes, NULL));
+  FLP_OK_(flp_read_device_status(ws, &st, NULL));
   FLP_OK_(flp_backward(&s, d_h, d_W, (const int64_t *)d_tg, (const int64_t *)d_rows, tau,
                        (const float *)d_g1, (const float *)d_g2, NULL, NULL, d_dh, (float *)d_dW, ws,
                        ws_bytes, NULL));
@@ -160,11 +169,14 @@ int main(int argc, char **argv) {
   CUDA_OK(cudaDeviceSynchronize());
 
   float *logp = malloc((size_t)N * 4 + 4), *ent = malloc((size_t)N * 4 + 4), *kl = malloc((size_t)N * 4 + 4);
-  float *klmx = malloc((size_t)N * 4 + 4);
+  float *klmx = malloc((size_t)N * 4 + 4), *lpmx = malloc((size_t)N * 4 + 4);
+  float *enmx = malloc((size_t)N * 4 + 4);
   void *dh = malloc(hb);
   float *dW = malloc((size_t)V * H * 4);
-  if (!logp || !ent || !kl || !klmx || !dh || !dW) return 2;
+  if (!logp || !ent || !kl || !klmx || !lpmx || !enmx || !dh || !dW) return 2;
   CUDA_OK(cudaMemcpy(klmx, d_klmx, (size_t)N * 4, cudaMemcpyDeviceToHost));
+  CUDA_OK(cudaMemcpy(lpmx, d_lpmx, (size_t)N * 4, cudaMemcpyDeviceToHost));
+  CUDA_OK(cudaMemcpy(enmx, d_enmx, (size_t)N * 4, cudaMemcpyDeviceToHost));
   CUDA_OK(cudaMemcpy(logp, d_logp, (size_t)N * 4, cudaMemcpyDeviceToHost));
   CUDA_OK(cudaMemcpy(ent, d_ent, (size_t)N * 4, cudaMemcpyDeviceToHost));
   CUDA_OK(cudaMemcpy(kl, d_kl, (size_t)N * 4, cudaMemcpyDeviceToHost));
@@ -172,6 +184,8 @@ int main(int argc, char **argv) {
   CUDA_OK(cudaMemcpy(dW, d_dW, (size_t)V * H * 4, cudaMemcpyDeviceToHost));
   if (write_file(dir, "logp.bin", logp, (size_t)N * 4) || write_file(dir, "ent.bin", ent, (size_t)N * 4) ||
       write_file(dir, "kl.bin", kl, (size_t)N * 4) || write_file(dir, "klmx.bin", klmx, (size_t)N * 4) ||
+      write_file(dir, "logpmx.bin", lpmx, (size_t)N * 4) ||
+      write_file(dir, "entmx.bin", enmx, (size_t)N * 4) ||
       write_file(dir, "dh.bin", dh, hb) ||
       write_file(dir, "dW.bin", dW, (size_t)V * H * 4)) {
     fprintf(stderr, "writing the outputs failed\n");

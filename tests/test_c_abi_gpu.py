@@ -74,6 +74,11 @@ def test_plain_c_caller(tmp_path):
     packed, scales = coracle.mxfp4_quantize(k["W_t"], "bf16")
     want_klmx = coracle.kl_mx(d["h"], d["W"], k["h_t"], packed, scales, rows, "bf16")
     assert np.abs(out("klmx.bin", np.float32, (n,)) - want_klmx).max() <= 1e-3
+    # h scored against the teacher's head (MXFP4) on the block-scaled tensor cores
+    omx = coracle.logprob_entropy_mx(d["h"], packed, scales, V, d["targets"].numpy(), rows, tau,
+                                     "bf16")
+    assert np.abs(out("logpmx.bin", np.float32, (n,)) - omx["logp"]).max() <= 1e-3
+    assert np.abs(out("entmx.bin", np.float32, (n,)) - omx["ent"]).max() <= 1e-3
     dh_rows, dW = coracle.backward(d["h"], d["W"], d["targets"].numpy(), rows, tau,
                                    d["g1"].numpy(), d["g2"].numpy(), "bf16")
     dh = coracle.scatter_rows(dh_rows, rows, T)

@@ -10,8 +10,9 @@ random places: a part of a 128-row tile, of a 64-wide K block, of a
 32-column chunk and of a 512-column vocabulary tile, and the few-rows path
 (n <= 128) against the pair path.  Each case is small enough for the C
 oracle to finish in about a second.  The same cases also run the K-target
-forward, the forward and backward under a sampling support, and the KL with
-an MXFP4 teacher head, decoded and on the block-scaled tensor cores.
+forward, the forward and backward under a sampling support, the KL with an
+MXFP4 teacher head, decoded and on the block-scaled tensor cores, and the
+forward on the block-scaled tensor cores.
 
 Tolerances are those of the fixed-shape tests: |d logp|, |d ent|, |d KL|
 <= 1e-3 absolute; gradients within 1e-2 relative (Frobenius, and every
@@ -241,3 +242,27 @@ def test_kl_block_scaled_sweep(case):
     want = coracle.kl_mx(d["h_s"].cpu(), d["W_s"].cpu(), d["h_t"].cpu(), packed, scales, rows,
                          dtype)
     _abs(kl, want, "kl (block-scaled teacher)")
+
+
+MXF_CASES = CASES[2::3]
+
+
+@pytest.mark.parametrize("case", MXF_CASES, ids=[_id(c) for c in MXF_CASES])
+def test_forward_block_scaled_sweep(case):
+    """Scoring on the block-scaled tensor cores (MXFP8 rows, MXFP4 head),
+    bf16 and fp16, the case's temperature and rows; H rounded up to a
+    multiple of 128 (whole k-chunks)."""
+    T, H, V, dtype, tau, rows, seed = case
+    H = 128 * ((H + 127) // 128)
+    d = _scaled("fwd", T, H, V, dtype, tau, seed)
+    head = flp.mx_head_quantize(d["W"])
+    ri = None if rows is None else torch.from_numpy(rows).cuda()
+    logp, ent, lse, ez = flp.logprob_entropy_mx(d["h"], head, V, d["targets"], ri, tau,
+                                                return_stats=True)
+    torch.cuda.synchronize()
+    packed, scales = coracle.mxfp4_quantize(d["W"].cpu(), dtype)
+    o = coracle.logprob_entropy_mx(d["h"].cpu(), packed, scales, V, d["targets"].cpu().numpy(),
+                                   rows, tau, dtype)
+    _abs(logp, o["logp"], "logp (block-scaled)")
+    _abs(ent, o["ent"], "ent (block-scaled)")
+    _abs(lse, o["lse"], "lse (block-scaled)")
