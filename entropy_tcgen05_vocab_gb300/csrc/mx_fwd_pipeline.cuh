@@ -35,10 +35,9 @@
 // than the stages, so before it rewrites slot g % kMxFSlots for k-chunk g
 // the copier waits for the release of k-chunk g - kMxFSlots, whose MMAs were
 // that slot's last readers.  (With the copies and that wait on the issuer's
-// own thread, the issuer spent about 12 % of its time in that wait, with
-// the tensor pipe idle.)  Eight epilogue warps
-// (two per TMEM lane quarter, 224 columns each) fold the accumulator 32
-// columns at a time.
+// own thread, the issuer spent about 12 % of its time in that wait and a
+// call took a quarter longer.)  Eight epilogue warps (two per TMEM lane
+// quarter, 224 columns each) fold the accumulator 32 columns at a time.
 #pragma once
 
 #include "launch.h"
@@ -53,8 +52,10 @@ constexpr int kMxFSlots = 3;
 // copier (leader CTA)
 constexpr int kMxFScaleWarp = 2 + kMxFEpiWarps;
 constexpr int kMxFThreads = 32 * (kMxFScaleWarp + 1);
-static_assert(kMxFStages > kMxFSlots, "a slot's last readers are released before the issuer "
-                                      "can reach the chunk after next in their stage");
+// The copier's parity wait for the release of chunk g - kMxFSlots is
+// unambiguous: that stage's next release (chunk g - kMxFSlots + kMxFStages)
+// comes after chunk g's MMAs, which wait for this copier.
+static_assert(kMxFStages > kMxFSlots, "the release waited for is its stage's latest");
 
 struct MxFwdLayout {
   static constexpr int kA = kBM * kMxChunk;             // 16384: 128 rows x 128 E4M3
