@@ -189,6 +189,19 @@ def test_planner_covers_all_tiles_and_balances(L, wid, sms):
         assert p["max_tiles_per_cta"] <= 1.04 * total / units + 1
 
 
+@pytest.mark.parametrize("n,V", [(4096, 151936), (256, 8192), (1, 224), (29492, 38016)])
+def test_planner_block_scaled_ops(L, n, V):
+    """The block-scaled KL plans 256 x 224 pair tiles and the block-scaled
+    forward 256 x 448 (two head tiles), every split non-empty."""
+    for op, bn in ((3, 224), (4, 448)):
+        p = flp.plan(_shape(T=n, H=4096, V=V, n=n), op, 152)
+        assert p["cta_group"] == 2 and p["block_m"] == 256 and p["block_n"] == bn
+        assert p["vocab_tiles"] == math.ceil(V / bn)
+        S, tps = p["splits"], p["tiles_per_split"]
+        assert tps * (S - 1) < p["vocab_tiles"] <= tps * S
+        assert p["items"] == p["row_tiles"] * S and p["grid"] == 2 * min(p["items"], 76)
+
+
 def test_row_chunks_match_the_pages_example(L):
     rows = [list(map(int, ln.split())) for ln in open(os.path.join(ROOT, "tests", "golden",
                                                                      "chunk_shapes.txt"))
