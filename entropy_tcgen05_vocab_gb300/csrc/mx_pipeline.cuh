@@ -56,7 +56,8 @@
 namespace flp {
 
 constexpr int kMxBRows = kMxBN / 2;   // B rows per CTA
-constexpr int kMxSStages = 2;
+constexpr int kMxSKb = 1;      // 64-wide k-blocks per student stage
+constexpr int kMxSStages = 4;
 constexpr int kMxTStages = 3;
 // warps: 0 student producer, 1 TMEM allocation + student MMA issuer, 2..9
 // epilogue, 10 teacher producer, 11 teacher MMA issuer
@@ -68,7 +69,7 @@ constexpr int kMxUmmaK = 32;          // K per block-scaled MMA
 struct MxPipeLayout {
   static constexpr int kSA = kBM * kBK * 2;             // 16384: one 64-wide k-block of A_s
   static constexpr int kSB = kMxBRows * kBK * 2;        // 14336: one k-block of B_s
-  static constexpr int kSStage = 2 * (kSA + kSB);       // 61440: A_s kb 0, 1 then B_s kb 0, 1
+  static constexpr int kSStage = kMxSKb * (kSA + kSB);  // A_s k-blocks, then B_s k-blocks
   static constexpr int kTA = kBM * kMxChunk;            // 16384: 128 rows x 128 E4M3
   static constexpr int kTB = kMxBRows * kMxChunk;       // 14336: padded E2M1 in shared memory
   static constexpr int kTBTx = kMxBRows * kMxChunk / 2; // 7168: code bytes the copy counts
@@ -207,19 +208,33 @@ __global__ void __launch_bounds__(kMxThreads, 1)
               tma_load_2d_pair(base + L::kTA + L::kTB, &tmSfa, fb, 0, (ablk * kc_n + c) * 32);
               tma_load_2d_pair(base + L::kTA + L::kTB + L::kSfa, &tmSfb, fb, 0,
                                (vt * kc_n + c) * 64);
+              ++issued;
+              if (++st == stages) {
+                st = 0;
+                ph ^= 1u;
+              }
             } else {
-              // student k-blocks 2c and 2c + 1
-              uint8_t *sa = smem + st * L::kSStage;
-              if (leader) mbar_arrive_expect_tx(&sfull[st], CG * L::kSStage);
-              tma_load_2d_pair(sa, &tmAs, fb, 2 * c * kBK, arow);
-              tma_load_2d_pair(sa + L::kSA, &tmAs, fb, (2 * c + 1) * kBK, arow);
-              tma_load_2d_pair(sa + 2 * L::kSA, &tmBs, fb, 2 * c * kBK, brow);
-              tma_load_2d_pair(sa + 2 * L::kSA + L::kSB, &tmBs, fb, (2 * c + 1) * kBK, brow);
-            }
-            ++issued;
-            if (++st == stages) {
-              st = 0;
-              ph ^= 1u;
+              // student k-blocks 2c and 2c + 1, kMxSKb per stage
+              for (int hb = 0; hb < 2; hb += kMxSKb) {
+                if (hb > 0) {
+                  ok = mbar_wait(&empty[st], ph ^ 1u, abort_flag, lim);
+                  if (!ok) break;
+                }
+                uint8_t *sa = smem + st * L::kSStage;
+                if (leader) mbar_arrive_expect_tx(&sfull[st], CG * L::kSStage);
+                const uint32_t fbs = full_dst + st * 8;
+                for (int h = 0; h < kMxSKb; ++h) {
+                  const int kb = 2 * c + hb + h;
+                  tma_load_2d_pair(sa + h * L::kSA, &tmAs, fbs, kb * kBK, arow);
+                  tma_load_2d_pair(sa + kMxSKb * L::kSA + h * L::kSB, &tmBs, fbs, kb * kBK, brow);
+                }
+                ++issued;
+                if (++st == stages) {
+                  st = 0;
+                  ph ^= 1u;
+                }
+              }
+              if (!ok) break;
             }
           }
         }
@@ -272,22 +287,36 @@ __global__ void __launch_bounds__(kMxThreads, 1)
                 mma_mx_pair(d_teacher, ad, bd, idesc_mx_sf(idesc_t, static_cast<uint32_t>(j)), sf,
                             sf + 4, (c | j) != 0 ? 1u : 0u);
               }
+              mma_commit_pair(&empty[st], 0x3);
+              if (++st == stages) {
+                st = 0;
+                ph ^= 1u;
+              }
             } else {
-              const uint32_t sa = smem_u32(smem + st * L::kSStage);
-#pragma unroll
-              for (int h = 0; h < 2; ++h)
-#pragma unroll
-                for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
-                  const uint64_t ad = sdesc_sw128(sa + h * L::kSA + kk * kUmmaK * 2, 16, 1024);
-                  const uint64_t bd =
-                      sdesc_sw128(sa + 2 * L::kSA + h * L::kSB + kk * kUmmaK * 2, 16, 1024);
-                  mma_f16_pair(d_student, ad, bd, idesc_s, (c | h | kk) != 0 ? 1u : 0u);
+              // student k-blocks 2c and 2c + 1, kMxSKb per stage
+              for (int hb = 0; hb < 2; hb += kMxSKb) {
+                if (hb > 0) {
+                  ok = mbar_wait(&full[st], ph, abort_flag, lim);
+                  if (!ok) break;
+                  tc_fence_after();
                 }
-            }
-            mma_commit_pair(&empty[st], 0x3);
-            if (++st == stages) {
-              st = 0;
-              ph ^= 1u;
+                const uint32_t sa = smem_u32(smem + st * L::kSStage);
+#pragma unroll
+                for (int h = 0; h < kMxSKb; ++h)
+#pragma unroll
+                  for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
+                    const uint64_t ad = sdesc_sw128(sa + h * L::kSA + kk * kUmmaK * 2, 16, 1024);
+                    const uint64_t bd = sdesc_sw128(
+                        sa + kMxSKb * L::kSA + h * L::kSB + kk * kUmmaK * 2, 16, 1024);
+                    mma_f16_pair(d_student, ad, bd, idesc_s, (c | hb | h | kk) != 0 ? 1u : 0u);
+                  }
+                mma_commit_pair(&empty[st], 0x3);
+                if (++st == stages) {
+                  st = 0;
+                  ph ^= 1u;
+                }
+              }
+              if (!ok) break;
             }
           }
           if (!ok) break;
