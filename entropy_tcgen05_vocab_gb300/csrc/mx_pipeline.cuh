@@ -13,9 +13,9 @@
 // item = (256-row tile, vocabulary split) as in vocab_pipeline.cuh.  Two
 // operand rings per CTA, each with its own producer warp and (in the leader
 // CTA) its own MMA-issuing thread:
-//   student ring  kMxSStages stages of one 128-wide k-chunk: A_s (128 x 128
-//                 bf16, two 64-wide k-blocks) and B_s (112 x 128 bf16),
-//                 128B-swizzled, four tensor-map copies;
+//   student ring  kMxSStages stages of kMxSKb 64-wide k-blocks: A_s (128
+//                 rows) and B_s (112 rows) bf16, 128B-swizzled, two
+//                 tensor-map copies per k-block;
 //   teacher ring  kMxTStages stages of one 128-wide k-chunk: A_t (128 x 128
 //                 E4M3), B_t (112 x 128 E2M1 in the padded layout the MMA
 //                 reads: each 16 elements as 8 bytes of codes and an 8-byte
@@ -32,18 +32,19 @@
 // TMEM (512 columns): student accumulator [0, 224), teacher accumulator
 // [224, 448), and 12 scale columns per teacher stage from 448 (4 for A, 8 for
 // B).  Per 128-wide k-chunk the teacher's issuer copies the chunk's scales
-// into its stage's columns and issues four block-scaled MMAs (K = 32, scale
-// id = step) into the teacher accumulator; the student's issuer issues
-// eight bf16 MMAs (K = 16) into the student accumulator; each commits once
-// to release its stage.  Issuing an MMA blocks the thread for about the
-// MMA's own execution time (the tensor pipe's queue is shallow), so every
-// other operation an issuing thread adds between MMAs -- a commit, a wait
-// -- would stretch the pipe's critical path if one thread issued both
-// heads; with two issuers one keeps the pipe fed while the other waits or
-// commits.  For the same reason a student stage is a whole 128-wide k-chunk
-// (one commit and one wait per eight MMAs).  The copies and MMAs of one
-// thread execute in issue order, and a stage's scale columns are rewritten
-// only after the MMAs that read them released that stage.  Each issuer
+// into its stage's columns, issues four block-scaled MMAs (K = 32, scale
+// id = step) into the teacher accumulator and commits once to release the
+// stage; the student's issuer issues four bf16 MMAs (K = 16) per k-block
+// stage into the student accumulator and commits each stage.  Issuing an
+// MMA blocks the thread for about the MMA's own execution time (the tensor
+// pipe's queue is shallow), so every other operation an issuing thread adds
+// between MMAs -- a commit, a wait -- would stretch the pipe's critical path
+// if one thread issued both heads; with two issuers one keeps the pipe fed
+// while the other waits or commits.  Small student stages keep more of that
+// ring's bytes in flight: with two 128-wide stages the student issuer
+// waited for data 44 % of its time.  The copies and MMAs of one thread
+// execute in issue order, and a stage's scale columns are rewritten only
+// after the MMAs that read them released that stage.  Each issuer
 // commits to the accumulators' "full" barrier once per tile (two arrivals)
 // and both wait for the epilogue to hand the accumulators back.
 // Eight epilogue warps (two per TMEM lane quarter, 112 columns each) fold
