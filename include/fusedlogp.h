@@ -352,7 +352,12 @@ flp_status flp_kl_mx(const flp_shape *shape, const void *h_s, const void *W_s,
  * n_rows == T).  Bad rows and targets are handled as in flp_logprob_entropy.
  * Workspace: flp_workspace_size(shape, FLP_OP_LOGPROB_ENTROPY_MX) (it holds
  * the quantised rows: n_rows * H bytes plus their scales).  shape->ld_w is
- * not used but must pass the shape checks (set it to H).
+ * not used but must pass the shape checks (set it to H).  The head buffer
+ * must hold flp_mx_head_bytes(V, H) bytes (the library cannot check its
+ * size).  Errors: FLP_ERR_INVALID_ARG for H not a multiple of 128, a
+ * non-finite or non-positive temperature, a missing or misaligned pointer,
+ * or sizes beyond the 32-bit coordinates of the scale atoms;
+ * FLP_ERR_WORKSPACE for a missing or short workspace.
  */
 flp_status flp_logprob_entropy_mx(const flp_shape *shape, const void *h, const void *head,
                                   const int64_t *targets, const int64_t *row_idx,
