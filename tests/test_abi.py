@@ -352,6 +352,12 @@ def test_block_scaled_forward_validates_on_host(L):
     assert call(s, a0=ctypes.c_void_p((1 << 20) + 8)) == 1               # h alignment
     assert call(s, a9=None) == 3                                         # workspace
     assert call(s, a10=ctypes.c_size_t(16)) == 3
+    # a vocabulary whose scale atoms would pass the 32-bit coordinates of the
+    # tiling (cdiv(V, 224) * H/128 * 64 rows of atoms); rejected on the host
+    huge = _shape(T=256, H=4096, V=300_000_000, n=256, ld_h=4096, ld_w=4096)
+    assert call(huge) == 1 and "tiling range" in flp.lib().flp_last_error().decode()
+    assert L.flp_kl_mx(ctypes.byref(huge), FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, big,
+                       None) == 1
 
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
