@@ -9,6 +9,8 @@ vocabulary rows past it.  Each output is compared with the float64 C oracle
 on those rows only (the oracle is given just the sampled rows of h):
 log-prob and entropy within 1e-3, KL within 1e-3, dh and dW rows within the
 backward tolerance (1e-2 of the reference's norm and of its largest entry).
+The block-scaled forward scores every row of h, so its MXFP8 copy of the rows
+in the workspace also passes 2**31 bytes.
 """
 import numpy as np
 import pytest
@@ -103,4 +105,25 @@ def test_kl_past_32_bit_offsets():
     want = coracle.kl(d["h_s"].cpu(), d["W_s"].cpu(), d["h_t"].cpu(), d["W_t"].cpu(), None, "bf16")
     _close(kl, want, 1e-3, "kl")
     d.clear()
+    torch.cuda.empty_cache()
+
+
+def test_block_scaled_forward_past_32_bit_offsets(big):
+    """Every row of h scored on the block-scaled tensor cores against a
+    4096-row head: the MXFP8 rows in the workspace take 2.15e9 bytes, so
+    their offsets, like h's, need 33 bits past row EDGE."""
+    d = big
+    Vs = 4096
+    head = flp.mx_head_quantize(d["W"][:Vs].contiguous())
+    tg = d["targets"] % Vs
+    logp, ent = flp.logprob_entropy_mx(d["h"], head, Vs, tg, None, d["tau"])
+    torch.cuda.synchronize()
+    pos = d["pos"]
+    packed, scales = coracle.mxfp4_quantize(d["W_cpu"][:Vs], "bf16")
+    o = coracle.logprob_entropy_mx(d["h_rows"], packed, scales, Vs,
+                                   tg[d["row_idx"]].cpu().numpy(), None, d["tau"], "bf16")
+    idx = torch.from_numpy(pos).cuda()
+    _close(logp[idx], o["logp"], 1e-3, "logp (block-scaled)")
+    _close(ent[idx], o["ent"], 1e-3, "ent (block-scaled)")
+    del head, logp, ent
     torch.cuda.empty_cache()
