@@ -5,9 +5,9 @@ and its own workspace; the library's shared host state (the tiling-plan
 cache, the per-device information, the tensor-map encoder) is reached from
 all of them at once.  Every kernel is deterministic, so each concurrent
 result must equal, bit for bit, the same call made alone on the default
-stream.  The calls mix forward scoring, K-candidate scoring, KL and the
-backward on different shapes, so that the threads also ask for different
-plans at the same time.
+stream.  The calls mix forward scoring, K-candidate scoring, KL, the
+backward and the block-scaled forward and KL on different shapes, so that
+the threads also ask for different plans at the same time.
 """
 import threading
 
@@ -36,7 +36,12 @@ def _jobs():
     k = workloads.make(workloads.WORKLOADS[3].scaled(T=700, H=768, V=25000, seed=92), "cuda")
     b = workloads.make(workloads.WORKLOADS[4].scaled(T=900, H=512, V=17000, seed=93), "cuda")
     cand = torch.stack([f["targets"], f["targets"].flip(0), (f["targets"] + 7) % 30000], 1)
+    fhead = flp.mx_head_quantize(f["W"])
+    khead = flp.mx_head_quantize(k["W_t"])
     return {
+        "block-scaled forward": lambda: flp.logprob_entropy_mx(f["h"], fhead, 30000, f["targets"],
+                                                               None, 0.8),
+        "block-scaled kl": lambda: (flp.kl_divergence_mx(k["h_s"], k["W_s"], k["h_t"], khead),),
         "forward": lambda: flp.logprob_entropy(f["h"], f["W"], f["targets"], None, 0.8),
         "packed": lambda: flp.logprob_entropy(p["h"], p["W"], p["targets"], p["row_idx"], 1.0),
         "k-candidates": lambda: flp.logprob_entropy_k(f["h"], f["W"], cand, None, 0.8),
