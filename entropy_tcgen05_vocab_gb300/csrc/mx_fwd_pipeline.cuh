@@ -15,26 +15,32 @@
 // vocabulary split) as in vocab_pipeline.cuh, on 256-row x 448-column tiles:
 // two N = 224 MMAs, one per 224-row tile of the head, share the A operand
 // (as the bf16 forward's 512-column tiles do) and fill 448 TMEM columns, one
-// accumulator buffer.  One ring of kMxFStages stages of one 128-wide k-chunk
-// each, per CTA:
+// accumulator buffer.  Per CTA, an operand ring of kMxFStages stages of one
+// 128-wide k-chunk each:
 //   A     128 rows x 128 E4M3, 128B-swizzled
 //   B0/1  112 rows x 128 E2M1 of head tiles 2 vt and 2 vt + 1, in the padded
 //         layout the MMA reads (each 16 elements as 8 bytes of codes and an
 //         8-byte gap, written so by the tensor-map copy of type
 //         16U4_ALIGN16B), 128B-swizzled
-//   scale atoms of A's 128 rows (512 B) and of both whole 224-row head tiles
-//         (1 KB each: every CTA of the pair needs the scales of all N columns)
+// and a scale ring of kMxFSfStages entries, one per k-chunk: the scale atoms
+// of A's 128 rows (512 B) and of both whole 224-row head tiles (1 KB each:
+// every CTA of the pair needs the scales of all N columns).  The scale ring
+// has its own producer lane, so a chunk's atoms are in shared memory well
+// before its operands.
 // TMEM: the accumulator at [0, 448) (MMA 0 at columns [0, 224), MMA 1 at
 // [224, 448), so tile column c is vocabulary column 448 vt + c), then
 // kMxFSlots slots of 20 scale columns (4 for A, 8 per head tile).  Per
 // k-chunk a scale-copier warp copies the chunk's five atoms into the chunk's
 // slot with tcgen05.cp (the layout the block-scaled MMA reads; see
-// mx_pipeline.cuh) and commits that to the slot's "ready" barrier; the MMA
-// issuer waits for it, issues the four K = 32 steps of both MMAs with scale
-// id = step, and commits once to release the stage.  The slots are fewer
-// than the stages, so before it rewrites slot g % kMxFSlots for k-chunk g
-// the copier waits for the release of k-chunk g - kMxFSlots, whose MMAs were
-// that slot's last readers.  (With the copies and that wait on the issuer's
+// mx_pipeline.cuh), commits that to the slot's "ready" barrier and frees the
+// ring entry; the MMA issuer waits for "ready" and the operand stage, issues
+// the four K = 32 steps of both MMAs with scale id = step, and commits once
+// to release the stage.  The slots are fewer than the stages, so before it
+// rewrites slot g % kMxFSlots for k-chunk g the copier waits for the release
+// of k-chunk g - kMxFSlots, whose MMAs were that slot's last readers.  The
+// tensor pipe runs a copy after the MMAs issued before it, so the earlier
+// the copier issues a chunk's copies -- with the atoms already in shared
+// memory, right after that release -- the less the chunk's MMAs wait.  (With the copies and that wait on the issuer's
 // own thread, the issuer spent about 12 % of its time in that wait and a
 // call took a quarter longer.)  Eight epilogue warps (two per TMEM lane
 // quarter, 224 columns each) fold the accumulator 32 columns at a time.
@@ -48,10 +54,12 @@ namespace flp {
 
 constexpr int kMxFStages = 4;
 constexpr int kMxFSlots = 3;
-// warps: 0 producer, 1 TMEM allocation + MMA issuer, 2..9 epilogue, 10 scale
-// copier (leader CTA)
+constexpr int kMxFSfStages = 8;
+// warps: 0 operand producer, 1 TMEM allocation + MMA issuer, 2..9 epilogue,
+// 10 scale copier (leader CTA), 11 scale producer
 constexpr int kMxFScaleWarp = 2 + kMxFEpiWarps;
-constexpr int kMxFThreads = 32 * (kMxFScaleWarp + 1);
+constexpr int kMxFSfProdWarp = kMxFScaleWarp + 1;
+constexpr int kMxFThreads = 32 * (kMxFSfProdWarp + 1);
 // The copier's parity wait for the release of chunk g - kMxFSlots is
 // unambiguous: that stage's next release (chunk g - kMxFSlots + kMxFStages)
 // comes after chunk g's MMAs, which wait for this copier.
@@ -65,14 +73,16 @@ struct MxFwdLayout {
   static constexpr int kSfb = 1024;                     // per head tile
   static constexpr int kOffB0 = kA;
   static constexpr int kOffB1 = kA + kB;
-  static constexpr int kOffSfa = kA + 2 * kB;
-  static constexpr int kOffSfb0 = kOffSfa + kSfa;
+  static constexpr int kStage = kA + 2 * kB;            // 45056
+  static constexpr int kTx = kA + 2 * kBTx;             // operand bytes one CTA's copies count
+  static constexpr int kOffSfb0 = kSfa;                 // within a scale-ring entry
   static constexpr int kOffSfb1 = kOffSfb0 + kSfb;
-  static constexpr int kStage = 48 * 1024;
-  static constexpr int kTx = kA + 2 * kBTx + kSfa + 2 * kSfb;  // bytes one CTA's copies count
+  static constexpr int kSfStage = kSfa + 2 * kSfb;      // 2560
   static constexpr int kRingBytes = kMxFStages * kStage;
-  static constexpr int kBarrierBytes = 8 * (2 * kMxFStages + kMxFSlots + 4) + 32;
-  static constexpr int kSmemBytes = kRingBytes + kBarrierBytes + 1024;
+  static constexpr int kSfRingBytes = kMxFSfStages * kSfStage;
+  static constexpr int kBarrierBytes =
+      8 * (2 * kMxFStages + kMxFSlots + 4 + 2 * kMxFSfStages) + 32;
+  static constexpr int kSmemBytes = kRingBytes + kSfRingBytes + kBarrierBytes + 1024;
   static constexpr int kTmemCols = 512;
   static constexpr int kAccCols = kMxFwdTileCols;        // 448
   static constexpr int kSfCols = 20;
@@ -80,10 +90,9 @@ struct MxFwdLayout {
 static_assert(MxFwdLayout::kAccCols == 2 * kMxBN, "two head tiles per tile");
 static_assert(MxFwdLayout::kStage % 1024 == 0 && MxFwdLayout::kOffB1 % 1024 == 0,
               "swizzled operands stay aligned to swizzle atoms");
-static_assert(MxFwdLayout::kOffSfa % 128 == 0 && MxFwdLayout::kOffSfb0 % 128 == 0 &&
-                  MxFwdLayout::kOffSfb1 % 128 == 0,
+static_assert(MxFwdLayout::kRingBytes % 128 == 0 && MxFwdLayout::kSfStage % 128 == 0 &&
+                  MxFwdLayout::kOffSfb0 % 128 == 0 && MxFwdLayout::kOffSfb1 % 128 == 0,
               "tensor-copy destinations are 128-byte aligned");
-static_assert(MxFwdLayout::kOffSfb1 + MxFwdLayout::kSfb <= MxFwdLayout::kStage, "stage fits");
 static_assert(MxFwdLayout::kAccCols + kMxFSlots * MxFwdLayout::kSfCols <= MxFwdLayout::kTmemCols,
               "scale columns fit beside the accumulator");
 static_assert(MxFwdLayout::kSmemBytes <= 227 * 1024, "shared memory per CTA");
@@ -108,16 +117,20 @@ __global__ void __launch_bounds__(kMxFThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::kRingBytes);
+  uint8_t *sring = smem + L::kRingBytes;
+  uint64_t *full = reinterpret_cast<uint64_t *>(sring + L::kSfRingBytes);
   uint64_t *empty = full + kMxFStages;
   uint64_t *afull = empty + kMxFStages;  // accumulator ready for the epilogue
   uint64_t *aempty = afull + 1;          // accumulator drained
   uint64_t *drain = aempty + 1;          // MMA issuer's teardown
   uint64_t *sready = drain + 1;          // [kMxFSlots] a k-chunk's scales are in TMEM
   uint64_t *sdrain = sready + kMxFSlots;  // scale copier's teardown
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sdrain + 1);
+  uint64_t *sfull = sdrain + 1;           // [kMxFSfStages] a k-chunk's atoms landed (leader)
+  uint64_t *sempty = sfull + kMxFSfStages;  // [kMxFSfStages] the copier's copies read them
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sempty + kMxFSfStages);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-  // k-chunks the peer's producer issued (written at teardown)
+  // k-chunks the peer's operand [0] and scale [1] producers issued (written
+  // at teardown)
   volatile uint32_t *peer_issued = reinterpret_cast<volatile uint32_t *>(tmem_slot + 2);
 
   const int warp = threadIdx.x >> 5;
@@ -128,7 +141,8 @@ __global__ void __launch_bounds__(kMxFThreads, 1)
   const int num_units = gridDim.x / CG;
   const int kc_n = sch.k_blocks;  // 128-wide k-chunks
   const uint64_t lim = wait_limit(sch.wait_ns);
-  uint32_t issued = 0;  // producer: k-chunks issued
+  uint32_t issued = 0;     // operand producer: k-chunks issued
+  uint32_t sf_issued = 0;  // scale producer: k-chunks issued
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kMxFStages; ++s) {
@@ -140,8 +154,13 @@ __global__ void __launch_bounds__(kMxFThreads, 1)
     mbar_init(drain, 1);
     for (int s = 0; s < kMxFSlots; ++s) mbar_init(&sready[s], 1);
     mbar_init(sdrain, 1);
+    for (int s = 0; s < kMxFSfStages; ++s) {
+      mbar_init(&sfull[s], 1);
+      mbar_init(&sempty[s], 1);
+    }
     *abort_flag = 0;
     peer_issued[0] = 0;
+    peer_issued[1] = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -171,7 +190,6 @@ __global__ void __launch_bounds__(kMxFThreads, 1)
         int mt, sp, vt0, vt1;
         sch.item(it, mt, sp, vt0, vt1);
         const int arow = mt * (kBM * CG) + static_cast<int>(rank) * kBM;
-        const int ablk = mt * CG + static_cast<int>(rank);  // 128-row block of the scale atoms
         for (int vt = vt0; ok && vt < vt1; ++vt) {
           const int t0 = 2 * vt, t1 = 2 * vt + 1;  // the tile's two 224-row head tiles
           const int brow0 = t0 * kMxBN + static_cast<int>(rank) * kMxBRows;
@@ -185,11 +203,42 @@ __global__ void __launch_bounds__(kMxFThreads, 1)
             tma_load_2d_pair(base, &tmA, fb, c * kMxChunk, arow);
             tma_load_2d_pair(base + L::kOffB0, &tmB, fb, c * kMxChunk, brow0);
             tma_load_2d_pair(base + L::kOffB1, &tmB, fb, c * kMxChunk, brow1);
-            tma_load_2d_pair(base + L::kOffSfa, &tmSfa, fb, 0, (ablk * kc_n + c) * 32);
-            tma_load_2d_pair(base + L::kOffSfb0, &tmSfb, fb, 0, (t0 * kc_n + c) * 64);
-            tma_load_2d_pair(base + L::kOffSfb1, &tmSfb, fb, 0, (t1 * kc_n + c) * 64);
             ++issued;
             if (++st == kMxFStages) {
+              st = 0;
+              ph ^= 1u;
+            }
+          }
+        }
+      }
+      if (!ok) record_timeout<CG>(status, abort_flag);
+    }
+    __syncwarp();
+  } else if (warp == kMxFSfProdWarp) {
+    // ------------------------------------------------------ scale producer
+    // Both CTAs' atoms counted on the leader's barrier, as the operands are.
+    if (lane == 0) {
+      int st = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      const uint32_t sfull_dst = mapa_shared(smem_u32(sfull), 0);
+      for (int it = unit; ok && it < sch.items; it += num_units) {
+        int mt, sp, vt0, vt1;
+        sch.item(it, mt, sp, vt0, vt1);
+        const int ablk = mt * CG + static_cast<int>(rank);  // 128-row block of the A atoms
+        for (int vt = vt0; ok && vt < vt1; ++vt) {
+          const int t0 = 2 * vt, t1 = 2 * vt + 1;
+          for (int c = 0; c < kc_n; ++c) {
+            ok = mbar_wait(&sempty[st], ph ^ 1u, abort_flag, lim);
+            if (!ok) break;
+            uint8_t *base = sring + st * L::kSfStage;
+            if (leader) mbar_arrive_expect_tx(&sfull[st], CG * L::kSfStage);
+            const uint32_t fb = sfull_dst + st * 8;
+            tma_load_2d_pair(base, &tmSfa, fb, 0, (ablk * kc_n + c) * 32);
+            tma_load_2d_pair(base + L::kOffSfb0, &tmSfb, fb, 0, (t0 * kc_n + c) * 64);
+            tma_load_2d_pair(base + L::kOffSfb1, &tmSfb, fb, 0, (t1 * kc_n + c) * 64);
+            ++sf_issued;
+            if (++st == kMxFSfStages) {
               st = 0;
               ph ^= 1u;
             }
@@ -213,8 +262,8 @@ __global__ void __launch_bounds__(kMxFThreads, 1)
           if (!ok) break;
           tc_fence_after();
           for (int c = 0; c < kc_n; ++c) {
-            // the scale copier put this k-chunk's scales into its slot (after
-            // it saw the stage land), then the stage itself
+            // the scale copier put this k-chunk's scales into its slot, then
+            // the operand stage landed
             ok = mbar_wait(&sready[g % kMxFSlots], (g / kMxFSlots) & 1u, abort_flag, lim) &&
                  mbar_wait(&full[st], ph, abort_flag, lim);
             if (!ok) break;
@@ -249,8 +298,9 @@ __global__ void __launch_bounds__(kMxFThreads, 1)
     __syncwarp();
   } else if (warp == kMxFScaleWarp) {
     // ------------------------------------------------------- scale copier
-    // Copies each k-chunk's five scale atoms from its stage into the chunk's
-    // TMEM slot and commits that to the slot's "ready" barrier.  A slot is
+    // Copies each k-chunk's five scale atoms from its ring entry into the
+    // chunk's TMEM slot, commits that to the slot's "ready" barrier and, once
+    // the copies have read the entry, frees it in both CTAs.  A slot is
     // rewritten only after the MMAs of the chunk kMxFSlots earlier, its last
     // readers, were released; waiting for that here, off the MMA issuer,
     // keeps the issuer's thread on MMAs.  The release also paces this warp:
@@ -265,24 +315,25 @@ __global__ void __launch_bounds__(kMxFThreads, 1)
         sch.item(it, mt, sp, vt0, vt1);
         for (int vt = vt0; ok && vt < vt1; ++vt) {
           for (int c = 0; c < kc_n; ++c) {
-            ok = mbar_wait(&full[st], ph, abort_flag, lim);
+            ok = mbar_wait(&sfull[st], ph, abort_flag, lim);
             if (ok && g >= static_cast<uint32_t>(kMxFSlots)) {
               const uint32_t gp = g - kMxFSlots;
               ok = mbar_wait(&empty[gp % kMxFStages], (gp / kMxFStages) & 1u, abort_flag, lim);
             }
             if (!ok) break;
             tc_fence_after();
-            const uint32_t tb = smem_u32(smem + st * L::kStage);
+            const uint32_t tb = smem_u32(sring + st * L::kSfStage);
             const uint32_t sf =
                 tmem_base + static_cast<uint32_t>(L::kAccCols + (g % kMxFSlots) * L::kSfCols);
-            tmem_cp_32x128b_x4_pair(sf, sdesc_rows16(tb + L::kOffSfa));
+            tmem_cp_32x128b_x4_pair(sf, sdesc_rows16(tb));
             tmem_cp_32x128b_x4_pair(sf + 4, sdesc_rows16(tb + L::kOffSfb0));
             tmem_cp_32x128b_x4_pair(sf + 8, sdesc_rows16(tb + L::kOffSfb0 + 512));
             tmem_cp_32x128b_x4_pair(sf + 12, sdesc_rows16(tb + L::kOffSfb1));
             tmem_cp_32x128b_x4_pair(sf + 16, sdesc_rows16(tb + L::kOffSfb1 + 512));
             mma_commit_pair_local(&sready[g % kMxFSlots]);
+            mma_commit_pair(&sempty[st], 0x3);
             ++g;
-            if (++st == kMxFStages) {
+            if (++st == kMxFSfStages) {
               st = 0;
               ph ^= 1u;
             }
@@ -324,16 +375,19 @@ __global__ void __launch_bounds__(kMxFThreads, 1)
     if (!ok && lane == 0) record_timeout<CG>(status, abort_flag);
   }
 
-  // Teardown (as in vocab_pipeline_kernel).
-  if (warp == 0 && lane == 0 && !leader) {
-    const uint32_t pi = mapa_shared(smem_u32(const_cast<uint32_t *>(peer_issued)), 0);
-    st_cluster_u32(pi, issued);
+  // Teardown (as in vocab_pipeline_kernel, for both rings).
+  if ((warp == 0 || warp == kMxFSfProdWarp) && lane == 0 && !leader) {
+    const int k = warp == 0 ? 0 : 1;
+    const uint32_t pi = mapa_shared(smem_u32(const_cast<uint32_t *>(peer_issued + k)), 0);
+    st_cluster_u32(pi, warp == 0 ? issued : sf_issued);
   }
   pipe_sync<CG>();
   if (*abort_flag) {
     if (leader && lane == 0) {
       if (warp == 0)
         drain_copies<kMxFStages, CG>(full, issued, peer_issued[0], L::kTx);
+      else if (warp == kMxFSfProdWarp)
+        drain_copies<kMxFSfStages, CG>(sfull, sf_issued, peer_issued[1], L::kSfStage);
       else if (warp == 1)
         drain_mmas<CG>(drain);
       else if (warp == kMxFScaleWarp)
