@@ -48,6 +48,30 @@ import torch  # noqa: E402
 METRIC = "scored tokens/s and TFLOP/s (% of GB300 dense BF16 peak), fused logp+entropy"
 UNIT = "scored tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# Nominal dense rate of tcgen05.mma kind::mxf8f6f4 (E4M3 x E2M1 with E8M0
+# block scales) over kind::f16 with bf16 operands: 4.5 against 2.25 PFLOP/s.
+MX_OVER_BF16 = 2.0
+
+
+def own_peak(P, arith, sustained=False):
+    """Peak of the arithmetic a kernel runs, in bf16-equivalent TFLOP/s (the
+    flops counted are 2nVH per head), from the measured bf16 figure.
+    arith: "bf16"; "mx" (every MMA block-scaled); "bf16+mx" (half the flops,
+    the student's, in bf16 and half, the teacher's, block-scaled, which the
+    tensor pipe runs one after the other)."""
+    b = P["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+    return {"bf16": b, "mx": MX_OVER_BF16 * b,
+            "bf16+mx": 2.0 / (1.0 / b + 1.0 / (MX_OVER_BF16 * b))}[arith]
+
+
+PEAK_KIND = {
+    "bf16": "bf16 dense, burst, %s",
+    "mx": "kind::mxf8f6f4 dense (E4M3 x E2M1), burst: %s bf16 x 2, the nominal fp8:bf16 ratio",
+    "bf16+mx": ("student bf16 + teacher kind::mxf8f6f4, burst: %s bf16 x 4/3 (half the flops "
+                "at twice the rate)"),
+}
+DTYPE = {"mx": "e4m3 x e2m1 (MX block-scaled), f32 accumulate",
+         "bf16+mx": "bf16 student + e4m3 x e2m1 (MX block-scaled) teacher, f32 accumulate"}
 FWD_KERNEL_SOURCES = ["ptx.cuh", "schedule.h", "vocab_pipeline.cuh", "kernels_fwd.cu", "launch.h",
                       "lse_epilogue.cuh", "support.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "vocab_pipeline_forward-scoring.txt")
@@ -519,6 +543,8 @@ def run_ours(args):
             targets=d["targets"].cpu().numpy())).to(device)
         variant["support"] = "each token kept with probability 2^-%d, targets kept" % args.support_j
     headline = w0.kind == "fwd" and args.workload == 1 and args.T is None and not variant
+    arith = ("mx" if w0.kind == "fwd" and args.head == "mx" else
+             "bf16+mx" if w0.kind == "kl" and args.teacher == "mx" else "bf16")
     sampler = ClockSampler(device.index) if rank == 0 else None
     if sampler:
         sampler.start()
@@ -544,15 +570,15 @@ def run_ours(args):
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": d["workload"].dtype,
+        "scaling": "weak", "vs_baseline": None, "dtype": DTYPE.get(arith, d["workload"].dtype),
         "data": "synthetic (seeded; shapes and distributions of the pages' workloads)",
         "config": dict(describe(d), parallelism="replicas" if world > 1 else "single GPU",
                        **variant),
         "tflops": world * fl * args.steps / (total_ms / 1e3) / 1e12,
         "pct_of_bf16_peak": 100.0 * fl * args.steps / (total_ms / 1e3) / 1e12 / P["bf16_tflops"],
         "kernel_ms": kernel_ms,
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": P["bf16_tflops"],
-                     "unit": "TFLOP/s", "frac": achieved / P["bf16_tflops"], "traffic": traffic,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": own_peak(P, arith),
+                     "unit": "TFLOP/s", "frac": achieved / own_peak(P, arith), "traffic": traffic,
                      "kernel": {"fwd": ("mx_fwd_pipeline_kernel<LseEpi<1,false>>"
                                         if "head" in variant else
                                         "vocab_pipeline_kernel<256,4,2,LseEpi<1,%s>,2,1,8,true>"
@@ -562,8 +588,8 @@ def run_ours(args):
                                        "vocab_pipeline_kernel<256,3,2,KlEpi,2,1,%s>"
                                        % ("4,false,true" if "teacher_head" in variant else "8")),
                                 "bwd": "grad pass + dh and dW GEMMs"}[w0.kind],
-                     "peak_kind": "bf16 dense, burst, %s" % P["source"],
-                     "frac_of_sustained": achieved / P["bf16_tflops_sustained"],
+                     "peak_kind": PEAK_KIND[arith] % P["source"],
+                     "frac_of_sustained": achieved / own_peak(P, arith, sustained=True),
                      "algorithmic_flops_per_launch": fl,
                      "traffic_source": traffic_src},
         "e2e": e2e,
@@ -608,7 +634,7 @@ def run_ours(args):
                 flp.logprob_entropy(d["h"], d["W"], d["targets"], d["row_idx"], d["tau"],
                                     workspace=wsk)
 
-            def variant_line(name, fn, note):
+            def variant_line(name, fn, note, arith_v="bf16"):
                 try:
                     # blocks of 10 calls in ABBA order, so a drift of the clock over
                     # the run (heating towards the power cap) weighs on both alike
@@ -628,6 +654,9 @@ def run_ours(args):
                         ms_per_step=t_var / 40, tflops=fl / (t_var / 40 / 1e3) / 1e12,
                         pct_of_bf16_peak=100 * fl / (t_var / 40 / 1e3) / 1e12 / P["bf16_tflops"],
                         plain_ms_same_clocks=t_plain / 40)
+                    if arith_v != "bf16":
+                        extra[name]["pct_of_own_peak"] = float("%.4g" % (
+                            100 * fl / (t_var / 40 / 1e3) / 1e12 / own_peak(P, arith_v)))
                 except Exception as e:  # reported, not fatal
                     extra[name] = {"unavailable": str(e)[:200]}
 
@@ -660,7 +689,8 @@ def run_ours(args):
                              {"head": "MXFP4 head (%.3f GB against %.3f GB in bf16) x MXFP8 rows "
                                       "on the block-scaled tensor cores (tcgen05.mma "
                                       "kind::mxf8f6f4)"
-                                      % (mxh.numel() / 1e9, w.V * w.H * 2 / 1e9)})
+                                      % (mxh.numel() / 1e9, w.V * w.H * 2 / 1e9),
+                              "own_peak": PEAK_KIND["mx"] % P["source"]}, "mx")
                 del mxh, wsm
             except Exception as e:  # reported, not fatal
                 extra[w.name + "-mx-head"] = {"unavailable": str(e)[:200]}
@@ -683,20 +713,21 @@ def run_ours(args):
             def bf16_teacher():
                 flp.kl_divergence(dk["h_s"], dk["W_s"], dk["h_t"], dk["W_t"], None, workspace=wsk)
 
-            variants = (
+            variants = (  # (suffix, call, note, arithmetic of the MMAs)
                 ("-mxfp4-teacher",
                  lambda: flp.kl_divergence_mxfp4(dk["h_s"], dk["W_s"], dk["h_t"], packed, scales,
                                                  None, workspace=wsk),
                  "MXFP4 (E2M1, E8M0 per 32) decoded to bf16 in shared memory, %.3f GB against "
-                 "%.3f GB in bf16" % (packed.numel() / 1e9 + scales.numel() / 1e9, bf16_gb)),
+                 "%.3f GB in bf16" % (packed.numel() / 1e9 + scales.numel() / 1e9, bf16_gb),
+                 "bf16"),
                 ("-mx-teacher",
                  lambda: flp.kl_divergence_mx(dk["h_s"], dk["W_s"], dk["h_t"], head, None,
                                               workspace=wsk),
                  "MXFP4 head (%.3f GB against %.3f GB in bf16) x MXFP8 teacher rows on the "
                  "block-scaled tensor cores (tcgen05.mma kind::mxf8f6f4)"
-                 % (head.numel() / 1e9, bf16_gb)),
+                 % (head.numel() / 1e9, bf16_gb), "bf16+mx"),
             )
-            for suffix, fn, note in variants:
+            for suffix, fn, note, arith_v in variants:
                 t_mx = t_bf = 0.0
                 for order in ((bf16_teacher, fn), (fn, bf16_teacher)):  # ABBA
                     for f in order:
@@ -708,11 +739,16 @@ def run_ours(args):
                 t_mx = max_over_ranks(t_mx, world, device)
                 t_bf = max_over_ranks(t_bf, world, device)
                 configs[wk.name + suffix] = dict(describe(dk), steps=20, teacher_head=note)
+                if arith_v != "bf16":
+                    configs[wk.name + suffix]["own_peak"] = PEAK_KIND[arith_v] % P["source"]
                 extra[wk.name + suffix] = compact(
                     n_rows=dk["n"], scored_tokens_per_s=job_throughput(dk["n"], 20, t_mx, world),
                     ms_per_step=t_mx / 20, tflops=flk / (t_mx / 20 / 1e3) / 1e12,
                     pct_of_bf16_peak=100 * flk / (t_mx / 20 / 1e3) / 1e12 / P["bf16_tflops"],
                     plain_ms_same_clocks=t_bf / 20)
+                if arith_v != "bf16":
+                    extra[wk.name + suffix]["pct_of_own_peak"] = float("%.4g" % (
+                        100 * flk / (t_mx / 20 / 1e3) / 1e12 / own_peak(P, arith_v)))
             del dk, packed, scales, head, wsk
         except Exception as e:  # reported, not fatal
             extra[workloads.WORKLOADS[3].name + "-mx-teacher"] = {"unavailable": str(e)[:200]}

@@ -86,3 +86,17 @@ def test_reference_arm_prints_the_contract_line(monkeypatch, capsys):
     cb = line["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"]
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_own_peak_of_block_scaled_lines():
+    """Block-scaled lines are judged against the rate of their own MMAs:
+    kind::mxf8f6f4 runs at twice the bf16 rate (4.5 against 2.25 PFLOP/s
+    nominal), and the KL with a block-scaled teacher does half its flops at
+    each rate, one after the other on the tensor pipe."""
+    P = {"bf16_tflops": 1800.0, "bf16_tflops_sustained": 1600.0}
+    assert bench.own_peak(P, "bf16") == 1800.0
+    assert bench.own_peak(P, "mx") == 3600.0
+    assert bench.own_peak(P, "mx", sustained=True) == 3200.0
+    # time for F flops, half at b and half at 2b: F/2/b + F/2/(2b) = 3F/(4b)
+    assert abs(bench.own_peak(P, "bf16+mx") - 2400.0) < 1e-9
+    assert set(bench.PEAK_KIND) == {"bf16", "mx", "bf16+mx"}
