@@ -40,10 +40,11 @@
 // of k-chunk g - kMxFSlots, whose MMAs were that slot's last readers.  The
 // tensor pipe runs a copy after the MMAs issued before it, so the earlier
 // the copier issues a chunk's copies -- with the atoms already in shared
-// memory, right after that release -- the less the chunk's MMAs wait.  (With the copies and that wait on the issuer's
-// own thread, the issuer spent about 12 % of its time in that wait and a
-// call took a quarter longer.)  Eight epilogue warps (two per TMEM lane
-// quarter, 224 columns each) fold the accumulator 32 columns at a time.
+// memory, right after that release -- the less the chunk's MMAs wait.
+// (With the copies and that wait on the issuer's own thread, the issuer
+// spent about 12 % of its time in that wait and a call took a quarter
+// longer.)  Eight epilogue warps (two per TMEM lane quarter, 224 columns
+// each) fold the accumulator 32 columns at a time.
 #pragma once
 
 #include "launch.h"
